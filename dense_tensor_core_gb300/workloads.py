@@ -1,0 +1,108 @@
+"""Seeded synthetic workloads for the dense GEMM: shapes, seeds and host-side input bytes.
+
+This module holds no GEMM arithmetic. It only draws random numbers and stores them in the
+operand formats, so the same bytes can be handed to the CUDA library and to the CPU oracle.
+
+Recipe (the pages measure on random matrices, not on a dataset: TileLang SM100 Support (Preview),
+"Compilation and Usage", draws ``torch.randn(M, K)`` and ``torch.randn(N, K)``):
+
+* 16-bit operands: ``torch.Generator().manual_seed(seed)``, then ``torch.randn`` in fp32 for A
+  (shape [M,K]) and then B ([N,K] for "NT", [K,N] for "NN"), each rounded to bf16 or fp16 by
+  torch's round-to-nearest-even conversion. Returned as uint16 code arrays.
+* MXFP8 operands: the same generator draws x_A ~ N(0,1) [M,K], x_B ~ N(0,1) [N,K], then integer
+  exponents u_A [M, ceil(K/128)] and u_B [N, ceil(K/128)] uniform in {-3..3}. Each element is
+  stored as e4m3(x / 2^u) (torch's RNE conversion to float8_e4m3fn) and each scale as the E8M0
+  code 127 + u, so that e4m3 * 2^(sf-127) is close to x. |x / 2^u| stays far below e4m3's
+  largest finite value 448, so no element saturates.
+"""
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+SF_BLOCK = 128  # K-elements per E8M0 scale (granularity 128 along K for both operands)
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    kind: str  # "bf16", "f16" or "mxfp8"
+    layout: str  # "NT" (B is [N,K]) or "NN" (B is [K,N])
+    M: int
+    N: int
+    K: int
+    seed: int
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+    @property
+    def min_bytes(self) -> int:
+        """Compulsory HBM traffic: read A and B (and the scales) once, write C once."""
+        if self.kind == "mxfp8":
+            kb = (self.K + SF_BLOCK - 1) // SF_BLOCK
+            return self.M * self.K + self.N * self.K + (self.M + self.N) * kb + 2 * self.M * self.N
+        return 2 * (self.M * self.K + self.N * self.K + self.M * self.N)
+
+
+# The pages' example shapes (TileLang SM100 Support (Preview): NT 4096x4096x8192 with a
+# 128x256x128 tile; tilelang (velog) 1.1-1.3: fp16 NN 1024^3) plus the large 2-CTA square, the
+# memory-bound skinny product and the block-scaled variant.
+WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("bf16_nt_256x256x512", "bf16", "NT", 256, 256, 512, 0),
+        Workload("f16_nn_1024x1024x1024", "f16", "NN", 1024, 1024, 1024, 1),
+        Workload("bf16_nt_4096x4096x8192", "bf16", "NT", 4096, 4096, 8192, 2),
+        Workload("bf16_nt_8192x8192x8192", "bf16", "NT", 8192, 8192, 8192, 3),
+        Workload("bf16_nt_128x8192x8192", "bf16", "NT", 128, 8192, 8192, 3),
+        Workload("mxfp8_nt_4096x4096x8192", "mxfp8", "NT", 4096, 4096, 8192, 4),
+    ]
+}
+
+HEADLINE = "bf16_nt_4096x4096x8192"
+
+_TORCH_16 = {"bf16": torch.bfloat16, "f16": torch.float16}
+
+
+def randn16(kind: str, shape, gen: torch.Generator) -> np.ndarray:
+    """N(0,1) fp32 draws rounded to bf16/fp16; returned as uint16 codes."""
+    x = torch.randn(tuple(shape), generator=gen, dtype=torch.float32).to(_TORCH_16[kind])
+    return x.view(torch.int16).numpy().view(np.uint16)
+
+
+def make16(kind: str, layout: str, M: int, N: int, K: int, seed: int):
+    """(A [M,K], B [N,K] or [K,N]) as uint16 codes."""
+    g = torch.Generator().manual_seed(seed)
+    A = randn16(kind, (M, K), g)
+    B = randn16(kind, (N, K) if layout == "NT" else (K, N), g)
+    return A, B
+
+
+def make_mxfp8(M: int, N: int, K: int, seed: int):
+    """(A [M,K] e4m3, B [N,K] e4m3, sfA [M,kb] E8M0, sfB [N,kb] E8M0) as uint8 codes."""
+    g = torch.Generator().manual_seed(seed)
+    kb = (K + SF_BLOCK - 1) // SF_BLOCK
+    xa = torch.randn((M, K), generator=g, dtype=torch.float32)
+    xb = torch.randn((N, K), generator=g, dtype=torch.float32)
+    ua = torch.randint(-3, 4, (M, kb), generator=g, dtype=torch.int32)
+    ub = torch.randint(-3, 4, (N, kb), generator=g, dtype=torch.int32)
+
+    def quantise(x, u):
+        # per-element exponent of its (row, K-block); dividing by a power of two is exact in fp32
+        ue = u.repeat_interleave(SF_BLOCK, dim=1)[:, : x.shape[1]]
+        q = torch.ldexp(x, -ue.to(torch.float32)).to(torch.float8_e4m3fn)
+        return q.view(torch.uint8).numpy()
+
+    A = quantise(xa, ua)
+    B = quantise(xb, ub)
+    sfA = (ua + 127).to(torch.uint8).numpy()
+    sfB = (ub + 127).to(torch.uint8).numpy()
+    return A, B, sfA, sfB
+
+
+def make(w: Workload):
+    if w.kind == "mxfp8":
+        return make_mxfp8(w.M, w.N, w.K, w.seed)
+    return make16(w.kind, w.layout, w.M, w.N, w.K, w.seed)

@@ -1,0 +1,333 @@
+/*
+ * dtc_oracle.c -- plain, slow, obviously correct CPU oracle for the dense GEMM.
+ *
+ * TEST INFRASTRUCTURE ONLY. The tests, the smoke check and the benchmark's CPU-baseline leg
+ * load this file's shared library; the CUDA library never calls it, and the two share no
+ * source, header, table or helper.
+ *
+ * What it computes -- the plain definition, written out, with one rounding at the end:
+ *
+ *   16-bit operands (bf16 or fp16):
+ *     C[m,n] = round_out( sum_{k<K} dec(A[m,k]) * dec(Bop[k,n]) )
+ *     "NT": B is stored [N,K] and Bop[k,n] = B[n,k]
+ *           (TileLang SM100 Support (Preview), "Code Example": B is (N, K) and the gemm uses
+ *            trans_B=True; "Compilation and Usage": ref_c = (a.float() @ b.T.float()).to(bf16))
+ *     "NN": B is stored [K,N] and Bop[k,n] = B[k,n]
+ *           (tilelang (velog), section 1.1 Front-End DSL: B is T.Tensor((K, N)) and
+ *            T.gemm(A_shared, B_shared, C_local) with no transpose)
+ *
+ *   MXFP8 block-scaled (both operands e4m3, one E8M0 scale per row per 128 K-elements,
+ *   "1d1d" granularity 128 for A and B:
+ *   05 Blackwell TCGEN05 GEMM tutorial, section "Advanced (not implemented here)",
+ *   gemm_blockscaled with sf_a_granularity_k = sf_b_granularity_k = 128):
+ *     C[m,n] = round_bf16( sum_k  e4m3(A[m,k]) * 2^(sfA[m,k/128]-127)
+ *                               * e4m3(B[n,k]) * 2^(sfB[n,k/128]-127) )
+ *
+ * Accumulation is in double. Every product of two bf16/fp16/e4m3 values, times powers of two
+ * from the scales, is exact in double; only the sum carries rounding error, which for the
+ * sizes used (K <= 8192, |terms| < 2^20) is below 1e-10 relative -- far inside the pages'
+ * rtol = atol = 1e-2. The single final rounding is IEEE round-to-nearest-even straight from
+ * double to the output format (never double -> float -> 16-bit, which would round twice).
+ *
+ * Format definitions used by the codecs:
+ *   bf16  : the upper 16 bits of an IEEE binary32 (1 sign, 8 exponent, 7 fraction bits).
+ *   fp16  : IEEE binary16 (1, 5, 10; bias 15; subnormals; exponent 31 = inf/NaN).
+ *   e4m3  : OCP FP8 E4M3 "fn" variant (1, 4, 3; bias 7; no infinities; S.1111.111 = NaN;
+ *           largest finite 448; subnormals m/8 * 2^-6).
+ *   E8M0  : unsigned 8-bit exponent, value 2^(e-127); 0xFF = NaN.
+ *
+ * Degenerate sizes: M == 0 or N == 0 computes nothing; K == 0 gives the empty sum, +0.
+ *
+ * Threads: rows of C are split across POSIX threads, one per requested worker; the
+ * arithmetic for each output element is identical whatever the split.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+#define DTC_ORACLE_BF16 0
+#define DTC_ORACLE_F16 1
+#define DTC_ORACLE_NT 0
+#define DTC_ORACLE_NN 1
+
+/* ------------------------------------------------------------------------------------------ */
+/* Decoders: code -> exact double value                                                        */
+/* ------------------------------------------------------------------------------------------ */
+
+double dtc_oracle_dec_bf16(uint16_t h) {
+    /* bf16 is the top half of a binary32: widen and reinterpret. */
+    uint32_t w = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+double dtc_oracle_dec_f16(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int m = h & 0x3ff;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)m, -24); /* subnormal: m * 2^-10 * 2^-14 */
+    } else if (e == 31) {
+        v = (m == 0) ? INFINITY : NAN;
+    } else {
+        v = ldexp((double)(1024 + m), e - 25); /* (1 + m/1024) * 2^(e-15) */
+    }
+    return sign ? -v : v;
+}
+
+double dtc_oracle_dec_e4m3(uint8_t b) {
+    int sign = (b >> 7) & 1;
+    int e = (b >> 3) & 0xf;
+    int m = b & 0x7;
+    double v;
+    if (e == 15 && m == 7) {
+        return NAN; /* the only NaN encodings: S.1111.111 */
+    } else if (e == 0) {
+        v = ldexp((double)m, -9); /* subnormal: m/8 * 2^-6 */
+    } else {
+        v = ldexp((double)(8 + m), e - 10); /* (1 + m/8) * 2^(e-7) */
+    }
+    return sign ? -v : v;
+}
+
+double dtc_oracle_dec_e8m0(uint8_t b) {
+    if (b == 0xff) return NAN;
+    return ldexp(1.0, (int)b - 127);
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Encoders: double -> nearest representable code, ties to even, one rounding                  */
+/* ------------------------------------------------------------------------------------------ */
+
+/* Round x to a binary format with p significand bits (implicit bit included), smallest normal
+ * exponent emin and largest finite value maxfin. Returns the rounded value as a double (exact:
+ * every value of these formats is a double), +-inf on overflow. x must be finite. */
+static double round_to_format(double x, int p, int emin, double maxfin) {
+    if (x == 0.0) return x;
+    int e;
+    frexp(fabs(x), &e); /* |x| = f * 2^e with 0.5 <= f < 1, so the leading bit is 2^(e-1) */
+    int lead = e - 1;
+    if (lead < emin) lead = emin; /* subnormal range keeps the smallest normal's quantum */
+    int qexp = lead - (p - 1);    /* weight of the last significand bit */
+    double scaled = ldexp(x, -qexp);       /* exact: a power-of-two scaling */
+    double r = nearbyint(scaled);          /* default mode: round half to even */
+    double y = ldexp(r, qexp);
+    if (fabs(y) > maxfin) return x > 0 ? INFINITY : -INFINITY;
+    return y;
+}
+
+uint16_t dtc_oracle_enc_bf16(double x) {
+    if (isnan(x)) return 0x7fc0;
+    double y = isinf(x) ? x : round_to_format(x, 8, -126, ldexp(255.0, 120)); /* max (2-2^-7)*2^127 */
+    /* y is a bf16 value, hence exactly a binary32 value: its top 16 bits are the code. */
+    float f = (float)y;
+    uint32_t w;
+    memcpy(&w, &f, sizeof w);
+    return (uint16_t)(w >> 16);
+}
+
+uint16_t dtc_oracle_enc_f16(double x) {
+    if (isnan(x)) return 0x7e00;
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    if (isinf(x)) return sign | 0x7c00;
+    double y = round_to_format(x, 11, -14, 65504.0);
+    if (isinf(y)) return sign | 0x7c00;
+    double a = fabs(y);
+    if (a == 0.0) return sign;
+    if (a < ldexp(1.0, -14)) {
+        /* subnormal: a = m * 2^-24, 1 <= m <= 1023 */
+        return sign | (uint16_t)ldexp(a, 24);
+    }
+    int e;
+    double f = frexp(a, &e); /* a = f * 2^e, f in [0.5, 1) -> (2f) * 2^(e-1) */
+    int biased = (e - 1) + 15;
+    uint16_t mant = (uint16_t)(ldexp(f, 11) - 1024.0); /* (2f - 1) * 1024, exact */
+    return sign | (uint16_t)(biased << 10) | mant;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* 16-bit GEMM                                                                                 */
+/* ------------------------------------------------------------------------------------------ */
+
+typedef struct {
+    const double* a;  /* decoded A, [M][K] */
+    const double* bt; /* decoded Bop, gathered as [N][K] so that Bop[k][n] = bt[n*K + k] */
+    int64_t M, N, K;
+    int dtype;        /* output format */
+    uint16_t* c;      /* [M][N] codes, may be NULL */
+    double* s;        /* [M][N] unrounded sums, may be NULL */
+    int64_t row0, row1;
+} gemm_job;
+
+static void* gemm_rows(void* arg) {
+    gemm_job* j = (gemm_job*)arg;
+    for (int64_t m = j->row0; m < j->row1; ++m) {
+        const double* arow = j->a + m * j->K;
+        for (int64_t n = 0; n < j->N; ++n) {
+            const double* brow = j->bt + n * j->K;
+            double acc = 0.0;
+            for (int64_t k = 0; k < j->K; ++k) acc += arow[k] * brow[k];
+            if (j->s) j->s[m * j->N + n] = acc;
+            if (j->c)
+                j->c[m * j->N + n] =
+                    j->dtype == DTC_ORACLE_F16 ? dtc_oracle_enc_f16(acc) : dtc_oracle_enc_bf16(acc);
+        }
+    }
+    return NULL;
+}
+
+static int run_rows(gemm_job* proto, int nthreads) {
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 1024) nthreads = 1024;
+    if ((int64_t)nthreads > proto->M) nthreads = (int)(proto->M > 0 ? proto->M : 1);
+    pthread_t tids[1024];
+    int joined[1024];
+    gemm_job jobs[1024];
+    int64_t per = (proto->M + nthreads - 1) / nthreads;
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t] = *proto;
+        jobs[t].row0 = t * per < proto->M ? t * per : proto->M;
+        jobs[t].row1 = (t + 1) * per < proto->M ? (t + 1) * per : proto->M;
+    }
+    for (int t = 1; t < nthreads; ++t) {
+        joined[t] = pthread_create(&tids[t], NULL, gemm_rows, &jobs[t]) == 0;
+        if (!joined[t]) gemm_rows(&jobs[t]); /* could not start a thread: do that share here */
+    }
+    gemm_rows(&jobs[0]);
+    for (int t = 1; t < nthreads; ++t)
+        if (joined[t]) pthread_join(tids[t], NULL);
+    return 0;
+}
+
+static double dec16(int dtype, uint16_t h) {
+    return dtype == DTC_ORACLE_F16 ? dtc_oracle_dec_f16(h) : dtc_oracle_dec_bf16(h);
+}
+
+/* Decode A to [M][K] doubles and Bop to [N][K] doubles (a gather, no arithmetic). */
+static int decode16(int dtype, int layout, const uint16_t* A, const uint16_t* B, int64_t M,
+                    int64_t N, int64_t K, double** a_out, double** bt_out) {
+    double* a = (double*)malloc(sizeof(double) * (size_t)(M * K > 0 ? M * K : 1));
+    double* bt = (double*)malloc(sizeof(double) * (size_t)(N * K > 0 ? N * K : 1));
+    if (!a || !bt) {
+        free(a);
+        free(bt);
+        return -1;
+    }
+    for (int64_t i = 0; i < M * K; ++i) a[i] = dec16(dtype, A[i]);
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k)
+            bt[n * K + k] = dec16(dtype, layout == DTC_ORACLE_NN ? B[k * N + n] : B[n * K + k]);
+    *a_out = a;
+    *bt_out = bt;
+    return 0;
+}
+
+/* Full C. Returns 0 on success, -1 on bad arguments or out of memory. */
+int dtc_oracle_gemm16(int dtype, int layout, const uint16_t* A, const uint16_t* B, int64_t M,
+                      int64_t N, int64_t K, uint16_t* C, double* S, int nthreads) {
+    if (M < 0 || N < 0 || K < 0) return -1;
+    if (dtype != DTC_ORACLE_BF16 && dtype != DTC_ORACLE_F16) return -1;
+    if (layout != DTC_ORACLE_NT && layout != DTC_ORACLE_NN) return -1;
+    if (M == 0 || N == 0) return 0;
+    double *a, *bt;
+    if (decode16(dtype, layout, A, B, M, N, K, &a, &bt) != 0) return -1;
+    gemm_job proto = {a, bt, M, N, K, dtype, C, S, 0, 0};
+    run_rows(&proto, nthreads);
+    free(a);
+    free(bt);
+    return 0;
+}
+
+/* Selected outputs only: out[i] = C[rows[i], cols[i]] (and its unrounded sum). Used at sizes
+ * where the full product would take the oracle too long. Decodes only what it touches. */
+int dtc_oracle_gemm16_sampled(int dtype, int layout, const uint16_t* A, const uint16_t* B,
+                              int64_t M, int64_t N, int64_t K, const int64_t* rows,
+                              const int64_t* cols, int64_t count, uint16_t* Cout, double* Sout) {
+    if (M < 0 || N < 0 || K < 0 || count < 0) return -1;
+    if (dtype != DTC_ORACLE_BF16 && dtype != DTC_ORACLE_F16) return -1;
+    if (layout != DTC_ORACLE_NT && layout != DTC_ORACLE_NN) return -1;
+    for (int64_t i = 0; i < count; ++i) {
+        int64_t m = rows[i], n = cols[i];
+        if (m < 0 || m >= M || n < 0 || n >= N) return -1;
+        double acc = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            uint16_t b = layout == DTC_ORACLE_NN ? B[k * N + n] : B[n * K + k];
+            acc += dec16(dtype, A[m * K + k]) * dec16(dtype, b);
+        }
+        if (Sout) Sout[i] = acc;
+        if (Cout) Cout[i] = dtype == DTC_ORACLE_F16 ? dtc_oracle_enc_f16(acc) : dtc_oracle_enc_bf16(acc);
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* MXFP8 block-scaled GEMM (NT: A [M,K], B [N,K], scales [rows, ceil(K/128)])                   */
+/* ------------------------------------------------------------------------------------------ */
+
+#define DTC_ORACLE_SF_BLOCK 128
+
+/* Decode one operand with its scales applied: out[r][k] = e4m3(X[r,k]) * 2^(sf[r,k/128]-127).
+ * Exact in double. */
+static double* decode_scaled(const uint8_t* X, const uint8_t* sf, int64_t R, int64_t K) {
+    int64_t kb = (K + DTC_ORACLE_SF_BLOCK - 1) / DTC_ORACLE_SF_BLOCK;
+    double* out = (double*)malloc(sizeof(double) * (size_t)(R * K > 0 ? R * K : 1));
+    if (!out) return NULL;
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t k = 0; k < K; ++k)
+            out[r * K + k] = dtc_oracle_dec_e4m3(X[r * K + k]) *
+                             dtc_oracle_dec_e8m0(sf[r * kb + k / DTC_ORACLE_SF_BLOCK]);
+    return out;
+}
+
+int dtc_oracle_gemm_mxfp8(const uint8_t* A, const uint8_t* B, const uint8_t* sfA,
+                          const uint8_t* sfB, int64_t M, int64_t N, int64_t K, uint16_t* C,
+                          double* S, int nthreads) {
+    if (M < 0 || N < 0 || K < 0) return -1;
+    if (M == 0 || N == 0) return 0;
+    double* a = decode_scaled(A, sfA, M, K);
+    double* bt = decode_scaled(B, sfB, N, K);
+    if (!a || !bt) {
+        free(a);
+        free(bt);
+        return -1;
+    }
+    gemm_job proto = {a, bt, M, N, K, DTC_ORACLE_BF16, C, S, 0, 0};
+    run_rows(&proto, nthreads);
+    free(a);
+    free(bt);
+    return 0;
+}
+
+int dtc_oracle_gemm_mxfp8_sampled(const uint8_t* A, const uint8_t* B, const uint8_t* sfA,
+                                  const uint8_t* sfB, int64_t M, int64_t N, int64_t K,
+                                  const int64_t* rows, const int64_t* cols, int64_t count,
+                                  uint16_t* Cout, double* Sout) {
+    if (M < 0 || N < 0 || K < 0 || count < 0) return -1;
+    int64_t kb = (K + DTC_ORACLE_SF_BLOCK - 1) / DTC_ORACLE_SF_BLOCK;
+    for (int64_t i = 0; i < count; ++i) {
+        int64_t m = rows[i], n = cols[i];
+        if (m < 0 || m >= M || n < 0 || n >= N) return -1;
+        double acc = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double av = dtc_oracle_dec_e4m3(A[m * K + k]) *
+                        dtc_oracle_dec_e8m0(sfA[m * kb + k / DTC_ORACLE_SF_BLOCK]);
+            double bv = dtc_oracle_dec_e4m3(B[n * K + k]) *
+                        dtc_oracle_dec_e8m0(sfB[n * kb + k / DTC_ORACLE_SF_BLOCK]);
+            acc += av * bv;
+        }
+        if (Sout) Sout[i] = acc;
+        if (Cout) Cout[i] = dtc_oracle_enc_bf16(acc);
+    }
+    return 0;
+}
+
+/* Host cores this process may use (what the oracle's default thread count is based on). */
+int dtc_oracle_default_threads(void) {
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n > 0 ? (int)n : 1;
+}
