@@ -1,0 +1,202 @@
+"""ctypes binding of libdtc_gemm.so: argument marshalling only.
+
+Each function takes torch CUDA tensors, checks dtype/shape/contiguity/device, passes raw device
+pointers, sizes and the current (or given) stream to the C entry point of the same name, and
+raises GemmError with the library's message on a non-OK status. Every arithmetic step runs in
+the library's kernels.
+"""
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(HERE, "libdtc_gemm.so")
+
+GEMM_LAYOUT_NT, GEMM_LAYOUT_NN = 0, 1
+GEMM_VARIANT_AUTO, GEMM_VARIANT_1CTA, GEMM_VARIANT_2CTA, GEMM_VARIANT_SPLITK = 0, 1, 2, 3
+_STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTED", 3: "GEMM_ERR_CUDA",
+           4: "GEMM_ERR_TIMEOUT"}
+_DTYPE = {"bf16": 0, "f16": 1, "mxfp8": 2}
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__(f"{_STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class gemm_options(ctypes.Structure):
+    _fields_ = [("variant", ctypes.c_int), ("split_k", ctypes.c_int),
+                ("timeout_ns", ctypes.c_uint64), ("fault_inject", ctypes.c_int)]
+
+
+_lib = None
+
+
+def library_path():
+    return _LIB_PATH
+
+
+def lib():
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: build it with dense_tensor_core_gb300.build.build() "
+                "(there is no CPU fallback)")
+        L = ctypes.CDLL(_LIB_PATH)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        for name in ("gemm_bf16", "gemm_f16"):
+            f = getattr(L, name)
+            f.restype = i32
+            f.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp]
+        L.gemm_mxfp8.restype = i32
+        L.gemm_mxfp8.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, vp]
+        L.gemm_ex.restype = i32
+        L.gemm_ex.argtypes = [i32, vp, vp, vp, vp, vp, i64, i64, i64, i32,
+                              ctypes.POINTER(gemm_options), vp]
+        L.gemm_plan.restype = i32
+        L.gemm_plan.argtypes = [i32, i64, i64, i64, i32, ctypes.POINTER(gemm_options)]
+        L.gemm_last_error.restype = ctypes.c_char_p
+        L.gemm_last_error.argtypes = []
+        L.gemm_stream_status.restype = i32
+        L.gemm_stream_status.argtypes = [vp]
+        _lib = L
+    return _lib
+
+
+def gemm_last_error():
+    return lib().gemm_last_error().decode(errors="replace")
+
+
+def _check(status):
+    if status != 0:
+        raise GemmError(status, gemm_last_error())
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None and t.numel() > 0 else ctypes.c_void_p(0)
+
+
+def _layout_code(layout):
+    return {"NT": 0, "NN": 1, 0: 0, 1: 1}[layout]
+
+
+def _shapes16(A, B, layout):
+    if A.dim() != 2 or B.dim() != 2:
+        raise ValueError("A and B must be 2-D")
+    M, K = A.shape
+    if _layout_code(layout) == GEMM_LAYOUT_NT:
+        N, Kb = B.shape
+    else:
+        Kb, N = B.shape
+    if Kb != K:
+        raise ValueError(f"inner sizes differ: A is {tuple(A.shape)}, B is {tuple(B.shape)} ({layout})")
+    return M, N, K
+
+
+def _check_tensor(t, dtype, name):
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (dense row-major)")
+
+
+def _out(C, M, N, dtype, device):
+    if C is None:
+        return torch.empty((M, N), dtype=dtype, device=device)
+    _check_tensor(C, dtype, "C")
+    if tuple(C.shape) != (M, N):
+        raise ValueError(f"C must be {(M, N)}, got {tuple(C.shape)}")
+    return C
+
+
+def _options(variant, split_k, timeout_ns, fault_inject):
+    return gemm_options(variant, split_k, timeout_ns, fault_inject)
+
+
+def _gemm16(name, dtype, A, B, C, layout, stream):
+    _check_tensor(A, dtype, "A")
+    _check_tensor(B, dtype, "B")
+    M, N, K = _shapes16(A, B, layout)
+    C = _out(C, M, N, dtype, A.device)
+    _check(getattr(lib(), name)(_ptr(A), _ptr(B), _ptr(C), M, N, K, _layout_code(layout),
+                                _stream_handle(stream)))
+    return C
+
+
+def gemm_bf16(A, B, C=None, layout="NT", stream=None):
+    """C[M,N] = A[M,K] . B^T (NT: B is [N,K]) or A . B (NN: B is [K,N]); bf16 in/out."""
+    return _gemm16("gemm_bf16", torch.bfloat16, A, B, C, layout, stream)
+
+
+def gemm_f16(A, B, C=None, layout="NT", stream=None):
+    """As gemm_bf16 with fp16 operands and output."""
+    return _gemm16("gemm_f16", torch.float16, A, B, C, layout, stream)
+
+
+def _check_mxfp8(A, B, sfA, sfB):
+    _check_tensor(A, torch.uint8, "A")
+    _check_tensor(B, torch.uint8, "B")
+    _check_tensor(sfA, torch.uint8, "sfA")
+    _check_tensor(sfB, torch.uint8, "sfB")
+    M, K = A.shape
+    N, Kb = B.shape
+    if Kb != K:
+        raise ValueError("A and B must both be [rows, K]")
+    kb = (K + 127) // 128
+    if tuple(sfA.shape) != (M, kb) or tuple(sfB.shape) != (N, kb):
+        raise ValueError(f"scales must be [M, {kb}] and [N, {kb}]")
+    return M, N, K
+
+
+def gemm_mxfp8(A, B, sfA, sfB, C=None, stream=None):
+    """Block-scaled e4m3 NT GEMM. A [M,K], B [N,K] e4m3 codes (uint8 tensors), sfA [M,ceil(K/128)],
+    sfB [N,ceil(K/128)] E8M0 codes (uint8); C bf16 [M,N]."""
+    M, N, K = _check_mxfp8(A, B, sfA, sfB)
+    C = _out(C, M, N, torch.bfloat16, A.device)
+    _check(lib().gemm_mxfp8(_ptr(A), _ptr(B), _ptr(sfA), _ptr(sfB), _ptr(C), M, N, K,
+                            _stream_handle(stream)))
+    return C
+
+
+def gemm_ex(kind, A, B, C=None, layout="NT", sfA=None, sfB=None, variant=0, split_k=0,
+            timeout_ns=0, fault_inject=0, stream=None):
+    """Any of the three products with options (variant, split_k, wait limit, test hook)."""
+    if kind == "mxfp8":
+        M, N, K = _check_mxfp8(A, B, sfA, sfB)
+        C = _out(C, M, N, torch.bfloat16, A.device)
+    else:
+        dt = torch.bfloat16 if kind == "bf16" else torch.float16
+        _check_tensor(A, dt, "A")
+        _check_tensor(B, dt, "B")
+        M, N, K = _shapes16(A, B, layout)
+        C = _out(C, M, N, dt, A.device)
+    opts = _options(variant, split_k, timeout_ns, fault_inject)
+    _check(lib().gemm_ex(_DTYPE[kind], _ptr(A), _ptr(B), _ptr(sfA), _ptr(sfB), _ptr(C), M, N, K,
+                         _layout_code(layout), ctypes.byref(opts), _stream_handle(stream)))
+    return C
+
+
+def gemm_plan(kind, M, N, K, layout="NT", variant=0, split_k=0):
+    """The variant the library would launch for these sizes (raises if they would be rejected)."""
+    opts = _options(variant, split_k, 0, 0)
+    v = lib().gemm_plan(_DTYPE[kind], M, N, K, _layout_code(layout), ctypes.byref(opts))
+    if v < 0:
+        raise GemmError(-v, gemm_last_error())
+    return v
+
+
+def gemm_stream_status(stream=None):
+    """Synchronise the stream and raise GemmError if a device-side wait gave up."""
+    _check(lib().gemm_stream_status(_stream_handle(stream)))

@@ -1,0 +1,135 @@
+/*
+ * dtc_gemm.h -- C ABI of the GB300 (sm_103a) dense GEMM library.
+ *
+ * The operation (all entry points):  C[M,N] = A[M,K] . Bop[K,N], accumulated in fp32 in Tensor
+ * Memory and rounded once to the output format (round to nearest even).
+ *   - "NT": B is stored row-major [N,K] and Bop = B^T. This is the product of TileLang SM100
+ *     Support (Preview), "Code Example" (A is (M, K), B is (N, K), the gemm uses trans_B=True,
+ *     accumulator T.alloc_tmem(..., "float")) and "Compilation and Usage"
+ *     (ref_c = (a.float() @ b.T.float()).to(torch.bfloat16)).
+ *   - "NN": B is stored row-major [K,N] and Bop = B. This is the product of tilelang (velog),
+ *     section 1.1 Front-End DSL (A is (M, K), B is (K, N), accum_dtype "float").
+ *   A is always row-major [M,K]; C is always row-major [M,N]. Every row is dense (row stride =
+ *   number of columns), as the generated host code of tilelang (velog) section 1.3 also requires.
+ *
+ * Pointers: A, B, C (and sfA, sfB) are DEVICE pointers on the current CUDA device, owned by the
+ * caller; the library keeps no reference after the call returns. C must not overlap A, B or the
+ * scales. All pointers must be 16-byte aligned (the tensor-memory-access unit's global address
+ * rule), and every row must start on a 16-byte boundary (see each function).
+ *
+ * Asynchrony: every GEMM call only enqueues work on `stream` (0 = the legacy default stream) and
+ * returns; the status it returns covers argument checks and the launch. A device-side wait that
+ * gave up (see GEMM_ERR_TIMEOUT) is reported by gemm_stream_status().
+ *
+ * Errors: a non-zero status leaves a one-line message for the calling thread in
+ * gemm_last_error(). No call ever aborts the process or traps on the device.
+ *
+ * Degenerate sizes: M == 0 or N == 0 does nothing and returns GEMM_OK. K == 0 writes C = +0 (the
+ * empty sum) with an asynchronous memset on `stream`.
+ */
+#ifndef DTC_GEMM_H
+#define DTC_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* CUDA's stream handle, without including the CUDA headers. */
+typedef struct CUstream_st* dtc_stream_t;
+
+typedef enum {
+    GEMM_LAYOUT_NT = 0, /* B is [N,K] row-major: C = A . B^T */
+    GEMM_LAYOUT_NN = 1  /* B is [K,N] row-major: C = A . B   */
+} gemm_layout;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1, /* rejected before any CUDA call: see the rules per function */
+    GEMM_ERR_UNSUPPORTED = 2, /* the current device is not an sm_103 GPU, or a variant that the
+                                 requested shape or layout does not allow was forced */
+    GEMM_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed; the message names it */
+    GEMM_ERR_TIMEOUT = 4      /* a device-side wait gave up (reported by gemm_stream_status) */
+} gemm_status;
+
+/* Kernel variants (gemm_options.variant). AUTO picks per shape. */
+typedef enum {
+    GEMM_VARIANT_AUTO = 0,
+    GEMM_VARIANT_1CTA = 1,   /* persistent 128x256 tiles, one CTA per tile */
+    GEMM_VARIANT_2CTA = 2,   /* persistent 256x256 tiles on a CTA pair (cluster 2x1) */
+    GEMM_VARIANT_SPLITK = 3  /* 128 x BN tiles with K split across CTAs (skinny, memory-bound) */
+} gemm_variant;
+
+typedef struct {
+    int variant;          /* a gemm_variant; GEMM_VARIANT_AUTO (0) chooses per shape */
+    int split_k;          /* SPLITK only: number of K-slices, 0 = choose */
+    uint64_t timeout_ns;  /* limit of every device-side wait; 0 = the default (2 s) */
+    int fault_inject;     /* test hook, 0 in normal use. 1 = the load producer skips its first
+                             stage, so the consumer's bounded wait runs out and the call reports
+                             GEMM_ERR_TIMEOUT through gemm_stream_status. */
+} gemm_options;
+
+/*
+ * bf16 operands, fp32 accumulation, bf16 output.
+ *   A: [M,K] bf16. B: [N,K] bf16 (NT) or [K,N] bf16 (NN). C: [M,N] bf16.
+ *   INVALID_ARG when: M, N or K is negative or above 2^31-1; layout is not NT or NN; a pointer
+ *   needed for the sizes is NULL or not 16-byte aligned; a row is not a multiple of 16 bytes
+ *   (K % 8 != 0 for A and for NT B; N % 8 != 0 for NN B and for C).
+ * (TileLang SM100 Support (Preview), "Code Example" / "Compilation and Usage".)
+ */
+int gemm_bf16(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int layout,
+              dtc_stream_t stream);
+
+/*
+ * fp16 operands, fp32 accumulation, fp16 output (IEEE round to nearest even; overflow gives
+ * +-inf). Same layouts and argument rules as gemm_bf16.
+ * (tilelang (velog), section 1.1 Front-End DSL: dtype "float16", accum_dtype "float"; section 1.3
+ * Generated Kernel Source: the fp32 accumulator is cast to half on output.)
+ */
+int gemm_f16(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int layout,
+             dtc_stream_t stream);
+
+/*
+ * MXFP8 block-scaled GEMM, NT only:
+ *   C[m,n] = bf16( sum_k e4m3(A[m,k]) 2^(sfA[m,k/128]-127) * e4m3(B[n,k]) 2^(sfB[n,k/128]-127) )
+ *   A: [M,K] e4m3 (OCP "fn" encoding). B: [N,K] e4m3. sfA: [M, ceil(K/128)] E8M0 bytes.
+ *   sfB: [N, ceil(K/128)] E8M0 bytes. C: [M,N] bf16. One scale per row per 128 K-elements for
+ *   both operands (05 Blackwell TCGEN05 GEMM tutorial, "Advanced": gemm_blockscaled with
+ *   sf_a_granularity_k = sf_b_granularity_k = 128, the "1d1d" example).
+ *   INVALID_ARG as for gemm_bf16, with K % 16 != 0 for the e4m3 rows; the scale arrays have no
+ *   alignment rule.
+ */
+int gemm_mxfp8(const void* A, const void* B, const void* sfA, const void* sfB, void* C,
+               int64_t M, int64_t N, int64_t K, dtc_stream_t stream);
+
+/*
+ * The same three operations with options (variant choice, wait limit, test hook).
+ * dtype: 0 = bf16, 1 = fp16, 2 = mxfp8 (sfA/sfB are ignored for 0 and 1; layout must be NT
+ * for 2). opts may be NULL (all defaults).
+ */
+int gemm_ex(int dtype, const void* A, const void* B, const void* sfA, const void* sfB, void* C,
+            int64_t M, int64_t N, int64_t K, int layout, const gemm_options* opts,
+            dtc_stream_t stream);
+
+/* The variant that gemm_ex/gemm_* would launch for these arguments (GEMM_VARIANT_*), or a
+ * negative gemm_status if they would be rejected. Makes no CUDA call except device queries. */
+int gemm_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm_options* opts);
+
+/* Message for the calling thread's most recent non-OK return ("" if none). Valid until that
+ * thread's next call into the library. */
+const char* gemm_last_error(void);
+
+/*
+ * Synchronises `stream`, then reports and clears the device status word of the current device:
+ * GEMM_ERR_TIMEOUT if a kernel's bounded wait gave up since the last check (the kernel then
+ * released its tensor memory and returned early, so C is incomplete), GEMM_ERR_CUDA if the
+ * stream reported an error, GEMM_OK otherwise.
+ */
+int gemm_stream_status(dtc_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DTC_GEMM_H */

@@ -1,0 +1,104 @@
+"""The C ABI without a GPU: the library loads, exports every function include/dtc_gemm.h
+declares, and rejects bad arguments before making any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(HEADER_DIR)):
+        if not h.endswith(".h"):
+            continue
+        src = open(os.path.join(HEADER_DIR, h)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        src = re.sub(r"typedef[^;]*;", "", src, flags=re.S)
+        for m in re.finditer(r"\b([A-Za-z_][A-Za-z0-9_]*)\s*\([^;{]*\)\s*;", src):
+            names.append(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def L():
+    from dense_tensor_core_gb300 import _binding, build
+
+    build.build()
+    return _binding.lib()
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("gemm_bf16", "gemm_f16", "gemm_mxfp8", "gemm_ex", "gemm_plan", "gemm_last_error",
+              "gemm_stream_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for n in declared_functions():
+        assert hasattr(L, n), f"{n} is declared in include/ but not exported"
+
+
+def _call16(L, name, A=0x1000, B=0x2000, C=0x3000, M=16, N=16, K=16, layout=0):
+    return getattr(L, name)(ctypes.c_void_p(A), ctypes.c_void_p(B), ctypes.c_void_p(C), M, N, K,
+                            layout, None)
+
+
+INVALID, UNSUPPORTED = 1, 2
+
+
+@pytest.mark.parametrize("name", ["gemm_bf16", "gemm_f16"])
+@pytest.mark.parametrize(
+    "kw",
+    [
+        dict(layout=2),
+        dict(M=-1),
+        dict(K=-8),
+        dict(N=2 ** 31),
+        dict(A=0),
+        dict(B=0),
+        dict(C=0),
+        dict(A=0x1008),  # 8-byte aligned only
+        dict(C=0x3004),
+        dict(K=12),  # A rows of 24 bytes
+        dict(N=12),  # C rows of 24 bytes
+        dict(N=12, layout=1),
+    ],
+)
+def test_invalid_arguments_rejected_before_cuda(L, name, kw):
+    assert _call16(L, name, **kw) == INVALID
+    assert L.gemm_last_error()  # a message is left for the caller
+
+
+def test_empty_output_is_a_no_op(L):
+    assert _call16(L, "gemm_bf16", A=0, B=0, C=0, M=0) == 0
+    assert _call16(L, "gemm_f16", A=0, B=0, C=0, N=0, layout=1) == 0
+
+
+def test_mxfp8_rules(L):
+    vp = ctypes.c_void_p
+    # K must keep e4m3 rows 16-byte aligned
+    assert L.gemm_mxfp8(vp(0x1000), vp(0x2000), vp(0x10), vp(0x20), vp(0x3000), 16, 16, 24, None) == INVALID
+    # scale arrays are required
+    assert L.gemm_mxfp8(vp(0x1000), vp(0x2000), vp(0), vp(0x20), vp(0x3000), 16, 16, 32, None) == INVALID
+    # NN is not offered for the block-scaled product
+    rc = L.gemm_ex(2, vp(0x1000), vp(0x2000), vp(0x10), vp(0x20), vp(0x3000), 16, 16, 32, 1, None, None)
+    assert rc == UNSUPPORTED
+
+
+def test_binding_checks_tensors_without_gpu():
+    import torch
+
+    import dense_tensor_core_gb300 as dtc
+
+    A = torch.zeros(4, 8, dtype=torch.bfloat16)
+    with pytest.raises((ValueError, TypeError)):
+        dtc.gemm_bf16(A, A)  # CPU tensors are refused before any call
+    with pytest.raises(TypeError):
+        dtc.gemm_f16(A, A)

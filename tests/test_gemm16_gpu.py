@@ -1,0 +1,152 @@
+"""GPU parity of the bf16/fp16 GEMM (NT and NN) against the CPU oracle, through the C ABI.
+
+Small and medium sizes are compared on every element of C; the benchmark sizes (in the launch
+configuration the benchmark times) on sampled elements, which the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dense_tensor_core_gb300 import workloads
+from parity import check_close, sample_positions, to_device16, values16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from dense_tensor_core_gb300 import build
+
+    build.build()
+    import dense_tensor_core_gb300 as dtc
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return dtc
+
+
+def run16(kind, layout, A, B, M, N, K, variant=0, **kw):
+    import dense_tensor_core_gb300 as dtc
+
+    At, Bt = to_device16(A, kind), to_device16(B, kind)
+    C = dtc.gemm_ex(kind, At, Bt, layout=layout, variant=variant, **kw)
+    dtc.gemm_stream_status()
+    return C.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def full_check(kind, layout, M, N, K, seed, variant=0):
+    A, B = workloads.make16(kind, layout, M, N, K, seed)
+    C = run16(kind, layout, A, B, M, N, K, variant)
+    ref = oracle.gemm16(kind, layout, A, B, M, N, K)
+    return check_close(values16(C, kind), values16(ref, kind), f"{kind} {layout} {M}x{N}x{K}")
+
+
+SHAPES = [
+    (128, 256, 64),    # one tile, one K-block
+    (256, 256, 512),   # two tiles, eight K-blocks
+    (300, 520, 200),   # ragged in M, N and K (partial tiles and a partial K-block)
+    (1, 8, 8),         # smallest legal product
+    (129, 264, 72),    # one row / one 8-column group past a tile; K = one block + 8
+    (640, 768, 1024),  # 15 tiles, 16 K-blocks
+]
+
+
+@pytest.mark.parametrize("kind", ["bf16", "f16"])
+@pytest.mark.parametrize("layout", ["NT", "NN"])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_small_shapes_full_parity(kind, layout, shape):
+    M, N, K = shape
+    full_check(kind, layout, M, N, K, seed=M + N + K)
+
+
+@pytest.mark.parametrize("kind,layout", [("bf16", "NT"), ("f16", "NN")])
+def test_more_tiles_than_sms_full_parity(kind, layout):
+    # 256 tiles (> 152 SMs): CTAs loop over several tiles, the two accumulators alternate, and
+    # with K = 128 the epilogue of one tile overlaps the short main loop of the next.
+    full_check(kind, layout, 4096, 2048, 128, seed=77)
+
+
+def test_config_bf16_nt_256x256x512_full():
+    w = workloads.WORKLOADS["bf16_nt_256x256x512"]
+    full_check(w.kind, w.layout, w.M, w.N, w.K, w.seed)
+
+
+def test_config_f16_nn_1024_full():
+    w = workloads.WORKLOADS["f16_nn_1024x1024x1024"]
+    full_check(w.kind, w.layout, w.M, w.N, w.K, w.seed)
+
+
+@pytest.mark.parametrize("name", ["bf16_nt_4096x4096x8192", "bf16_nt_8192x8192x8192",
+                                  "bf16_nt_128x8192x8192"])
+def test_benchmark_sizes_sampled(name):
+    w = workloads.WORKLOADS[name]
+    A, B = workloads.make(w)
+    C = run16(w.kind, w.layout, A, B, w.M, w.N, w.K)
+    r, c = sample_positions(w.M, w.N, count=3000, seed=w.seed)
+    # plus one full row and one full column
+    r = np.concatenate([r, np.full(w.N, w.M // 3), np.arange(w.M)])
+    c = np.concatenate([c, np.arange(w.N), np.full(w.M, w.N // 5)])
+    ref, _ = oracle.gemm16_sampled(w.kind, w.layout, A, B, w.M, w.N, w.K, r, c)
+    check_close(values16(C[r, c], w.kind), values16(ref, w.kind), name)
+
+
+def test_k_zero_writes_zeros_and_empty_is_noop():
+    import dense_tensor_core_gb300 as dtc
+
+    A = torch.empty((64, 0), dtype=torch.bfloat16, device="cuda")
+    B = torch.empty((32, 0), dtype=torch.bfloat16, device="cuda")
+    C = torch.full((64, 32), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dtc.gemm_bf16(A, B, C)
+    dtc.gemm_stream_status()
+    assert torch.equal(C, torch.zeros_like(C))
+    A0 = torch.empty((0, 16), dtype=torch.float16, device="cuda")
+    B0 = torch.empty((16, 16), dtype=torch.float16, device="cuda")
+    C0 = dtc.gemm_f16(A0, B0, layout="NN")
+    assert C0.shape == (0, 16)
+
+
+@pytest.mark.parametrize("layout", ["NT", "NN"])
+def test_writes_exactly_C(layout):
+    # C sits inside a larger buffer filled with NaN: every element of C must be overwritten and
+    # nothing around it touched (ragged edges clip stores to [M, N]).
+    import dense_tensor_core_gb300 as dtc
+
+    M, N, K = 200, 264, 136
+    A, B = workloads.make16("bf16", layout, M, N, K, 5)
+    guard = 4096
+    buf = torch.full((guard * 2 + M * N,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    C = buf[guard:guard + M * N].view(M, N)
+    dtc.gemm_bf16(to_device16(A, "bf16"), to_device16(B, "bf16"), C, layout=layout)
+    dtc.gemm_stream_status()
+    h = buf.float().cpu()
+    assert torch.isnan(h[:guard]).all() and torch.isnan(h[guard + M * N:]).all()
+    assert not torch.isnan(h[guard:guard + M * N]).any()
+
+
+def test_runs_on_a_side_stream():
+    import dense_tensor_core_gb300 as dtc
+
+    M, N, K = 256, 512, 256
+    A, B = workloads.make16("f16", "NT", M, N, K, 6)
+    s = torch.cuda.Stream()
+    At, Bt = to_device16(A, "f16"), to_device16(B, "f16")
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        C = dtc.gemm_f16(At, Bt, stream=s)
+    dtc.gemm_stream_status(s)
+    ref = oracle.gemm16("f16", "NT", A, B, M, N, K)
+    got = C.view(torch.int16).cpu().numpy().view(np.uint16)
+    check_close(values16(got, "f16"), values16(ref, "f16"), "side stream")
+
+
+def test_repeated_calls_are_deterministic():
+    import dense_tensor_core_gb300 as dtc
+
+    M, N, K = 512, 512, 1024
+    A, B = workloads.make16("bf16", "NT", M, N, K, 8)
+    At, Bt = to_device16(A, "bf16"), to_device16(B, "bf16")
+    C1 = dtc.gemm_bf16(At, Bt)
+    C2 = dtc.gemm_bf16(At, Bt)
+    dtc.gemm_stream_status()
+    assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
