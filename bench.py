@@ -1,0 +1,449 @@
+"""Benchmark: GEMM TFLOP/s (2MNK / device time) and % of the GB300 dense tensor peak.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one GEMM through the C ABI (argument checks, tensor-map encoding, launch, kernel) on
+the workload's synthetic inputs, already resident in HBM. W untimed warm-up steps, then exactly K
+timed steps; L2 is flushed (a 256 MiB device write) before every timed step and each step is
+timed on its own with CUDA events on the launching stream, so the flush is outside the timed
+work. Under torchrun each rank runs an independent replica on its own GPU (the GEMM does not
+shard across GPUs here: replicas only, no collective), the step time is the max over ranks and
+rank 0 prints one JSON line.
+
+--impl reference times the CPU oracle (the plain fp64 definition) on the host cores on a bounded
+sample of the same workload per step (a block of output rows), in the same metric and unit.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s (2MNK/device time) and % of GB300 dense tensor peak, 1 GPU"
+UNIT = "TFLOP/s"
+FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+CSRC = os.path.join(ROOT, "dense_tensor_core_gb300", "csrc")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+# ------------------------------------------------------------------------------------------------
+# helpers (no GPU needed; the CPU tests exercise them)
+# ------------------------------------------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(value, world):
+    """Max of a float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(CSRC)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(CSRC, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload, kernel):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current source."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = rec.get(workload, {})
+    if e.get("kernel") != kernel or e.get("source_sha") != source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def parse_clocks(csv_text, t0=None, t1=None):
+    """Summarise nvidia-smi samples (the recipe's query, with a leading timestamp column)."""
+    rows = []
+    for line in csv_text.strip().splitlines():
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 10 or not parts[0].replace(".", "", 1).isdigit():
+            continue
+        try:
+            rows.append({"t": float(parts[0]), "sm": float(parts[2].split()[0]),
+                         "max": float(parts[3].split()[0]), "hw": parts[6], "hwt": parts[7],
+                         "swt": parts[8], "swp": parts[9]})
+        except (ValueError, IndexError):
+            continue
+    window = "timed"
+    sel = [r for r in rows if t0 is not None and t0 <= r["t"] <= t1]
+    if not sel:
+        sel, window = rows, "whole run"
+    if not sel:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": "none"}
+    reasons = set()
+    for r in sel:
+        for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                          ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+            if r[key].lower() == "active":
+                reasons.add(name)
+    return {"sm_mhz": statistics.median(r["sm"] for r in sel),
+            "sm_max_mhz": max(r["max"] for r in sel), "reasons": sorted(reasons),
+            "samples": len(sel), "window": window}
+
+
+class ClockSampler:
+    """nvidia-smi in the background (the recipe's clocks line) with host timestamps."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index, period_ms=20):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.out = tempfile.TemporaryFile(mode="w+")
+
+    def __enter__(self):
+        cmd = ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+               "--format=csv,noheader", f"-lms", str(self.period)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True, bufsize=1)
+        except OSError:
+            self.proc = None
+        self.lines = []
+        if self.proc:
+            import threading
+
+            def pump():
+                for line in self.proc.stdout:
+                    self.lines.append(f"{time.time():.6f}, {line.strip()}")
+
+            self.thread = threading.Thread(target=pump, daemon=True)
+            self.thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(self.period / 1000.0 * 2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def text(self):
+        return "\n".join(self.lines)
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle leg
+# ------------------------------------------------------------------------------------------------
+
+def oracle_rows(w, inputs, rows):
+    """Run the oracle on the first `rows` output rows of workload w; returns seconds taken."""
+    import numpy as np
+
+    import oracle
+
+    t0 = time.perf_counter()
+    if w.kind == "mxfp8":
+        A, B, sfA, sfB = inputs
+        kb = (w.K + 127) // 128
+        oracle.gemm_mxfp8(A[:rows], B, sfA[:rows].reshape(rows, kb), sfB, rows, w.N, w.K)
+    else:
+        A, B = inputs
+        oracle.gemm16(w.kind, w.layout, np.ascontiguousarray(A[:rows]), B, rows, w.N, w.K)
+    return time.perf_counter() - t0
+
+
+def calibrate_rows(w, inputs, target_s):
+    """Rows of C the oracle computes in about target_s seconds (at least 1, at most M).
+
+    Two probes separate the fixed cost of a call (decoding B) from the cost per output row."""
+    import oracle
+
+    T = oracle.threads()  # probes are whole multiples of the worker count
+    r1, r2 = min(4 * T, w.M), min(16 * T, w.M)
+    t1 = oracle_rows(w, inputs, r1)
+    t2 = oracle_rows(w, inputs, r2)
+    per_row = (t2 - t1) / (r2 - r1) if r2 > r1 else 0.0
+    if per_row <= 0.0:
+        per_row = t2 / max(r2, 1)
+    fixed = max(t1 - r1 * per_row, 0.0)
+    return max(1, min(w.M, int((target_s - fixed) / per_row))), per_row
+
+
+def cpu_baseline(w, inputs, target_s=15.0):
+    import oracle
+
+    rows, _ = calibrate_rows(w, inputs, target_s)
+    dt = oracle_rows(w, inputs, rows)
+    flops = 2.0 * rows * w.N * w.K
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"{rows} of {w.M} output rows of {w.name} (all N={w.N} columns, full K), "
+                      f"{dt:.1f} s"}
+
+
+# ------------------------------------------------------------------------------------------------
+# arms
+# ------------------------------------------------------------------------------------------------
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+
+    inputs = __import__("dense_tensor_core_gb300.workloads", fromlist=["make"]).make(w)
+    per_step_budget = min(10.0, 150.0 / max(1, args.steps + args.warmup))
+    rows, _ = calibrate_rows(w, inputs, per_step_budget)
+    for _ in range(args.warmup):
+        oracle_rows(w, inputs, rows)
+    times = [oracle_rows(w, inputs, rows) for _ in range(args.steps)]
+    total = sum(times)
+    flops = 2.0 * rows * w.N * w.K * args.steps
+    value = flops / total / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout,
+                   "kind": w.kind, "step": f"oracle on {rows} output rows (bounded sample)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+                         "sample": f"{rows} of {w.M} output rows per step, full N and K"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w):
+    import numpy as np
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    from dense_tensor_core_gb300 import build as cuda_build
+
+    cuda_build.build()
+    import dense_tensor_core_gb300 as dtc
+    from dense_tensor_core_gb300 import workloads
+
+    inputs = workloads.make(w)
+    if w.kind == "mxfp8":
+        A_h, B_h, sfA_h, sfB_h = inputs
+        A = torch.from_numpy(A_h).to(dev)
+        B = torch.from_numpy(B_h).to(dev)
+        sfA = torch.from_numpy(sfA_h).to(dev)
+        sfB = torch.from_numpy(sfB_h).to(dev)
+        out_dtype = torch.bfloat16
+        host_in = [torch.from_numpy(x).pin_memory() for x in inputs]
+        dev_in = [A, B, sfA, sfB]
+    else:
+        A_h, B_h = inputs
+        t16 = torch.bfloat16 if w.kind == "bf16" else torch.float16
+        A = torch.from_numpy(A_h.view(np.int16)).view(t16).to(dev)
+        B = torch.from_numpy(B_h.view(np.int16)).view(t16).to(dev)
+        out_dtype = t16
+        host_in = [A.cpu().pin_memory(), B.cpu().pin_memory()]
+        dev_in = [A, B]
+    C = torch.empty((w.M, w.N), dtype=out_dtype, device=dev)
+    host_out = torch.empty((w.M, w.N), dtype=out_dtype).pin_memory()
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        if w.kind == "mxfp8":
+            dtc.gemm_ex("mxfp8", A, B, C, sfA=sfA, sfB=sfB, variant=args.variant, stream=stream)
+        else:
+            dtc.gemm_ex(w.kind, A, B, C, layout=w.layout, variant=args.variant,
+                        split_k=args.split_k, stream=stream)
+
+    variant = dtc.gemm_plan(w.kind, w.M, w.N, w.K, w.layout, variant=args.variant,
+                            split_k=args.split_k)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    dtc.gemm_stream_status(stream)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local if world > 1 else 0) as clk:
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        t0 = time.time()
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        t1 = time.time()
+    dtc.gemm_stream_status(stream)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = max_over_ranks(sum(step_ms), world)
+    ms_per_step = total_ms / args.steps
+    flops_step = float(w.flops)
+    value = world * flops_step * args.steps / (total_ms / 1e3) / 1e12
+    kernel_ms = statistics.mean(step_ms)  # one launch of our kernel per step
+
+    # end to end through the public call with host buffers: H2D inputs, GEMM, D2H result
+    e2e_steps = max(1, min(args.steps, 20))  # each step moves the whole workload over the host link
+    for _ in range(2):
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        step()
+        host_out.copy_(C, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        step()
+        host_out.copy_(C, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    dtc.gemm_stream_status(stream)
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+    e2e_value = world * flops_step * e2e_steps / (e2e_ms / 1e3) / 1e12
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    if w.kind == "mxfp8":
+        # fp8 dense rate = 2x the bf16 rate (nominal 4.5 vs 2.25 PFLOP/s)
+        peak = 2.0 * peaks["bf16_tflops"]
+        peak_note = f"2 x {peak_src} bf16 burst (nominal fp8:bf16 ratio)"
+    else:
+        peak = peaks["bf16_tflops"]
+        peak_note = f"{peak_src} bf16 burst (kernel timed alone)"
+    kernel_name = {0: "auto", 1: "gemm16_1cta_kernel", 2: "gemm16_2cta_kernel",
+                   3: "gemm16_splitk_kernel"}.get(variant, str(variant))
+    if w.kind == "mxfp8":
+        kernel_name = "gemm_mxfp8_kernel"
+    achieved = flops_step / (kernel_ms / 1e3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": recorded_traffic(w.name, kernel_name),
+                "kernel": kernel_name, "peak_source": peak_note,
+                "algorithmic_flops_per_launch": flops_step}
+    if w.name == "bf16_nt_128x8192x8192" or (w.M <= 256 and w.kind != "mxfp8"):
+        bw = w.min_bytes / (kernel_ms / 1e3) / 1e9
+        roofline = {"bound": "hbm", "achieved": bw, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": bw / peaks["hbm_gbs"], "traffic": recorded_traffic(w.name, kernel_name),
+                    "kernel": kernel_name, "peak_source": f"{peak_src} HBM copy bandwidth",
+                    "algorithmic_bytes_per_launch": w.min_bytes}
+    clocks = parse_clocks(clk.text(), t0, t1)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.kind == "bf16" else ("f16" if w.kind == "f16" else "e4m3"),
+        "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout,
+                   "kind": w.kind, "variant": kernel_name, "parallelism": f"replicas x{world}",
+                   "l2": "flushed (256 MiB device write) before every timed step, outside the "
+                         "step's CUDA-event pair",
+                   "pct_of_dense_peak_nominal": 100.0 * achieved /
+                   (4500.0 if w.kind == "mxfp8" else 2250.0),
+                   "timed_wall_ms": 1e3 * (t1 - t0)},
+        "roofline": roofline,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if not args.skip_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, inputs, target_s=args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=None, help="workload name (default: the headline)")
+    p.add_argument("--variant", type=int, default=0, help="0 auto, 1 one-CTA, 2 CTA pair, 3 split-K")
+    p.add_argument("--split-k", type=int, default=0)
+    p.add_argument("--skip-cpu-baseline", action="store_true",
+                   help="omit the oracle timing (profiling runs)")
+    p.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be at least 3")
+    from dense_tensor_core_gb300 import workloads
+
+    w = workloads.WORKLOADS[args.workload or workloads.HEADLINE]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,96 @@
+"""The benchmark's host logic on CPU: clock parsing, traffic staleness, max-over-ranks with two
+gloo ranks, and the reference (oracle) arm end to end on the small workload."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+import bench
+from conftest import ROOT
+
+
+def test_parse_clocks_selects_the_timed_window_and_flags_reasons():
+    lines = [
+        "100.0, 0, 1900 MHz, 2070 MHz, 900 W, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "101.0, 0, 2000 MHz, 2070 MHz, 1300 W, 0x4, Not Active, Not Active, Not Active, Active",
+        "102.0, 0, 1950 MHz, 2070 MHz, 1300 W, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "109.0, 0, 300 MHz, 2070 MHz, 100 W, 0x0, Not Active, Not Active, Not Active, Not Active",
+    ]
+    c = bench.parse_clocks("\n".join(lines), 100.5, 102.5)
+    assert c["samples"] == 2 and c["window"] == "timed"
+    assert c["sm_mhz"] == 1975.0 and c["sm_max_mhz"] == 2070.0
+    assert c["reasons"] == ["sw_power_cap"]
+    c2 = bench.parse_clocks("\n".join(lines), 200.0, 201.0)
+    assert c2["window"] == "whole run" and c2["samples"] == 4
+    assert bench.parse_clocks("", 0, 1)["samples"] == 0
+
+
+def test_traffic_record_is_dropped_when_the_kernel_source_changes(tmp_path, monkeypatch):
+    rec = {"w": {"kernel": "k", "source_sha": bench.source_hash(), "dram_bytes_per_launch": 123}}
+    f = tmp_path / "traffic.json"
+    f.write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.recorded_traffic("w", "k") == 123
+    assert bench.recorded_traffic("w", "other_kernel") is None
+    rec["w"]["source_sha"] = "0" * 16
+    f.write_text(json.dumps(rec))
+    assert bench.recorded_traffic("w", "k") is None
+
+
+_WORKER = r"""
+import os, sys
+sys.path.insert(0, {root!r})
+import torch.distributed as dist
+import bench
+dist.init_process_group("gloo")
+rank = dist.get_rank()
+v = bench.max_over_ranks(10.0 + 5.0 * rank, dist.get_world_size())
+bench.barrier(dist.get_world_size())
+print("RESULT", rank, v, flush=True)
+dist.destroy_process_group()
+"""
+
+
+def test_max_over_ranks_with_two_gloo_ranks(tmp_path):
+    script = tmp_path / "w.py"
+    script.write_text(_WORKER.format(root=ROOT))
+    env = dict(os.environ, MASTER_ADDR="127.0.0.1", MASTER_PORT="29531", WORLD_SIZE="2")
+    procs = []
+    for r in range(2):
+        e = dict(env, RANK=str(r), LOCAL_RANK=str(r))
+        procs.append(subprocess.Popen([sys.executable, str(script)], env=e, stdout=subprocess.PIPE,
+                                      stderr=subprocess.PIPE, text=True))
+    outs = [p.communicate(timeout=120) for p in procs]
+    for p, (o, e) in zip(procs, outs):
+        assert p.returncode == 0, e
+    vals = sorted(line.split()[1:] for o, _ in outs for line in o.splitlines()
+                  if line.startswith("RESULT"))
+    assert vals == [["0", "15.0"], ["1", "15.0"]]
+
+
+def test_reference_arm_prints_one_json_line():
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload",
+                        "bf16_nt_256x256x512", "--steps", "3", "--warmup", "3"], cwd=ROOT,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["steps"] == 3
+
+
+def test_reference_arm_non_zero_ranks_exit_quietly():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload",
+                        "bf16_nt_256x256x512", "--steps", "3", "--warmup", "3"], cwd=ROOT,
+                       capture_output=True, text=True, timeout=300, env=env)
+    assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_warmup_below_three_is_refused():
+    with pytest.raises(SystemExit):
+        bench.main(["--warmup", "2"])
