@@ -258,6 +258,14 @@ def run_reference(args, w):
     return 0
 
 
+def kernel_of(w, plan):
+    """The name of the kernel the plan launches (as in the ncu launch list)."""
+    if w.kind == "mxfp8":
+        return "gemm_mxfp8_kernel"
+    return {1: "gemm16_1cta_kernel", 2: "gemm16_2cta_kernel",
+            3: "gemm16_splitk_kernel"}.get(plan["variant"], str(plan["variant"]))
+
+
 def run_ours(args, w):
     import numpy as np
     import torch
@@ -305,10 +313,11 @@ def run_ours(args, w):
             dtc.gemm_ex("mxfp8", A, B, C, sfA=sfA, sfB=sfB, variant=args.variant, stream=stream)
         else:
             dtc.gemm_ex(w.kind, A, B, C, layout=w.layout, variant=args.variant,
-                        split_k=args.split_k, stream=stream)
+                        split_k=args.split_k, tile_n=args.tile_n, cluster_m=args.cluster_m,
+                        stream=stream)
 
-    variant = dtc.gemm_plan(w.kind, w.M, w.N, w.K, w.layout, variant=args.variant,
-                            split_k=args.split_k)
+    plan = dtc.gemm_plan(w.kind, w.M, w.N, w.K, w.layout, variant=args.variant,
+                         split_k=args.split_k, tile_n=args.tile_n, cluster_m=args.cluster_m)
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
@@ -377,10 +386,7 @@ def run_ours(args, w):
     else:
         peak = peaks["bf16_tflops"]
         peak_note = f"{peak_src} bf16 burst (kernel timed alone)"
-    kernel_name = {0: "auto", 1: "gemm16_1cta_kernel", 2: "gemm16_2cta_kernel",
-                   3: "gemm16_splitk_kernel"}.get(variant, str(variant))
-    if w.kind == "mxfp8":
-        kernel_name = "gemm_mxfp8_kernel"
+    kernel_name = kernel_of(w, plan)
     achieved = flops_step / (kernel_ms / 1e3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": recorded_traffic(w.name, kernel_name),
@@ -400,7 +406,11 @@ def run_ours(args, w):
         "dtype": "bf16" if w.kind == "bf16" else ("f16" if w.kind == "f16" else "e4m3"),
         "data": "synthetic",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout,
-                   "kind": w.kind, "variant": kernel_name, "parallelism": f"replicas x{world}",
+                   "kind": w.kind, "variant": kernel_name,
+                   "tile": f"{plan['tile_m']}x{plan['tile_n']}x{plan['tile_k']}",
+                   "stages": plan["stages"], "split_k": plan["split_k"], "ctas": plan["ctas"],
+                   "cluster": plan["cluster"],
+                   "parallelism": f"replicas x{world}",
                    "l2": "flushed (256 MiB device write) before every timed step, outside the "
                          "step's CUDA-event pair",
                    "pct_of_dense_peak_nominal": 100.0 * achieved /
@@ -431,6 +441,8 @@ def main(argv=None):
     p.add_argument("--workload", default=None, help="workload name (default: the headline)")
     p.add_argument("--variant", type=int, default=0, help="0 auto, 1 one-CTA, 2 CTA pair, 3 split-K")
     p.add_argument("--split-k", type=int, default=0)
+    p.add_argument("--tile-n", type=int, default=0, help="force the N-tile (256 or 224)")
+    p.add_argument("--cluster-m", type=int, default=0, help="force the one-CTA cluster size")
     p.add_argument("--skip-cpu-baseline", action="store_true",
                    help="omit the oracle timing (profiling runs)")
     p.add_argument("--cpu-seconds", type=float, default=15.0)

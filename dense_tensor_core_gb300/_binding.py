@@ -28,7 +28,14 @@ class GemmError(RuntimeError):
 
 class gemm_options(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("split_k", ctypes.c_int),
-                ("timeout_ns", ctypes.c_uint64), ("fault_inject", ctypes.c_int)]
+                ("timeout_ns", ctypes.c_uint64), ("fault_inject", ctypes.c_int),
+                ("tile_n", ctypes.c_int), ("cluster_m", ctypes.c_int), ("tile_k", ctypes.c_int)]
+
+
+class gemm_plan_info(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in
+                ("variant", "tile_m", "tile_n", "tile_k", "stages", "split_k", "ctas", "tiles",
+                 "cluster")]
 
 
 _lib = None
@@ -58,7 +65,8 @@ def lib():
         L.gemm_ex.argtypes = [i32, vp, vp, vp, vp, vp, i64, i64, i64, i32,
                               ctypes.POINTER(gemm_options), vp]
         L.gemm_plan.restype = i32
-        L.gemm_plan.argtypes = [i32, i64, i64, i64, i32, ctypes.POINTER(gemm_options)]
+        L.gemm_plan.argtypes = [i32, i64, i64, i64, i32, ctypes.POINTER(gemm_options),
+                                ctypes.POINTER(gemm_plan_info)]
         L.gemm_last_error.restype = ctypes.c_char_p
         L.gemm_last_error.argtypes = []
         L.gemm_stream_status.restype = i32
@@ -121,8 +129,8 @@ def _out(C, M, N, dtype, device):
     return C
 
 
-def _options(variant, split_k, timeout_ns, fault_inject):
-    return gemm_options(variant, split_k, timeout_ns, fault_inject)
+def _options(variant, split_k, timeout_ns, fault_inject, tile_n=0, cluster_m=0, tile_k=0):
+    return gemm_options(variant, split_k, timeout_ns, fault_inject, tile_n, cluster_m, tile_k)
 
 
 def _gemm16(name, dtype, A, B, C, layout, stream):
@@ -171,7 +179,7 @@ def gemm_mxfp8(A, B, sfA, sfB, C=None, stream=None):
 
 
 def gemm_ex(kind, A, B, C=None, layout="NT", sfA=None, sfB=None, variant=0, split_k=0,
-            timeout_ns=0, fault_inject=0, stream=None):
+            timeout_ns=0, fault_inject=0, tile_n=0, cluster_m=0, tile_k=0, stream=None):
     """Any of the three products with options (variant, split_k, wait limit, test hook)."""
     if kind == "mxfp8":
         M, N, K = _check_mxfp8(A, B, sfA, sfB)
@@ -182,19 +190,21 @@ def gemm_ex(kind, A, B, C=None, layout="NT", sfA=None, sfB=None, variant=0, spli
         _check_tensor(B, dt, "B")
         M, N, K = _shapes16(A, B, layout)
         C = _out(C, M, N, dt, A.device)
-    opts = _options(variant, split_k, timeout_ns, fault_inject)
+    opts = _options(variant, split_k, timeout_ns, fault_inject, tile_n, cluster_m, tile_k)
     _check(lib().gemm_ex(_DTYPE[kind], _ptr(A), _ptr(B), _ptr(sfA), _ptr(sfB), _ptr(C), M, N, K,
                          _layout_code(layout), ctypes.byref(opts), _stream_handle(stream)))
     return C
 
 
-def gemm_plan(kind, M, N, K, layout="NT", variant=0, split_k=0):
-    """The variant the library would launch for these sizes (raises if they would be rejected)."""
-    opts = _options(variant, split_k, 0, 0)
-    v = lib().gemm_plan(_DTYPE[kind], M, N, K, _layout_code(layout), ctypes.byref(opts))
-    if v < 0:
-        raise GemmError(-v, gemm_last_error())
-    return v
+def gemm_plan(kind, M, N, K, layout="NT", variant=0, split_k=0, tile_n=0, cluster_m=0, tile_k=0):
+    """The launch the library would make for these sizes: a dict with variant, tile_m, tile_n,
+    tile_k, stages, split_k, ctas, tiles, cluster (raises GemmError if the call would be
+    rejected)."""
+    opts = _options(variant, split_k, 0, 0, tile_n, cluster_m, tile_k)
+    info = gemm_plan_info()
+    _check(lib().gemm_plan(_DTYPE[kind], M, N, K, _layout_code(layout), ctypes.byref(opts),
+                           ctypes.byref(info)))
+    return {n: getattr(info, n) for n, _ in gemm_plan_info._fields_}
 
 
 def gemm_stream_status(stream=None):

@@ -16,9 +16,11 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <unordered_set>
 
 #include "dtc_gemm.h"
 #include "gemm16_1cta.cuh"
+#include "gemm16_2cta.cuh"
 
 namespace {
 
@@ -46,7 +48,8 @@ struct DeviceInfo {
     bool supported = false;
     int sms = 0;
     int major = 0, minor = 0;
-    bool attr_set[8] = {};
+    std::unordered_set<const void*> smem_attr_set;  // kernels whose smem limit was raised
+    int clusters_for[5] = {0, 0, 0, 0, 0};         // co-resident clusters of 1, 2, 4 CTAs
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -125,6 +128,7 @@ int validate(int dtype, const void* A, const void* B, const void* sfA, const voi
     if (o && (o->variant < 0 || o->variant > 3))
         return fail(GEMM_ERR_INVALID_ARG, "unknown variant %d", o->variant);
     if (o && o->split_k < 0) return fail(GEMM_ERR_INVALID_ARG, "split_k must be >= 0");
+    if (o && o->tile_n < 0) return fail(GEMM_ERR_INVALID_ARG, "tile_n must be >= 0");
     if (M == 0 || N == 0) return GEMM_OK;
     if (!C) return fail(GEMM_ERR_INVALID_ARG, "C is NULL");
     if (!aligned16(C)) return fail(GEMM_ERR_INVALID_ARG, "C is not 16-byte aligned");
@@ -145,51 +149,287 @@ int validate(int dtype, const void* A, const void* B, const void* sfA, const voi
     return GEMM_OK;
 }
 
-int choose_variant(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm_options* o,
-                   int sms) {
-    (void)M; (void)N; (void)K; (void)layout; (void)sms;
-    const int v = o ? o->variant : GEMM_VARIANT_AUTO;
-    if (v != GEMM_VARIANT_AUTO) return v;
-    if (dtype == 2) return GEMM_VARIANT_1CTA;
-    return GEMM_VARIANT_1CTA;
+struct Plan {
+    int variant = 0, tile_m = 0, tile_n = 0, tile_k = 64, stages = 0, split_k = 1, ctas = 0,
+        tiles = 0, cluster = 1;
+};
+
+int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+template <typename Kern>
+int ensure_smem_attr(Kern kern, int bytes, DeviceInfo* dev) {
+    const void* key = reinterpret_cast<const void*>(kern);
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!dev->smem_attr_set.count(key)) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+        dev->smem_attr_set.insert(key);
+    }
+    return GEMM_OK;
 }
 
-template <bool kBF16, bool kNN>
+constexpr int kPairStages = 6;
+
+// Ring depth of the one-CTA kernel for each (tile width, K-block): as many stages as about
+// 220 KB of shared memory holds.
+constexpr int stages_for(int bn, int bk) {
+    return bk == 64 ? (bn == 224 ? 5 : 4) : (bn == 224 ? 10 : 9);
+}
+
+// How many clusters of `cm` one-CTA GEMM CTAs (about 200 KB of shared memory each, so one per
+// SM) the device keeps resident at once. Asked once per device and cluster size.
+int resident_clusters(int cm, DeviceInfo* dev) {
+    if (dev->clusters_for[cm]) return dev->clusters_for[cm];
+    int n = dev->sms / cm;
+    if (cm > 1) {
+        auto kern = dtc::gemm16_1cta_kernel<true, false, 256, 64, 4, 2>;
+        using Cfg = dtc::g16::Cfg<256, 64, 4>;
+        if (ensure_smem_attr(kern, Cfg::kSmemBytes, dev) == GEMM_OK) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(cm * n, 1, 1);
+            cfg.blockDim = dim3(dtc::g16::kThreads, 1, 1);
+            cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = cm;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int q = 0;
+            if (cudaOccupancyMaxActiveClusters(&q, kern, &cfg) == cudaSuccess && q > 0) n = q;
+            else cudaGetLastError();
+        }
+    }
+    dev->clusters_for[cm] = std::max(1, n);
+    return dev->clusters_for[cm];
+}
+
+// Busy time of the slowest cluster, in tile-width units, when every tile costs time proportional
+// to its width: (waves of tiles over the resident clusters) x (tile width).
+int64_t wave_cost(int64_t tiles, int clusters, int bn) { return (int64_t)ceil_div(tiles, clusters) * bn; }
+
+// Sustained fraction of tensor peak that one busy unit (an SM running 128 x BN tiles, or a CTA
+// pair running 256 x BN tiles) reaches in the main loop, measured on GB300 with bf16 NT operands
+// at K = 8192 (4096 x 4096 and 8192 x 8192 products, L2 flushed). The rest of the time goes to
+// waiting for operands: the kernels are bound by L2 -> shared-memory delivery, and the wider and
+// taller tiles need fewer bytes per flop.
+struct TileChoice {
+    int variant, tile_n;
+    double efficiency;
+};
+constexpr TileChoice kChoices[] = {
+    {GEMM_VARIANT_1CTA, 256, 0.61},
+    {GEMM_VARIANT_1CTA, 224, 0.58},
+    {GEMM_VARIANT_2CTA, 256, 0.64},
+    {GEMM_VARIANT_2CTA, 224, 0.56},
+};
+
+// Busy time of the slowest SM, in units of (128 x 1 x K) MMA work at full rate: waves of tiles
+// over the resident units x per-SM tile width / efficiency.
+double plan_cost(int variant, int bn, double eff, int64_t M, int64_t N, int sms) {
+    const int units = variant == GEMM_VARIANT_2CTA ? std::max(1, sms / 2) : sms;
+    const int64_t rows = variant == GEMM_VARIANT_2CTA ? ceil_div(M, 256) : ceil_div(M, 128);
+    const int64_t tiles = rows * ceil_div(N, bn);
+    return (double)ceil_div(tiles, units) * bn / eff;
+}
+
+int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm_options* o,
+              DeviceInfo* d, Plan* p) {
+    (void)K;
+    int v = o ? o->variant : GEMM_VARIANT_AUTO;
+    const int want_n = o ? o->tile_n : 0;
+    if (want_n && want_n != 256 && !(want_n == 224 && layout == GEMM_LAYOUT_NT))
+        return fail(GEMM_ERR_UNSUPPORTED, "tile width %d is not offered for this layout", want_n);
+    if (dtype == 2 && v != GEMM_VARIANT_AUTO && v != GEMM_VARIANT_1CTA)
+        return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 product has a one-CTA kernel only");
+    if (v == GEMM_VARIANT_SPLITK)
+        return fail(GEMM_ERR_UNSUPPORTED, "variant %d is not available in this build", v);
+    int auto_n = 0;
+    if (v == GEMM_VARIANT_AUTO) {
+        // Cheapest (variant, width) by the cost model; 224-wide tiles exist for NT only. Below
+        // one wave of tiles either way, the one-CTA kernel (shorter ring fill) is preferred.
+        double best = -1.0;
+        int best_v = GEMM_VARIANT_1CTA, best_n = 256;
+        for (const TileChoice& c : kChoices) {
+            if (c.tile_n == 224 && layout != GEMM_LAYOUT_NT) continue;
+            if (dtype == 2 && c.variant != GEMM_VARIANT_1CTA) continue;
+            if (want_n && c.tile_n != want_n) continue;
+            double cost = plan_cost(c.variant, c.tile_n, c.efficiency, M, N, d->sms);
+            if (c.variant == GEMM_VARIANT_2CTA && ceil_div(M, 256) * ceil_div(N, c.tile_n) < d->sms / 2)
+                cost *= 1.25;
+            if (best < 0 || cost < best) {
+                best = cost;
+                best_v = c.variant;
+                best_n = c.tile_n;
+            }
+        }
+        v = best_v;
+        auto_n = best_n;
+    }
+    p->variant = v;
+    if (v == GEMM_VARIANT_1CTA) {
+        const int num_m = ceil_div(M, 128);
+        int cm = o ? o->cluster_m : 0;
+        if (cm != 0 && cm != 1 && cm != 2)
+            return fail(GEMM_ERR_INVALID_ARG, "cluster_m %d is not 1 or 2", cm);
+        if (cm == 0) cm = 1;
+        int bk = o ? o->tile_k : 0;
+        if (bk != 0 && bk != 32 && bk != 64)
+            return fail(GEMM_ERR_INVALID_ARG, "tile_k %d is not 32 or 64", bk);
+        if (bk == 0) bk = 64;
+        const int clusters = resident_clusters(cm, d);
+        const int64_t cluster_rows = ceil_div(num_m, cm);
+        int best = auto_n ? auto_n : 256;
+        if (want_n) {
+            best = want_n;
+        } else if (!auto_n && layout == GEMM_LAYOUT_NT) {
+            if (wave_cost(cluster_rows * ceil_div(N, 224), clusters, 224) <
+                wave_cost(cluster_rows * ceil_div(N, 256), clusters, 256))
+                best = 224;
+        }
+        p->cluster = cm;
+        p->tile_m = 128;
+        p->tile_n = best;
+        p->tile_k = bk;
+        p->stages = stages_for(best, bk);
+        p->tiles = (int)cluster_rows * ceil_div(N, best);  // cluster tiles
+        p->ctas = cm * std::min(p->tiles, clusters);
+    } else {
+        const int pairs = std::max(1, d->sms / 2);
+        p->cluster = 2;
+        p->tile_m = 256;
+        if (layout == GEMM_LAYOUT_NN) {
+            if (want_n && want_n != 256)
+                return fail(GEMM_ERR_UNSUPPORTED, "the pair kernel offers 256-wide tiles for NN");
+            p->tile_n = 256;
+        } else if (want_n) {
+            p->tile_n = want_n;
+        } else if (auto_n) {
+            p->tile_n = auto_n;
+        } else {
+            const int64_t rows = ceil_div(M, 256);
+            p->tile_n = wave_cost(rows * ceil_div(N, 224), pairs, 224) <
+                                wave_cost(rows * ceil_div(N, 256), pairs, 256)
+                            ? 224
+                            : 256;
+        }
+        p->stages = kPairStages;
+        p->tiles = ceil_div(M, 256) * ceil_div(N, p->tile_n);
+        p->ctas = 2 * std::min(p->tiles, pairs);
+    }
+    return GEMM_OK;
+}
+
+Gemm16Args make_args(void* C, int M, int N, int K, int tile_m, int tile_n, int tile_k,
+                     const gemm_options* o) {
+    Gemm16Args a;
+    a.C = C;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.num_m = (M + tile_m - 1) / tile_m;
+    a.num_n = (N + tile_n - 1) / tile_n;
+    a.num_kb = (K + tile_k - 1) / tile_k;
+    a.timeout_ns = (o && o->timeout_ns) ? o->timeout_ns : kDefaultTimeoutNs;
+    a.fault = o ? o->fault_inject : 0;
+    return a;
+}
+
+template <typename Kern>
+int launch_cluster(Kern kern, int grid, int threads, int smem, int cluster, cudaStream_t stream,
+                   const CUtensorMap& tA, const CUtensorMap& tB, const Gemm16Args& args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = cluster > 1 ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tA, tB, args);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    return GEMM_OK;
+}
+
+template <bool kBF16, bool kNN, int kBN, int kBK, int kStages, int kCM>
 int launch_gemm16_1cta(const void* A, const void* B, void* C, int M, int N, int K,
-                       const gemm_options* o, DeviceInfo* dev, int attr_slot, cudaStream_t stream) {
+                       const gemm_options* o, DeviceInfo* dev, const Plan& p,
+                       cudaStream_t stream) {
     using namespace dtc::g16;
+    using Cfg = Cfg<kBN, kBK, kStages>;
     const CUtensorMapDataType dt = kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUtensorMapSwizzle kmaj = kBK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     CUtensorMap tA, tB;
-    int rc = make_tmap(&tA, dt, 2, A, (uint64_t)K, (uint64_t)M, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B, "A");
+    int rc = make_tmap(&tA, dt, 2, A, (uint64_t)K, (uint64_t)M, kBK, kBM, kmaj, "A");
     if (rc) return rc;
     if (!kNN)
-        rc = make_tmap(&tB, dt, 2, B, (uint64_t)K, (uint64_t)N, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B, "B");
+        rc = make_tmap(&tB, dt, 2, B, (uint64_t)K, (uint64_t)N, kBK, kBN / kCM, kmaj, "B");
     else
         rc = make_tmap(&tB, dt, 2, B, (uint64_t)N, (uint64_t)K, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B, "B");
     if (rc) return rc;
+    auto kern = dtc::gemm16_1cta_kernel<kBF16, kNN, kBN, kBK, kStages, kCM>;
+    if ((rc = ensure_smem_attr(kern, Cfg::kSmemBytes, dev))) return rc;
+    const Gemm16Args args = make_args(C, M, N, K, kBM, kBN, kBK, o);
+    return launch_cluster(kern, p.ctas, kThreads, Cfg::kSmemBytes, kCM, stream, tA, tB, args);
+}
 
-    auto kern = dtc::gemm16_1cta_kernel<kBF16, kNN>;
-    if (!dev->attr_set[attr_slot]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-        dev->attr_set[attr_slot] = true;
+template <bool kBF16, bool kNN, int kBN>
+int launch_gemm16_2cta(const void* A, const void* B, void* C, int M, int N, int K,
+                       const gemm_options* o, DeviceInfo* dev, const Plan& p,
+                       cudaStream_t stream) {
+    using Cfg = dtc::g2::Cfg<kBN, kPairStages>;
+    const CUtensorMapDataType dt = kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUtensorMap tA, tB;
+    int rc = make_tmap(&tA, dt, 2, A, (uint64_t)K, (uint64_t)M, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "A");
+    if (rc) return rc;
+    if (!kNN)
+        rc = make_tmap(&tB, dt, 2, B, (uint64_t)K, (uint64_t)N, 64, Cfg::kHalfN, CU_TENSOR_MAP_SWIZZLE_128B, "B");
+    else
+        rc = make_tmap(&tB, dt, 2, B, (uint64_t)N, (uint64_t)K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, "B");
+    if (rc) return rc;
+    auto kern = dtc::gemm16_2cta_kernel<kBF16, kNN, kBN, kPairStages>;
+    if ((rc = ensure_smem_attr(kern, Cfg::kSmemBytes, dev))) return rc;
+    const Gemm16Args args = make_args(C, M, N, K, 256, kBN, 64, o);
+    return launch_cluster(kern, p.ctas, dtc::g2::kThreads, Cfg::kSmemBytes, 2, stream, tA, tB, args);
+}
+
+template <bool kBF16, bool kNN, int kBN, int kBK, int kStages>
+int launch_1cta_cm(const Plan& p, const void* A, const void* B, void* C, int m, int n, int k,
+                   const gemm_options* o, DeviceInfo* dev, cudaStream_t stream) {
+    if (p.cluster == 2)
+        return launch_gemm16_1cta<kBF16, kNN, kBN, kBK, kStages, 2>(A, B, C, m, n, k, o, dev, p, stream);
+    return launch_gemm16_1cta<kBF16, kNN, kBN, kBK, kStages, 1>(A, B, C, m, n, k, o, dev, p, stream);
+}
+
+
+
+template <bool kBF16>
+int launch16(int layout, const Plan& p, const void* A, const void* B, void* C, int m, int n, int k,
+             const gemm_options* o, DeviceInfo* dev, cudaStream_t stream) {
+    if (p.variant == GEMM_VARIANT_1CTA) {
+        if (p.tile_k == 32) {
+            if (layout == GEMM_LAYOUT_NN)
+                return launch_1cta_cm<kBF16, true, 256, 32, stages_for(256, 32)>(p, A, B, C, m, n, k, o, dev, stream);
+            if (p.tile_n == 224)
+                return launch_1cta_cm<kBF16, false, 224, 32, stages_for(224, 32)>(p, A, B, C, m, n, k, o, dev, stream);
+            return launch_1cta_cm<kBF16, false, 256, 32, stages_for(256, 32)>(p, A, B, C, m, n, k, o, dev, stream);
+        }
+        if (layout == GEMM_LAYOUT_NN)
+            return launch_1cta_cm<kBF16, true, 256, 64, stages_for(256, 64)>(p, A, B, C, m, n, k, o, dev, stream);
+        if (p.tile_n == 224)
+            return launch_1cta_cm<kBF16, false, 224, 64, stages_for(224, 64)>(p, A, B, C, m, n, k, o, dev, stream);
+        return launch_1cta_cm<kBF16, false, 256, 64, stages_for(256, 64)>(p, A, B, C, m, n, k, o, dev, stream);
     }
-    Gemm16Args args;
-    args.C = C;
-    args.M = M;
-    args.N = N;
-    args.K = K;
-    args.num_m = (M + kBM - 1) / kBM;
-    args.num_n = (N + kBN - 1) / kBN;
-    args.num_kb = (K + kBK - 1) / kBK;
-    args.timeout_ns = (o && o->timeout_ns) ? o->timeout_ns : kDefaultTimeoutNs;
-    args.fault = o ? o->fault_inject : 0;
-    const int tiles = args.num_m * args.num_n;
-    const int grid = std::min(tiles, dev->sms);
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(tA, tB, args);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
-    return GEMM_OK;
+    if (layout == GEMM_LAYOUT_NN)
+        return launch_gemm16_2cta<kBF16, true, 256>(A, B, C, m, n, k, o, dev, p, stream);
+    if (p.tile_n == 224) return launch_gemm16_2cta<kBF16, false, 224>(A, B, C, m, n, k, o, dev, p, stream);
+    return launch_gemm16_2cta<kBF16, false, 256>(A, B, C, m, n, k, o, dev, p, stream);
 }
 
 int run(int dtype, const void* A, const void* B, const void* sfA, const void* sfB, void* C,
@@ -205,19 +445,12 @@ int run(int dtype, const void* A, const void* B, const void* sfA, const void* sf
         cudaError_t e = cudaMemsetAsync(C, 0, (size_t)M * (size_t)N * 2, stream);
         return e == cudaSuccess ? GEMM_OK : cuda_fail(e, "cudaMemsetAsync");
     }
-    const int v = choose_variant(dtype, M, N, K, layout, o, info->sms);
-    if (dtype == 2)
-        return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 kernel is not available in this build");
-    if (v != GEMM_VARIANT_1CTA)
-        return fail(GEMM_ERR_UNSUPPORTED, "variant %d is not available in this build", v);
+    Plan p;
+    if ((rc = make_plan(dtype, M, N, K, layout, o, info, &p))) return rc;
+    if (dtype == 2) return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 kernel is not available in this build");
     const int m = (int)M, n = (int)N, k = (int)K;
-    if (dtype == 0)
-        return layout == GEMM_LAYOUT_NT
-                   ? launch_gemm16_1cta<true, false>(A, B, C, m, n, k, o, info, 0, stream)
-                   : launch_gemm16_1cta<true, true>(A, B, C, m, n, k, o, info, 1, stream);
-    return layout == GEMM_LAYOUT_NT
-               ? launch_gemm16_1cta<false, false>(A, B, C, m, n, k, o, info, 2, stream)
-               : launch_gemm16_1cta<false, true>(A, B, C, m, n, k, o, info, 3, stream);
+    return dtype == 0 ? launch16<true>(layout, p, A, B, C, m, n, k, o, info, stream)
+                      : launch16<false>(layout, p, A, B, C, m, n, k, o, info, stream);
 }
 
 }  // namespace
@@ -245,20 +478,36 @@ int gemm_ex(int dtype, const void* A, const void* B, const void* sfA, const void
     return run(dtype, A, B, sfA, sfB, C, M, N, K, layout, opts, (cudaStream_t)stream);
 }
 
-int gemm_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm_options* opts) {
+int gemm_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm_options* opts,
+              gemm_plan_info* info) {
     g_err[0] = '\0';
-    // Sizes only: pointer rules are not part of the plan.
     const int64_t kMax = 2147483647;
-    if (dtype < 0 || dtype > 2) return -fail(GEMM_ERR_INVALID_ARG, "dtype %d is not 0, 1 or 2", dtype);
+    if (!info) return fail(GEMM_ERR_INVALID_ARG, "info is NULL");
+    if (dtype < 0 || dtype > 2) return fail(GEMM_ERR_INVALID_ARG, "dtype %d is not 0, 1 or 2", dtype);
     if (layout != GEMM_LAYOUT_NT && layout != GEMM_LAYOUT_NN)
-        return -fail(GEMM_ERR_INVALID_ARG, "layout %d is not NT (0) or NN (1)", layout);
+        return fail(GEMM_ERR_INVALID_ARG, "layout %d is not NT (0) or NN (1)", layout);
+    if (dtype == 2 && layout != GEMM_LAYOUT_NT)
+        return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 GEMM supports the NT layout only");
     if (M < 0 || N < 0 || K < 0 || M > kMax || N > kMax || K > kMax)
-        return -fail(GEMM_ERR_INVALID_ARG, "sizes must be in [0, 2^31-1]");
+        return fail(GEMM_ERR_INVALID_ARG, "sizes must be in [0, 2^31-1]");
+    if (opts && (opts->variant < 0 || opts->variant > 3))
+        return fail(GEMM_ERR_INVALID_ARG, "unknown variant %d", opts->variant);
     int dev;
-    DeviceInfo* info;
-    int rc = current_device(&dev, &info);
-    if (rc) return -rc;
-    return choose_variant(dtype, M, N, K, layout, opts, info->sms);
+    DeviceInfo* d;
+    int rc = current_device(&dev, &d);
+    if (rc) return rc;
+    Plan p;
+    if ((rc = make_plan(dtype, M, N, K, layout, opts, d, &p))) return rc;
+    info->variant = p.variant;
+    info->tile_m = p.tile_m;
+    info->tile_n = p.tile_n;
+    info->tile_k = p.tile_k;
+    info->stages = p.stages;
+    info->split_k = p.split_k;
+    info->ctas = p.ctas;
+    info->tiles = p.tiles;
+    info->cluster = p.cluster;
+    return GEMM_OK;
 }
 
 const char* gemm_last_error(void) { return g_err; }

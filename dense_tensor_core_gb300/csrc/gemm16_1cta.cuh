@@ -1,4 +1,5 @@
-// gemm16_1cta.cuh -- persistent, warp-specialised bf16/fp16 GEMM on one CTA per 128x256 tile.
+// gemm16_1cta.cuh -- persistent, warp-specialised bf16/fp16 GEMM, one CTA per 128 x kBN tile,
+// optionally in clusters of kCM CTAs stacked along M that share the B tile by TMA multicast.
 //
 // C[M,N] = A[M,K] . Bop, fp32 accumulation in Tensor Memory, bf16/fp16 output.
 // The tile (128 x 256, K-blocks of 64) follows the example shape of TileLang SM100 Support
@@ -9,76 +10,68 @@
 // Differences from the pages' kernels: there the SM100 preview ran without TMA and without warp
 // specialisation, one stage, and waited for each MMA (TileLang SM100 Support (Preview),
 // "Compilation and Usage" pass configs and "Code Example"); here
-//   warp 0      : TMA producer (one lane) filling a 4-stage ring of 128B-swizzled A/B tiles,
+//   warp 0      : TMA producer (one lane) filling a kStages ring of 128B-swizzled A/B tiles,
 //   warp 1      : Tensor Memory allocator and single-thread tcgen05.mma issuer,
 //   warps 2..5  : epilogue (tcgen05.ld -> cvt -> global stores),
 // with full/empty barriers per stage (the producer waits on the inverted parity, as in the
 // 3-stage ring of tilelang (velog) section 1.3) and a double-buffered accumulator (2 x 256
 // columns) so the epilogue of one tile overlaps the main loop of the next. CTAs are persistent:
-// CTA i takes tiles i, i + grid, ... in a grouped order that keeps A and B panels in L2.
+// cluster i takes cluster tiles i, i + clusters, ... in a grouped order that keeps A and B panels
+// in L2.
+//
+// Clusters (kCM = 2 or 4): the kCM CTAs of a cluster compute the 128-row tiles mc*kCM + rank of
+// the same N-tile, so they need the same B tile. CTA `rank` loads the rank-th 1/kCM of it once
+// and multicasts it into every CTA of the cluster; each CTA still loads its own A. The stage's
+// full barrier in every CTA counts all bytes landing there, and the stage's empty barrier counts
+// one release from every CTA's MMA thread (a copy into stage s of all kCM CTAs may start only
+// when all of them are done with it). This cuts the L2 -> SM traffic per CTA and K-block from
+// 48 KiB to 16 + 32/kCM KiB, which is what bounds the kernel without clusters.
 #pragma once
 
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
-
-#include "sm103_ptx.cuh"
+#include "gemm_common.cuh"
 
 namespace dtc {
 
-__device__ int g_dtc_status;  // first device-side wait that gave up (0 = none)
-
 namespace g16 {
 constexpr int kBM = 128;
-constexpr int kBN = 256;
-constexpr int kBK = 64;  // one 128-byte swizzle atom of 16-bit elements
-constexpr int kStages = 4;
-constexpr int kAStage = kBM * kBK * 2;  // 16 KiB
-constexpr int kBStage = kBN * kBK * 2;  // 32 KiB
-constexpr int kStageBytes = kAStage + kBStage;
-constexpr int kTmemCols = 512;  // two fp32 accumulators of 256 columns
+constexpr int kTmemCols = 512;          // two fp32 accumulators
+constexpr int kAccStride = 256;         // column offset of the second accumulator
 constexpr int kThreads = 192;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
-constexpr int kGroupM = 8;                                // M-tiles per rasterisation group
+constexpr int kGroupM = 8;  // cluster rows per rasterisation group
 constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
+
+// K-blocks of 64 (one 128-byte swizzle row of 16-bit elements) or 32 (a 64-byte swizzle row):
+// the shallower block halves a stage, so the same shared memory holds twice as many stages and a
+// larger share of the ring is in flight while one stage is being consumed.
+template <int kBN, int kBK, int kStages>
+struct Cfg {
+    static constexpr int kAStage = kBM * kBK * 2;
+    static constexpr int kBStage = kBN * kBK * 2;
+    static constexpr int kStageBytes = kAStage + kBStage;
+    static constexpr int kPitch = kBK * 2;  // bytes per K-major row = swizzle width
+    static_assert(kBK == 64 || kBK == 32, "K-block of 64 or 32");
+    static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
+    static_assert(kBN % 16 == 0 && kBN <= 256, "UMMA N for M = 128");
+    static_assert(kSmemBytes <= 227 * 1024 - 256, "shared memory budget");
+};
 }  // namespace g16
 
-struct Gemm16Args {
-    void* C;
-    int M, N, K;
-    int num_m, num_n, num_kb;
-    uint64_t timeout_ns;
-    int fault;
-};
-
-// Grouped rasterisation: tiles are numbered down groups of kGroupM M-tiles, N-tile by N-tile.
-__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int group_m, int& mt,
-                                            int& nt) {
-    const int per_group = group_m * num_n;
-    const int g = t / per_group;
-    const int first_m = g * group_m;
-    const int gm = min(num_m - first_m, group_m);
-    const int r = t - g * per_group;
-    mt = first_m + r % gm;
-    nt = r / gm;
-}
-
-template <bool kBF16>
-__device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi) {
-    const float a = __uint_as_float(lo), b = __uint_as_float(hi);
-    if constexpr (kBF16) {
-        __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-        return *reinterpret_cast<uint32_t*>(&v);
-    } else {
-        __half2 v = __floats2half2_rn(a, b);
-        return *reinterpret_cast<uint32_t*>(&v);
-    }
-}
-
-template <bool kBF16, bool kNN>
+template <bool kBF16, bool kNN, int kBN, int kBK, int kStages, int kCM>
 __global__ void __launch_bounds__(g16::kThreads, 1)
     gemm16_1cta_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const Gemm16Args args) {
     using namespace g16;
+    using C_ = Cfg<kBN, kBK, kStages>;
+    constexpr int kAStage = C_::kAStage;
+    constexpr int kPitch = C_::kPitch;
+    static_assert(kCM == 1 || kCM == 2 || kCM == 4, "cluster of 1, 2 or 4 CTAs");
+    static_assert((kBN / kCM) % 8 == 0, "each CTA's share of B is whole 8-row swizzle atoms");
+    static_assert(!kNN || (kBN % 64 == 0 && (kBN / 64) % kCM == 0),
+                  "NN: B is loaded as 64-column boxes, split evenly over the cluster");
+    constexpr int kBPartRows = kBN / kCM;                 // NT: rows of B^T this CTA loads
+    constexpr int kBPartBytes = kBPartRows * kBK * 2;     // bytes of B this CTA loads
+    constexpr uint16_t kMask = (uint16_t)((1u << kCM) - 1);
+
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[kStages];
     __shared__ __align__(8) uint64_t bar_empty[kStages];
@@ -89,17 +82,21 @@ __global__ void __launch_bounds__(g16::kThreads, 1)
     __shared__ int abort_flag;
 
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-    const uint32_t sA = base;                      // kStages x 16 KiB
-    const uint32_t sB = base + kStages * kAStage;  // kStages x 32 KiB
+    const uint32_t sA = base;                      // kStages x kAStage
+    const uint32_t sB = base + kStages * kAStage;  // kStages x kBStage
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int total = args.num_m * args.num_n;
+    const uint32_t rank = kCM > 1 ? cluster_ctarank() : 0;
+    const int cluster = blockIdx.x / kCM;
+    const int clusters = gridDim.x / kCM;
+    const int num_mc = (args.num_m + kCM - 1) / kCM;  // cluster rows of kCM * 128
+    const int total = num_mc * args.num_n;
     volatile int* abort = &abort_flag;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&bar_full[s]), 1);
-            mbar_init(smem_u32(&bar_empty[s]), 1);
+            mbar_init(smem_u32(&bar_empty[s]), kCM);  // one release per CTA of the cluster
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&bar_tfull[b]), 1);
@@ -120,6 +117,7 @@ __global__ void __launch_bounds__(g16::kThreads, 1)
     }
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (kCM > 1) cluster_sync();  // every CTA's barriers exist before any multicast
     tc_fence_after_sync();
     const uint32_t tmem_base = tmem_slot;
 
@@ -128,9 +126,10 @@ __global__ void __launch_bounds__(g16::kThreads, 1)
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                int mt, nt;
-                tile_coords(t, args.num_m, args.num_n, kGroupM, mt, nt);
+            for (int t = cluster; t < total && ok; t += clusters) {
+                int mc, nt;
+                tile_coords(t, num_mc, args.num_n, kGroupM, mc, nt);
+                const int mt = mc * kCM + (int)rank;
                 for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
                     const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
                     if (!wait_bounded(smem_u32(&bar_empty[s]), ph ^ 1u, abort, args.timeout_ns,
@@ -140,20 +139,33 @@ __global__ void __launch_bounds__(g16::kThreads, 1)
                     }
                     if (args.fault == 1 && it == 0) continue;  // test hook: stage never filled
                     const uint32_t full = smem_u32(&bar_full[s]);
-                    mbar_arrive_expect_tx(full, kStageBytes);
+                    mbar_arrive_expect_tx(full, C_::kStageBytes);
                     tma_load_2d(sA + s * kAStage, &tmA, full, kb * kBK, mt * kBM);
+                    const uint32_t bdst = sB + s * C_::kBStage;
                     if constexpr (!kNN) {
-                        tma_load_2d(sB + s * kBStage, &tmB, full, kb * kBK, nt * kBN);
+                        const uint32_t dst = bdst + rank * kBPartBytes;
+                        const int row = nt * kBN + (int)rank * kBPartRows;
+                        if constexpr (kCM == 1)
+                            tma_load_2d(dst, &tmB, full, kb * kBK, row);
+                        else
+                            tma_load_2d_multicast(dst, &tmB, full, kb * kBK, row, kMask);
                     } else {
+                        constexpr int kBoxes = kBN / 64 / kCM;  // 64-column boxes per CTA
 #pragma unroll
-                        for (int j = 0; j < kBN / 64; ++j)
-                            tma_load_2d(sB + s * kBStage + j * (64 * kBK * 2), &tmB, full,
-                                        nt * kBN + j * 64, kb * kBK);
+                        for (int j = 0; j < kBoxes; ++j) {
+                            const int box = (int)rank * kBoxes + j;
+                            const uint32_t dst = bdst + box * (64 * kBK * 2);
+                            if constexpr (kCM == 1)
+                                tma_load_2d(dst, &tmB, full, nt * kBN + box * 64, kb * kBK);
+                            else
+                                tma_load_2d_multicast(dst, &tmB, full, nt * kBN + box * 64,
+                                                      kb * kBK, kMask);
+                        }
                     }
                 }
             }
             if (!ok) {
-                // Let the copies already issued land before the CTA exits.
+                // Let the copies already issued (ours and the multicasts into this CTA) land.
                 const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0;
                 for (uint32_t i = first; i < it; ++i) {
                     if (args.fault == 1 && i == 0) continue;
@@ -167,7 +179,7 @@ __global__ void __launch_bounds__(g16::kThreads, 1)
             constexpr uint32_t idesc = idesc_f16(kBF16, kNN, kBM, kBN);
             uint32_t it = 0, acc = 0;
             bool ok = true, issued = false;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            for (int t = cluster; t < total && ok; t += clusters) {
                 const uint32_t b = acc & 1u, aph = (acc >> 1) & 1u;
                 if (!wait_bounded(smem_u32(&bar_tempty[b]), aph ^ 1u, abort, args.timeout_ns,
                                   &g_dtc_status, 2)) {
@@ -175,7 +187,7 @@ __global__ void __launch_bounds__(g16::kThreads, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + b * kBN;
+                const uint32_t d_tmem = tmem_base + b * kAccStride;
                 for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
                     const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
                     if (!wait_bounded(smem_u32(&bar_full[s]), ph, abort, args.timeout_ns,
@@ -184,17 +196,23 @@ __global__ void __launch_bounds__(g16::kThreads, 1)
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t a0 = sA + s * kAStage, b0 = sB + s * kBStage;
+                    const uint32_t a0 = sA + s * kAStage, b0 = sB + s * C_::kBStage;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint64_t adesc = smem_desc_sw128(a0 + kk * 32, 16, 1024);
+                        const uint64_t adesc = smem_desc<kPitch>(a0 + kk * 32, 16, 8 * kPitch);
                         const uint64_t bdesc =
-                            kNN ? smem_desc_sw128(b0 + kk * 16 * 128, 64 * kBK * 2, 1024)
-                                : smem_desc_sw128(b0 + kk * 32, 16, 1024);
+                            kNN ? smem_desc<128>(b0 + kk * 16 * 128, 64 * kBK * 2, 1024)
+                                : smem_desc<kPitch>(b0 + kk * 32, 16, 8 * kPitch);
                         mma_f16_cta1(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     issued = true;
-                    mma_commit_cta1(smem_u32(&bar_empty[s]));
+                    const uint32_t e = smem_u32(&bar_empty[s]);
+                    if constexpr (kCM == 1) {
+                        mma_commit_cta1(e);
+                    } else {
+#pragma unroll
+                        for (int r = 0; r < kCM; ++r) mma_commit_cta1(map_to_cta(e, r));
+                    }
                 }
                 if (!ok) break;
                 mma_commit_cta1(smem_u32(&bar_tfull[b]));
@@ -211,9 +229,10 @@ __global__ void __launch_bounds__(g16::kThreads, 1)
         const int q = warp & 3;  // Tensor Memory lane quarter this warp may access
         const int row_in_tile = q * 32 + lane;
         uint32_t acc = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x, ++acc) {
-            int mt, nt;
-            tile_coords(t, args.num_m, args.num_n, kGroupM, mt, nt);
+        for (int t = cluster; t < total; t += clusters, ++acc) {
+            int mc, nt;
+            tile_coords(t, num_mc, args.num_n, kGroupM, mc, nt);
+            const int mt = mc * kCM + (int)rank;
             const uint32_t b = acc & 1u, aph = (acc >> 1) & 1u;
             int ok = 1;
             if (lane == 0)
@@ -224,7 +243,7 @@ __global__ void __launch_bounds__(g16::kThreads, 1)
             tc_fence_after_sync();
             const int64_t row = (int64_t)mt * kBM + row_in_tile;
             uint16_t* crow = reinterpret_cast<uint16_t*>(args.C) + row * args.N;
-            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + b * kBN;
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + b * kAccStride;
 #pragma unroll 1
             for (int c = 0; c < kBN / 32; ++c) {
                 uint32_t v[32];
@@ -257,7 +276,14 @@ __global__ void __launch_bounds__(g16::kThreads, 1)
     // ------------------------------ teardown ------------------------------
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (kCM > 1) cluster_sync();  // no CTA leaves while others may still write to it
     if (warp == 1) {
+        if (kCM > 1 && *abort && lane == 0) {
+            // After an abort, copies multicast into this CTA for a phase it never armed may
+            // still be in flight: give them a fixed, bounded time to land.
+            const uint64_t t0 = globaltimer_ns();
+            while (globaltimer_ns() - t0 < 1000ull * 1000) __nanosleep(1000);
+        }
         __syncwarp();
         tc_fence_after_sync();
         tmem_dealloc<1>(tmem_base, kTmemCols);

@@ -1,0 +1,255 @@
+// gemm16_2cta.cuh -- persistent bf16/fp16 GEMM on CTA pairs (cluster 2x1, tcgen05 cta_group::2).
+//
+// The 2-CTA variant named by the 05 Blackwell TCGEN05 GEMM tutorial, "Advanced" (use_2cta with
+// cluster_dims (2,1,1), the persistent warp-specialised example), written for sm_103a.
+//
+// A pair computes a 256 x kBN tile of C. CTA r of the pair (r = 0 is the leader):
+//   - loads its own 128 rows of A (rows 256*mt + 128*r) and its own kBN/2 rows of B^T
+//     (columns kBN*nt + r*kBN/2 of C) into its own shared memory, 64-deep K-blocks, a kStages ring;
+//     both CTAs' copies complete on the LEADER's full barrier (cp.async.bulk.tensor .cta_group::2),
+//     which the leader arms with the bytes of both CTAs;
+//   - holds rows 128*r..128*r+127 of the accumulator in its own Tensor Memory.
+// The leader's single MMA thread issues tcgen05.mma.cta_group::2 (M = 256, N = kBN, K = 16); the
+// tensor cores of both SMs read A and B from both CTAs' shared memory at the same offsets. Its
+// commits arrive on the empty / accumulator-full barriers of both CTAs (one commit per CTA, at
+// shared::cluster addresses; no multicast). Each CTA's epilogue drains its own 128 rows and
+// arrives on the leader's accumulator-empty barrier (8 arrivals: 4 warps x 2 CTAs).
+// Compared with one CTA per 128 x 256 tile, every SM loads half as much of B per FLOP, and a stage
+// takes 16 + kBN/8 KiB of shared memory, which leaves room for a deeper ring.
+#pragma once
+
+#include "gemm_common.cuh"
+
+namespace dtc {
+
+namespace g2 {
+constexpr int kBMc = 128;  // rows of C per CTA
+constexpr int kBK = 64;
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;
+constexpr int kAccStride = 256;  // column offset of the second accumulator
+constexpr int kGroupM = 8;
+constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
+constexpr uint64_t kPeerSettleNs = 1000ull * 1000;  // 1 ms
+
+template <int kBN, int kStages>
+struct Cfg {
+    static constexpr int kHalfN = kBN / 2;
+    static constexpr int kAStage = kBMc * kBK * 2;
+    static constexpr int kBStage = kHalfN * kBK * 2;
+    static constexpr int kStageBytes = kAStage + kBStage;
+    static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+    static_assert(kBN % 32 == 0 && kBN >= 64 && kBN <= 256, "pair tile N must be 64..256, /32");
+    static_assert(kSmemBytes <= 227 * 1024 - 256, "shared memory budget");
+};
+}  // namespace g2
+
+template <bool kBF16, bool kNN, int kBN, int kStages>
+__global__ void __launch_bounds__(g2::kThreads, 1)
+    gemm16_2cta_kernel(const __grid_constant__ CUtensorMap tmA,
+                       const __grid_constant__ CUtensorMap tmB, const Gemm16Args args) {
+    using namespace g2;
+    using C_ = Cfg<kBN, kStages>;
+    static_assert(!kNN || C_::kHalfN % 64 == 0, "NN needs whole 64-column B boxes per CTA");
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_full[kStages];
+    __shared__ __align__(8) uint64_t bar_empty[kStages];
+    __shared__ __align__(8) uint64_t bar_tfull[2];
+    __shared__ __align__(8) uint64_t bar_tempty[2];
+    __shared__ __align__(8) uint64_t bar_drain;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t sA = base;
+    const uint32_t sB = base + kStages * C_::kAStage;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1;
+    const int num_pairs = gridDim.x >> 1;
+    const int total = args.num_m * args.num_n;  // num_m counts 256-row pair tiles
+    volatile int* abort = &abort_flag;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&bar_full[s]), 1);
+            mbar_init(smem_u32(&bar_empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&bar_tfull[b]), 1);
+            mbar_init(smem_u32(&bar_tempty[b]), 8);  // 4 epilogue warps in each CTA
+        }
+        mbar_init(smem_u32(&bar_drain), 1);
+        abort_flag = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc<2>(smem_u32(&tmem_slot), kTmemCols);
+        tmem_relinquish<2>();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers exist before any copy or arrival targets them
+    tc_fence_after_sync();
+    const uint32_t tmem_base = tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer (both CTAs) ------------------------------
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = pair; t < total && ok; t += num_pairs) {
+                int mt, nt;
+                tile_coords(t, args.num_m, args.num_n, kGroupM, mt, nt);
+                const int a_row = mt * 256 + (int)rank * kBMc;
+                const int b_row = nt * kBN + (int)rank * C_::kHalfN;
+                for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
+                    const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+                    if (!wait_bounded(smem_u32(&bar_empty[s]), ph ^ 1u, abort, args.timeout_ns,
+                                      &g_dtc_status, 11)) {
+                        ok = false;
+                        break;
+                    }
+                    if (args.fault == 1 && it == 0) continue;  // test hook: stage never filled
+                    const uint32_t full_local = smem_u32(&bar_full[s]);
+                    const uint32_t full_leader = map_to_cta(full_local, 0);
+                    if (leader) mbar_arrive_expect_tx(full_local, 2 * C_::kStageBytes);
+                    tma_load_2d_pair(sA + s * C_::kAStage, &tmA, full_leader, kb * kBK, a_row);
+                    if constexpr (!kNN) {
+                        tma_load_2d_pair(sB + s * C_::kBStage, &tmB, full_leader, kb * kBK, b_row);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < C_::kHalfN / 64; ++j)
+                            tma_load_2d_pair(sB + s * C_::kBStage + j * (64 * kBK * 2), &tmB,
+                                             full_leader, b_row + j * 64, kb * kBK);
+                    }
+                }
+            }
+            if (!ok && leader) {
+                // The leader's full barriers count both CTAs' copies: let those in flight land.
+                const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0;
+                for (uint32_t i = first; i < it; ++i) {
+                    if (args.fault == 1 && i == 0) continue;
+                    wait_drain(smem_u32(&bar_full[i % kStages]), (i / kStages) & 1u, kDrainNs);
+                }
+            } else if (!ok) {
+                // The peer's copies complete on the leader's barriers, which it cannot observe:
+                // give them a fixed, bounded time to land before this CTA may exit.
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < kPeerSettleNs) __nanosleep(1000);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer (leader CTA) ------------------------------
+        if (lane == 0 && leader) {
+            constexpr uint32_t idesc = idesc_f16(kBF16, kNN, 256, kBN);
+            uint32_t it = 0, acc = 0;
+            bool ok = true, issued = false;
+            for (int t = pair; t < total && ok; t += num_pairs) {
+                const uint32_t b = acc & 1u, aph = (acc >> 1) & 1u;
+                if (!wait_bounded(smem_u32(&bar_tempty[b]), aph ^ 1u, abort, args.timeout_ns,
+                                  &g_dtc_status, 12)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + b * kAccStride;
+                for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
+                    const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+                    if (!wait_bounded(smem_u32(&bar_full[s]), ph, abort, args.timeout_ns,
+                                      &g_dtc_status, 13)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a0 = sA + s * C_::kAStage, b0 = sB + s * C_::kBStage;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint64_t adesc = smem_desc_sw128(a0 + kk * 32, 16, 1024);
+                        const uint64_t bdesc =
+                            kNN ? smem_desc_sw128(b0 + kk * 16 * 128, 64 * kBK * 2, 1024)
+                                : smem_desc_sw128(b0 + kk * 32, 16, 1024);
+                        mma_f16_cta2(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    issued = true;
+                    const uint32_t e = smem_u32(&bar_empty[s]);
+                    mma_commit_cta2(e);
+                    mma_commit_cta2(map_to_cta(e, 1));
+                }
+                if (!ok) break;
+                const uint32_t f = smem_u32(&bar_tfull[b]);
+                mma_commit_cta2(f);
+                mma_commit_cta2(map_to_cta(f, 1));
+                ++acc;
+            }
+            if (!ok && issued) {
+                mma_commit_cta2(smem_u32(&bar_drain));
+                wait_drain(smem_u32(&bar_drain), 0, kDrainNs);
+            }
+        }
+    } else {
+        // ------------------------------ epilogue (warps 2..5, both CTAs) ---------------------
+        const int q = warp & 3;
+        const int row_in_tile = q * 32 + lane;
+        uint32_t acc = 0;
+        for (int t = pair; t < total; t += num_pairs, ++acc) {
+            int mt, nt;
+            tile_coords(t, args.num_m, args.num_n, kGroupM, mt, nt);
+            const uint32_t b = acc & 1u, aph = (acc >> 1) & 1u;
+            int ok = 1;
+            if (lane == 0)
+                ok = wait_bounded(smem_u32(&bar_tfull[b]), aph, abort, args.timeout_ns,
+                                  &g_dtc_status, 14);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after_sync();
+            const int64_t row = (int64_t)mt * 256 + (int64_t)rank * kBMc + row_in_tile;
+            uint16_t* crow = reinterpret_cast<uint16_t*>(args.C) + row * args.N;
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + b * kAccStride;
+#pragma unroll 1
+            for (int c = 0; c < kBN / 32; ++c) {
+                uint32_t v[32];
+                tmem_load_32cols(taddr + c * 32, v);
+                if (c == kBN / 32 - 1) {
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&bar_tempty[b]), 0));
+                }
+                if (row < args.M) {
+                    const int col0 = nt * kBN + c * 32;
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const int col = col0 + g * 8;
+                        if (col < args.N) {
+                            uint4 w;
+                            w.x = pack2<kBF16>(v[g * 8 + 0], v[g * 8 + 1]);
+                            w.y = pack2<kBF16>(v[g * 8 + 2], v[g * 8 + 3]);
+                            w.z = pack2<kBF16>(v[g * 8 + 4], v[g * 8 + 5]);
+                            w.w = pack2<kBF16>(v[g * 8 + 6], v[g * 8 + 7]);
+                            *reinterpret_cast<uint4*>(crow + col) = w;
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    // ------------------------------ teardown ------------------------------
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync();  // no CTA leaves while its peer may still signal its barriers
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc<2>(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace dtc

@@ -31,6 +31,27 @@ __device__ __forceinline__ uint32_t lane_id() {
 }
 
 // ---------------------------------------------------------------------------------------------
+// Clusters
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// The shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_cta(uint32_t smem_addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+    return r;
+}
+
+// Every thread of every CTA in the cluster arrives, then waits (release / acquire).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------------------------
 // mbarrier (shared::cta)
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -119,6 +140,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+// Multicast form: the tile is written at offset `dst` of every CTA in `cta_mask` (bit i = CTA
+// rank i of the cluster) and each destination's barrier at offset `bar` receives the byte count.
+__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* m,
+                                                      uint32_t bar, int32_t c0, int32_t c1,
+                                                      uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "h"(cta_mask)
         : "memory");
 }
 
@@ -260,23 +293,31 @@ __device__ __forceinline__ void tmem_store_wait() {
 // ---------------------------------------------------------------------------------------------
 // Descriptors
 // ---------------------------------------------------------------------------------------------
-// Shared-memory matrix descriptor, 128-byte swizzle (the layout a TMA load with
-// CU_TENSOR_MAP_SWIZZLE_128B writes). Fields: start address >> 4 in bits 0-13, leading-dimension
+// Shared-memory matrix descriptor. Fields: start address >> 4 in bits 0-13, leading-dimension
 // byte offset >> 4 in bits 16-29, stride-dimension byte offset >> 4 in bits 32-45, the fixed
-// value 1 in bits 46-47, base offset 0 (atoms are 1024-byte aligned), swizzle mode 2 (128B) in
-// bits 61-63.
-//   K-major operand: rows of 128 bytes; SBO = 1024 (8 rows); LBO unused (set to 16 bytes).
-//   MN-major operand: 128-byte rows along MN, one row per K index; SBO = 1024 (8 K rows),
-//   LBO = byte distance between consecutive 64-element MN chunks.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes,
-                                                    uint32_t sbo_bytes) {
+// value 1 in bits 46-47, base offset 0 (swizzle atoms start on 1024-byte boundaries), swizzle
+// mode in bits 61-63 (2 = 128-byte, 4 = 64-byte): the layouts TMA writes with
+// CU_TENSOR_MAP_SWIZZLE_128B / _64B.
+//   K-major operand: rows of 128 (or 64) bytes; SBO = 8 rows (1024 or 512 bytes); LBO unused
+//   (set to 16 bytes).
+//   MN-major operand (128-byte swizzle): 128-byte rows along MN, one row per K index;
+//   SBO = 1024 (8 K rows), LBO = byte distance between consecutive 64-element MN chunks.
+template <int kSwizzleBytes>
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes,
+                                              uint32_t sbo_bytes) {
+    static_assert(kSwizzleBytes == 128 || kSwizzleBytes == 64, "128- or 64-byte swizzle");
     uint64_t d = 0;
     d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
     d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
     d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
     d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
+    d |= (uint64_t)(kSwizzleBytes == 128 ? 2 : 4) << 61;
     return d;
+}
+
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes,
+                                                    uint32_t sbo_bytes) {
+    return smem_desc<128>(saddr, lbo_bytes, sbo_bytes);
 }
 
 // Instruction descriptor, kind::f16: D format f32 (bits 4-5 = 1), A/B format (bits 7-9, 10-12:

@@ -56,8 +56,10 @@ typedef enum {
 /* Kernel variants (gemm_options.variant). AUTO picks per shape. */
 typedef enum {
     GEMM_VARIANT_AUTO = 0,
-    GEMM_VARIANT_1CTA = 1,   /* persistent 128x256 tiles, one CTA per tile */
-    GEMM_VARIANT_2CTA = 2,   /* persistent 256x256 tiles on a CTA pair (cluster 2x1) */
+    GEMM_VARIANT_1CTA = 1,   /* persistent 128 x 256 or 128 x 224 tiles, one CTA per tile, in
+                                clusters of 1 or 2 CTAs along M sharing B by TMA multicast */
+    GEMM_VARIANT_2CTA = 2,   /* persistent 256 x 256 or 256 x 224 tiles on a CTA pair
+                                (cluster 2x1, tcgen05 cta_group::2) */
     GEMM_VARIANT_SPLITK = 3  /* 128 x BN tiles with K split across CTAs (skinny, memory-bound) */
 } gemm_variant;
 
@@ -68,6 +70,10 @@ typedef struct {
     int fault_inject;     /* test hook, 0 in normal use. 1 = the load producer skips its first
                              stage, so the consumer's bounded wait runs out and the call reports
                              GEMM_ERR_TIMEOUT through gemm_stream_status. */
+    int tile_n;           /* force the N-tile (256 or 224; 224 for NT only); 0 = choose */
+    int cluster_m;        /* 1CTA only: CTAs per cluster along M sharing B by multicast (1 or
+                             2); 0 = choose */
+    int tile_k;           /* 1CTA only: K-elements per pipeline stage (64 or 32); 0 = choose */
 } gemm_options;
 
 /*
@@ -112,9 +118,24 @@ int gemm_ex(int dtype, const void* A, const void* B, const void* sfA, const void
             int64_t M, int64_t N, int64_t K, int layout, const gemm_options* opts,
             dtc_stream_t stream);
 
-/* The variant that gemm_ex/gemm_* would launch for these arguments (GEMM_VARIANT_*), or a
- * negative gemm_status if they would be rejected. Makes no CUDA call except device queries. */
-int gemm_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm_options* opts);
+/* What a call with these sizes and options would launch. */
+typedef struct {
+    int variant;  /* GEMM_VARIANT_1CTA, _2CTA or _SPLITK (never AUTO) */
+    int tile_m;   /* rows of C per tile (per CTA pair for 2CTA) */
+    int tile_n;   /* columns of C per tile */
+    int tile_k;   /* K-elements per pipeline stage */
+    int stages;   /* depth of the shared-memory ring */
+    int split_k;  /* K-slices (1 unless SPLITK) */
+    int ctas;     /* CTAs launched (persistent grid) */
+    int tiles;    /* output tiles (times split_k work units for SPLITK) */
+    int cluster;  /* CTAs per cluster */
+} gemm_plan_info;
+
+/* Fills *info with the launch that gemm_ex would make for these sizes and options. Returns
+ * GEMM_OK, or the status the call would fail with (sizes/layout/dtype only; pointers are not
+ * part of the plan). Makes no CUDA call except device queries. */
+int gemm_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm_options* opts,
+              gemm_plan_info* info);
 
 /* Message for the calling thread's most recent non-OK return ("" if none). Valid until that
  * thread's next call into the library. */

@@ -35,9 +35,19 @@ def run16(kind, layout, A, B, M, N, K, variant=0, **kw):
     return C.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def full_check(kind, layout, M, N, K, seed, variant=0):
+_INPUT_CACHE = {}
+
+
+def _cached_inputs(name):
+    if name not in _INPUT_CACHE:
+        _INPUT_CACHE.clear()
+        _INPUT_CACHE[name] = workloads.make(workloads.WORKLOADS[name])
+    return _INPUT_CACHE[name]
+
+
+def full_check(kind, layout, M, N, K, seed, variant=0, **kw):
     A, B = workloads.make16(kind, layout, M, N, K, seed)
-    C = run16(kind, layout, A, B, M, N, K, variant)
+    C = run16(kind, layout, A, B, M, N, K, variant, **kw)
     ref = oracle.gemm16(kind, layout, A, B, M, N, K)
     return check_close(values16(C, kind), values16(ref, kind), f"{kind} {layout} {M}x{N}x{K}")
 
@@ -52,19 +62,76 @@ SHAPES = [
 ]
 
 
+VARIANTS = {"1cta": 1, "2cta": 2}
+
+
+@pytest.mark.parametrize("variant", list(VARIANTS))
 @pytest.mark.parametrize("kind", ["bf16", "f16"])
 @pytest.mark.parametrize("layout", ["NT", "NN"])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
-def test_small_shapes_full_parity(kind, layout, shape):
+def test_small_shapes_full_parity(kind, layout, shape, variant):
     M, N, K = shape
-    full_check(kind, layout, M, N, K, seed=M + N + K)
+    full_check(kind, layout, M, N, K, seed=M + N + K, variant=VARIANTS[variant])
 
 
-@pytest.mark.parametrize("kind,layout", [("bf16", "NT"), ("f16", "NN")])
-def test_more_tiles_than_sms_full_parity(kind, layout):
-    # 256 tiles (> 152 SMs): CTAs loop over several tiles, the two accumulators alternate, and
-    # with K = 128 the epilogue of one tile overlaps the short main loop of the next.
-    full_check(kind, layout, 4096, 2048, 128, seed=77)
+@pytest.mark.parametrize("variant", list(VARIANTS))
+@pytest.mark.parametrize("kind,layout", [("bf16", "NT"), ("f16", "NN"), ("f16", "NT")])
+def test_more_tiles_than_sms_full_parity(kind, layout, variant):
+    # 256 one-CTA tiles or 128-152 pair tiles (more than the resident CTAs / pairs): CTAs loop over
+    # several tiles, the two accumulators alternate, and with K = 128 the epilogue of one tile
+    # overlaps the short main loop of the next.
+    full_check(kind, layout, 4096, 2048, 128, seed=77, variant=VARIANTS[variant])
+
+
+@pytest.mark.parametrize("tile_k", [64, 32])
+@pytest.mark.parametrize("cluster_m", [1, 2])
+@pytest.mark.parametrize("tile_n", [256, 224])
+@pytest.mark.parametrize("layout", ["NT", "NN"])
+@pytest.mark.parametrize("M,N,K", [(640, 520, 200), (384, 264, 136), (1152, 1792, 512)])
+def test_one_cta_configurations_full_parity(M, N, K, layout, tile_n, cluster_m, tile_k):
+    # every tile width, K-block depth and cluster size; 640 and 384 rows give an odd number of
+    # 128-row tiles, so with clusters of 2 one CTA of the last cluster computes rows past M (loads
+    # zeros, stores nothing); K = 200 and 136 end in a partial K-block
+    if layout == "NN" and tile_n == 224:
+        pytest.skip("224-wide tiles are offered for NT only")
+    import dense_tensor_core_gb300 as dtc
+
+    p = dtc.gemm_plan("bf16", M, N, K, layout, variant=1, tile_n=tile_n, cluster_m=cluster_m,
+                      tile_k=tile_k)
+    assert p["cluster"] == cluster_m and p["tile_n"] == tile_n and p["tile_k"] == tile_k
+    assert p["ctas"] % cluster_m == 0
+    full_check("bf16", layout, M, N, K, seed=M + N, variant=1, tile_n=tile_n,
+               cluster_m=cluster_m, tile_k=tile_k)
+
+
+def test_automatic_choice_follows_the_cost_model():
+    import dense_tensor_core_gb300 as dtc
+
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the expected choices are worked out for 152 SMs")
+    p = dtc.gemm_plan("bf16", 4096, 4096, 8192, "NT")  # 608 one-CTA 128x224 tiles = 4 waves
+    assert (p["variant"], p["tile_n"], p["tile_k"], p["cluster"]) == (1, 224, 64, 1)
+    p = dtc.gemm_plan("bf16", 8192, 8192, 8192, "NT")  # 1024 pair tiles of 256x256
+    assert (p["variant"], p["tile_m"], p["tile_n"]) == (2, 256, 256)
+    p = dtc.gemm_plan("f16", 1024, 1024, 1024, "NN")  # under one wave: one-CTA tiles
+    assert p["variant"] == 1 and p["tile_n"] == 256
+
+
+@pytest.mark.parametrize("M,N,tile_n", [(4096, 4096, 224), (8192, 8192, 256), (512, 448, 224)])
+def test_pair_tile_width_choice(M, N, tile_n):
+    import dense_tensor_core_gb300 as dtc
+
+    p = dtc.gemm_plan("bf16", M, N, 8192, "NT", variant=2)
+    assert p["variant"] == 2 and p["tile_m"] == 256 and p["tile_n"] == tile_n
+    assert p["ctas"] % 2 == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(512, 448, 320), (600, 904, 264), (4096, 4096, 256)])
+def test_pair_kernel_224_wide_tiles_full_parity(M, N, K):
+    import dense_tensor_core_gb300 as dtc
+
+    assert dtc.gemm_plan("bf16", M, N, K, "NT", variant=2)["tile_n"] == 224
+    full_check("bf16", "NT", M, N, K, seed=M + K, variant=2)
 
 
 def test_config_bf16_nt_256x256x512_full():
@@ -77,12 +144,14 @@ def test_config_f16_nn_1024_full():
     full_check(w.kind, w.layout, w.M, w.N, w.K, w.seed)
 
 
+@pytest.mark.parametrize("variant", [0, 1, 2])
 @pytest.mark.parametrize("name", ["bf16_nt_4096x4096x8192", "bf16_nt_8192x8192x8192",
                                   "bf16_nt_128x8192x8192"])
-def test_benchmark_sizes_sampled(name):
+def test_benchmark_sizes_sampled(name, variant):
+    # variant 0 is the launch the benchmark times (the library's own choice)
     w = workloads.WORKLOADS[name]
-    A, B = workloads.make(w)
-    C = run16(w.kind, w.layout, A, B, w.M, w.N, w.K)
+    A, B = _cached_inputs(name)
+    C = run16(w.kind, w.layout, A, B, w.M, w.N, w.K, variant=variant)
     r, c = sample_positions(w.M, w.N, count=3000, seed=w.seed)
     # plus one full row and one full column
     r = np.concatenate([r, np.full(w.N, w.M // 3), np.arange(w.M)])
