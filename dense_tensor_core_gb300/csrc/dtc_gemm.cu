@@ -21,6 +21,8 @@
 #include "dtc_gemm.h"
 #include "gemm16_1cta.cuh"
 #include "gemm16_2cta.cuh"
+#include "gemm16_splitk.cuh"
+#include "gemm_mxfp8.cuh"
 
 namespace {
 
@@ -92,8 +94,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// Row-major 2-D tensor [outer, inner] with dense rows; box [box_outer, box_inner]; 128-byte
-// swizzle (box_inner * element size must be 128 bytes); out-of-bounds elements read as zero.
+// Row-major 2-D tensor [outer, inner] with dense rows; box [box_outer, box_inner]; with a swizzle
+// the box's inner extent is the swizzle width (128 or 64 bytes); out-of-bounds elements read as
+// zero.
 int make_tmap(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* ptr,
               uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
               CUtensorMapSwizzle swz, const char* name) {
@@ -243,8 +246,47 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
         return fail(GEMM_ERR_UNSUPPORTED, "tile width %d is not offered for this layout", want_n);
     if (dtype == 2 && v != GEMM_VARIANT_AUTO && v != GEMM_VARIANT_1CTA)
         return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 product has a one-CTA kernel only");
-    if (v == GEMM_VARIANT_SPLITK)
-        return fail(GEMM_ERR_UNSUPPORTED, "variant %d is not available in this build", v);
+    if (dtype == 2) {
+        if (v != GEMM_VARIANT_AUTO && v != GEMM_VARIANT_1CTA)
+            return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 product has a one-CTA kernel only");
+        if (want_n && want_n != dtc::gmx::kBN)
+            return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 kernel uses 224-wide tiles");
+        p->variant = GEMM_VARIANT_1CTA;
+        p->tile_m = dtc::gmx::kBM;
+        p->tile_n = dtc::gmx::kBN;
+        p->tile_k = dtc::gmx::kBK;
+        p->stages = dtc::gmx::kStages;
+        p->tiles = ceil_div(M, p->tile_m) * ceil_div(N, p->tile_n);
+        p->ctas = std::min(p->tiles, d->sms);
+        return GEMM_OK;
+    }
+    const int num_kb = ceil_div(K, 64);
+    const int64_t tiles256 = (int64_t)ceil_div(M, 128) * ceil_div(N, 256);
+    int split = o ? o->split_k : 0;
+    if (split != 0 && split != 2 && split != 4)
+        return fail(GEMM_ERR_INVALID_ARG, "split_k %d is not 2 or 4", split);
+    if (v == GEMM_VARIANT_AUTO && dtype != 2 && split == 0 && tiles256 * 2 <= d->sms) {
+        // Fewer 128 x 256 tiles than half the SMs: split K over a cluster of 4 (or 2) CTAs per
+        // tile, if the split still fits one wave and leaves each CTA at least 4 K-blocks.
+        if (num_kb >= 16 && tiles256 * 4 <= (int64_t)resident_clusters(4, d) * 4) split = 4;
+        else if (num_kb >= 8 && tiles256 * 2 <= (int64_t)resident_clusters(2, d) * 2) split = 2;
+        if (split) v = GEMM_VARIANT_SPLITK;
+    }
+    if (v == GEMM_VARIANT_SPLITK) {
+        if (dtype == 2) return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 product has no split-K kernel");
+        if (want_n && want_n != 256)
+            return fail(GEMM_ERR_UNSUPPORTED, "the split-K kernel uses 256-wide tiles");
+        p->variant = v;
+        p->split_k = split ? split : 4;
+        p->cluster = p->split_k;
+        p->tile_m = 128;
+        p->tile_n = 256;
+        p->tile_k = 64;
+        p->stages = 4;
+        p->tiles = (int)tiles256;
+        p->ctas = (int)tiles256 * p->split_k;
+        return GEMM_OK;
+    }
     int auto_n = 0;
     if (v == GEMM_VARIANT_AUTO) {
         // Cheapest (variant, width) by the cost model; 224-wide tiles exist for NT only. Below
@@ -409,9 +451,68 @@ int launch_1cta_cm(const Plan& p, const void* A, const void* B, void* C, int m, 
 
 
 
+template <bool kBF16, bool kNN, int kS>
+int launch_gemm16_splitk(const void* A, const void* B, void* C, int M, int N, int K,
+                         const gemm_options* o, DeviceInfo* dev, const Plan& p,
+                         cudaStream_t stream) {
+    using Cfg = dtc::gsk::Cfg<256, 4>;
+    const CUtensorMapDataType dt = kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUtensorMap tA, tB;
+    int rc = make_tmap(&tA, dt, 2, A, (uint64_t)K, (uint64_t)M, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "A");
+    if (rc) return rc;
+    if (!kNN)
+        rc = make_tmap(&tB, dt, 2, B, (uint64_t)K, (uint64_t)N, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B, "B");
+    else
+        rc = make_tmap(&tB, dt, 2, B, (uint64_t)N, (uint64_t)K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, "B");
+    if (rc) return rc;
+    auto kern = dtc::gemm16_splitk_kernel<kBF16, kNN, 256, 4, kS>;
+    if ((rc = ensure_smem_attr(kern, Cfg::kSmemBytes, dev))) return rc;
+    const Gemm16Args args = make_args(C, M, N, K, 128, 256, 64, o);
+    return launch_cluster(kern, p.ctas, dtc::gsk::kThreads, Cfg::kSmemBytes, kS, stream, tA, tB, args);
+}
+
+int launch_mxfp8(const void* A, const void* B, const void* sfA, const void* sfB, void* C, int M,
+                 int N, int K, const gemm_options* o, DeviceInfo* dev, const Plan& p,
+                 cudaStream_t stream) {
+    using namespace dtc::gmx;
+    CUtensorMap tA, tB;
+    int rc = make_tmap(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, (uint64_t)K, (uint64_t)M, kBK, kBM,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "A");
+    if (rc) return rc;
+    rc = make_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, (uint64_t)K, (uint64_t)N, kBK, kBN,
+                   CU_TENSOR_MAP_SWIZZLE_128B, "B");
+    if (rc) return rc;
+    auto kern = dtc::gemm_mxfp8_kernel<0>;
+    if ((rc = ensure_smem_attr(kern, kSmemBytes, dev))) return rc;
+    dtc::GemmMxArgs a;
+    a.C = C;
+    a.sfA = static_cast<const uint8_t*>(sfA);
+    a.sfB = static_cast<const uint8_t*>(sfB);
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.num_m = ceil_div(M, kBM);
+    a.num_n = ceil_div(N, kBN);
+    a.num_kb = ceil_div(K, kBK);
+    a.sf_cols = ceil_div(K, 128);
+    a.timeout_ns = (o && o->timeout_ns) ? o->timeout_ns : kDefaultTimeoutNs;
+    a.fault = o ? o->fault_inject : 0;
+    kern<<<p.ctas, kThreads, kSmemBytes, stream>>>(tA, tB, a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "MXFP8 kernel launch");
+    return GEMM_OK;
+}
+
 template <bool kBF16>
 int launch16(int layout, const Plan& p, const void* A, const void* B, void* C, int m, int n, int k,
              const gemm_options* o, DeviceInfo* dev, cudaStream_t stream) {
+    if (p.variant == GEMM_VARIANT_SPLITK) {
+        if (layout == GEMM_LAYOUT_NN)
+            return p.split_k == 2 ? launch_gemm16_splitk<kBF16, true, 2>(A, B, C, m, n, k, o, dev, p, stream)
+                                  : launch_gemm16_splitk<kBF16, true, 4>(A, B, C, m, n, k, o, dev, p, stream);
+        return p.split_k == 2 ? launch_gemm16_splitk<kBF16, false, 2>(A, B, C, m, n, k, o, dev, p, stream)
+                              : launch_gemm16_splitk<kBF16, false, 4>(A, B, C, m, n, k, o, dev, p, stream);
+    }
     if (p.variant == GEMM_VARIANT_1CTA) {
         if (p.tile_k == 32) {
             if (layout == GEMM_LAYOUT_NN)
@@ -447,7 +548,8 @@ int run(int dtype, const void* A, const void* B, const void* sfA, const void* sf
     }
     Plan p;
     if ((rc = make_plan(dtype, M, N, K, layout, o, info, &p))) return rc;
-    if (dtype == 2) return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 kernel is not available in this build");
+    if (dtype == 2)
+        return launch_mxfp8(A, B, sfA, sfB, C, (int)M, (int)N, (int)K, o, info, p, stream);
     const int m = (int)M, n = (int)N, k = (int)K;
     return dtype == 0 ? launch16<true>(layout, p, A, B, C, m, n, k, o, info, stream)
                       : launch16<false>(layout, p, A, B, C, m, n, k, o, info, stream);

@@ -60,12 +60,14 @@ typedef enum {
                                 clusters of 1 or 2 CTAs along M sharing B by TMA multicast */
     GEMM_VARIANT_2CTA = 2,   /* persistent 256 x 256 or 256 x 224 tiles on a CTA pair
                                 (cluster 2x1, tcgen05 cta_group::2) */
-    GEMM_VARIANT_SPLITK = 3  /* 128 x BN tiles with K split across CTAs (skinny, memory-bound) */
+    GEMM_VARIANT_SPLITK = 3  /* 128 x 256 tiles, K split over a cluster of 2 or 4 CTAs that
+                                reduce their partial sums in shared memory (few-tile products,
+                                such as the skinny memory-bound M = 128 case) */
 } gemm_variant;
 
 typedef struct {
     int variant;          /* a gemm_variant; GEMM_VARIANT_AUTO (0) chooses per shape */
-    int split_k;          /* SPLITK only: number of K-slices, 0 = choose */
+    int split_k;          /* SPLITK only: number of K-slices (2 or 4), 0 = choose */
     uint64_t timeout_ns;  /* limit of every device-side wait; 0 = the default (2 s) */
     int fault_inject;     /* test hook, 0 in normal use. 1 = the load producer skips its first
                              stage, so the consumer's bounded wait runs out and the call reports

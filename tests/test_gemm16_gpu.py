@@ -104,6 +104,22 @@ def test_one_cta_configurations_full_parity(M, N, K, layout, tile_n, cluster_m, 
                cluster_m=cluster_m, tile_k=tile_k)
 
 
+@pytest.mark.parametrize("split_k", [2, 4])
+@pytest.mark.parametrize("layout", ["NT", "NN"])
+@pytest.mark.parametrize("M,N,K", [(128, 2048, 4096), (300, 520, 1000), (64, 264, 64),
+                                   (129, 256, 200)])
+def test_split_k_full_parity(M, N, K, layout, split_k):
+    # K split over a cluster of CTAs that reduce in shared memory; K = 64 is one K-block, so all
+    # CTAs but one have an empty K-range and must contribute zeros; 300 x 520 and 129 x 256 leave
+    # partial tiles in M and N
+    import dense_tensor_core_gb300 as dtc
+
+    p = dtc.gemm_plan("bf16", M, N, K, layout, variant=3, split_k=split_k)
+    assert p["variant"] == 3 and p["split_k"] == split_k and p["cluster"] == split_k
+    full_check("bf16", layout, M, N, K, seed=M + K, variant=3, split_k=split_k)
+    full_check("f16", layout, M, N, K, seed=M + K + 1, variant=3, split_k=split_k)
+
+
 def test_automatic_choice_follows_the_cost_model():
     import dense_tensor_core_gb300 as dtc
 
@@ -113,8 +129,8 @@ def test_automatic_choice_follows_the_cost_model():
     assert (p["variant"], p["tile_n"], p["tile_k"], p["cluster"]) == (1, 224, 64, 1)
     p = dtc.gemm_plan("bf16", 8192, 8192, 8192, "NT")  # 1024 pair tiles of 256x256
     assert (p["variant"], p["tile_m"], p["tile_n"]) == (2, 256, 256)
-    p = dtc.gemm_plan("f16", 1024, 1024, 1024, "NN")  # under one wave: one-CTA tiles
-    assert p["variant"] == 1 and p["tile_n"] == 256
+    p = dtc.gemm_plan("bf16", 128, 8192, 8192, "NT")  # 32 tiles: K split over clusters of 4
+    assert (p["variant"], p["split_k"], p["ctas"]) == (3, 4, 128)
 
 
 @pytest.mark.parametrize("M,N,tile_n", [(4096, 4096, 224), (8192, 8192, 256), (512, 448, 224)])

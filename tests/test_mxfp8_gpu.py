@@ -1,0 +1,129 @@
+"""GPU parity of the MXFP8 block-scaled GEMM (e4m3 x e4m3, E8M0 scale per row per 128 K-elements,
+bf16 output) against the CPU oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dense_tensor_core_gb300 import workloads
+from parity import check_close, sample_positions, to_device8, values16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from dense_tensor_core_gb300 import build
+
+    build.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def run_mx(A, B, sfA, sfB, **kw):
+    import dense_tensor_core_gb300 as dtc
+
+    C = dtc.gemm_ex("mxfp8", to_device8(A), to_device8(B), sfA=to_device8(sfA),
+                    sfB=to_device8(sfB), **kw)
+    dtc.gemm_stream_status()
+    return C.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def check_mx(A, B, sfA, sfB, what):
+    M, K = A.shape
+    N = B.shape[0]
+    C = run_mx(A, B, sfA, sfB)
+    ref = oracle.gemm_mxfp8(A, B, sfA, sfB, M, N, K)
+    return check_close(values16(C, "bf16"), values16(ref, "bf16"), what)
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (128, 224, 128),    # one tile, one K-block, one scale group
+    (256, 448, 1024),   # 4 tiles, 8 K-blocks = 2 scale groups
+    (300, 520, 400),    # ragged M and N; K = 3 K-blocks + 16 (partial block and group)
+    (1, 8, 16),         # smallest legal product
+    (129, 232, 656),    # a row / 8 columns past a tile; 6 K-blocks (one partial group)
+    (640, 896, 2048),   # 20 tiles, 16 K-blocks
+])
+def test_small_shapes_full_parity(M, N, K):
+    A, B, sfA, sfB = workloads.make_mxfp8(M, N, K, seed=M + N + K)
+    check_mx(A, B, sfA, sfB, f"mxfp8 {M}x{N}x{K}")
+
+
+def test_unit_scales_reduce_to_plain_e4m3():
+    M, N, K = 256, 448, 512
+    A, B, sfA, sfB = workloads.make_mxfp8(M, N, K, seed=3)
+    check_mx(A, B, np.full_like(sfA, 127), np.full_like(sfB, 127), "unit scales")
+
+
+@pytest.mark.parametrize("which", ["a_rows", "b_rows", "k_blocks"])
+def test_scales_varying_along_one_axis(which):
+    # Scales that vary along a single axis: a wrong row / column / K-block mapping of the scale
+    # layout in Tensor Memory shows up as a failure of exactly one of these.
+    M, N, K = 256, 448, 1024
+    A, B, sfA, sfB = workloads.make_mxfp8(M, N, K, seed=4)
+    kb = sfA.shape[1]
+    sfA[:] = 127
+    sfB[:] = 127
+    if which == "a_rows":
+        sfA[:] = (120 + (np.arange(M) % 13))[:, None]
+    elif which == "b_rows":
+        sfB[:] = (121 + (np.arange(N) % 11))[:, None]
+    else:
+        sfA[:] = (123 + (np.arange(kb) % 7))[None, :]
+        sfB[:] = (130 - (np.arange(kb) % 5))[None, :]
+    check_mx(A, B, sfA, sfB, f"scales along {which}")
+
+
+def test_wide_scale_range():
+    M, N, K = 128, 224, 512
+    A, B, sfA, sfB = workloads.make_mxfp8(M, N, K, seed=5)
+    rng = np.random.default_rng(0)
+    sfA[:] = rng.integers(110, 145, sfA.shape)
+    sfB[:] = rng.integers(110, 145, sfB.shape)
+    check_mx(A, B, sfA, sfB, "wide scale range")
+
+
+def test_more_tiles_than_sms():
+    # 20 x 10 = 200 tiles of 128 x 224 over 152 SMs: persistent loop, both accumulators
+    M, N, K = 2560, 2240, 256
+    A, B, sfA, sfB = workloads.make_mxfp8(M, N, K, seed=6)
+    check_mx(A, B, sfA, sfB, "more tiles than SMs")
+
+
+def test_benchmark_size_sampled():
+    w = workloads.WORKLOADS["mxfp8_nt_4096x4096x8192"]
+    A, B, sfA, sfB = workloads.make(w)
+    C = run_mx(A, B, sfA, sfB)
+    r, c = sample_positions(w.M, w.N, count=3000, seed=w.seed, tile_m=128, tile_n=224)
+    r = np.concatenate([r, np.full(w.N, 1000), np.arange(w.M)])
+    c = np.concatenate([c, np.arange(w.N), np.full(w.M, 999)])
+    ref, _ = oracle.gemm_mxfp8_sampled(A, B, sfA, sfB, w.M, w.N, w.K, r, c)
+    check_close(values16(C[r, c], "bf16"), values16(ref, "bf16"), w.name)
+
+
+def test_k_zero_and_empty():
+    import dense_tensor_core_gb300 as dtc
+
+    A = torch.empty((64, 0), dtype=torch.uint8, device="cuda")
+    B = torch.empty((32, 0), dtype=torch.uint8, device="cuda")
+    sf = torch.empty((64, 0), dtype=torch.uint8, device="cuda")
+    sfb = torch.empty((32, 0), dtype=torch.uint8, device="cuda")
+    C = torch.full((64, 32), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dtc.gemm_mxfp8(A, B, sf, sfb, C)
+    dtc.gemm_stream_status()
+    assert torch.equal(C, torch.zeros_like(C))
+
+
+def test_timeout_reports_and_recovers():
+    import dense_tensor_core_gb300 as dtc
+
+    M, N, K = 256, 448, 512
+    A, B, sfA, sfB = workloads.make_mxfp8(M, N, K, seed=7)
+    dtc.gemm_stream_status()
+    dtc.gemm_ex("mxfp8", to_device8(A), to_device8(B), sfA=to_device8(sfA), sfB=to_device8(sfB),
+                timeout_ns=20_000_000, fault_inject=1)
+    with pytest.raises(dtc.GemmError) as e:
+        dtc.gemm_stream_status()
+    assert e.value.status == 4
+    check_mx(A, B, sfA, sfB, "after timeout")

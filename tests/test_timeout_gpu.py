@@ -24,7 +24,7 @@ def built():
         pytest.skip("no CUDA device")
 
 
-@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("variant", [1, 2, 3])
 def test_wait_that_nothing_completes_reports_timeout_then_recovers(variant):
     import dense_tensor_core_gb300 as dtc
 
