@@ -114,6 +114,25 @@ int make_tmap(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void
     return GEMM_OK;
 }
 
+// A K-major row-major [rows, K] operand seen as the 3-D tensor {64, rows, ceil(K/64)} with
+// strides (row, 128 bytes): a box {64, box_rows, 2} is two 128-byte K-chunks of box_rows rows in
+// one instruction. Requires K % 64 == 0 (a partial last chunk would read into the next row).
+int make_tmap_kchunks(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t K,
+                      uint64_t rows, uint32_t box_rows, const char* name) {
+    auto fn = encode_fn();
+    if (!fn) return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
+    cuuint64_t dims[3] = {64, rows, (K + 63) / 64};
+    cuuint64_t strides[2] = {K * 2, 128};
+    cuuint32_t box[3] = {64, box_rows, 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled(%s, 3-D) failed with CUresult %d", name, (int)r);
+    return GEMM_OK;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Shared argument rules of every entry point. Returns GEMM_OK or an error (message set).
@@ -171,7 +190,8 @@ int ensure_smem_attr(Kern kern, int bytes, DeviceInfo* dev) {
     return GEMM_OK;
 }
 
-constexpr int kPairStages = 6;
+// Ring depth of the pair kernel: 6 stages of 64-deep K-blocks, or 3 of 128-deep ones.
+constexpr int pair_stages(int bn, int bk) { return bk == 128 ? 3 : 6 + 0 * bn; }
 
 // Ring depth of the one-CTA kernel for each (tile width, K-block): as many stages as about
 // 220 KB of shared memory holds.
@@ -214,18 +234,21 @@ int64_t wave_cost(int64_t tiles, int clusters, int bn) { return (int64_t)ceil_di
 
 // Sustained fraction of tensor peak that one busy unit (an SM running 128 x BN tiles, or a CTA
 // pair running 256 x BN tiles) reaches in the main loop, measured on GB300 with bf16 NT operands
-// at K = 8192 (4096 x 4096 and 8192 x 8192 products, L2 flushed). The rest of the time goes to
-// waiting for operands: the kernels are bound by L2 -> shared-memory delivery, and the wider and
-// taller tiles need fewer bytes per flop.
+// at K = 8192 (4096 x 4096 and 8192 x 8192 products, L2 flushed). The kernels are bound by operand
+// delivery from L2 into shared memory, which is fastest with few, large TMA instructions: the
+// pair kernel's 128-deep stages (one 3-D box of two K-chunks per operand, needs K % 64 == 0)
+// beat its 64-deep ones, and the wider, taller tiles need fewer bytes per flop.
 struct TileChoice {
-    int variant, tile_n;
+    int variant, tile_n, tile_k;
     double efficiency;
 };
 constexpr TileChoice kChoices[] = {
-    {GEMM_VARIANT_1CTA, 256, 0.61},
-    {GEMM_VARIANT_1CTA, 224, 0.58},
-    {GEMM_VARIANT_2CTA, 256, 0.64},
-    {GEMM_VARIANT_2CTA, 224, 0.56},
+    {GEMM_VARIANT_1CTA, 256, 64, 0.61},
+    {GEMM_VARIANT_1CTA, 224, 64, 0.585},
+    {GEMM_VARIANT_2CTA, 256, 128, 0.70},
+    {GEMM_VARIANT_2CTA, 224, 128, 0.635},
+    {GEMM_VARIANT_2CTA, 256, 64, 0.64},
+    {GEMM_VARIANT_2CTA, 224, 64, 0.56},
 };
 
 // Busy time of the slowest SM, in units of (128 x 1 x K) MMA work at full rate: waves of tiles
@@ -295,8 +318,8 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
         int best_v = GEMM_VARIANT_1CTA, best_n = 256;
         for (const TileChoice& c : kChoices) {
             if (c.tile_n == 224 && layout != GEMM_LAYOUT_NT) continue;
-            if (dtype == 2 && c.variant != GEMM_VARIANT_1CTA) continue;
             if (want_n && c.tile_n != want_n) continue;
+            if (c.variant == GEMM_VARIANT_2CTA && (c.tile_k == 128) != (K % 64 == 0)) continue;
             double cost = plan_cost(c.variant, c.tile_n, c.efficiency, M, N, d->sms);
             if (c.variant == GEMM_VARIANT_2CTA && ceil_div(M, 256) * ceil_div(N, c.tile_n) < d->sms / 2)
                 cost *= 1.25;
@@ -356,7 +379,14 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
                             ? 224
                             : 256;
         }
-        p->stages = kPairStages;
+        int bk = o ? o->tile_k : 0;
+        if (bk != 0 && bk != 64 && bk != 128)
+            return fail(GEMM_ERR_INVALID_ARG, "tile_k %d is not 64 or 128 for the pair kernel", bk);
+        if (bk == 128 && K % 64)
+            return fail(GEMM_ERR_UNSUPPORTED, "128-deep pair stages need K %% 64 == 0");
+        if (bk == 0) bk = K % 64 == 0 ? 128 : 64;
+        p->tile_k = bk;
+        p->stages = pair_stages(p->tile_n, bk);
         p->tiles = ceil_div(M, 256) * ceil_div(N, p->tile_n);
         p->ctas = 2 * std::min(p->tiles, pairs);
     }
@@ -421,23 +451,26 @@ int launch_gemm16_1cta(const void* A, const void* B, void* C, int M, int N, int 
     return launch_cluster(kern, p.ctas, kThreads, Cfg::kSmemBytes, kCM, stream, tA, tB, args);
 }
 
-template <bool kBF16, bool kNN, int kBN>
+template <bool kBF16, bool kNN, int kBN, int kBK>
 int launch_gemm16_2cta(const void* A, const void* B, void* C, int M, int N, int K,
                        const gemm_options* o, DeviceInfo* dev, const Plan& p,
                        cudaStream_t stream) {
-    using Cfg = dtc::g2::Cfg<kBN, kPairStages>;
+    constexpr int kStages = pair_stages(kBN, kBK);
+    using Cfg = dtc::g2::Cfg<kBN, kBK, kStages>;
     const CUtensorMapDataType dt = kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUtensorMap tA, tB;
-    int rc = make_tmap(&tA, dt, 2, A, (uint64_t)K, (uint64_t)M, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "A");
+    int rc = kBK == 128 ? make_tmap_kchunks(&tA, dt, A, (uint64_t)K, (uint64_t)M, 128, "A")
+                        : make_tmap(&tA, dt, 2, A, (uint64_t)K, (uint64_t)M, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "A");
     if (rc) return rc;
     if (!kNN)
-        rc = make_tmap(&tB, dt, 2, B, (uint64_t)K, (uint64_t)N, 64, Cfg::kHalfN, CU_TENSOR_MAP_SWIZZLE_128B, "B");
+        rc = kBK == 128 ? make_tmap_kchunks(&tB, dt, B, (uint64_t)K, (uint64_t)N, Cfg::kHalfN, "B")
+                        : make_tmap(&tB, dt, 2, B, (uint64_t)K, (uint64_t)N, 64, Cfg::kHalfN, CU_TENSOR_MAP_SWIZZLE_128B, "B");
     else
-        rc = make_tmap(&tB, dt, 2, B, (uint64_t)N, (uint64_t)K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, "B");
+        rc = make_tmap(&tB, dt, 2, B, (uint64_t)N, (uint64_t)K, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B, "B");
     if (rc) return rc;
-    auto kern = dtc::gemm16_2cta_kernel<kBF16, kNN, kBN, kPairStages>;
+    auto kern = dtc::gemm16_2cta_kernel<kBF16, kNN, kBN, kBK, kStages>;
     if ((rc = ensure_smem_attr(kern, Cfg::kSmemBytes, dev))) return rc;
-    const Gemm16Args args = make_args(C, M, N, K, 256, kBN, 64, o);
+    const Gemm16Args args = make_args(C, M, N, K, 256, kBN, kBK, o);
     return launch_cluster(kern, p.ctas, dtc::g2::kThreads, Cfg::kSmemBytes, 2, stream, tA, tB, args);
 }
 
@@ -527,10 +560,17 @@ int launch16(int layout, const Plan& p, const void* A, const void* B, void* C, i
             return launch_1cta_cm<kBF16, false, 224, 64, stages_for(224, 64)>(p, A, B, C, m, n, k, o, dev, stream);
         return launch_1cta_cm<kBF16, false, 256, 64, stages_for(256, 64)>(p, A, B, C, m, n, k, o, dev, stream);
     }
+    if (p.tile_k == 128) {
+        if (layout == GEMM_LAYOUT_NN)
+            return launch_gemm16_2cta<kBF16, true, 256, 128>(A, B, C, m, n, k, o, dev, p, stream);
+        if (p.tile_n == 224)
+            return launch_gemm16_2cta<kBF16, false, 224, 128>(A, B, C, m, n, k, o, dev, p, stream);
+        return launch_gemm16_2cta<kBF16, false, 256, 128>(A, B, C, m, n, k, o, dev, p, stream);
+    }
     if (layout == GEMM_LAYOUT_NN)
-        return launch_gemm16_2cta<kBF16, true, 256>(A, B, C, m, n, k, o, dev, p, stream);
-    if (p.tile_n == 224) return launch_gemm16_2cta<kBF16, false, 224>(A, B, C, m, n, k, o, dev, p, stream);
-    return launch_gemm16_2cta<kBF16, false, 256>(A, B, C, m, n, k, o, dev, p, stream);
+        return launch_gemm16_2cta<kBF16, true, 256, 64>(A, B, C, m, n, k, o, dev, p, stream);
+    if (p.tile_n == 224) return launch_gemm16_2cta<kBF16, false, 224, 64>(A, B, C, m, n, k, o, dev, p, stream);
+    return launch_gemm16_2cta<kBF16, false, 256, 64>(A, B, C, m, n, k, o, dev, p, stream);
 }
 
 int run(int dtype, const void* A, const void* B, const void* sfA, const void* sfB, void* C,

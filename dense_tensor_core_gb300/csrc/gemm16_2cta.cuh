@@ -24,7 +24,6 @@ namespace dtc {
 
 namespace g2 {
 constexpr int kBMc = 128;  // rows of C per CTA
-constexpr int kBK = 64;
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;
 constexpr int kAccStride = 256;  // column offset of the second accumulator
@@ -32,11 +31,16 @@ constexpr int kGroupM = 8;
 constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
 constexpr uint64_t kPeerSettleNs = 1000ull * 1000;  // 1 ms
 
-template <int kBN, int kStages>
+// K-blocks of 64 (one 128-byte swizzle row; one 2-D box per operand) or 128 (two rows; for
+// NT one 3-D box {64, rows, 2} per operand). A TMA instruction's cost does not grow much with its
+// size, and measured per-SM delivery is highest with the large 3-D boxes: a 128-deep stage feeds
+// the tensor pipe better than two 64-deep ones, although fewer stages fit.
+template <int kBN, int kBK, int kStages>
 struct Cfg {
     static constexpr int kHalfN = kBN / 2;
     static constexpr int kAStage = kBMc * kBK * 2;
     static constexpr int kBStage = kHalfN * kBK * 2;
+    static_assert(kBK == 64 || kBK == 128, "K-block of 64 or 128");
     static constexpr int kStageBytes = kAStage + kBStage;
     static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
     static_assert(kBN % 32 == 0 && kBN >= 64 && kBN <= 256, "pair tile N must be 64..256, /32");
@@ -44,12 +48,13 @@ struct Cfg {
 };
 }  // namespace g2
 
-template <bool kBF16, bool kNN, int kBN, int kStages>
+template <bool kBF16, bool kNN, int kBN, int kBK, int kStages>
 __global__ void __launch_bounds__(g2::kThreads, 1)
     gemm16_2cta_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const Gemm16Args args) {
     using namespace g2;
-    using C_ = Cfg<kBN, kStages>;
+    using C_ = Cfg<kBN, kBK, kStages>;
+    constexpr int kChunks = kBK / 64;  // 128-byte K-chunks per stage
     static_assert(!kNN || C_::kHalfN % 64 == 0, "NN needs whole 64-column B boxes per CTA");
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[kStages];
@@ -121,9 +126,17 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
                     const uint32_t full_local = smem_u32(&bar_full[s]);
                     const uint32_t full_leader = map_to_cta(full_local, 0);
                     if (leader) mbar_arrive_expect_tx(full_local, 2 * C_::kStageBytes);
-                    tma_load_2d_pair(sA + s * C_::kAStage, &tmA, full_leader, kb * kBK, a_row);
+                    if constexpr (kChunks == 2)
+                        tma_load_3d_pair(sA + s * C_::kAStage, &tmA, full_leader, 0, a_row, kb * 2);
+                    else
+                        tma_load_2d_pair(sA + s * C_::kAStage, &tmA, full_leader, kb * kBK, a_row);
                     if constexpr (!kNN) {
-                        tma_load_2d_pair(sB + s * C_::kBStage, &tmB, full_leader, kb * kBK, b_row);
+                        if constexpr (kChunks == 2)
+                            tma_load_3d_pair(sB + s * C_::kBStage, &tmB, full_leader, 0, b_row,
+                                             kb * 2);
+                        else
+                            tma_load_2d_pair(sB + s * C_::kBStage, &tmB, full_leader, kb * kBK,
+                                             b_row);
                     } else {
 #pragma unroll
                         for (int j = 0; j < C_::kHalfN / 64; ++j)
@@ -172,10 +185,13 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
                     const uint32_t a0 = sA + s * C_::kAStage, b0 = sB + s * C_::kBStage;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint64_t adesc = smem_desc_sw128(a0 + kk * 32, 16, 1024);
+                        // K-chunk kk/4 of the stage, 32-byte step kk%4 inside its swizzle row
+                        const uint32_t koff = (kk % 4) * 32;
+                        const uint64_t adesc =
+                            smem_desc_sw128(a0 + (kk / 4) * (kBMc * 128) + koff, 16, 1024);
                         const uint64_t bdesc =
                             kNN ? smem_desc_sw128(b0 + kk * 16 * 128, 64 * kBK * 2, 1024)
-                                : smem_desc_sw128(b0 + kk * 32, 16, 1024);
+                                : smem_desc_sw128(b0 + (kk / 4) * (C_::kHalfN * 128) + koff, 16, 1024);
                         mma_f16_cta2(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     issued = true;

@@ -125,12 +125,31 @@ def test_automatic_choice_follows_the_cost_model():
 
     if torch.cuda.get_device_properties(0).multi_processor_count != 152:
         pytest.skip("the expected choices are worked out for 152 SMs")
-    p = dtc.gemm_plan("bf16", 4096, 4096, 8192, "NT")  # 608 one-CTA 128x224 tiles = 4 waves
-    assert (p["variant"], p["tile_n"], p["tile_k"], p["cluster"]) == (1, 224, 64, 1)
+    p = dtc.gemm_plan("bf16", 4096, 4096, 8192, "NT")  # 304 pair tiles of 256x224 = 4 waves
+    assert (p["variant"], p["tile_m"], p["tile_n"], p["tile_k"]) == (2, 256, 224, 128)
     p = dtc.gemm_plan("bf16", 8192, 8192, 8192, "NT")  # 1024 pair tiles of 256x256
-    assert (p["variant"], p["tile_m"], p["tile_n"]) == (2, 256, 256)
+    assert (p["variant"], p["tile_m"], p["tile_n"], p["tile_k"]) == (2, 256, 256, 128)
+    p = dtc.gemm_plan("bf16", 4096, 4096, 8200, "NT")  # K % 64 != 0: 64-deep stages only
+    assert p["tile_k"] == 64
     p = dtc.gemm_plan("bf16", 128, 8192, 8192, "NT")  # 32 tiles: K split over clusters of 4
     assert (p["variant"], p["split_k"], p["ctas"]) == (3, 4, 128)
+
+
+@pytest.mark.parametrize("tile_k", [64, 128])
+@pytest.mark.parametrize("tile_n", [256, 224])
+@pytest.mark.parametrize("layout", ["NT", "NN"])
+@pytest.mark.parametrize("M,N,K", [(640, 520, 192), (384, 264, 320), (1280, 1792, 1024)])
+def test_pair_kernel_configurations_full_parity(M, N, K, layout, tile_n, tile_k):
+    # 128-deep stages load each operand with one 3-D box of two 128-byte K-chunks; K = 192 and
+    # 320 end in a half-filled 128-deep stage; 640 and 384 rows leave a partial pair tile
+    if layout == "NN" and tile_n == 224:
+        pytest.skip("224-wide tiles are offered for NT only")
+    import dense_tensor_core_gb300 as dtc
+
+    p = dtc.gemm_plan("bf16", M, N, K, layout, variant=2, tile_n=tile_n, tile_k=tile_k)
+    assert (p["tile_m"], p["tile_n"], p["tile_k"]) == (256, tile_n, tile_k)
+    full_check("bf16", layout, M, N, K, seed=M + K, variant=2, tile_n=tile_n, tile_k=tile_k)
+    full_check("f16", layout, M, N, K, seed=M + K + 1, variant=2, tile_n=tile_n, tile_k=tile_k)
 
 
 @pytest.mark.parametrize("M,N,tile_n", [(4096, 4096, 224), (8192, 8192, 256), (512, 448, 224)])
