@@ -5,12 +5,14 @@
 // warp, single-thread tcgen05.mma issuer, Tensor Memory accumulator), but a cluster of kS CTAs
 // computes one tile: CTA r accumulates the r-th of kS contiguous K-ranges. The partial sums are
 // reduced on chip, without a global workspace:
-//   1. each CTA's epilogue copies its fp32 accumulator (tcgen05.ld) into its own shared memory,
-//      over the ring buffers, which are idle once the tile's last MMA has completed;
+//   1. each CTA's epilogue copies its fp32 accumulator (tcgen05.ld, 64 columns per round trip)
+//      into its own shared memory, over the ring buffers, which are idle once the tile's last
+//      MMA has completed;
 //   2. cluster barrier;
 //   3. CTA r sums rows [r*128/kS, (r+1)*128/kS) of the tile over the kS CTAs' copies, reading
 //      them through distributed shared memory in the fixed order 0..kS-1 (so the result does not
-//      depend on which CTA finished first), rounds once to the output type and stores;
+//      depend on which CTA finished first; each thread keeps 4 column groups x kS loads in
+//      flight), rounds once to the output type and stores;
 //   4. cluster barrier (no CTA leaves while a peer may still read its copy).
 // One cluster per tile, not persistent: a product of T tiles launches T * kS CTAs.
 #pragma once
@@ -47,6 +49,7 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
     using namespace gsk;
     using C_ = Cfg<kBN, kStages>;
     static_assert(kS == 2 || kS == 4, "K split over 2 or 4 CTAs");
+    static_assert(kBN % 64 == 0, "the accumulator is read 64 columns at a time");
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[kStages];
     __shared__ __align__(8) uint64_t bar_empty[kStages];
@@ -158,7 +161,8 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
                 wait_drain(smem_u32(&bar_drain), 0, kDrainNs);
             }
         }
-    } else {
+    }
+    if (warp >= 2) {
         // -------------------- epilogue part 1: accumulator -> own shared memory --------------
         const int q = warp & 3;
         const int row = q * 32 + lane;
@@ -172,16 +176,16 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
             const uint32_t xrow = sX + row * C_::kXPitch;
             const bool empty_slice = kb1 <= kb0;  // no K-blocks: this CTA's share is zero
 #pragma unroll 1
-            for (int c = 0; c < kBN / 32; ++c) {
-                uint32_t v[32];
-                tmem_load_32cols(taddr + c * 32, v);
+            for (int c = 0; c < kBN / 64; ++c) {
+                uint32_t v[64];
+                tmem_load_64cols(taddr + c * 64, v);
 #pragma unroll
-                for (int g = 0; g < 8; ++g) {
+                for (int g = 0; g < 16; ++g) {
+                    const uint32_t a = xrow + (c * 64 + g * 4) * 4;
                     if (empty_slice)
-                        st_shared_u4(xrow + (c * 32 + g * 4) * 4, 0u, 0u, 0u, 0u);
+                        st_shared_u4(a, 0u, 0u, 0u, 0u);
                     else
-                        st_shared_u4(xrow + (c * 32 + g * 4) * 4, v[g * 4 + 0], v[g * 4 + 1],
-                                     v[g * 4 + 2], v[g * 4 + 3]);
+                        st_shared_u4(a, v[g * 4 + 0], v[g * 4 + 1], v[g * 4 + 2], v[g * 4 + 3]);
                 }
             }
         }
@@ -192,31 +196,53 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
     __syncthreads();
     cluster_sync();  // every CTA's partial sums are in its shared memory
     {
-        constexpr int kRows = kBM / kS;      // rows of the tile this CTA reduces
-        constexpr int kGroups = kBN / 4;     // 4-column groups per row
+        constexpr int kRows = kBM / kS;   // rows of the tile this CTA reduces
+        constexpr int kGroups = kBN / 4;  // 4-column groups per row
+        constexpr int kItems = kRows * kGroups;
+        constexpr int kUnroll = 4;        // column groups per thread per round
         uint32_t peer[kS];
 #pragma unroll
         for (int s = 0; s < kS; ++s) peer[s] = map_to_cta(sX, (uint32_t)s);
-        for (int i = threadIdx.x; i < kRows * kGroups; i += kThreads) {
-            const int r = (int)rank * kRows + i / kGroups;
-            const int g = i % kGroups;
-            const int64_t grow = (int64_t)mt * kBM + r;
-            const int gcol = nt * kBN + g * 4;
-            if (grow >= args.M || gcol >= args.N) continue;
-            const uint32_t off = r * C_::kXPitch + g * 16;
-            float4 acc = ld_shared_cluster_f4(peer[0] + off);
+        for (int i0 = threadIdx.x; i0 < kItems; i0 += kThreads * kUnroll) {
+            float4 acc[kUnroll];
+            uint32_t off[kUnroll];
+            bool live[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int i = i0 + u * kThreads;
+                live[u] = i < kItems;
+                const int r = (int)rank * kRows + (live[u] ? i / kGroups : 0);
+                const int g = live[u] ? i % kGroups : 0;
+                off[u] = r * C_::kXPitch + g * 16;
+                acc[u] = live[u] ? ld_shared_cluster_f4(peer[0] + off[u]) : make_float4(0, 0, 0, 0);
+            }
 #pragma unroll
             for (int s = 1; s < kS; ++s) {
-                const float4 v = ld_shared_cluster_f4(peer[s] + off);
-                acc.x += v.x;
-                acc.y += v.y;
-                acc.z += v.z;
-                acc.w += v.w;
+                float4 v[kUnroll];
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u)
+                    v[u] = live[u] ? ld_shared_cluster_f4(peer[s] + off[u]) : make_float4(0, 0, 0, 0);
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    acc[u].x += v[u].x;
+                    acc[u].y += v[u].y;
+                    acc[u].z += v[u].z;
+                    acc[u].w += v[u].w;
+                }
             }
-            uint2 out;
-            out.x = pack2<kBF16>(__float_as_uint(acc.x), __float_as_uint(acc.y));
-            out.y = pack2<kBF16>(__float_as_uint(acc.z), __float_as_uint(acc.w));
-            *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(args.C) + grow * args.N + gcol) = out;
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int i = i0 + u * kThreads;
+                if (!live[u]) continue;
+                const int64_t grow = (int64_t)mt * kBM + (int64_t)rank * kRows + i / kGroups;
+                const int gcol = nt * kBN + (i % kGroups) * 4;
+                if (grow >= args.M || gcol >= args.N) continue;
+                uint2 out;
+                out.x = pack2<kBF16>(__float_as_uint(acc[u].x), __float_as_uint(acc[u].y));
+                out.y = pack2<kBF16>(__float_as_uint(acc[u].z), __float_as_uint(acc[u].w));
+                *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(args.C) + grow * args.N +
+                                          gcol) = out;
+            }
         }
     }
     cluster_sync();  // peers are done reading this CTA's copy
