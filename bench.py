@@ -263,7 +263,7 @@ def run_reference(args, w):
 def kernel_of(w, plan):
     """The name of the kernel the plan launches (as in the ncu launch list)."""
     if w.kind == "mxfp8":
-        return "gemm_mxfp8_kernel"
+        return "gemm_mxfp8_2cta_kernel" if plan["variant"] == 2 else "gemm_mxfp8_kernel"
     return {1: "gemm16_1cta_kernel", 2: "gemm16_2cta_kernel",
             3: "gemm16_splitk_kernel"}.get(plan["variant"], str(plan["variant"]))
 

@@ -23,6 +23,7 @@
 #include "gemm16_2cta.cuh"
 #include "gemm16_splitk.cuh"
 #include "gemm_mxfp8.cuh"
+#include "gemm_mxfp8_2cta.cuh"
 
 namespace {
 
@@ -114,16 +115,18 @@ int make_tmap(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void
     return GEMM_OK;
 }
 
-// A K-major row-major [rows, K] operand seen as the 3-D tensor {64, rows, ceil(K/64)} with
-// strides (row, 128 bytes): a box {64, box_rows, 2} is two 128-byte K-chunks of box_rows rows in
-// one instruction. Requires K % 64 == 0 (a partial last chunk would read into the next row).
-int make_tmap_kchunks(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t K,
-                      uint64_t rows, uint32_t box_rows, const char* name) {
+// A K-major row-major [rows, K] operand seen as the 3-D tensor {E, rows, ceil(K/E)}, E = the
+// elements in 128 bytes, with strides (row, 128 bytes): a box {E, box_rows, 2} is two 128-byte
+// K-chunks of box_rows rows in one instruction. Requires K % E == 0 (a partial last chunk would
+// read into the next row).
+int make_tmap_kchunks(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* ptr,
+                      uint64_t K, uint64_t rows, uint32_t box_rows, const char* name) {
     auto fn = encode_fn();
     if (!fn) return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
-    cuuint64_t dims[3] = {64, rows, (K + 63) / 64};
-    cuuint64_t strides[2] = {K * 2, 128};
-    cuuint32_t box[3] = {64, box_rows, 2};
+    const uint64_t e = 128 / elem_bytes;
+    cuuint64_t dims[3] = {e, rows, (K + e - 1) / e};
+    cuuint64_t strides[2] = {K * (uint64_t)elem_bytes, 128};
+    cuuint32_t box[3] = {(cuuint32_t)e, box_rows, 2};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -267,13 +270,28 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
     const int want_n = o ? o->tile_n : 0;
     if (want_n && want_n != 256 && !(want_n == 224 && layout == GEMM_LAYOUT_NT))
         return fail(GEMM_ERR_UNSUPPORTED, "tile width %d is not offered for this layout", want_n);
-    if (dtype == 2 && v != GEMM_VARIANT_AUTO && v != GEMM_VARIANT_1CTA)
-        return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 product has a one-CTA kernel only");
     if (dtype == 2) {
-        if (v != GEMM_VARIANT_AUTO && v != GEMM_VARIANT_1CTA)
-            return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 product has a one-CTA kernel only");
+        if (v != GEMM_VARIANT_AUTO && v != GEMM_VARIANT_1CTA && v != GEMM_VARIANT_2CTA)
+            return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 product has one-CTA and pair kernels");
         if (want_n && want_n != dtc::gmx::kBN)
-            return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 kernel uses 224-wide tiles");
+            return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 kernels use 224-wide tiles");
+        if (v == GEMM_VARIANT_2CTA && K % 128)
+            return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 pair kernel needs K %% 128 == 0");
+        const int64_t pair_tiles = (int64_t)ceil_div(M, 256) * ceil_div(N, dtc::gmx2::kBN);
+        // The pair kernel is correct but measured slower than the one-CTA kernel on GB300
+        // (2008 vs 2357 TFLOP/s on 4096 x 4096 x 8192): it is an option, never chosen here.
+        if (v == GEMM_VARIANT_AUTO) v = GEMM_VARIANT_1CTA;
+        if (v == GEMM_VARIANT_2CTA) {
+            p->variant = v;
+            p->cluster = 2;
+            p->tile_m = 256;
+            p->tile_n = dtc::gmx2::kBN;
+            p->tile_k = dtc::gmx2::kBK;
+            p->stages = dtc::gmx2::kStages;
+            p->tiles = (int)pair_tiles;
+            p->ctas = 2 * std::min(p->tiles, std::max(1, d->sms / 2));
+            return GEMM_OK;
+        }
         p->variant = GEMM_VARIANT_1CTA;
         p->tile_m = dtc::gmx::kBM;
         p->tile_n = dtc::gmx::kBN;
@@ -459,11 +477,11 @@ int launch_gemm16_2cta(const void* A, const void* B, void* C, int M, int N, int 
     using Cfg = dtc::g2::Cfg<kBN, kBK, kStages>;
     const CUtensorMapDataType dt = kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUtensorMap tA, tB;
-    int rc = kBK == 128 ? make_tmap_kchunks(&tA, dt, A, (uint64_t)K, (uint64_t)M, 128, "A")
+    int rc = kBK == 128 ? make_tmap_kchunks(&tA, dt, 2, A, (uint64_t)K, (uint64_t)M, 128, "A")
                         : make_tmap(&tA, dt, 2, A, (uint64_t)K, (uint64_t)M, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "A");
     if (rc) return rc;
     if (!kNN)
-        rc = kBK == 128 ? make_tmap_kchunks(&tB, dt, B, (uint64_t)K, (uint64_t)N, Cfg::kHalfN, "B")
+        rc = kBK == 128 ? make_tmap_kchunks(&tB, dt, 2, B, (uint64_t)K, (uint64_t)N, Cfg::kHalfN, "B")
                         : make_tmap(&tB, dt, 2, B, (uint64_t)K, (uint64_t)N, 64, Cfg::kHalfN, CU_TENSOR_MAP_SWIZZLE_128B, "B");
     else
         rc = make_tmap(&tB, dt, 2, B, (uint64_t)N, (uint64_t)K, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B, "B");
@@ -504,9 +522,61 @@ int launch_gemm16_splitk(const void* A, const void* B, void* C, int M, int N, in
     return launch_cluster(kern, p.ctas, dtc::gsk::kThreads, Cfg::kSmemBytes, kS, stream, tA, tB, args);
 }
 
+dtc::GemmMxArgs mx_args(const void* sfA, const void* sfB, void* C, int M, int N, int K, int tile_m,
+                        int tile_n, int tile_k, const gemm_options* o) {
+    dtc::GemmMxArgs a;
+    a.C = C;
+    a.sfA = static_cast<const uint8_t*>(sfA);
+    a.sfB = static_cast<const uint8_t*>(sfB);
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.num_m = ceil_div(M, tile_m);
+    a.num_n = ceil_div(N, tile_n);
+    a.num_kb = ceil_div(K, tile_k);
+    a.sf_cols = ceil_div(K, 128);
+    a.timeout_ns = (o && o->timeout_ns) ? o->timeout_ns : kDefaultTimeoutNs;
+    a.fault = o ? o->fault_inject : 0;
+    return a;
+}
+
+int launch_mxfp8_2cta(const void* A, const void* B, const void* sfA, const void* sfB, void* C,
+                      int M, int N, int K, const gemm_options* o, DeviceInfo* dev, const Plan& p,
+                      cudaStream_t stream) {
+    using namespace dtc::gmx2;
+    CUtensorMap tA, tB;
+    int rc = make_tmap_kchunks(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, (uint64_t)K, (uint64_t)M,
+                               kBMc, "A");
+    if (rc) return rc;
+    rc = make_tmap_kchunks(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, (uint64_t)K, (uint64_t)N,
+                           kHalfN, "B");
+    if (rc) return rc;
+    auto kern = dtc::gemm_mxfp8_2cta_kernel<0>;
+    if ((rc = ensure_smem_attr(kern, kSmemBytes, dev))) return rc;
+    const dtc::GemmMxArgs a = mx_args(sfA, sfB, C, M, N, K, 256, kBN, kBK, o);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.ctas, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tA, tB, a);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "MXFP8 pair kernel launch");
+    return GEMM_OK;
+}
+
 int launch_mxfp8(const void* A, const void* B, const void* sfA, const void* sfB, void* C, int M,
                  int N, int K, const gemm_options* o, DeviceInfo* dev, const Plan& p,
                  cudaStream_t stream) {
+    if (p.variant == GEMM_VARIANT_2CTA)
+        return launch_mxfp8_2cta(A, B, sfA, sfB, C, M, N, K, o, dev, p, stream);
     using namespace dtc::gmx;
     CUtensorMap tA, tB;
     int rc = make_tmap(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, (uint64_t)K, (uint64_t)M, kBK, kBM,
@@ -517,19 +587,7 @@ int launch_mxfp8(const void* A, const void* B, const void* sfA, const void* sfB,
     if (rc) return rc;
     auto kern = dtc::gemm_mxfp8_kernel<0>;
     if ((rc = ensure_smem_attr(kern, kSmemBytes, dev))) return rc;
-    dtc::GemmMxArgs a;
-    a.C = C;
-    a.sfA = static_cast<const uint8_t*>(sfA);
-    a.sfB = static_cast<const uint8_t*>(sfB);
-    a.M = M;
-    a.N = N;
-    a.K = K;
-    a.num_m = ceil_div(M, kBM);
-    a.num_n = ceil_div(N, kBN);
-    a.num_kb = ceil_div(K, kBK);
-    a.sf_cols = ceil_div(K, 128);
-    a.timeout_ns = (o && o->timeout_ns) ? o->timeout_ns : kDefaultTimeoutNs;
-    a.fault = o ? o->fault_inject : 0;
+    const dtc::GemmMxArgs a = mx_args(sfA, sfB, C, M, N, K, kBM, kBN, kBK, o);
     kern<<<p.ctas, kThreads, kSmemBytes, stream>>>(tA, tB, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "MXFP8 kernel launch");

@@ -1,0 +1,331 @@
+// gemm_mxfp8_2cta.cuh -- persistent MXFP8 block-scaled GEMM on CTA pairs (cluster 2x1,
+// tcgen05 cta_group::2), NT layout, e4m3 x e4m3 with one E8M0 scale per row per 128 K-elements
+// for A and B, fp32 accumulation in Tensor Memory, bf16 output.
+//
+// The product of gemm_mxfp8.cuh (05 Blackwell TCGEN05 GEMM tutorial, "Advanced": gemm_blockscaled
+// with granularity 128 for both operands), on the tile shape and load pattern that feed the tensor
+// pipe best on GB300 (see gemm16_2cta.cuh): a pair computes a 256 x 224 tile; CTA r loads its own
+// 128 rows of A and its own 112 rows of B^T, each stage 256 K-elements deep (two 128-byte K-chunks
+// per row, one 3-D TMA box per operand), both CTAs' copies completing on the leader's full
+// barrier; the leader issues tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X
+// (M = 256, N = 224, K = 32), eight per stage, the four of each 128-deep half sharing its scales.
+//
+// Scales: as in the one-CTA kernel, R rows take R/32 Tensor Memory columns (row r in lane r % 32
+// of column r / 32, repeated in all four lane quarters), 4 consecutive 128-blocks packed per cell
+// and selected by the instruction's a_sf_id / b_sf_id. Each CTA holds the scales of its own 128 A
+// rows and of all 224 B rows (each CTA's datapath computes all 224 columns of its rows); its four
+// scale warps write them with tcgen05.st and arrive on the leader's scale-full barrier (8 arrivals
+// per set), and the leader's MMA thread releases a set to both CTAs with one commit each.
+//
+// Tensor Memory per CTA: accumulators at columns [0,224) and [224,448), scale sets at
+// 448 + 12*set (4 columns for A, 8 for B), set = 0..3.
+#pragma once
+
+#include "gemm_mxfp8.cuh"
+
+namespace dtc {
+
+namespace gmx2 {
+constexpr int kBMc = 128;  // rows of C per CTA
+constexpr int kBN = 224;   // columns of C per pair tile
+constexpr int kHalfN = kBN / 2;
+constexpr int kBK = 256;   // e4m3 elements per stage: two 128-byte K-chunks
+constexpr int kStages = 3;
+constexpr int kThreads = 320;
+constexpr int kAStage = kBMc * kBK;
+constexpr int kBStage = kHalfN * kBK;
+constexpr int kStageBytes = kAStage + kBStage;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+constexpr int kTmemCols = 512;
+constexpr int kAccStride = 224;
+constexpr int kSfBase = 448;
+constexpr int kSfSet = 12;
+constexpr int kSfSets = 4;
+constexpr int kGroup = 4;  // 128-blocks per scale set
+constexpr int kGroupM = 8;
+constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
+constexpr uint64_t kPeerSettleNs = 1000ull * 1000;
+static_assert(kSmemBytes <= 227 * 1024 - 512, "shared memory budget");
+static_assert(kSfBase + kSfSets * kSfSet <= kTmemCols, "Tensor Memory budget");
+}  // namespace gmx2
+
+template <int kUnused = 0>
+__global__ void __launch_bounds__(gmx2::kThreads, 1)
+    gemm_mxfp8_2cta_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB, const GemmMxArgs args) {
+    using namespace gmx2;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_full[kStages];
+    __shared__ __align__(8) uint64_t bar_empty[kStages];
+    __shared__ __align__(8) uint64_t bar_tfull[2];
+    __shared__ __align__(8) uint64_t bar_tempty[2];
+    __shared__ __align__(8) uint64_t bar_sfull[kSfSets];
+    __shared__ __align__(8) uint64_t bar_sempty[kSfSets];
+    __shared__ __align__(8) uint64_t bar_drain;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t sA = base;
+    const uint32_t sB = base + kStages * kAStage;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1;
+    const int num_pairs = gridDim.x >> 1;
+    const int total = args.num_m * args.num_n;  // num_m counts 256-row pair tiles
+    const int nk128 = 2 * args.num_kb;          // 128-blocks per tile (the last may be padding)
+    const int groups = (nk128 + kGroup - 1) / kGroup;
+    volatile int* abort = &abort_flag;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&bar_full[s]), 1);
+            mbar_init(smem_u32(&bar_empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&bar_tfull[b]), 1);
+            mbar_init(smem_u32(&bar_tempty[b]), 8);  // 4 epilogue warps in each CTA
+        }
+        for (int b = 0; b < kSfSets; ++b) {
+            mbar_init(smem_u32(&bar_sfull[b]), 8);  // 4 scale warps in each CTA
+            mbar_init(smem_u32(&bar_sempty[b]), 1);
+        }
+        mbar_init(smem_u32(&bar_drain), 1);
+        abort_flag = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc<2>(smem_u32(&tmem_slot), kTmemCols);
+        tmem_relinquish<2>();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer (both CTAs) ------------------------------
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = pair; t < total && ok; t += num_pairs) {
+                int mt, nt;
+                tile_coords(t, args.num_m, args.num_n, kGroupM, mt, nt);
+                const int a_row = mt * 256 + (int)rank * kBMc;
+                const int b_row = nt * kBN + (int)rank * kHalfN;
+                for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
+                    const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+                    if (!wait_bounded(smem_u32(&bar_empty[s]), ph ^ 1u, abort, args.timeout_ns,
+                                      &g_dtc_status, 41)) {
+                        ok = false;
+                        break;
+                    }
+                    if (args.fault == 1 && it == 0) continue;  // test hook: stage never filled
+                    const uint32_t full_local = smem_u32(&bar_full[s]);
+                    const uint32_t full_leader = map_to_cta(full_local, 0);
+                    if (leader) mbar_arrive_expect_tx(full_local, 2 * kStageBytes);
+                    tma_load_3d_pair(sA + s * kAStage, &tmA, full_leader, 0, a_row, kb * 2);
+                    tma_load_3d_pair(sB + s * kBStage, &tmB, full_leader, 0, b_row, kb * 2);
+                }
+            }
+            if (!ok && leader) {
+                const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0;
+                for (uint32_t i = first; i < it; ++i) {
+                    if (args.fault == 1 && i == 0) continue;
+                    wait_drain(smem_u32(&bar_full[i % kStages]), (i / kStages) & 1u, kDrainNs);
+                }
+            } else if (!ok) {
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < kPeerSettleNs) __nanosleep(1000);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer (leader CTA) ------------------------------
+        if (lane == 0 && leader) {
+            constexpr uint32_t idesc0 = idesc_mxf8(256, kBN, 0, 0);
+            uint32_t it = 0, acc = 0, sit = 0;
+            bool ok = true, issued = false;
+            for (int t = pair; t < total && ok; t += num_pairs) {
+                const uint32_t b = acc & 1u, aph = (acc >> 1) & 1u;
+                if (!wait_bounded(smem_u32(&bar_tempty[b]), aph ^ 1u, abort, args.timeout_ns,
+                                  &g_dtc_status, 42)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + b * kAccStride;
+                for (int kb = 0; kb < args.num_kb && ok; ++kb, ++it) {
+                    const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+                    if (!wait_bounded(smem_u32(&bar_full[s]), ph, abort, args.timeout_ns,
+                                      &g_dtc_status, 43)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a0 = sA + s * kAStage, b0 = sB + s * kBStage;
+#pragma unroll 1
+                    for (int ch = 0; ch < 2; ++ch) {
+                        const int k128 = 2 * kb + ch;
+                        const uint32_t set = sit % kSfSets;
+                        if (k128 % kGroup == 0) {
+                            if (!wait_bounded(smem_u32(&bar_sfull[set]), (sit / kSfSets) & 1u,
+                                              abort, args.timeout_ns, &g_dtc_status, 45)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after_sync();
+                        }
+                        const uint32_t sf_id = (uint32_t)(k128 % kGroup);
+                        const uint32_t idesc = idesc0 | (sf_id << 4) | (sf_id << 29);
+                        const uint32_t sfa = tmem_base + kSfBase + set * kSfSet;
+                        const uint32_t sfb = sfa + 4;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t adesc =
+                                smem_desc_sw128(a0 + ch * (kBMc * 128) + kk * 32, 16, 1024);
+                            const uint64_t bdesc =
+                                smem_desc_sw128(b0 + ch * (kHalfN * 128) + kk * 32, 16, 1024);
+                            mma_mxf8_cta2(d_tmem, adesc, bdesc, idesc, sfa, sfb,
+                                          (kb | ch | kk) != 0 ? 1u : 0u);
+                        }
+                        issued = true;
+                        if (k128 % kGroup == kGroup - 1 || k128 == nk128 - 1) {
+                            const uint32_t e = smem_u32(&bar_sempty[set]);
+                            mma_commit_cta2(e);
+                            mma_commit_cta2(map_to_cta(e, 1));
+                            ++sit;
+                        }
+                    }
+                    if (!ok) break;
+                    const uint32_t e = smem_u32(&bar_empty[s]);
+                    mma_commit_cta2(e);
+                    mma_commit_cta2(map_to_cta(e, 1));
+                }
+                if (!ok) break;
+                const uint32_t f = smem_u32(&bar_tfull[b]);
+                mma_commit_cta2(f);
+                mma_commit_cta2(map_to_cta(f, 1));
+                ++acc;
+            }
+            if (!ok && issued) {
+                mma_commit_cta2(smem_u32(&bar_drain));
+                wait_drain(smem_u32(&bar_drain), 0, kDrainNs);
+            }
+        }
+    } else if (warp < 6) {
+        // ------------------------------ epilogue (warps 2..5, both CTAs) ---------------------
+        const int q = warp & 3;
+        const int row_in_tile = q * 32 + lane;
+        uint32_t acc = 0;
+        for (int t = pair; t < total; t += num_pairs, ++acc) {
+            int mt, nt;
+            tile_coords(t, args.num_m, args.num_n, kGroupM, mt, nt);
+            const uint32_t b = acc & 1u, aph = (acc >> 1) & 1u;
+            int ok = 1;
+            if (lane == 0)
+                ok = wait_bounded(smem_u32(&bar_tfull[b]), aph, abort, args.timeout_ns,
+                                  &g_dtc_status, 44);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after_sync();
+            const int64_t row = (int64_t)mt * 256 + (int64_t)rank * kBMc + row_in_tile;
+            uint16_t* crow = reinterpret_cast<uint16_t*>(args.C) + row * args.N;
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + b * kAccStride;
+#pragma unroll 1
+            for (int c = 0; c < kBN / 32; ++c) {
+                uint32_t v[32];
+                tmem_load_32cols(taddr + c * 32, v);
+                if (c == kBN / 32 - 1) {
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&bar_tempty[b]), 0));
+                }
+                if (row < args.M) {
+                    const int col0 = nt * kBN + c * 32;
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const int col = col0 + g * 8;
+                        if (col < args.N) {
+                            uint4 w;
+                            w.x = pack2<true>(v[g * 8 + 0], v[g * 8 + 1]);
+                            w.y = pack2<true>(v[g * 8 + 2], v[g * 8 + 3]);
+                            w.z = pack2<true>(v[g * 8 + 4], v[g * 8 + 5]);
+                            w.w = pack2<true>(v[g * 8 + 6], v[g * 8 + 7]);
+                            *reinterpret_cast<uint4*>(crow + col) = w;
+                        }
+                    }
+                }
+            }
+        }
+    } else {
+        // ------------------------------ scale writers (warps 6..9, both CTAs) ----------------
+        const int q = warp & 3;
+        const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+        const int my_tiles = pair < total ? (total - 1 - pair) / num_pairs + 1 : 0;
+        const int steps = my_tiles * groups;
+        const uint32_t sfull_leader0 = map_to_cta(smem_u32(&bar_sfull[0]), 0);
+        uint32_t wa[4], wb[8];
+        auto gather = [&](int step, uint32_t (&ga)[4], uint32_t (&gb)[8]) {
+            const int t = pair + (step / groups) * num_pairs;
+            const int g = step % groups;
+            int mt, nt;
+            tile_coords(t, args.num_m, args.num_n, kGroupM, mt, nt);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                ga[j] = sf_word(args.sfA, args.M, args.sf_cols,
+                                mt * 256 + (int)rank * kBMc + lane + 32 * j, g);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                gb[j] = j < kBN / 32
+                            ? sf_word(args.sfB, args.N, args.sf_cols, nt * kBN + lane + 32 * j, g)
+                            : 0u;
+        };
+        if (steps > 0) gather(0, wa, wb);
+        for (int step = 0; step < steps; ++step) {
+            uint32_t na[4], nb[8];
+            if (step + 1 < steps) gather(step + 1, na, nb);
+            const uint32_t sit = (uint32_t)step;
+            const uint32_t set = sit % kSfSets;
+            int w_ok = 1;
+            if (lane == 0)
+                w_ok = wait_bounded(smem_u32(&bar_sempty[set]), ((sit / kSfSets) & 1u) ^ 1u, abort,
+                                    args.timeout_ns, &g_dtc_status, 46);
+            w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+            if (!w_ok) break;
+            tc_fence_after_sync();
+            const uint32_t col = tmem_base + kSfBase + set * kSfSet;
+            tmem_store_4cols(col + lane_addr, wa[0], wa[1], wa[2], wa[3]);
+            tmem_store_8cols(col + 4 + lane_addr, wb);
+            tmem_store_wait();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(sfull_leader0 + set * 8);
+            if (step + 1 < steps) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) wa[j] = na[j];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) wb[j] = nb[j];
+            }
+        }
+    }
+
+    // ------------------------------ teardown ------------------------------
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc<2>(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace dtc

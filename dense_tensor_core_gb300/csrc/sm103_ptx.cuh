@@ -301,6 +301,19 @@ __device__ __forceinline__ void mma_mxf8_cta1(uint32_t d_tmem, uint64_t adesc, u
         : "memory");
 }
 
+// CTA-pair form of the block-scaled MMA (M = 256 over the two CTAs of the pair).
+__device__ __forceinline__ void mma_mxf8_cta2(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
+        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` (own CTA) when every tcgen05 op issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit_cta1(uint32_t bar) {
     asm volatile(

@@ -59,7 +59,8 @@ typedef enum {
     GEMM_VARIANT_1CTA = 1,   /* persistent 128 x 256 or 128 x 224 tiles, one CTA per tile, in
                                 clusters of 1 or 2 CTAs along M sharing B by TMA multicast */
     GEMM_VARIANT_2CTA = 2,   /* persistent 256 x 256 or 256 x 224 tiles on a CTA pair
-                                (cluster 2x1, tcgen05 cta_group::2) */
+                                (cluster 2x1, tcgen05 cta_group::2); for MXFP8 (256 x 224,
+                                K % 128 == 0) an option that is never chosen automatically */
     GEMM_VARIANT_SPLITK = 3  /* 128 x 256 tiles, K split over a cluster of 2 or 4 CTAs that
                                 reduce their partial sums in shared memory (few-tile products,
                                 such as the skinny memory-bound M = 128 case) */

@@ -20,6 +20,15 @@ def built():
         pytest.skip("no CUDA device")
 
 
+_BENCH = []
+
+
+def _bench_inputs():
+    if not _BENCH:
+        _BENCH.append(workloads.make(workloads.WORKLOADS["mxfp8_nt_4096x4096x8192"]))
+    return _BENCH[0]
+
+
 def run_mx(A, B, sfA, sfB, **kw):
     import dense_tensor_core_gb300 as dtc
 
@@ -29,10 +38,10 @@ def run_mx(A, B, sfA, sfB, **kw):
     return C.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def check_mx(A, B, sfA, sfB, what):
+def check_mx(A, B, sfA, sfB, what, **kw):
     M, K = A.shape
     N = B.shape[0]
-    C = run_mx(A, B, sfA, sfB)
+    C = run_mx(A, B, sfA, sfB, **kw)
     ref = oracle.gemm_mxfp8(A, B, sfA, sfB, M, N, K)
     return check_close(values16(C, "bf16"), values16(ref, "bf16"), what)
 
@@ -47,7 +56,23 @@ def check_mx(A, B, sfA, sfB, what):
 ])
 def test_small_shapes_full_parity(M, N, K):
     A, B, sfA, sfB = workloads.make_mxfp8(M, N, K, seed=M + N + K)
-    check_mx(A, B, sfA, sfB, f"mxfp8 {M}x{N}x{K}")
+    check_mx(A, B, sfA, sfB, f"mxfp8 {M}x{N}x{K}", variant=1)
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (256, 224, 256),    # one pair tile, one 256-deep stage = 2 scale blocks
+    (512, 448, 1024),   # 4 pair tiles, 4 stages = 2 scale groups
+    (300, 520, 384),    # ragged M and N; the last stage is half padding (K = 3 x 128)
+    (1, 8, 128),        # smallest K the pair kernel takes
+    (640, 896, 2048),
+    (1280, 2240, 640),  # 50 pair tiles, 640 = 2.5 stages of 256 (half-padded last stage)
+])
+def test_pair_kernel_full_parity(M, N, K):
+    import dense_tensor_core_gb300 as dtc
+
+    assert dtc.gemm_plan("mxfp8", M, N, K, variant=2)["tile_m"] == 256
+    A, B, sfA, sfB = workloads.make_mxfp8(M, N, K, seed=M + N + K + 1)
+    check_mx(A, B, sfA, sfB, f"mxfp8 pair {M}x{N}x{K}", variant=2)
 
 
 def test_unit_scales_reduce_to_plain_e4m3():
@@ -56,8 +81,9 @@ def test_unit_scales_reduce_to_plain_e4m3():
     check_mx(A, B, np.full_like(sfA, 127), np.full_like(sfB, 127), "unit scales")
 
 
+@pytest.mark.parametrize("variant", [1, 2])
 @pytest.mark.parametrize("which", ["a_rows", "b_rows", "k_blocks"])
-def test_scales_varying_along_one_axis(which):
+def test_scales_varying_along_one_axis(which, variant):
     # Scales that vary along a single axis: a wrong row / column / K-block mapping of the scale
     # layout in Tensor Memory shows up as a failure of exactly one of these.
     M, N, K = 256, 448, 1024
@@ -72,7 +98,7 @@ def test_scales_varying_along_one_axis(which):
     else:
         sfA[:] = (123 + (np.arange(kb) % 7))[None, :]
         sfB[:] = (130 - (np.arange(kb) % 5))[None, :]
-    check_mx(A, B, sfA, sfB, f"scales along {which}")
+    check_mx(A, B, sfA, sfB, f"scales along {which}", variant=variant)
 
 
 def test_wide_scale_range():
@@ -84,17 +110,20 @@ def test_wide_scale_range():
     check_mx(A, B, sfA, sfB, "wide scale range")
 
 
-def test_more_tiles_than_sms():
-    # 20 x 10 = 200 tiles of 128 x 224 over 152 SMs: persistent loop, both accumulators
+@pytest.mark.parametrize("variant", [1, 2])
+def test_more_tiles_than_sms(variant):
+    # 200 one-CTA tiles of 128 x 224 over 152 SMs, or 100 pair tiles over 76 pairs: persistent
+    # loop, both accumulators, scale sets reused across tiles
     M, N, K = 2560, 2240, 256
     A, B, sfA, sfB = workloads.make_mxfp8(M, N, K, seed=6)
-    check_mx(A, B, sfA, sfB, "more tiles than SMs")
+    check_mx(A, B, sfA, sfB, "more tiles than SMs", variant=variant)
 
 
-def test_benchmark_size_sampled():
+@pytest.mark.parametrize("variant", [0, 1, 2])
+def test_benchmark_size_sampled(variant):
     w = workloads.WORKLOADS["mxfp8_nt_4096x4096x8192"]
-    A, B, sfA, sfB = workloads.make(w)
-    C = run_mx(A, B, sfA, sfB)
+    A, B, sfA, sfB = _bench_inputs()
+    C = run_mx(A, B, sfA, sfB, variant=variant)
     r, c = sample_positions(w.M, w.N, count=3000, seed=w.seed, tile_m=128, tile_n=224)
     r = np.concatenate([r, np.full(w.N, 1000), np.arange(w.M)])
     c = np.concatenate([c, np.arange(w.N), np.full(w.M, 999)])
@@ -115,15 +144,28 @@ def test_k_zero_and_empty():
     assert torch.equal(C, torch.zeros_like(C))
 
 
-def test_timeout_reports_and_recovers():
+@pytest.mark.parametrize("variant", [1, 2])
+def test_timeout_reports_and_recovers(variant):
     import dense_tensor_core_gb300 as dtc
 
     M, N, K = 256, 448, 512
     A, B, sfA, sfB = workloads.make_mxfp8(M, N, K, seed=7)
     dtc.gemm_stream_status()
     dtc.gemm_ex("mxfp8", to_device8(A), to_device8(B), sfA=to_device8(sfA), sfB=to_device8(sfB),
-                timeout_ns=20_000_000, fault_inject=1)
+                variant=variant, timeout_ns=20_000_000, fault_inject=1)
     with pytest.raises(dtc.GemmError) as e:
         dtc.gemm_stream_status()
     assert e.value.status == 4
-    check_mx(A, B, sfA, sfB, "after timeout")
+    check_mx(A, B, sfA, sfB, "after timeout", variant=variant)
+
+
+def test_automatic_choice():
+    import dense_tensor_core_gb300 as dtc
+
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the expected choices are worked out for 152 SMs")
+    # the pair kernel is an option (variant 2); the one-CTA kernel measured faster
+    assert dtc.gemm_plan("mxfp8", 4096, 4096, 8192)["variant"] == 1
+    assert dtc.gemm_plan("mxfp8", 4096, 4096, 8192, variant=2)["variant"] == 2
+    with pytest.raises(dtc.GemmError):
+        dtc.gemm_plan("mxfp8", 4096, 4096, 8208, variant=2)  # the pair kernel needs K % 128 == 0
