@@ -268,7 +268,7 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
     (void)K;
     int v = o ? o->variant : GEMM_VARIANT_AUTO;
     const int want_n = o ? o->tile_n : 0;
-    if (want_n && want_n != 256 && !(want_n == 224 && layout == GEMM_LAYOUT_NT))
+    if (want_n && want_n != 256 && want_n != 128 && !(want_n == 224 && layout == GEMM_LAYOUT_NT))
         return fail(GEMM_ERR_UNSUPPORTED, "tile width %d is not offered for this layout", want_n);
     if (dtype == 2) {
         if (v != GEMM_VARIANT_AUTO && v != GEMM_VARIANT_1CTA && v != GEMM_VARIANT_2CTA)
@@ -303,31 +303,56 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
     }
     const int num_kb = ceil_div(K, 64);
     const int64_t tiles256 = (int64_t)ceil_div(M, 128) * ceil_div(N, 256);
+    const int64_t tiles128 = (int64_t)ceil_div(M, 128) * ceil_div(N, 128);
     int split = o ? o->split_k : 0;
     if (split != 0 && split != 2 && split != 4)
         return fail(GEMM_ERR_INVALID_ARG, "split_k %d is not 2 or 4", split);
-    if (v == GEMM_VARIANT_AUTO && dtype != 2 && split == 0 && tiles256 * 2 <= d->sms) {
-        // Fewer 128 x 256 tiles than half the SMs: split K over a cluster of 4 (or 2) CTAs per
-        // tile, if the split still fits one wave and leaves each CTA at least 4 K-blocks.
-        if (num_kb >= 16 && tiles256 * 4 <= (int64_t)resident_clusters(4, d) * 4) split = 4;
-        else if (num_kb >= 8 && tiles256 * 2 <= (int64_t)resident_clusters(2, d) * 2) split = 2;
+    int split_n = want_n;
+    if (v == GEMM_VARIANT_AUTO && dtype != 2 && split == 0 && want_n != 224 &&
+        tiles256 * 2 <= d->sms) {
+        // Fewer 128 x 256 tiles than half the SMs: split K over a cluster of 2 or 4 CTAs per
+        // 128 x 128 or 128 x 256 tile. Take the (width, split) that occupies the most SMs in one
+        // wave, each CTA keeping at least 4 K-blocks of 64; on a tie the smaller split (less to
+        // reduce), then the narrower tile (a smaller exchange).
+        struct Cand { int bn, s; };
+        const Cand cands[4] = {{128, 2}, {128, 4}, {256, 2}, {256, 4}};
+        int64_t best_ctas = 0;
+        for (const Cand& c : cands) {
+            if (want_n && c.bn != want_n) continue;
+            const int64_t tl = c.bn == 128 ? tiles128 : tiles256;
+            const int64_t ctas = tl * c.s;
+            if (num_kb < 4 * c.s || ctas > (int64_t)resident_clusters(c.s, d) * c.s) continue;
+            if (ctas > best_ctas || (ctas == best_ctas && c.s < split)) {
+                best_ctas = ctas;
+                split = c.s;
+                split_n = c.bn;
+            }
+        }
         if (split) v = GEMM_VARIANT_SPLITK;
     }
     if (v == GEMM_VARIANT_SPLITK) {
         if (dtype == 2) return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 product has no split-K kernel");
-        if (want_n && want_n != 256)
-            return fail(GEMM_ERR_UNSUPPORTED, "the split-K kernel uses 256-wide tiles");
+        if (split_n && split_n != 256 && split_n != 128)
+            return fail(GEMM_ERR_UNSUPPORTED, "the split-K kernel uses 128- or 256-wide tiles");
+        const int bk_want = o ? o->tile_k : 0;
+        if (bk_want && bk_want != 64 && bk_want != 128)
+            return fail(GEMM_ERR_INVALID_ARG, "tile_k %d is not 64 or 128 for the split-K kernel", bk_want);
         p->variant = v;
-        p->split_k = split ? split : 4;
+        p->split_k = split ? split : 2;
         p->cluster = p->split_k;
         p->tile_m = 128;
-        p->tile_n = 256;
-        p->tile_k = 64;
-        p->stages = 4;
-        p->tiles = (int)tiles256;
-        p->ctas = (int)tiles256 * p->split_k;
+        p->tile_n = split_n ? split_n : 128;
+        // 128-deep stages (3-D boxes over 128-byte K-chunks) need K % 64 == 0; 256-wide tiles
+        // keep 64-deep stages, or too few stages would fit beside the exchange area
+        p->tile_k = bk_want ? bk_want : (p->tile_n == 128 && K % 64 == 0 ? 128 : 64);
+        if (p->tile_k == 128 && (K % 64 || p->tile_n != 128))
+            return fail(GEMM_ERR_UNSUPPORTED, "128-deep split-K stages need K %% 64 == 0 and 128-wide tiles");
+        p->stages = dtc::gsk::stages_for(p->tile_n, p->tile_k, p->split_k);
+        p->tiles = (int)(p->tile_n == 128 ? tiles128 : tiles256);
+        p->ctas = p->tiles * p->split_k;
         return GEMM_OK;
     }
+    if (want_n == 128) return fail(GEMM_ERR_UNSUPPORTED, "128-wide tiles are offered by the split-K kernel only");
     int auto_n = 0;
     if (v == GEMM_VARIANT_AUTO) {
         // Cheapest (variant, width) by the cost model; 224-wide tiles exist for NT only. Below
@@ -502,24 +527,41 @@ int launch_1cta_cm(const Plan& p, const void* A, const void* B, void* C, int m, 
 
 
 
-template <bool kBF16, bool kNN, int kS>
+template <bool kBF16, bool kNN, int kBN, int kBK, int kS>
 int launch_gemm16_splitk(const void* A, const void* B, void* C, int M, int N, int K,
                          const gemm_options* o, DeviceInfo* dev, const Plan& p,
                          cudaStream_t stream) {
-    using Cfg = dtc::gsk::Cfg<256, 4>;
+    constexpr int kStages = dtc::gsk::stages_for(kBN, kBK, kS);
+    using Cfg = dtc::gsk::Cfg<kBN, kBK, kStages, kS>;
     const CUtensorMapDataType dt = kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUtensorMap tA, tB;
-    int rc = make_tmap(&tA, dt, 2, A, (uint64_t)K, (uint64_t)M, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "A");
+    int rc = kBK == 128 ? make_tmap_kchunks(&tA, dt, 2, A, (uint64_t)K, (uint64_t)M, 128, "A")
+                        : make_tmap(&tA, dt, 2, A, (uint64_t)K, (uint64_t)M, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "A");
     if (rc) return rc;
     if (!kNN)
-        rc = make_tmap(&tB, dt, 2, B, (uint64_t)K, (uint64_t)N, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B, "B");
+        rc = kBK == 128 ? make_tmap_kchunks(&tB, dt, 2, B, (uint64_t)K, (uint64_t)N, kBN, "B")
+                        : make_tmap(&tB, dt, 2, B, (uint64_t)K, (uint64_t)N, 64, kBN, CU_TENSOR_MAP_SWIZZLE_128B, "B");
     else
-        rc = make_tmap(&tB, dt, 2, B, (uint64_t)N, (uint64_t)K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, "B");
+        rc = make_tmap(&tB, dt, 2, B, (uint64_t)N, (uint64_t)K, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B, "B");
     if (rc) return rc;
-    auto kern = dtc::gemm16_splitk_kernel<kBF16, kNN, 256, 4, kS>;
+    auto kern = dtc::gemm16_splitk_kernel<kBF16, kNN, kBN, kBK, kStages, kS>;
     if ((rc = ensure_smem_attr(kern, Cfg::kSmemBytes, dev))) return rc;
-    const Gemm16Args args = make_args(C, M, N, K, 128, 256, 64, o);
+    const Gemm16Args args = make_args(C, M, N, K, 128, kBN, kBK, o);
     return launch_cluster(kern, p.ctas, dtc::gsk::kThreads, Cfg::kSmemBytes, kS, stream, tA, tB, args);
+}
+
+template <bool kBF16, bool kNN>
+int launch_splitk_any(const Plan& p, const void* A, const void* B, void* C, int m, int n, int k,
+                      const gemm_options* o, DeviceInfo* dev, cudaStream_t stream) {
+    if (p.tile_n == 128) {
+        if (p.tile_k == 128)
+            return p.split_k == 2 ? launch_gemm16_splitk<kBF16, kNN, 128, 128, 2>(A, B, C, m, n, k, o, dev, p, stream)
+                                  : launch_gemm16_splitk<kBF16, kNN, 128, 128, 4>(A, B, C, m, n, k, o, dev, p, stream);
+        return p.split_k == 2 ? launch_gemm16_splitk<kBF16, kNN, 128, 64, 2>(A, B, C, m, n, k, o, dev, p, stream)
+                              : launch_gemm16_splitk<kBF16, kNN, 128, 64, 4>(A, B, C, m, n, k, o, dev, p, stream);
+    }
+    return p.split_k == 2 ? launch_gemm16_splitk<kBF16, kNN, 256, 64, 2>(A, B, C, m, n, k, o, dev, p, stream)
+                          : launch_gemm16_splitk<kBF16, kNN, 256, 64, 4>(A, B, C, m, n, k, o, dev, p, stream);
 }
 
 dtc::GemmMxArgs mx_args(const void* sfA, const void* sfB, void* C, int M, int N, int K, int tile_m,
@@ -599,10 +641,8 @@ int launch16(int layout, const Plan& p, const void* A, const void* B, void* C, i
              const gemm_options* o, DeviceInfo* dev, cudaStream_t stream) {
     if (p.variant == GEMM_VARIANT_SPLITK) {
         if (layout == GEMM_LAYOUT_NN)
-            return p.split_k == 2 ? launch_gemm16_splitk<kBF16, true, 2>(A, B, C, m, n, k, o, dev, p, stream)
-                                  : launch_gemm16_splitk<kBF16, true, 4>(A, B, C, m, n, k, o, dev, p, stream);
-        return p.split_k == 2 ? launch_gemm16_splitk<kBF16, false, 2>(A, B, C, m, n, k, o, dev, p, stream)
-                              : launch_gemm16_splitk<kBF16, false, 4>(A, B, C, m, n, k, o, dev, p, stream);
+            return launch_splitk_any<kBF16, true>(p, A, B, C, m, n, k, o, dev, stream);
+        return launch_splitk_any<kBF16, false>(p, A, B, C, m, n, k, o, dev, stream);
     }
     if (p.variant == GEMM_VARIANT_1CTA) {
         if (p.tile_k == 32) {

@@ -1,19 +1,24 @@
 // gemm16_splitk.cuh -- bf16/fp16 GEMM with K split across the CTAs of a cluster, for products
-// with too few output tiles to occupy the GPU (the skinny, memory-bound M = 128 case).
+// with too few output tiles to occupy the GPU (the skinny, memory-bound M = 128 case, and small
+// M x N with a long K).
 //
-// C[M,N] = A[M,K] . Bop as in the one-CTA kernel (128 x kBN tiles, 64-deep K-blocks, TMA producer
+// C[M,N] = A[M,K] . Bop as in the one-CTA kernel (128 x kBN tiles, kBK-deep K-blocks, TMA producer
 // warp, single-thread tcgen05.mma issuer, Tensor Memory accumulator), but a cluster of kS CTAs
 // computes one tile: CTA r accumulates the r-th of kS contiguous K-ranges. The partial sums are
-// reduced on chip, without a global workspace:
-//   1. each CTA's epilogue copies its fp32 accumulator (tcgen05.ld, 64 columns per round trip)
-//      into its own shared memory, over the ring buffers, which are idle once the tile's last
-//      MMA has completed;
-//   2. cluster barrier;
-//   3. CTA r sums rows [r*128/kS, (r+1)*128/kS) of the tile over the kS CTAs' copies, reading
-//      them through distributed shared memory in the fixed order 0..kS-1 (so the result does not
-//      depend on which CTA finished first; each thread keeps 4 column groups x kS loads in
-//      flight), rounds once to the output type and stores;
-//   4. cluster barrier (no CTA leaves while a peer may still read its copy).
+// reduced on chip, without a global workspace. CTA r owns rows [r*128/kS, (r+1)*128/kS) of the
+// tile, i.e. 4/kS of the four 32-lane quarters of the accumulator:
+//   1. an epilogue warp whose quarter another CTA owns reads it from Tensor Memory (64 columns
+//      per round trip) and pushes it, with remote shared-memory stores, into the owner's exchange
+//      area (a region of its own, not the ring, so no CTA waits for a peer's main loop to end
+//      before writing); each lane then arrives on the owner's exchange barrier (release, cluster
+//      scope);
+//   2. an epilogue warp whose quarter this CTA owns waits on its exchange barrier (acquire,
+//      cluster scope), then sums its own accumulator rows with the kS - 1 pushed copies in the
+//      fixed order 0..kS-1 (the result does not depend on which CTA finished first), rounds once
+//      to the output type and stores;
+//   3. cluster barrier (no CTA leaves while a peer may still write into it).
+// Pushing (posted stores) instead of pulling (remote loads, one latency per round trip) keeps the
+// distributed-shared-memory traffic off the critical path of the owner.
 // One cluster per tile, not persistent: a product of T tiles launches T * kS CTAs.
 #pragma once
 
@@ -23,37 +28,50 @@ namespace dtc {
 
 namespace gsk {
 constexpr int kBM = 128;
-constexpr int kBK = 64;
 constexpr int kThreads = 192;
-constexpr int kTmemCols = 256;
 constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
 
-template <int kBN, int kStages>
+// Ring depth: as many stages as fit beside the exchange area, at most 6.
+constexpr int stages_for(int bn, int bk, int s) {
+    const int room = 227 * 1024 - 256 - 1024 - (s - 1) * (kBM / s) * (bn * 4 + 16);
+    const int n = room / (kBM * bk * 2 + bn * bk * 2);
+    return n < 6 ? n : 6;
+}
+
+// K-blocks of 64 (one 128-byte swizzle row, one 2-D box per operand) or 128 (two rows; for A and
+// for B in NT one 3-D box {64, rows, 2}).
+template <int kBN, int kBK, int kStages, int kS>
 struct Cfg {
     static constexpr int kAStage = kBM * kBK * 2;
     static constexpr int kBStage = kBN * kBK * 2;
     static constexpr int kStageBytes = kAStage + kBStage;
     static constexpr int kRing = kStages * kStageBytes;
-    static constexpr int kXPitch = kBN * 4 + 16;  // fp32 row + 16 bytes: conflict-free v4 stores
-    static constexpr int kXBytes = kBM * kXPitch;
-    static constexpr int kSmemBytes = kRing + 1024;
-    static_assert(kXBytes <= kRing, "the partial-sum copy must fit over the ring");
+    static constexpr int kXPitch = kBN * 4 + 16;         // fp32 row + 16 bytes: conflict-free v4
+    static constexpr int kBandRows = kBM / kS;           // rows of the tile one CTA owns
+    static constexpr int kXRows = (kS - 1) * kBandRows;  // one band from each peer
+    static constexpr int kXBytes = kXRows * kXPitch;
+    static constexpr int kSmemBytes = kRing + kXBytes + 1024;
+    static constexpr int kTmemCols = kBN <= 128 ? 128 : 256;
+    static_assert(kBK == 64 || kBK == 128, "K-block of 64 or 128");
+    static_assert(kS == 2 || kS == 4, "K split over 2 or 4 CTAs");
+    static_assert(kBN % 64 == 0 && kBN <= 256, "the accumulator is read 64 columns at a time");
     static_assert(kSmemBytes <= 227 * 1024 - 256, "shared memory budget");
 };
 }  // namespace gsk
 
-template <bool kBF16, bool kNN, int kBN, int kStages, int kS>
+template <bool kBF16, bool kNN, int kBN, int kBK, int kStages, int kS>
 __global__ void __launch_bounds__(gsk::kThreads, 1)
     gemm16_splitk_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB, const Gemm16Args args) {
     using namespace gsk;
-    using C_ = Cfg<kBN, kStages>;
-    static_assert(kS == 2 || kS == 4, "K split over 2 or 4 CTAs");
-    static_assert(kBN % 64 == 0, "the accumulator is read 64 columns at a time");
+    using C_ = Cfg<kBN, kBK, kStages, kS>;
+    constexpr int kChunks = kBK / 64;    // 128-byte K-chunks per stage
+    constexpr int kQPerBand = 4 / kS;    // accumulator quarters per owned band
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[kStages];
     __shared__ __align__(8) uint64_t bar_empty[kStages];
     __shared__ __align__(8) uint64_t bar_tfull;
+    __shared__ __align__(8) uint64_t bar_xchg;
     __shared__ __align__(8) uint64_t bar_drain;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
@@ -61,7 +79,7 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t sA = base;
     const uint32_t sB = base + kStages * C_::kAStage;
-    const uint32_t sX = base;  // partial-sum copy, over the ring after the main loop
+    const uint32_t sX = base + C_::kRing;  // exchange area: peers' partial sums of owned rows
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
@@ -78,6 +96,8 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
             mbar_init(smem_u32(&bar_empty[s]), 1);
         }
         mbar_init(smem_u32(&bar_tfull), 1);
+        // every lane of each peer warp whose quarter this CTA owns arrives once
+        mbar_init(smem_u32(&bar_xchg), (kS - 1) * kQPerBand * 32);
         mbar_init(smem_u32(&bar_drain), 1);
         abort_flag = 0;
         fence_barrier_init();
@@ -88,11 +108,12 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
         tma_prefetch_desc(&tmB);
     }
     if (warp == 1) {
-        tmem_alloc<1>(smem_u32(&tmem_slot), kTmemCols);
+        tmem_alloc<1>(smem_u32(&tmem_slot), C_::kTmemCols);
         tmem_relinquish<1>();
     }
     tc_fence_before_sync();
     __syncthreads();
+    cluster_sync();  // every CTA's exchange barrier exists before a peer arrives on it
     tc_fence_after_sync();
     const uint32_t tmem_base = tmem_slot;
 
@@ -111,9 +132,15 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
                 if (args.fault == 1 && it == 0) continue;  // test hook: stage never filled
                 const uint32_t full = smem_u32(&bar_full[s]);
                 mbar_arrive_expect_tx(full, C_::kStageBytes);
-                tma_load_2d(sA + s * C_::kAStage, &tmA, full, kb * kBK, mt * kBM);
+                if constexpr (kChunks == 2)
+                    tma_load_3d(sA + s * C_::kAStage, &tmA, full, 0, mt * kBM, kb * 2);
+                else
+                    tma_load_2d(sA + s * C_::kAStage, &tmA, full, kb * kBK, mt * kBM);
                 if constexpr (!kNN) {
-                    tma_load_2d(sB + s * C_::kBStage, &tmB, full, kb * kBK, nt * kBN);
+                    if constexpr (kChunks == 2)
+                        tma_load_3d(sB + s * C_::kBStage, &tmB, full, 0, nt * kBN, kb * 2);
+                    else
+                        tma_load_2d(sB + s * C_::kBStage, &tmB, full, kb * kBK, nt * kBN);
                 } else {
 #pragma unroll
                     for (int j = 0; j < kBN / 64; ++j)
@@ -146,9 +173,13 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
                 const uint32_t a0 = sA + s * C_::kAStage, b0 = sB + s * C_::kBStage;
 #pragma unroll
                 for (int kk = 0; kk < kBK / 16; ++kk) {
-                    const uint64_t adesc = smem_desc_sw128(a0 + kk * 32, 16, 1024);
-                    const uint64_t bdesc = kNN ? smem_desc_sw128(b0 + kk * 16 * 128, 64 * kBK * 2, 1024)
-                                               : smem_desc_sw128(b0 + kk * 32, 16, 1024);
+                    // K-chunk kk/4 of the stage, 32-byte step kk%4 inside its swizzle row
+                    const uint32_t koff = (kk % 4) * 32;
+                    const uint64_t adesc =
+                        smem_desc_sw128(a0 + (kk / 4) * (kBM * 128) + koff, 16, 1024);
+                    const uint64_t bdesc =
+                        kNN ? smem_desc_sw128(b0 + kk * 16 * 128, 64 * kBK * 2, 1024)
+                            : smem_desc_sw128(b0 + (kk / 4) * (kBN * 128) + koff, 16, 1024);
                     mma_f16_cta1(tmem_base, adesc, bdesc, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
                 }
                 issued = true;
@@ -161,95 +192,111 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
                 wait_drain(smem_u32(&bar_drain), 0, kDrainNs);
             }
         }
-    }
-    if (warp >= 2) {
-        // -------------------- epilogue part 1: accumulator -> own shared memory --------------
-        const int q = warp & 3;
-        const int row = q * 32 + lane;
+    } else {
+        // ------------------------------ epilogue (warps 2..5) ------------------------------
+        const int q = warp & 3;  // Tensor Memory lane quarter this warp may access
+        const uint32_t owner = (uint32_t)(q / kQPerBand);
+        const int qb = q % kQPerBand;  // quarter within the owner's band
+        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16);
+        const bool empty_slice = kb1 <= kb0;  // no K-blocks: this CTA's share is zero
         int ok = 1;
         if (lane == 0)
             ok = wait_bounded(smem_u32(&bar_tfull), 0, abort, args.timeout_ns, &g_dtc_status, 24);
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (ok) {
-            tc_fence_after_sync();
-            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16);
-            const uint32_t xrow = sX + row * C_::kXPitch;
-            const bool empty_slice = kb1 <= kb0;  // no K-blocks: this CTA's share is zero
+        if (ok) tc_fence_after_sync();
+        if (owner != rank) {
+            // push this quarter into the owner's exchange area, slot of source rank `rank`
+            const uint32_t slot = rank < owner ? rank : rank - 1;
+            const uint32_t xrow = sX + (slot * C_::kBandRows + qb * 32 + lane) * C_::kXPitch;
+            const uint32_t dst = map_to_cta(xrow, owner);
+            if (ok) {
 #pragma unroll 1
-            for (int c = 0; c < kBN / 64; ++c) {
-                uint32_t v[64];
-                tmem_load_64cols(taddr + c * 64, v);
+                for (int c = 0; c < kBN / 64; ++c) {
+                    uint32_t v[64];
+                    tmem_load_64cols(taddr + c * 64, v);
 #pragma unroll
-                for (int g = 0; g < 16; ++g) {
-                    const uint32_t a = xrow + (c * 64 + g * 4) * 4;
-                    if (empty_slice)
-                        st_shared_u4(a, 0u, 0u, 0u, 0u);
-                    else
-                        st_shared_u4(a, v[g * 4 + 0], v[g * 4 + 1], v[g * 4 + 2], v[g * 4 + 3]);
+                    for (int g = 0; g < 16; ++g) {
+                        const uint32_t a = dst + (c * 64 + g * 4) * 4;
+                        if (empty_slice)
+                            st_shared_cluster_u4(a, 0u, 0u, 0u, 0u);
+                        else
+                            st_shared_cluster_u4(a, v[g * 4 + 0], v[g * 4 + 1], v[g * 4 + 2],
+                                                 v[g * 4 + 3]);
+                    }
+                }
+            }
+            // arrive even after a timeout, so the owner does not wait for the full limit
+            mbar_arrive_cluster(map_to_cta(smem_u32(&bar_xchg), owner));
+        } else {
+            int xok = 1;
+            if (lane == 0)
+                xok = wait_bounded<true>(smem_u32(&bar_xchg), 0, abort, args.timeout_ns,
+                                         &g_dtc_status, 25);
+            xok = __shfl_sync(0xffffffffu, xok, 0);
+            // the phase has completed: every lane takes its own cluster-scope acquire of it
+            if (xok) (void)mbar_try_wait_cluster(smem_u32(&bar_xchg), 0);
+            const int64_t grow = (int64_t)mt * kBM + q * 32 + lane;
+            if (ok && xok) {
+                uint16_t* crow = reinterpret_cast<uint16_t*>(args.C) + grow * args.N;
+#pragma unroll 1
+                for (int c = 0; c < kBN / 64; ++c) {
+                    uint32_t v[64];
+                    tmem_load_64cols(taddr + c * 64, v);
+                    if (grow >= args.M) continue;  // all lanes took part in the Tensor Memory load
+                    float acc[64];
+                    // sum over source ranks 0..kS-1 in that order (own rows from Tensor Memory)
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+#pragma unroll
+                    for (int src = 0; src < kS; ++src) {
+                        if (src == (int)rank) {
+#pragma unroll
+                            for (int i = 0; i < 64; ++i)
+                                acc[i] += empty_slice ? 0.0f : __uint_as_float(v[i]);
+                        } else {
+                            const int slot = src < (int)rank ? src : src - 1;
+                            const uint32_t xrow = sX + (slot * C_::kBandRows + qb * 32 + lane) *
+                                                           C_::kXPitch + c * 256;
+#pragma unroll
+                            for (int g = 0; g < 16; ++g) {
+                                const float4 p = ld_shared_f4(xrow + g * 16);
+                                acc[g * 4 + 0] += p.x;
+                                acc[g * 4 + 1] += p.y;
+                                acc[g * 4 + 2] += p.z;
+                                acc[g * 4 + 3] += p.w;
+                            }
+                        }
+                    }
+                    const int col0 = nt * kBN + c * 64;
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        const int col = col0 + g * 8;
+                        if (col < args.N) {
+                            uint4 w;
+                            w.x = pack2<kBF16>(__float_as_uint(acc[g * 8 + 0]),
+                                               __float_as_uint(acc[g * 8 + 1]));
+                            w.y = pack2<kBF16>(__float_as_uint(acc[g * 8 + 2]),
+                                               __float_as_uint(acc[g * 8 + 3]));
+                            w.z = pack2<kBF16>(__float_as_uint(acc[g * 8 + 4]),
+                                               __float_as_uint(acc[g * 8 + 5]));
+                            w.w = pack2<kBF16>(__float_as_uint(acc[g * 8 + 6]),
+                                               __float_as_uint(acc[g * 8 + 7]));
+                            *reinterpret_cast<uint4*>(crow + col) = w;
+                        }
+                    }
                 }
             }
         }
     }
 
-    // -------------------- epilogue part 2: reduce the band of rows this CTA owns ------------
+    // ------------------------------ teardown ------------------------------
     tc_fence_before_sync();
     __syncthreads();
-    cluster_sync();  // every CTA's partial sums are in its shared memory
-    {
-        constexpr int kRows = kBM / kS;   // rows of the tile this CTA reduces
-        constexpr int kGroups = kBN / 4;  // 4-column groups per row
-        constexpr int kItems = kRows * kGroups;
-        constexpr int kUnroll = 4;        // column groups per thread per round
-        uint32_t peer[kS];
-#pragma unroll
-        for (int s = 0; s < kS; ++s) peer[s] = map_to_cta(sX, (uint32_t)s);
-        for (int i0 = threadIdx.x; i0 < kItems; i0 += kThreads * kUnroll) {
-            float4 acc[kUnroll];
-            uint32_t off[kUnroll];
-            bool live[kUnroll];
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int i = i0 + u * kThreads;
-                live[u] = i < kItems;
-                const int r = (int)rank * kRows + (live[u] ? i / kGroups : 0);
-                const int g = live[u] ? i % kGroups : 0;
-                off[u] = r * C_::kXPitch + g * 16;
-                acc[u] = live[u] ? ld_shared_cluster_f4(peer[0] + off[u]) : make_float4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int s = 1; s < kS; ++s) {
-                float4 v[kUnroll];
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u)
-                    v[u] = live[u] ? ld_shared_cluster_f4(peer[s] + off[u]) : make_float4(0, 0, 0, 0);
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    acc[u].x += v[u].x;
-                    acc[u].y += v[u].y;
-                    acc[u].z += v[u].z;
-                    acc[u].w += v[u].w;
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int i = i0 + u * kThreads;
-                if (!live[u]) continue;
-                const int64_t grow = (int64_t)mt * kBM + (int64_t)rank * kRows + i / kGroups;
-                const int gcol = nt * kBN + (i % kGroups) * 4;
-                if (grow >= args.M || gcol >= args.N) continue;
-                uint2 out;
-                out.x = pack2<kBF16>(__float_as_uint(acc[u].x), __float_as_uint(acc[u].y));
-                out.y = pack2<kBF16>(__float_as_uint(acc[u].z), __float_as_uint(acc[u].w));
-                *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(args.C) + grow * args.N +
-                                          gcol) = out;
-            }
-        }
-    }
-    cluster_sync();  // peers are done reading this CTA's copy
+    cluster_sync();  // no CTA leaves while a peer may still write into its exchange area
     if (warp == 1) {
         __syncwarp();
         tc_fence_after_sync();
-        tmem_dealloc<1>(tmem_base, kTmemCols);
+        tmem_dealloc<1>(tmem_base, C_::kTmemCols);
     }
 }
 

@@ -128,6 +128,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with cluster-scope acquire: for barriers that peers of the cluster arrive on after
+// writing into this CTA's shared memory (their arrivals release at cluster scope).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Device status word: the first wait that gives up records where; the host reads and clears it.
 // Codes: 0x100 | site.
 #define DTC_STATUS_TIMEOUT 0x100
@@ -135,12 +149,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Bounded wait for the phase with `parity` of barrier `bar`. Gives up (returns false) if
 // `*abort` becomes non-zero, or after `timeout_ns` of waiting, in which case it sets `*abort`
 // and records `site` in `*status` (first writer wins).
+// With kCluster, the wait acquires at cluster scope (see mbar_try_wait_cluster).
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
                                              uint64_t timeout_ns, int* status, int site) {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto try_wait = [&]() {
+        return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    };
+    if (try_wait()) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (try_wait()) return true;
         if (*abort) return false;
         if (globaltimer_ns() - t0 > timeout_ns) {
             *abort = 1;

@@ -61,9 +61,11 @@ typedef enum {
     GEMM_VARIANT_2CTA = 2,   /* persistent 256 x 256 or 256 x 224 tiles on a CTA pair
                                 (cluster 2x1, tcgen05 cta_group::2); for MXFP8 (256 x 224,
                                 K % 128 == 0) an option that is never chosen automatically */
-    GEMM_VARIANT_SPLITK = 3  /* 128 x 256 tiles, K split over a cluster of 2 or 4 CTAs that
-                                reduce their partial sums in shared memory (few-tile products,
-                                such as the skinny memory-bound M = 128 case) */
+    GEMM_VARIANT_SPLITK = 3  /* 128 x 128 or 128 x 256 tiles, K split over a cluster of 2 or 4
+                                CTAs; each CTA pushes the partial sums of the rows another CTA
+                                owns into that CTA's shared memory, and the owner reduces and
+                                stores them (few-tile products, such as the skinny memory-bound
+                                M = 128 case) */
 } gemm_variant;
 
 typedef struct {
@@ -73,10 +75,12 @@ typedef struct {
     int fault_inject;     /* test hook, 0 in normal use. 1 = the load producer skips its first
                              stage, so the consumer's bounded wait runs out and the call reports
                              GEMM_ERR_TIMEOUT through gemm_stream_status. */
-    int tile_n;           /* force the N-tile (256 or 224; 224 for NT only); 0 = choose */
+    int tile_n;           /* force the N-tile: 256, 224 (NT only; not SPLITK) or 128 (SPLITK
+                             only); 0 = choose */
     int cluster_m;        /* 1CTA only: CTAs per cluster along M sharing B by multicast (1 or
                              2); 0 = choose */
-    int tile_k;           /* 1CTA only: K-elements per pipeline stage (64 or 32); 0 = choose */
+    int tile_k;           /* K-elements per pipeline stage: 64 or 32 (1CTA), 64 or 128 (2CTA;
+                             SPLITK with 128-wide tiles); 128 needs K % 64 == 0; 0 = choose */
 } gemm_options;
 
 /*

@@ -104,20 +104,26 @@ def test_one_cta_configurations_full_parity(M, N, K, layout, tile_n, cluster_m, 
                cluster_m=cluster_m, tile_k=tile_k)
 
 
+@pytest.mark.parametrize("tile_n,tile_k", [(128, 0), (128, 64), (256, 0)])
 @pytest.mark.parametrize("split_k", [2, 4])
 @pytest.mark.parametrize("layout", ["NT", "NN"])
 @pytest.mark.parametrize("M,N,K", [(128, 2048, 4096), (300, 520, 1000), (64, 264, 64),
-                                   (129, 256, 200)])
-def test_split_k_full_parity(M, N, K, layout, split_k):
-    # K split over a cluster of CTAs that reduce in shared memory; K = 64 is one K-block, so all
-    # CTAs but one have an empty K-range and must contribute zeros; 300 x 520 and 129 x 256 leave
-    # partial tiles in M and N
+                                   (129, 256, 200), (256, 392, 192)])
+def test_split_k_full_parity(M, N, K, layout, split_k, tile_n, tile_k):
+    # K split over a cluster of CTAs that push their partial sums into the owning CTA's shared
+    # memory; K = 64 is one K-block, so all CTAs but one have an empty K-range and must contribute
+    # zeros; 300 x 520 and 129 x 256 leave partial tiles in M and N; K = 192 ends in a half-filled
+    # 128-deep stage; K = 1000 and 200 take 64-deep stages (K % 64 != 0)
     import dense_tensor_core_gb300 as dtc
 
-    p = dtc.gemm_plan("bf16", M, N, K, layout, variant=3, split_k=split_k)
-    assert p["variant"] == 3 and p["split_k"] == split_k and p["cluster"] == split_k
-    full_check("bf16", layout, M, N, K, seed=M + K, variant=3, split_k=split_k)
-    full_check("f16", layout, M, N, K, seed=M + K + 1, variant=3, split_k=split_k)
+    p = dtc.gemm_plan("bf16", M, N, K, layout, variant=3, split_k=split_k, tile_n=tile_n,
+                      tile_k=tile_k)
+    want_k = tile_k or (128 if tile_n == 128 and K % 64 == 0 else 64)
+    assert (p["variant"], p["split_k"], p["cluster"]) == (3, split_k, split_k)
+    assert (p["tile_n"], p["tile_k"]) == (tile_n, want_k)
+    kw = dict(variant=3, split_k=split_k, tile_n=tile_n, tile_k=tile_k)
+    full_check("bf16", layout, M, N, K, seed=M + K, **kw)
+    full_check("f16", layout, M, N, K, seed=M + K + 1, **kw)
 
 
 def test_automatic_choice_follows_the_cost_model():
@@ -131,8 +137,12 @@ def test_automatic_choice_follows_the_cost_model():
     assert (p["variant"], p["tile_m"], p["tile_n"], p["tile_k"]) == (2, 256, 256, 128)
     p = dtc.gemm_plan("bf16", 4096, 4096, 8200, "NT")  # K % 64 != 0: 64-deep stages only
     assert p["tile_k"] == 64
-    p = dtc.gemm_plan("bf16", 128, 8192, 8192, "NT")  # 32 tiles: K split over clusters of 4
-    assert (p["variant"], p["split_k"], p["ctas"]) == (3, 4, 128)
+    p = dtc.gemm_plan("bf16", 128, 8192, 8192, "NT")  # 64 tiles of 128x128, K split in 2
+    assert (p["variant"], p["split_k"], p["tile_n"], p["tile_k"], p["ctas"]) == (3, 2, 128, 128, 128)
+    p = dtc.gemm_plan("bf16", 128, 2048, 8192, "NT")  # 16 tiles: K split in 4
+    assert (p["variant"], p["split_k"], p["tile_n"], p["ctas"]) == (3, 4, 128, 64)
+    p = dtc.gemm_plan("f16", 1024, 1024, 1000, "NN")  # K % 64 != 0: 64-deep stages
+    assert (p["variant"], p["split_k"], p["tile_n"], p["tile_k"]) == (3, 2, 128, 64)
 
 
 @pytest.mark.parametrize("tile_k", [64, 128])
