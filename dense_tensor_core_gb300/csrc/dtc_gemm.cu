@@ -315,7 +315,7 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
         // wave, each CTA keeping at least 4 K-blocks of 64; on a tie the smaller split (less to
         // reduce), then the narrower tile (a smaller exchange).
         struct Cand { int bn, s; };
-        const Cand cands[4] = {{128, 2}, {128, 4}, {256, 2}, {256, 4}};
+        const Cand cands[3] = {{128, 2}, {128, 4}, {256, 2}};
         int64_t best_ctas = 0;
         for (const Cand& c : cands) {
             if (want_n && c.bn != want_n) continue;
@@ -334,6 +334,8 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
         if (dtype == 2) return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 product has no split-K kernel");
         if (split_n && split_n != 256 && split_n != 128)
             return fail(GEMM_ERR_UNSUPPORTED, "the split-K kernel uses 128- or 256-wide tiles");
+        if (split_n == 256 && split == 4)
+            return fail(GEMM_ERR_UNSUPPORTED, "256-wide split-K tiles take a split of 2");
         const int bk_want = o ? o->tile_k : 0;
         if (bk_want && bk_want != 64 && bk_want != 128)
             return fail(GEMM_ERR_INVALID_ARG, "tile_k %d is not 64 or 128 for the split-K kernel", bk_want);
@@ -560,8 +562,7 @@ int launch_splitk_any(const Plan& p, const void* A, const void* B, void* C, int 
         return p.split_k == 2 ? launch_gemm16_splitk<kBF16, kNN, 128, 64, 2>(A, B, C, m, n, k, o, dev, p, stream)
                               : launch_gemm16_splitk<kBF16, kNN, 128, 64, 4>(A, B, C, m, n, k, o, dev, p, stream);
     }
-    return p.split_k == 2 ? launch_gemm16_splitk<kBF16, kNN, 256, 64, 2>(A, B, C, m, n, k, o, dev, p, stream)
-                          : launch_gemm16_splitk<kBF16, kNN, 256, 64, 4>(A, B, C, m, n, k, o, dev, p, stream);
+    return launch_gemm16_splitk<kBF16, kNN, 256, 64, 2>(A, B, C, m, n, k, o, dev, p, stream);
 }
 
 dtc::GemmMxArgs mx_args(const void* sfA, const void* sfB, void* C, int M, int N, int K, int tile_m,

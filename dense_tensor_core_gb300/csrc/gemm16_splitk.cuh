@@ -7,18 +7,25 @@
 // computes one tile: CTA r accumulates the r-th of kS contiguous K-ranges. The partial sums are
 // reduced on chip, without a global workspace. CTA r owns rows [r*128/kS, (r+1)*128/kS) of the
 // tile, i.e. 4/kS of the four 32-lane quarters of the accumulator:
-//   1. an epilogue warp whose quarter another CTA owns reads it from Tensor Memory (64 columns
-//      per round trip) and pushes it, with remote shared-memory stores, into the owner's exchange
-//      area (a region of its own, not the ring, so no CTA waits for a peer's main loop to end
-//      before writing); each lane then arrives on the owner's exchange barrier (release, cluster
-//      scope);
-//   2. an epilogue warp whose quarter this CTA owns waits on its exchange barrier (acquire,
-//      cluster scope), then sums its own accumulator rows with the kS - 1 pushed copies in the
+//   1. an epilogue warp whose quarter another CTA owns reads it from Tensor Memory, 64 columns
+//      per round trip, into a staging copy in its own ring (idle once the last MMA has
+//      completed), laid out as the owner's exchange area is, and hands each 64-column piece to
+//      the copy engine as soon as it is staged: one bulk shared-memory copy into the owner's
+//      exchange area, counted in bytes on the owner's barrier for that piece (the owner armed it
+//      with the bytes it expects);
+//   2. an epilogue warp whose quarter this CTA owns takes the pieces in order: once a piece's
+//      barrier completes it sums its own accumulator columns with the kS - 1 copies in the
 //      fixed order 0..kS-1 (the result does not depend on which CTA finished first), rounds once
-//      to the output type and stores;
-//   3. cluster barrier (no CTA leaves while a peer may still write into it).
-// Pushing (posted stores) instead of pulling (remote loads, one latency per round trip) keeps the
-// distributed-shared-memory traffic off the critical path of the owner.
+//      to the output type and stores, while later pieces are still in flight;
+//   3. cluster barrier (no CTA leaves while a copy into it, or out of it, may be in flight).
+// The exchange area is a region of its own, not the ring, so no CTA waits for a peer's main loop
+// to end before copying into it. The exchange is laid out piece-major ([piece][row][64 floats],
+// the 16-byte chunk j of row r stored at chunk position j ^ (r % 8), so that a warp's lanes,
+// one row each, hit distinct banks) so that each copy is one contiguous range; whole-piece bulk copies move full 32-byte
+// sectors over the cluster network, where per-lane 16-byte remote stores to 32 different rows
+// would move half-filled ones. The start-up cluster barrier is split: every thread arrives after
+// the set-up, and a thread waits only before its first copy into a peer (or at the end), so the
+// main loop does not wait for the other CTAs to start.
 // One cluster per tile, not persistent: a product of T tiles launches T * kS CTAs.
 #pragma once
 
@@ -33,7 +40,7 @@ constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
 
 // Ring depth: as many stages as fit beside the exchange area, at most 6.
 constexpr int stages_for(int bn, int bk, int s) {
-    const int room = 227 * 1024 - 256 - 1024 - (s - 1) * (kBM / s) * (bn * 4 + 16);
+    const int room = 227 * 1024 - 256 - 1024 - (s - 1) * (kBM / s) * (bn * 4);
     const int n = room / (kBM * bk * 2 + bn * bk * 2);
     return n < 6 ? n : 6;
 }
@@ -46,12 +53,17 @@ struct Cfg {
     static constexpr int kBStage = kBN * kBK * 2;
     static constexpr int kStageBytes = kAStage + kBStage;
     static constexpr int kRing = kStages * kStageBytes;
-    static constexpr int kXPitch = kBN * 4 + 16;         // fp32 row + 16 bytes: conflict-free v4
+    static constexpr int kPieces = kBN / 64;             // 64-column pieces of a row
+    static constexpr int kXPitch = 64 * 4;               // fp32 piece row (16-byte chunks swizzled)
     static constexpr int kBandRows = kBM / kS;           // rows of the tile one CTA owns
-    static constexpr int kXRows = (kS - 1) * kBandRows;  // one band from each peer
-    static constexpr int kXBytes = kXRows * kXPitch;
+    static constexpr int kXSlot = kPieces * kBandRows * kXPitch;  // one peer's band
+    static constexpr int kXBytes = (kS - 1) * kXSlot;             // one band from each peer
+    static constexpr int kXPieceBytes = (kS - 1) * kBandRows * kXPitch;  // expected per piece
     static constexpr int kSmemBytes = kRing + kXBytes + 1024;
     static constexpr int kTmemCols = kBN <= 128 ? 128 : 256;
+    static constexpr int kQPieceBytes = 32 * kXPitch;                   // one quarter's piece
+    static constexpr int kStaging = (4 - 4 / kS) * kPieces * kQPieceBytes;  // all pushed quarters
+    static_assert(kStaging <= kRing, "the staging copies must fit over the ring");
     static_assert(kBK == 64 || kBK == 128, "K-block of 64 or 128");
     static_assert(kS == 2 || kS == 4, "K split over 2 or 4 CTAs");
     static_assert(kBN % 64 == 0 && kBN <= 256, "the accumulator is read 64 columns at a time");
@@ -71,7 +83,7 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
     __shared__ __align__(8) uint64_t bar_full[kStages];
     __shared__ __align__(8) uint64_t bar_empty[kStages];
     __shared__ __align__(8) uint64_t bar_tfull;
-    __shared__ __align__(8) uint64_t bar_xchg;
+    __shared__ __align__(8) uint64_t bar_xchg[C_::kPieces];
     __shared__ __align__(8) uint64_t bar_drain;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
@@ -96,8 +108,11 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
             mbar_init(smem_u32(&bar_empty[s]), 1);
         }
         mbar_init(smem_u32(&bar_tfull), 1);
-        // every lane of each peer warp whose quarter this CTA owns arrives once
-        mbar_init(smem_u32(&bar_xchg), (kS - 1) * kQPerBand * 32);
+        // each armed once with every byte the peers will copy into its piece
+        for (int c = 0; c < C_::kPieces; ++c) {
+            mbar_init(smem_u32(&bar_xchg[c]), 1);
+            mbar_arrive_expect_tx(smem_u32(&bar_xchg[c]), C_::kXPieceBytes);
+        }
         mbar_init(smem_u32(&bar_drain), 1);
         abort_flag = 0;
         fence_barrier_init();
@@ -113,7 +128,8 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
     }
     tc_fence_before_sync();
     __syncthreads();
-    cluster_sync();  // every CTA's exchange barrier exists before a peer arrives on it
+    cluster_arrive();  // this CTA's exchange barriers exist (a peer waits before copying in)
+    bool cluster_waited = false;
     tc_fence_after_sync();
     const uint32_t tmem_base = tmem_slot;
 
@@ -205,84 +221,94 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (ok) tc_fence_after_sync();
         if (owner != rank) {
-            // push this quarter into the owner's exchange area, slot of source rank `rank`
+            // stage this quarter piece by piece in the ring and copy each piece into the owner's
+            // exchange area, in the slot of source rank `rank`
             const uint32_t slot = rank < owner ? rank : rank - 1;
-            const uint32_t xrow = sX + (slot * C_::kBandRows + qb * 32 + lane) * C_::kXPitch;
-            const uint32_t dst = map_to_cta(xrow, owner);
+            const uint32_t first_own = rank * kQPerBand;
+            const uint32_t pidx = (uint32_t)q < first_own ? (uint32_t)q : (uint32_t)q - kQPerBand;
+            const uint32_t stage = sA + pidx * (C_::kPieces * C_::kQPieceBytes);
+            cluster_wait();  // the owner's barriers exist
+            cluster_waited = true;
             if (ok) {
 #pragma unroll 1
-                for (int c = 0; c < kBN / 64; ++c) {
+                for (int c = 0; c < C_::kPieces; ++c) {
                     uint32_t v[64];
                     tmem_load_64cols(taddr + c * 64, v);
+                    const uint32_t spiece = stage + c * C_::kQPieceBytes;
+                    const uint32_t srow = spiece + lane * C_::kXPitch;
 #pragma unroll
                     for (int g = 0; g < 16; ++g) {
-                        const uint32_t a = dst + (c * 64 + g * 4) * 4;
+                        const uint32_t a = srow + ((g ^ (lane & 7)) << 4);
                         if (empty_slice)
-                            st_shared_cluster_u4(a, 0u, 0u, 0u, 0u);
+                            st_shared_u4(a, 0u, 0u, 0u, 0u);
                         else
-                            st_shared_cluster_u4(a, v[g * 4 + 0], v[g * 4 + 1], v[g * 4 + 2],
-                                                 v[g * 4 + 3]);
+                            st_shared_u4(a, v[g * 4 + 0], v[g * 4 + 1], v[g * 4 + 2], v[g * 4 + 3]);
+                    }
+                    fence_proxy_async_smem();  // the staging writes, before the copy engine reads
+                    __syncwarp();
+                    if (lane == 0) {
+                        const uint32_t dst = sX + slot * C_::kXSlot +
+                                             (c * C_::kBandRows + qb * 32) * C_::kXPitch;
+                        bulk_copy_smem_to_cta(map_to_cta(dst, owner), spiece, C_::kQPieceBytes,
+                                              map_to_cta(smem_u32(&bar_xchg[c]), owner));
                     }
                 }
             }
-            // arrive even after a timeout, so the owner does not wait for the full limit
-            mbar_arrive_cluster(map_to_cta(smem_u32(&bar_xchg), owner));
-        } else {
-            int xok = 1;
-            if (lane == 0)
-                xok = wait_bounded<true>(smem_u32(&bar_xchg), 0, abort, args.timeout_ns,
-                                         &g_dtc_status, 25);
-            xok = __shfl_sync(0xffffffffu, xok, 0);
-            // the phase has completed: every lane takes its own cluster-scope acquire of it
-            if (xok) (void)mbar_try_wait_cluster(smem_u32(&bar_xchg), 0);
+        } else if (ok) {
             const int64_t grow = (int64_t)mt * kBM + q * 32 + lane;
-            if (ok && xok) {
-                uint16_t* crow = reinterpret_cast<uint16_t*>(args.C) + grow * args.N;
+            uint16_t* crow = reinterpret_cast<uint16_t*>(args.C) + grow * args.N;
 #pragma unroll 1
-                for (int c = 0; c < kBN / 64; ++c) {
-                    uint32_t v[64];
-                    tmem_load_64cols(taddr + c * 64, v);
-                    if (grow >= args.M) continue;  // all lanes took part in the Tensor Memory load
-                    float acc[64];
-                    // sum over source ranks 0..kS-1 in that order (own rows from Tensor Memory)
+            for (int c = 0; c < C_::kPieces; ++c) {
+                uint32_t v[64];
+                tmem_load_64cols(taddr + c * 64, v);  // own partial sums, ready since tfull
+                int xok = 1;
+                if (lane == 0)
+                    xok = wait_bounded<true>(smem_u32(&bar_xchg[c]), 0, abort, args.timeout_ns,
+                                             &g_dtc_status, 25);
+                xok = __shfl_sync(0xffffffffu, xok, 0);
+                if (!xok) break;
+                // the phase has completed: every lane takes its own acquire of it
+                (void)mbar_try_wait_cluster(smem_u32(&bar_xchg[c]), 0);
+                if (grow >= args.M) continue;  // all lanes took part in the Tensor Memory load
+                float acc[64];
+                // sum over source ranks 0..kS-1 in that order (own rows from Tensor Memory)
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+                for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
 #pragma unroll
-                    for (int src = 0; src < kS; ++src) {
-                        if (src == (int)rank) {
+                for (int src = 0; src < kS; ++src) {
+                    if (src == (int)rank) {
 #pragma unroll
-                            for (int i = 0; i < 64; ++i)
-                                acc[i] += empty_slice ? 0.0f : __uint_as_float(v[i]);
-                        } else {
-                            const int slot = src < (int)rank ? src : src - 1;
-                            const uint32_t xrow = sX + (slot * C_::kBandRows + qb * 32 + lane) *
-                                                           C_::kXPitch + c * 256;
+                        for (int i = 0; i < 64; ++i)
+                            acc[i] += empty_slice ? 0.0f : __uint_as_float(v[i]);
+                    } else {
+                        const int slot = src < (int)rank ? src : src - 1;
+                        const uint32_t xrow = sX + slot * C_::kXSlot +
+                                              (c * C_::kBandRows + qb * 32 + lane) * C_::kXPitch;
 #pragma unroll
-                            for (int g = 0; g < 16; ++g) {
-                                const float4 p = ld_shared_f4(xrow + g * 16);
-                                acc[g * 4 + 0] += p.x;
-                                acc[g * 4 + 1] += p.y;
-                                acc[g * 4 + 2] += p.z;
-                                acc[g * 4 + 3] += p.w;
-                            }
+                        for (int g = 0; g < 16; ++g) {
+                            const float4 p = ld_shared_f4(xrow + ((g ^ (lane & 7)) << 4));
+                            acc[g * 4 + 0] += p.x;
+                            acc[g * 4 + 1] += p.y;
+                            acc[g * 4 + 2] += p.z;
+                            acc[g * 4 + 3] += p.w;
                         }
                     }
-                    const int col0 = nt * kBN + c * 64;
+                }
+                const int col0 = nt * kBN + c * 64;
 #pragma unroll
-                    for (int g = 0; g < 8; ++g) {
-                        const int col = col0 + g * 8;
-                        if (col < args.N) {
-                            uint4 w;
-                            w.x = pack2<kBF16>(__float_as_uint(acc[g * 8 + 0]),
-                                               __float_as_uint(acc[g * 8 + 1]));
-                            w.y = pack2<kBF16>(__float_as_uint(acc[g * 8 + 2]),
-                                               __float_as_uint(acc[g * 8 + 3]));
-                            w.z = pack2<kBF16>(__float_as_uint(acc[g * 8 + 4]),
-                                               __float_as_uint(acc[g * 8 + 5]));
-                            w.w = pack2<kBF16>(__float_as_uint(acc[g * 8 + 6]),
-                                               __float_as_uint(acc[g * 8 + 7]));
-                            *reinterpret_cast<uint4*>(crow + col) = w;
-                        }
+                for (int g = 0; g < 8; ++g) {
+                    const int col = col0 + g * 8;
+                    if (col < args.N) {
+                        uint4 w;
+                        w.x = pack2<kBF16>(__float_as_uint(acc[g * 8 + 0]),
+                                           __float_as_uint(acc[g * 8 + 1]));
+                        w.y = pack2<kBF16>(__float_as_uint(acc[g * 8 + 2]),
+                                           __float_as_uint(acc[g * 8 + 3]));
+                        w.z = pack2<kBF16>(__float_as_uint(acc[g * 8 + 4]),
+                                           __float_as_uint(acc[g * 8 + 5]));
+                        w.w = pack2<kBF16>(__float_as_uint(acc[g * 8 + 6]),
+                                           __float_as_uint(acc[g * 8 + 7]));
+                        *reinterpret_cast<uint4*>(crow + col) = w;
                     }
                 }
             }
@@ -290,9 +316,16 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
     }
 
     // ------------------------------ teardown ------------------------------
+    if (!cluster_waited) cluster_wait();  // complete the start-up cluster barrier
     tc_fence_before_sync();
     __syncthreads();
-    cluster_sync();  // no CTA leaves while a peer may still write into its exchange area
+    cluster_sync();  // owners have seen every copy land: none is in flight into or out of a CTA
+    if (*abort && threadIdx.x == 0) {
+        // After a timeout an owner may have stopped waiting: give copies still in flight a
+        // fixed, bounded time to land before the CTAs' shared memory is released.
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 1000ull * 1000) __nanosleep(1000);
+    }
     if (warp == 1) {
         __syncwarp();
         tc_fence_after_sync();

@@ -51,6 +51,15 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
+// The two halves of cluster_sync, for work that can run between them (every thread of the
+// cluster must arrive once before any thread's wait returns; a thread waits before arriving again).
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
 // 16-byte load from the shared memory of any CTA of the cluster (a shared::cluster address).
 __device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t cluster_addr) {
     float4 v;
@@ -216,6 +225,17 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from this CTA's shared
+// memory into the shared memory of a CTA of the cluster (`dst` and `bar` are shared::cluster
+// addresses); the copy engine counts the bytes on that CTA's barrier `bar` as they land.
+__device__ __forceinline__ void bulk_copy_smem_to_cta(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                      uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "r"(src), "r"(bytes), "r"(bar)
         : "memory");
 }
 

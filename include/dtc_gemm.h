@@ -61,11 +61,11 @@ typedef enum {
     GEMM_VARIANT_2CTA = 2,   /* persistent 256 x 256 or 256 x 224 tiles on a CTA pair
                                 (cluster 2x1, tcgen05 cta_group::2); for MXFP8 (256 x 224,
                                 K % 128 == 0) an option that is never chosen automatically */
-    GEMM_VARIANT_SPLITK = 3  /* 128 x 128 or 128 x 256 tiles, K split over a cluster of 2 or 4
-                                CTAs; each CTA pushes the partial sums of the rows another CTA
-                                owns into that CTA's shared memory, and the owner reduces and
-                                stores them (few-tile products, such as the skinny memory-bound
-                                M = 128 case) */
+    GEMM_VARIANT_SPLITK = 3  /* 128 x 128 tiles with K split over a cluster of 2 or 4 CTAs, or
+                                128 x 256 tiles split over 2; each CTA copies the partial sums
+                                of the rows another CTA owns into that CTA's shared memory, and
+                                the owner reduces and stores them (few-tile products, such as
+                                the skinny memory-bound M = 128 case) */
 } gemm_variant;
 
 typedef struct {

@@ -110,6 +110,8 @@ def test_one_cta_configurations_full_parity(M, N, K, layout, tile_n, cluster_m, 
 @pytest.mark.parametrize("M,N,K", [(128, 2048, 4096), (300, 520, 1000), (64, 264, 64),
                                    (129, 256, 200), (256, 392, 192)])
 def test_split_k_full_parity(M, N, K, layout, split_k, tile_n, tile_k):
+    if tile_n == 256 and split_k == 4:
+        pytest.skip("256-wide split-K tiles take a split of 2")
     # K split over a cluster of CTAs that push their partial sums into the owning CTA's shared
     # memory; K = 64 is one K-block, so all CTAs but one have an empty K-range and must contribute
     # zeros; 300 x 520 and 129 x 256 leave partial tiles in M and N; K = 192 ends in a half-filled
