@@ -27,7 +27,7 @@ SF_BLOCK = 128  # K-elements per E8M0 scale (granularity 128 along K for both op
 class Workload:
     name: str
     kind: str  # "bf16", "f16" or "mxfp8"
-    layout: str  # "NT" (B is [N,K]) or "NN" (B is [K,N])
+    layout: str  # "NT" (B is [N,K]), "NN" (B is [K,N]); a leading "T" stores A as [K,M]
     M: int
     N: int
     K: int
@@ -73,10 +73,11 @@ def randn16(kind: str, shape, gen: torch.Generator) -> np.ndarray:
 
 
 def make16(kind: str, layout: str, M: int, N: int, K: int, seed: int):
-    """(A [M,K], B [N,K] or [K,N]) as uint16 codes."""
+    """(A, B) as uint16 codes: A [M,K] ([K,M] for layouts TN, TT), B [N,K] (NT, TT) or [K,N]
+    (NN, TN)."""
     g = torch.Generator().manual_seed(seed)
-    A = randn16(kind, (M, K), g)
-    B = randn16(kind, (N, K) if layout == "NT" else (K, N), g)
+    A = randn16(kind, (K, M) if layout[0] == "T" else (M, K), g)
+    B = randn16(kind, (N, K) if layout[1] == "T" else (K, N), g)
     return A, B
 
 

@@ -20,7 +20,7 @@ import numpy as np
 from . import build as _build
 
 BF16, F16 = 0, 1
-NT, NN = 0, 1
+NT, NN, TN, TT = 0, 1, 2, 3
 
 _lib = None
 
@@ -94,7 +94,17 @@ def _dtype_code(dtype):
 
 
 def _layout_code(layout):
-    return {"NT": NT, "NN": NN, NT: NT, NN: NN}[layout]
+    return {"NT": NT, "NN": NN, "TN": TN, "TT": TT, NT: NT, NN: NN, TN: TN, TT: TT}[layout]
+
+
+def a_shape(layout, M, K):
+    """Storage shape of A: [M,K], or [K,M] when the layout's first letter is T."""
+    return (K, M) if layout[0] == "T" else (M, K)
+
+
+def b_shape(layout, N, K):
+    """Storage shape of B: [N,K] when the layout's second letter is T, else [K,N]."""
+    return (N, K) if layout[1] == "T" else (K, N)
 
 
 # --- codecs -----------------------------------------------------------------------------------

@@ -15,6 +15,10 @@
  *     "NN": B is stored [K,N] and Bop[k,n] = B[k,n]
  *           (tilelang (velog), section 1.1 Front-End DSL: B is T.Tensor((K, N)) and
  *            T.gemm(A_shared, B_shared, C_local) with no transpose)
+ *     "TN", "TT": as "NN", "NT", with A stored [K,M] and Aop[m,k] = A[k,m] (the first letter is
+ *           A's transpose flag, the second B's: the trans_A / trans_B arguments of T.gemm in
+ *           TileLang SM100 Support (Preview), "Current Limitations" and "Code Example");
+ *           for "NT"/"NN" Aop[m,k] = A[m,k] with A stored [M,K]
  *
  *   MXFP8 block-scaled (both operands e4m3, one E8M0 scale per row per 128 K-elements,
  *   "1d1d" granularity 128 for A and B:
@@ -52,6 +56,13 @@
 #define DTC_ORACLE_F16 1
 #define DTC_ORACLE_NT 0
 #define DTC_ORACLE_NN 1
+#define DTC_ORACLE_TN 2
+#define DTC_ORACLE_TT 3
+
+/* A stored [K,M] (transposed)? B stored [K,N]? */
+static int a_is_km(int layout) { return layout == DTC_ORACLE_TN || layout == DTC_ORACLE_TT; }
+static int b_is_kn(int layout) { return layout == DTC_ORACLE_NN || layout == DTC_ORACLE_TN; }
+static int layout_ok(int layout) { return layout >= DTC_ORACLE_NT && layout <= DTC_ORACLE_TT; }
 
 /* ------------------------------------------------------------------------------------------ */
 /* Decoders: code -> exact double value                                                        */
@@ -208,7 +219,7 @@ static double dec16(int dtype, uint16_t h) {
     return dtype == DTC_ORACLE_F16 ? dtc_oracle_dec_f16(h) : dtc_oracle_dec_bf16(h);
 }
 
-/* Decode A to [M][K] doubles and Bop to [N][K] doubles (a gather, no arithmetic). */
+/* Decode Aop to [M][K] doubles and Bop to [N][K] doubles (a gather, no arithmetic). */
 static int decode16(int dtype, int layout, const uint16_t* A, const uint16_t* B, int64_t M,
                     int64_t N, int64_t K, double** a_out, double** bt_out) {
     double* a = (double*)malloc(sizeof(double) * (size_t)(M * K > 0 ? M * K : 1));
@@ -218,10 +229,12 @@ static int decode16(int dtype, int layout, const uint16_t* A, const uint16_t* B,
         free(bt);
         return -1;
     }
-    for (int64_t i = 0; i < M * K; ++i) a[i] = dec16(dtype, A[i]);
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k)
+            a[m * K + k] = dec16(dtype, a_is_km(layout) ? A[k * M + m] : A[m * K + k]);
     for (int64_t n = 0; n < N; ++n)
         for (int64_t k = 0; k < K; ++k)
-            bt[n * K + k] = dec16(dtype, layout == DTC_ORACLE_NN ? B[k * N + n] : B[n * K + k]);
+            bt[n * K + k] = dec16(dtype, b_is_kn(layout) ? B[k * N + n] : B[n * K + k]);
     *a_out = a;
     *bt_out = bt;
     return 0;
@@ -232,7 +245,7 @@ int dtc_oracle_gemm16(int dtype, int layout, const uint16_t* A, const uint16_t* 
                       int64_t N, int64_t K, uint16_t* C, double* S, int nthreads) {
     if (M < 0 || N < 0 || K < 0) return -1;
     if (dtype != DTC_ORACLE_BF16 && dtype != DTC_ORACLE_F16) return -1;
-    if (layout != DTC_ORACLE_NT && layout != DTC_ORACLE_NN) return -1;
+    if (!layout_ok(layout)) return -1;
     if (M == 0 || N == 0) return 0;
     double *a, *bt;
     if (decode16(dtype, layout, A, B, M, N, K, &a, &bt) != 0) return -1;
@@ -250,14 +263,15 @@ int dtc_oracle_gemm16_sampled(int dtype, int layout, const uint16_t* A, const ui
                               const int64_t* cols, int64_t count, uint16_t* Cout, double* Sout) {
     if (M < 0 || N < 0 || K < 0 || count < 0) return -1;
     if (dtype != DTC_ORACLE_BF16 && dtype != DTC_ORACLE_F16) return -1;
-    if (layout != DTC_ORACLE_NT && layout != DTC_ORACLE_NN) return -1;
+    if (!layout_ok(layout)) return -1;
     for (int64_t i = 0; i < count; ++i) {
         int64_t m = rows[i], n = cols[i];
         if (m < 0 || m >= M || n < 0 || n >= N) return -1;
         double acc = 0.0;
         for (int64_t k = 0; k < K; ++k) {
-            uint16_t b = layout == DTC_ORACLE_NN ? B[k * N + n] : B[n * K + k];
-            acc += dec16(dtype, A[m * K + k]) * dec16(dtype, b);
+            uint16_t a = a_is_km(layout) ? A[k * M + m] : A[m * K + k];
+            uint16_t b = b_is_kn(layout) ? B[k * N + n] : B[n * K + k];
+            acc += dec16(dtype, a) * dec16(dtype, b);
         }
         if (Sout) Sout[i] = acc;
         if (Cout) Cout[i] = dtype == DTC_ORACLE_F16 ? dtc_oracle_enc_f16(acc) : dtc_oracle_enc_bf16(acc);

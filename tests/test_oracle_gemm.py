@@ -3,7 +3,8 @@ and an independent library routine (torch float64 matmul on torch-decoded operan
 
 The method's definition: C = A . B^T with B stored [N,K] ("NT": TileLang SM100 Support (Preview),
 "Code Example" / "Compilation and Usage") or C = A . B with B stored [K,N] ("NN": tilelang
-(velog), 1.1 Front-End DSL); MXFP8 per the 05 Blackwell TCGEN05 GEMM tutorial, "Advanced"
+(velog), 1.1 Front-End DSL); a leading "T" stores A as [K,M] (trans_A of T.gemm, TileLang SM100
+Support (Preview), "Current Limitations"); MXFP8 per the 05 Blackwell TCGEN05 GEMM tutorial, "Advanced"
 (gemm_blockscaled, K-granularity 128 for both operands).
 """
 import math
@@ -44,6 +45,16 @@ def test_golden_2x2(kind, layout):
     A, B = matrix(g["A"]), matrix(g["B"])
     C = oracle.gemm16(kind, layout, codes_of(A, kind), codes_of(B, kind), 2, 2, 2)
     assert np.array_equal(values_of(C, kind), matrix(g[f"C_{layout}_{kind}"]))
+
+
+@pytest.mark.parametrize("kind", ["bf16", "f16"])
+@pytest.mark.parametrize("layout", ["TN", "TT"])
+def test_golden_transposed_a(kind, layout):
+    g = read_golden("gemm16_2x3_k3_transposed_a.txt")
+    A, B = matrix(g["A"]), matrix(g[f"B_{layout}"])
+    C, S = oracle.gemm16(kind, layout, codes_of(A, kind), codes_of(B, kind), 2, 3, 3, sums=True)
+    assert np.array_equal(S, matrix(g["C"]))
+    assert np.array_equal(values_of(C, kind), matrix(g["C"]))
 
 
 @pytest.mark.parametrize("kind", ["bf16", "f16"])
@@ -88,38 +99,53 @@ def _rand16(kind, shape, seed):
     return workloads.randn16(kind, shape, torch.Generator().manual_seed(seed))
 
 
+def store_a(Aop, layout):
+    """Aop [M,K] in the layout's storage order for A."""
+    return np.ascontiguousarray(Aop.T if layout[0] == "T" else Aop)
+
+
+def store_b(Bop, layout):
+    """Bop [K,N] in the layout's storage order for B ([N,K] when its second letter is T)."""
+    return np.ascontiguousarray(Bop.T if layout[1] == "T" else Bop)
+
+
+def op_b(B, layout):
+    return B.T if layout[1] == "T" else B
+
+
+LAYOUTS = ["NT", "NN", "TN", "TT"]
+
+
 @pytest.mark.parametrize("kind", ["bf16", "f16"])
-@pytest.mark.parametrize("layout", ["NT", "NN"])
+@pytest.mark.parametrize("layout", LAYOUTS)
 def test_identity_gives_B(kind, layout):
     # A = I (M = K): C = Bop exactly (each sum has one nonzero term, already a 16-bit value)
     K, N = 24, 40
     A = codes_of(np.eye(K), kind)
-    B = _rand16(kind, (N, K) if layout == "NT" else (K, N), 11)
+    B = _rand16(kind, oracle.b_shape(layout, N, K), 11)
     C = oracle.gemm16(kind, layout, A, B, K, N, K)
-    Bop = B.T if layout == "NT" else B
-    assert np.array_equal(C, Bop)
+    assert np.array_equal(C, op_b(B, layout))
 
 
 @pytest.mark.parametrize("kind", ["bf16", "f16"])
-@pytest.mark.parametrize("layout", ["NT", "NN"])
+@pytest.mark.parametrize("layout", LAYOUTS)
 def test_permutations_permute_exactly(kind, layout):
-    M, N, K = 16, 12, 16
+    M, N, K = 16, 12, 20  # M != K: a transposed A read as untransposed would not even line up
     rng = np.random.default_rng(5)
-    p = rng.permutation(M)
+    p = rng.permutation(K)[:M]
     P = np.zeros((M, K))
     P[np.arange(M), p] = 1.0  # (P X)[i] = X[p[i]]
-    B = _rand16(kind, (N, K) if layout == "NT" else (K, N), 12)
-    C = oracle.gemm16(kind, layout, codes_of(P, kind), B, M, N, K)
-    Bop = B.T if layout == "NT" else B
-    assert np.array_equal(C, Bop[p, :])
-    # permutation on the other side: Bop = Q with Q[k, n] = 1 iff k = q[n] -> C[:, n] = A[:, q[n]]
+    B = _rand16(kind, oracle.b_shape(layout, N, K), 12)
+    C = oracle.gemm16(kind, layout, codes_of(store_a(P, layout), kind), B, M, N, K)
+    assert np.array_equal(C, op_b(B, layout)[p, :])
+    # permutation on the other side: Bop = Q with Q[k, n] = 1 iff k = q[n] -> C[:, n] = Aop[:, q[n]]
     q = rng.permutation(K)[:N]
     Q = np.zeros((K, N))
     Q[q, np.arange(N)] = 1.0
-    A = _rand16(kind, (M, K), 13)
-    Bst = Q.T if layout == "NT" else Q
-    C2 = oracle.gemm16(kind, layout, A, codes_of(np.ascontiguousarray(Bst), kind), M, N, K)
-    assert np.array_equal(C2, A[:, q])
+    A = _rand16(kind, oracle.a_shape(layout, M, K), 13)
+    Aop = A.T if layout[0] == "T" else A
+    C2 = oracle.gemm16(kind, layout, A, codes_of(store_b(Q, layout), kind), M, N, K)
+    assert np.array_equal(C2, Aop[:, q])
 
 
 @pytest.mark.parametrize("kind", ["bf16", "f16"])
@@ -166,15 +192,16 @@ def test_degenerate_sizes():
 
 # --- an independent library routine --------------------------------------------------------------
 
-@pytest.mark.parametrize("kind,layout", [("bf16", "NT"), ("f16", "NN"), ("bf16", "NN"), ("f16", "NT")])
+@pytest.mark.parametrize("kind,layout", [("bf16", "NT"), ("f16", "NN"), ("bf16", "NN"), ("f16", "NT"),
+                                         ("bf16", "TN"), ("f16", "TT"), ("f16", "TN"), ("bf16", "TT")])
 def test_matches_torch_float64_matmul(kind, layout):
     # ragged sizes (not multiples of any tile)
     M, N, K = 67, 45, 200
     A, B = workloads.make16(kind, layout, M, N, K, 31)
     C, S = oracle.gemm16(kind, layout, A, B, M, N, K, sums=True)
-    At = torch.from_numpy(values_of(A, kind).reshape(M, K))
-    Bt = torch.from_numpy(values_of(B, kind).reshape((N, K) if layout == "NT" else (K, N)))
-    ref = (At @ (Bt.T if layout == "NT" else Bt)).numpy()
+    At = torch.from_numpy(values_of(A, kind).reshape(oracle.a_shape(layout, M, K)))
+    Bt = torch.from_numpy(values_of(B, kind).reshape(oracle.b_shape(layout, N, K)))
+    ref = ((At.T if layout[0] == "T" else At) @ (Bt.T if layout[1] == "T" else Bt)).numpy()
     assert np.allclose(S, ref, rtol=1e-12, atol=1e-12)
     if kind == "f16":
         assert np.array_equal(C, ref.astype(np.float16).view(np.uint16))  # numpy: direct RNE
@@ -188,7 +215,7 @@ def test_matches_torch_float64_matmul(kind, layout):
 
 
 def test_sampled_equals_full():
-    for kind, layout in (("bf16", "NT"), ("f16", "NN")):
+    for kind, layout in (("bf16", "NT"), ("f16", "NN"), ("bf16", "TN"), ("f16", "TT")):
         M, N, K = 33, 29, 130
         A, B = workloads.make16(kind, layout, M, N, K, 41)
         C, S = oracle.gemm16(kind, layout, A, B, M, N, K, sums=True)

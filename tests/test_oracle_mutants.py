@@ -17,8 +17,16 @@ PINS = ["tests/test_oracle_codecs.py", "tests/test_oracle_gemm.py"]
 
 MUTANTS = {
     "nn_operand_read_as_nt": (
-        "bt[n * K + k] = dec16(dtype, layout == DTC_ORACLE_NN ? B[k * N + n] : B[n * K + k]);",
+        "bt[n * K + k] = dec16(dtype, b_is_kn(layout) ? B[k * N + n] : B[n * K + k]);",
         "bt[n * K + k] = dec16(dtype, B[n * K + k]);",
+    ),
+    "transposed_a_read_untransposed": (
+        "a[m * K + k] = dec16(dtype, a_is_km(layout) ? A[k * M + m] : A[m * K + k]);",
+        "a[m * K + k] = dec16(dtype, A[m * K + k]);",
+    ),
+    "tt_b_read_as_kn": (
+        "static int b_is_kn(int layout) { return layout == DTC_ORACLE_NN || layout == DTC_ORACLE_TN; }",
+        "static int b_is_kn(int layout) { return layout != DTC_ORACLE_NT; }",
     ),
     "last_k_term_dropped": (
         "for (int64_t k = 0; k < j->K; ++k) acc += arow[k] * brow[k];",
