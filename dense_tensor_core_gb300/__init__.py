@@ -8,6 +8,8 @@ There is no CPU fallback: if the library is missing, every call raises.
 from ._binding import (  # noqa: F401
     GEMM_LAYOUT_NN,
     GEMM_LAYOUT_NT,
+    GEMM_LAYOUT_TN,
+    GEMM_LAYOUT_TT,
     GEMM_VARIANT_1CTA,
     GEMM_VARIANT_2CTA,
     GEMM_VARIANT_AUTO,

@@ -13,7 +13,8 @@ import torch
 HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(HERE, "libdtc_gemm.so")
 
-GEMM_LAYOUT_NT, GEMM_LAYOUT_NN = 0, 1
+GEMM_LAYOUT_NT, GEMM_LAYOUT_NN, GEMM_LAYOUT_TN, GEMM_LAYOUT_TT = 0, 1, 2, 3
+_LAYOUTS = {"NT": 0, "NN": 1, "TN": 2, "TT": 3}
 GEMM_VARIANT_AUTO, GEMM_VARIANT_1CTA, GEMM_VARIANT_2CTA, GEMM_VARIANT_SPLITK = 0, 1, 2, 3
 _STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTED", 3: "GEMM_ERR_CUDA",
            4: "GEMM_ERR_TIMEOUT"}
@@ -29,7 +30,8 @@ class GemmError(RuntimeError):
 class gemm_options(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("split_k", ctypes.c_int),
                 ("timeout_ns", ctypes.c_uint64), ("fault_inject", ctypes.c_int),
-                ("tile_n", ctypes.c_int), ("cluster_m", ctypes.c_int), ("tile_k", ctypes.c_int)]
+                ("tile_n", ctypes.c_int), ("cluster_m", ctypes.c_int), ("tile_k", ctypes.c_int),
+                ("lda", ctypes.c_int64), ("ldb", ctypes.c_int64), ("ldc", ctypes.c_int64)]
 
 
 class gemm_plan_info(ctypes.Structure):
@@ -95,42 +97,66 @@ def _ptr(t):
 
 
 def _layout_code(layout):
-    return {"NT": 0, "NN": 1, 0: 0, 1: 1}[layout]
+    if layout in _LAYOUTS:
+        return _LAYOUTS[layout]
+    if layout in _LAYOUTS.values():
+        return layout
+    raise ValueError(f"unknown layout {layout!r}: NT, NN, TN or TT")
+
+
+def _layout_name(layout):
+    code = _layout_code(layout)
+    return next(k for k, v in _LAYOUTS.items() if v == code)
 
 
 def _shapes16(A, B, layout):
+    """(M, N, K) from the stored shapes: A is [M,K] or, for TN / TT, [K,M]; B is [N,K] for NT /
+    TT, else [K,N]."""
     if A.dim() != 2 or B.dim() != 2:
         raise ValueError("A and B must be 2-D")
-    M, K = A.shape
-    if _layout_code(layout) == GEMM_LAYOUT_NT:
-        N, Kb = B.shape
-    else:
-        Kb, N = B.shape
+    name = _layout_name(layout)
+    K, M = A.shape if name[0] == "T" else A.shape[::-1]
+    N, Kb = B.shape if name[1] == "T" else B.shape[::-1]
     if Kb != K:
-        raise ValueError(f"inner sizes differ: A is {tuple(A.shape)}, B is {tuple(B.shape)} ({layout})")
+        raise ValueError(f"inner sizes differ: A is {tuple(A.shape)}, B is {tuple(B.shape)} ({name})")
     return M, N, K
 
 
-def _check_tensor(t, dtype, name):
+def _check_tensor(t, dtype, name, rows_of_larger=False):
+    """dtype and device checks; the tensor must be dense row-major, or, with rows_of_larger, may
+    be rows of a larger row-major array (unit column stride, row stride >= its row length)."""
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous (dense row-major)")
+    if t.is_contiguous():
+        return
+    if rows_of_larger and t.dim() == 2 and t.stride(1) == 1 and t.stride(0) >= t.shape[1]:
+        return
+    raise ValueError(f"{name} must be dense row-major" +
+                     (" or rows of a larger row-major array" if rows_of_larger else ""))
 
 
-def _out(C, M, N, dtype, device):
+def _ld(t):
+    """Leading dimension to pass: 0 (dense) unless the rows are further apart than their length."""
+    if t is None or t.dim() != 2 or t.shape[0] <= 1 or t.stride(0) == t.shape[1]:
+        return 0
+    return t.stride(0)
+
+
+def _out(C, M, N, dtype, device, rows_of_larger=False):
     if C is None:
         return torch.empty((M, N), dtype=dtype, device=device)
-    _check_tensor(C, dtype, "C")
+    _check_tensor(C, dtype, "C", rows_of_larger)
     if tuple(C.shape) != (M, N):
         raise ValueError(f"C must be {(M, N)}, got {tuple(C.shape)}")
     return C
 
 
-def _options(variant, split_k, timeout_ns, fault_inject, tile_n=0, cluster_m=0, tile_k=0):
-    return gemm_options(variant, split_k, timeout_ns, fault_inject, tile_n, cluster_m, tile_k)
+def _options(variant, split_k, timeout_ns, fault_inject, tile_n=0, cluster_m=0, tile_k=0,
+             lda=0, ldb=0, ldc=0):
+    return gemm_options(variant, split_k, timeout_ns, fault_inject, tile_n, cluster_m, tile_k,
+                        lda, ldb, ldc)
 
 
 def _gemm16(name, dtype, A, B, C, layout, stream):
@@ -144,7 +170,8 @@ def _gemm16(name, dtype, A, B, C, layout, stream):
 
 
 def gemm_bf16(A, B, C=None, layout="NT", stream=None):
-    """C[M,N] = A[M,K] . B^T (NT: B is [N,K]) or A . B (NN: B is [K,N]); bf16 in/out."""
+    """C[M,N] = Aop . Bop; bf16 in/out. A is [M,K] (NT, NN) or [K,M] (TN, TT); B is [N,K] (NT,
+    TT) or [K,N] (NN, TN); all dense row-major."""
     return _gemm16("gemm_bf16", torch.bfloat16, A, B, C, layout, stream)
 
 
@@ -153,9 +180,9 @@ def gemm_f16(A, B, C=None, layout="NT", stream=None):
     return _gemm16("gemm_f16", torch.float16, A, B, C, layout, stream)
 
 
-def _check_mxfp8(A, B, sfA, sfB):
-    _check_tensor(A, torch.uint8, "A")
-    _check_tensor(B, torch.uint8, "B")
+def _check_mxfp8(A, B, sfA, sfB, rows_of_larger=False):
+    _check_tensor(A, torch.uint8, "A", rows_of_larger)
+    _check_tensor(B, torch.uint8, "B", rows_of_larger)
     _check_tensor(sfA, torch.uint8, "sfA")
     _check_tensor(sfB, torch.uint8, "sfB")
     M, K = A.shape
@@ -180,17 +207,20 @@ def gemm_mxfp8(A, B, sfA, sfB, C=None, stream=None):
 
 def gemm_ex(kind, A, B, C=None, layout="NT", sfA=None, sfB=None, variant=0, split_k=0,
             timeout_ns=0, fault_inject=0, tile_n=0, cluster_m=0, tile_k=0, stream=None):
-    """Any of the three products with options (variant, split_k, wait limit, test hook)."""
+    """Any of the three products with options (variant, split_k, wait limit, test hook). A, B
+    and C may be rows of larger row-major arrays (e.g. ``big[:, :n]``); their row strides are
+    passed as the leading dimensions."""
     if kind == "mxfp8":
-        M, N, K = _check_mxfp8(A, B, sfA, sfB)
-        C = _out(C, M, N, torch.bfloat16, A.device)
+        M, N, K = _check_mxfp8(A, B, sfA, sfB, rows_of_larger=True)
+        C = _out(C, M, N, torch.bfloat16, A.device, rows_of_larger=True)
     else:
         dt = torch.bfloat16 if kind == "bf16" else torch.float16
-        _check_tensor(A, dt, "A")
-        _check_tensor(B, dt, "B")
+        _check_tensor(A, dt, "A", rows_of_larger=True)
+        _check_tensor(B, dt, "B", rows_of_larger=True)
         M, N, K = _shapes16(A, B, layout)
-        C = _out(C, M, N, dt, A.device)
-    opts = _options(variant, split_k, timeout_ns, fault_inject, tile_n, cluster_m, tile_k)
+        C = _out(C, M, N, dt, A.device, rows_of_larger=True)
+    opts = _options(variant, split_k, timeout_ns, fault_inject, tile_n, cluster_m, tile_k,
+                    _ld(A), _ld(B), _ld(C))
     _check(lib().gemm_ex(_DTYPE[kind], _ptr(A), _ptr(B), _ptr(sfA), _ptr(sfB), _ptr(C), M, N, K,
                          _layout_code(layout), ctypes.byref(opts), _stream_handle(stream)))
     return C

@@ -95,16 +95,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// Row-major 2-D tensor [outer, inner] with dense rows; box [box_outer, box_inner]; with a swizzle
-// the box's inner extent is the swizzle width (128 or 64 bytes); out-of-bounds elements read as
-// zero.
+// Row-major 2-D tensor [outer, inner] with rows `ld` elements apart; box [box_outer, box_inner];
+// with a swizzle the box's inner extent is the swizzle width (128 or 64 bytes); out-of-bounds
+// elements read as zero.
 int make_tmap(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* ptr,
-              uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+              uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_inner, uint32_t box_outer,
               CUtensorMapSwizzle swz, const char* name) {
     auto fn = encode_fn();
     if (!fn) return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
     cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {inner * (uint64_t)elem_bytes};
+    cuuint64_t strides[1] = {ld * (uint64_t)elem_bytes};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
@@ -115,17 +115,17 @@ int make_tmap(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void
     return GEMM_OK;
 }
 
-// A K-major row-major [rows, K] operand seen as the 3-D tensor {E, rows, ceil(K/E)}, E = the
-// elements in 128 bytes, with strides (row, 128 bytes): a box {E, box_rows, 2} is two 128-byte
-// K-chunks of box_rows rows in one instruction. Requires K % E == 0 (a partial last chunk would
-// read into the next row).
+// A K-major row-major [rows, K] operand (rows `ld` elements apart) seen as the 3-D tensor
+// {E, rows, ceil(K/E)}, E = the elements in 128 bytes, with strides (row, 128 bytes): a box
+// {E, box_rows, 2} is two 128-byte K-chunks of box_rows rows in one instruction. Requires
+// K % E == 0 (a partial last chunk would read past the row's K elements).
 int make_tmap_kchunks(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* ptr,
-                      uint64_t K, uint64_t rows, uint32_t box_rows, const char* name) {
+                      uint64_t K, uint64_t rows, uint64_t ld, uint32_t box_rows, const char* name) {
     auto fn = encode_fn();
     if (!fn) return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
     const uint64_t e = 128 / elem_bytes;
     cuuint64_t dims[3] = {e, rows, (K + e - 1) / e};
-    cuuint64_t strides[2] = {K * (uint64_t)elem_bytes, 128};
+    cuuint64_t strides[2] = {ld * (uint64_t)elem_bytes, 128};
     cuuint32_t box[3] = {(cuuint32_t)e, box_rows, 2};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
@@ -136,15 +136,47 @@ int make_tmap_kchunks(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, co
     return GEMM_OK;
 }
 
+// Where the operands live, after the defaults are applied: storage order and row pitch.
+struct Operands {
+    const void* A;
+    const void* B;
+    const void* sfA;
+    const void* sfB;
+    void* C;
+    int64_t lda, ldb, ldc;  // elements between consecutive stored rows
+    bool a_mn;              // A stored [K,M] (layouts TN, TT); else [M,K]
+    bool b_mn;              // B stored [K,N] (layouts NN, TN); else [N,K]
+};
+
+bool layout_a_mn(int layout) { return layout == GEMM_LAYOUT_TN || layout == GEMM_LAYOUT_TT; }
+bool layout_b_mn(int layout) { return layout == GEMM_LAYOUT_NN || layout == GEMM_LAYOUT_TN; }
+
+// Tensor map of a 16-bit operand with `mn` elements along M (or N) and K along the reduction:
+// MN-major storage [K, mn] -> 2-D boxes {64, kBK} (128-byte swizzle); K-major storage [mn, K] ->
+// one 3-D box {64, box_rows, 2} per 128-deep stage, or a 2-D box {kBK, box_rows} with the
+// swizzle as wide as a kBK-element row.
+int tmap_operand16(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, int64_t ld, bool mn_major,
+                   int64_t mn, int64_t K, int kBK, uint32_t box_rows, const char* name) {
+    if (mn_major)
+        return make_tmap(m, dt, 2, ptr, (uint64_t)mn, (uint64_t)K, (uint64_t)ld, 64, (uint32_t)kBK,
+                         CU_TENSOR_MAP_SWIZZLE_128B, name);
+    if (kBK == 128)
+        return make_tmap_kchunks(m, dt, 2, ptr, (uint64_t)K, (uint64_t)mn, (uint64_t)ld, box_rows, name);
+    return make_tmap(m, dt, 2, ptr, (uint64_t)K, (uint64_t)mn, (uint64_t)ld, (uint32_t)kBK, box_rows,
+                     kBK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, name);
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Shared argument rules of every entry point. Returns GEMM_OK or an error (message set).
+// Shared argument rules of every entry point; on success fills `ops` (defaults applied).
+// Returns GEMM_OK or an error (message set).
 int validate(int dtype, const void* A, const void* B, const void* sfA, const void* sfB,
-             const void* C, int64_t M, int64_t N, int64_t K, int layout, const gemm_options* o) {
+             void* C, int64_t M, int64_t N, int64_t K, int layout, const gemm_options* o,
+             Operands* ops) {
     const int64_t kMax = 2147483647;
     if (dtype < 0 || dtype > 2) return fail(GEMM_ERR_INVALID_ARG, "dtype %d is not 0, 1 or 2", dtype);
-    if (layout != GEMM_LAYOUT_NT && layout != GEMM_LAYOUT_NN)
-        return fail(GEMM_ERR_INVALID_ARG, "layout %d is not NT (0) or NN (1)", layout);
+    if (layout < GEMM_LAYOUT_NT || layout > GEMM_LAYOUT_TT)
+        return fail(GEMM_ERR_INVALID_ARG, "layout %d is not NT (0), NN (1), TN (2) or TT (3)", layout);
     if (dtype == 2 && layout != GEMM_LAYOUT_NT)
         return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 GEMM supports the NT layout only");
     if (M < 0 || N < 0 || K < 0 || M > kMax || N > kMax || K > kMax)
@@ -154,23 +186,41 @@ int validate(int dtype, const void* A, const void* B, const void* sfA, const voi
         return fail(GEMM_ERR_INVALID_ARG, "unknown variant %d", o->variant);
     if (o && o->split_k < 0) return fail(GEMM_ERR_INVALID_ARG, "split_k must be >= 0");
     if (o && o->tile_n < 0) return fail(GEMM_ERR_INVALID_ARG, "tile_n must be >= 0");
+    if (o && (o->lda < 0 || o->ldb < 0 || o->ldc < 0))
+        return fail(GEMM_ERR_INVALID_ARG, "lda, ldb and ldc must be >= 0");
+    const int eb = dtype == 2 ? 1 : 2;  // operand element bytes
+    ops->A = A;
+    ops->B = B;
+    ops->sfA = sfA;
+    ops->sfB = sfB;
+    ops->C = C;
+    ops->a_mn = layout_a_mn(layout);
+    ops->b_mn = layout_b_mn(layout);
+    const int64_t a_inner = ops->a_mn ? M : K, b_inner = ops->b_mn ? N : K;
+    ops->lda = (o && o->lda) ? o->lda : a_inner;
+    ops->ldb = (o && o->ldb) ? o->ldb : b_inner;
+    ops->ldc = (o && o->ldc) ? o->ldc : N;
+    if (ops->lda < a_inner || ops->ldb < b_inner || ops->ldc < N)
+        return fail(GEMM_ERR_INVALID_ARG,
+                    "lda=%lld ldb=%lld ldc=%lld: a leading dimension is below its row length "
+                    "(A %lld, B %lld, C %lld elements)", (long long)ops->lda, (long long)ops->ldb,
+                    (long long)ops->ldc, (long long)a_inner, (long long)b_inner, (long long)N);
+    if (ops->lda > kMax || ops->ldb > kMax || ops->ldc > kMax)
+        return fail(GEMM_ERR_INVALID_ARG, "leading dimensions must be at most 2^31-1");
     if (M == 0 || N == 0) return GEMM_OK;
     if (!C) return fail(GEMM_ERR_INVALID_ARG, "C is NULL");
     if (!aligned16(C)) return fail(GEMM_ERR_INVALID_ARG, "C is not 16-byte aligned");
-    if (N % 8) return fail(GEMM_ERR_INVALID_ARG, "N=%lld: C rows must be a multiple of 16 bytes (N %% 8 == 0)", (long long)N);
+    if (ops->ldc % 8)
+        return fail(GEMM_ERR_INVALID_ARG, "ldc=%lld: C rows must start 16 bytes apart (a multiple of 8 elements)",
+                    (long long)ops->ldc);
     if (K == 0) return GEMM_OK;
     if (!A || !B) return fail(GEMM_ERR_INVALID_ARG, "A or B is NULL");
     if (!aligned16(A) || !aligned16(B)) return fail(GEMM_ERR_INVALID_ARG, "A or B is not 16-byte aligned");
-    if (dtype == 2) {
-        if (!sfA || !sfB) return fail(GEMM_ERR_INVALID_ARG, "sfA or sfB is NULL");
-        if (K % 16)
-            return fail(GEMM_ERR_INVALID_ARG, "K=%lld: e4m3 rows must be a multiple of 16 bytes", (long long)K);
-    } else {
-        if (K % 8)
-            return fail(GEMM_ERR_INVALID_ARG, "K=%lld: A rows must be a multiple of 16 bytes (K %% 8 == 0)", (long long)K);
-        if (layout == GEMM_LAYOUT_NN && N % 8)
-            return fail(GEMM_ERR_INVALID_ARG, "N=%lld: B rows must be a multiple of 16 bytes", (long long)N);
-    }
+    if (dtype == 2 && (!sfA || !sfB)) return fail(GEMM_ERR_INVALID_ARG, "sfA or sfB is NULL");
+    if ((ops->lda * eb) % 16)
+        return fail(GEMM_ERR_INVALID_ARG, "lda=%lld: rows of A must start 16 bytes apart", (long long)ops->lda);
+    if ((ops->ldb * eb) % 16)
+        return fail(GEMM_ERR_INVALID_ARG, "ldb=%lld: rows of B must start 16 bytes apart", (long long)ops->ldb);
     return GEMM_OK;
 }
 
@@ -208,7 +258,7 @@ int resident_clusters(int cm, DeviceInfo* dev) {
     if (dev->clusters_for[cm]) return dev->clusters_for[cm];
     int n = dev->sms / cm;
     if (cm > 1) {
-        auto kern = dtc::gemm16_1cta_kernel<true, false, 256, 64, 4, 2>;
+        auto kern = dtc::gemm16_1cta_kernel<true, false, false, 256, 64, 4, 2>;
         using Cfg = dtc::g16::Cfg<256, 64, 4>;
         if (ensure_smem_attr(kern, Cfg::kSmemBytes, dev) == GEMM_OK) {
             cudaLaunchConfig_t cfg = {};
@@ -268,7 +318,8 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
     (void)K;
     int v = o ? o->variant : GEMM_VARIANT_AUTO;
     const int want_n = o ? o->tile_n : 0;
-    if (want_n && want_n != 256 && want_n != 128 && !(want_n == 224 && layout == GEMM_LAYOUT_NT))
+    const bool b_mn = layout_b_mn(layout);  // B stored [K,N]: 64-column boxes, no 224-wide tiles
+    if (want_n && want_n != 256 && want_n != 128 && !(want_n == 224 && !b_mn))
         return fail(GEMM_ERR_UNSUPPORTED, "tile width %d is not offered for this layout", want_n);
     if (dtype == 2) {
         if (v != GEMM_VARIANT_AUTO && v != GEMM_VARIANT_1CTA && v != GEMM_VARIANT_2CTA)
@@ -357,12 +408,13 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
     if (want_n == 128) return fail(GEMM_ERR_UNSUPPORTED, "128-wide tiles are offered by the split-K kernel only");
     int auto_n = 0;
     if (v == GEMM_VARIANT_AUTO) {
-        // Cheapest (variant, width) by the cost model; 224-wide tiles exist for NT only. Below
-        // one wave of tiles either way, the one-CTA kernel (shorter ring fill) is preferred.
+        // Cheapest (variant, width) by the cost model; 224-wide tiles exist for a K-major B (NT,
+        // TT) only. Below one wave of tiles either way, the one-CTA kernel (shorter ring fill)
+        // is preferred.
         double best = -1.0;
         int best_v = GEMM_VARIANT_1CTA, best_n = 256;
         for (const TileChoice& c : kChoices) {
-            if (c.tile_n == 224 && layout != GEMM_LAYOUT_NT) continue;
+            if (c.tile_n == 224 && b_mn) continue;
             if (want_n && c.tile_n != want_n) continue;
             if (c.variant == GEMM_VARIANT_2CTA && (c.tile_k == 128) != (K % 64 == 0)) continue;
             double cost = plan_cost(c.variant, c.tile_n, c.efficiency, M, N, d->sms);
@@ -393,7 +445,7 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
         int best = auto_n ? auto_n : 256;
         if (want_n) {
             best = want_n;
-        } else if (!auto_n && layout == GEMM_LAYOUT_NT) {
+        } else if (!auto_n && !b_mn) {
             if (wave_cost(cluster_rows * ceil_div(N, 224), clusters, 224) <
                 wave_cost(cluster_rows * ceil_div(N, 256), clusters, 256))
                 best = 224;
@@ -409,9 +461,9 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
         const int pairs = std::max(1, d->sms / 2);
         p->cluster = 2;
         p->tile_m = 256;
-        if (layout == GEMM_LAYOUT_NN) {
+        if (b_mn) {
             if (want_n && want_n != 256)
-                return fail(GEMM_ERR_UNSUPPORTED, "the pair kernel offers 256-wide tiles for NN");
+                return fail(GEMM_ERR_UNSUPPORTED, "the pair kernel offers 256-wide tiles for a [K,N] B");
             p->tile_n = 256;
         } else if (want_n) {
             p->tile_n = want_n;
@@ -438,10 +490,11 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
     return GEMM_OK;
 }
 
-Gemm16Args make_args(void* C, int M, int N, int K, int tile_m, int tile_n, int tile_k,
+Gemm16Args make_args(const Operands& ops, int M, int N, int K, int tile_m, int tile_n, int tile_k,
                      const gemm_options* o) {
     Gemm16Args a;
-    a.C = C;
+    a.C = ops.C;
+    a.ldc = ops.ldc;
     a.M = M;
     a.N = N;
     a.K = K;
@@ -474,103 +527,84 @@ int launch_cluster(Kern kern, int grid, int threads, int smem, int cluster, cuda
     return GEMM_OK;
 }
 
-template <bool kBF16, bool kNN, int kBN, int kBK, int kStages, int kCM>
-int launch_gemm16_1cta(const void* A, const void* B, void* C, int M, int N, int K,
-                       const gemm_options* o, DeviceInfo* dev, const Plan& p,
-                       cudaStream_t stream) {
+template <bool kBF16, bool kAMN, bool kNN, int kBN, int kBK, int kStages, int kCM>
+int launch_gemm16_1cta(const Operands& ops, int M, int N, int K, const gemm_options* o,
+                       DeviceInfo* dev, const Plan& p, cudaStream_t stream) {
     using namespace dtc::g16;
     using Cfg = Cfg<kBN, kBK, kStages>;
     const CUtensorMapDataType dt = kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    const CUtensorMapSwizzle kmaj = kBK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     CUtensorMap tA, tB;
-    int rc = make_tmap(&tA, dt, 2, A, (uint64_t)K, (uint64_t)M, kBK, kBM, kmaj, "A");
+    int rc = tmap_operand16(&tA, dt, ops.A, ops.lda, kAMN, M, K, kBK, kBM, "A");
     if (rc) return rc;
-    if (!kNN)
-        rc = make_tmap(&tB, dt, 2, B, (uint64_t)K, (uint64_t)N, kBK, kBN / kCM, kmaj, "B");
-    else
-        rc = make_tmap(&tB, dt, 2, B, (uint64_t)N, (uint64_t)K, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B, "B");
-    if (rc) return rc;
-    auto kern = dtc::gemm16_1cta_kernel<kBF16, kNN, kBN, kBK, kStages, kCM>;
+    if ((rc = tmap_operand16(&tB, dt, ops.B, ops.ldb, kNN, N, K, kBK, kBN / kCM, "B"))) return rc;
+    auto kern = dtc::gemm16_1cta_kernel<kBF16, kAMN, kNN, kBN, kBK, kStages, kCM>;
     if ((rc = ensure_smem_attr(kern, Cfg::kSmemBytes, dev))) return rc;
-    const Gemm16Args args = make_args(C, M, N, K, kBM, kBN, kBK, o);
+    const Gemm16Args args = make_args(ops, M, N, K, kBM, kBN, kBK, o);
     return launch_cluster(kern, p.ctas, kThreads, Cfg::kSmemBytes, kCM, stream, tA, tB, args);
 }
 
-template <bool kBF16, bool kNN, int kBN, int kBK>
-int launch_gemm16_2cta(const void* A, const void* B, void* C, int M, int N, int K,
-                       const gemm_options* o, DeviceInfo* dev, const Plan& p,
-                       cudaStream_t stream) {
+template <bool kBF16, bool kAMN, bool kNN, int kBN, int kBK>
+int launch_gemm16_2cta(const Operands& ops, int M, int N, int K, const gemm_options* o,
+                       DeviceInfo* dev, const Plan& p, cudaStream_t stream) {
     constexpr int kStages = pair_stages(kBN, kBK);
     using Cfg = dtc::g2::Cfg<kBN, kBK, kStages>;
     const CUtensorMapDataType dt = kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUtensorMap tA, tB;
-    int rc = kBK == 128 ? make_tmap_kchunks(&tA, dt, 2, A, (uint64_t)K, (uint64_t)M, 128, "A")
-                        : make_tmap(&tA, dt, 2, A, (uint64_t)K, (uint64_t)M, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "A");
+    int rc = tmap_operand16(&tA, dt, ops.A, ops.lda, kAMN, M, K, kBK, 128, "A");
     if (rc) return rc;
-    if (!kNN)
-        rc = kBK == 128 ? make_tmap_kchunks(&tB, dt, 2, B, (uint64_t)K, (uint64_t)N, Cfg::kHalfN, "B")
-                        : make_tmap(&tB, dt, 2, B, (uint64_t)K, (uint64_t)N, 64, Cfg::kHalfN, CU_TENSOR_MAP_SWIZZLE_128B, "B");
-    else
-        rc = make_tmap(&tB, dt, 2, B, (uint64_t)N, (uint64_t)K, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B, "B");
-    if (rc) return rc;
-    auto kern = dtc::gemm16_2cta_kernel<kBF16, kNN, kBN, kBK, kStages>;
+    if ((rc = tmap_operand16(&tB, dt, ops.B, ops.ldb, kNN, N, K, kBK, Cfg::kHalfN, "B"))) return rc;
+    auto kern = dtc::gemm16_2cta_kernel<kBF16, kAMN, kNN, kBN, kBK, kStages>;
     if ((rc = ensure_smem_attr(kern, Cfg::kSmemBytes, dev))) return rc;
-    const Gemm16Args args = make_args(C, M, N, K, 256, kBN, kBK, o);
+    const Gemm16Args args = make_args(ops, M, N, K, 256, kBN, kBK, o);
     return launch_cluster(kern, p.ctas, dtc::g2::kThreads, Cfg::kSmemBytes, 2, stream, tA, tB, args);
 }
 
-template <bool kBF16, bool kNN, int kBN, int kBK, int kStages>
-int launch_1cta_cm(const Plan& p, const void* A, const void* B, void* C, int m, int n, int k,
+template <bool kBF16, bool kAMN, bool kNN, int kBN, int kBK, int kStages>
+int launch_1cta_cm(const Plan& p, const Operands& ops, int m, int n, int k,
                    const gemm_options* o, DeviceInfo* dev, cudaStream_t stream) {
     if (p.cluster == 2)
-        return launch_gemm16_1cta<kBF16, kNN, kBN, kBK, kStages, 2>(A, B, C, m, n, k, o, dev, p, stream);
-    return launch_gemm16_1cta<kBF16, kNN, kBN, kBK, kStages, 1>(A, B, C, m, n, k, o, dev, p, stream);
+        return launch_gemm16_1cta<kBF16, kAMN, kNN, kBN, kBK, kStages, 2>(ops, m, n, k, o, dev, p, stream);
+    return launch_gemm16_1cta<kBF16, kAMN, kNN, kBN, kBK, kStages, 1>(ops, m, n, k, o, dev, p, stream);
 }
 
 
 
-template <bool kBF16, bool kNN, int kBN, int kBK, int kS>
-int launch_gemm16_splitk(const void* A, const void* B, void* C, int M, int N, int K,
-                         const gemm_options* o, DeviceInfo* dev, const Plan& p,
-                         cudaStream_t stream) {
+template <bool kBF16, bool kAMN, bool kNN, int kBN, int kBK, int kS>
+int launch_gemm16_splitk(const Operands& ops, int M, int N, int K, const gemm_options* o,
+                         DeviceInfo* dev, const Plan& p, cudaStream_t stream) {
     constexpr int kStages = dtc::gsk::stages_for(kBN, kBK, kS);
     using Cfg = dtc::gsk::Cfg<kBN, kBK, kStages, kS>;
     const CUtensorMapDataType dt = kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUtensorMap tA, tB;
-    int rc = kBK == 128 ? make_tmap_kchunks(&tA, dt, 2, A, (uint64_t)K, (uint64_t)M, 128, "A")
-                        : make_tmap(&tA, dt, 2, A, (uint64_t)K, (uint64_t)M, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "A");
+    int rc = tmap_operand16(&tA, dt, ops.A, ops.lda, kAMN, M, K, kBK, 128, "A");
     if (rc) return rc;
-    if (!kNN)
-        rc = kBK == 128 ? make_tmap_kchunks(&tB, dt, 2, B, (uint64_t)K, (uint64_t)N, kBN, "B")
-                        : make_tmap(&tB, dt, 2, B, (uint64_t)K, (uint64_t)N, 64, kBN, CU_TENSOR_MAP_SWIZZLE_128B, "B");
-    else
-        rc = make_tmap(&tB, dt, 2, B, (uint64_t)N, (uint64_t)K, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B, "B");
-    if (rc) return rc;
-    auto kern = dtc::gemm16_splitk_kernel<kBF16, kNN, kBN, kBK, kStages, kS>;
+    if ((rc = tmap_operand16(&tB, dt, ops.B, ops.ldb, kNN, N, K, kBK, kBN, "B"))) return rc;
+    auto kern = dtc::gemm16_splitk_kernel<kBF16, kAMN, kNN, kBN, kBK, kStages, kS>;
     if ((rc = ensure_smem_attr(kern, Cfg::kSmemBytes, dev))) return rc;
-    const Gemm16Args args = make_args(C, M, N, K, 128, kBN, kBK, o);
+    const Gemm16Args args = make_args(ops, M, N, K, 128, kBN, kBK, o);
     return launch_cluster(kern, p.ctas, dtc::gsk::kThreads, Cfg::kSmemBytes, kS, stream, tA, tB, args);
 }
 
-template <bool kBF16, bool kNN>
-int launch_splitk_any(const Plan& p, const void* A, const void* B, void* C, int m, int n, int k,
+template <bool kBF16, bool kAMN, bool kNN>
+int launch_splitk_any(const Plan& p, const Operands& ops, int m, int n, int k,
                       const gemm_options* o, DeviceInfo* dev, cudaStream_t stream) {
     if (p.tile_n == 128) {
         if (p.tile_k == 128)
-            return p.split_k == 2 ? launch_gemm16_splitk<kBF16, kNN, 128, 128, 2>(A, B, C, m, n, k, o, dev, p, stream)
-                                  : launch_gemm16_splitk<kBF16, kNN, 128, 128, 4>(A, B, C, m, n, k, o, dev, p, stream);
-        return p.split_k == 2 ? launch_gemm16_splitk<kBF16, kNN, 128, 64, 2>(A, B, C, m, n, k, o, dev, p, stream)
-                              : launch_gemm16_splitk<kBF16, kNN, 128, 64, 4>(A, B, C, m, n, k, o, dev, p, stream);
+            return p.split_k == 2 ? launch_gemm16_splitk<kBF16, kAMN, kNN, 128, 128, 2>(ops, m, n, k, o, dev, p, stream)
+                                  : launch_gemm16_splitk<kBF16, kAMN, kNN, 128, 128, 4>(ops, m, n, k, o, dev, p, stream);
+        return p.split_k == 2 ? launch_gemm16_splitk<kBF16, kAMN, kNN, 128, 64, 2>(ops, m, n, k, o, dev, p, stream)
+                              : launch_gemm16_splitk<kBF16, kAMN, kNN, 128, 64, 4>(ops, m, n, k, o, dev, p, stream);
     }
-    return launch_gemm16_splitk<kBF16, kNN, 256, 64, 2>(A, B, C, m, n, k, o, dev, p, stream);
+    return launch_gemm16_splitk<kBF16, kAMN, kNN, 256, 64, 2>(ops, m, n, k, o, dev, p, stream);
 }
 
-dtc::GemmMxArgs mx_args(const void* sfA, const void* sfB, void* C, int M, int N, int K, int tile_m,
-                        int tile_n, int tile_k, const gemm_options* o) {
+dtc::GemmMxArgs mx_args(const Operands& ops, int M, int N, int K, int tile_m, int tile_n,
+                        int tile_k, const gemm_options* o) {
     dtc::GemmMxArgs a;
-    a.C = C;
-    a.sfA = static_cast<const uint8_t*>(sfA);
-    a.sfB = static_cast<const uint8_t*>(sfB);
+    a.C = ops.C;
+    a.ldc = ops.ldc;
+    a.sfA = static_cast<const uint8_t*>(ops.sfA);
+    a.sfB = static_cast<const uint8_t*>(ops.sfB);
     a.M = M;
     a.N = N;
     a.K = K;
@@ -583,20 +617,19 @@ dtc::GemmMxArgs mx_args(const void* sfA, const void* sfB, void* C, int M, int N,
     return a;
 }
 
-int launch_mxfp8_2cta(const void* A, const void* B, const void* sfA, const void* sfB, void* C,
-                      int M, int N, int K, const gemm_options* o, DeviceInfo* dev, const Plan& p,
-                      cudaStream_t stream) {
+int launch_mxfp8_2cta(const Operands& ops, int M, int N, int K, const gemm_options* o,
+                      DeviceInfo* dev, const Plan& p, cudaStream_t stream) {
     using namespace dtc::gmx2;
     CUtensorMap tA, tB;
-    int rc = make_tmap_kchunks(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, (uint64_t)K, (uint64_t)M,
-                               kBMc, "A");
+    int rc = make_tmap_kchunks(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ops.A, (uint64_t)K,
+                               (uint64_t)M, (uint64_t)ops.lda, kBMc, "A");
     if (rc) return rc;
-    rc = make_tmap_kchunks(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, (uint64_t)K, (uint64_t)N,
-                           kHalfN, "B");
+    rc = make_tmap_kchunks(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ops.B, (uint64_t)K, (uint64_t)N,
+                           (uint64_t)ops.ldb, kHalfN, "B");
     if (rc) return rc;
     auto kern = dtc::gemm_mxfp8_2cta_kernel<0>;
     if ((rc = ensure_smem_attr(kern, kSmemBytes, dev))) return rc;
-    const dtc::GemmMxArgs a = mx_args(sfA, sfB, C, M, N, K, 256, kBN, kBK, o);
+    const dtc::GemmMxArgs a = mx_args(ops, M, N, K, 256, kBN, kBK, o);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.ctas, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -615,83 +648,82 @@ int launch_mxfp8_2cta(const void* A, const void* B, const void* sfA, const void*
     return GEMM_OK;
 }
 
-int launch_mxfp8(const void* A, const void* B, const void* sfA, const void* sfB, void* C, int M,
-                 int N, int K, const gemm_options* o, DeviceInfo* dev, const Plan& p,
-                 cudaStream_t stream) {
-    if (p.variant == GEMM_VARIANT_2CTA)
-        return launch_mxfp8_2cta(A, B, sfA, sfB, C, M, N, K, o, dev, p, stream);
+int launch_mxfp8(const Operands& ops, int M, int N, int K, const gemm_options* o, DeviceInfo* dev,
+                 const Plan& p, cudaStream_t stream) {
+    if (p.variant == GEMM_VARIANT_2CTA) return launch_mxfp8_2cta(ops, M, N, K, o, dev, p, stream);
     using namespace dtc::gmx;
     CUtensorMap tA, tB;
-    int rc = make_tmap(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, (uint64_t)K, (uint64_t)M, kBK, kBM,
-                       CU_TENSOR_MAP_SWIZZLE_128B, "A");
+    int rc = make_tmap(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ops.A, (uint64_t)K, (uint64_t)M,
+                       (uint64_t)ops.lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B, "A");
     if (rc) return rc;
-    rc = make_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, (uint64_t)K, (uint64_t)N, kBK, kBN,
-                   CU_TENSOR_MAP_SWIZZLE_128B, "B");
+    rc = make_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ops.B, (uint64_t)K, (uint64_t)N,
+                   (uint64_t)ops.ldb, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B, "B");
     if (rc) return rc;
     auto kern = dtc::gemm_mxfp8_kernel<0>;
     if ((rc = ensure_smem_attr(kern, kSmemBytes, dev))) return rc;
-    const dtc::GemmMxArgs a = mx_args(sfA, sfB, C, M, N, K, kBM, kBN, kBK, o);
+    const dtc::GemmMxArgs a = mx_args(ops, M, N, K, kBM, kBN, kBK, o);
     kern<<<p.ctas, kThreads, kSmemBytes, stream>>>(tA, tB, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "MXFP8 kernel launch");
     return GEMM_OK;
 }
 
-template <bool kBF16>
-int launch16(int layout, const Plan& p, const void* A, const void* B, void* C, int m, int n, int k,
-             const gemm_options* o, DeviceInfo* dev, cudaStream_t stream) {
+template <bool kBF16, bool kAMN>
+int launch16(const Plan& p, const Operands& ops, int m, int n, int k, const gemm_options* o,
+             DeviceInfo* dev, cudaStream_t stream) {
+    const bool bmn = ops.b_mn;  // B stored [K,N]: MN-major B, 64-column boxes
     if (p.variant == GEMM_VARIANT_SPLITK) {
-        if (layout == GEMM_LAYOUT_NN)
-            return launch_splitk_any<kBF16, true>(p, A, B, C, m, n, k, o, dev, stream);
-        return launch_splitk_any<kBF16, false>(p, A, B, C, m, n, k, o, dev, stream);
+        if (bmn) return launch_splitk_any<kBF16, kAMN, true>(p, ops, m, n, k, o, dev, stream);
+        return launch_splitk_any<kBF16, kAMN, false>(p, ops, m, n, k, o, dev, stream);
     }
     if (p.variant == GEMM_VARIANT_1CTA) {
         if (p.tile_k == 32) {
-            if (layout == GEMM_LAYOUT_NN)
-                return launch_1cta_cm<kBF16, true, 256, 32, stages_for(256, 32)>(p, A, B, C, m, n, k, o, dev, stream);
+            if (bmn)
+                return launch_1cta_cm<kBF16, kAMN, true, 256, 32, stages_for(256, 32)>(p, ops, m, n, k, o, dev, stream);
             if (p.tile_n == 224)
-                return launch_1cta_cm<kBF16, false, 224, 32, stages_for(224, 32)>(p, A, B, C, m, n, k, o, dev, stream);
-            return launch_1cta_cm<kBF16, false, 256, 32, stages_for(256, 32)>(p, A, B, C, m, n, k, o, dev, stream);
+                return launch_1cta_cm<kBF16, kAMN, false, 224, 32, stages_for(224, 32)>(p, ops, m, n, k, o, dev, stream);
+            return launch_1cta_cm<kBF16, kAMN, false, 256, 32, stages_for(256, 32)>(p, ops, m, n, k, o, dev, stream);
         }
-        if (layout == GEMM_LAYOUT_NN)
-            return launch_1cta_cm<kBF16, true, 256, 64, stages_for(256, 64)>(p, A, B, C, m, n, k, o, dev, stream);
+        if (bmn)
+            return launch_1cta_cm<kBF16, kAMN, true, 256, 64, stages_for(256, 64)>(p, ops, m, n, k, o, dev, stream);
         if (p.tile_n == 224)
-            return launch_1cta_cm<kBF16, false, 224, 64, stages_for(224, 64)>(p, A, B, C, m, n, k, o, dev, stream);
-        return launch_1cta_cm<kBF16, false, 256, 64, stages_for(256, 64)>(p, A, B, C, m, n, k, o, dev, stream);
+            return launch_1cta_cm<kBF16, kAMN, false, 224, 64, stages_for(224, 64)>(p, ops, m, n, k, o, dev, stream);
+        return launch_1cta_cm<kBF16, kAMN, false, 256, 64, stages_for(256, 64)>(p, ops, m, n, k, o, dev, stream);
     }
     if (p.tile_k == 128) {
-        if (layout == GEMM_LAYOUT_NN)
-            return launch_gemm16_2cta<kBF16, true, 256, 128>(A, B, C, m, n, k, o, dev, p, stream);
+        if (bmn) return launch_gemm16_2cta<kBF16, kAMN, true, 256, 128>(ops, m, n, k, o, dev, p, stream);
         if (p.tile_n == 224)
-            return launch_gemm16_2cta<kBF16, false, 224, 128>(A, B, C, m, n, k, o, dev, p, stream);
-        return launch_gemm16_2cta<kBF16, false, 256, 128>(A, B, C, m, n, k, o, dev, p, stream);
+            return launch_gemm16_2cta<kBF16, kAMN, false, 224, 128>(ops, m, n, k, o, dev, p, stream);
+        return launch_gemm16_2cta<kBF16, kAMN, false, 256, 128>(ops, m, n, k, o, dev, p, stream);
     }
-    if (layout == GEMM_LAYOUT_NN)
-        return launch_gemm16_2cta<kBF16, true, 256, 64>(A, B, C, m, n, k, o, dev, p, stream);
-    if (p.tile_n == 224) return launch_gemm16_2cta<kBF16, false, 224, 64>(A, B, C, m, n, k, o, dev, p, stream);
-    return launch_gemm16_2cta<kBF16, false, 256, 64>(A, B, C, m, n, k, o, dev, p, stream);
+    if (bmn) return launch_gemm16_2cta<kBF16, kAMN, true, 256, 64>(ops, m, n, k, o, dev, p, stream);
+    if (p.tile_n == 224) return launch_gemm16_2cta<kBF16, kAMN, false, 224, 64>(ops, m, n, k, o, dev, p, stream);
+    return launch_gemm16_2cta<kBF16, kAMN, false, 256, 64>(ops, m, n, k, o, dev, p, stream);
 }
 
 int run(int dtype, const void* A, const void* B, const void* sfA, const void* sfB, void* C,
         int64_t M, int64_t N, int64_t K, int layout, const gemm_options* o, cudaStream_t stream) {
     g_err[0] = '\0';
-    int rc = validate(dtype, A, B, sfA, sfB, C, M, N, K, layout, o);
+    Operands ops;
+    int rc = validate(dtype, A, B, sfA, sfB, C, M, N, K, layout, o, &ops);
     if (rc) return rc;
     if (M == 0 || N == 0) return GEMM_OK;
     int dev;
     DeviceInfo* info;
     if ((rc = current_device(&dev, &info))) return rc;
-    if (K == 0) {
-        cudaError_t e = cudaMemsetAsync(C, 0, (size_t)M * (size_t)N * 2, stream);
-        return e == cudaSuccess ? GEMM_OK : cuda_fail(e, "cudaMemsetAsync");
+    if (K == 0) {  // the empty sum: C = 0 (only the M x N region of a strided C)
+        cudaError_t e = cudaMemset2DAsync(C, (size_t)ops.ldc * 2, 0, (size_t)N * 2, (size_t)M, stream);
+        return e == cudaSuccess ? GEMM_OK : cuda_fail(e, "cudaMemset2DAsync");
     }
     Plan p;
     if ((rc = make_plan(dtype, M, N, K, layout, o, info, &p))) return rc;
-    if (dtype == 2)
-        return launch_mxfp8(A, B, sfA, sfB, C, (int)M, (int)N, (int)K, o, info, p, stream);
     const int m = (int)M, n = (int)N, k = (int)K;
-    return dtype == 0 ? launch16<true>(layout, p, A, B, C, m, n, k, o, info, stream)
-                      : launch16<false>(layout, p, A, B, C, m, n, k, o, info, stream);
+    if (dtype == 2) return launch_mxfp8(ops, m, n, k, o, info, p, stream);
+    if (dtype == 0)
+        return ops.a_mn ? launch16<true, true>(p, ops, m, n, k, o, info, stream)
+                        : launch16<true, false>(p, ops, m, n, k, o, info, stream);
+    return ops.a_mn ? launch16<false, true>(p, ops, m, n, k, o, info, stream)
+                    : launch16<false, false>(p, ops, m, n, k, o, info, stream);
 }
 
 }  // namespace
@@ -725,8 +757,8 @@ int gemm_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
     const int64_t kMax = 2147483647;
     if (!info) return fail(GEMM_ERR_INVALID_ARG, "info is NULL");
     if (dtype < 0 || dtype > 2) return fail(GEMM_ERR_INVALID_ARG, "dtype %d is not 0, 1 or 2", dtype);
-    if (layout != GEMM_LAYOUT_NT && layout != GEMM_LAYOUT_NN)
-        return fail(GEMM_ERR_INVALID_ARG, "layout %d is not NT (0) or NN (1)", layout);
+    if (layout < GEMM_LAYOUT_NT || layout > GEMM_LAYOUT_TT)
+        return fail(GEMM_ERR_INVALID_ARG, "layout %d is not NT (0), NN (1), TN (2) or TT (3)", layout);
     if (dtype == 2 && layout != GEMM_LAYOUT_NT)
         return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 GEMM supports the NT layout only");
     if (M < 0 || N < 0 || K < 0 || M > kMax || N > kMax || K > kMax)

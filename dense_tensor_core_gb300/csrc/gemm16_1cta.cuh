@@ -56,7 +56,7 @@ struct Cfg {
 };
 }  // namespace g16
 
-template <bool kBF16, bool kNN, int kBN, int kBK, int kStages, int kCM>
+template <bool kBF16, bool kAMN, bool kNN, int kBN, int kBK, int kStages, int kCM>
 __global__ void __launch_bounds__(g16::kThreads, 1)
     gemm16_1cta_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const Gemm16Args args) {
@@ -140,7 +140,14 @@ __global__ void __launch_bounds__(g16::kThreads, 1)
                     if (args.fault == 1 && it == 0) continue;  // test hook: stage never filled
                     const uint32_t full = smem_u32(&bar_full[s]);
                     mbar_arrive_expect_tx(full, C_::kStageBytes);
-                    tma_load_2d(sA + s * kAStage, &tmA, full, kb * kBK, mt * kBM);
+                    if constexpr (kAMN) {
+                        // A stored [K,M]: two 64-column boxes of kBK K-rows (128-byte swizzle)
+                        tma_load_2d(sA + s * kAStage, &tmA, full, mt * kBM, kb * kBK);
+                        tma_load_2d(sA + s * kAStage + 64 * kBK * 2, &tmA, full, mt * kBM + 64,
+                                    kb * kBK);
+                    } else {
+                        tma_load_2d(sA + s * kAStage, &tmA, full, kb * kBK, mt * kBM);
+                    }
                     const uint32_t bdst = sB + s * C_::kBStage;
                     if constexpr (!kNN) {
                         const uint32_t dst = bdst + rank * kBPartBytes;
@@ -176,7 +183,7 @@ __global__ void __launch_bounds__(g16::kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16(kBF16, kNN, kBM, kBN);
+            constexpr uint32_t idesc = idesc_f16(kBF16, kNN, kBM, kBN, kAMN);
             uint32_t it = 0, acc = 0;
             bool ok = true, issued = false;
             for (int t = cluster; t < total && ok; t += clusters) {
@@ -199,7 +206,9 @@ __global__ void __launch_bounds__(g16::kThreads, 1)
                     const uint32_t a0 = sA + s * kAStage, b0 = sB + s * C_::kBStage;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint64_t adesc = smem_desc<kPitch>(a0 + kk * 32, 16, 8 * kPitch);
+                        const uint64_t adesc =
+                            kAMN ? smem_desc<128>(a0 + kk * 16 * 128, 64 * kBK * 2, 1024)
+                                      : smem_desc<kPitch>(a0 + kk * 32, 16, 8 * kPitch);
                         const uint64_t bdesc =
                             kNN ? smem_desc<128>(b0 + kk * 16 * 128, 64 * kBK * 2, 1024)
                                 : smem_desc<kPitch>(b0 + kk * 32, 16, 8 * kPitch);
@@ -242,7 +251,7 @@ __global__ void __launch_bounds__(g16::kThreads, 1)
             if (!ok) break;
             tc_fence_after_sync();
             const int64_t row = (int64_t)mt * kBM + row_in_tile;
-            uint16_t* crow = reinterpret_cast<uint16_t*>(args.C) + row * args.N;
+            uint16_t* crow = reinterpret_cast<uint16_t*>(args.C) + row * args.ldc;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + b * kAccStride;
 #pragma unroll 1
             for (int c = 0; c < kBN / 32; ++c) {

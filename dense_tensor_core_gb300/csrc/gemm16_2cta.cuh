@@ -48,7 +48,7 @@ struct Cfg {
 };
 }  // namespace g2
 
-template <bool kBF16, bool kNN, int kBN, int kBK, int kStages>
+template <bool kBF16, bool kAMN, bool kNN, int kBN, int kBK, int kStages>
 __global__ void __launch_bounds__(g2::kThreads, 1)
     gemm16_2cta_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const Gemm16Args args) {
@@ -126,10 +126,16 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
                     const uint32_t full_local = smem_u32(&bar_full[s]);
                     const uint32_t full_leader = map_to_cta(full_local, 0);
                     if (leader) mbar_arrive_expect_tx(full_local, 2 * C_::kStageBytes);
-                    if constexpr (kChunks == 2)
+                    if constexpr (kAMN) {
+                        // A stored [K,M]: two 64-column boxes of kBK K-rows (128-byte swizzle)
+                        tma_load_2d_pair(sA + s * C_::kAStage, &tmA, full_leader, a_row, kb * kBK);
+                        tma_load_2d_pair(sA + s * C_::kAStage + 64 * kBK * 2, &tmA, full_leader,
+                                         a_row + 64, kb * kBK);
+                    } else if constexpr (kChunks == 2) {
                         tma_load_3d_pair(sA + s * C_::kAStage, &tmA, full_leader, 0, a_row, kb * 2);
-                    else
+                    } else {
                         tma_load_2d_pair(sA + s * C_::kAStage, &tmA, full_leader, kb * kBK, a_row);
+                    }
                     if constexpr (!kNN) {
                         if constexpr (kChunks == 2)
                             tma_load_3d_pair(sB + s * C_::kBStage, &tmB, full_leader, 0, b_row,
@@ -162,7 +168,7 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------ MMA issuer (leader CTA) ------------------------------
         if (lane == 0 && leader) {
-            constexpr uint32_t idesc = idesc_f16(kBF16, kNN, 256, kBN);
+            constexpr uint32_t idesc = idesc_f16(kBF16, kNN, 256, kBN, kAMN);
             uint32_t it = 0, acc = 0;
             bool ok = true, issued = false;
             for (int t = pair; t < total && ok; t += num_pairs) {
@@ -188,7 +194,8 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
                         // K-chunk kk/4 of the stage, 32-byte step kk%4 inside its swizzle row
                         const uint32_t koff = (kk % 4) * 32;
                         const uint64_t adesc =
-                            smem_desc_sw128(a0 + (kk / 4) * (kBMc * 128) + koff, 16, 1024);
+                            kAMN ? smem_desc_sw128(a0 + kk * 16 * 128, 64 * kBK * 2, 1024)
+                                      : smem_desc_sw128(a0 + (kk / 4) * (kBMc * 128) + koff, 16, 1024);
                         const uint64_t bdesc =
                             kNN ? smem_desc_sw128(b0 + kk * 16 * 128, 64 * kBK * 2, 1024)
                                 : smem_desc_sw128(b0 + (kk / 4) * (C_::kHalfN * 128) + koff, 16, 1024);
@@ -227,7 +234,7 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
             if (!ok) break;
             tc_fence_after_sync();
             const int64_t row = (int64_t)mt * 256 + (int64_t)rank * kBMc + row_in_tile;
-            uint16_t* crow = reinterpret_cast<uint16_t*>(args.C) + row * args.N;
+            uint16_t* crow = reinterpret_cast<uint16_t*>(args.C) + row * args.ldc;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + b * kAccStride;
 #pragma unroll 1
             for (int c = 0; c < kBN / 32; ++c) {

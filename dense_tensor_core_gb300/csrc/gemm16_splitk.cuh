@@ -71,7 +71,7 @@ struct Cfg {
 };
 }  // namespace gsk
 
-template <bool kBF16, bool kNN, int kBN, int kBK, int kStages, int kS>
+template <bool kBF16, bool kAMN, bool kNN, int kBN, int kBK, int kStages, int kS>
 __global__ void __launch_bounds__(gsk::kThreads, 1)
     gemm16_splitk_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB, const Gemm16Args args) {
@@ -148,10 +148,16 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
                 if (args.fault == 1 && it == 0) continue;  // test hook: stage never filled
                 const uint32_t full = smem_u32(&bar_full[s]);
                 mbar_arrive_expect_tx(full, C_::kStageBytes);
-                if constexpr (kChunks == 2)
+                if constexpr (kAMN) {
+                    // A stored [K,M]: two 64-column boxes of kBK K-rows (128-byte swizzle)
+                    tma_load_2d(sA + s * C_::kAStage, &tmA, full, mt * kBM, kb * kBK);
+                    tma_load_2d(sA + s * C_::kAStage + 64 * kBK * 2, &tmA, full, mt * kBM + 64,
+                                kb * kBK);
+                } else if constexpr (kChunks == 2) {
                     tma_load_3d(sA + s * C_::kAStage, &tmA, full, 0, mt * kBM, kb * 2);
-                else
+                } else {
                     tma_load_2d(sA + s * C_::kAStage, &tmA, full, kb * kBK, mt * kBM);
+                }
                 if constexpr (!kNN) {
                     if constexpr (kChunks == 2)
                         tma_load_3d(sB + s * C_::kBStage, &tmB, full, 0, nt * kBN, kb * 2);
@@ -175,7 +181,7 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16(kBF16, kNN, kBM, kBN);
+            constexpr uint32_t idesc = idesc_f16(kBF16, kNN, kBM, kBN, kAMN);
             uint32_t it = 0;
             bool ok = true, issued = false;
             for (int kb = kb0; kb < kb1; ++kb, ++it) {
@@ -192,7 +198,8 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
                     // K-chunk kk/4 of the stage, 32-byte step kk%4 inside its swizzle row
                     const uint32_t koff = (kk % 4) * 32;
                     const uint64_t adesc =
-                        smem_desc_sw128(a0 + (kk / 4) * (kBM * 128) + koff, 16, 1024);
+                        kAMN ? smem_desc_sw128(a0 + kk * 16 * 128, 64 * kBK * 2, 1024)
+                                  : smem_desc_sw128(a0 + (kk / 4) * (kBM * 128) + koff, 16, 1024);
                     const uint64_t bdesc =
                         kNN ? smem_desc_sw128(b0 + kk * 16 * 128, 64 * kBK * 2, 1024)
                             : smem_desc_sw128(b0 + (kk / 4) * (kBN * 128) + koff, 16, 1024);
@@ -256,7 +263,7 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
             }
         } else if (ok) {
             const int64_t grow = (int64_t)mt * kBM + q * 32 + lane;
-            uint16_t* crow = reinterpret_cast<uint16_t*>(args.C) + grow * args.N;
+            uint16_t* crow = reinterpret_cast<uint16_t*>(args.C) + grow * args.ldc;
 #pragma unroll 1
             for (int c = 0; c < C_::kPieces; ++c) {
                 uint32_t v[64];

@@ -14,6 +14,7 @@ __device__ int g_dtc_status;  // first device-side wait that gave up (0 = none)
 
 struct Gemm16Args {
     void* C;
+    int64_t ldc;  // elements between rows of C (>= N)
     int M, N, K;
     int num_m, num_n, num_kb;
     uint64_t timeout_ns;

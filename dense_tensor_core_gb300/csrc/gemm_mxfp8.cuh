@@ -33,6 +33,7 @@ namespace dtc {
 
 struct GemmMxArgs {
     void* C;
+    int64_t ldc;  // elements between rows of C (>= N)
     const uint8_t* sfA;
     const uint8_t* sfB;
     int M, N, K;
@@ -242,7 +243,7 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
             if (!ok) break;
             tc_fence_after_sync();
             const int64_t row = (int64_t)mt * kBM + row_in_tile;
-            uint16_t* crow = reinterpret_cast<uint16_t*>(args.C) + row * args.N;
+            uint16_t* crow = reinterpret_cast<uint16_t*>(args.C) + row * args.ldc;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + b * kAccStride;
 #pragma unroll 1
             for (int c = 0; c < kBN / 32; ++c) {

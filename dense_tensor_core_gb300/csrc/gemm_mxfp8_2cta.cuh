@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(gmx2::kThreads, 1)
             if (!ok) break;
             tc_fence_after_sync();
             const int64_t row = (int64_t)mt * 256 + (int64_t)rank * kBMc + row_in_tile;
-            uint16_t* crow = reinterpret_cast<uint16_t*>(args.C) + row * args.N;
+            uint16_t* crow = reinterpret_cast<uint16_t*>(args.C) + row * args.ldc;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + b * kAccStride;
 #pragma unroll 1
             for (int c = 0; c < kBN / 32; ++c) {

@@ -48,7 +48,8 @@ class Workload:
 
 # The pages' example shapes (TileLang SM100 Support (Preview): NT 4096x4096x8192 with a
 # 128x256x128 tile; tilelang (velog) 1.1-1.3: fp16 NN 1024^3) plus the large 2-CTA square, the
-# memory-bound skinny product and the block-scaled variant.
+# memory-bound skinny product and the block-scaled variant; then the same 4096x4096x8192 product
+# with A stored transposed (trans_A of T.gemm), to measure the MN-major A path.
 WORKLOADS = {
     w.name: w
     for w in [
@@ -58,6 +59,8 @@ WORKLOADS = {
         Workload("bf16_nt_8192x8192x8192", "bf16", "NT", 8192, 8192, 8192, 3),
         Workload("bf16_nt_128x8192x8192", "bf16", "NT", 128, 8192, 8192, 3),
         Workload("mxfp8_nt_4096x4096x8192", "mxfp8", "NT", 4096, 4096, 8192, 4),
+        Workload("bf16_tn_4096x4096x8192", "bf16", "TN", 4096, 4096, 8192, 5),
+        Workload("bf16_tt_4096x4096x8192", "bf16", "TT", 4096, 4096, 8192, 6),
     ]
 }
 

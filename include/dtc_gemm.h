@@ -9,8 +9,13 @@
  *     (ref_c = (a.float() @ b.T.float()).to(torch.bfloat16)).
  *   - "NN": B is stored row-major [K,N] and Bop = B. This is the product of tilelang (velog),
  *     section 1.1 Front-End DSL (A is (M, K), B is (K, N), accum_dtype "float").
- *   A is always row-major [M,K]; C is always row-major [M,N]. Every row is dense (row stride =
- *   number of columns), as the generated host code of tilelang (velog) section 1.3 also requires.
+ *   - "TN", "TT": as "NN", "NT" with A stored row-major [K,M] (Aop = A^T). The first letter is
+ *     A's transpose flag, the second B's: the trans_A / trans_B arguments of T.gemm in TileLang
+ *     SM100 Support (Preview), "Current Limitations" and "Code Example". 16-bit products only.
+ *   In NT and NN, A is row-major [M,K]. C is always row-major [M,N]. With the plain entry points
+ *   every row is dense (row stride = number of columns), as the generated host code of tilelang
+ *   (velog) section 1.3 also assumes; gemm_ex takes leading dimensions (lda, ldb, ldc in
+ *   gemm_options) for operands and results that are rows of larger row-major arrays.
  *
  * Pointers: A, B, C (and sfA, sfB) are DEVICE pointers on the current CUDA device, owned by the
  * caller; the library keeps no reference after the call returns. C must not overlap A, B or the
@@ -40,8 +45,10 @@ extern "C" {
 typedef struct CUstream_st* dtc_stream_t;
 
 typedef enum {
-    GEMM_LAYOUT_NT = 0, /* B is [N,K] row-major: C = A . B^T */
-    GEMM_LAYOUT_NN = 1  /* B is [K,N] row-major: C = A . B   */
+    GEMM_LAYOUT_NT = 0, /* A is [M,K], B is [N,K] row-major: C = A . B^T   */
+    GEMM_LAYOUT_NN = 1, /* A is [M,K], B is [K,N] row-major: C = A . B     */
+    GEMM_LAYOUT_TN = 2, /* A is [K,M], B is [K,N] row-major: C = A^T . B   */
+    GEMM_LAYOUT_TT = 3  /* A is [K,M], B is [N,K] row-major: C = A^T . B^T */
 } gemm_layout;
 
 typedef enum {
@@ -81,14 +88,19 @@ typedef struct {
                              2); 0 = choose */
     int tile_k;           /* K-elements per pipeline stage: 64 or 32 (1CTA), 64 or 128 (2CTA;
                              SPLITK with 128-wide tiles); 128 needs K % 64 == 0; 0 = choose */
+    int64_t lda;          /* elements between consecutive stored rows of A, B, C; 0 = dense (the */
+    int64_t ldb;          /* row length: K or M for A, K or N for B, N for C). At least the row */
+    int64_t ldc;          /* length, and rows must start 16 bytes apart (ld x element size %
+                             16 == 0). Only the M x N region of C is written. */
 } gemm_options;
 
 /*
  * bf16 operands, fp32 accumulation, bf16 output.
- *   A: [M,K] bf16. B: [N,K] bf16 (NT) or [K,N] bf16 (NN). C: [M,N] bf16.
- *   INVALID_ARG when: M, N or K is negative or above 2^31-1; layout is not NT or NN; a pointer
- *   needed for the sizes is NULL or not 16-byte aligned; a row is not a multiple of 16 bytes
- *   (K % 8 != 0 for A and for NT B; N % 8 != 0 for NN B and for C).
+ *   A: [M,K] bf16 (NT, NN) or [K,M] (TN, TT). B: [N,K] bf16 (NT, TT) or [K,N] (NN, TN).
+ *   C: [M,N] bf16.
+ *   INVALID_ARG when: M, N or K is negative or above 2^31-1; layout is not NT, NN, TN or TT; a
+ *   pointer needed for the sizes is NULL or not 16-byte aligned; a stored row is not a multiple
+ *   of 16 bytes (its length % 8 != 0: K or M for A, K or N for B, N for C).
  * (TileLang SM100 Support (Preview), "Code Example" / "Compilation and Usage".)
  */
 int gemm_bf16(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int layout,
@@ -117,9 +129,11 @@ int gemm_mxfp8(const void* A, const void* B, const void* sfA, const void* sfB, v
                int64_t M, int64_t N, int64_t K, dtc_stream_t stream);
 
 /*
- * The same three operations with options (variant choice, wait limit, test hook).
- * dtype: 0 = bf16, 1 = fp16, 2 = mxfp8 (sfA/sfB are ignored for 0 and 1; layout must be NT
- * for 2). opts may be NULL (all defaults).
+ * The same three operations with options (variant choice, leading dimensions, wait limit, test
+ * hook). dtype: 0 = bf16, 1 = fp16, 2 = mxfp8 (sfA/sfB are ignored for 0 and 1; layout must be
+ * NT for 2; the scale arrays stay dense). opts may be NULL (all defaults). INVALID_ARG also when
+ * a leading dimension is negative, below its row length, above 2^31-1 or not a multiple of 16
+ * bytes.
  */
 int gemm_ex(int dtype, const void* A, const void* B, const void* sfA, const void* sfB, void* C,
             int64_t M, int64_t N, int64_t K, int layout, const gemm_options* opts,

@@ -57,7 +57,8 @@ INVALID, UNSUPPORTED = 1, 2
 @pytest.mark.parametrize(
     "kw",
     [
-        dict(layout=2),
+        dict(layout=4),
+        dict(layout=-1),
         dict(M=-1),
         dict(K=-8),
         dict(N=2 ** 31),
@@ -69,6 +70,10 @@ INVALID, UNSUPPORTED = 1, 2
         dict(K=12),  # A rows of 24 bytes
         dict(N=12),  # C rows of 24 bytes
         dict(N=12, layout=1),
+        dict(M=12, layout=2),  # TN: A stored [K,M], rows of 24 bytes
+        dict(M=12, layout=3),
+        dict(N=12, layout=2),  # TN: B stored [K,N]
+        dict(K=12, layout=3),  # TT: B stored [N,K]
     ],
 )
 def test_invalid_arguments_rejected_before_cuda(L, name, kw):
@@ -90,6 +95,45 @@ def test_mxfp8_rules(L):
     # NN is not offered for the block-scaled product
     rc = L.gemm_ex(2, vp(0x1000), vp(0x2000), vp(0x10), vp(0x20), vp(0x3000), 16, 16, 32, 1, None, None)
     assert rc == UNSUPPORTED
+
+
+@pytest.mark.parametrize(
+    "ld,layout",
+    [
+        (dict(lda=8), 0),    # below K = 16
+        (dict(ldb=8), 0),
+        (dict(ldc=8), 0),    # below N = 16
+        (dict(lda=20), 0),   # 40-byte rows: not 16-byte aligned
+        (dict(ldc=20), 0),
+        (dict(ldb=20), 1),
+        (dict(lda=-16), 0),
+        (dict(lda=2 ** 31), 2),
+        (dict(lda=8), 2),    # TN: A rows hold M = 16 elements
+    ],
+)
+def test_leading_dimensions_rejected_before_cuda(L, ld, layout):
+    from dense_tensor_core_gb300._binding import gemm_options
+
+    vp = ctypes.c_void_p
+    o = gemm_options()
+    for k, v in ld.items():
+        setattr(o, k, v)
+    rc = L.gemm_ex(0, vp(0x1000), vp(0x2000), None, None, vp(0x3000), 16, 16, 16, layout,
+                   ctypes.byref(o), None)
+    assert rc == INVALID
+    assert L.gemm_last_error()
+
+
+def test_options_struct_matches_header():
+    # the binding's ctypes mirror of gemm_options lists the header's fields in order
+    from dense_tensor_core_gb300._binding import gemm_options
+
+    with open(os.path.join(ROOT, "include", "dtc_gemm.h")) as f:
+        text = f.read()
+    body = text[text.index("typedef struct {", text.index("gemm_variant;")):]
+    body = body[: body.index("} gemm_options;")]
+    fields = re.findall(r"^\s*(?:int|uint64_t|int64_t)\s+(\w+);", body, re.M)
+    assert fields == [n for n, _ in gemm_options._fields_]
 
 
 def test_binding_checks_tensors_without_gpu():

@@ -193,7 +193,8 @@ def test_config_f16_nn_1024_full():
 
 @pytest.mark.parametrize("variant", [0, 1, 2])
 @pytest.mark.parametrize("name", ["bf16_nt_4096x4096x8192", "bf16_nt_8192x8192x8192",
-                                  "bf16_nt_128x8192x8192"])
+                                  "bf16_nt_128x8192x8192", "bf16_tn_4096x4096x8192",
+                                  "bf16_tt_4096x4096x8192"])
 def test_benchmark_sizes_sampled(name, variant):
     # variant 0 is the launch the benchmark times (the library's own choice)
     w = workloads.WORKLOADS[name]
@@ -266,3 +267,72 @@ def test_repeated_calls_are_deterministic():
     C2 = dtc.gemm_bf16(At, Bt)
     dtc.gemm_stream_status()
     assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
+
+
+# --- A stored transposed (TN, TT) and rows of larger arrays (leading dimensions) ---------------
+
+@pytest.mark.parametrize("variant,extra", [(1, {}), (1, dict(tile_k=32)), (1, dict(cluster_m=2)),
+                                           (2, dict(tile_k=64)), (2, dict(tile_k=128)),
+                                           (3, dict(split_k=2)), (3, dict(split_k=4, tile_k=64))])
+@pytest.mark.parametrize("layout", ["TN", "TT"])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (264, 520, 200), (512, 448, 384), (8, 8, 8)])
+def test_transposed_a_full_parity(M, N, K, layout, variant, extra):
+    # A stored [K,M] is loaded as 64-column boxes and read through an MN-major descriptor;
+    # 264 rows leave a partial tile in M (and a partial 64-column box), K = 200 a partial K-block
+    if extra.get("tile_k") == 128 and K % 64:
+        pytest.skip("128-deep pair stages need K % 64 == 0")
+    kind = "bf16" if (M + N) % 2 == 0 else "f16"
+    full_check(kind, layout, M, N, K, seed=M + N + K, variant=variant, **extra)
+    full_check("f16" if kind == "bf16" else "bf16", layout, M, N, K, seed=M + N + K + 1,
+               variant=variant, **extra)
+
+
+@pytest.mark.parametrize("layout", ["NT", "NN", "TN", "TT"])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
+def test_rows_of_larger_arrays(layout, variant):
+    # A, B and C are views into wider row-major arrays: the row strides go to the library as
+    # lda / ldb / ldc; C's padding columns must be left untouched
+    import dense_tensor_core_gb300 as dtc
+
+    M, N, K = 264, 392, 320
+    A, B = workloads.make16("bf16", layout, M, N, K, seed=77)
+    pad = {"A": 24, "B": 40, "C": 16}
+    At = torch.full((A.shape[0], A.shape[1] + pad["A"]), 7.0, dtype=torch.bfloat16, device="cuda")
+    Bt = torch.full((B.shape[0], B.shape[1] + pad["B"]), 7.0, dtype=torch.bfloat16, device="cuda")
+    At[:, : A.shape[1]] = to_device16(A, "bf16")
+    Bt[:, : B.shape[1]] = to_device16(B, "bf16")
+    Cbig = torch.full((M, N + pad["C"]), float("nan"), dtype=torch.bfloat16, device="cuda")
+    kw = dict(split_k=2) if variant == 3 else {}
+    dtc.gemm_ex("bf16", At[:, : A.shape[1]], Bt[:, : B.shape[1]], Cbig[:, :N], layout=layout,
+                variant=variant, **kw)
+    dtc.gemm_stream_status()
+    assert torch.isnan(Cbig[:, N:].float()).all(), "padding columns of C were written"
+    C = Cbig[:, :N].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    ref = oracle.gemm16("bf16", layout, A, B, M, N, K)
+    check_close(values16(C, "bf16"), values16(ref, "bf16"), f"strided {layout} variant {variant}")
+
+
+def test_k_zero_with_strided_c_writes_only_the_region():
+    import dense_tensor_core_gb300 as dtc
+
+    A = torch.empty((64, 0), dtype=torch.bfloat16, device="cuda")
+    B = torch.empty((32, 0), dtype=torch.bfloat16, device="cuda")
+    Cbig = torch.full((64, 48), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dtc.gemm_ex("bf16", A, B, Cbig[:, :32])
+    dtc.gemm_stream_status()
+    assert torch.equal(Cbig[:, :32], torch.zeros((64, 32), dtype=torch.bfloat16, device="cuda"))
+    assert torch.isnan(Cbig[:, 32:].float()).all()
+
+
+def test_transposed_layout_plans():
+    import dense_tensor_core_gb300 as dtc
+
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the expected choices are worked out for 152 SMs")
+    # B stored [N,K] (TT) keeps the 224-wide pair tiles; B stored [K,N] (TN) takes 256
+    p = dtc.gemm_plan("bf16", 4096, 4096, 8192, "TT")
+    assert (p["variant"], p["tile_n"]) == (2, 224)
+    p = dtc.gemm_plan("bf16", 4096, 4096, 8192, "TN")
+    assert (p["variant"], p["tile_n"]) == (2, 256)
+    with pytest.raises(dtc.GemmError):
+        dtc.gemm_plan("bf16", 4096, 4096, 8192, "TN", variant=2, tile_n=224)
