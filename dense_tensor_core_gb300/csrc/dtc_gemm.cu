@@ -318,9 +318,11 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
     (void)K;
     int v = o ? o->variant : GEMM_VARIANT_AUTO;
     const int want_n = o ? o->tile_n : 0;
-    const bool b_mn = layout_b_mn(layout);  // B stored [K,N]: 64-column boxes, no 224-wide tiles
-    if (want_n && want_n != 256 && want_n != 128 && !(want_n == 224 && !b_mn))
-        return fail(GEMM_ERR_UNSUPPORTED, "tile width %d is not offered for this layout", want_n);
+    const bool b_mn = layout_b_mn(layout);  // B stored [K,N]: 64-column boxes
+    if (want_n && want_n != 256 && want_n != 128 && want_n != 224)
+        return fail(GEMM_ERR_UNSUPPORTED, "tile width %d is not offered", want_n);
+    if (want_n == 224 && b_mn && v == GEMM_VARIANT_1CTA)
+        return fail(GEMM_ERR_UNSUPPORTED, "224-wide one-CTA tiles need B stored [N,K]");
     if (dtype == 2) {
         if (v != GEMM_VARIANT_AUTO && v != GEMM_VARIANT_1CTA && v != GEMM_VARIANT_2CTA)
             return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 product has one-CTA and pair kernels");
@@ -414,7 +416,7 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
         double best = -1.0;
         int best_v = GEMM_VARIANT_1CTA, best_n = 256;
         for (const TileChoice& c : kChoices) {
-            if (c.tile_n == 224 && b_mn) continue;
+            if (c.tile_n == 224 && b_mn && c.variant == GEMM_VARIANT_1CTA) continue;
             if (want_n && c.tile_n != want_n) continue;
             if (c.variant == GEMM_VARIANT_2CTA && (c.tile_k == 128) != (K % 64 == 0)) continue;
             double cost = plan_cost(c.variant, c.tile_n, c.efficiency, M, N, d->sms);
@@ -443,6 +445,8 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
         const int clusters = resident_clusters(cm, d);
         const int64_t cluster_rows = ceil_div(num_m, cm);
         int best = auto_n ? auto_n : 256;
+        if (want_n == 224 && b_mn)
+            return fail(GEMM_ERR_UNSUPPORTED, "224-wide one-CTA tiles need B stored [N,K]");
         if (want_n) {
             best = want_n;
         } else if (!auto_n && !b_mn) {
@@ -461,11 +465,7 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
         const int pairs = std::max(1, d->sms / 2);
         p->cluster = 2;
         p->tile_m = 256;
-        if (b_mn) {
-            if (want_n && want_n != 256)
-                return fail(GEMM_ERR_UNSUPPORTED, "the pair kernel offers 256-wide tiles for a [K,N] B");
-            p->tile_n = 256;
-        } else if (want_n) {
+        if (want_n) {
             p->tile_n = want_n;
         } else if (auto_n) {
             p->tile_n = auto_n;
@@ -547,7 +547,7 @@ template <bool kBF16, bool kAMN, bool kNN, int kBN, int kBK>
 int launch_gemm16_2cta(const Operands& ops, int M, int N, int K, const gemm_options* o,
                        DeviceInfo* dev, const Plan& p, cudaStream_t stream) {
     constexpr int kStages = pair_stages(kBN, kBK);
-    using Cfg = dtc::g2::Cfg<kBN, kBK, kStages>;
+    using Cfg = dtc::g2::Cfg<kBN, kBK, kStages, kNN>;
     const CUtensorMapDataType dt = kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUtensorMap tA, tB;
     int rc = tmap_operand16(&tA, dt, ops.A, ops.lda, kAMN, M, K, kBK, 128, "A");
@@ -668,6 +668,18 @@ int launch_mxfp8(const Operands& ops, int M, int N, int K, const gemm_options* o
     return GEMM_OK;
 }
 
+template <bool kBF16, bool kAMN, bool kNN>
+int launch_pair_width(const Plan& p, const Operands& ops, int m, int n, int k,
+                      const gemm_options* o, DeviceInfo* dev, cudaStream_t stream) {
+    if (p.tile_k == 128) {
+        if (p.tile_n == 224)
+            return launch_gemm16_2cta<kBF16, kAMN, kNN, 224, 128>(ops, m, n, k, o, dev, p, stream);
+        return launch_gemm16_2cta<kBF16, kAMN, kNN, 256, 128>(ops, m, n, k, o, dev, p, stream);
+    }
+    if (p.tile_n == 224) return launch_gemm16_2cta<kBF16, kAMN, kNN, 224, 64>(ops, m, n, k, o, dev, p, stream);
+    return launch_gemm16_2cta<kBF16, kAMN, kNN, 256, 64>(ops, m, n, k, o, dev, p, stream);
+}
+
 template <bool kBF16, bool kAMN>
 int launch16(const Plan& p, const Operands& ops, int m, int n, int k, const gemm_options* o,
              DeviceInfo* dev, cudaStream_t stream) {
@@ -690,15 +702,8 @@ int launch16(const Plan& p, const Operands& ops, int m, int n, int k, const gemm
             return launch_1cta_cm<kBF16, kAMN, false, 224, 64, stages_for(224, 64)>(p, ops, m, n, k, o, dev, stream);
         return launch_1cta_cm<kBF16, kAMN, false, 256, 64, stages_for(256, 64)>(p, ops, m, n, k, o, dev, stream);
     }
-    if (p.tile_k == 128) {
-        if (bmn) return launch_gemm16_2cta<kBF16, kAMN, true, 256, 128>(ops, m, n, k, o, dev, p, stream);
-        if (p.tile_n == 224)
-            return launch_gemm16_2cta<kBF16, kAMN, false, 224, 128>(ops, m, n, k, o, dev, p, stream);
-        return launch_gemm16_2cta<kBF16, kAMN, false, 256, 128>(ops, m, n, k, o, dev, p, stream);
-    }
-    if (bmn) return launch_gemm16_2cta<kBF16, kAMN, true, 256, 64>(ops, m, n, k, o, dev, p, stream);
-    if (p.tile_n == 224) return launch_gemm16_2cta<kBF16, kAMN, false, 224, 64>(ops, m, n, k, o, dev, p, stream);
-    return launch_gemm16_2cta<kBF16, kAMN, false, 256, 64>(ops, m, n, k, o, dev, p, stream);
+    if (bmn) return launch_pair_width<kBF16, kAMN, true>(p, ops, m, n, k, o, dev, stream);
+    return launch_pair_width<kBF16, kAMN, false>(p, ops, m, n, k, o, dev, stream);
 }
 
 int run(int dtype, const void* A, const void* B, const void* sfA, const void* sfB, void* C,

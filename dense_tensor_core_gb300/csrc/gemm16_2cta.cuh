@@ -35,11 +35,15 @@ constexpr uint64_t kPeerSettleNs = 1000ull * 1000;  // 1 ms
 // NT one 3-D box {64, rows, 2} per operand). A TMA instruction's cost does not grow much with its
 // size, and measured per-SM delivery is highest with the large 3-D boxes: a 128-deep stage feeds
 // the tensor pipe better than two 64-deep ones, although fewer stages fit.
-template <int kBN, int kBK, int kStages>
+// A B stored [K,N] (kBMN) is loaded as 64-column boxes, kBBoxes per CTA; with a 224-wide tile a
+// CTA's 112 columns take two boxes, the second only partly used (the MMA reads 112 columns through
+// the MN-major descriptor), so its stage holds whole boxes.
+template <int kBN, int kBK, int kStages, bool kBMN = false>
 struct Cfg {
     static constexpr int kHalfN = kBN / 2;
+    static constexpr int kBBoxes = (kHalfN + 63) / 64;
     static constexpr int kAStage = kBMc * kBK * 2;
-    static constexpr int kBStage = kHalfN * kBK * 2;
+    static constexpr int kBStage = kBMN ? kBBoxes * 64 * kBK * 2 : kHalfN * kBK * 2;
     static_assert(kBK == 64 || kBK == 128, "K-block of 64 or 128");
     static constexpr int kStageBytes = kAStage + kBStage;
     static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
@@ -53,9 +57,9 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
     gemm16_2cta_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const Gemm16Args args) {
     using namespace g2;
-    using C_ = Cfg<kBN, kBK, kStages>;
+    using C_ = Cfg<kBN, kBK, kStages, kNN>;
     constexpr int kChunks = kBK / 64;  // 128-byte K-chunks per stage
-    static_assert(!kNN || C_::kHalfN % 64 == 0, "NN needs whole 64-column B boxes per CTA");
+    static_assert(!kNN || C_::kHalfN % 16 == 0, "B stored [K,N]: 16-column steps per CTA");
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[kStages];
     __shared__ __align__(8) uint64_t bar_empty[kStages];
@@ -145,7 +149,7 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
                                              b_row);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < C_::kHalfN / 64; ++j)
+                        for (int j = 0; j < C_::kBBoxes; ++j)
                             tma_load_2d_pair(sB + s * C_::kBStage + j * (64 * kBK * 2), &tmB,
                                              full_leader, b_row + j * 64, kb * kBK);
                     }

@@ -93,7 +93,7 @@ def test_one_cta_configurations_full_parity(M, N, K, layout, tile_n, cluster_m, 
     # 128-row tiles, so with clusters of 2 one CTA of the last cluster computes rows past M (loads
     # zeros, stores nothing); K = 200 and 136 end in a partial K-block
     if layout == "NN" and tile_n == 224:
-        pytest.skip("224-wide tiles are offered for NT only")
+        pytest.skip("224-wide one-CTA tiles are offered for a B stored [N,K] only")
     import dense_tensor_core_gb300 as dtc
 
     p = dtc.gemm_plan("bf16", M, N, K, layout, variant=1, tile_n=tile_n, cluster_m=cluster_m,
@@ -153,9 +153,9 @@ def test_automatic_choice_follows_the_cost_model():
 @pytest.mark.parametrize("M,N,K", [(640, 520, 192), (384, 264, 320), (1280, 1792, 1024)])
 def test_pair_kernel_configurations_full_parity(M, N, K, layout, tile_n, tile_k):
     # 128-deep stages load each operand with one 3-D box of two 128-byte K-chunks; K = 192 and
-    # 320 end in a half-filled 128-deep stage; 640 and 384 rows leave a partial pair tile
-    if layout == "NN" and tile_n == 224:
-        pytest.skip("224-wide tiles are offered for NT only")
+    # 320 end in a half-filled 128-deep stage; 640 and 384 rows leave a partial pair tile. With NN
+    # and 224-wide tiles each CTA's 112 columns of B come in two 64-column boxes, the second
+    # partly used
     import dense_tensor_core_gb300 as dtc
 
     p = dtc.gemm_plan("bf16", M, N, K, layout, variant=2, tile_n=tile_n, tile_k=tile_k)
@@ -329,10 +329,10 @@ def test_transposed_layout_plans():
 
     if torch.cuda.get_device_properties(0).multi_processor_count != 152:
         pytest.skip("the expected choices are worked out for 152 SMs")
-    # B stored [N,K] (TT) keeps the 224-wide pair tiles; B stored [K,N] (TN) takes 256
-    p = dtc.gemm_plan("bf16", 4096, 4096, 8192, "TT")
-    assert (p["variant"], p["tile_n"]) == (2, 224)
-    p = dtc.gemm_plan("bf16", 4096, 4096, 8192, "TN")
-    assert (p["variant"], p["tile_n"]) == (2, 256)
+    # 304 pair tiles of 256 x 224 = 4 full waves, whatever the storage of A and B
+    for layout in ("TT", "TN", "NN"):
+        p = dtc.gemm_plan("bf16", 4096, 4096, 8192, layout)
+        assert (p["variant"], p["tile_n"]) == (2, 224), layout
+    # one-CTA 224-wide tiles need B stored [N,K]
     with pytest.raises(dtc.GemmError):
-        dtc.gemm_plan("bf16", 4096, 4096, 8192, "TN", variant=2, tile_n=224)
+        dtc.gemm_plan("bf16", 4096, 4096, 8192, "TN", variant=1, tile_n=224)
