@@ -348,8 +348,15 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
         p->variant = GEMM_VARIANT_1CTA;
         p->tile_m = dtc::gmx::kBM;
         p->tile_n = dtc::gmx::kBN;
-        p->tile_k = dtc::gmx::kBK;
-        p->stages = dtc::gmx::kStages;
+        // 256-deep stages (3-D boxes over 128-byte K-chunks) need K % 128 == 0
+        const int bk_want = o ? o->tile_k : 0;
+        if (bk_want && bk_want != 128 && bk_want != 256)
+            return fail(GEMM_ERR_INVALID_ARG, "tile_k %d is not 128 or 256 for the MXFP8 kernel", bk_want);
+        if (bk_want == 256 && K % 128)
+            return fail(GEMM_ERR_UNSUPPORTED, "256-deep MXFP8 stages need K %% 128 == 0");
+        const bool deep = bk_want ? bk_want == 256 : K % 128 == 0;
+        p->tile_k = deep ? 2 * dtc::gmx::kBK : dtc::gmx::kBK;
+        p->stages = deep ? dtc::gmx::Cfg<true>::kStages : dtc::gmx::Cfg<false>::kStages;
         p->tiles = ceil_div(M, p->tile_m) * ceil_div(N, p->tile_n);
         p->ctas = std::min(p->tiles, d->sms);
         return GEMM_OK;
@@ -648,24 +655,42 @@ int launch_mxfp8_2cta(const Operands& ops, int M, int N, int K, const gemm_optio
     return GEMM_OK;
 }
 
-int launch_mxfp8(const Operands& ops, int M, int N, int K, const gemm_options* o, DeviceInfo* dev,
-                 const Plan& p, cudaStream_t stream) {
-    if (p.variant == GEMM_VARIANT_2CTA) return launch_mxfp8_2cta(ops, M, N, K, o, dev, p, stream);
+template <bool kDeep>
+int launch_mxfp8_1cta(const Operands& ops, int M, int N, int K, const gemm_options* o,
+                      DeviceInfo* dev, const Plan& p, cudaStream_t stream) {
     using namespace dtc::gmx;
+    using C_ = Cfg<kDeep>;
     CUtensorMap tA, tB;
-    int rc = make_tmap(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ops.A, (uint64_t)K, (uint64_t)M,
-                       (uint64_t)ops.lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B, "A");
-    if (rc) return rc;
-    rc = make_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ops.B, (uint64_t)K, (uint64_t)N,
-                   (uint64_t)ops.ldb, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B, "B");
-    if (rc) return rc;
-    auto kern = dtc::gemm_mxfp8_kernel<0>;
-    if ((rc = ensure_smem_attr(kern, kSmemBytes, dev))) return rc;
+    int rc;
+    if (kDeep) {  // one 3-D box {128, rows, 2} per operand and stage (K % 128 == 0)
+        if ((rc = make_tmap_kchunks(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ops.A, (uint64_t)K,
+                                    (uint64_t)M, (uint64_t)ops.lda, kBM, "A")))
+            return rc;
+        if ((rc = make_tmap_kchunks(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ops.B, (uint64_t)K,
+                                    (uint64_t)N, (uint64_t)ops.ldb, kBN, "B")))
+            return rc;
+    } else {
+        if ((rc = make_tmap(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ops.A, (uint64_t)K, (uint64_t)M,
+                            (uint64_t)ops.lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B, "A")))
+            return rc;
+        if ((rc = make_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ops.B, (uint64_t)K, (uint64_t)N,
+                            (uint64_t)ops.ldb, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B, "B")))
+            return rc;
+    }
+    auto kern = dtc::gemm_mxfp8_kernel<kDeep>;
+    if ((rc = ensure_smem_attr(kern, C_::kSmemBytes, dev))) return rc;
     const dtc::GemmMxArgs a = mx_args(ops, M, N, K, kBM, kBN, kBK, o);
-    kern<<<p.ctas, kThreads, kSmemBytes, stream>>>(tA, tB, a);
+    kern<<<p.ctas, kThreads, C_::kSmemBytes, stream>>>(tA, tB, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "MXFP8 kernel launch");
     return GEMM_OK;
+}
+
+int launch_mxfp8(const Operands& ops, int M, int N, int K, const gemm_options* o, DeviceInfo* dev,
+                 const Plan& p, cudaStream_t stream) {
+    if (p.variant == GEMM_VARIANT_2CTA) return launch_mxfp8_2cta(ops, M, N, K, o, dev, p, stream);
+    if (p.tile_k == 2 * dtc::gmx::kBK) return launch_mxfp8_1cta<true>(ops, M, N, K, o, dev, p, stream);
+    return launch_mxfp8_1cta<false>(ops, M, N, K, o, dev, p, stream);
 }
 
 template <bool kBF16, bool kAMN, bool kNN>

@@ -7,9 +7,11 @@
 // tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X, M = 128, N = 224, K = 32.
 //
 // The instruction takes one scale per row per 32 K-elements. With granularity 128 the four MMAs
-// of a 128-deep K-block all use the same scales, so the K-block is also the pipeline stage:
-// 128 e4m3 = 128 bytes per row = one 128-byte swizzle row, and the shared-memory descriptors are
-// those of the bf16 kernels (32 bytes per MMA step).
+// of a 128-deep K-block all use the same scales. A K-block of 128 e4m3 = 128 bytes per row = one
+// 128-byte swizzle row, and the shared-memory descriptors are those of the bf16 kernels (32 bytes
+// per MMA step). A pipeline stage is one K-block (2-D boxes, any K) or, with kDeep, two (one 3-D
+// box {128, rows, 2} per operand, K % 128 == 0): the larger TMA instructions stream faster per SM,
+// though only two 88 KB stages fit.
 //
 // Scales live in Tensor Memory. For an operand of R rows (128 for A, 224 for B) they take R/32
 // columns: row r sits in lane r % 32 of column r / 32, repeated in each of the four 32-lane
@@ -47,12 +49,7 @@ namespace gmx {
 constexpr int kBM = 128;
 constexpr int kBN = 224;
 constexpr int kBK = 128;  // e4m3 elements (= bytes) per K-block, one 128-byte swizzle row
-constexpr int kStages = 4;
 constexpr int kThreads = 320;
-constexpr int kAStage = kBM * kBK;
-constexpr int kBStage = kBN * kBK;
-constexpr int kStageBytes = kAStage + kBStage;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024;
 constexpr int kTmemCols = 512;
 constexpr int kAccStride = 224;
 constexpr int kSfBase = 448;   // first scale column
@@ -61,8 +58,20 @@ constexpr int kSfSets = 4;     // scale sets in flight
 constexpr int kGroup = 4;      // K-blocks per scale set (one byte each per 32-bit cell)
 constexpr int kGroupM = 8;
 constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
-static_assert(kSmemBytes <= 227 * 1024 - 256, "shared memory budget");
 static_assert(kSfBase + kSfSets * kSfSet <= kTmemCols, "Tensor Memory budget");
+
+// Stage geometry: kBlocks K-blocks per stage (1: 2-D boxes, 4 stages; 2: 3-D boxes, 2 stages).
+template <bool kDeep>
+struct Cfg {
+    static constexpr int kBlocks = kDeep ? 2 : 1;
+    static constexpr int kStages = kDeep ? 2 : 4;
+    static constexpr int kAStage = kBM * kBK * kBlocks;
+    static constexpr int kBStage = kBN * kBK * kBlocks;
+    static constexpr int kStageBytes = kAStage + kBStage;
+    static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+    static_assert(kSmemBytes <= 227 * 1024 - 256, "shared memory budget");
+    static_assert(kGroup % kBlocks == 0, "a scale group is whole stages");
+};
 }  // namespace gmx
 
 // Scale word of row `row` for K-block group g: the E8M0 bytes of K-blocks 4g..4g+3 (byte j =
@@ -81,11 +90,16 @@ __device__ __forceinline__ uint32_t sf_word(const uint8_t* sf, int rows, int col
     return w;
 }
 
-template <int kUnused = 0>
+template <bool kDeep>
 __global__ void __launch_bounds__(gmx::kThreads, 1)
     gemm_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const GemmMxArgs args) {
     using namespace gmx;
+    using C_ = Cfg<kDeep>;
+    constexpr int kStages = C_::kStages;
+    constexpr int kAStage = C_::kAStage;
+    constexpr int kBStage = C_::kBStage;
+    constexpr int kBlocks = C_::kBlocks;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[kStages];
     __shared__ __align__(8) uint64_t bar_empty[kStages];
@@ -104,6 +118,7 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int total = args.num_m * args.num_n;
     const int groups = (args.num_kb + kGroup - 1) / kGroup;
+    const int num_st = (args.num_kb + kBlocks - 1) / kBlocks;  // stages per tile
     volatile int* abort = &abort_flag;
 
     if (threadIdx.x == 0) {
@@ -145,7 +160,7 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 int mt, nt;
                 tile_coords(t, args.num_m, args.num_n, kGroupM, mt, nt);
-                for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
+                for (int st = 0; st < num_st; ++st, ++it) {
                     const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
                     if (!wait_bounded(smem_u32(&bar_empty[s]), ph ^ 1u, abort, args.timeout_ns,
                                       &g_dtc_status, 31)) {
@@ -154,9 +169,14 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
                     }
                     if (args.fault == 1 && it == 0) continue;  // test hook: stage never filled
                     const uint32_t full = smem_u32(&bar_full[s]);
-                    mbar_arrive_expect_tx(full, kStageBytes);
-                    tma_load_2d(sA + s * kAStage, &tmA, full, kb * kBK, mt * kBM);
-                    tma_load_2d(sB + s * kBStage, &tmB, full, kb * kBK, nt * kBN);
+                    mbar_arrive_expect_tx(full, C_::kStageBytes);
+                    if constexpr (kDeep) {
+                        tma_load_3d(sA + s * kAStage, &tmA, full, 0, mt * kBM, st * 2);
+                        tma_load_3d(sB + s * kBStage, &tmB, full, 0, nt * kBN, st * 2);
+                    } else {
+                        tma_load_2d(sA + s * kAStage, &tmA, full, st * kBK, mt * kBM);
+                        tma_load_2d(sB + s * kBStage, &tmB, full, st * kBK, nt * kBN);
+                    }
                 }
             }
             if (!ok) {
@@ -182,9 +202,10 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * kAccStride;
-                for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
+                for (int st = 0; st < num_st; ++st, ++it) {
+                    const int kb0 = st * kBlocks;  // first K-block of the stage
                     const uint32_t set = sit % kSfSets;
-                    if (kb % kGroup == 0) {
+                    if (kb0 % kGroup == 0) {
                         if (!wait_bounded(smem_u32(&bar_sfull[set]), (sit / kSfSets) & 1u, abort,
                                           args.timeout_ns, &g_dtc_status, 35)) {
                             ok = false;
@@ -198,21 +219,29 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t a0 = sA + s * kAStage, b0 = sB + s * kBStage;
-                    const uint32_t sf_id = (uint32_t)(kb % kGroup);
-                    const uint32_t idesc = idesc0 | (sf_id << 4) | (sf_id << 29);
                     const uint32_t sfa = tmem_base + kSfBase + set * kSfSet;
                     const uint32_t sfb = sfa + 4;
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 32; ++kk) {
-                        const uint64_t adesc = smem_desc_sw128(a0 + kk * 32, 16, 1024);
-                        const uint64_t bdesc = smem_desc_sw128(b0 + kk * 32, 16, 1024);
-                        mma_mxf8_cta1(d_tmem, adesc, bdesc, idesc, sfa, sfb,
-                                      (kb | kk) != 0 ? 1u : 0u);
+                    for (int h = 0; h < kBlocks; ++h) {
+                        const int kb = kb0 + h;
+                        if (kb >= args.num_kb) break;  // a K-block past K: zero-filled, skipped
+                        // K-block h of the stage: 128-byte chunk h of each operand's box
+                        const uint32_t a0 = sA + s * kAStage + h * (kBM * kBK);
+                        const uint32_t b0 = sB + s * kBStage + h * (kBN * kBK);
+                        const uint32_t sf_id = (uint32_t)(kb % kGroup);
+                        const uint32_t idesc = idesc0 | (sf_id << 4) | (sf_id << 29);
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 32; ++kk) {
+                            const uint64_t adesc = smem_desc_sw128(a0 + kk * 32, 16, 1024);
+                            const uint64_t bdesc = smem_desc_sw128(b0 + kk * 32, 16, 1024);
+                            mma_mxf8_cta1(d_tmem, adesc, bdesc, idesc, sfa, sfb,
+                                          (kb | kk) != 0 ? 1u : 0u);
+                        }
                     }
                     issued = true;
                     mma_commit_cta1(smem_u32(&bar_empty[s]));
-                    if (kb % kGroup == kGroup - 1 || kb == args.num_kb - 1) {
+                    const int kb_last = kb0 + kBlocks - 1;
+                    if (kb_last % kGroup == kGroup - 1 || kb_last >= args.num_kb - 1) {
                         mma_commit_cta1(smem_u32(&bar_sempty[set]));  // scale set consumed
                         ++sit;
                     }

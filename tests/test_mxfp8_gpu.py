@@ -46,17 +46,25 @@ def check_mx(A, B, sfA, sfB, what, **kw):
     return check_close(values16(C, "bf16"), values16(ref, "bf16"), what)
 
 
+@pytest.mark.parametrize("tile_k", [128, 256])
 @pytest.mark.parametrize("M,N,K", [
     (128, 224, 128),    # one tile, one K-block, one scale group
     (256, 448, 1024),   # 4 tiles, 8 K-blocks = 2 scale groups
+    (256, 448, 384),    # 3 K-blocks: with 256-deep stages the last stage is half past K
     (300, 520, 400),    # ragged M and N; K = 3 K-blocks + 16 (partial block and group)
     (1, 8, 16),         # smallest legal product
     (129, 232, 656),    # a row / 8 columns past a tile; 6 K-blocks (one partial group)
     (640, 896, 2048),   # 20 tiles, 16 K-blocks
 ])
-def test_small_shapes_full_parity(M, N, K):
+def test_small_shapes_full_parity(M, N, K, tile_k):
+    # 128-deep stages (2-D boxes, any K) or 256-deep ones (3-D boxes of two K-blocks, K % 128 == 0)
+    if tile_k == 256 and K % 128:
+        pytest.skip("256-deep stages need K % 128 == 0")
+    import dense_tensor_core_gb300 as dtc
+
+    assert dtc.gemm_plan("mxfp8", M, N, K, variant=1, tile_k=tile_k)["tile_k"] == tile_k
     A, B, sfA, sfB = workloads.make_mxfp8(M, N, K, seed=M + N + K)
-    check_mx(A, B, sfA, sfB, f"mxfp8 {M}x{N}x{K}", variant=1)
+    check_mx(A, B, sfA, sfB, f"mxfp8 {M}x{N}x{K} tile_k {tile_k}", variant=1, tile_k=tile_k)
 
 
 @pytest.mark.parametrize("M,N,K", [
@@ -81,9 +89,9 @@ def test_unit_scales_reduce_to_plain_e4m3():
     check_mx(A, B, np.full_like(sfA, 127), np.full_like(sfB, 127), "unit scales")
 
 
-@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("variant,tile_k", [(1, 128), (1, 256), (2, 0)])
 @pytest.mark.parametrize("which", ["a_rows", "b_rows", "k_blocks"])
-def test_scales_varying_along_one_axis(which, variant):
+def test_scales_varying_along_one_axis(which, variant, tile_k):
     # Scales that vary along a single axis: a wrong row / column / K-block mapping of the scale
     # layout in Tensor Memory shows up as a failure of exactly one of these.
     M, N, K = 256, 448, 1024
@@ -98,7 +106,7 @@ def test_scales_varying_along_one_axis(which, variant):
     else:
         sfA[:] = (123 + (np.arange(kb) % 7))[None, :]
         sfB[:] = (130 - (np.arange(kb) % 5))[None, :]
-    check_mx(A, B, sfA, sfB, f"scales along {which}", variant=variant)
+    check_mx(A, B, sfA, sfB, f"scales along {which}", variant=variant, tile_k=tile_k)
 
 
 def test_wide_scale_range():
@@ -119,11 +127,11 @@ def test_more_tiles_than_sms(variant):
     check_mx(A, B, sfA, sfB, "more tiles than SMs", variant=variant)
 
 
-@pytest.mark.parametrize("variant", [0, 1, 2])
-def test_benchmark_size_sampled(variant):
+@pytest.mark.parametrize("variant,tile_k", [(0, 0), (1, 128), (1, 256), (2, 0)])
+def test_benchmark_size_sampled(variant, tile_k):
     w = workloads.WORKLOADS["mxfp8_nt_4096x4096x8192"]
     A, B, sfA, sfB = _bench_inputs()
-    C = run_mx(A, B, sfA, sfB, variant=variant)
+    C = run_mx(A, B, sfA, sfB, variant=variant, tile_k=tile_k)
     r, c = sample_positions(w.M, w.N, count=3000, seed=w.seed, tile_m=128, tile_n=224)
     r = np.concatenate([r, np.full(w.N, 1000), np.arange(w.M)])
     c = np.concatenate([c, np.arange(w.N), np.full(w.M, 999)])
@@ -145,7 +153,7 @@ def test_k_zero_and_empty():
 
 
 @pytest.mark.parametrize("variant", [1, 2])
-def test_timeout_reports_and_recovers(variant):
+def test_timeout_reports_and_recovers(variant):  # (variant 1 takes 256-deep stages: K = 512)
     import dense_tensor_core_gb300 as dtc
 
     M, N, K = 256, 448, 512
@@ -164,8 +172,11 @@ def test_automatic_choice():
 
     if torch.cuda.get_device_properties(0).multi_processor_count != 152:
         pytest.skip("the expected choices are worked out for 152 SMs")
-    # the pair kernel is an option (variant 2); the one-CTA kernel measured faster
-    assert dtc.gemm_plan("mxfp8", 4096, 4096, 8192)["variant"] == 1
+    # the pair kernel is an option (variant 2); the one-CTA kernel measured faster, with 256-deep
+    # stages when K % 128 == 0
+    p = dtc.gemm_plan("mxfp8", 4096, 4096, 8192)
+    assert (p["variant"], p["tile_k"]) == (1, 256)
+    assert dtc.gemm_plan("mxfp8", 4096, 4096, 8208)["tile_k"] == 128
     assert dtc.gemm_plan("mxfp8", 4096, 4096, 8192, variant=2)["variant"] == 2
     with pytest.raises(dtc.GemmError):
         dtc.gemm_plan("mxfp8", 4096, 4096, 8208, variant=2)  # the pair kernel needs K % 128 == 0
