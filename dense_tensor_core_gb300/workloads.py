@@ -84,26 +84,38 @@ def make16(kind: str, layout: str, M: int, N: int, K: int, seed: int):
     return A, B
 
 
-def make_mxfp8(M: int, N: int, K: int, seed: int):
-    """(A [M,K] e4m3, B [N,K] e4m3, sfA [M,kb] E8M0, sfB [N,kb] E8M0) as uint8 codes."""
+_TORCH_8 = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+
+
+def make_mx(M: int, N: int, K: int, seed: int, a_fmt: str = "e4m3", b_fmt: str = "e4m3",
+            block: int = SF_BLOCK):
+    """(A [M,K], B [N,K], sfA [M,kb], sfB [N,kb]) as uint8 codes: fp8 elements (e4m3 or e5m2) and
+    E8M0 scales, one per row per `block` K-elements (kb = ceil(K/block)). Element = fp8(x / 2^u)
+    with x ~ N(0,1) and u uniform in {-3..3} per (row, block); scale = 127 + u."""
     g = torch.Generator().manual_seed(seed)
-    kb = (K + SF_BLOCK - 1) // SF_BLOCK
+    kb = (K + block - 1) // block
     xa = torch.randn((M, K), generator=g, dtype=torch.float32)
     xb = torch.randn((N, K), generator=g, dtype=torch.float32)
     ua = torch.randint(-3, 4, (M, kb), generator=g, dtype=torch.int32)
     ub = torch.randint(-3, 4, (N, kb), generator=g, dtype=torch.int32)
 
-    def quantise(x, u):
+    def quantise(x, u, fmt):
         # per-element exponent of its (row, K-block); dividing by a power of two is exact in fp32
-        ue = u.repeat_interleave(SF_BLOCK, dim=1)[:, : x.shape[1]]
-        q = torch.ldexp(x, -ue.to(torch.float32)).to(torch.float8_e4m3fn)
+        ue = u.repeat_interleave(block, dim=1)[:, : x.shape[1]]
+        q = torch.ldexp(x, -ue.to(torch.float32)).to(_TORCH_8[fmt])
         return q.view(torch.uint8).numpy()
 
-    A = quantise(xa, ua)
-    B = quantise(xb, ub)
+    A = quantise(xa, ua, a_fmt)
+    B = quantise(xb, ub, b_fmt)
     sfA = (ua + 127).to(torch.uint8).numpy()
     sfB = (ub + 127).to(torch.uint8).numpy()
     return A, B, sfA, sfB
+
+
+def make_mxfp8(M: int, N: int, K: int, seed: int):
+    """(A [M,K] e4m3, B [N,K] e4m3, sfA [M,kb] E8M0, sfB [N,kb] E8M0) as uint8 codes, kb =
+    ceil(K/128)."""
+    return make_mx(M, N, K, seed)
 
 
 def make(w: Workload):

@@ -38,6 +38,8 @@ def _bind(path):
     L.dtc_oracle_dec_f16.argtypes = [ctypes.c_uint16]
     L.dtc_oracle_dec_e4m3.restype = ctypes.c_double
     L.dtc_oracle_dec_e4m3.argtypes = [ctypes.c_uint8]
+    L.dtc_oracle_dec_e5m2.restype = ctypes.c_double
+    L.dtc_oracle_dec_e5m2.argtypes = [ctypes.c_uint8]
     L.dtc_oracle_dec_e8m0.restype = ctypes.c_double
     L.dtc_oracle_dec_e8m0.argtypes = [ctypes.c_uint8]
     L.dtc_oracle_enc_bf16.restype = ctypes.c_uint16
@@ -56,6 +58,12 @@ def _bind(path):
     L.dtc_oracle_gemm_mxfp8_sampled.restype = ctypes.c_int
     L.dtc_oracle_gemm_mxfp8_sampled.argtypes = [u8p, u8p, u8p, u8p, i64, i64, i64, i64p,
                                                 i64p, i64, u16p, dp]
+    L.dtc_oracle_gemm_mx.restype = ctypes.c_int
+    L.dtc_oracle_gemm_mx.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, u8p, u8p, u8p, u8p,
+                                     i64, i64, i64, u16p, dp, ctypes.c_int]
+    L.dtc_oracle_gemm_mx_sampled.restype = ctypes.c_int
+    L.dtc_oracle_gemm_mx_sampled.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, u8p, u8p,
+                                             u8p, u8p, i64, i64, i64, i64p, i64p, i64, u16p, dp]
     L.dtc_oracle_default_threads.restype = ctypes.c_int
     return L
 
@@ -121,6 +129,11 @@ def dec_f16(codes):
 
 def dec_e4m3(codes):
     f = _L().dtc_oracle_dec_e4m3
+    return np.array([f(int(c)) for c in np.asarray(codes, dtype=np.uint8).ravel()])
+
+
+def dec_e5m2(codes):
+    f = _L().dtc_oracle_dec_e5m2
     return np.array([f(int(c)) for c in np.asarray(codes, dtype=np.uint8).ravel()])
 
 
@@ -211,4 +224,52 @@ def gemm_mxfp8_sampled(A, B, sfA, sfB, M, N, K, rows, cols):
                                              _ptr(C, ctypes.c_uint16), _ptr(S, ctypes.c_double))
     if rc != 0:
         raise ValueError("oracle gemm_mxfp8_sampled rejected its arguments")
+    return C, S
+
+
+FP8_FORMATS = {"e4m3": 0, "e5m2": 1}
+
+
+def _mx_inputs(A, B, sfA, sfB, M, N, K, block):
+    A = np.ascontiguousarray(A, dtype=np.uint8)
+    B = np.ascontiguousarray(B, dtype=np.uint8)
+    sfA = np.ascontiguousarray(sfA, dtype=np.uint8)
+    sfB = np.ascontiguousarray(sfB, dtype=np.uint8)
+    kb = (K + block - 1) // block
+    assert A.size == M * K and B.size == N * K and sfA.size == M * kb and sfB.size == N * kb
+    return A, B, sfA, sfB
+
+
+def gemm_mx(A, B, sfA, sfB, M, N, K, *, a_fmt="e4m3", b_fmt="e4m3", block=128, sums=False,
+            nthreads=None):
+    """Block-scaled fp8 GEMM, NT: A [M,K] and B [N,K] as e4m3 or e5m2 codes, scales
+    [rows, ceil(K/block)] E8M0 codes with block 128 or 32. Output bf16 codes."""
+    A, B, sfA, sfB = _mx_inputs(A, B, sfA, sfB, M, N, K, block)
+    C = np.zeros((M, N), dtype=np.uint16)
+    S = np.zeros((M, N), dtype=np.float64) if sums else None
+    rc = _L().dtc_oracle_gemm_mx(FP8_FORMATS[a_fmt], FP8_FORMATS[b_fmt], block,
+                                  _ptr(A, ctypes.c_uint8), _ptr(B, ctypes.c_uint8),
+                                  _ptr(sfA, ctypes.c_uint8), _ptr(sfB, ctypes.c_uint8), M, N, K,
+                                  _ptr(C, ctypes.c_uint16), _ptr(S, ctypes.c_double),
+                                  nthreads or threads())
+    if rc != 0:
+        raise ValueError("oracle gemm_mx rejected its arguments")
+    return (C, S) if sums else C
+
+
+def gemm_mx_sampled(A, B, sfA, sfB, M, N, K, rows, cols, *, a_fmt="e4m3", b_fmt="e4m3",
+                    block=128):
+    A, B, sfA, sfB = _mx_inputs(A, B, sfA, sfB, M, N, K, block)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    C = np.zeros(rows.size, dtype=np.uint16)
+    S = np.zeros(rows.size, dtype=np.float64)
+    rc = _L().dtc_oracle_gemm_mx_sampled(FP8_FORMATS[a_fmt], FP8_FORMATS[b_fmt], block,
+                                          _ptr(A, ctypes.c_uint8), _ptr(B, ctypes.c_uint8),
+                                          _ptr(sfA, ctypes.c_uint8), _ptr(sfB, ctypes.c_uint8),
+                                          M, N, K, _ptr(rows, ctypes.c_int64),
+                                          _ptr(cols, ctypes.c_int64), rows.size,
+                                          _ptr(C, ctypes.c_uint16), _ptr(S, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle gemm_mx_sampled rejected its arguments")
     return C, S

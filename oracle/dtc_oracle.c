@@ -26,6 +26,10 @@
  *   gemm_blockscaled with sf_a_granularity_k = sf_b_granularity_k = 128):
  *     C[m,n] = round_bf16( sum_k  e4m3(A[m,k]) * 2^(sfA[m,k/128]-127)
  *                               * e4m3(B[n,k]) * 2^(sfB[n,k/128]-127) )
+ *   and the "other block-scaled formats" of the same section read as the OCP MX family the
+ *   instruction supports: each operand e4m3 or e5m2, and scale blocks of g = 128 or 32
+ *   K-elements (the OCP MX block size), scales [rows, ceil(K/g)]:
+ *     C[m,n] = round_bf16( sum_k  fa(A[m,k]) * 2^(sfA[m,k/g]-127) * fb(B[n,k]) * 2^(sfB[n,k/g]-127) )
  *
  * Accumulation is in double. Every product of two bf16/fp16/e4m3 values, times powers of two
  * from the scales, is exact in double; only the sum carries rounding error, which for the
@@ -38,6 +42,8 @@
  *   fp16  : IEEE binary16 (1, 5, 10; bias 15; subnormals; exponent 31 = inf/NaN).
  *   e4m3  : OCP FP8 E4M3 "fn" variant (1, 4, 3; bias 7; no infinities; S.1111.111 = NaN;
  *           largest finite 448; subnormals m/8 * 2^-6).
+ *   e5m2  : OCP FP8 E5M2 (1, 5, 2; bias 15; exponent 31 = inf (m = 0) / NaN; subnormals
+ *           m/4 * 2^-14; largest finite 57344).
  *   E8M0  : unsigned 8-bit exponent, value 2^(e-127); 0xFF = NaN.
  *
  * Degenerate sizes: M == 0 or N == 0 computes nothing; K == 0 gives the empty sum, +0.
@@ -102,6 +108,21 @@ double dtc_oracle_dec_e4m3(uint8_t b) {
         v = ldexp((double)m, -9); /* subnormal: m/8 * 2^-6 */
     } else {
         v = ldexp((double)(8 + m), e - 10); /* (1 + m/8) * 2^(e-7) */
+    }
+    return sign ? -v : v;
+}
+
+double dtc_oracle_dec_e5m2(uint8_t b) {
+    int sign = (b >> 7) & 1;
+    int e = (b >> 2) & 0x1f;
+    int m = b & 0x3;
+    double v;
+    if (e == 31) {
+        v = (m == 0) ? INFINITY : NAN;
+    } else if (e == 0) {
+        v = ldexp((double)m, -16); /* subnormal: m/4 * 2^-14 */
+    } else {
+        v = ldexp((double)(4 + m), e - 17); /* (1 + m/4) * 2^(e-15) */
     }
     return sign ? -v : v;
 }
@@ -280,31 +301,41 @@ int dtc_oracle_gemm16_sampled(int dtype, int layout, const uint16_t* A, const ui
 }
 
 /* ------------------------------------------------------------------------------------------ */
-/* MXFP8 block-scaled GEMM (NT: A [M,K], B [N,K], scales [rows, ceil(K/128)])                   */
+/* Block-scaled fp8 GEMM (NT: A [M,K], B [N,K], scales [rows, ceil(K/g)] E8M0)                   */
 /* ------------------------------------------------------------------------------------------ */
 
-#define DTC_ORACLE_SF_BLOCK 128
+#define DTC_ORACLE_E4M3 0
+#define DTC_ORACLE_E5M2 1
 
-/* Decode one operand with its scales applied: out[r][k] = e4m3(X[r,k]) * 2^(sf[r,k/128]-127).
+static double dec_fp8(int fmt, uint8_t b) {
+    return fmt == DTC_ORACLE_E5M2 ? dtc_oracle_dec_e5m2(b) : dtc_oracle_dec_e4m3(b);
+}
+
+static int mx_args_ok(int fmt_a, int fmt_b, int block) {
+    return (fmt_a == DTC_ORACLE_E4M3 || fmt_a == DTC_ORACLE_E5M2) &&
+           (fmt_b == DTC_ORACLE_E4M3 || fmt_b == DTC_ORACLE_E5M2) && (block == 32 || block == 128);
+}
+
+/* Decode one operand with its scales applied: out[r][k] = fp8(X[r,k]) * 2^(sf[r,k/g]-127).
  * Exact in double. */
-static double* decode_scaled(const uint8_t* X, const uint8_t* sf, int64_t R, int64_t K) {
-    int64_t kb = (K + DTC_ORACLE_SF_BLOCK - 1) / DTC_ORACLE_SF_BLOCK;
+static double* decode_scaled(int fmt, int block, const uint8_t* X, const uint8_t* sf, int64_t R,
+                             int64_t K) {
+    int64_t kb = (K + block - 1) / block;
     double* out = (double*)malloc(sizeof(double) * (size_t)(R * K > 0 ? R * K : 1));
     if (!out) return NULL;
     for (int64_t r = 0; r < R; ++r)
         for (int64_t k = 0; k < K; ++k)
-            out[r * K + k] = dtc_oracle_dec_e4m3(X[r * K + k]) *
-                             dtc_oracle_dec_e8m0(sf[r * kb + k / DTC_ORACLE_SF_BLOCK]);
+            out[r * K + k] = dec_fp8(fmt, X[r * K + k]) * dtc_oracle_dec_e8m0(sf[r * kb + k / block]);
     return out;
 }
 
-int dtc_oracle_gemm_mxfp8(const uint8_t* A, const uint8_t* B, const uint8_t* sfA,
-                          const uint8_t* sfB, int64_t M, int64_t N, int64_t K, uint16_t* C,
-                          double* S, int nthreads) {
-    if (M < 0 || N < 0 || K < 0) return -1;
+int dtc_oracle_gemm_mx(int fmt_a, int fmt_b, int block, const uint8_t* A, const uint8_t* B,
+                       const uint8_t* sfA, const uint8_t* sfB, int64_t M, int64_t N, int64_t K,
+                       uint16_t* C, double* S, int nthreads) {
+    if (M < 0 || N < 0 || K < 0 || !mx_args_ok(fmt_a, fmt_b, block)) return -1;
     if (M == 0 || N == 0) return 0;
-    double* a = decode_scaled(A, sfA, M, K);
-    double* bt = decode_scaled(B, sfB, N, K);
+    double* a = decode_scaled(fmt_a, block, A, sfA, M, K);
+    double* bt = decode_scaled(fmt_b, block, B, sfB, N, K);
     if (!a || !bt) {
         free(a);
         free(bt);
@@ -317,27 +348,41 @@ int dtc_oracle_gemm_mxfp8(const uint8_t* A, const uint8_t* B, const uint8_t* sfA
     return 0;
 }
 
-int dtc_oracle_gemm_mxfp8_sampled(const uint8_t* A, const uint8_t* B, const uint8_t* sfA,
-                                  const uint8_t* sfB, int64_t M, int64_t N, int64_t K,
-                                  const int64_t* rows, const int64_t* cols, int64_t count,
-                                  uint16_t* Cout, double* Sout) {
-    if (M < 0 || N < 0 || K < 0 || count < 0) return -1;
-    int64_t kb = (K + DTC_ORACLE_SF_BLOCK - 1) / DTC_ORACLE_SF_BLOCK;
+int dtc_oracle_gemm_mx_sampled(int fmt_a, int fmt_b, int block, const uint8_t* A,
+                               const uint8_t* B, const uint8_t* sfA, const uint8_t* sfB, int64_t M,
+                               int64_t N, int64_t K, const int64_t* rows, const int64_t* cols,
+                               int64_t count, uint16_t* Cout, double* Sout) {
+    if (M < 0 || N < 0 || K < 0 || count < 0 || !mx_args_ok(fmt_a, fmt_b, block)) return -1;
+    int64_t kb = (K + block - 1) / block;
     for (int64_t i = 0; i < count; ++i) {
         int64_t m = rows[i], n = cols[i];
         if (m < 0 || m >= M || n < 0 || n >= N) return -1;
         double acc = 0.0;
         for (int64_t k = 0; k < K; ++k) {
-            double av = dtc_oracle_dec_e4m3(A[m * K + k]) *
-                        dtc_oracle_dec_e8m0(sfA[m * kb + k / DTC_ORACLE_SF_BLOCK]);
-            double bv = dtc_oracle_dec_e4m3(B[n * K + k]) *
-                        dtc_oracle_dec_e8m0(sfB[n * kb + k / DTC_ORACLE_SF_BLOCK]);
+            double av = dec_fp8(fmt_a, A[m * K + k]) * dtc_oracle_dec_e8m0(sfA[m * kb + k / block]);
+            double bv = dec_fp8(fmt_b, B[n * K + k]) * dtc_oracle_dec_e8m0(sfB[n * kb + k / block]);
             acc += av * bv;
         }
         if (Sout) Sout[i] = acc;
         if (Cout) Cout[i] = dtc_oracle_enc_bf16(acc);
     }
     return 0;
+}
+
+/* The pages' MXFP8 product: e4m3 x e4m3, scale blocks of 128. */
+int dtc_oracle_gemm_mxfp8(const uint8_t* A, const uint8_t* B, const uint8_t* sfA,
+                          const uint8_t* sfB, int64_t M, int64_t N, int64_t K, uint16_t* C,
+                          double* S, int nthreads) {
+    return dtc_oracle_gemm_mx(DTC_ORACLE_E4M3, DTC_ORACLE_E4M3, 128, A, B, sfA, sfB, M, N, K, C,
+                              S, nthreads);
+}
+
+int dtc_oracle_gemm_mxfp8_sampled(const uint8_t* A, const uint8_t* B, const uint8_t* sfA,
+                                  const uint8_t* sfB, int64_t M, int64_t N, int64_t K,
+                                  const int64_t* rows, const int64_t* cols, int64_t count,
+                                  uint16_t* Cout, double* Sout) {
+    return dtc_oracle_gemm_mx_sampled(DTC_ORACLE_E4M3, DTC_ORACLE_E4M3, 128, A, B, sfA, sfB, M, N,
+                                      K, rows, cols, count, Cout, Sout);
 }
 
 /* Host cores this process may use (what the oracle's default thread count is based on). */

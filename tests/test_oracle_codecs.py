@@ -47,6 +47,18 @@ def test_dec_e4m3_all_codes():
     assert [c for c in range(256) if math.isnan(got[c])] == [0x7F, 0xFF]
 
 
+def test_dec_e5m2_all_codes():
+    codes = np.arange(256, dtype=np.uint16).astype(np.uint8)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e5m2).to(torch.float64).numpy()
+    got = oracle.dec_e5m2(codes)
+    _same(got, ref)
+    # landmarks: largest finite 57344, smallest subnormal 2^-16, 1.0 = 0x3C, inf at exponent 31
+    # with a zero fraction, NaN with a non-zero one
+    assert got[0x7B] == 57344.0 and got[0x01] == 2.0 ** -16 and got[0x3C] == 1.0
+    assert got[0x7C] == math.inf and got[0xFC] == -math.inf
+    assert [c for c in range(256) if math.isnan(got[c])] == [0x7D, 0x7E, 0x7F, 0xFD, 0xFE, 0xFF]
+
+
 def test_dec_e8m0_all_codes():
     codes = np.arange(256, dtype=np.uint16).astype(np.uint8)
     got = oracle.dec_e8m0(codes)

@@ -269,6 +269,66 @@ def test_mxfp8_per_block_scales_equal_premultiplied_operands(K):
     assert np.array_equal(Cs, C.ravel()) and np.array_equal(Ss, S.ravel())
 
 
+# --- other block-scaled formats: e5m2 elements, 32-element scale blocks ----------------------------
+
+def _fp8_values(codes, fmt):
+    dt = torch.float8_e4m3fn if fmt == "e4m3" else torch.float8_e5m2
+    return torch.from_numpy(np.ascontiguousarray(codes)).view(dt).to(torch.float64)
+
+
+def test_golden_mx_block32_e5m2():
+    g = read_golden("mx_1x2_k64_e4m3_e5m2_block32.txt")
+    M, N, K = 1, 2, 64
+    A = np.zeros((M, K), np.uint8)
+    B = np.zeros((N, K), np.uint8)
+    for r, k, c in g["A_nz"]:
+        A[int(r), int(k)] = int(c, 16)
+    for r, k, c in g["B_nz"]:
+        B[int(r), int(k)] = int(c, 16)
+    sfA = np.array(g["sfA"], dtype=np.uint8)
+    sfB = np.array(g["sfB"], dtype=np.uint8)
+    C, S = oracle.gemm_mx(A, B, sfA, sfB, M, N, K, a_fmt="e4m3", b_fmt="e5m2", block=32, sums=True)
+    assert np.array_equal(S, matrix(g["C"]))
+    assert np.array_equal(values_of(C, "bf16"), matrix(g["C"]))
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", [("e5m2", "e5m2"), ("e4m3", "e5m2"), ("e5m2", "e4m3")])
+@pytest.mark.parametrize("block", [32, 128])
+@pytest.mark.parametrize("K", [256, 200, 8])  # whole blocks, a partial last block, K < 32
+def test_mx_per_block_scales_equal_premultiplied_operands(a_fmt, b_fmt, block, K):
+    # an independent routine: torch float64 matmul on torch-decoded, scaled operands
+    M, N = 22, 18
+    A, B, sfA, sfB = workloads.make_mx(M, N, K, 54, a_fmt, b_fmt, block)
+    C, S = oracle.gemm_mx(A, B, sfA, sfB, M, N, K, a_fmt=a_fmt, b_fmt=b_fmt, block=block, sums=True)
+    kidx = torch.arange(K) // block
+    sa = torch.from_numpy(sfA.astype(np.float64))[:, kidx] - 127
+    sb = torch.from_numpy(sfB.astype(np.float64))[:, kidx] - 127
+    ref = ((_fp8_values(A, a_fmt) * torch.pow(2.0, sa)) @ (_fp8_values(B, b_fmt) * torch.pow(2.0, sb)).T).numpy()
+    assert np.allclose(S, ref, rtol=1e-12, atol=1e-12)
+    r = np.arange(M).repeat(N)
+    c = np.tile(np.arange(N), M)
+    Cs, Ss = oracle.gemm_mx_sampled(A, B, sfA, sfB, M, N, K, r, c, a_fmt=a_fmt, b_fmt=b_fmt,
+                                    block=block)
+    assert np.array_equal(Cs, C.ravel()) and np.array_equal(Ss, S.ravel())
+
+
+def test_mx_block32_with_repeated_scales_equals_block128():
+    # 32-element blocks whose scales repeat 4x along K give exactly the 128-element result
+    M, N, K = 20, 24, 384
+    A, B, sfA, sfB = workloads.make_mx(M, N, K, 55)
+    C128, S128 = oracle.gemm_mx(A, B, sfA, sfB, M, N, K, block=128, sums=True)
+    C32, S32 = oracle.gemm_mx(A, B, np.repeat(sfA, 4, axis=1), np.repeat(sfB, 4, axis=1), M, N, K,
+                              block=32, sums=True)
+    assert np.array_equal(S32, S128) and np.array_equal(C32, C128)
+
+
+def test_mx_default_formats_are_the_mxfp8_product():
+    M, N, K = 16, 12, 256
+    A, B, sfA, sfB = workloads.make_mxfp8(M, N, K, 56)
+    assert np.array_equal(oracle.gemm_mx(A, B, sfA, sfB, M, N, K),
+                          oracle.gemm_mxfp8(A, B, sfA, sfB, M, N, K))
+
+
 def test_workload_recipe_shapes_and_ranges():
     A, B, sfA, sfB = workloads.make_mxfp8(64, 32, 300, 4)
     assert A.shape == (64, 300) and B.shape == (32, 300) and sfA.shape == (64, 3)

@@ -47,12 +47,24 @@ MUTANTS = {
         "v = ldexp((double)(8 + m), e - 9);",
     ),
     "scale_block_index_wrong": (
-        "out[r * K + k] = dtc_oracle_dec_e4m3(X[r * K + k]) *\n                             dtc_oracle_dec_e8m0(sf[r * kb + k / DTC_ORACLE_SF_BLOCK]);",
-        "out[r * K + k] = dtc_oracle_dec_e4m3(X[r * K + k]) *\n                             dtc_oracle_dec_e8m0(sf[r * kb]);",
+        "out[r * K + k] = dec_fp8(fmt, X[r * K + k]) * dtc_oracle_dec_e8m0(sf[r * kb + k / block]);",
+        "out[r * K + k] = dec_fp8(fmt, X[r * K + k]) * dtc_oracle_dec_e8m0(sf[r * kb]);",
     ),
     "b_scaled_with_a_scales": (
-        "double* bt = decode_scaled(B, sfB, N, K);",
-        "double* bt = decode_scaled(B, sfA, N, K);",
+        "double* bt = decode_scaled(fmt_b, block, B, sfB, N, K);",
+        "double* bt = decode_scaled(fmt_b, block, B, sfA, N, K);",
+    ),
+    "e5m2_bias_off_by_one": (
+        "v = ldexp((double)(4 + m), e - 17); /* (1 + m/4) * 2^(e-15) */",
+        "v = ldexp((double)(4 + m), e - 16); /* (1 + m/4) * 2^(e-15) */",
+    ),
+    "b_decoded_with_a_format": (
+        "double* bt = decode_scaled(fmt_b, block, B, sfB, N, K);",
+        "double* bt = decode_scaled(fmt_a, block, B, sfB, N, K);",
+    ),
+    "scale_block_fixed_at_128": (
+        "int64_t kb = (K + block - 1) / block;\n    double* out",
+        "block = 128;\n    int64_t kb = (K + block - 1) / block;\n    double* out",
     ),
     "f16_subnormal_scale_wrong": (
         "v = ldexp((double)m, -24); /* subnormal: m * 2^-10 * 2^-14 */",
