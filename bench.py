@@ -194,11 +194,13 @@ def oracle_rows(w, inputs, rows):
     t0 = time.perf_counter()
     if w.kind == "mxfp8":
         A, B, sfA, sfB = inputs
-        kb = (w.K + 127) // 128
-        oracle.gemm_mxfp8(A[:rows], B, sfA[:rows].reshape(rows, kb), sfB, rows, w.N, w.K)
+        oracle.gemm_mx(A[:rows], B, sfA[:rows], sfB, rows, w.N, w.K, a_fmt=w.a_fmt,
+                       b_fmt=w.b_fmt, block=w.block)
     else:
         A, B = inputs
-        oracle.gemm16(w.kind, w.layout, np.ascontiguousarray(A[:rows]), B, rows, w.N, w.K)
+        # output rows m are rows of A, or its columns when A is stored [K,M]
+        Ar = A[:, :rows] if w.layout[0] == "T" else A[:rows]
+        oracle.gemm16(w.kind, w.layout, np.ascontiguousarray(Ar), B, rows, w.N, w.K)
     return time.perf_counter() - t0
 
 
@@ -367,10 +369,13 @@ def run_ours(args, w):
         flush.fill_(float(i))
         torch.sum(flush_read, dim=0, out=flush_sink)  # evicts (writes back) the dirty lines
 
+    mx = (dict(a_format=w.a_fmt, b_format=w.b_fmt, scale_block=w.block) if w.kind == "mxfp8"
+          else {})
+
     def step_e2e(ins, Cout, st):
         if w.kind == "mxfp8":
             dtc.gemm_ex("mxfp8", ins[0], ins[1], Cout, sfA=ins[2], sfB=ins[3], variant=args.variant,
-                        stream=st)
+                        stream=st, **mx)
         else:
             dtc.gemm_ex(w.kind, ins[0], ins[1], Cout, layout=w.layout, variant=args.variant,
                         split_k=args.split_k, tile_n=args.tile_n, cluster_m=args.cluster_m,
@@ -378,14 +383,15 @@ def run_ours(args, w):
 
     def step():
         if w.kind == "mxfp8":
-            dtc.gemm_ex("mxfp8", A, B, C, sfA=sfA, sfB=sfB, variant=args.variant, stream=stream)
+            dtc.gemm_ex("mxfp8", A, B, C, sfA=sfA, sfB=sfB, variant=args.variant, stream=stream,
+                        **mx)
         else:
             dtc.gemm_ex(w.kind, A, B, C, layout=w.layout, variant=args.variant,
                         split_k=args.split_k, tile_n=args.tile_n, cluster_m=args.cluster_m,
                         stream=stream)
 
     plan = dtc.gemm_plan(w.kind, w.M, w.N, w.K, w.layout, variant=args.variant,
-                         split_k=args.split_k, tile_n=args.tile_n, cluster_m=args.cluster_m)
+                         split_k=args.split_k, tile_n=args.tile_n, cluster_m=args.cluster_m, **mx)
 
     for _ in range(args.warmup):
         flush_l2(1)
@@ -460,10 +466,12 @@ def run_ours(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if w.kind == "bf16" else ("f16" if w.kind == "f16" else "e4m3"),
+        "dtype": ("bf16" if w.kind == "bf16" else "f16" if w.kind == "f16"
+                  else w.a_fmt if w.a_fmt == w.b_fmt else f"{w.a_fmt}x{w.b_fmt}"),
         "data": "synthetic",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout,
                    "kind": w.kind, "variant": kernel_name,
+                   **({"scale_block": w.block} if w.kind == "mxfp8" else {}),
                    "tile": f"{plan['tile_m']}x{plan['tile_n']}x{plan['tile_k']}",
                    "stages": plan["stages"], "split_k": plan["split_k"], "ctas": plan["ctas"],
                    "cluster": plan["cluster"],

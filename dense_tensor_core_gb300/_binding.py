@@ -31,7 +31,9 @@ class gemm_options(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("split_k", ctypes.c_int),
                 ("timeout_ns", ctypes.c_uint64), ("fault_inject", ctypes.c_int),
                 ("tile_n", ctypes.c_int), ("cluster_m", ctypes.c_int), ("tile_k", ctypes.c_int),
-                ("lda", ctypes.c_int64), ("ldb", ctypes.c_int64), ("ldc", ctypes.c_int64)]
+                ("lda", ctypes.c_int64), ("ldb", ctypes.c_int64), ("ldc", ctypes.c_int64),
+                ("mx_a_format", ctypes.c_int), ("mx_b_format", ctypes.c_int),
+                ("mx_scale_block", ctypes.c_int)]
 
 
 class gemm_plan_info(ctypes.Structure):
@@ -153,10 +155,14 @@ def _out(C, M, N, dtype, device, rows_of_larger=False):
     return C
 
 
+_MX_FORMATS = {"e4m3": 0, "e5m2": 1}
+
+
 def _options(variant, split_k, timeout_ns, fault_inject, tile_n=0, cluster_m=0, tile_k=0,
-             lda=0, ldb=0, ldc=0):
+             lda=0, ldb=0, ldc=0, a_format="e4m3", b_format="e4m3", scale_block=0):
     return gemm_options(variant, split_k, timeout_ns, fault_inject, tile_n, cluster_m, tile_k,
-                        lda, ldb, ldc)
+                        lda, ldb, ldc, _MX_FORMATS[a_format], _MX_FORMATS[b_format],
+                        scale_block)
 
 
 def _gemm16(name, dtype, A, B, C, layout, stream):
@@ -180,7 +186,7 @@ def gemm_f16(A, B, C=None, layout="NT", stream=None):
     return _gemm16("gemm_f16", torch.float16, A, B, C, layout, stream)
 
 
-def _check_mxfp8(A, B, sfA, sfB, rows_of_larger=False):
+def _check_mxfp8(A, B, sfA, sfB, rows_of_larger=False, scale_block=128):
     _check_tensor(A, torch.uint8, "A", rows_of_larger)
     _check_tensor(B, torch.uint8, "B", rows_of_larger)
     _check_tensor(sfA, torch.uint8, "sfA")
@@ -189,7 +195,7 @@ def _check_mxfp8(A, B, sfA, sfB, rows_of_larger=False):
     N, Kb = B.shape
     if Kb != K:
         raise ValueError("A and B must both be [rows, K]")
-    kb = (K + 127) // 128
+    kb = (K + scale_block - 1) // scale_block
     if tuple(sfA.shape) != (M, kb) or tuple(sfB.shape) != (N, kb):
         raise ValueError(f"scales must be [M, {kb}] and [N, {kb}]")
     return M, N, K
@@ -206,12 +212,15 @@ def gemm_mxfp8(A, B, sfA, sfB, C=None, stream=None):
 
 
 def gemm_ex(kind, A, B, C=None, layout="NT", sfA=None, sfB=None, variant=0, split_k=0,
-            timeout_ns=0, fault_inject=0, tile_n=0, cluster_m=0, tile_k=0, stream=None):
+            timeout_ns=0, fault_inject=0, tile_n=0, cluster_m=0, tile_k=0, stream=None,
+            a_format="e4m3", b_format="e4m3", scale_block=0):
     """Any of the three products with options (variant, split_k, wait limit, test hook). A, B
     and C may be rows of larger row-major arrays (e.g. ``big[:, :n]``); their row strides are
-    passed as the leading dimensions."""
+    passed as the leading dimensions. For the block-scaled product ("mxfp8") the element formats
+    of A and B ("e4m3" or "e5m2") and the scale block (128, the default, or 32) may be chosen."""
     if kind == "mxfp8":
-        M, N, K = _check_mxfp8(A, B, sfA, sfB, rows_of_larger=True)
+        M, N, K = _check_mxfp8(A, B, sfA, sfB, rows_of_larger=True,
+                               scale_block=scale_block or 128)
         C = _out(C, M, N, torch.bfloat16, A.device, rows_of_larger=True)
     else:
         dt = torch.bfloat16 if kind == "bf16" else torch.float16
@@ -220,17 +229,19 @@ def gemm_ex(kind, A, B, C=None, layout="NT", sfA=None, sfB=None, variant=0, spli
         M, N, K = _shapes16(A, B, layout)
         C = _out(C, M, N, dt, A.device, rows_of_larger=True)
     opts = _options(variant, split_k, timeout_ns, fault_inject, tile_n, cluster_m, tile_k,
-                    _ld(A), _ld(B), _ld(C))
+                    _ld(A), _ld(B), _ld(C), a_format, b_format, scale_block)
     _check(lib().gemm_ex(_DTYPE[kind], _ptr(A), _ptr(B), _ptr(sfA), _ptr(sfB), _ptr(C), M, N, K,
                          _layout_code(layout), ctypes.byref(opts), _stream_handle(stream)))
     return C
 
 
-def gemm_plan(kind, M, N, K, layout="NT", variant=0, split_k=0, tile_n=0, cluster_m=0, tile_k=0):
+def gemm_plan(kind, M, N, K, layout="NT", variant=0, split_k=0, tile_n=0, cluster_m=0, tile_k=0,
+              a_format="e4m3", b_format="e4m3", scale_block=0):
     """The launch the library would make for these sizes: a dict with variant, tile_m, tile_n,
     tile_k, stages, split_k, ctas, tiles, cluster (raises GemmError if the call would be
     rejected)."""
-    opts = _options(variant, split_k, 0, 0, tile_n, cluster_m, tile_k)
+    opts = _options(variant, split_k, 0, 0, tile_n, cluster_m, tile_k, 0, 0, 0, a_format, b_format,
+                    scale_block)
     info = gemm_plan_info()
     _check(lib().gemm_plan(_DTYPE[kind], M, N, K, _layout_code(layout), ctypes.byref(opts),
                            ctypes.byref(info)))

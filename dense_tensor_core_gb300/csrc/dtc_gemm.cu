@@ -188,6 +188,12 @@ int validate(int dtype, const void* A, const void* B, const void* sfA, const voi
     if (o && o->tile_n < 0) return fail(GEMM_ERR_INVALID_ARG, "tile_n must be >= 0");
     if (o && (o->lda < 0 || o->ldb < 0 || o->ldc < 0))
         return fail(GEMM_ERR_INVALID_ARG, "lda, ldb and ldc must be >= 0");
+    if (o && (o->mx_a_format < 0 || o->mx_a_format > 1 || o->mx_b_format < 0 || o->mx_b_format > 1))
+        return fail(GEMM_ERR_INVALID_ARG, "mx formats must be 0 (e4m3) or 1 (e5m2)");
+    if (o && o->mx_scale_block != 0 && o->mx_scale_block != 32 && o->mx_scale_block != 128)
+        return fail(GEMM_ERR_INVALID_ARG, "mx_scale_block %d is not 32 or 128", o->mx_scale_block);
+    if (dtype != 2 && o && (o->mx_a_format || o->mx_b_format || o->mx_scale_block))
+        return fail(GEMM_ERR_INVALID_ARG, "the mx options apply to the block-scaled product only");
     const int eb = dtype == 2 ? 1 : 2;  // operand element bytes
     ops->A = A;
     ops->B = B;
@@ -330,6 +336,10 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
             return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 kernels use 224-wide tiles");
         if (v == GEMM_VARIANT_2CTA && K % 128)
             return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 pair kernel needs K %% 128 == 0");
+        const bool mx_default = !o || (o->mx_a_format == 0 && o->mx_b_format == 0 &&
+                                       (o->mx_scale_block == 0 || o->mx_scale_block == 128));
+        if (v == GEMM_VARIANT_2CTA && !mx_default)
+            return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 pair kernel takes e4m3 with 128-element scale blocks only");
         const int64_t pair_tiles = (int64_t)ceil_div(M, 256) * ceil_div(N, dtc::gmx2::kBN);
         // The pair kernel is correct but measured slower than the one-CTA kernel on GB300
         // (2008 vs 2357 TFLOP/s on 4096 x 4096 x 8192): it is an option, never chosen here.
@@ -618,7 +628,9 @@ dtc::GemmMxArgs mx_args(const Operands& ops, int M, int N, int K, int tile_m, in
     a.num_m = ceil_div(M, tile_m);
     a.num_n = ceil_div(N, tile_n);
     a.num_kb = ceil_div(K, tile_k);
-    a.sf_cols = ceil_div(K, 128);
+    const int block = (o && o->mx_scale_block) ? o->mx_scale_block : 128;
+    a.sf_cols = ceil_div(K, block);
+    a.fmt_bits = o ? ((uint32_t)o->mx_a_format << 7) | ((uint32_t)o->mx_b_format << 10) : 0u;
     a.timeout_ns = (o && o->timeout_ns) ? o->timeout_ns : kDefaultTimeoutNs;
     a.fault = o ? o->fault_inject : 0;
     return a;
@@ -655,7 +667,7 @@ int launch_mxfp8_2cta(const Operands& ops, int M, int N, int K, const gemm_optio
     return GEMM_OK;
 }
 
-template <bool kDeep>
+template <bool kDeep, bool kB32>
 int launch_mxfp8_1cta(const Operands& ops, int M, int N, int K, const gemm_options* o,
                       DeviceInfo* dev, const Plan& p, cudaStream_t stream) {
     using namespace dtc::gmx;
@@ -677,7 +689,7 @@ int launch_mxfp8_1cta(const Operands& ops, int M, int N, int K, const gemm_optio
                             (uint64_t)ops.ldb, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B, "B")))
             return rc;
     }
-    auto kern = dtc::gemm_mxfp8_kernel<kDeep>;
+    auto kern = dtc::gemm_mxfp8_kernel<kDeep, kB32>;
     if ((rc = ensure_smem_attr(kern, C_::kSmemBytes, dev))) return rc;
     const dtc::GemmMxArgs a = mx_args(ops, M, N, K, kBM, kBN, kBK, o);
     kern<<<p.ctas, kThreads, C_::kSmemBytes, stream>>>(tA, tB, a);
@@ -689,8 +701,12 @@ int launch_mxfp8_1cta(const Operands& ops, int M, int N, int K, const gemm_optio
 int launch_mxfp8(const Operands& ops, int M, int N, int K, const gemm_options* o, DeviceInfo* dev,
                  const Plan& p, cudaStream_t stream) {
     if (p.variant == GEMM_VARIANT_2CTA) return launch_mxfp8_2cta(ops, M, N, K, o, dev, p, stream);
-    if (p.tile_k == 2 * dtc::gmx::kBK) return launch_mxfp8_1cta<true>(ops, M, N, K, o, dev, p, stream);
-    return launch_mxfp8_1cta<false>(ops, M, N, K, o, dev, p, stream);
+    const bool b32 = o && o->mx_scale_block == 32;
+    if (p.tile_k == 2 * dtc::gmx::kBK)
+        return b32 ? launch_mxfp8_1cta<true, true>(ops, M, N, K, o, dev, p, stream)
+                   : launch_mxfp8_1cta<true, false>(ops, M, N, K, o, dev, p, stream);
+    return b32 ? launch_mxfp8_1cta<false, true>(ops, M, N, K, o, dev, p, stream)
+               : launch_mxfp8_1cta<false, false>(ops, M, N, K, o, dev, p, stream);
 }
 
 template <bool kBF16, bool kAMN, bool kNN>

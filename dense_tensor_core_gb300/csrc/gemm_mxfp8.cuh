@@ -16,8 +16,11 @@
 // Scales live in Tensor Memory. For an operand of R rows (128 for A, 224 for B) they take R/32
 // columns: row r sits in lane r % 32 of column r / 32, repeated in each of the four 32-lane
 // quarters (each quarter of the datapath reads the scales it needs from its own lanes). One
-// 32-bit cell holds the E8M0 bytes of 4 consecutive K-blocks; the instruction descriptor's scale
-// byte selectors (a_sf_id, b_sf_id) pick K-block kb % 4. Four "scale" warps (6..9, one per lane
+// 32-bit cell holds 4 consecutive scale bytes of the row: with 128-element scale blocks those of 4
+// consecutive K-blocks, and the instruction descriptor's scale byte selectors (a_sf_id, b_sf_id)
+// pick K-block kb % 4; with 32-element blocks (the OCP MX block size) the 4 bytes of one K-block,
+// one per MMA, and the selectors pick MMA kk of the K-block. Either way one scale set is one
+// 32-bit word per row, and the elements may be e4m3 or e5m2 (the descriptor's format fields). Four "scale" warps (6..9, one per lane
 // quarter) gather the bytes from global memory (one 32-bit load per row when the scale rows are
 // 4-byte aligned) and write them with tcgen05.st, one group of 4 K-blocks at a time, into a ring
 // of kSfSets scale sets; the gather for the next group is issued before the wait for a free set,
@@ -40,7 +43,8 @@ struct GemmMxArgs {
     const uint8_t* sfB;
     int M, N, K;
     int num_m, num_n, num_kb;  // num_kb: 128-element K-blocks
-    int sf_cols;               // bytes per scale row: ceil(K / 128)
+    int sf_cols;               // bytes per scale row: ceil(K / scale block)
+    uint32_t fmt_bits;         // instruction-descriptor element formats of A (bits 7-9), B (10-12)
     uint64_t timeout_ns;
     int fault;
 };
@@ -70,7 +74,6 @@ struct Cfg {
     static constexpr int kStageBytes = kAStage + kBStage;
     static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
     static_assert(kSmemBytes <= 227 * 1024 - 256, "shared memory budget");
-    static_assert(kGroup % kBlocks == 0, "a scale group is whole stages");
 };
 }  // namespace gmx
 
@@ -90,7 +93,7 @@ __device__ __forceinline__ uint32_t sf_word(const uint8_t* sf, int rows, int col
     return w;
 }
 
-template <bool kDeep>
+template <bool kDeep, bool kB32>
 __global__ void __launch_bounds__(gmx::kThreads, 1)
     gemm_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const GemmMxArgs args) {
@@ -117,7 +120,8 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int total = args.num_m * args.num_n;
-    const int groups = (args.num_kb + kGroup - 1) / kGroup;
+    constexpr int grp = kB32 ? 1 : kGroup;  // K-blocks per scale set
+    const int groups = (args.num_kb + grp - 1) / grp;
     const int num_st = (args.num_kb + kBlocks - 1) / kBlocks;  // stages per tile
     volatile int* abort = &abort_flag;
 
@@ -190,7 +194,7 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
-            constexpr uint32_t idesc0 = idesc_mxf8(kBM, kBN, 0, 0);
+            const uint32_t idesc0 = idesc_mxf8(kBM, kBN, 0, 0) | args.fmt_bits;
             uint32_t it = 0, acc = 0, sit = 0;
             bool ok = true, issued = false;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -202,16 +206,8 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * kAccStride;
-                for (int st = 0; st < num_st; ++st, ++it) {
+                for (int st = 0; st < num_st && ok; ++st, ++it) {
                     const int kb0 = st * kBlocks;  // first K-block of the stage
-                    const uint32_t set = sit % kSfSets;
-                    if (kb0 % kGroup == 0) {
-                        if (!wait_bounded(smem_u32(&bar_sfull[set]), (sit / kSfSets) & 1u, abort,
-                                          args.timeout_ns, &g_dtc_status, 35)) {
-                            ok = false;
-                            break;
-                        }
-                    }
                     const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
                     if (!wait_bounded(smem_u32(&bar_full[s]), ph, abort, args.timeout_ns,
                                       &g_dtc_status, 33)) {
@@ -219,32 +215,41 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t sfa = tmem_base + kSfBase + set * kSfSet;
-                    const uint32_t sfb = sfa + 4;
 #pragma unroll
                     for (int h = 0; h < kBlocks; ++h) {
                         const int kb = kb0 + h;
                         if (kb >= args.num_kb) break;  // a K-block past K: zero-filled, skipped
+                        const uint32_t set = sit % kSfSets;
+                        if (kb % grp == 0) {  // the first K-block of a scale set
+                            if (!wait_bounded(smem_u32(&bar_sfull[set]), (sit / kSfSets) & 1u,
+                                              abort, args.timeout_ns, &g_dtc_status, 35)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after_sync();
+                        }
                         // K-block h of the stage: 128-byte chunk h of each operand's box
                         const uint32_t a0 = sA + s * kAStage + h * (kBM * kBK);
                         const uint32_t b0 = sB + s * kBStage + h * (kBN * kBK);
-                        const uint32_t sf_id = (uint32_t)(kb % kGroup);
-                        const uint32_t idesc = idesc0 | (sf_id << 4) | (sf_id << 29);
+                        const uint32_t sfa = tmem_base + kSfBase + set * kSfSet;
+                        const uint32_t sfb = sfa + 4;
 #pragma unroll
                         for (int kk = 0; kk < kBK / 32; ++kk) {
+                            const uint32_t sf_id = kB32 ? (uint32_t)kk : (uint32_t)(kb % kGroup);
+                            const uint32_t idesc = idesc0 | (sf_id << 4) | (sf_id << 29);
                             const uint64_t adesc = smem_desc_sw128(a0 + kk * 32, 16, 1024);
                             const uint64_t bdesc = smem_desc_sw128(b0 + kk * 32, 16, 1024);
                             mma_mxf8_cta1(d_tmem, adesc, bdesc, idesc, sfa, sfb,
                                           (kb | kk) != 0 ? 1u : 0u);
                         }
+                        issued = true;
+                        if (kb % grp == grp - 1 || kb == args.num_kb - 1) {
+                            mma_commit_cta1(smem_u32(&bar_sempty[set]));  // scale set consumed
+                            ++sit;
+                        }
                     }
-                    issued = true;
+                    if (!ok) break;
                     mma_commit_cta1(smem_u32(&bar_empty[s]));
-                    const int kb_last = kb0 + kBlocks - 1;
-                    if (kb_last % kGroup == kGroup - 1 || kb_last >= args.num_kb - 1) {
-                        mma_commit_cta1(smem_u32(&bar_sempty[set]));  // scale set consumed
-                        ++sit;
-                    }
                 }
                 if (!ok) break;
                 mma_commit_cta1(smem_u32(&bar_tfull[b]));
@@ -266,8 +271,8 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
             const uint32_t b = acc & 1u, aph = (acc >> 1) & 1u;
             int ok = 1;
             if (lane == 0)
-                ok = wait_bounded(smem_u32(&bar_tfull[b]), aph, abort, args.timeout_ns,
-                                  &g_dtc_status, 34);
+                ok = wait_bounded<false, true>(smem_u32(&bar_tfull[b]), aph, abort,
+                                               args.timeout_ns, &g_dtc_status, 34);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after_sync();
@@ -309,7 +314,6 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
         const int my_tiles =
             (int)blockIdx.x < total ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
         const int steps = my_tiles * groups;
-        uint32_t wa[4], wb[8];
         auto gather = [&](int step, uint32_t (&ga)[4], uint32_t (&gb)[8]) {
             const int t = (int)blockIdx.x + (step / groups) * (int)gridDim.x;
             const int g = step % groups;
@@ -324,6 +328,7 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
                             ? sf_word(args.sfB, args.N, args.sf_cols, nt * kBN + lane + 32 * j, g)
                             : 0u;
         };
+        uint32_t wa[4], wb[8];
         if (steps > 0) gather(0, wa, wb);
         for (int step = 0; step < steps; ++step) {
             uint32_t na[4], nb[8];
@@ -332,8 +337,9 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
             const uint32_t set = sit % kSfSets;
             int w_ok = 1;
             if (lane == 0)
-                w_ok = wait_bounded(smem_u32(&bar_sempty[set]), ((sit / kSfSets) & 1u) ^ 1u, abort,
-                                    args.timeout_ns, &g_dtc_status, 36);
+                w_ok = wait_bounded<false, true>(smem_u32(&bar_sempty[set]),
+                                                 ((sit / kSfSets) & 1u) ^ 1u, abort,
+                                                 args.timeout_ns, &g_dtc_status, 36);
             w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
             if (!w_ok) break;
             tc_fence_after_sync();

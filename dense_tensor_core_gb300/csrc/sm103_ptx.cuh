@@ -158,8 +158,11 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 // Bounded wait for the phase with `parity` of barrier `bar`. Gives up (returns false) if
 // `*abort` becomes non-zero, or after `timeout_ns` of waiting, in which case it sets `*abort`
 // and records `site` in `*status` (first writer wins).
-// With kCluster, the wait acquires at cluster scope (see mbar_try_wait_cluster).
-template <bool kCluster = false>
+// With kCluster, the wait acquires at cluster scope (see mbar_try_wait_cluster). With kBackoff
+// the waiting thread sleeps briefly between polls: for roles off the critical path (epilogue,
+// scale writers) whose polling would otherwise take issue slots from the warps that share their
+// SM sub-partition.
+template <bool kCluster = false, bool kBackoff = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
                                              uint64_t timeout_ns, int* status, int site) {
     auto try_wait = [&]() {
@@ -168,6 +171,7 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
     if (try_wait()) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
+        if (kBackoff) __nanosleep(64);
         if (try_wait()) return true;
         if (*abort) return false;
         if (globaltimer_ns() - t0 > timeout_ns) {

@@ -32,6 +32,9 @@ class Workload:
     N: int
     K: int
     seed: int
+    a_fmt: str = "e4m3"  # block-scaled product: element formats of A and B
+    b_fmt: str = "e4m3"
+    block: int = SF_BLOCK  # block-scaled product: K-elements per scale
 
     @property
     def flops(self) -> int:
@@ -41,7 +44,7 @@ class Workload:
     def min_bytes(self) -> int:
         """Compulsory HBM traffic: read A and B (and the scales) once, write C once."""
         if self.kind == "mxfp8":
-            kb = (self.K + SF_BLOCK - 1) // SF_BLOCK
+            kb = (self.K + self.block - 1) // self.block
             return self.M * self.K + self.N * self.K + (self.M + self.N) * kb + 2 * self.M * self.N
         return 2 * (self.M * self.K + self.N * self.K + self.M * self.N)
 
@@ -49,7 +52,8 @@ class Workload:
 # The pages' example shapes (TileLang SM100 Support (Preview): NT 4096x4096x8192 with a
 # 128x256x128 tile; tilelang (velog) 1.1-1.3: fp16 NN 1024^3) plus the large 2-CTA square, the
 # memory-bound skinny product and the block-scaled variant; then the same 4096x4096x8192 product
-# with A stored transposed (trans_A of T.gemm), to measure the MN-major A path.
+# with A stored transposed (trans_A of T.gemm), to measure the MN-major A path, and block-scaled
+# with the OCP MX 32-element scale blocks, in e4m3 and in e5m2.
 WORKLOADS = {
     w.name: w
     for w in [
@@ -61,6 +65,10 @@ WORKLOADS = {
         Workload("mxfp8_nt_4096x4096x8192", "mxfp8", "NT", 4096, 4096, 8192, 4),
         Workload("bf16_tn_4096x4096x8192", "bf16", "TN", 4096, 4096, 8192, 5),
         Workload("bf16_tt_4096x4096x8192", "bf16", "TT", 4096, 4096, 8192, 6),
+        Workload("mxfp8_b32_nt_4096x4096x8192", "mxfp8", "NT", 4096, 4096, 8192, 7,
+                 block=32),
+        Workload("mx_e5m2_b32_nt_4096x4096x8192", "mxfp8", "NT", 4096, 4096, 8192, 8,
+                 a_fmt="e5m2", b_fmt="e5m2", block=32),
     ]
 }
 
@@ -120,5 +128,5 @@ def make_mxfp8(M: int, N: int, K: int, seed: int):
 
 def make(w: Workload):
     if w.kind == "mxfp8":
-        return make_mxfp8(w.M, w.N, w.K, w.seed)
+        return make_mx(w.M, w.N, w.K, w.seed, w.a_fmt, w.b_fmt, w.block)
     return make16(w.kind, w.layout, w.M, w.N, w.K, w.seed)

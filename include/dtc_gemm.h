@@ -92,6 +92,12 @@ typedef struct {
     int64_t ldb;          /* row length: K or M for A, K or N for B, N for C). At least the row */
     int64_t ldc;          /* length, and rows must start 16 bytes apart (ld x element size %
                              16 == 0). Only the M x N region of C is written. */
+    int mx_a_format;      /* block-scaled product only: element format of A, 0 = e4m3 (OCP FP8 */
+    int mx_b_format;      /* E4M3, the default), 1 = e5m2 (OCP FP8 E5M2); likewise B */
+    int mx_scale_block;   /* block-scaled product only: K-elements per E8M0 scale, 128 (0 = the
+                             default, the pages' granularity) or 32 (the OCP MX block); the
+                             scale arrays are then [rows, ceil(K / block)]. Non-default formats
+                             or blocks run on the one-CTA kernel. */
 } gemm_options;
 
 /*
@@ -129,8 +135,8 @@ int gemm_mxfp8(const void* A, const void* B, const void* sfA, const void* sfB, v
                int64_t M, int64_t N, int64_t K, dtc_stream_t stream);
 
 /*
- * The same three operations with options (variant choice, leading dimensions, wait limit, test
- * hook). dtype: 0 = bf16, 1 = fp16, 2 = mxfp8 (sfA/sfB are ignored for 0 and 1; layout must be
+ * The same three operations with options (variant choice, leading dimensions, block-scaled
+ * element formats and scale block, wait limit, test hook). dtype: 0 = bf16, 1 = fp16, 2 = mxfp8 (sfA/sfB are ignored for 0 and 1; layout must be
  * NT for 2; the scale arrays stay dense). opts may be NULL (all defaults). INVALID_ARG also when
  * a leading dimension is negative, below its row length, above 2^31-1 or not a multiple of 16
  * bytes.

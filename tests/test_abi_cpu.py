@@ -124,6 +124,22 @@ def test_leading_dimensions_rejected_before_cuda(L, ld, layout):
     assert L.gemm_last_error()
 
 
+@pytest.mark.parametrize("dtype,opt", [(0, dict(mx_a_format=1)), (1, dict(mx_scale_block=32)),
+                                       (2, dict(mx_b_format=2)), (2, dict(mx_scale_block=64)),
+                                       (2, dict(mx_a_format=-1))])
+def test_block_scaled_options_rejected_before_cuda(L, dtype, opt):
+    from dense_tensor_core_gb300._binding import gemm_options
+
+    vp = ctypes.c_void_p
+    o = gemm_options()
+    for k, v in opt.items():
+        setattr(o, k, v)
+    rc = L.gemm_ex(dtype, vp(0x1000), vp(0x2000), vp(0x10), vp(0x20), vp(0x3000), 16, 16, 32, 0,
+                   ctypes.byref(o), None)
+    assert rc == INVALID
+    assert L.gemm_last_error()
+
+
 def test_options_struct_matches_header():
     # the binding's ctypes mirror of gemm_options lists the header's fields in order
     from dense_tensor_core_gb300._binding import gemm_options

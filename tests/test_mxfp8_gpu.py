@@ -180,3 +180,69 @@ def test_automatic_choice():
     assert dtc.gemm_plan("mxfp8", 4096, 4096, 8192, variant=2)["variant"] == 2
     with pytest.raises(dtc.GemmError):
         dtc.gemm_plan("mxfp8", 4096, 4096, 8208, variant=2)  # the pair kernel needs K % 128 == 0
+
+
+# --- other block-scaled formats: e5m2 elements, 32-element (OCP MX) scale blocks ---------------
+
+def run_mx_fmt(A, B, sfA, sfB, a_fmt, b_fmt, block, **kw):
+    return run_mx(A, B, sfA, sfB, a_format=a_fmt, b_format=b_fmt, scale_block=block, **kw)
+
+
+@pytest.mark.parametrize("tile_k", [128, 256])
+@pytest.mark.parametrize("block", [32, 128])
+@pytest.mark.parametrize("a_fmt,b_fmt", [("e5m2", "e5m2"), ("e4m3", "e5m2"), ("e5m2", "e4m3"),
+                                         ("e4m3", "e4m3")])
+@pytest.mark.parametrize("M,N,K", [(256, 448, 1024), (300, 520, 400), (129, 232, 656),
+                                   (256, 224, 384)])
+def test_formats_and_blocks_full_parity(M, N, K, a_fmt, b_fmt, block, tile_k):
+    if tile_k == 256 and K % 128:
+        pytest.skip("256-deep stages need K % 128 == 0")
+    A, B, sfA, sfB = workloads.make_mx(M, N, K, M + N + K + block, a_fmt, b_fmt, block)
+    C = run_mx_fmt(A, B, sfA, sfB, a_fmt, b_fmt, block, variant=1, tile_k=tile_k)
+    ref = oracle.gemm_mx(A, B, sfA, sfB, M, N, K, a_fmt=a_fmt, b_fmt=b_fmt, block=block)
+    check_close(values16(C, "bf16"), values16(ref, "bf16"),
+                f"{a_fmt}x{b_fmt} block {block} {M}x{N}x{K} tile_k {tile_k}")
+
+
+@pytest.mark.parametrize("tile_k", [128, 256])
+@pytest.mark.parametrize("which", ["a_rows", "b_rows", "k_blocks"])
+def test_block32_scales_varying_along_one_axis(which, tile_k):
+    # with 32-element blocks each MMA of a K-block takes its own scale byte: scales that vary along
+    # K by 32-block pin that byte selection
+    M, N, K = 256, 448, 1024
+    A, B, sfA, sfB = workloads.make_mx(M, N, K, 9, block=32)
+    kb = sfA.shape[1]
+    sfA[:] = 127
+    sfB[:] = 127
+    if which == "a_rows":
+        sfA[:] = (120 + (np.arange(M) % 13))[:, None]
+    elif which == "b_rows":
+        sfB[:] = (121 + (np.arange(N) % 11))[:, None]
+    else:
+        sfA[:] = (123 + (np.arange(kb) % 7))[None, :]
+        sfB[:] = (130 - (np.arange(kb) % 5))[None, :]
+    C = run_mx_fmt(A, B, sfA, sfB, "e4m3", "e4m3", 32, variant=1, tile_k=tile_k)
+    ref = oracle.gemm_mx(A, B, sfA, sfB, M, N, K, block=32)
+    check_close(values16(C, "bf16"), values16(ref, "bf16"), f"block-32 scales along {which}")
+
+
+@pytest.mark.parametrize("name", ["mxfp8_b32_nt_4096x4096x8192", "mx_e5m2_b32_nt_4096x4096x8192"])
+def test_format_workloads_sampled(name):
+    w = workloads.WORKLOADS[name]
+    A, B, sfA, sfB = workloads.make(w)
+    C = run_mx_fmt(A, B, sfA, sfB, w.a_fmt, w.b_fmt, w.block)
+    r, c = sample_positions(w.M, w.N, count=3000, seed=w.seed, tile_m=128, tile_n=224)
+    r = np.concatenate([r, np.full(w.N, 777), np.arange(w.M)])
+    c = np.concatenate([c, np.arange(w.N), np.full(w.M, 555)])
+    ref, _ = oracle.gemm_mx_sampled(A, B, sfA, sfB, w.M, w.N, w.K, r, c, a_fmt=w.a_fmt,
+                                    b_fmt=w.b_fmt, block=w.block)
+    check_close(values16(C[r, c], "bf16"), values16(ref, "bf16"), name)
+
+
+def test_format_options_plan():
+    import dense_tensor_core_gb300 as dtc
+
+    p = dtc.gemm_plan("mxfp8", 4096, 4096, 8192, scale_block=32, a_format="e5m2")
+    assert (p["variant"], p["tile_k"]) == (1, 256)
+    with pytest.raises(dtc.GemmError):  # the pair kernel takes the pages' format only
+        dtc.gemm_plan("mxfp8", 4096, 4096, 8192, variant=2, scale_block=32)
