@@ -371,6 +371,13 @@ def run_ours(args, w):
 
     mx = (dict(a_format=w.a_fmt, b_format=w.b_fmt, scale_block=w.block) if w.kind == "mxfp8"
           else {})
+    # stream-K workspace, as a user would pass it (zero-filled before first use)
+    if w.kind != "mxfp8" and args.stream_k != 2:
+        ws_bytes = dtc.gemm_workspace_size(w.kind, w.M, w.N, w.K, w.layout, variant=args.variant,
+                                           tile_n=args.tile_n, stream_k=args.stream_k)
+        if ws_bytes:
+            mx = dict(workspace=torch.zeros(ws_bytes, dtype=torch.uint8, device=dev),
+                      stream_k=args.stream_k)
 
     def step_e2e(ins, Cout, st):
         if w.kind == "mxfp8":
@@ -379,7 +386,7 @@ def run_ours(args, w):
         else:
             dtc.gemm_ex(w.kind, ins[0], ins[1], Cout, layout=w.layout, variant=args.variant,
                         split_k=args.split_k, tile_n=args.tile_n, cluster_m=args.cluster_m,
-                        stream=st)
+                        stream=st, **mx)
 
     def step():
         if w.kind == "mxfp8":
@@ -388,7 +395,7 @@ def run_ours(args, w):
         else:
             dtc.gemm_ex(w.kind, A, B, C, layout=w.layout, variant=args.variant,
                         split_k=args.split_k, tile_n=args.tile_n, cluster_m=args.cluster_m,
-                        stream=stream)
+                        stream=stream, **mx)
 
     plan = dtc.gemm_plan(w.kind, w.M, w.N, w.K, w.layout, variant=args.variant,
                          split_k=args.split_k, tile_n=args.tile_n, cluster_m=args.cluster_m, **mx)
@@ -474,6 +481,7 @@ def run_ours(args, w):
                    **({"scale_block": w.block} if w.kind == "mxfp8" else {}),
                    "tile": f"{plan['tile_m']}x{plan['tile_n']}x{plan['tile_k']}",
                    "stages": plan["stages"], "split_k": plan["split_k"], "ctas": plan["ctas"],
+                   "stream_k_tiles": plan["sk_tiles"],
                    "cluster": plan["cluster"],
                    "parallelism": f"replicas x{world}",
                    "l2": "flushed before every timed step, outside the step's CUDA-event "
@@ -511,6 +519,9 @@ def main(argv=None):
     p.add_argument("--split-k", type=int, default=0)
     p.add_argument("--tile-n", type=int, default=0, help="force the N-tile (256 or 224)")
     p.add_argument("--cluster-m", type=int, default=0, help="force the one-CTA cluster size")
+    p.add_argument("--stream-k", type=int, default=0, choices=[0, 1, 2],
+                   help="stream-K on CTA pairs: 0 auto (a workspace is passed when it helps), "
+                        "1 required, 2 off")
     p.add_argument("--skip-cpu-baseline", action="store_true",
                    help="omit the oracle timing (profiling runs)")
     p.add_argument("--cpu-seconds", type=float, default=15.0)

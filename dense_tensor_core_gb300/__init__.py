@@ -22,6 +22,7 @@ from ._binding import (  # noqa: F401
     gemm_mxfp8,
     gemm_plan,
     gemm_stream_status,
+    gemm_workspace_size,
     lib,
     library_path,
 )

@@ -33,13 +33,14 @@ class gemm_options(ctypes.Structure):
                 ("tile_n", ctypes.c_int), ("cluster_m", ctypes.c_int), ("tile_k", ctypes.c_int),
                 ("lda", ctypes.c_int64), ("ldb", ctypes.c_int64), ("ldc", ctypes.c_int64),
                 ("mx_a_format", ctypes.c_int), ("mx_b_format", ctypes.c_int),
-                ("mx_scale_block", ctypes.c_int)]
+                ("mx_scale_block", ctypes.c_int), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_uint64), ("stream_k", ctypes.c_int)]
 
 
 class gemm_plan_info(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
                 ("variant", "tile_m", "tile_n", "tile_k", "stages", "split_k", "ctas", "tiles",
-                 "cluster")]
+                 "cluster", "sk_tiles")]
 
 
 _lib = None
@@ -71,6 +72,9 @@ def lib():
         L.gemm_plan.restype = i32
         L.gemm_plan.argtypes = [i32, i64, i64, i64, i32, ctypes.POINTER(gemm_options),
                                 ctypes.POINTER(gemm_plan_info)]
+        L.gemm_workspace_size.restype = i32
+        L.gemm_workspace_size.argtypes = [i32, i64, i64, i64, i32, ctypes.POINTER(gemm_options),
+                                          ctypes.POINTER(ctypes.c_uint64)]
         L.gemm_last_error.restype = ctypes.c_char_p
         L.gemm_last_error.argtypes = []
         L.gemm_stream_status.restype = i32
@@ -159,10 +163,13 @@ _MX_FORMATS = {"e4m3": 0, "e5m2": 1}
 
 
 def _options(variant, split_k, timeout_ns, fault_inject, tile_n=0, cluster_m=0, tile_k=0,
-             lda=0, ldb=0, ldc=0, a_format="e4m3", b_format="e4m3", scale_block=0):
+             lda=0, ldb=0, ldc=0, a_format="e4m3", b_format="e4m3", scale_block=0,
+             workspace=None, stream_k=0):
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     return gemm_options(variant, split_k, timeout_ns, fault_inject, tile_n, cluster_m, tile_k,
                         lda, ldb, ldc, _MX_FORMATS[a_format], _MX_FORMATS[b_format],
-                        scale_block)
+                        scale_block, ws_ptr, ws_bytes, stream_k)
 
 
 def _gemm16(name, dtype, A, B, C, layout, stream):
@@ -213,11 +220,15 @@ def gemm_mxfp8(A, B, sfA, sfB, C=None, stream=None):
 
 def gemm_ex(kind, A, B, C=None, layout="NT", sfA=None, sfB=None, variant=0, split_k=0,
             timeout_ns=0, fault_inject=0, tile_n=0, cluster_m=0, tile_k=0, stream=None,
-            a_format="e4m3", b_format="e4m3", scale_block=0):
+            a_format="e4m3", b_format="e4m3", scale_block=0, workspace=None, stream_k=0):
     """Any of the three products with options (variant, split_k, wait limit, test hook). A, B
     and C may be rows of larger row-major arrays (e.g. ``big[:, :n]``); their row strides are
     passed as the leading dimensions. For the block-scaled product ("mxfp8") the element formats
-    of A and B ("e4m3" or "e5m2") and the scale block (128, the default, or 32) may be chosen."""
+    of A and B ("e4m3" or "e5m2") and the scale block (128, the default, or 32) may be chosen.
+    `workspace` (a CUDA tensor of gemm_workspace_size bytes, zero-filled before its first use)
+    lets the 16-bit products use stream-K; stream_k: 0 auto, 1 required, 2 off."""
+    if workspace is not None and (not workspace.is_cuda or not workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor")
     if kind == "mxfp8":
         M, N, K = _check_mxfp8(A, B, sfA, sfB, rows_of_larger=True,
                                scale_block=scale_block or 128)
@@ -229,19 +240,19 @@ def gemm_ex(kind, A, B, C=None, layout="NT", sfA=None, sfB=None, variant=0, spli
         M, N, K = _shapes16(A, B, layout)
         C = _out(C, M, N, dt, A.device, rows_of_larger=True)
     opts = _options(variant, split_k, timeout_ns, fault_inject, tile_n, cluster_m, tile_k,
-                    _ld(A), _ld(B), _ld(C), a_format, b_format, scale_block)
+                    _ld(A), _ld(B), _ld(C), a_format, b_format, scale_block, workspace, stream_k)
     _check(lib().gemm_ex(_DTYPE[kind], _ptr(A), _ptr(B), _ptr(sfA), _ptr(sfB), _ptr(C), M, N, K,
                          _layout_code(layout), ctypes.byref(opts), _stream_handle(stream)))
     return C
 
 
 def gemm_plan(kind, M, N, K, layout="NT", variant=0, split_k=0, tile_n=0, cluster_m=0, tile_k=0,
-              a_format="e4m3", b_format="e4m3", scale_block=0):
+              a_format="e4m3", b_format="e4m3", scale_block=0, workspace=None, stream_k=0):
     """The launch the library would make for these sizes: a dict with variant, tile_m, tile_n,
-    tile_k, stages, split_k, ctas, tiles, cluster (raises GemmError if the call would be
-    rejected)."""
+    tile_k, stages, split_k, ctas, tiles, cluster, sk_tiles (raises GemmError if the call would
+    be rejected)."""
     opts = _options(variant, split_k, 0, 0, tile_n, cluster_m, tile_k, 0, 0, 0, a_format, b_format,
-                    scale_block)
+                    scale_block, workspace, stream_k)
     info = gemm_plan_info()
     _check(lib().gemm_plan(_DTYPE[kind], M, N, K, _layout_code(layout), ctypes.byref(opts),
                            ctypes.byref(info)))
@@ -251,3 +262,12 @@ def gemm_plan(kind, M, N, K, layout="NT", variant=0, split_k=0, tile_n=0, cluste
 def gemm_stream_status(stream=None):
     """Synchronise the stream and raise GemmError if a device-side wait gave up."""
     _check(lib().gemm_stream_status(_stream_handle(stream)))
+
+
+def gemm_workspace_size(kind, M, N, K, layout="NT", variant=0, tile_n=0, tile_k=0, stream_k=0):
+    """Bytes of workspace with which the call would use stream-K (0 if it would not)."""
+    opts = _options(variant, 0, 0, 0, tile_n, 0, tile_k, stream_k=stream_k)
+    out = ctypes.c_uint64(0)
+    _check(lib().gemm_workspace_size(_DTYPE[kind], M, N, K, _layout_code(layout),
+                                     ctypes.byref(opts), ctypes.byref(out)))
+    return out.value

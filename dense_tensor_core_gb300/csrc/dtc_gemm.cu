@@ -194,6 +194,10 @@ int validate(int dtype, const void* A, const void* B, const void* sfA, const voi
         return fail(GEMM_ERR_INVALID_ARG, "mx_scale_block %d is not 32 or 128", o->mx_scale_block);
     if (dtype != 2 && o && (o->mx_a_format || o->mx_b_format || o->mx_scale_block))
         return fail(GEMM_ERR_INVALID_ARG, "the mx options apply to the block-scaled product only");
+    if (o && (o->stream_k < 0 || o->stream_k > 2))
+        return fail(GEMM_ERR_INVALID_ARG, "stream_k %d is not 0 (auto), 1 (required) or 2 (off)", o->stream_k);
+    if (o && o->workspace && !aligned16(o->workspace))
+        return fail(GEMM_ERR_INVALID_ARG, "the workspace is not 16-byte aligned");
     const int eb = dtype == 2 ? 1 : 2;  // operand element bytes
     ops->A = A;
     ops->B = B;
@@ -232,8 +236,15 @@ int validate(int dtype, const void* A, const void* B, const void* sfA, const voi
 
 struct Plan {
     int variant = 0, tile_m = 0, tile_n = 0, tile_k = 64, stages = 0, split_k = 1, ctas = 0,
-        tiles = 0, cluster = 1;
+        tiles = 0, cluster = 1, sk_tiles = 0;
 };
+
+// Stream-K workspace of the pair kernel for `units` pairs and tile width bn: the flags (one
+// 32-bit word per CTA, padded to 1 KB), then one 128 x bn fp32 slot per CTA.
+constexpr uint64_t kSkFlagBytes = 1024;
+uint64_t sk_workspace_bytes(int units, int bn) {
+    return kSkFlagBytes + (uint64_t)units * 2 * 128 * (uint64_t)bn * 4;
+}
 
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
@@ -317,6 +328,56 @@ double plan_cost(int variant, int bn, double eff, int64_t M, int64_t N, int sms)
     const int64_t rows = variant == GEMM_VARIANT_2CTA ? ceil_div(M, 256) : ceil_div(M, 128);
     const int64_t tiles = rows * ceil_div(N, bn);
     return (double)ceil_div(tiles, units) * bn / eff;
+}
+
+double choice_efficiency(int variant, int bn, int bk) {
+    for (const TileChoice& c : kChoices)
+        if (c.variant == variant && c.tile_n == bn && c.tile_k == bk) return c.efficiency;
+    return 0.5;
+}
+
+// Stream-K on CTA pairs (256 x 256 x 128 tiles): when the tiles leave the last wave part-empty,
+// the leftover tiles are shared out over all pairs as equal runs of K-blocks, their pieces summed
+// through the caller's workspace. Taken when a large enough workspace is given, the request
+// allows the pair kernel with these tiles, and the cost model beats the plan already made: work
+// per pair / efficiency, plus half a tile's time for the pieces' exchange and the shorter runs
+// (measured on GB300: a gain on 8192^3, a wash against 224-wide whole tiles on 4096^2 x 8192).
+// Required or refused with opts->stream_k.
+int plan_stream_k(int64_t M, int64_t N, int64_t K, const gemm_options* o, DeviceInfo* d, Plan* p) {
+    const int mode = o ? o->stream_k : 0;
+    if (mode == 2) return GEMM_OK;
+    const int units = std::max(1, d->sms / 2);
+    const int64_t tiles = (int64_t)ceil_div(M, 256) * ceil_div(N, 256);
+    const int req_v = o ? o->variant : GEMM_VARIANT_AUTO;
+    const bool allowed = (req_v == GEMM_VARIANT_AUTO || req_v == GEMM_VARIANT_2CTA) &&
+                         (!o || o->tile_n == 0 || o->tile_n == 256) &&
+                         (!o || o->tile_k == 0 || o->tile_k == 128) && (!o || o->split_k == 0) &&
+                         K % 64 == 0 && p->variant != GEMM_VARIANT_SPLITK && tiles >= units &&
+                         tiles % units != 0;
+    const bool ws_ok = o && o->workspace && o->workspace_bytes >= sk_workspace_bytes(units, 256);
+    if (mode == 1 && !allowed)
+        return fail(GEMM_ERR_UNSUPPORTED, "stream-K needs the pair kernel with 256 x 256 x 128 tiles, "
+                    "K %% 64 == 0 and a tile count that is not a whole number of waves");
+    if (mode == 1 && !ws_ok)
+        return fail(GEMM_ERR_INVALID_ARG, "stream-K needs a workspace of %llu bytes",
+                    (unsigned long long)sk_workspace_bytes(units, 256));
+    if (!allowed || !ws_ok) return GEMM_OK;
+    const double eff = choice_efficiency(GEMM_VARIANT_2CTA, 256, 128);
+    const double sk_cost = ((double)tiles / units + 0.5) * 256 / eff;
+    const double dp_cost = plan_cost(p->variant, p->tile_n,
+                                     choice_efficiency(p->variant, p->tile_n, p->tile_k), M, N, d->sms);
+    if (mode == 0 && sk_cost >= dp_cost) return GEMM_OK;
+    p->variant = GEMM_VARIANT_2CTA;
+    p->cluster = 2;
+    p->tile_m = 256;
+    p->tile_n = 256;
+    p->tile_k = 128;
+    p->stages = pair_stages(256, 128);
+    p->split_k = 1;
+    p->tiles = (int)tiles;
+    p->sk_tiles = (int)(tiles % units);
+    p->ctas = 2 * units;
+    return GEMM_OK;
 }
 
 int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm_options* o,
@@ -504,12 +565,16 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
         p->tiles = ceil_div(M, 256) * ceil_div(N, p->tile_n);
         p->ctas = 2 * std::min(p->tiles, pairs);
     }
-    return GEMM_OK;
+    return plan_stream_k(M, N, K, o, d, p);
 }
 
 Gemm16Args make_args(const Operands& ops, int M, int N, int K, int tile_m, int tile_n, int tile_k,
-                     const gemm_options* o) {
+                     const gemm_options* o, int sk_tiles = 0) {
     Gemm16Args a;
+    a.sk_tiles = sk_tiles;
+    a.sk_flags = sk_tiles ? static_cast<uint32_t*>(o->workspace) : nullptr;
+    a.sk_partial = sk_tiles ? reinterpret_cast<float*>(static_cast<char*>(o->workspace) + kSkFlagBytes)
+                            : nullptr;
     a.C = ops.C;
     a.ldc = ops.ldc;
     a.M = M;
@@ -560,7 +625,7 @@ int launch_gemm16_1cta(const Operands& ops, int M, int N, int K, const gemm_opti
     return launch_cluster(kern, p.ctas, kThreads, Cfg::kSmemBytes, kCM, stream, tA, tB, args);
 }
 
-template <bool kBF16, bool kAMN, bool kNN, int kBN, int kBK>
+template <bool kBF16, bool kAMN, bool kNN, int kBN, int kBK, bool kSK = false>
 int launch_gemm16_2cta(const Operands& ops, int M, int N, int K, const gemm_options* o,
                        DeviceInfo* dev, const Plan& p, cudaStream_t stream) {
     constexpr int kStages = pair_stages(kBN, kBK);
@@ -570,9 +635,9 @@ int launch_gemm16_2cta(const Operands& ops, int M, int N, int K, const gemm_opti
     int rc = tmap_operand16(&tA, dt, ops.A, ops.lda, kAMN, M, K, kBK, 128, "A");
     if (rc) return rc;
     if ((rc = tmap_operand16(&tB, dt, ops.B, ops.ldb, kNN, N, K, kBK, Cfg::kHalfN, "B"))) return rc;
-    auto kern = dtc::gemm16_2cta_kernel<kBF16, kAMN, kNN, kBN, kBK, kStages>;
+    auto kern = dtc::gemm16_2cta_kernel<kBF16, kAMN, kNN, kBN, kBK, kStages, kSK>;
     if ((rc = ensure_smem_attr(kern, Cfg::kSmemBytes, dev))) return rc;
-    const Gemm16Args args = make_args(ops, M, N, K, 256, kBN, kBK, o);
+    const Gemm16Args args = make_args(ops, M, N, K, 256, kBN, kBK, o, p.sk_tiles);
     return launch_cluster(kern, p.ctas, dtc::g2::kThreads, Cfg::kSmemBytes, 2, stream, tA, tB, args);
 }
 
@@ -712,6 +777,8 @@ int launch_mxfp8(const Operands& ops, int M, int N, int K, const gemm_options* o
 template <bool kBF16, bool kAMN, bool kNN>
 int launch_pair_width(const Plan& p, const Operands& ops, int m, int n, int k,
                       const gemm_options* o, DeviceInfo* dev, cudaStream_t stream) {
+    if (p.sk_tiles)  // stream-K plans are 256 x 256 x 128
+        return launch_gemm16_2cta<kBF16, kAMN, kNN, 256, 128, true>(ops, m, n, k, o, dev, p, stream);
     if (p.tile_k == 128) {
         if (p.tile_n == 224)
             return launch_gemm16_2cta<kBF16, kAMN, kNN, 224, 128>(ops, m, n, k, o, dev, p, stream);
@@ -826,6 +893,29 @@ int gemm_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
     info->ctas = p.ctas;
     info->tiles = p.tiles;
     info->cluster = p.cluster;
+    info->sk_tiles = p.sk_tiles;
+    return GEMM_OK;
+}
+
+int gemm_workspace_size(int dtype, int64_t M, int64_t N, int64_t K, int layout,
+                        const gemm_options* opts, uint64_t* bytes) {
+    g_err[0] = '\0';
+    if (!bytes) return fail(GEMM_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = 0;
+    gemm_options o = {};
+    if (opts) o = *opts;
+    if (o.stream_k == 2 || dtype == 2) return GEMM_OK;
+    o.workspace = reinterpret_cast<void*>(uintptr_t(256));  // stands for "large enough"
+    o.workspace_bytes = ~0ull;
+    gemm_plan_info info;
+    int rc = gemm_plan(dtype, M, N, K, layout, &o, &info);
+    if (rc) return rc;
+    if (info.sk_tiles) {
+        int dev;
+        DeviceInfo* d;
+        if ((rc = current_device(&dev, &d))) return rc;
+        *bytes = sk_workspace_bytes(std::max(1, d->sms / 2), 256);
+    }
     return GEMM_OK;
 }
 

@@ -16,6 +16,14 @@
 // arrives on the leader's accumulator-empty barrier (8 arrivals: 4 warps x 2 CTAs).
 // Compared with one CTA per 128 x 256 tile, every SM loads half as much of B per FLOP, and a stage
 // takes 16 + kBN/8 KiB of shared memory, which leaves room for a deeper ring.
+//
+// Stream-K (args.sk_tiles > 0): when the tiles do not fill the last wave, sk_tiles tiles are
+// shared out as equal runs of K-blocks over all pairs, before the whole tiles (WorkIter). A pair
+// whose run starts inside a tile writes that piece's fp32 partial sums to the workspace and raises
+// its flag (release, GPU scope); the pair whose run holds the tile's first K-block waits for those
+// flags (acquire, bounded), adds the pieces in K order (deterministic), stores C and lowers the
+// flags again, while its MMAs go on with the next tile. A pair waits only at the end of its run,
+// for pairs that produce their pieces at the start of theirs, so no cycle of waits can form.
 #pragma once
 
 #include "gemm_common.cuh"
@@ -52,7 +60,7 @@ struct Cfg {
 };
 }  // namespace g2
 
-template <bool kBF16, bool kAMN, bool kNN, int kBN, int kBK, int kStages>
+template <bool kBF16, bool kAMN, bool kNN, int kBN, int kBK, int kStages, bool kSK = false>
 __global__ void __launch_bounds__(g2::kThreads, 1)
     gemm16_2cta_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const Gemm16Args args) {
@@ -66,6 +74,7 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
     __shared__ __align__(8) uint64_t bar_tfull[2];
     __shared__ __align__(8) uint64_t bar_tempty[2];
     __shared__ __align__(8) uint64_t bar_drain;
+    __shared__ __align__(8) uint64_t bar_ep;  // stream-K: the epilogue threads are done with a piece
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
@@ -79,6 +88,7 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
     const int pair = blockIdx.x >> 1;
     const int num_pairs = gridDim.x >> 1;
     const int total = args.num_m * args.num_n;  // num_m counts 256-row pair tiles
+    const int sk_tiles = kSK ? args.sk_tiles : 0;  // whole tiles only unless built for stream-K
     volatile int* abort = &abort_flag;
 
     if (threadIdx.x == 0) {
@@ -91,6 +101,7 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
             mbar_init(smem_u32(&bar_tempty[b]), 8);  // 4 epilogue warps in each CTA
         }
         mbar_init(smem_u32(&bar_drain), 1);
+        mbar_init(smem_u32(&bar_ep), 128);
         abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -114,12 +125,14 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            for (int t = pair; t < total && ok; t += num_pairs) {
+            WorkIter wi(pair, num_pairs, total, sk_tiles, args.num_kb);
+            WorkItem w;
+            while (ok && wi.next(w)) {
                 int mt, nt;
-                tile_coords(t, args.num_m, args.num_n, kGroupM, mt, nt);
+                tile_coords(w.tile, args.num_m, args.num_n, kGroupM, mt, nt);
                 const int a_row = mt * 256 + (int)rank * kBMc;
                 const int b_row = nt * kBN + (int)rank * C_::kHalfN;
-                for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
+                for (int kb = w.k0; kb < w.k1; ++kb, ++it) {
                     const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
                     if (!wait_bounded(smem_u32(&bar_empty[s]), ph ^ 1u, abort, args.timeout_ns,
                                       &g_dtc_status, 11)) {
@@ -175,7 +188,9 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
             constexpr uint32_t idesc = idesc_f16(kBF16, kNN, 256, kBN, kAMN);
             uint32_t it = 0, acc = 0;
             bool ok = true, issued = false;
-            for (int t = pair; t < total && ok; t += num_pairs) {
+            WorkIter wi(pair, num_pairs, total, sk_tiles, args.num_kb);
+            WorkItem w;
+            while (ok && wi.next(w)) {
                 const uint32_t b = acc & 1u, aph = (acc >> 1) & 1u;
                 if (!wait_bounded(smem_u32(&bar_tempty[b]), aph ^ 1u, abort, args.timeout_ns,
                                   &g_dtc_status, 12)) {
@@ -184,7 +199,7 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * kAccStride;
-                for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
+                for (int kb = w.k0; kb < w.k1; ++kb, ++it) {
                     const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
                     if (!wait_bounded(smem_u32(&bar_full[s]), ph, abort, args.timeout_ns,
                                       &g_dtc_status, 13)) {
@@ -203,7 +218,7 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
                         const uint64_t bdesc =
                             kNN ? smem_desc_sw128(b0 + kk * 16 * 128, 64 * kBK * 2, 1024)
                                 : smem_desc_sw128(b0 + (kk / 4) * (C_::kHalfN * 128) + koff, 16, 1024);
-                        mma_f16_cta2(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+                        mma_f16_cta2(d_tmem, adesc, bdesc, idesc, (kb != w.k0 || kk != 0) ? 1u : 0u);
                     }
                     issued = true;
                     const uint32_t e = smem_u32(&bar_empty[s]);
@@ -225,46 +240,130 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
         // ------------------------------ epilogue (warps 2..5, both CTAs) ---------------------
         const int q = warp & 3;
         const int row_in_tile = q * 32 + lane;
-        uint32_t acc = 0;
-        for (int t = pair; t < total; t += num_pairs, ++acc) {
+        uint32_t acc = 0, ep_phase = 0;
+        WorkIter wi(pair, num_pairs, total, sk_tiles, args.num_kb);
+        WorkItem w;
+        while (wi.next(w)) {
             int mt, nt;
-            tile_coords(t, args.num_m, args.num_n, kGroupM, mt, nt);
+            tile_coords(w.tile, args.num_m, args.num_n, kGroupM, mt, nt);
             const uint32_t b = acc & 1u, aph = (acc >> 1) & 1u;
+            ++acc;
             int ok = 1;
             if (lane == 0)
-                ok = wait_bounded(smem_u32(&bar_tfull[b]), aph, abort, args.timeout_ns,
-                                  &g_dtc_status, 14);
+                ok = wait_bounded<false, true>(smem_u32(&bar_tfull[b]), aph, abort,
+                                               args.timeout_ns, &g_dtc_status, 14);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after_sync();
+            // stream-K: this CTA's workspace slot; for a first piece, the later units whose runs
+            // hold the rest of the tile (units pair+1 .. last_unit with a non-empty run)
+            float* my_slot = args.sk_partial + ((size_t)(pair * 2 + (int)rank) * kBMc + row_in_tile) * kBN;
+            int last_unit = pair;
+            auto sk_run_empty = [&](int u) {
+                return sk_start(u + 1, num_pairs, sk_tiles, args.num_kb) ==
+                       sk_start(u, num_pairs, sk_tiles, args.num_kb);
+            };
+            if (kSK && w.kind == kFirst) {
+                const int64_t tile_end = (int64_t)(w.tile + 1) * args.num_kb;
+                while (last_unit + 1 < num_pairs &&
+                       sk_start(last_unit + 1, num_pairs, sk_tiles, args.num_kb) < tile_end)
+                    ++last_unit;
+                for (int u = pair + 1; u <= last_unit && ok; ++u) {
+                    if (sk_run_empty(u)) continue;  // a unit with no K-blocks wrote nothing
+                    const uint32_t* f = args.sk_flags + u * 2 + (int)rank;
+                    if (lane == 0) ok = wait_flag_bounded(f, abort, args.timeout_ns, &g_dtc_status, 15);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (ok) (void)ld_acquire_gpu_u32(f);  // every lane takes its own acquire
+                }
+            }
             const int64_t row = (int64_t)mt * 256 + (int64_t)rank * kBMc + row_in_tile;
             uint16_t* crow = reinterpret_cast<uint16_t*>(args.C) + row * args.ldc;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + b * kAccStride;
-#pragma unroll 1
-            for (int c = 0; c < kBN / 32; ++c) {
-                uint32_t v[32];
-                tmem_load_32cols(taddr + c * 32, v);
+            // 32 accumulator columns of this thread's row -> 8 C elements per 16-byte store
+            auto store_chunk = [&](int c, const uint32_t (&v)[32]) {
+                if (row >= args.M) return;
+                const int col0 = nt * kBN + c * 32;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const int col = col0 + g * 8;
+                    if (col < args.N) {
+                        uint4 o;
+                        o.x = pack2<kBF16>(v[g * 8 + 0], v[g * 8 + 1]);
+                        o.y = pack2<kBF16>(v[g * 8 + 2], v[g * 8 + 3]);
+                        o.z = pack2<kBF16>(v[g * 8 + 4], v[g * 8 + 5]);
+                        o.w = pack2<kBF16>(v[g * 8 + 6], v[g * 8 + 7]);
+                        *reinterpret_cast<uint4*>(crow + col) = o;
+                    }
+                }
+            };
+            auto hand_back = [&](int c) {  // accumulator fully read: back to the MMA issuer
                 if (c == kBN / 32 - 1) {
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&bar_tempty[b]), 0));
                 }
-                if (row < args.M) {
-                    const int col0 = nt * kBN + c * 32;
+            };
+            if (!kSK || w.kind == kWhole) {
+#pragma unroll 1
+                for (int c = 0; c < kBN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_load_32cols(taddr + c * 32, v);
+                    hand_back(c);
+                    store_chunk(c, v);
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < kBN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_load_32cols(taddr + c * 32, v);
+                    hand_back(c);
+                    if (!ok) continue;
+                    if (w.kind == kOther) {  // partial sums of a piece another unit finishes
+                        float4* dst = reinterpret_cast<float4*>(my_slot + c * 32);
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        const int col = col0 + g * 8;
-                        if (col < args.N) {
-                            uint4 w;
-                            w.x = pack2<kBF16>(v[g * 8 + 0], v[g * 8 + 1]);
-                            w.y = pack2<kBF16>(v[g * 8 + 2], v[g * 8 + 3]);
-                            w.z = pack2<kBF16>(v[g * 8 + 4], v[g * 8 + 5]);
-                            w.w = pack2<kBF16>(v[g * 8 + 6], v[g * 8 + 7]);
-                            *reinterpret_cast<uint4*>(crow + col) = w;
+                        for (int g = 0; g < 8; ++g)
+                            dst[g] = make_float4(__uint_as_float(v[g * 4 + 0]), __uint_as_float(v[g * 4 + 1]),
+                                                 __uint_as_float(v[g * 4 + 2]), __uint_as_float(v[g * 4 + 3]));
+                        continue;
+                    }
+                    for (int u = pair + 1; u <= last_unit; ++u) {  // later pieces, in K order
+                        if (sk_run_empty(u)) continue;
+                        const float4* src = reinterpret_cast<const float4*>(
+                            my_slot + (size_t)(u - pair) * 2 * kBMc * kBN + c * 32);
+                        float4 p[8];
+#pragma unroll
+                        for (int g = 0; g < 8; ++g) p[g] = ld_global_cg_f4(src + g);
+#pragma unroll
+                        for (int g = 0; g < 8; ++g) {
+                            v[g * 4 + 0] = __float_as_uint(__uint_as_float(v[g * 4 + 0]) + p[g].x);
+                            v[g * 4 + 1] = __float_as_uint(__uint_as_float(v[g * 4 + 1]) + p[g].y);
+                            v[g * 4 + 2] = __float_as_uint(__uint_as_float(v[g * 4 + 2]) + p[g].z);
+                            v[g * 4 + 3] = __float_as_uint(__uint_as_float(v[g * 4 + 3]) + p[g].w);
+                        }
+                    }
+                    store_chunk(c, v);
+                }
+            }
+            if (kSK && w.kind != kWhole) {
+                // every epilogue thread of this CTA is done with the piece (an mbarrier, so a
+                // thread that gave up cannot leave the others waiting without a bound)
+                mbar_arrive(smem_u32(&bar_ep));
+                if (warp == 2 && lane == 0) {
+                    const bool all = wait_bounded(smem_u32(&bar_ep), ep_phase, abort,
+                                                  args.timeout_ns, &g_dtc_status, 16);
+                    if (all && ok) {
+                        if (w.kind == kOther) {
+                            __threadfence();
+                            st_release_gpu_u32(args.sk_flags + pair * 2 + (int)rank, 1u);
+                        } else {
+                            for (int u = pair + 1; u <= last_unit; ++u)  // consumed: back to zero
+                                if (!sk_run_empty(u)) args.sk_flags[u * 2 + (int)rank] = 0u;
                         }
                     }
                 }
+                ep_phase ^= 1u;
             }
+            if (!ok) break;
         }
     }
 

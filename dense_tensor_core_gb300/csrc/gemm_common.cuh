@@ -19,7 +19,62 @@ struct Gemm16Args {
     int num_m, num_n, num_kb;
     uint64_t timeout_ns;
     int fault;
+    // Stream-K (pair kernel): the last sk_tiles tiles are shared out as equal runs of K-blocks
+    // over all units; 0 = every tile whole. Partial sums go through the caller's workspace.
+    int sk_tiles;
+    uint32_t* sk_flags;  // one per (unit, CTA of the pair): 1 = that CTA's partial is written
+    float* sk_partial;   // per (unit, CTA): 128 rows x tile width fp32
 };
+
+// One unit of a persistent kernel's work: K-blocks [k0, k1) of tile `tile`.
+//   kind kWhole: the whole K range; kOther: a later piece of a tile another unit finishes (its
+//   partial sums go to the workspace); kFirst: the first piece, finished here with the pieces of
+//   units unit+1 .. unit+contrib.
+struct WorkItem {
+    int tile, k0, k1, kind;
+};
+constexpr int kWhole = 0, kOther = 1, kFirst = 2;
+
+// The work of `unit` of `units`: first its equal share [s0, s1) of the sk_tiles * kiters K-blocks
+// of tiles 0 .. sk_tiles-1 in (tile, K-block) order, then tiles sk_tiles + unit, + units, ...
+// whole. Shared tiles come first so that finishing them (waiting for other units' pieces, adding
+// them) overlaps the main loops of whole tiles instead of trailing the kernel. Every role of the
+// kernel walks the same sequence.
+struct WorkIter {
+    int t, total, units, kiters, sk_tiles;
+    int64_t i, s1;
+    __device__ WorkIter(int unit, int units_, int total_, int sk_tiles_, int kiters_)
+        : t(sk_tiles_ + unit), total(total_), units(units_), kiters(kiters_), sk_tiles(sk_tiles_) {
+        const int64_t S = (int64_t)sk_tiles_ * kiters_;
+        i = (int64_t)unit * S / units_;
+        s1 = (int64_t)(unit + 1) * S / units_;
+    }
+    __device__ bool next(WorkItem& w) {
+        if (i < s1) {
+            const int j = (int)(i / kiters);
+            w.tile = j;
+            w.k0 = (int)(i - (int64_t)j * kiters);
+            w.k1 = (int)min((int64_t)kiters, (int64_t)w.k0 + (s1 - i));
+            w.kind = w.k0 > 0 ? kOther : (w.k1 < kiters ? kFirst : kWhole);
+            i += w.k1 - w.k0;
+            return true;
+        }
+        if (t < total) {
+            w.tile = t;
+            w.k0 = 0;
+            w.k1 = kiters;
+            w.kind = kWhole;
+            t += units;
+            return true;
+        }
+        return false;
+    }
+};
+
+// First K-block of `unit`'s stream-K share (the start of its range).
+__device__ __forceinline__ int64_t sk_start(int unit, int units, int sk_tiles, int kiters) {
+    return (int64_t)unit * ((int64_t)sk_tiles * kiters) / units;
+}
 
 // Grouped rasterisation: tiles are numbered down groups of kGroupM M-tiles, N-tile by N-tile.
 __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int group_m, int& mt,

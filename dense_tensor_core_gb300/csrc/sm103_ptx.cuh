@@ -94,6 +94,25 @@ __device__ __forceinline__ void st_shared_u4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
+// Global-memory flags between CTAs of one grid: release store / acquire load at GPU scope, and
+// 16-byte loads that bypass L1 (data another CTA wrote).
+__device__ __forceinline__ void st_release_gpu_u32(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu_u32(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ float4 ld_global_cg_f4(const float4* p) {
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+
 // ---------------------------------------------------------------------------------------------
 // mbarrier (shared::cta)
 // ---------------------------------------------------------------------------------------------
@@ -173,6 +192,24 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
     while (true) {
         if (kBackoff) __nanosleep(64);
         if (try_wait()) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > timeout_ns) {
+            *abort = 1;
+            atomicCAS(status, 0, DTC_STATUS_TIMEOUT | site);
+            return false;
+        }
+    }
+}
+
+// Bounded wait for a global flag (set to 1 with a release store by another CTA of the grid).
+// Same give-up rules as wait_bounded.
+__device__ __forceinline__ bool wait_flag_bounded(const uint32_t* flag, volatile int* abort,
+                                                  uint64_t timeout_ns, int* status, int site) {
+    if (ld_acquire_gpu_u32(flag) == 1u) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        __nanosleep(128);
+        if (ld_acquire_gpu_u32(flag) == 1u) return true;
         if (*abort) return false;
         if (globaltimer_ns() - t0 > timeout_ns) {
             *abort = 1;

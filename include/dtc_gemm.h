@@ -98,6 +98,15 @@ typedef struct {
                              default, the pages' granularity) or 32 (the OCP MX block); the
                              scale arrays are then [rows, ceil(K / block)]. Non-default formats
                              or blocks run on the one-CTA kernel. */
+    void* workspace;      /* 16-bit products: device scratch for stream-K (see
+                             gemm_workspace_size), owned by the caller, 16-byte aligned; NULL =
+                             none. Its first 1 KB holds flags that must be zero before the first
+                             call that uses it; every completed call leaves them zero again (after
+                             a GEMM_ERR_TIMEOUT, zero them before reuse). Calls that may run at
+                             the same time (other streams) must not share a workspace. */
+    uint64_t workspace_bytes;
+    int stream_k;         /* 0 = use stream-K when a large enough workspace is given and the
+                             cost model prefers it; 1 = required (error if not possible); 2 = off */
 } gemm_options;
 
 /*
@@ -156,6 +165,7 @@ typedef struct {
     int ctas;     /* CTAs launched (persistent grid) */
     int tiles;    /* output tiles (times split_k work units for SPLITK) */
     int cluster;  /* CTAs per cluster */
+    int sk_tiles; /* tiles shared out by stream-K (0 = none) */
 } gemm_plan_info;
 
 /* Fills *info with the launch that gemm_ex would make for these sizes and options. Returns
@@ -163,6 +173,16 @@ typedef struct {
  * part of the plan). Makes no CUDA call except device queries. */
 int gemm_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm_options* opts,
               gemm_plan_info* info);
+
+/*
+ * Bytes of workspace (gemm_options.workspace) with which the call would use stream-K on CTA pairs
+ * (the last, part-full wave's tiles shared out over all pairs as equal runs of K-blocks, the
+ * pieces summed through the workspace); 0 when it would not (or stream_k == 2). The pages have
+ * no counterpart: their persistent 2-CTA variant (05 Blackwell TCGEN05 GEMM tutorial,
+ * "Advanced") takes whole tiles. INVALID_ARG as gemm_ex; bytes must not be NULL.
+ */
+int gemm_workspace_size(int dtype, int64_t M, int64_t N, int64_t K, int layout,
+                        const gemm_options* opts, uint64_t* bytes);
 
 /* Message for the calling thread's most recent non-OK return ("" if none). Valid until that
  * thread's next call into the library. */

@@ -148,7 +148,7 @@ def test_options_struct_matches_header():
         text = f.read()
     body = text[text.index("typedef struct {", text.index("gemm_variant;")):]
     body = body[: body.index("} gemm_options;")]
-    fields = re.findall(r"^\s*(?:int|uint64_t|int64_t)\s+(\w+);", body, re.M)
+    fields = re.findall(r"^\s*(?:int|uint64_t|int64_t|void\*)\s+(\w+);", body, re.M)
     assert fields == [n for n, _ in gemm_options._fields_]
 
 

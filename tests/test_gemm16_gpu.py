@@ -336,3 +336,78 @@ def test_transposed_layout_plans():
     # one-CTA 224-wide tiles need B stored [N,K]
     with pytest.raises(dtc.GemmError):
         dtc.gemm_plan("bf16", 4096, 4096, 8192, "TN", variant=1, tile_n=224)
+
+
+# --- stream-K on CTA pairs (the leftover tiles of the last wave shared out over all pairs) ------
+
+def _workspace(kind, M, N, K, layout):
+    import dense_tensor_core_gb300 as dtc
+
+    nbytes = dtc.gemm_workspace_size(kind, M, N, K, layout, stream_k=1)
+    assert nbytes > 0
+    return torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+
+
+@pytest.mark.parametrize("layout", ["NT", "NN", "TN", "TT"])
+@pytest.mark.parametrize("M,N,K", [(2560, 2560, 1024), (2560, 2304, 384), (2304, 2560, 640)])
+def test_stream_k_full_parity(M, N, K, layout):
+    # 100 (or 90) pair tiles of 256 x 256 over 76 pairs: one whole wave, then 24 (or 14) tiles
+    # shared out as runs of K-blocks; K = 384 gives fewer K-blocks than pairs, so some pairs have
+    # an empty share and tiles are split over up to 3 pairs; every piece, the flags and the fixup
+    # are exercised, and the flags must be back at zero afterwards
+    import dense_tensor_core_gb300 as dtc
+
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the shapes are chosen for 76 pairs")
+    kind = "bf16" if layout in ("NT", "TN") else "f16"
+    ws = _workspace(kind, M, N, K, layout)
+    p = dtc.gemm_plan(kind, M, N, K, layout, workspace=ws, stream_k=1)
+    assert (p["variant"], p["tile_n"], p["tile_k"]) == (2, 256, 128) and p["sk_tiles"] > 0
+    A, B = workloads.make16(kind, layout, M, N, K, seed=M + K)
+    At, Bt = to_device16(A, kind), to_device16(B, kind)
+    C1 = dtc.gemm_ex(kind, At, Bt, layout=layout, workspace=ws, stream_k=1)
+    C2 = dtc.gemm_ex(kind, At, Bt, layout=layout, workspace=ws, stream_k=1)
+    dtc.gemm_stream_status()
+    assert torch.equal(C1.view(torch.int16), C2.view(torch.int16)), "two runs differ"
+    assert int(ws[:1024].count_nonzero()) == 0, "stream-K flags not back at zero"
+    ref = oracle.gemm16(kind, layout, A, B, M, N, K)
+    check_close(values16(C1.view(torch.int16).cpu().numpy().view(np.uint16), kind),
+                values16(ref, kind), f"stream-K {layout} {M}x{N}x{K}")
+
+
+def test_stream_k_benchmark_size_sampled():
+    import dense_tensor_core_gb300 as dtc
+
+    w = workloads.WORKLOADS["bf16_nt_4096x4096x8192"]
+    A, B = _cached_inputs(w.name)
+    ws = _workspace(w.kind, w.M, w.N, w.K, w.layout)
+    C = dtc.gemm_ex(w.kind, to_device16(A, w.kind), to_device16(B, w.kind), layout=w.layout,
+                    workspace=ws, stream_k=1)
+    dtc.gemm_stream_status()
+    C = C.view(torch.int16).cpu().numpy().view(np.uint16)
+    r, c = sample_positions(w.M, w.N, count=3000, seed=w.seed, tile_m=256, tile_n=256)
+    r = np.concatenate([r, np.full(w.N, 4000), np.arange(w.M)])  # the stream-K rows are at the end
+    c = np.concatenate([c, np.arange(w.N), np.full(w.M, 3333)])
+    ref, _ = oracle.gemm16_sampled(w.kind, w.layout, A, B, w.M, w.N, w.K, r, c)
+    check_close(values16(C[r, c], w.kind), values16(ref, w.kind), "stream-K 4096x4096x8192")
+
+
+def test_stream_k_plan_choice():
+    import dense_tensor_core_gb300 as dtc
+
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the expected choices are worked out for 152 SMs")
+    ws = _workspace("bf16", 8192, 8192, 8192, "NT")
+    # 1024 pair tiles of 256 x 256 = 13.47 waves: with a workspace, the last 36 are shared out
+    p = dtc.gemm_plan("bf16", 8192, 8192, 8192, workspace=ws)
+    assert (p["variant"], p["tile_n"], p["sk_tiles"]) == (2, 256, 1024 % 76)
+    assert dtc.gemm_plan("bf16", 8192, 8192, 8192)["sk_tiles"] == 0  # no workspace: whole tiles
+    assert dtc.gemm_plan("bf16", 8192, 8192, 8192, workspace=ws, stream_k=2)["sk_tiles"] == 0
+    # 4096^2 x 8192: 304 tiles of 256 x 224 fill exactly 4 waves; the model keeps them
+    p = dtc.gemm_plan("bf16", 4096, 4096, 8192, workspace=ws)
+    assert (p["variant"], p["tile_n"], p["sk_tiles"]) == (2, 224, 0)
+    assert dtc.gemm_plan("bf16", 4096, 4096, 8192, workspace=ws, stream_k=1)["sk_tiles"] == 256 % 76
+    # a whole number of waves (76 x 2 tiles) needs no stream-K
+    assert dtc.gemm_workspace_size("bf16", 256 * 19, 256 * 8, 8192) == 0
+    with pytest.raises(dtc.GemmError):  # too small a workspace when stream-K is required
+        dtc.gemm_plan("bf16", 4096, 4096, 8192, workspace=ws[:1024], stream_k=1)

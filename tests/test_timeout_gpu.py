@@ -44,3 +44,29 @@ def test_wait_that_nothing_completes_reports_timeout_then_recovers(variant):
     ref = oracle.gemm16("bf16", "NT", A, B, M, N, K)
     got = C.view(torch.int16).cpu().numpy().view(np.uint16)
     check_close(values16(got, "bf16"), values16(ref, "bf16"), "after timeout")
+
+
+def test_stream_k_timeout_reports_and_recovers():
+    # a pair that never gets its first stage times out; the pairs waiting for its stream-K piece
+    # give up too (bounded), the call reports GEMM_ERR_TIMEOUT, and after the workspace is zeroed
+    # the next call is correct
+    import dense_tensor_core_gb300 as dtc
+
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the shape is chosen for 76 pairs")
+    M, N, K = 2560, 2560, 512
+    nbytes = dtc.gemm_workspace_size("bf16", M, N, K, stream_k=1)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    Ah, Bh = workloads.make16("bf16", "NT", M, N, K, seed=5)
+    A, B = to_device16(Ah, "bf16"), to_device16(Bh, "bf16")
+    dtc.gemm_stream_status()
+    dtc.gemm_ex("bf16", A, B, workspace=ws, stream_k=1, timeout_ns=20_000_000, fault_inject=1)
+    with pytest.raises(dtc.GemmError) as e:
+        dtc.gemm_stream_status()
+    assert e.value.status == 4
+    ws.zero_()
+    C = dtc.gemm_ex("bf16", A, B, workspace=ws, stream_k=1)
+    dtc.gemm_stream_status()
+    ref = oracle.gemm16("bf16", "NT", Ah, Bh, M, N, K)
+    check_close(values16(C.view(torch.int16).cpu().numpy().view(np.uint16), "bf16"),
+                values16(ref, "bf16"), "stream-K after a timeout")
