@@ -17,6 +17,7 @@ from ._binding import (  # noqa: F401
     GemmError,
     gemm_bf16,
     gemm_ex,
+    gemm_ex_static_workspace,
     gemm_f16,
     gemm_last_error,
     gemm_mxfp8,

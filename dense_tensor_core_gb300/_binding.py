@@ -72,6 +72,9 @@ def lib():
         L.gemm_plan.restype = i32
         L.gemm_plan.argtypes = [i32, i64, i64, i64, i32, ctypes.POINTER(gemm_options),
                                 ctypes.POINTER(gemm_plan_info)]
+        L.gemm_ex_static_workspace.restype = i32
+        L.gemm_ex_static_workspace.argtypes = [i32, vp, vp, vp, vp, vp, i64, i64, i64, i32,
+                                               ctypes.POINTER(gemm_options), vp]
         L.gemm_workspace_size.restype = i32
         L.gemm_workspace_size.argtypes = [i32, i64, i64, i64, i32, ctypes.POINTER(gemm_options),
                                           ctypes.POINTER(ctypes.c_uint64)]
@@ -271,3 +274,20 @@ def gemm_workspace_size(kind, M, N, K, layout="NT", variant=0, tile_n=0, tile_k=
     _check(lib().gemm_workspace_size(_DTYPE[kind], M, N, K, _layout_code(layout),
                                      ctypes.byref(opts), ctypes.byref(out)))
     return out.value
+
+
+def gemm_ex_static_workspace(kind, A, B, C=None, layout="NT", variant=0, tile_n=0, tile_k=0,
+                             stream_k=0, stream=None):
+    """gemm_ex for the 16-bit products, with the library's own (module-memory) stream-K workspace:
+    allocates nothing. Calls on one device must not overlap (they share that workspace)."""
+    dt = torch.bfloat16 if kind == "bf16" else torch.float16
+    _check_tensor(A, dt, "A", rows_of_larger=True)
+    _check_tensor(B, dt, "B", rows_of_larger=True)
+    M, N, K = _shapes16(A, B, layout)
+    C = _out(C, M, N, dt, A.device, rows_of_larger=True)
+    opts = _options(variant, 0, 0, 0, tile_n, 0, tile_k, _ld(A), _ld(B), _ld(C),
+                    stream_k=stream_k)
+    _check(lib().gemm_ex_static_workspace(_DTYPE[kind], _ptr(A), _ptr(B), None, None, _ptr(C),
+                                          M, N, K, _layout_code(layout), ctypes.byref(opts),
+                                          _stream_handle(stream)))
+    return C

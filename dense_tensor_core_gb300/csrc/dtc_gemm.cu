@@ -53,6 +53,7 @@ struct DeviceInfo {
     int major = 0, minor = 0;
     std::unordered_set<const void*> smem_attr_set;  // kernels whose smem limit was raised
     int clusters_for[5] = {0, 0, 0, 0, 0};         // co-resident clusters of 1, 2, 4 CTAs
+    void* static_ws = nullptr;                      // address of g_static_ws on this device
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -862,6 +863,38 @@ int gemm_ex(int dtype, const void* A, const void* B, const void* sfA, const void
             int64_t M, int64_t N, int64_t K, int layout, const gemm_options* opts,
             dtc_stream_t stream) {
     return run(dtype, A, B, sfA, sfB, C, M, N, K, layout, opts, (cudaStream_t)stream);
+}
+
+int gemm_ex_static_workspace(int dtype, const void* A, const void* B, const void* sfA,
+                             const void* sfB, void* C, int64_t M, int64_t N, int64_t K,
+                             int layout, const gemm_options* opts, dtc_stream_t stream) {
+    g_err[0] = '\0';
+    if (opts && opts->workspace)
+        return fail(GEMM_ERR_INVALID_ARG, "this entry point supplies its own workspace: leave opts->workspace NULL");
+    int dev;
+    DeviceInfo* info;
+    int rc = current_device(&dev, &info);
+    if (rc) return rc;
+    {
+        std::lock_guard<std::mutex> lk(g_dev_mu);
+        if (!info->static_ws) {  // once per device (a synchronous call: not inside stream capture)
+            void* p = nullptr;
+            cudaError_t e = cudaGetSymbolAddress(&p, dtc::g_static_ws);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static workspace)");
+            info->static_ws = p;
+        }
+    }
+    gemm_options o = {};
+    if (opts) o = *opts;
+    o.workspace = info->static_ws;
+    o.workspace_bytes = dtc::kStaticWsBytes;
+    // the flags must be zero when a launch starts: every completed call leaves them zero, but a
+    // call that gave up (GEMM_ERR_TIMEOUT) may not, so clear them, in stream order, each time
+    if (dtype != 2) {
+        cudaError_t e = cudaMemsetAsync(info->static_ws, 0, kSkFlagBytes, (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static workspace flags)");
+    }
+    return run(dtype, A, B, sfA, sfB, C, M, N, K, layout, &o, (cudaStream_t)stream);
 }
 
 int gemm_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm_options* opts,

@@ -11,6 +11,13 @@ namespace dtc {
 
 __device__ int g_dtc_status;  // first device-side wait that gave up (0 = none)
 
+// Scratch of gemm_ex_static_workspace: the stream-K workspace (flags, then the pieces' partial
+// sums) in module memory, zero at load, so that entry point allocates nothing. 20 MiB holds the
+// stream-K workspace of 76 CTA pairs (152 SMs) with 256-wide tiles: 1 KB of flags + 76 x 2 x 128
+// x 256 fp32.
+constexpr uint64_t kStaticWsBytes = 20ull << 20;
+static __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
+
 
 struct Gemm16Args {
     void* C;

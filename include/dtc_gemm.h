@@ -175,6 +175,25 @@ int gemm_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
               gemm_plan_info* info);
 
 /*
+ * gemm_ex, with the library's own stream-K workspace instead of a caller's: a 20 MiB region of
+ * module memory (a file-scope device array, zero when the library is loaded), so this call
+ * allocates nothing, on the host or the device. The pages have no counterpart.
+ *   - opts->workspace must be NULL (INVALID_ARG otherwise); the other options are gemm_ex's.
+ *   - A product whose stream-K plan needs more than 20 MiB (a device with more than 152 SMs)
+ *     runs without stream-K, or fails with INVALID_ARG when opts->stream_k = 1 (required).
+ *   - The first call on a device looks up the region's address with cudaGetSymbolAddress (a
+ *     synchronous call): make one call on the device before capturing a stream into a graph.
+ *   - The region's first 1 KB (flags) must be zero when a launch starts: each call clears it
+ *     with cudaMemsetAsync on `stream` before its launch (so a call after a GEMM_ERR_TIMEOUT
+ *     starts clean), and every completed launch leaves it zero.
+ *   - There is one region per device: calls that may overlap (on different streams, or from
+ *     different threads) race on it and may return wrong results. Serialise them.
+ */
+int gemm_ex_static_workspace(int dtype, const void* A, const void* B, const void* sfA,
+                             const void* sfB, void* C, int64_t M, int64_t N, int64_t K,
+                             int layout, const gemm_options* opts, dtc_stream_t stream);
+
+/*
  * Bytes of workspace (gemm_options.workspace) with which the call would use stream-K on CTA pairs
  * (the last, part-full wave's tiles shared out over all pairs as equal runs of K-blocks, the
  * pieces summed through the workspace); 0 when it would not (or stream_k == 2). The pages have

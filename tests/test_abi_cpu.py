@@ -140,6 +140,19 @@ def test_block_scaled_options_rejected_before_cuda(L, dtype, opt):
     assert L.gemm_last_error()
 
 
+def test_static_workspace_entry_refuses_a_caller_workspace(L):
+    from dense_tensor_core_gb300._binding import gemm_options
+
+    vp = ctypes.c_void_p
+    o = gemm_options()
+    o.workspace = 0x4000
+    o.workspace_bytes = 1 << 20
+    rc = L.gemm_ex_static_workspace(0, vp(0x1000), vp(0x2000), None, None, vp(0x3000), 16, 16, 16,
+                                    0, ctypes.byref(o), None)
+    assert rc == INVALID
+    assert L.gemm_last_error()
+
+
 def test_options_struct_matches_header():
     # the binding's ctypes mirror of gemm_options lists the header's fields in order
     from dense_tensor_core_gb300._binding import gemm_options
