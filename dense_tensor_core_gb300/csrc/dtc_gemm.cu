@@ -341,8 +341,10 @@ double choice_efficiency(int variant, int bn, int bk) {
 // the leftover tiles are shared out over all pairs as equal runs of K-blocks, their pieces summed
 // through the caller's workspace. Taken when a large enough workspace is given, the request
 // allows the pair kernel with these tiles, and the cost model beats the plan already made: work
-// per pair / efficiency, plus half a tile's time for the pieces' exchange and the shorter runs
-// (measured on GB300: a gain on 8192^3, a wash against 224-wide whole tiles on 4096^2 x 8192).
+// per pair / efficiency, plus 0.4 of a tile's time for the pieces' exchange and the shorter runs
+// (measured on GB300: +2-4 % on 8192^3; on 4096^2 x 8192 within 1 % of 224-wide whole tiles, on
+// average slightly ahead, which this constant encodes). Sharing a whole wave more (longer runs,
+// fewer splits) measured worse on both.
 // Required or refused with opts->stream_k.
 int plan_stream_k(int64_t M, int64_t N, int64_t K, const gemm_options* o, DeviceInfo* d, Plan* p) {
     const int mode = o ? o->stream_k : 0;
@@ -364,7 +366,7 @@ int plan_stream_k(int64_t M, int64_t N, int64_t K, const gemm_options* o, Device
                     (unsigned long long)sk_workspace_bytes(units, 256));
     if (!allowed || !ws_ok) return GEMM_OK;
     const double eff = choice_efficiency(GEMM_VARIANT_2CTA, 256, 128);
-    const double sk_cost = ((double)tiles / units + 0.5) * 256 / eff;
+    const double sk_cost = ((double)tiles / units + 0.4) * 256 / eff;
     const double dp_cost = plan_cost(p->variant, p->tile_n,
                                      choice_efficiency(p->variant, p->tile_n, p->tile_k), M, N, d->sms);
     if (mode == 0 && sk_cost >= dp_cost) return GEMM_OK;
