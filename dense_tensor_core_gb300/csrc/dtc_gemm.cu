@@ -385,7 +385,6 @@ int plan_stream_k(int64_t M, int64_t N, int64_t K, const gemm_options* o, Device
 
 int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm_options* o,
               DeviceInfo* d, Plan* p) {
-    (void)K;
     int v = o ? o->variant : GEMM_VARIANT_AUTO;
     const int want_n = o ? o->tile_n : 0;
     const bool b_mn = layout_b_mn(layout);  // B stored [K,N]: 64-column boxes

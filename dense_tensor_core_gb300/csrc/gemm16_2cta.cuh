@@ -5,9 +5,10 @@
 //
 // A pair computes a 256 x kBN tile of C. CTA r of the pair (r = 0 is the leader):
 //   - loads its own 128 rows of A (rows 256*mt + 128*r) and its own kBN/2 rows of B^T
-//     (columns kBN*nt + r*kBN/2 of C) into its own shared memory, 64-deep K-blocks, a kStages ring;
-//     both CTAs' copies complete on the LEADER's full barrier (cp.async.bulk.tensor .cta_group::2),
-//     which the leader arms with the bytes of both CTAs;
+//     (columns kBN*nt + r*kBN/2 of C) into its own shared memory, kBK-deep K-blocks (64, or 128
+//     as two 128-byte K-chunks per 3-D box), a kStages ring; either operand K-major or MN-major
+//     (kAMN, kNN); both CTAs' copies complete on the LEADER's full barrier (cp.async.bulk.tensor
+//     .cta_group::2), which the leader arms with the bytes of both CTAs;
 //   - holds rows 128*r..128*r+127 of the accumulator in its own Tensor Memory.
 // The leader's single MMA thread issues tcgen05.mma.cta_group::2 (M = 256, N = kBN, K = 16); the
 // tensor cores of both SMs read A and B from both CTAs' shared memory at the same offsets. Its
@@ -17,7 +18,7 @@
 // Compared with one CTA per 128 x 256 tile, every SM loads half as much of B per FLOP, and a stage
 // takes 16 + kBN/8 KiB of shared memory, which leaves room for a deeper ring.
 //
-// Stream-K (args.sk_tiles > 0): when the tiles do not fill the last wave, sk_tiles tiles are
+// Stream-K (kSK and args.sk_tiles > 0): when the tiles do not fill the last wave, sk_tiles tiles are
 // shared out as equal runs of K-blocks over all pairs, before the whole tiles (WorkIter). A pair
 // whose run starts inside a tile writes that piece's fp32 partial sums to the workspace and raises
 // its flag (release, GPU scope); the pair whose run holds the tile's first K-block waits for those

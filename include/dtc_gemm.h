@@ -82,8 +82,8 @@ typedef struct {
     int fault_inject;     /* test hook, 0 in normal use. 1 = the load producer skips its first
                              stage, so the consumer's bounded wait runs out and the call reports
                              GEMM_ERR_TIMEOUT through gemm_stream_status. */
-    int tile_n;           /* force the N-tile: 256, 224 (NT only; not SPLITK) or 128 (SPLITK
-                             only); 0 = choose */
+    int tile_n;           /* force the N-tile: 256, 224 (not SPLITK; one-CTA tiles need B stored
+                             [N,K]) or 128 (SPLITK only); 0 = choose */
     int cluster_m;        /* 1CTA only: CTAs per cluster along M sharing B by multicast (1 or
                              2); 0 = choose */
     int tile_k;           /* K-elements per pipeline stage: 64 or 32 (1CTA), 64 or 128 (2CTA;
