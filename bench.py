@@ -185,29 +185,36 @@ class ClockSampler:
 # CPU oracle leg
 # ------------------------------------------------------------------------------------------------
 
-def oracle_rows(w, inputs, rows):
-    """Run the oracle on the first `rows` output rows of workload w; returns seconds taken."""
+def oracle_rows(w, inputs, rows, cols=None):
+    """Run the oracle on the first `rows` output rows (and the first `cols` output columns, all of
+    them by default) of workload w; returns seconds taken."""
     import numpy as np
 
     import oracle
 
+    cols = w.N if cols is None else cols
     t0 = time.perf_counter()
     if w.kind == "mxfp8":
         A, B, sfA, sfB = inputs
-        oracle.gemm_mx(A[:rows], B, sfA[:rows], sfB, rows, w.N, w.K, a_fmt=w.a_fmt,
+        oracle.gemm_mx(A[:rows], B[:cols], sfA[:rows], sfB[:cols], rows, cols, w.K, a_fmt=w.a_fmt,
                        b_fmt=w.b_fmt, block=w.block)
     else:
         A, B = inputs
-        # output rows m are rows of A, or its columns when A is stored [K,M]
+        # output rows m are rows of A, or its columns when A is stored [K,M]; output columns n
+        # are rows of B when it is stored [N,K], else its columns
         Ar = A[:, :rows] if w.layout[0] == "T" else A[:rows]
-        oracle.gemm16(w.kind, w.layout, np.ascontiguousarray(Ar), B, rows, w.N, w.K)
+        Bc = B[:cols] if w.layout[1] == "T" else B[:, :cols]
+        oracle.gemm16(w.kind, w.layout, np.ascontiguousarray(Ar), np.ascontiguousarray(Bc), rows,
+                      cols, w.K)
     return time.perf_counter() - t0
 
 
 def calibrate_rows(w, inputs, target_s):
-    """Rows of C the oracle computes in about target_s seconds (at least 1, at most M).
+    """(rows, cols) of C the oracle computes in about target_s seconds.
 
-    Two probes separate the fixed cost of a call (decoding B) from the cost per output row."""
+    Two probes over all N columns separate the fixed cost of a call (decoding B) from the cost per
+    output row. When the fixed cost alone would take more than half the budget, the sample keeps
+    fewer columns (both costs scale with them), so that many short steps stay short."""
     import oracle
 
     T = oracle.threads()  # probes are whole multiples of the worker count
@@ -218,18 +225,25 @@ def calibrate_rows(w, inputs, target_s):
     if per_row <= 0.0:
         per_row = t2 / max(r2, 1)
     fixed = max(t1 - r1 * per_row, 0.0)
-    return max(1, min(w.M, int((target_s - fixed) / per_row))), per_row
+    cols = w.N
+    if fixed > target_s / 2:
+        frac = (target_s / 2) / fixed
+        cols = max(8, min(w.N, int(w.N * frac)) // 8 * 8)
+        per_row *= cols / w.N
+        fixed *= cols / w.N
+    rows = max(1, min(w.M, int((target_s - fixed) / per_row)))
+    return rows, cols
 
 
 def cpu_baseline(w, inputs, target_s=15.0):
     import oracle
 
-    rows, _ = calibrate_rows(w, inputs, target_s)
-    dt = oracle_rows(w, inputs, rows)
-    flops = 2.0 * rows * w.N * w.K
+    rows, cols = calibrate_rows(w, inputs, target_s)
+    dt = oracle_rows(w, inputs, rows, cols)
+    flops = 2.0 * rows * cols * w.K
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
-            "sample": f"{rows} of {w.M} output rows of {w.name} (all N={w.N} columns, full K), "
-                      f"{dt:.1f} s"}
+            "sample": f"{rows} of {w.M} output rows x {cols} of {w.N} columns of {w.name} "
+                      f"(full K), {dt:.1f} s"}
 
 
 # ------------------------------------------------------------------------------------------------
@@ -244,12 +258,12 @@ def run_reference(args, w):
 
     inputs = __import__("dense_tensor_core_gb300.workloads", fromlist=["make"]).make(w)
     per_step_budget = min(10.0, 150.0 / max(1, args.steps + args.warmup))
-    rows, _ = calibrate_rows(w, inputs, per_step_budget)
+    rows, cols = calibrate_rows(w, inputs, per_step_budget)
     for _ in range(args.warmup):
-        oracle_rows(w, inputs, rows)
-    times = [oracle_rows(w, inputs, rows) for _ in range(args.steps)]
+        oracle_rows(w, inputs, rows, cols)
+    times = [oracle_rows(w, inputs, rows, cols) for _ in range(args.steps)]
     total = sum(times)
-    flops = 2.0 * rows * w.N * w.K * args.steps
+    flops = 2.0 * rows * cols * w.K * args.steps
     value = flops / total / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -257,9 +271,11 @@ def run_reference(args, w):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout,
-                   "kind": w.kind, "step": f"oracle on {rows} output rows (bounded sample)"},
+                   "kind": w.kind,
+                   "step": f"oracle on {rows} output rows x {cols} columns (bounded sample)"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
-                         "sample": f"{rows} of {w.M} output rows per step, full N and K"},
+                         "sample": f"{rows} of {w.M} output rows x {cols} of {w.N} columns per "
+                                   f"step, full K"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
