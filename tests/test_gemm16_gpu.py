@@ -413,3 +413,24 @@ def test_stream_k_plan_choice():
     assert dtc.gemm_workspace_size("bf16", 256 * 19, 256 * 8, 8192) == 0
     with pytest.raises(dtc.GemmError):  # too small a workspace when stream-K is required
         dtc.gemm_plan("bf16", 4096, 4096, 8192, workspace=ws[:1024], stream_k=1)
+
+
+def test_stream_k_with_rows_of_larger_arrays():
+    # stream-K pieces and fixup with A stored [K,M] in a wider array and C a view with ldc > N
+    import dense_tensor_core_gb300 as dtc
+
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the shape is chosen for 76 pairs")
+    M, N, K = 2560, 2560, 768
+    A, B = workloads.make16("bf16", "TN", M, N, K, seed=99)
+    Ab = torch.zeros((K, M + 64), dtype=torch.bfloat16, device="cuda")
+    Ab[:, :M] = to_device16(A, "bf16")
+    Cb = torch.full((M, N + 32), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = _workspace("bf16", M, N, K, "TN")
+    dtc.gemm_ex("bf16", Ab[:, :M], to_device16(B, "bf16"), Cb[:, :N], layout="TN", workspace=ws,
+                stream_k=1)
+    dtc.gemm_stream_status()
+    assert torch.isnan(Cb[:, N:].float()).all()
+    C = Cb[:, :N].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    ref = oracle.gemm16("bf16", "TN", A, B, M, N, K)
+    check_close(values16(C, "bf16"), values16(ref, "bf16"), "stream-K, strided")

@@ -246,3 +246,25 @@ def test_format_options_plan():
     assert (p["variant"], p["tile_k"]) == (1, 256)
     with pytest.raises(dtc.GemmError):  # the pair kernel takes the pages' format only
         dtc.gemm_plan("mxfp8", 4096, 4096, 8192, variant=2, scale_block=32)
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+def test_rows_of_larger_arrays(variant):
+    # A, B and C as views into wider row-major arrays: lda, ldb (bytes of e4m3) and ldc go to the
+    # library; C's padding columns stay untouched
+    import dense_tensor_core_gb300 as dtc
+
+    M, N, K = 384, 448, 512
+    A, B, sfA, sfB = workloads.make_mxfp8(M, N, K, seed=21)
+    Ab = torch.zeros((M, K + 48), dtype=torch.uint8, device="cuda")
+    Bb = torch.zeros((N, K + 16), dtype=torch.uint8, device="cuda")
+    Ab[:, :K] = to_device8(A)
+    Bb[:, :K] = to_device8(B)
+    Cb = torch.full((M, N + 24), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dtc.gemm_ex("mxfp8", Ab[:, :K], Bb[:, :K], Cb[:, :N], sfA=to_device8(sfA), sfB=to_device8(sfB),
+                variant=variant)
+    dtc.gemm_stream_status()
+    assert torch.isnan(Cb[:, N:].float()).all(), "padding columns of C were written"
+    C = Cb[:, :N].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    ref = oracle.gemm_mxfp8(A, B, sfA, sfB, M, N, K)
+    check_close(values16(C, "bf16"), values16(ref, "bf16"), f"strided mxfp8 variant {variant}")
