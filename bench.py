@@ -337,6 +337,37 @@ def run_e2e(w, dtc, host_in, dev_in, C, host_out, step_e2e, stream, steps, dev):
     return e0.elapsed_time(e1)
 
 
+def library_context(w, A, B, flush_l2, stream, steps, dev):
+    """torch.matmul (cuBLAS) on the same device operands, with the same L2 flush and per-step
+    CUDA-event timing: a context figure beside ours, not a baseline and not on our path. None for
+    the block-scaled workloads (torch has no product with one E8M0 scale per row per 128 or 32
+    K-elements in this row-major scale layout)."""
+    import torch
+
+    if w.kind == "mxfp8":
+        return None
+    a_op = A.t() if w.layout[0] == "T" else A  # A stored [K,M] for TN and TT
+    b_op = B.t() if w.layout[1] == "T" else B  # B stored [N,K] for NT and TT
+    out = torch.empty((w.M, w.N), dtype=A.dtype, device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            flush_l2(1)
+            torch.matmul(a_op, b_op, out=out)
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        for i in range(steps):
+            flush_l2(i)
+            starts[i].record(stream)
+            torch.matmul(a_op, b_op, out=out)
+            ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    return {"torch_matmul": w.flops / (ms / 1e3) / 1e12, "unit": UNIT, "steps": steps,
+            "what": "cuBLAS through torch.matmul on the same device tensors (transposed views "
+                    "for the stored layouts), same L2 flush and CUDA-event timing, outside our "
+                    "timed region: context only"}
+
+
 def run_ours(args, w):
     import numpy as np
     import torch
@@ -457,6 +488,8 @@ def run_ours(args, w):
     d2h = host_out.numel() * host_out.element_size()
     e2e_value = world * flops_step * e2e_steps / (e2e_ms / 1e3) / 1e12
 
+    library = library_context(w, A, B, flush_l2, stream, min(args.steps, 50), dev)
+
     if rank != 0:
         if world > 1:
             import torch.distributed as dist
@@ -513,6 +546,7 @@ def run_ours(args, w):
                         "(3 streams, 2 device buffers); pinned host memory"},
         "gpu_launches": args.steps,
         "clocks": clocks,
+        "library_context": library,
     }
     if not args.skip_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, inputs, target_s=args.cpu_seconds)

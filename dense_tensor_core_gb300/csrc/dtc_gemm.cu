@@ -590,9 +590,9 @@ Gemm16Args make_args(const Operands& ops, int M, int N, int K, int tile_m, int t
     return a;
 }
 
-template <typename Kern>
+template <typename Kern, typename... Params>
 int launch_cluster(Kern kern, int grid, int threads, int smem, int cluster, cudaStream_t stream,
-                   const CUtensorMap& tA, const CUtensorMap& tB, const Gemm16Args& args) {
+                   const Params&... params) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(threads, 1, 1);
@@ -605,10 +605,22 @@ int launch_cluster(Kern kern, int grid, int threads, int smem, int cluster, cuda
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = cluster > 1 ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tA, tB, args);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, params...);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     return GEMM_OK;
+}
+
+// Tensor maps of a 16-bit C [M, N] (rows ldc elements apart) for the TMA-store epilogues: boxes
+// of 32 rows x 64 columns with the 128-byte swizzle, and of 32 rows x 32 columns with the 64-byte
+// swizzle (the last chunk of a 224-wide tile).
+int tmap_c16(CUtensorMap* c64, CUtensorMap* c32, CUtensorMapDataType dt, const Operands& ops,
+             int64_t M, int64_t N) {
+    int rc = make_tmap(c64, dt, 2, ops.C, (uint64_t)N, (uint64_t)M, (uint64_t)ops.ldc, 64, 32,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "C");
+    if (rc) return rc;
+    return make_tmap(c32, dt, 2, ops.C, (uint64_t)N, (uint64_t)M, (uint64_t)ops.ldc, 32, 32,
+                     CU_TENSOR_MAP_SWIZZLE_64B, "C");
 }
 
 template <bool kBF16, bool kAMN, bool kNN, int kBN, int kBK, int kStages, int kCM>
@@ -637,10 +649,13 @@ int launch_gemm16_2cta(const Operands& ops, int M, int N, int K, const gemm_opti
     int rc = tmap_operand16(&tA, dt, ops.A, ops.lda, kAMN, M, K, kBK, 128, "A");
     if (rc) return rc;
     if ((rc = tmap_operand16(&tB, dt, ops.B, ops.ldb, kNN, N, K, kBK, Cfg::kHalfN, "B"))) return rc;
+    CUtensorMap tC, tC32;
+    if ((rc = tmap_c16(&tC, &tC32, dt, ops, M, N))) return rc;
     auto kern = dtc::gemm16_2cta_kernel<kBF16, kAMN, kNN, kBN, kBK, kStages, kSK>;
     if ((rc = ensure_smem_attr(kern, Cfg::kSmemBytes, dev))) return rc;
     const Gemm16Args args = make_args(ops, M, N, K, 256, kBN, kBK, o, p.sk_tiles);
-    return launch_cluster(kern, p.ctas, dtc::g2::kThreads, Cfg::kSmemBytes, 2, stream, tA, tB, args);
+    return launch_cluster(kern, p.ctas, dtc::g2::kThreads, Cfg::kSmemBytes, 2, stream, tA, tB, tC,
+                          tC32, args);
 }
 
 template <bool kBF16, bool kAMN, bool kNN, int kBN, int kBK, int kStages>

@@ -55,7 +55,10 @@ struct Cfg {
     static constexpr int kBStage = kBMN ? kBBoxes * 64 * kBK * 2 : kHalfN * kBK * 2;
     static_assert(kBK == 64 || kBK == 128, "K-block of 64 or 128");
     static constexpr int kStageBytes = kAStage + kBStage;
-    static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+    static_assert(kStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+    // output staging: two 4 KB slots (32 rows x 64 columns of 16-bit C) per epilogue warp
+    static constexpr int kCBytes = 4 * 2 * 4096;
+    static constexpr int kSmemBytes = kStages * kStageBytes + kCBytes + 1024;
     static_assert(kBN % 32 == 0 && kBN >= 64 && kBN <= 256, "pair tile N must be 64..256, /32");
     static_assert(kSmemBytes <= 227 * 1024 - 256, "shared memory budget");
 };
@@ -64,7 +67,9 @@ struct Cfg {
 template <bool kBF16, bool kAMN, bool kNN, int kBN, int kBK, int kStages, bool kSK = false>
 __global__ void __launch_bounds__(g2::kThreads, 1)
     gemm16_2cta_kernel(const __grid_constant__ CUtensorMap tmA,
-                       const __grid_constant__ CUtensorMap tmB, const Gemm16Args args) {
+                       const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmC,
+                       const __grid_constant__ CUtensorMap tmC32, const Gemm16Args args) {
     using namespace g2;
     using C_ = Cfg<kBN, kBK, kStages, kNN>;
     constexpr int kChunks = kBK / 64;  // 128-byte K-chunks per stage
@@ -110,6 +115,7 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmC);
     }
     if (warp == 1) {
         tmem_alloc<2>(smem_u32(&tmem_slot), kTmemCols);
@@ -240,8 +246,8 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
     } else {
         // ------------------------------ epilogue (warps 2..5, both CTAs) ---------------------
         const int q = warp & 3;
-        const int row_in_tile = q * 32 + lane;
-        uint32_t acc = 0, ep_phase = 0;
+        const uint32_t my_slots = base + kStages * C_::kStageBytes + (uint32_t)q * 8192u;
+        uint32_t acc = 0, ep_phase = 0, stores = 0;
         WorkIter wi(pair, num_pairs, total, sk_tiles, args.num_kb);
         WorkItem w;
         while (wi.next(w)) {
@@ -258,7 +264,6 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
             tc_fence_after_sync();
             // stream-K: this CTA's workspace slot; for a first piece, the later units whose runs
             // hold the rest of the tile (units pair+1 .. last_unit with a non-empty run)
-            float* my_slot = args.sk_partial + ((size_t)(pair * 2 + (int)rank) * kBMc + row_in_tile) * kBN;
             int last_unit = pair;
             auto sk_run_empty = [&](int u) {
                 return sk_start(u + 1, num_pairs, sk_tiles, args.num_kb) ==
@@ -277,72 +282,95 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
                     if (ok) (void)ld_acquire_gpu_u32(f);  // every lane takes its own acquire
                 }
             }
-            const int64_t row = (int64_t)mt * 256 + (int64_t)rank * kBMc + row_in_tile;
-            uint16_t* crow = reinterpret_cast<uint16_t*>(args.C) + row * args.ldc;
+            const int band_y = mt * 256 + (int)rank * kBMc + q * 32;  // C row of lane 0
+            const int x0 = nt * kBN;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + b * kAccStride;
-            // 32 accumulator columns of this thread's row -> 8 C elements per 16-byte store
-            auto store_chunk = [&](int c, const uint32_t (&v)[32]) {
-                if (row >= args.M) return;
-                const int col0 = nt * kBN + c * 32;
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const int col = col0 + g * 8;
-                    if (col < args.N) {
-                        uint4 o;
-                        o.x = pack2<kBF16>(v[g * 8 + 0], v[g * 8 + 1]);
-                        o.y = pack2<kBF16>(v[g * 8 + 2], v[g * 8 + 3]);
-                        o.z = pack2<kBF16>(v[g * 8 + 4], v[g * 8 + 5]);
-                        o.w = pack2<kBF16>(v[g * 8 + 6], v[g * 8 + 7]);
-                        *reinterpret_cast<uint4*>(crow + col) = o;
-                    }
-                }
+            auto hand_back = [&]() {  // accumulator fully read: back to the MMA issuer
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&bar_tempty[b]), 0));
             };
-            auto hand_back = [&](int c) {  // accumulator fully read: back to the MMA issuer
-                if (c == kBN / 32 - 1) {
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&bar_tempty[b]), 0));
-                }
-            };
+            // 64-column chunks (and a last 32-column one for 224-wide tiles): TMEM -> registers
+            // -> 16-bit in a staging slot -> TMA store
+            constexpr int kFull = kBN / 64;
+            constexpr bool kTail = (kBN % 64) != 0;
             if (!kSK || w.kind == kWhole) {
 #pragma unroll 1
-                for (int c = 0; c < kBN / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_load_32cols(taddr + c * 32, v);
-                    hand_back(c);
-                    store_chunk(c, v);
+                for (int c = 0; c < kFull; ++c) {
+                    uint32_t v[64];
+                    tmem_load_64cols(taddr + c * 64, v);
+                    if (!kTail && c == kFull - 1) hand_back();
+                    store_chunk16<kBF16, 64>(&tmC, my_slots, stores, v, x0 + c * 64, band_y,
+                                             args.M, args.N, lane);
                 }
-            } else {
-#pragma unroll 1
-                for (int c = 0; c < kBN / 32; ++c) {
+                if constexpr (kTail) {
                     uint32_t v[32];
-                    tmem_load_32cols(taddr + c * 32, v);
-                    hand_back(c);
+                    tmem_load_32cols(taddr + kFull * 64, v);
+                    hand_back();
+                    store_chunk16<kBF16, 32>(&tmC32, my_slots, stores, v, x0 + kFull * 64, band_y,
+                                             args.M, args.N, lane);
+                }
+            } else if constexpr (kSK) {
+                // Pieces of shared tiles, 64-column chunks. The workspace slot of a CTA holds its
+                // 128 x 256 fp32 partial sums warp-interleaved (float4 number ((c*4 + q)*16 + g)*32
+                // + lane = columns 64c + 4g .. +3 of row 32q + lane), so every warp-wide access
+                // moves 512 contiguous bytes.
+                static_assert(!kTail, "stream-K tiles are 64-column multiples");
+                float4* const mine4 = reinterpret_cast<float4*>(
+                    args.sk_partial + (size_t)(pair * 2 + (int)rank) * kBMc * kBN);
+                auto piece4 = [&](int u, int c, int g) -> const float4* {
+                    return mine4 + (size_t)(u - pair) * 2 * kBMc * kBN / 4 +
+                           ((c * 4 + q) * 16 + g) * 32 + lane;
+                };
+#pragma unroll 1
+                for (int c = 0; c < kFull; ++c) {
+                    uint32_t v[64];
+                    tmem_load_64cols(taddr + c * 64, v);
+                    if (c == kFull - 1) hand_back();
                     if (!ok) continue;
                     if (w.kind == kOther) {  // partial sums of a piece another unit finishes
-                        float4* dst = reinterpret_cast<float4*>(my_slot + c * 32);
 #pragma unroll
-                        for (int g = 0; g < 8; ++g)
-                            dst[g] = make_float4(__uint_as_float(v[g * 4 + 0]), __uint_as_float(v[g * 4 + 1]),
-                                                 __uint_as_float(v[g * 4 + 2]), __uint_as_float(v[g * 4 + 3]));
+                        for (int g = 0; g < 16; ++g)
+                            mine4[((c * 4 + q) * 16 + g) * 32 + lane] =
+                                make_float4(__uint_as_float(v[g * 4 + 0]), __uint_as_float(v[g * 4 + 1]),
+                                            __uint_as_float(v[g * 4 + 2]), __uint_as_float(v[g * 4 + 3]));
                         continue;
                     }
-                    for (int u = pair + 1; u <= last_unit; ++u) {  // later pieces, in K order
-                        if (sk_run_empty(u)) continue;
-                        const float4* src = reinterpret_cast<const float4*>(
-                            my_slot + (size_t)(u - pair) * 2 * kBMc * kBN + c * 32);
-                        float4 p[8];
+                    // the later pieces, added in K order, two pieces' loads in flight at a time
+                    int u = pair + 1;
+                    while (true) {
+                        while (u <= last_unit && sk_run_empty(u)) ++u;
+                        if (u > last_unit) break;
+                        int u2 = u + 1;
+                        while (u2 <= last_unit && sk_run_empty(u2)) ++u2;
+                        const bool two = u2 <= last_unit;
+                        float4 pa[16], pb[16];
 #pragma unroll
-                        for (int g = 0; g < 8; ++g) p[g] = ld_global_cg_f4(src + g);
+                        for (int g = 0; g < 16; ++g) pa[g] = ld_global_cg_f4(piece4(u, c, g));
+                        if (two) {
 #pragma unroll
-                        for (int g = 0; g < 8; ++g) {
-                            v[g * 4 + 0] = __float_as_uint(__uint_as_float(v[g * 4 + 0]) + p[g].x);
-                            v[g * 4 + 1] = __float_as_uint(__uint_as_float(v[g * 4 + 1]) + p[g].y);
-                            v[g * 4 + 2] = __float_as_uint(__uint_as_float(v[g * 4 + 2]) + p[g].z);
-                            v[g * 4 + 3] = __float_as_uint(__uint_as_float(v[g * 4 + 3]) + p[g].w);
+                            for (int g = 0; g < 16; ++g) pb[g] = ld_global_cg_f4(piece4(u2, c, g));
                         }
+#pragma unroll
+                        for (int g = 0; g < 16; ++g) {
+                            v[g * 4 + 0] = __float_as_uint(__uint_as_float(v[g * 4 + 0]) + pa[g].x);
+                            v[g * 4 + 1] = __float_as_uint(__uint_as_float(v[g * 4 + 1]) + pa[g].y);
+                            v[g * 4 + 2] = __float_as_uint(__uint_as_float(v[g * 4 + 2]) + pa[g].z);
+                            v[g * 4 + 3] = __float_as_uint(__uint_as_float(v[g * 4 + 3]) + pa[g].w);
+                        }
+                        if (two) {
+#pragma unroll
+                            for (int g = 0; g < 16; ++g) {
+                                v[g * 4 + 0] = __float_as_uint(__uint_as_float(v[g * 4 + 0]) + pb[g].x);
+                                v[g * 4 + 1] = __float_as_uint(__uint_as_float(v[g * 4 + 1]) + pb[g].y);
+                                v[g * 4 + 2] = __float_as_uint(__uint_as_float(v[g * 4 + 2]) + pb[g].z);
+                                v[g * 4 + 3] = __float_as_uint(__uint_as_float(v[g * 4 + 3]) + pb[g].w);
+                            }
+                        }
+                        u = u2 + 1;
                     }
-                    store_chunk(c, v);
+                    store_chunk16<kBF16, 64>(&tmC, my_slots, stores, v, x0 + c * 64, band_y,
+                                             args.M, args.N, lane);
                 }
             }
             if (kSK && w.kind != kWhole) {
@@ -366,6 +394,8 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
             }
             if (!ok) break;
         }
+        if (lane == 0) bulk_wait_group<0>();  // this warp's C stores have landed
+        __syncwarp();
     }
 
     // ------------------------------ teardown ------------------------------

@@ -107,4 +107,46 @@ __device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi) {
     }
 }
 
+// Staged 16-bit output: one warp's 32 rows (lane = row) x W fp32 accumulator columns, converted
+// to 16-bit and written into a shared-memory slot in the layout a TMA store with the matching
+// swizzle reads: W = 64 -> 128-byte rows, 16-byte chunk j of row r at chunk j ^ (r % 8) (128-byte
+// swizzle, slot 1024-byte aligned); W = 32 -> 64-byte rows, chunk j at j ^ ((r / 2) % 4) (64-byte
+// swizzle, slot 512-byte aligned). Eight consecutive lanes cover every 16-byte position of a
+// 128-byte line, so each warp-wide 16-byte store takes the minimum four shared-memory wavefronts.
+template <bool kBF16, int W>
+__device__ __forceinline__ void stage_rows16(uint32_t slot, const uint32_t (&v)[W], int lane) {
+    static_assert(W == 64 || W == 32, "64 or 32 columns per staged chunk");
+#pragma unroll
+    for (int j = 0; j < W / 8; ++j) {
+        const uint32_t off = W == 64 ? (uint32_t)lane * 128u + ((uint32_t)(j ^ (lane & 7)) << 4)
+                                     : (uint32_t)lane * 64u + ((uint32_t)(j ^ ((lane >> 1) & 3)) << 4);
+        st_shared_u4(slot + off, pack2<kBF16>(v[j * 8 + 0], v[j * 8 + 1]),
+                     pack2<kBF16>(v[j * 8 + 2], v[j * 8 + 3]), pack2<kBF16>(v[j * 8 + 4], v[j * 8 + 5]),
+                     pack2<kBF16>(v[j * 8 + 6], v[j * 8 + 7]));
+    }
+}
+
+// One warp's path from registers to C through two 4 KB staging slots: wait until the store issued
+// two chunks ago has read the slot, stage the chunk, and let lane 0 issue the TMA store of the
+// box {W columns, 32 rows} at C column x, row y (a box that starts past C's last row or column is
+// skipped; one that only overlaps the edge is clipped by the TMA). Call with the whole warp;
+// `count` is the warp's running chunk number (it picks the slot).
+template <bool kBF16, int W>
+__device__ __forceinline__ void store_chunk16(const CUtensorMap* tmC, uint32_t slots,
+                                              uint32_t& count, const uint32_t (&v)[W], int x,
+                                              int y, int M, int N, int lane) {
+    if (x >= N || y >= M) return;
+    const uint32_t slot = slots + (count & 1u) * 4096u;
+    if (lane == 0) bulk_wait_group_read<1>();
+    __syncwarp();
+    stage_rows16<kBF16, W>(slot, v, lane);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(tmC, slot, x, y);
+        bulk_commit_group();
+    }
+    ++count;
+}
+
 }  // namespace dtc

@@ -269,6 +269,33 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// TMA tensor store of a 2-D box from this CTA's shared memory to global memory (box origin
+// {c0, c1}, c0 innermost); box elements outside the tensor are not written. The shared-memory
+// source must be written before, and made visible to the async proxy (fence_proxy_async_smem).
+// Completion is tracked per issuing thread with bulk async-groups: bulk_commit_group closes a
+// group, bulk_wait_group_read<N> waits until at most N groups still read shared memory,
+// bulk_wait_group<N> until at most N groups are still writing global memory.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int32_t c0,
+                                             int32_t c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(m)), "r"(src), "r"(c0), "r"(c1)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_group() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from this CTA's shared
 // memory into the shared memory of a CTA of the cluster (`dst` and `bar` are shared::cluster
 // addresses); the copy engine counts the bytes on that CTA's barrier `bar` as they land.
