@@ -728,6 +728,8 @@ int launch_mxfp8_2cta(const Operands& ops, int M, int N, int K, const gemm_optio
     rc = make_tmap_kchunks(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ops.B, (uint64_t)K, (uint64_t)N,
                            (uint64_t)ops.ldb, kHalfN, "B");
     if (rc) return rc;
+    CUtensorMap tC, tC32;
+    if ((rc = tmap_c16(&tC, &tC32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ops, M, N))) return rc;
     auto kern = dtc::gemm_mxfp8_2cta_kernel<0>;
     if ((rc = ensure_smem_attr(kern, kSmemBytes, dev))) return rc;
     const dtc::GemmMxArgs a = mx_args(ops, M, N, K, 256, kBN, kBK, o);
@@ -743,7 +745,7 @@ int launch_mxfp8_2cta(const Operands& ops, int M, int N, int K, const gemm_optio
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tA, tB, a);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tA, tB, tC, tC32, a);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "MXFP8 pair kernel launch");
     return GEMM_OK;
@@ -771,10 +773,12 @@ int launch_mxfp8_1cta(const Operands& ops, int M, int N, int K, const gemm_optio
                             (uint64_t)ops.ldb, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B, "B")))
             return rc;
     }
+    CUtensorMap tC, tC32;
+    if ((rc = tmap_c16(&tC, &tC32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ops, M, N))) return rc;
     auto kern = dtc::gemm_mxfp8_kernel<kDeep, kB32>;
     if ((rc = ensure_smem_attr(kern, C_::kSmemBytes, dev))) return rc;
     const dtc::GemmMxArgs a = mx_args(ops, M, N, K, kBM, kBN, kBK, o);
-    kern<<<p.ctas, kThreads, C_::kSmemBytes, stream>>>(tA, tB, a);
+    kern<<<p.ctas, kThreads, C_::kSmemBytes, stream>>>(tA, tB, tC, tC32, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "MXFP8 kernel launch");
     return GEMM_OK;

@@ -293,29 +293,15 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
             // 64-column chunks (and a last 32-column one for 224-wide tiles): TMEM -> registers
             // -> 16-bit in a staging slot -> TMA store
             constexpr int kFull = kBN / 64;
-            constexpr bool kTail = (kBN % 64) != 0;
             if (!kSK || w.kind == kWhole) {
-#pragma unroll 1
-                for (int c = 0; c < kFull; ++c) {
-                    uint32_t v[64];
-                    tmem_load_64cols(taddr + c * 64, v);
-                    if (!kTail && c == kFull - 1) hand_back();
-                    store_chunk16<kBF16, 64>(&tmC, my_slots, stores, v, x0 + c * 64, band_y,
-                                             args.M, args.N, lane);
-                }
-                if constexpr (kTail) {
-                    uint32_t v[32];
-                    tmem_load_32cols(taddr + kFull * 64, v);
-                    hand_back();
-                    store_chunk16<kBF16, 32>(&tmC32, my_slots, stores, v, x0 + kFull * 64, band_y,
-                                             args.M, args.N, lane);
-                }
+                drain_tile16<kBF16, kBN>(taddr, &tmC, &tmC32, my_slots, stores, x0, band_y, args.M,
+                                         args.N, lane, hand_back);
             } else if constexpr (kSK) {
                 // Pieces of shared tiles, 64-column chunks. The workspace slot of a CTA holds its
                 // 128 x 256 fp32 partial sums warp-interleaved (float4 number ((c*4 + q)*16 + g)*32
                 // + lane = columns 64c + 4g .. +3 of row 32q + lane), so every warp-wide access
                 // moves 512 contiguous bytes.
-                static_assert(!kTail, "stream-K tiles are 64-column multiples");
+                static_assert(kBN % 64 == 0, "stream-K tiles are 64-column multiples");
                 float4* const mine4 = reinterpret_cast<float4*>(
                     args.sk_partial + (size_t)(pair * 2 + (int)rank) * kBMc * kBN);
                 auto piece4 = [&](int u, int c, int g) -> const float4* {

@@ -149,4 +149,31 @@ __device__ __forceinline__ void store_chunk16(const CUtensorMap* tmC, uint32_t s
     ++count;
 }
 
+// Drains one warp's 32 accumulator rows x kBN columns (Tensor Memory address `taddr`) into C
+// rows y0.., columns x0.. through its staging slots: 64-column chunks, and a last 32-column chunk
+// (through tmC32) when kBN % 64 == 32. `hand_back` runs right after the last Tensor Memory load,
+// from which point the accumulator may be overwritten.
+template <bool kBF16, int kBN, typename HandBack>
+__device__ __forceinline__ void drain_tile16(uint32_t taddr, const CUtensorMap* tmC,
+                                             const CUtensorMap* tmC32, uint32_t slots,
+                                             uint32_t& count, int x0, int y0, int M, int N,
+                                             int lane, HandBack hand_back) {
+    static_assert(kBN % 32 == 0, "tile width in 32-column steps");
+    constexpr int kFull = kBN / 64;
+    constexpr bool kTail = (kBN % 64) != 0;
+#pragma unroll 1
+    for (int c = 0; c < kFull; ++c) {
+        uint32_t v[64];
+        tmem_load_64cols(taddr + c * 64, v);
+        if (!kTail && c == kFull - 1) hand_back();
+        store_chunk16<kBF16, 64>(tmC, slots, count, v, x0 + c * 64, y0, M, N, lane);
+    }
+    if constexpr (kTail) {
+        uint32_t v[32];
+        tmem_load_32cols(taddr + kFull * 64, v);
+        hand_back();
+        store_chunk16<kBF16, 32>(tmC32, slots, count, v, x0 + kFull * 64, y0, M, N, lane);
+    }
+}
+
 }  // namespace dtc

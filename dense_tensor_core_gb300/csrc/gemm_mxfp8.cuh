@@ -72,7 +72,9 @@ struct Cfg {
     static constexpr int kAStage = kBM * kBK * kBlocks;
     static constexpr int kBStage = kBN * kBK * kBlocks;
     static constexpr int kStageBytes = kAStage + kBStage;
-    static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+    static_assert(kStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+    static constexpr int kCBytes = 4 * 2 * 4096;  // two 4 KB output staging slots per epilogue warp
+    static constexpr int kSmemBytes = kStages * kStageBytes + kCBytes + 1024;
     static_assert(kSmemBytes <= 227 * 1024 - 256, "shared memory budget");
 };
 }  // namespace gmx
@@ -96,7 +98,9 @@ __device__ __forceinline__ uint32_t sf_word(const uint8_t* sf, int rows, int col
 template <bool kDeep, bool kB32>
 __global__ void __launch_bounds__(gmx::kThreads, 1)
     gemm_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA,
-                      const __grid_constant__ CUtensorMap tmB, const GemmMxArgs args) {
+                      const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmC,
+                      const __grid_constant__ CUtensorMap tmC32, const GemmMxArgs args) {
     using namespace gmx;
     using C_ = Cfg<kDeep>;
     constexpr int kStages = C_::kStages;
@@ -263,8 +267,8 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
     } else if (warp < 6) {
         // ------------------------------ epilogue (warps 2..5) ------------------------------
         const int q = warp & 3;
-        const int row_in_tile = q * 32 + lane;
-        uint32_t acc = 0;
+        const uint32_t my_slots = base + kStages * C_::kStageBytes + (uint32_t)q * 8192u;
+        uint32_t acc = 0, stores = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++acc) {
             int mt, nt;
             tile_coords(t, args.num_m, args.num_n, kGroupM, mt, nt);
@@ -276,35 +280,16 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after_sync();
-            const int64_t row = (int64_t)mt * kBM + row_in_tile;
-            uint16_t* crow = reinterpret_cast<uint16_t*>(args.C) + row * args.ldc;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + b * kAccStride;
-#pragma unroll 1
-            for (int c = 0; c < kBN / 32; ++c) {
-                uint32_t v[32];
-                tmem_load_32cols(taddr + c * 32, v);
-                if (c == kBN / 32 - 1) {
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&bar_tempty[b]));
-                }
-                if (row < args.M) {
-                    const int col0 = nt * kBN + c * 32;
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        const int col = col0 + g * 8;
-                        if (col < args.N) {
-                            uint4 w;
-                            w.x = pack2<true>(v[g * 8 + 0], v[g * 8 + 1]);
-                            w.y = pack2<true>(v[g * 8 + 2], v[g * 8 + 3]);
-                            w.z = pack2<true>(v[g * 8 + 4], v[g * 8 + 5]);
-                            w.w = pack2<true>(v[g * 8 + 6], v[g * 8 + 7]);
-                            *reinterpret_cast<uint4*>(crow + col) = w;
-                        }
-                    }
-                }
-            }
+            drain_tile16<true, kBN>(taddr, &tmC, &tmC32, my_slots, stores, nt * kBN, mt * kBM + q * 32,
+                                    args.M, args.N, lane, [&]() {
+                                        tc_fence_before_sync();
+                                        __syncwarp();
+                                        if (lane == 0) mbar_arrive(smem_u32(&bar_tempty[b]));
+                                    });
         }
+        if (lane == 0) bulk_wait_group<0>();  // this warp's C stores have landed
+        __syncwarp();
     } else {
         // ------------------------------ scale writers (warps 6..9) ------------------------------
         // The (tile, group) sequence of this CTA, flattened so the gather of the next group
