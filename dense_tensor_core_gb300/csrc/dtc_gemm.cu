@@ -264,11 +264,9 @@ int ensure_smem_attr(Kern kern, int bytes, DeviceInfo* dev) {
 // Ring depth of the pair kernel: 6 stages of 64-deep K-blocks, or 3 of 128-deep ones.
 constexpr int pair_stages(int bn, int bk) { return bk == 128 ? 3 : 6 + 0 * bn; }
 
-// Ring depth of the one-CTA kernel for each (tile width, K-block): as many stages as about
-// 220 KB of shared memory holds.
-constexpr int stages_for(int bn, int bk) {
-    return bk == 64 ? (bn == 224 ? 5 : 4) : (bn == 224 ? 10 : 9);
-}
+// Ring depth of the one-CTA kernel for each (tile width, K-block): as many stages as fit beside
+// the 32 KB of output staging (at most 225 KB in all).
+constexpr int stages_for(int bn, int bk) { return bk == 64 ? 4 + 0 * bn : 8; }
 
 // How many clusters of `cm` one-CTA GEMM CTAs (about 200 KB of shared memory each, so one per
 // SM) the device keeps resident at once. Asked once per device and cluster size.
@@ -633,10 +631,13 @@ int launch_gemm16_1cta(const Operands& ops, int M, int N, int K, const gemm_opti
     int rc = tmap_operand16(&tA, dt, ops.A, ops.lda, kAMN, M, K, kBK, kBM, "A");
     if (rc) return rc;
     if ((rc = tmap_operand16(&tB, dt, ops.B, ops.ldb, kNN, N, K, kBK, kBN / kCM, "B"))) return rc;
+    CUtensorMap tC, tC32;
+    if ((rc = tmap_c16(&tC, &tC32, dt, ops, M, N))) return rc;
     auto kern = dtc::gemm16_1cta_kernel<kBF16, kAMN, kNN, kBN, kBK, kStages, kCM>;
     if ((rc = ensure_smem_attr(kern, Cfg::kSmemBytes, dev))) return rc;
     const Gemm16Args args = make_args(ops, M, N, K, kBM, kBN, kBK, o);
-    return launch_cluster(kern, p.ctas, kThreads, Cfg::kSmemBytes, kCM, stream, tA, tB, args);
+    return launch_cluster(kern, p.ctas, kThreads, Cfg::kSmemBytes, kCM, stream, tA, tB, tC, tC32,
+                          args);
 }
 
 template <bool kBF16, bool kAMN, bool kNN, int kBN, int kBK, bool kSK = false>
@@ -678,10 +679,13 @@ int launch_gemm16_splitk(const Operands& ops, int M, int N, int K, const gemm_op
     int rc = tmap_operand16(&tA, dt, ops.A, ops.lda, kAMN, M, K, kBK, 128, "A");
     if (rc) return rc;
     if ((rc = tmap_operand16(&tB, dt, ops.B, ops.ldb, kNN, N, K, kBK, kBN, "B"))) return rc;
+    CUtensorMap tC, tC32;
+    if ((rc = tmap_c16(&tC, &tC32, dt, ops, M, N))) return rc;
     auto kern = dtc::gemm16_splitk_kernel<kBF16, kAMN, kNN, kBN, kBK, kStages, kS>;
     if ((rc = ensure_smem_attr(kern, Cfg::kSmemBytes, dev))) return rc;
     const Gemm16Args args = make_args(ops, M, N, K, 128, kBN, kBK, o);
-    return launch_cluster(kern, p.ctas, dtc::gsk::kThreads, Cfg::kSmemBytes, kS, stream, tA, tB, args);
+    return launch_cluster(kern, p.ctas, dtc::gsk::kThreads, Cfg::kSmemBytes, kS, stream, tA, tB, tC,
+                          args);
 }
 
 template <bool kBF16, bool kAMN, bool kNN>

@@ -12,7 +12,7 @@
 // "Compilation and Usage" pass configs and "Code Example"); here
 //   warp 0      : TMA producer (one lane) filling a kStages ring of 128B-swizzled A/B tiles,
 //   warp 1      : Tensor Memory allocator and single-thread tcgen05.mma issuer,
-//   warps 2..5  : epilogue (tcgen05.ld -> cvt -> global stores),
+//   warps 2..5  : epilogue (tcgen05.ld -> cvt -> swizzled shared-memory staging -> TMA store),
 // with full/empty barriers per stage (the producer waits on the inverted parity, as in the
 // 3-stage ring of tilelang (velog) section 1.3) and a double-buffered accumulator (2 x 256
 // columns) so the epilogue of one tile overlaps the main loop of the next. CTAs are persistent:
@@ -50,7 +50,9 @@ struct Cfg {
     static constexpr int kStageBytes = kAStage + kBStage;
     static constexpr int kPitch = kBK * 2;  // bytes per K-major row = swizzle width
     static_assert(kBK == 64 || kBK == 32, "K-block of 64 or 32");
-    static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
+    static_assert(kStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+    static constexpr int kCBytes = 4 * 2 * 4096;  // two 4 KB output staging slots per epilogue warp
+    static constexpr int kSmemBytes = kStages * kStageBytes + kCBytes + 1024;  // + alignment slack
     static_assert(kBN % 16 == 0 && kBN <= 256, "UMMA N for M = 128");
     static_assert(kSmemBytes <= 227 * 1024 - 256, "shared memory budget");
 };
@@ -59,7 +61,9 @@ struct Cfg {
 template <bool kBF16, bool kAMN, bool kNN, int kBN, int kBK, int kStages, int kCM>
 __global__ void __launch_bounds__(g16::kThreads, 1)
     gemm16_1cta_kernel(const __grid_constant__ CUtensorMap tmA,
-                       const __grid_constant__ CUtensorMap tmB, const Gemm16Args args) {
+                       const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmC,
+                       const __grid_constant__ CUtensorMap tmC32, const Gemm16Args args) {
     using namespace g16;
     using C_ = Cfg<kBN, kBK, kStages>;
     constexpr int kAStage = C_::kAStage;
@@ -236,8 +240,8 @@ __global__ void __launch_bounds__(g16::kThreads, 1)
     } else {
         // ------------------------------ epilogue (warps 2..5) ------------------------------
         const int q = warp & 3;  // Tensor Memory lane quarter this warp may access
-        const int row_in_tile = q * 32 + lane;
-        uint32_t acc = 0;
+        const uint32_t my_slots = base + kStages * C_::kStageBytes + (uint32_t)q * 8192u;
+        uint32_t acc = 0, stores = 0;
         for (int t = cluster; t < total; t += clusters, ++acc) {
             int mc, nt;
             tile_coords(t, num_mc, args.num_n, kGroupM, mc, nt);
@@ -250,36 +254,18 @@ __global__ void __launch_bounds__(g16::kThreads, 1)
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after_sync();
-            const int64_t row = (int64_t)mt * kBM + row_in_tile;
-            uint16_t* crow = reinterpret_cast<uint16_t*>(args.C) + row * args.ldc;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + b * kAccStride;
-#pragma unroll 1
-            for (int c = 0; c < kBN / 32; ++c) {
-                uint32_t v[32];
-                tmem_load_32cols(taddr + c * 32, v);
-                if (c == kBN / 32 - 1) {
-                    // accumulator fully read: hand the buffer back to the MMA issuer
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&bar_tempty[b]));
-                }
-                if (row < args.M) {
-                    const int col0 = nt * kBN + c * 32;
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        const int col = col0 + g * 8;
-                        if (col < args.N) {
-                            uint4 w;
-                            w.x = pack2<kBF16>(v[g * 8 + 0], v[g * 8 + 1]);
-                            w.y = pack2<kBF16>(v[g * 8 + 2], v[g * 8 + 3]);
-                            w.z = pack2<kBF16>(v[g * 8 + 4], v[g * 8 + 5]);
-                            w.w = pack2<kBF16>(v[g * 8 + 6], v[g * 8 + 7]);
-                            *reinterpret_cast<uint4*>(crow + col) = w;
-                        }
-                    }
-                }
-            }
+            // accumulator -> 16-bit staging -> TMA store; the buffer goes back to the MMA issuer
+            // once fully read
+            drain_tile16<kBF16, kBN>(taddr, &tmC, &tmC32, my_slots, stores, nt * kBN,
+                                     mt * kBM + q * 32, args.M, args.N, lane, [&]() {
+                                         tc_fence_before_sync();
+                                         __syncwarp();
+                                         if (lane == 0) mbar_arrive(smem_u32(&bar_tempty[b]));
+                                     });
         }
+        if (lane == 0) bulk_wait_group<0>();  // this warp's C stores have landed
+        __syncwarp();
     }
 
     // ------------------------------ teardown ------------------------------

@@ -16,7 +16,8 @@
 //   2. an epilogue warp whose quarter this CTA owns takes the pieces in order: once a piece's
 //      barrier completes it sums its own accumulator columns with the kS - 1 copies in the
 //      fixed order 0..kS-1 (the result does not depend on which CTA finished first), rounds once
-//      to the output type and stores, while later pieces are still in flight;
+//      to the output type into a swizzled staging slot over the idle ring and stores it with a
+//      TMA tensor store, while later pieces are still in flight;
 //   3. cluster barrier (no CTA leaves while a copy into it, or out of it, may be in flight).
 // The exchange area is a region of its own, not the ring, so no CTA waits for a peer's main loop
 // to end before copying into it. The exchange is laid out piece-major ([piece][row][64 floats],
@@ -63,7 +64,9 @@ struct Cfg {
     static constexpr int kTmemCols = kBN <= 128 ? 128 : 256;
     static constexpr int kQPieceBytes = 32 * kXPitch;                   // one quarter's piece
     static constexpr int kStaging = (4 - 4 / kS) * kPieces * kQPieceBytes;  // all pushed quarters
-    static_assert(kStaging <= kRing, "the staging copies must fit over the ring");
+    // the owner warps' output staging (two 4 KB slots each) follows the pushed quarters
+    static constexpr int kCStaging = kStaging + (4 / kS) * 2 * 4096;
+    static_assert(kCStaging <= kRing, "the staging copies must fit over the ring");
     static_assert(kBK == 64 || kBK == 128, "K-block of 64 or 128");
     static_assert(kS == 2 || kS == 4, "K split over 2 or 4 CTAs");
     static_assert(kBN % 64 == 0 && kBN <= 256, "the accumulator is read 64 columns at a time");
@@ -74,7 +77,8 @@ struct Cfg {
 template <bool kBF16, bool kAMN, bool kNN, int kBN, int kBK, int kStages, int kS>
 __global__ void __launch_bounds__(gsk::kThreads, 1)
     gemm16_splitk_kernel(const __grid_constant__ CUtensorMap tmA,
-                         const __grid_constant__ CUtensorMap tmB, const Gemm16Args args) {
+                         const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmC, const Gemm16Args args) {
     using namespace gsk;
     using C_ = Cfg<kBN, kBK, kStages, kS>;
     constexpr int kChunks = kBK / 64;    // 128-byte K-chunks per stage
@@ -262,8 +266,9 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
                 }
             }
         } else if (ok) {
-            const int64_t grow = (int64_t)mt * kBM + q * 32 + lane;
-            uint16_t* crow = reinterpret_cast<uint16_t*>(args.C) + grow * args.ldc;
+            // C through two staging slots over the idle ring (after the pushed quarters' copies)
+            const uint32_t my_slots = sA + C_::kStaging + (uint32_t)qb * 8192u;
+            uint32_t stores = 0;
 #pragma unroll 1
             for (int c = 0; c < C_::kPieces; ++c) {
                 uint32_t v[64];
@@ -276,7 +281,6 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
                 if (!xok) break;
                 // the phase has completed: every lane takes its own acquire of it
                 (void)mbar_try_wait_cluster(smem_u32(&bar_xchg[c]), 0);
-                if (grow >= args.M) continue;  // all lanes took part in the Tensor Memory load
                 float acc[64];
                 // sum over source ranks 0..kS-1 in that order (own rows from Tensor Memory)
 #pragma unroll
@@ -301,24 +305,13 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
                         }
                     }
                 }
-                const int col0 = nt * kBN + c * 64;
 #pragma unroll
-                for (int g = 0; g < 8; ++g) {
-                    const int col = col0 + g * 8;
-                    if (col < args.N) {
-                        uint4 w;
-                        w.x = pack2<kBF16>(__float_as_uint(acc[g * 8 + 0]),
-                                           __float_as_uint(acc[g * 8 + 1]));
-                        w.y = pack2<kBF16>(__float_as_uint(acc[g * 8 + 2]),
-                                           __float_as_uint(acc[g * 8 + 3]));
-                        w.z = pack2<kBF16>(__float_as_uint(acc[g * 8 + 4]),
-                                           __float_as_uint(acc[g * 8 + 5]));
-                        w.w = pack2<kBF16>(__float_as_uint(acc[g * 8 + 6]),
-                                           __float_as_uint(acc[g * 8 + 7]));
-                        *reinterpret_cast<uint4*>(crow + col) = w;
-                    }
-                }
+                for (int i = 0; i < 64; ++i) v[i] = __float_as_uint(acc[i]);
+                store_chunk16<kBF16, 64>(&tmC, my_slots, stores, v, nt * kBN + c * 64,
+                                         mt * kBM + q * 32, args.M, args.N, lane);
             }
+            if (lane == 0) bulk_wait_group<0>();  // this warp's C stores have landed
+            __syncwarp();
         }
     }
 
