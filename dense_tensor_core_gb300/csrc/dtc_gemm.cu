@@ -335,7 +335,8 @@ double choice_efficiency(int variant, int bn, int bk) {
     return 0.5;
 }
 
-// Stream-K on CTA pairs (256 x 256 x 128 tiles): when the tiles leave the last wave part-empty,
+// Stream-K on CTA pairs (256 x 256 tiles, 128-deep stages; 64-deep on request): when the tiles
+// leave the last wave part-empty,
 // the leftover tiles are shared out over all pairs as equal runs of K-blocks, their pieces summed
 // through the caller's workspace. Taken when a large enough workspace is given, the request
 // allows the pair kernel with these tiles, and the cost model beats the plan already made: work
@@ -352,12 +353,13 @@ int plan_stream_k(int64_t M, int64_t N, int64_t K, const gemm_options* o, Device
     const int req_v = o ? o->variant : GEMM_VARIANT_AUTO;
     const bool allowed = (req_v == GEMM_VARIANT_AUTO || req_v == GEMM_VARIANT_2CTA) &&
                          (!o || o->tile_n == 0 || o->tile_n == 256) &&
-                         (!o || o->tile_k == 0 || o->tile_k == 128) && (!o || o->split_k == 0) &&
+                         (!o || o->tile_k == 0 || o->tile_k == 128 || o->tile_k == 64) &&
+                         (!o || o->split_k == 0) &&
                          K % 64 == 0 && p->variant != GEMM_VARIANT_SPLITK && tiles >= units &&
                          tiles % units != 0;
     const bool ws_ok = o && o->workspace && o->workspace_bytes >= sk_workspace_bytes(units, 256);
     if (mode == 1 && !allowed)
-        return fail(GEMM_ERR_UNSUPPORTED, "stream-K needs the pair kernel with 256 x 256 x 128 tiles, "
+        return fail(GEMM_ERR_UNSUPPORTED, "stream-K needs the pair kernel with 256 x 256 tiles, "
                     "K %% 64 == 0 and a tile count that is not a whole number of waves");
     if (mode == 1 && !ws_ok)
         return fail(GEMM_ERR_INVALID_ARG, "stream-K needs a workspace of %llu bytes",
@@ -372,8 +374,8 @@ int plan_stream_k(int64_t M, int64_t N, int64_t K, const gemm_options* o, Device
     p->cluster = 2;
     p->tile_m = 256;
     p->tile_n = 256;
-    p->tile_k = 128;
-    p->stages = pair_stages(256, 128);
+    p->tile_k = (o && o->tile_k == 64) ? 64 : 128;
+    p->stages = pair_stages(256, p->tile_k);
     p->split_k = 1;
     p->tiles = (int)tiles;
     p->sk_tiles = (int)(tiles % units);
@@ -802,8 +804,11 @@ int launch_mxfp8(const Operands& ops, int M, int N, int K, const gemm_options* o
 template <bool kBF16, bool kAMN, bool kNN>
 int launch_pair_width(const Plan& p, const Operands& ops, int m, int n, int k,
                       const gemm_options* o, DeviceInfo* dev, cudaStream_t stream) {
-    if (p.sk_tiles)  // stream-K plans are 256 x 256 x 128
+    if (p.sk_tiles) {  // stream-K plans are 256 wide, 128- or 64-deep
+        if (p.tile_k == 64)
+            return launch_gemm16_2cta<kBF16, kAMN, kNN, 256, 64, true>(ops, m, n, k, o, dev, p, stream);
         return launch_gemm16_2cta<kBF16, kAMN, kNN, 256, 128, true>(ops, m, n, k, o, dev, p, stream);
+    }
     if (p.tile_k == 128) {
         if (p.tile_n == 224)
             return launch_gemm16_2cta<kBF16, kAMN, kNN, 224, 128>(ops, m, n, k, o, dev, p, stream);

@@ -193,7 +193,13 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
         // ------------------------------ MMA issuer (leader CTA) ------------------------------
         if (lane == 0 && leader) {
             constexpr uint32_t idesc = idesc_f16(kBF16, kNN, 256, kBN, kAMN);
-            uint32_t it = 0, acc = 0;
+            // Operand descriptors: only the start-address field (bits 0-13: address >> 4)
+            // changes, by fixed offsets per stage and per K-step, so it is built once and
+            // advanced with 32-bit adds (shared addresses stay below 256 KB: no carry out).
+            const uint64_t a_desc0 = smem_desc_sw128(sA, kAMN ? 64 * kBK * 2 : 16, 1024);
+            const uint64_t b_desc0 = smem_desc_sw128(sB, kNN ? 64 * kBK * 2 : 16, 1024);
+            const uint32_t a_hi = (uint32_t)(a_desc0 >> 32), b_hi = (uint32_t)(b_desc0 >> 32);
+            uint32_t s = 0, ph = 0, acc = 0;
             bool ok = true, issued = false;
             WorkIter wi(pair, num_pairs, total, sk_tiles, args.num_kb);
             WorkItem w;
@@ -206,36 +212,37 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * kAccStride;
-                for (int kb = w.k0; kb < w.k1; ++kb, ++it) {
-                    const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+                for (int kb = w.k0; kb < w.k1; ++kb) {
                     if (!wait_bounded(smem_u32(&bar_full[s]), ph, abort, args.timeout_ns,
                                       &g_dtc_status, 13)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t a0 = sA + s * C_::kAStage, b0 = sB + s * C_::kBStage;
+                    const uint32_t a_lo = (uint32_t)a_desc0 + s * (uint32_t)(C_::kAStage >> 4);
+                    const uint32_t b_lo = (uint32_t)b_desc0 + s * (uint32_t)(C_::kBStage >> 4);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
-                        // K-chunk kk/4 of the stage, 32-byte step kk%4 inside its swizzle row
-                        const uint32_t koff = (kk % 4) * 32;
-                        const uint64_t adesc =
-                            kAMN ? smem_desc_sw128(a0 + kk * 16 * 128, 64 * kBK * 2, 1024)
-                                      : smem_desc_sw128(a0 + (kk / 4) * (kBMc * 128) + koff, 16, 1024);
-                        const uint64_t bdesc =
-                            kNN ? smem_desc_sw128(b0 + kk * 16 * 128, 64 * kBK * 2, 1024)
-                                : smem_desc_sw128(b0 + (kk / 4) * (C_::kHalfN * 128) + koff, 16, 1024);
+                        // K-major: K-chunk kk/4 of the stage, 32-byte step kk%4 inside its
+                        // swizzle row; MN-major: 16 K-rows of 128 bytes per step
+                        constexpr int kRowsA = kBMc, kRowsB = C_::kHalfN;
+                        const uint32_t a_off =
+                            kAMN ? kk * 16 * 128 : (kk / 4) * (kRowsA * 128) + (kk % 4) * 32;
+                        const uint32_t b_off =
+                            kNN ? kk * 16 * 128 : (kk / 4) * (kRowsB * 128) + (kk % 4) * 32;
+                        const uint64_t adesc = ((uint64_t)a_hi << 32) | (a_lo + (a_off >> 4));
+                        const uint64_t bdesc = ((uint64_t)b_hi << 32) | (b_lo + (b_off >> 4));
                         mma_f16_cta2(d_tmem, adesc, bdesc, idesc, (kb != w.k0 || kk != 0) ? 1u : 0u);
                     }
                     issued = true;
-                    const uint32_t e = smem_u32(&bar_empty[s]);
-                    mma_commit_cta2(e);
-                    mma_commit_cta2(map_to_cta(e, 1));
+                    mma_commit_cta2_both(smem_u32(&bar_empty[s]));  // stage free in both CTAs
+                    if (++s == (uint32_t)kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
                 if (!ok) break;
-                const uint32_t f = smem_u32(&bar_tfull[b]);
-                mma_commit_cta2(f);
-                mma_commit_cta2(map_to_cta(f, 1));
+                mma_commit_cta2_both(smem_u32(&bar_tfull[b]));
                 ++acc;
             }
             if (!ok && issued) {

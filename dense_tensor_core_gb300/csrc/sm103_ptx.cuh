@@ -435,6 +435,15 @@ __device__ __forceinline__ void mma_commit_cta2(uint32_t bar) {
         : "memory");
 }
 
+// The same completion signalled at once on the barrier at offset `bar` of both CTAs of the pair
+// (multicast to CTA ranks 0 and 1 of the cluster).
+__device__ __forceinline__ void mma_commit_cta2_both(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar), "h"((uint16_t)0x3)
+        : "memory");
+}
+
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp receives lane (base + i).
 // The load and its completion wait are one asm statement, so no consumer of `r` can be
 // scheduled before the data has arrived.

@@ -348,9 +348,10 @@ def _workspace(kind, M, N, K, layout):
     return torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
 
 
+@pytest.mark.parametrize("tile_k", [0, 64])
 @pytest.mark.parametrize("layout", ["NT", "NN", "TN", "TT"])
 @pytest.mark.parametrize("M,N,K", [(2560, 2560, 1024), (2560, 2304, 384), (2304, 2560, 640)])
-def test_stream_k_full_parity(M, N, K, layout):
+def test_stream_k_full_parity(M, N, K, layout, tile_k):
     # 100 (or 90) pair tiles of 256 x 256 over 76 pairs: one whole wave, then 24 (or 14) tiles
     # shared out as runs of K-blocks; K = 384 gives fewer K-blocks than pairs, so some pairs have
     # an empty share and tiles are split over up to 3 pairs; every piece, the flags and the fixup
@@ -360,13 +361,14 @@ def test_stream_k_full_parity(M, N, K, layout):
     if torch.cuda.get_device_properties(0).multi_processor_count != 152:
         pytest.skip("the shapes are chosen for 76 pairs")
     kind = "bf16" if layout in ("NT", "TN") else "f16"
+    # (tile_k 64: 64-deep stages, twice the K-blocks per tile to share out)
     ws = _workspace(kind, M, N, K, layout)
-    p = dtc.gemm_plan(kind, M, N, K, layout, workspace=ws, stream_k=1)
-    assert (p["variant"], p["tile_n"], p["tile_k"]) == (2, 256, 128) and p["sk_tiles"] > 0
+    p = dtc.gemm_plan(kind, M, N, K, layout, workspace=ws, stream_k=1, tile_k=tile_k)
+    assert (p["variant"], p["tile_n"], p["tile_k"]) == (2, 256, tile_k or 128) and p["sk_tiles"] > 0
     A, B = workloads.make16(kind, layout, M, N, K, seed=M + K)
     At, Bt = to_device16(A, kind), to_device16(B, kind)
-    C1 = dtc.gemm_ex(kind, At, Bt, layout=layout, workspace=ws, stream_k=1)
-    C2 = dtc.gemm_ex(kind, At, Bt, layout=layout, workspace=ws, stream_k=1)
+    C1 = dtc.gemm_ex(kind, At, Bt, layout=layout, workspace=ws, stream_k=1, tile_k=tile_k)
+    C2 = dtc.gemm_ex(kind, At, Bt, layout=layout, workspace=ws, stream_k=1, tile_k=tile_k)
     dtc.gemm_stream_status()
     assert torch.equal(C1.view(torch.int16), C2.view(torch.int16)), "two runs differ"
     assert int(ws[:1024].count_nonzero()) == 0, "stream-K flags not back at zero"
