@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(g16::kThreads, 1)
                                          if (lane == 0) mbar_arrive(smem_u32(&bar_tempty[b]));
                                      });
         }
-        if (lane == 0) bulk_wait_group<0>();  // this warp's C stores have landed
+        if (lane == 0) bulk_wait_group_read<0>();  // the C stores have read their slots
         __syncwarp();
     }
 

@@ -387,7 +387,7 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
             }
             if (!ok) break;
         }
-        if (lane == 0) bulk_wait_group<0>();  // this warp's C stores have landed
+        if (lane == 0) bulk_wait_group_read<0>();  // the C stores have read their slots
         __syncwarp();
     }
 

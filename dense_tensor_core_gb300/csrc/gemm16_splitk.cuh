@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
                 store_chunk16<kBF16, 64>(&tmC, my_slots, stores, v, nt * kBN + c * 64,
                                          mt * kBM + q * 32, args.M, args.N, lane);
             }
-            if (lane == 0) bulk_wait_group<0>();  // this warp's C stores have landed
+            if (lane == 0) bulk_wait_group_read<0>();  // the C stores have read their slots
             __syncwarp();
         }
     }

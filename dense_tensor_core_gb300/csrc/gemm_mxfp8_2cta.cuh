@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(gmx2::kThreads, 1)
                                             mbar_arrive_cluster(map_to_cta(smem_u32(&bar_tempty[b]), 0));
                                     });
         }
-        if (lane == 0) bulk_wait_group<0>();  // this warp's C stores have landed
+        if (lane == 0) bulk_wait_group_read<0>();  // the C stores have read their slots
         __syncwarp();
     } else {
         // ------------------------------ scale writers (warps 6..9, both CTAs) ----------------

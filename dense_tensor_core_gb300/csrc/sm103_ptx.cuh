@@ -274,7 +274,9 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
 // source must be written before, and made visible to the async proxy (fence_proxy_async_smem).
 // Completion is tracked per issuing thread with bulk async-groups: bulk_commit_group closes a
 // group, bulk_wait_group_read<N> waits until at most N groups still read shared memory,
-// bulk_wait_group<N> until at most N groups are still writing global memory.
+// bulk_wait_group<N> until at most N groups are still writing global memory. A kernel that
+// stores C this way waits only for the reads before it exits (its shared memory is then free);
+// the writes complete with the grid, like ordinary stores, before any later work in the stream.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int32_t c0,
                                              int32_t c1) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
