@@ -223,10 +223,12 @@ def test_k_zero_writes_zeros_and_empty_is_noop():
     assert C0.shape == (0, 16)
 
 
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
 @pytest.mark.parametrize("layout", ["NT", "NN"])
-def test_writes_exactly_C(layout):
+def test_writes_exactly_C(layout, variant):
     # C sits inside a larger buffer filled with NaN: every element of C must be overwritten and
-    # nothing around it touched (ragged edges clip stores to [M, N]).
+    # nothing around it touched (the TMA stores clip ragged edges to [M, N]; 264 columns end in a
+    # partial 64-column chunk, 200 rows in a partial 32-row band)
     import dense_tensor_core_gb300 as dtc
 
     M, N, K = 200, 264, 136
@@ -234,7 +236,9 @@ def test_writes_exactly_C(layout):
     guard = 4096
     buf = torch.full((guard * 2 + M * N,), float("nan"), dtype=torch.bfloat16, device="cuda")
     C = buf[guard:guard + M * N].view(M, N)
-    dtc.gemm_bf16(to_device16(A, "bf16"), to_device16(B, "bf16"), C, layout=layout)
+    kw = dict(split_k=2) if variant == 3 else {}
+    dtc.gemm_ex("bf16", to_device16(A, "bf16"), to_device16(B, "bf16"), C, layout=layout,
+                variant=variant, **kw)
     dtc.gemm_stream_status()
     h = buf.float().cpu()
     assert torch.isnan(h[:guard]).all() and torch.isnan(h[guard + M * N:]).all()

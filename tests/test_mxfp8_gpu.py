@@ -268,3 +268,25 @@ def test_rows_of_larger_arrays(variant):
     C = Cb[:, :N].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
     ref = oracle.gemm_mxfp8(A, B, sfA, sfB, M, N, K)
     check_close(values16(C, "bf16"), values16(ref, "bf16"), f"strided mxfp8 variant {variant}")
+
+
+@pytest.mark.parametrize("variant,tile_k", [(1, 128), (1, 256), (2, 0)])
+def test_writes_exactly_C(variant, tile_k):
+    # C inside a NaN-filled buffer: every element overwritten, nothing around it touched (224-wide
+    # tiles end in a 32-column chunk; 520 columns and 300 rows leave partial chunks and bands)
+    import dense_tensor_core_gb300 as dtc
+
+    M, N, K = 300, 520, 512
+    A, B, sfA, sfB = workloads.make_mxfp8(M, N, K, seed=21)
+    guard = 4096
+    buf = torch.full((guard * 2 + M * N,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    C = buf[guard:guard + M * N].view(M, N)
+    dtc.gemm_ex("mxfp8", to_device8(A), to_device8(B), C, sfA=to_device8(sfA), sfB=to_device8(sfB),
+                variant=variant, tile_k=tile_k)
+    dtc.gemm_stream_status()
+    h = buf.float().cpu()
+    assert torch.isnan(h[:guard]).all() and torch.isnan(h[guard + M * N:]).all()
+    got = h[guard:guard + M * N].view(M, N)
+    assert not torch.isnan(got).any()
+    ref = oracle.gemm_mxfp8(A, B, sfA, sfB, M, N, K)
+    check_close(got.double().numpy(), values16(ref, "bf16"), f"mxfp8 variant {variant} in a buffer")
