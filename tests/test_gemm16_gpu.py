@@ -316,6 +316,28 @@ def test_rows_of_larger_arrays(layout, variant):
     check_close(values16(C, "bf16"), values16(ref, "bf16"), f"strided {layout} variant {variant}")
 
 
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
+def test_c_view_at_an_offset(variant):
+    # C is a window of a larger array starting 8 columns and 3 rows in: its base is 16-byte but not
+    # 128-byte aligned, its rows are ldc apart; only the window may be written
+    import dense_tensor_core_gb300 as dtc
+
+    M, N, K = 136, 200, 192
+    A, B = workloads.make16("f16", "NT", M, N, K, seed=31)
+    big = torch.full((M + 6, N + 24), float("nan"), dtype=torch.float16, device="cuda")
+    C = big[3:3 + M, 8:8 + N]
+    kw = dict(split_k=2) if variant == 3 else {}
+    dtc.gemm_ex("f16", to_device16(A, "f16"), to_device16(B, "f16"), C, variant=variant, **kw)
+    dtc.gemm_stream_status()
+    h = big.float().cpu()
+    inside = torch.zeros_like(h, dtype=torch.bool)
+    inside[3:3 + M, 8:8 + N] = True
+    assert torch.isnan(h[~inside]).all(), "written outside the C window"
+    got = C.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    ref = oracle.gemm16("f16", "NT", A, B, M, N, K)
+    check_close(values16(got, "f16"), values16(ref, "f16"), f"C window, variant {variant}")
+
+
 def test_k_zero_with_strided_c_writes_only_the_region():
     import dense_tensor_core_gb300 as dtc
 
