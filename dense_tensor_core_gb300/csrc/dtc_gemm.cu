@@ -445,8 +445,10 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
         tiles256 * 2 <= d->sms) {
         // Fewer 128 x 256 tiles than half the SMs: split K over a cluster of 2 or 4 CTAs per
         // 128 x 128 or 128 x 256 tile. Take the (width, split) that occupies the most SMs in one
-        // wave, each CTA keeping at least 4 K-blocks of 64; on a tie the smaller split (less to
-        // reduce), then the narrower tile (a smaller exchange).
+        // wave, each CTA keeping at least 8 K-blocks of 64 (with less, the on-chip exchange of
+        // the partial sums costs more than the split saves: 256 x 256 x 512 ran 12.3 us split in
+        // 2 against 10.3 us on one-CTA tiles); on a tie the smaller split (less to reduce), then
+        // the narrower tile (a smaller exchange).
         struct Cand { int bn, s; };
         const Cand cands[3] = {{128, 2}, {128, 4}, {256, 2}};
         int64_t best_ctas = 0;
@@ -454,7 +456,7 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
             if (want_n && c.bn != want_n) continue;
             const int64_t tl = c.bn == 128 ? tiles128 : tiles256;
             const int64_t ctas = tl * c.s;
-            if (num_kb < 4 * c.s || ctas > (int64_t)resident_clusters(c.s, d) * c.s) continue;
+            if (num_kb < 8 * c.s || ctas > (int64_t)resident_clusters(c.s, d) * c.s) continue;
             if (ctas > best_ctas || (ctas == best_ctas && c.s < split)) {
                 best_ctas = ctas;
                 split = c.s;
