@@ -106,7 +106,9 @@ typedef struct {
                              the same time (other streams) must not share a workspace. */
     uint64_t workspace_bytes;
     int stream_k;         /* 0 = use stream-K when a large enough workspace is given and the
-                             cost model prefers it; 1 = required (error if not possible); 2 = off */
+                             cost model prefers it; 1 = required (error if not possible); 2 = off.
+                             Stream-K runs the pair kernel on 256 x 256 tiles with 128-deep
+                             stages, or 64-deep ones when tile_k = 64. */
 } gemm_options;
 
 /*
