@@ -5,8 +5,11 @@
 // C[M,N] = A[M,K] . Bop as in the one-CTA kernel (128 x kBN tiles, kBK-deep K-blocks, TMA producer
 // warp, single-thread tcgen05.mma issuer, Tensor Memory accumulator), but a cluster of kS CTAs
 // computes one tile: CTA r accumulates the r-th of kS contiguous K-ranges. The partial sums are
-// reduced on chip, without a global workspace. CTA r owns rows [r*128/kS, (r+1)*128/kS) of the
-// tile, i.e. 4/kS of the four 32-lane quarters of the accumulator:
+// reduced on chip, without a global workspace. Split in 2, CTA r owns columns
+// [r*kBN/2, (r+1)*kBN/2) of the tile (all 128 rows): each epilogue warp copies its 32 rows of the
+// peer's columns into the peer's exchange area, then sums its rows of its own columns with the
+// copy it received and stores them, so all four warps share the reduction. Split in 4, CTA r owns
+// rows [r*32, (r+1)*32) (one 32-lane quarter of the accumulator):
 //   1. an epilogue warp whose quarter another CTA owns reads it from Tensor Memory, 64 columns
 //      per round trip, into a staging copy in its own ring (idle once the last MMA has
 //      completed), laid out as the owner's exchange area is, and hands each 64-column piece to
@@ -64,8 +67,14 @@ struct Cfg {
     static constexpr int kTmemCols = kBN <= 128 ? 128 : 256;
     static constexpr int kQPieceBytes = 32 * kXPitch;                   // one quarter's piece
     static constexpr int kStaging = (4 - 4 / kS) * kPieces * kQPieceBytes;  // all pushed quarters
-    // the owner warps' output staging (two 4 KB slots each) follows the pushed quarters
-    static constexpr int kCStaging = kStaging + (4 / kS) * 2 * 4096;
+    // Split in 2: each CTA owns half of the tile's columns (kOwnPieces 64-column pieces, all 128
+    // rows), so every epilogue warp pushes and reduces alike; split in 4: each owns 32 rows.
+    static constexpr bool kColOwn = kS == 2;
+    static constexpr int kOwnPieces = kPieces / 2;
+    static constexpr int kColPieceBytes = kBM * kXPitch;  // one owned piece, all 128 rows
+    static_assert(!kColOwn || kOwnPieces * kColPieceBytes == kXBytes, "same exchange area");
+    // the owner warps' output staging (two 4 KB slots each) follows the pushed pieces
+    static constexpr int kCStaging = kStaging + (kColOwn ? 4 : 4 / kS) * 2 * 4096;
     static_assert(kCStaging <= kRing, "the staging copies must fit over the ring");
     static_assert(kBK == 64 || kBK == 128, "K-block of 64 or 128");
     static_assert(kS == 2 || kS == 4, "K split over 2 or 4 CTAs");
@@ -115,7 +124,10 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
         // each armed once with every byte the peers will copy into its piece
         for (int c = 0; c < C_::kPieces; ++c) {
             mbar_init(smem_u32(&bar_xchg[c]), 1);
-            mbar_arrive_expect_tx(smem_u32(&bar_xchg[c]), C_::kXPieceBytes);
+            if (!C_::kColOwn)
+                mbar_arrive_expect_tx(smem_u32(&bar_xchg[c]), C_::kXPieceBytes);
+            else if (c < C_::kOwnPieces)
+                mbar_arrive_expect_tx(smem_u32(&bar_xchg[c]), C_::kColPieceBytes);
         }
         mbar_init(smem_u32(&bar_drain), 1);
         abort_flag = 0;
@@ -222,30 +234,29 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
     } else {
         // ------------------------------ epilogue (warps 2..5) ------------------------------
         const int q = warp & 3;  // Tensor Memory lane quarter this warp may access
-        const uint32_t owner = (uint32_t)(q / kQPerBand);
-        const int qb = q % kQPerBand;  // quarter within the owner's band
-        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16);
-        const bool empty_slice = kb1 <= kb0;  // no K-blocks: this CTA's share is zero
-        int ok = 1;
-        if (lane == 0)
-            ok = wait_bounded(smem_u32(&bar_tfull), 0, abort, args.timeout_ns, &g_dtc_status, 24);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (ok) tc_fence_after_sync();
-        if (owner != rank) {
-            // stage this quarter piece by piece in the ring and copy each piece into the owner's
-            // exchange area, in the slot of source rank `rank`
-            const uint32_t slot = rank < owner ? rank : rank - 1;
-            const uint32_t first_own = rank * kQPerBand;
-            const uint32_t pidx = (uint32_t)q < first_own ? (uint32_t)q : (uint32_t)q - kQPerBand;
-            const uint32_t stage = sA + pidx * (C_::kPieces * C_::kQPieceBytes);
-            cluster_wait();  // the owner's barriers exist
+        if constexpr (C_::kColOwn) {
+            // Split in 2, column ownership: CTA r owns pieces [r*kOwnPieces, (r+1)*kOwnPieces).
+            // Every warp first copies its 32 rows of the peer's pieces into the peer's exchange
+            // area (piece j of the peer at rows 32q..32q+31, the bytes counted on the peer's
+            // bar_xchg[j]), then sums its rows of its own pieces with the peer's copies, in rank
+            // order, and stores them.
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16);
+            const bool empty_slice = kb1 <= kb0;  // no K-blocks: this CTA's share is zero
+            const uint32_t peer = rank ^ 1u;
+            int ok = 1;
+            if (lane == 0)
+                ok = wait_bounded(smem_u32(&bar_tfull), 0, abort, args.timeout_ns, &g_dtc_status, 24);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (ok) tc_fence_after_sync();
+            cluster_wait();  // the peer's barriers exist
             cluster_waited = true;
             if (ok) {
+                const uint32_t stage = sA + (uint32_t)q * (C_::kOwnPieces * C_::kQPieceBytes);
 #pragma unroll 1
-                for (int c = 0; c < C_::kPieces; ++c) {
+                for (int j = 0; j < C_::kOwnPieces; ++j) {
                     uint32_t v[64];
-                    tmem_load_64cols(taddr + c * 64, v);
-                    const uint32_t spiece = stage + c * C_::kQPieceBytes;
+                    tmem_load_64cols(taddr + (peer * C_::kOwnPieces + j) * 64, v);
+                    const uint32_t spiece = stage + j * C_::kQPieceBytes;
                     const uint32_t srow = spiece + lane * C_::kXPitch;
 #pragma unroll
                     for (int g = 0; g < 16; ++g) {
@@ -258,60 +269,147 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
                     fence_proxy_async_smem();  // the staging writes, before the copy engine reads
                     __syncwarp();
                     if (lane == 0) {
-                        const uint32_t dst = sX + slot * C_::kXSlot +
-                                             (c * C_::kBandRows + qb * 32) * C_::kXPitch;
-                        bulk_copy_smem_to_cta(map_to_cta(dst, owner), spiece, C_::kQPieceBytes,
-                                              map_to_cta(smem_u32(&bar_xchg[c]), owner));
+                        const uint32_t dst = sX + (j * kBM + q * 32) * C_::kXPitch;
+                        bulk_copy_smem_to_cta(map_to_cta(dst, peer), spiece, C_::kQPieceBytes,
+                                              map_to_cta(smem_u32(&bar_xchg[j]), peer));
                     }
                 }
-            }
-        } else if (ok) {
-            // C through two staging slots over the idle ring (after the pushed quarters' copies)
-            const uint32_t my_slots = sA + C_::kStaging + (uint32_t)qb * 8192u;
-            uint32_t stores = 0;
+                const uint32_t my_slots = sA + C_::kStaging + (uint32_t)q * 8192u;
+                uint32_t stores = 0;
 #pragma unroll 1
-            for (int c = 0; c < C_::kPieces; ++c) {
-                uint32_t v[64];
-                tmem_load_64cols(taddr + c * 64, v);  // own partial sums, ready since tfull
-                int xok = 1;
-                if (lane == 0)
-                    xok = wait_bounded<true>(smem_u32(&bar_xchg[c]), 0, abort, args.timeout_ns,
-                                             &g_dtc_status, 25);
-                xok = __shfl_sync(0xffffffffu, xok, 0);
-                if (!xok) break;
-                // the phase has completed: every lane takes its own acquire of it
-                (void)mbar_try_wait_cluster(smem_u32(&bar_xchg[c]), 0);
-                float acc[64];
-                // sum over source ranks 0..kS-1 in that order (own rows from Tensor Memory)
+                for (int j = 0; j < C_::kOwnPieces; ++j) {
+                    const int gp = (int)rank * C_::kOwnPieces + j;  // piece index within the tile
+                    uint32_t v[64];
+                    tmem_load_64cols(taddr + gp * 64, v);  // own partial sums, ready since tfull
+                    int xok = 1;
+                    if (lane == 0)
+                        xok = wait_bounded<true>(smem_u32(&bar_xchg[j]), 0, abort, args.timeout_ns,
+                                                 &g_dtc_status, 25);
+                    xok = __shfl_sync(0xffffffffu, xok, 0);
+                    if (!xok) break;
+                    // the phase has completed: every lane takes its own acquire of it
+                    (void)mbar_try_wait_cluster(smem_u32(&bar_xchg[j]), 0);
+                    const uint32_t xrow = sX + (j * kBM + q * 32 + lane) * C_::kXPitch;
+                    float acc[64];
 #pragma unroll
-                for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+                    for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
 #pragma unroll
-                for (int src = 0; src < kS; ++src) {
-                    if (src == (int)rank) {
+                    for (int src = 0; src < 2; ++src) {  // rank order: the same sum either way
+                        if (src == (int)rank) {
 #pragma unroll
-                        for (int i = 0; i < 64; ++i)
-                            acc[i] += empty_slice ? 0.0f : __uint_as_float(v[i]);
-                    } else {
-                        const int slot = src < (int)rank ? src : src - 1;
-                        const uint32_t xrow = sX + slot * C_::kXSlot +
-                                              (c * C_::kBandRows + qb * 32 + lane) * C_::kXPitch;
+                            for (int i = 0; i < 64; ++i)
+                                acc[i] += empty_slice ? 0.0f : __uint_as_float(v[i]);
+                        } else {
 #pragma unroll
+                            for (int g = 0; g < 16; ++g) {
+                                const float4 pp = ld_shared_f4(xrow + ((g ^ (lane & 7)) << 4));
+                                acc[g * 4 + 0] += pp.x;
+                                acc[g * 4 + 1] += pp.y;
+                                acc[g * 4 + 2] += pp.z;
+                                acc[g * 4 + 3] += pp.w;
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) v[i] = __float_as_uint(acc[i]);
+                    store_chunk16<kBF16, 64>(&tmC, my_slots, stores, v, nt * kBN + gp * 64,
+                                             mt * kBM + q * 32, args.M, args.N, lane);
+                }
+                if (lane == 0) bulk_wait_group_read<0>();  // the C stores have read their slots
+                __syncwarp();
+            }
+        } else {
+            const uint32_t owner = (uint32_t)(q / kQPerBand);
+            const int qb = q % kQPerBand;  // quarter within the owner's band
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16);
+            const bool empty_slice = kb1 <= kb0;  // no K-blocks: this CTA's share is zero
+            int ok = 1;
+            if (lane == 0)
+                ok = wait_bounded(smem_u32(&bar_tfull), 0, abort, args.timeout_ns, &g_dtc_status, 24);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (ok) tc_fence_after_sync();
+            if (owner != rank) {
+                // stage this quarter piece by piece in the ring and copy each piece into the owner's
+                // exchange area, in the slot of source rank `rank`
+                const uint32_t slot = rank < owner ? rank : rank - 1;
+                const uint32_t first_own = rank * kQPerBand;
+                const uint32_t pidx = (uint32_t)q < first_own ? (uint32_t)q : (uint32_t)q - kQPerBand;
+                const uint32_t stage = sA + pidx * (C_::kPieces * C_::kQPieceBytes);
+                cluster_wait();  // the owner's barriers exist
+                cluster_waited = true;
+                if (ok) {
+    #pragma unroll 1
+                    for (int c = 0; c < C_::kPieces; ++c) {
+                        uint32_t v[64];
+                        tmem_load_64cols(taddr + c * 64, v);
+                        const uint32_t spiece = stage + c * C_::kQPieceBytes;
+                        const uint32_t srow = spiece + lane * C_::kXPitch;
+    #pragma unroll
                         for (int g = 0; g < 16; ++g) {
-                            const float4 p = ld_shared_f4(xrow + ((g ^ (lane & 7)) << 4));
-                            acc[g * 4 + 0] += p.x;
-                            acc[g * 4 + 1] += p.y;
-                            acc[g * 4 + 2] += p.z;
-                            acc[g * 4 + 3] += p.w;
+                            const uint32_t a = srow + ((g ^ (lane & 7)) << 4);
+                            if (empty_slice)
+                                st_shared_u4(a, 0u, 0u, 0u, 0u);
+                            else
+                                st_shared_u4(a, v[g * 4 + 0], v[g * 4 + 1], v[g * 4 + 2], v[g * 4 + 3]);
+                        }
+                        fence_proxy_async_smem();  // the staging writes, before the copy engine reads
+                        __syncwarp();
+                        if (lane == 0) {
+                            const uint32_t dst = sX + slot * C_::kXSlot +
+                                                 (c * C_::kBandRows + qb * 32) * C_::kXPitch;
+                            bulk_copy_smem_to_cta(map_to_cta(dst, owner), spiece, C_::kQPieceBytes,
+                                                  map_to_cta(smem_u32(&bar_xchg[c]), owner));
                         }
                     }
                 }
-#pragma unroll
-                for (int i = 0; i < 64; ++i) v[i] = __float_as_uint(acc[i]);
-                store_chunk16<kBF16, 64>(&tmC, my_slots, stores, v, nt * kBN + c * 64,
-                                         mt * kBM + q * 32, args.M, args.N, lane);
+            } else if (ok) {
+                // C through two staging slots over the idle ring (after the pushed quarters' copies)
+                const uint32_t my_slots = sA + C_::kStaging + (uint32_t)qb * 8192u;
+                uint32_t stores = 0;
+    #pragma unroll 1
+                for (int c = 0; c < C_::kPieces; ++c) {
+                    uint32_t v[64];
+                    tmem_load_64cols(taddr + c * 64, v);  // own partial sums, ready since tfull
+                    int xok = 1;
+                    if (lane == 0)
+                        xok = wait_bounded<true>(smem_u32(&bar_xchg[c]), 0, abort, args.timeout_ns,
+                                                 &g_dtc_status, 25);
+                    xok = __shfl_sync(0xffffffffu, xok, 0);
+                    if (!xok) break;
+                    // the phase has completed: every lane takes its own acquire of it
+                    (void)mbar_try_wait_cluster(smem_u32(&bar_xchg[c]), 0);
+                    float acc[64];
+                    // sum over source ranks 0..kS-1 in that order (own rows from Tensor Memory)
+    #pragma unroll
+                    for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+    #pragma unroll
+                    for (int src = 0; src < kS; ++src) {
+                        if (src == (int)rank) {
+    #pragma unroll
+                            for (int i = 0; i < 64; ++i)
+                                acc[i] += empty_slice ? 0.0f : __uint_as_float(v[i]);
+                        } else {
+                            const int slot = src < (int)rank ? src : src - 1;
+                            const uint32_t xrow = sX + slot * C_::kXSlot +
+                                                  (c * C_::kBandRows + qb * 32 + lane) * C_::kXPitch;
+    #pragma unroll
+                            for (int g = 0; g < 16; ++g) {
+                                const float4 p = ld_shared_f4(xrow + ((g ^ (lane & 7)) << 4));
+                                acc[g * 4 + 0] += p.x;
+                                acc[g * 4 + 1] += p.y;
+                                acc[g * 4 + 2] += p.z;
+                                acc[g * 4 + 3] += p.w;
+                            }
+                        }
+                    }
+    #pragma unroll
+                    for (int i = 0; i < 64; ++i) v[i] = __float_as_uint(acc[i]);
+                    store_chunk16<kBF16, 64>(&tmC, my_slots, stores, v, nt * kBN + c * 64,
+                                             mt * kBM + q * 32, args.M, args.N, lane);
+                }
+                if (lane == 0) bulk_wait_group_read<0>();  // the C stores have read their slots
+                __syncwarp();
             }
-            if (lane == 0) bulk_wait_group_read<0>();  // the C stores have read their slots
-            __syncwarp();
         }
     }
 
