@@ -82,12 +82,39 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def code_text(src):
+    """C/C++ source with its comments removed and whitespace runs collapsed (string and character
+    literals kept intact), so that a hash of it changes with the code but not with its comments."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":  # a literal: copy it whole, escapes included
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def source_hash():
+    """Hash of the kernel sources' code (comments and layout ignored): the DRAM traffic recorded by
+    an ncu capture stays valid while the code it was taken on is unchanged."""
     h = hashlib.sha256()
     for f in sorted(os.listdir(CSRC)):
         if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(CSRC, f), "rb") as fh:
-                h.update(f.encode() + b"\0" + fh.read())
+            with open(os.path.join(CSRC, f), encoding="utf-8") as fh:
+                h.update(f.encode() + b"\0" + code_text(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -11,10 +11,11 @@
 //     .cta_group::2), which the leader arms with the bytes of both CTAs;
 //   - holds rows 128*r..128*r+127 of the accumulator in its own Tensor Memory.
 // The leader's single MMA thread issues tcgen05.mma.cta_group::2 (M = 256, N = kBN, K = 16); the
-// tensor cores of both SMs read A and B from both CTAs' shared memory at the same offsets. Its
-// commits arrive on the empty / accumulator-full barriers of both CTAs (one commit per CTA, at
-// shared::cluster addresses; no multicast). Each CTA's epilogue drains its own 128 rows and
-// arrives on the leader's accumulator-empty barrier (8 arrivals: 4 warps x 2 CTAs).
+// tensor cores of both SMs read A and B from both CTAs' shared memory at the same offsets. Each of
+// its commits arrives on the empty / accumulator-full barrier at the same offset in both CTAs (one
+// tcgen05.commit with .multicast::cluster, mask 0b11). Each CTA's epilogue drains its own 128 rows
+// through swizzled shared-memory staging and TMA tensor stores, and arrives on the leader's
+// accumulator-empty barrier (8 arrivals: 4 warps x 2 CTAs) once it has read the accumulator.
 // Compared with one CTA per 128 x 256 tile, every SM loads half as much of B per FLOP, and a stage
 // takes 16 + kBN/8 KiB of shared memory, which leaves room for a deeper ring.
 //

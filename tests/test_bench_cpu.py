@@ -39,6 +39,17 @@ def test_traffic_record_is_dropped_when_the_kernel_source_changes(tmp_path, monk
     assert bench.recorded_traffic("w", "k") is None
 
 
+def test_code_hash_ignores_comments_but_not_code():
+    a = 'int f(int x) {  // add one\n    return x + 1; /* done */ }\nconst char* s = "a // b";\n'
+    b = 'int f(int x) {\n  return x + 1;   }\n// a note\nconst char* s = "a // b";\n'
+    c = 'int f(int x) {\n  return x + 2; }\nconst char* s = "a // b";\n'
+    d = 'int f(int x) {\n  return x + 1; }\nconst char* s = "a // c";\n'
+    assert bench.code_text(a) == bench.code_text(b)
+    assert bench.code_text(a) != bench.code_text(c)
+    assert bench.code_text(a) != bench.code_text(d)  # text inside a literal is code
+    assert "note" not in bench.code_text(b) and '"a // b"' in bench.code_text(b)
+
+
 _WORKER = r"""
 import os, sys
 sys.path.insert(0, {root!r})
