@@ -208,6 +208,123 @@ class ClockSampler:
         return "\n".join(self.lines)
 
 
+# NVML clock-event reason bits (nvml.h: nvmlClocksEventReason*), the ones the record names
+NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+def summarise_samples(samples, t0, t1):
+    """Clocks record from NVML samples (dicts with t, sm, max, reasons bits): the median SM clock,
+    the highest max clock and the active reasons, over the samples taken inside [t0, t1] (the
+    timed region), else over all of them."""
+    sel = [s for s in samples if t0 <= s["t"] <= t1]
+    window = "timed"
+    if not sel:
+        sel, window = list(samples), "whole run"
+    if not sel:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": "none"}
+    bits = 0
+    for s in sel:
+        bits |= s["reasons"]
+    return {"sm_mhz": statistics.median(s["sm"] for s in sel),
+            "sm_max_mhz": max(s["max"] for s in sel),
+            "reasons": sorted(name for bit, name in NVML_REASONS.items() if bits & bit),
+            "samples": len(sel), "window": window,
+            "power_w_max": max(s.get("power", 0.0) for s in sel)}
+
+
+class NvmlSampler:
+    """SM clock, power and clock-event reasons of one GPU, read through NVML (the driver's
+    libnvidia-ml, loaded with ctypes; reads only) every `period_s` in a background thread, with
+    host timestamps. Unavailable (ok() is False) where NVML cannot be loaded."""
+
+    NVML_CLOCK_SM = 1
+
+    def __init__(self, uuid, period_s=0.001):
+        self.uuid = uuid
+        self.period = period_s
+        self.samples = []
+        self.lib = None
+        self.handle = None
+        self._stop = False
+
+    def ok(self):
+        return self.handle is not None
+
+    def __enter__(self):
+        import ctypes
+        import threading
+
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return self
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByUUID(("GPU-" + str(self.uuid)).encode(), ctypes.byref(h)) != 0:
+                lib.nvmlShutdown()
+                return self
+            self.lib, self.handle = lib, h
+        except (OSError, AttributeError):
+            return self
+        get_reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(self.lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        mx = ctypes.c_uint(0)
+        self.lib.nvmlDeviceGetMaxClockInfo(self.handle, self.NVML_CLOCK_SM, ctypes.byref(mx))
+
+        def poll():
+            clk, mw, rs = ctypes.c_uint(0), ctypes.c_uint(0), ctypes.c_ulonglong(0)
+            while not self._stop:
+                if self.lib.nvmlDeviceGetClockInfo(self.handle, self.NVML_CLOCK_SM,
+                                                   ctypes.byref(clk)) == 0:
+                    self.lib.nvmlDeviceGetPowerUsage(self.handle, ctypes.byref(mw))
+                    get_reasons(self.handle, ctypes.byref(rs))
+                    self.samples.append({"t": time.time(), "sm": float(clk.value),
+                                         "max": float(mx.value), "power": mw.value / 1000.0,
+                                         "reasons": int(rs.value)})
+                time.sleep(self.period)
+
+        self.thread = threading.Thread(target=poll, daemon=True)
+        self.thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.handle is not None:
+            time.sleep(2 * self.period)
+            self._stop = True
+            self.thread.join(timeout=5)
+            self.lib.nvmlShutdown()
+
+
+class Clocks:
+    """NVML sampling at 1 ms where available, else nvidia-smi at 20 ms; `record(t0, t1)` gives the
+    clocks record of a timed region."""
+
+    def __init__(self, uuid, gpu_index):
+        self.nvml = NvmlSampler(uuid)
+        self.smi = None
+        self.gpu_index = gpu_index
+
+    def __enter__(self):
+        self.nvml.__enter__()
+        if not self.nvml.ok():
+            self.smi = ClockSampler(self.gpu_index).__enter__()
+        return self
+
+    def __exit__(self, *exc):
+        if self.smi is not None:
+            self.smi.__exit__(*exc)
+        self.nvml.__exit__(*exc)
+
+    def record(self, t0, t1):
+        if self.nvml.ok():
+            r = summarise_samples(self.nvml.samples, t0, t1)
+            r["source"] = "NVML, 1 ms period"
+            return r
+        r = parse_clocks(self.smi.text(), t0, t1) if self.smi else parse_clocks("", t0, t1)
+        r["source"] = "nvidia-smi, 20 ms period"
+        return r
+
+
 # ------------------------------------------------------------------------------------------------
 # CPU oracle leg
 # ------------------------------------------------------------------------------------------------
@@ -395,8 +512,111 @@ def library_context(w, A, B, flush_l2, stream, steps, dev):
                     "timed region: context only"}
 
 
-def run_ours(args, w):
+# The benchmark configurations of the pages' workloads (one JSON row each in `configs`), with the
+# roofline that bounds each: the tiny and the 1024^3 products are launch- and occupancy-bound, the
+# skinny M = 128 product is HBM-bound, the rest tensor-bound.
+BASELINE_CONFIGS = [
+    ("1", "bf16_nt_256x256x512", "latency"),
+    ("2", "f16_nn_1024x1024x1024", "latency"),
+    ("3", "bf16_nt_4096x4096x8192", "tensor"),
+    ("4a", "bf16_nt_8192x8192x8192", "tensor"),
+    ("4b", "bf16_nt_128x8192x8192", "hbm"),
+    ("5", "mxfp8_nt_4096x4096x8192", "tensor"),
+]
+
+
+def device_inputs(w, dev):
+    """The workload's seeded host inputs, on the device: (dev_in, out_dtype, inputs)."""
     import numpy as np
+    import torch
+
+    from dense_tensor_core_gb300 import workloads
+
+    inputs = workloads.make(w)
+    if w.kind == "mxfp8":
+        dev_in = [torch.from_numpy(x).to(dev) for x in inputs]
+        return dev_in, torch.bfloat16, inputs
+    t16 = torch.bfloat16 if w.kind == "bf16" else torch.float16
+    dev_in = [torch.from_numpy(x.view(np.int16)).view(t16).to(dev) for x in inputs]
+    return dev_in, t16, inputs
+
+
+def gemm_kwargs(args, w, dtc, dev):
+    """Options of the call a user would make for this workload: the automatic plan, and the
+    stream-K workspace the library asks for (zero-filled before first use)."""
+    import torch
+
+    if w.kind == "mxfp8":
+        return dict(a_format=w.a_fmt, b_format=w.b_fmt, scale_block=w.block, variant=args.variant)
+    kw = dict(layout=w.layout, variant=args.variant, split_k=args.split_k, tile_n=args.tile_n)
+    if args.stream_k != 2:
+        ws_bytes = dtc.gemm_workspace_size(w.kind, w.M, w.N, w.K, w.layout, variant=args.variant,
+                                           tile_n=args.tile_n, stream_k=args.stream_k)
+        if ws_bytes:
+            kw.update(workspace=torch.zeros(ws_bytes, dtype=torch.uint8, device=dev),
+                      stream_k=args.stream_k)
+    return kw
+
+
+def call(dtc, w, ins, C, kw, stream):
+    if w.kind == "mxfp8":
+        dtc.gemm_ex("mxfp8", ins[0], ins[1], C, sfA=ins[2], sfB=ins[3], stream=stream, **kw)
+    else:
+        dtc.gemm_ex(w.kind, ins[0], ins[1], C, stream=stream, **kw)
+
+
+def plan_of(dtc, w, kw):
+    keys = ("layout", "variant", "split_k", "tile_n", "workspace", "stream_k", "a_format",
+            "b_format", "scale_block")
+    return dtc.gemm_plan(w.kind, w.M, w.N, w.K, **{k: v for k, v in kw.items() if k in keys})
+
+
+def timed_steps(step, flush_l2, steps, warmup, stream, dev, world):
+    """W warm-up steps, then `steps` timed ones, each bracketed by CUDA events on the launching
+    stream after an L2 flush outside the events; returns (per-step ms, t0, t1 host times)."""
+    import torch
+
+    for _ in range(warmup):
+        flush_l2(1)
+        step()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    for i in range(steps):
+        flush_l2(i)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t1 = time.time()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)], t0, t1
+
+
+def roofline_of(w, kernel_ms, bound, kernel_name, peaks, peak_src):
+    """The roofline record of one launch of `kernel_name` on workload w."""
+    if bound == "hbm":
+        bw = w.min_bytes / (kernel_ms / 1e3) / 1e9
+        return {"bound": "hbm", "achieved": bw, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": bw / peaks["hbm_gbs"], "traffic": recorded_traffic(w.name, kernel_name),
+                "kernel": kernel_name, "peak_source": f"{peak_src} HBM copy bandwidth",
+                "algorithmic_bytes_per_launch": w.min_bytes}
+    achieved = w.flops / (kernel_ms / 1e3) / 1e12
+    if w.kind == "mxfp8":
+        # fp8 dense rate = 2x the bf16 rate (nominal 4.5 vs 2.25 PFLOP/s)
+        peak = 2.0 * peaks["bf16_tflops"]
+        note = f"2 x {peak_src} bf16 burst (nominal fp8:bf16 ratio)"
+    else:
+        peak = peaks["bf16_tflops"]
+        note = f"{peak_src} bf16 burst (kernel timed alone)"
+    return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": recorded_traffic(w.name, kernel_name),
+            "kernel": kernel_name, "peak_source": note, "algorithmic_flops_per_launch": w.flops}
+
+
+def run_ours(args, w):
     import torch
 
     rank, world, local = dist_env()
@@ -414,26 +634,6 @@ def run_ours(args, w):
     import dense_tensor_core_gb300 as dtc
     from dense_tensor_core_gb300 import workloads
 
-    inputs = workloads.make(w)
-    if w.kind == "mxfp8":
-        A_h, B_h, sfA_h, sfB_h = inputs
-        A = torch.from_numpy(A_h).to(dev)
-        B = torch.from_numpy(B_h).to(dev)
-        sfA = torch.from_numpy(sfA_h).to(dev)
-        sfB = torch.from_numpy(sfB_h).to(dev)
-        out_dtype = torch.bfloat16
-        host_in = [torch.from_numpy(x).pin_memory() for x in inputs]
-        dev_in = [A, B, sfA, sfB]
-    else:
-        A_h, B_h = inputs
-        t16 = torch.bfloat16 if w.kind == "bf16" else torch.float16
-        A = torch.from_numpy(A_h.view(np.int16)).view(t16).to(dev)
-        B = torch.from_numpy(B_h.view(np.int16)).view(t16).to(dev)
-        out_dtype = t16
-        host_in = [A.cpu().pin_memory(), B.cpu().pin_memory()]
-        dev_in = [A, B]
-    C = torch.empty((w.M, w.N), dtype=out_dtype, device=dev)
-    host_out = torch.empty((w.M, w.N), dtype=out_dtype).pin_memory()
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_read = flush[: FLUSH_READ_BYTES // 4]
     flush_sink = torch.zeros((), dtype=torch.float32, device=dev)
@@ -443,79 +643,84 @@ def run_ours(args, w):
         flush.fill_(float(i))
         torch.sum(flush_read, dim=0, out=flush_sink)  # evicts (writes back) the dirty lines
 
-    mx = (dict(a_format=w.a_fmt, b_format=w.b_fmt, scale_block=w.block) if w.kind == "mxfp8"
-          else {})
-    # stream-K workspace, as a user would pass it (zero-filled before first use)
-    if w.kind != "mxfp8" and args.stream_k != 2:
-        ws_bytes = dtc.gemm_workspace_size(w.kind, w.M, w.N, w.K, w.layout, variant=args.variant,
-                                           tile_n=args.tile_n, stream_k=args.stream_k)
-        if ws_bytes:
-            mx = dict(workspace=torch.zeros(ws_bytes, dtype=torch.uint8, device=dev),
-                      stream_k=args.stream_k)
+    props = torch.cuda.get_device_properties(dev)
+    peaks, peak_src = load_peaks()
+    launches = 0
+    with Clocks(getattr(props, "uuid", ""), local if world > 1 else 0) as clk:
+        dev_in, out_dtype, inputs = device_inputs(w, dev)
+        C = torch.empty((w.M, w.N), dtype=out_dtype, device=dev)
+        kw = gemm_kwargs(args, w, dtc, dev)
+        plan = plan_of(dtc, w, kw)
+        step_ms, t0, t1 = timed_steps(lambda: call(dtc, w, dev_in, C, kw, stream), flush_l2,
+                                      args.steps, args.warmup, stream, dev, world)
+        launches += args.steps
+        dtc.gemm_stream_status(stream)
+        clocks = clk.record(t0, t1)
 
-    def step_e2e(ins, Cout, st):
-        if w.kind == "mxfp8":
-            dtc.gemm_ex("mxfp8", ins[0], ins[1], Cout, sfA=ins[2], sfB=ins[3], variant=args.variant,
-                        stream=st, **mx)
-        else:
-            dtc.gemm_ex(w.kind, ins[0], ins[1], Cout, layout=w.layout, variant=args.variant,
-                        split_k=args.split_k, tile_n=args.tile_n, cluster_m=args.cluster_m,
-                        stream=st, **mx)
+        total_ms = max_over_ranks(sum(step_ms), world)
+        ms_per_step = total_ms / args.steps
+        value = world * float(w.flops) * args.steps / (total_ms / 1e3) / 1e12
+        kernel_ms = statistics.mean(step_ms)  # one launch of our kernel per step
+        kernel_name = kernel_of(w, plan)
 
-    def step():
-        if w.kind == "mxfp8":
-            dtc.gemm_ex("mxfp8", A, B, C, sfA=sfA, sfB=sfB, variant=args.variant, stream=stream,
-                        **mx)
-        else:
-            dtc.gemm_ex(w.kind, A, B, C, layout=w.layout, variant=args.variant,
-                        split_k=args.split_k, tile_n=args.tile_n, cluster_m=args.cluster_m,
-                        stream=stream, **mx)
+        # End to end through the public call with host buffers: every step copies its inputs
+        # from pinned host memory (H2D), runs the GEMM and copies the result back (D2H). The steps
+        # are pipelined as a streaming user would run them: two device copies of the inputs and
+        # of C, H2D on one stream, the GEMM on another, D2H on a third, so step i+1's inputs cross
+        # the host link while step i computes and step i-1's result comes back. Events order
+        # every reuse of a buffer after its previous reader.
+        host_in = [t.cpu().pin_memory() for t in dev_in]
+        host_out = torch.empty((w.M, w.N), dtype=out_dtype).pin_memory()
+        e2e_steps = max(1, min(args.steps, 20))  # each step moves the workload over the host link
+        e2e_ms = run_e2e(w, dtc, host_in, dev_in, C, host_out,
+                         lambda ins, Cout, st: call(dtc, w, ins, Cout, kw, st), stream, e2e_steps,
+                         dev)
+        launches += e2e_steps
+        e2e_ms = max_over_ranks(e2e_ms, world)
+        dtc.gemm_stream_status(stream)
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = host_out.numel() * host_out.element_size()
+        e2e_value = world * float(w.flops) * e2e_steps / (e2e_ms / 1e3) / 1e12
+        library = library_context(w, dev_in[0], dev_in[1], flush_l2, stream,
+                                  min(args.steps, 50), dev)
+        del host_in, host_out
 
-    plan = dtc.gemm_plan(w.kind, w.M, w.N, w.K, w.layout, variant=args.variant,
-                         split_k=args.split_k, tile_n=args.tile_n, cluster_m=args.cluster_m, **mx)
-
-    for _ in range(args.warmup):
-        flush_l2(1)
-        step()
-    dtc.gemm_stream_status(stream)
-
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    with ClockSampler(local if world > 1 else 0) as clk:
-        barrier(world)
-        torch.cuda.synchronize(dev)
-        t0 = time.time()
-        for i in range(args.steps):
-            flush_l2(i)
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
-        torch.cuda.synchronize(dev)
-        barrier(world)
-        t1 = time.time()
-    dtc.gemm_stream_status(stream)
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = max_over_ranks(sum(step_ms), world)
-    ms_per_step = total_ms / args.steps
-    flops_step = float(w.flops)
-    value = world * flops_step * args.steps / (total_ms / 1e3) / 1e12
-    kernel_ms = statistics.mean(step_ms)  # one launch of our kernel per step
-
-    # End to end through the public call with host buffers: every step copies its inputs from
-    # pinned host memory (H2D), runs the GEMM and copies the result back (D2H). The steps are
-    # pipelined as a streaming user would run them: two device copies of the inputs and of C,
-    # H2D on one stream, the GEMM on another, D2H on a third, so step i+1's inputs cross the host
-    # link while step i computes and step i-1's result comes back. Events order every reuse of a
-    # buffer after its previous reader.
-    e2e_steps = max(1, min(args.steps, 20))  # each step moves the whole workload over the host link
-    e2e_ms = run_e2e(w, dtc, host_in, dev_in, C, host_out, step_e2e, stream, e2e_steps, dev)
-    e2e_ms = max_over_ranks(e2e_ms, world)
-    dtc.gemm_stream_status(stream)
-    h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = host_out.numel() * host_out.element_size()
-    e2e_value = world * flops_step * e2e_steps / (e2e_ms / 1e3) / 1e12
-
-    library = library_context(w, A, B, flush_l2, stream, min(args.steps, 50), dev)
+        # every benchmark configuration of the pages' workloads, timed the same way
+        configs = {}
+        if not args.no_configs and world == 1:
+            cfg_steps = max(20, min(args.steps, 200))
+            for cid, name, bound in BASELINE_CONFIGS:
+                cw = workloads.WORKLOADS[name]
+                if name == w.name:
+                    cms, cplan, ct0, ct1, cname, clib = kernel_ms, plan, t0, t1, kernel_name, library
+                    csteps = args.steps
+                else:
+                    cin, cdt, _ = device_inputs(cw, dev)
+                    cC = torch.empty((cw.M, cw.N), dtype=cdt, device=dev)
+                    ckw = gemm_kwargs(args, cw, dtc, dev)
+                    cplan = plan_of(dtc, cw, ckw)
+                    cms_list, ct0, ct1 = timed_steps(
+                        lambda: call(dtc, cw, cin, cC, ckw, stream), flush_l2, cfg_steps, 5,
+                        stream, dev, world)
+                    launches += cfg_steps
+                    dtc.gemm_stream_status(stream)
+                    cms = statistics.mean(cms_list)
+                    cname = kernel_of(cw, cplan)
+                    clib = library_context(cw, cin[0], cin[1], flush_l2, stream, cfg_steps, dev)
+                    csteps = cfg_steps
+                    del cin, cC, ckw
+                rl = roofline_of(cw, cms, "hbm" if bound == "hbm" else "tensor", cname, peaks,
+                                 peak_src)
+                configs[cid] = {
+                    "workload": name, "bound": bound, "kernel": cname, "steps": csteps,
+                    "us_per_launch": 1e3 * cms, "tflops": cw.flops / (cms / 1e3) / 1e12,
+                    "gbs_compulsory": cw.min_bytes / (cms / 1e3) / 1e9,
+                    "frac": rl["frac"], "frac_of": f'{rl["peak"]:.1f} {rl["unit"]} ({rl["peak_source"]})',
+                    "tile": f"{cplan['tile_m']}x{cplan['tile_n']}x{cplan['tile_k']}",
+                    "split_k": cplan["split_k"], "stream_k_tiles": cplan["sk_tiles"],
+                    "library_context_tflops": clib["torch_matmul"] if clib else None,
+                    "clocks": clk.record(ct0, ct1),
+                }
 
     if rank != 0:
         if world > 1:
@@ -524,27 +729,10 @@ def run_ours(args, w):
             dist.destroy_process_group()
         return 0
 
-    peaks, peak_src = load_peaks()
-    if w.kind == "mxfp8":
-        # fp8 dense rate = 2x the bf16 rate (nominal 4.5 vs 2.25 PFLOP/s)
-        peak = 2.0 * peaks["bf16_tflops"]
-        peak_note = f"2 x {peak_src} bf16 burst (nominal fp8:bf16 ratio)"
-    else:
-        peak = peaks["bf16_tflops"]
-        peak_note = f"{peak_src} bf16 burst (kernel timed alone)"
-    kernel_name = kernel_of(w, plan)
-    achieved = flops_step / (kernel_ms / 1e3) / 1e12
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": recorded_traffic(w.name, kernel_name),
-                "kernel": kernel_name, "peak_source": peak_note,
-                "algorithmic_flops_per_launch": flops_step}
-    if w.name == "bf16_nt_128x8192x8192" or (w.M <= 256 and w.kind != "mxfp8"):
-        bw = w.min_bytes / (kernel_ms / 1e3) / 1e9
-        roofline = {"bound": "hbm", "achieved": bw, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": bw / peaks["hbm_gbs"], "traffic": recorded_traffic(w.name, kernel_name),
-                    "kernel": kernel_name, "peak_source": f"{peak_src} HBM copy bandwidth",
-                    "algorithmic_bytes_per_launch": w.min_bytes}
-    clocks = parse_clocks(clk.text(), t0, t1)
+    bound = "hbm" if (w.name == "bf16_nt_128x8192x8192" or (w.M <= 256 and w.kind != "mxfp8")) \
+        else "tensor"
+    roofline = roofline_of(w, kernel_ms, bound, kernel_name, peaks, peak_src)
+    achieved_tflops = w.flops / (kernel_ms / 1e3) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -563,7 +751,7 @@ def run_ours(args, w):
                    "l2": "flushed before every timed step, outside the step's CUDA-event "
                          "pair: 1 GiB device write, then a 256 MiB device read that writes the "
                          "flush's dirty lines back (cold, clean L2)",
-                   "pct_of_dense_peak_nominal": 100.0 * achieved /
+                   "pct_of_dense_peak_nominal": 100.0 * achieved_tflops /
                    (4500.0 if w.kind == "mxfp8" else 2250.0),
                    "timed_wall_ms": 1e3 * (t1 - t0)},
         "roofline": roofline,
@@ -571,10 +759,13 @@ def run_ours(args, w):
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "mode": "pipelined: step i+1's H2D and step i-1's D2H overlap step i's GEMM "
                         "(3 streams, 2 device buffers); pinned host memory"},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps,  # our kernel, once per timed step of the headline
+        "gpu_launches_whole_run": launches,  # with the end-to-end steps and the other configs
         "clocks": clocks,
         "library_context": library,
     }
+    if configs:
+        line["configs"] = configs
     if not args.skip_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, inputs, target_s=args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -595,10 +786,11 @@ def main(argv=None):
     p.add_argument("--variant", type=int, default=0, help="0 auto, 1 one-CTA, 2 CTA pair, 3 split-K")
     p.add_argument("--split-k", type=int, default=0)
     p.add_argument("--tile-n", type=int, default=0, help="force the N-tile (256 or 224)")
-    p.add_argument("--cluster-m", type=int, default=0, help="force the one-CTA cluster size")
     p.add_argument("--stream-k", type=int, default=0, choices=[0, 1, 2],
                    help="stream-K on CTA pairs: 0 auto (a workspace is passed when it helps), "
                         "1 required, 2 off")
+    p.add_argument("--no-configs", action="store_true",
+                   help="time only the chosen workload (not every benchmark configuration)")
     p.add_argument("--skip-cpu-baseline", action="store_true",
                    help="omit the oracle timing (profiling runs)")
     p.add_argument("--cpu-seconds", type=float, default=15.0)

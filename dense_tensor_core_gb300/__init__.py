@@ -14,8 +14,10 @@ from ._binding import (  # noqa: F401
     GEMM_VARIANT_2CTA,
     GEMM_VARIANT_AUTO,
     GEMM_VARIANT_SPLITK,
+    GB300_MODEL,
     GemmError,
     gemm_bf16,
+    gemm_device_model_query,
     gemm_ex,
     gemm_ex_static_workspace,
     gemm_f16,

@@ -30,7 +30,7 @@ class GemmError(RuntimeError):
 class gemm_options(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("split_k", ctypes.c_int),
                 ("timeout_ns", ctypes.c_uint64), ("fault_inject", ctypes.c_int),
-                ("tile_n", ctypes.c_int), ("cluster_m", ctypes.c_int), ("tile_k", ctypes.c_int),
+                ("tile_n", ctypes.c_int), ("tile_k", ctypes.c_int),
                 ("lda", ctypes.c_int64), ("ldb", ctypes.c_int64), ("ldc", ctypes.c_int64),
                 ("mx_a_format", ctypes.c_int), ("mx_b_format", ctypes.c_int),
                 ("mx_scale_block", ctypes.c_int), ("workspace", ctypes.c_void_p),
@@ -42,6 +42,14 @@ class gemm_plan_info(ctypes.Structure):
                 ("variant", "tile_m", "tile_n", "tile_k", "stages", "split_k", "ctas", "tiles",
                  "cluster", "sk_tiles")]
 
+
+class gemm_device_model(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in
+                ("sm_count", "pair_clusters", "split2_clusters", "split4_clusters")]
+
+
+# GB300: 152 SMs; clusters of 2 fill all 76 pairs; clusters of 4 fit 36 times
+GB300_MODEL = dict(sm_count=152, pair_clusters=76, split2_clusters=76, split4_clusters=36)
 
 _lib = None
 
@@ -72,6 +80,11 @@ def lib():
         L.gemm_plan.restype = i32
         L.gemm_plan.argtypes = [i32, i64, i64, i64, i32, ctypes.POINTER(gemm_options),
                                 ctypes.POINTER(gemm_plan_info)]
+        L.gemm_plan_model.restype = i32
+        L.gemm_plan_model.argtypes = [ctypes.POINTER(gemm_device_model), i32, i64, i64, i64, i32,
+                                      ctypes.POINTER(gemm_options), ctypes.POINTER(gemm_plan_info)]
+        L.gemm_device_model_query.restype = i32
+        L.gemm_device_model_query.argtypes = [ctypes.POINTER(gemm_device_model)]
         L.gemm_ex_static_workspace.restype = i32
         L.gemm_ex_static_workspace.argtypes = [i32, vp, vp, vp, vp, vp, i64, i64, i64, i32,
                                                ctypes.POINTER(gemm_options), vp]
@@ -95,10 +108,19 @@ def _check(status):
         raise GemmError(status, gemm_last_error())
 
 
-def _stream_handle(stream):
+def _stream_handle(stream, device=None):
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _same_device(*tensors):
+    """The one CUDA device all given tensors live on (the library works on the current device
+    only, so the call is made with that device current)."""
+    devs = {t.device for t in tensors if t is not None}
+    if len(devs) != 1:
+        raise ValueError(f"all tensors must be on one CUDA device, got {sorted(map(str, devs))}")
+    return devs.pop()
 
 
 def _ptr(t):
@@ -165,12 +187,12 @@ def _out(C, M, N, dtype, device, rows_of_larger=False):
 _MX_FORMATS = {"e4m3": 0, "e5m2": 1}
 
 
-def _options(variant, split_k, timeout_ns, fault_inject, tile_n=0, cluster_m=0, tile_k=0,
+def _options(variant, split_k, timeout_ns, fault_inject, tile_n=0, tile_k=0,
              lda=0, ldb=0, ldc=0, a_format="e4m3", b_format="e4m3", scale_block=0,
              workspace=None, stream_k=0):
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    return gemm_options(variant, split_k, timeout_ns, fault_inject, tile_n, cluster_m, tile_k,
+    return gemm_options(variant, split_k, timeout_ns, fault_inject, tile_n, tile_k,
                         lda, ldb, ldc, _MX_FORMATS[a_format], _MX_FORMATS[b_format],
                         scale_block, ws_ptr, ws_bytes, stream_k)
 
@@ -180,8 +202,10 @@ def _gemm16(name, dtype, A, B, C, layout, stream):
     _check_tensor(B, dtype, "B")
     M, N, K = _shapes16(A, B, layout)
     C = _out(C, M, N, dtype, A.device)
-    _check(getattr(lib(), name)(_ptr(A), _ptr(B), _ptr(C), M, N, K, _layout_code(layout),
-                                _stream_handle(stream)))
+    dev = _same_device(A, B, C)
+    with torch.cuda.device(dev):
+        _check(getattr(lib(), name)(_ptr(A), _ptr(B), _ptr(C), M, N, K, _layout_code(layout),
+                                    _stream_handle(stream, dev)))
     return C
 
 
@@ -216,13 +240,15 @@ def gemm_mxfp8(A, B, sfA, sfB, C=None, stream=None):
     sfB [N,ceil(K/128)] E8M0 codes (uint8); C bf16 [M,N]."""
     M, N, K = _check_mxfp8(A, B, sfA, sfB)
     C = _out(C, M, N, torch.bfloat16, A.device)
-    _check(lib().gemm_mxfp8(_ptr(A), _ptr(B), _ptr(sfA), _ptr(sfB), _ptr(C), M, N, K,
-                            _stream_handle(stream)))
+    dev = _same_device(A, B, sfA, sfB, C)
+    with torch.cuda.device(dev):
+        _check(lib().gemm_mxfp8(_ptr(A), _ptr(B), _ptr(sfA), _ptr(sfB), _ptr(C), M, N, K,
+                                _stream_handle(stream, dev)))
     return C
 
 
 def gemm_ex(kind, A, B, C=None, layout="NT", sfA=None, sfB=None, variant=0, split_k=0,
-            timeout_ns=0, fault_inject=0, tile_n=0, cluster_m=0, tile_k=0, stream=None,
+            timeout_ns=0, fault_inject=0, tile_n=0, tile_k=0, stream=None,
             a_format="e4m3", b_format="e4m3", scale_block=0, workspace=None, stream_k=0):
     """Any of the three products with options (variant, split_k, wait limit, test hook). A, B
     and C may be rows of larger row-major arrays (e.g. ``big[:, :n]``); their row strides are
@@ -242,24 +268,41 @@ def gemm_ex(kind, A, B, C=None, layout="NT", sfA=None, sfB=None, variant=0, spli
         _check_tensor(B, dt, "B", rows_of_larger=True)
         M, N, K = _shapes16(A, B, layout)
         C = _out(C, M, N, dt, A.device, rows_of_larger=True)
-    opts = _options(variant, split_k, timeout_ns, fault_inject, tile_n, cluster_m, tile_k,
+    opts = _options(variant, split_k, timeout_ns, fault_inject, tile_n, tile_k,
                     _ld(A), _ld(B), _ld(C), a_format, b_format, scale_block, workspace, stream_k)
-    _check(lib().gemm_ex(_DTYPE[kind], _ptr(A), _ptr(B), _ptr(sfA), _ptr(sfB), _ptr(C), M, N, K,
-                         _layout_code(layout), ctypes.byref(opts), _stream_handle(stream)))
+    dev = _same_device(A, B, C, sfA, sfB, workspace)
+    with torch.cuda.device(dev):
+        _check(lib().gemm_ex(_DTYPE[kind], _ptr(A), _ptr(B), _ptr(sfA), _ptr(sfB), _ptr(C), M, N,
+                             K, _layout_code(layout), ctypes.byref(opts),
+                             _stream_handle(stream, dev)))
     return C
 
 
-def gemm_plan(kind, M, N, K, layout="NT", variant=0, split_k=0, tile_n=0, cluster_m=0, tile_k=0,
-              a_format="e4m3", b_format="e4m3", scale_block=0, workspace=None, stream_k=0):
+def gemm_plan(kind, M, N, K, layout="NT", variant=0, split_k=0, tile_n=0, tile_k=0,
+              a_format="e4m3", b_format="e4m3", scale_block=0, workspace=None, stream_k=0,
+              model=None):
     """The launch the library would make for these sizes: a dict with variant, tile_m, tile_n,
     tile_k, stages, split_k, ctas, tiles, cluster, sk_tiles (raises GemmError if the call would
-    be rejected)."""
-    opts = _options(variant, split_k, 0, 0, tile_n, cluster_m, tile_k, 0, 0, 0, a_format, b_format,
+    be rejected). With `model` (a dict of gemm_device_model's fields, e.g. GB300_MODEL) the plan
+    is made for that device description, without a GPU; otherwise for the current device."""
+    opts = _options(variant, split_k, 0, 0, tile_n, tile_k, 0, 0, 0, a_format, b_format,
                     scale_block, workspace, stream_k)
     info = gemm_plan_info()
-    _check(lib().gemm_plan(_DTYPE[kind], M, N, K, _layout_code(layout), ctypes.byref(opts),
-                           ctypes.byref(info)))
+    if model is not None:
+        m = gemm_device_model(**model)
+        _check(lib().gemm_plan_model(ctypes.byref(m), _DTYPE[kind], M, N, K, _layout_code(layout),
+                                     ctypes.byref(opts), ctypes.byref(info)))
+    else:
+        _check(lib().gemm_plan(_DTYPE[kind], M, N, K, _layout_code(layout), ctypes.byref(opts),
+                               ctypes.byref(info)))
     return {n: getattr(info, n) for n, _ in gemm_plan_info._fields_}
+
+
+def gemm_device_model_query():
+    """The current device as the planner sees it (gemm_device_model's fields, as a dict)."""
+    m = gemm_device_model()
+    _check(lib().gemm_device_model_query(ctypes.byref(m)))
+    return {n: getattr(m, n) for n, _ in gemm_device_model._fields_}
 
 
 def gemm_stream_status(stream=None):
@@ -269,7 +312,7 @@ def gemm_stream_status(stream=None):
 
 def gemm_workspace_size(kind, M, N, K, layout="NT", variant=0, tile_n=0, tile_k=0, stream_k=0):
     """Bytes of workspace with which the call would use stream-K (0 if it would not)."""
-    opts = _options(variant, 0, 0, 0, tile_n, 0, tile_k, stream_k=stream_k)
+    opts = _options(variant, 0, 0, 0, tile_n, tile_k, stream_k=stream_k)
     out = ctypes.c_uint64(0)
     _check(lib().gemm_workspace_size(_DTYPE[kind], M, N, K, _layout_code(layout),
                                      ctypes.byref(opts), ctypes.byref(out)))
@@ -285,9 +328,11 @@ def gemm_ex_static_workspace(kind, A, B, C=None, layout="NT", variant=0, tile_n=
     _check_tensor(B, dt, "B", rows_of_larger=True)
     M, N, K = _shapes16(A, B, layout)
     C = _out(C, M, N, dt, A.device, rows_of_larger=True)
-    opts = _options(variant, 0, 0, 0, tile_n, 0, tile_k, _ld(A), _ld(B), _ld(C),
+    opts = _options(variant, 0, 0, 0, tile_n, tile_k, _ld(A), _ld(B), _ld(C),
                     stream_k=stream_k)
-    _check(lib().gemm_ex_static_workspace(_DTYPE[kind], _ptr(A), _ptr(B), None, None, _ptr(C),
-                                          M, N, K, _layout_code(layout), ctypes.byref(opts),
-                                          _stream_handle(stream)))
+    dev = _same_device(A, B, C)
+    with torch.cuda.device(dev):
+        _check(lib().gemm_ex_static_workspace(_DTYPE[kind], _ptr(A), _ptr(B), None, None,
+                                              _ptr(C), M, N, K, _layout_code(layout),
+                                              ctypes.byref(opts), _stream_handle(stream, dev)))
     return C

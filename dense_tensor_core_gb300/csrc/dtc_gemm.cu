@@ -1,35 +1,28 @@
 // dtc_gemm.cu -- host side of the C ABI declared in include/dtc_gemm.h: argument checks, variant
-// choice, TMA descriptor encoding and kernel launches.
+// choice, TMA descriptor encoding and the entry points. The kernels' launchers live in the
+// launch_*.cu translation units.
 //
 // The host-side checks mirror what the generated host function of tilelang (velog) section 1.2
 // (Host IRModule) asserts before launching: 2-D operands of the expected dtype and shape, unit
 // inner stride, non-null data, and row lengths divisible by 8 elements (16 bytes). Tensor maps are
 // encoded per call, as the generated call() of section 1.3 does with cuTensorMapEncodeTiled
 // (there: fp16, rank 2, a 128-byte inner box, L2 promotion, zero fill out of bounds), and passed
-// to the kernel as __grid_constant__ parameters.
-#include <cuda.h>
-#include <cuda_runtime.h>
-#include <cudaTypedefs.h>
-
+// to the kernel as __grid_constant__ parameters. That call() returns an int status and keeps the
+// message of its last CUDA error in a static buffer; gemm_last_error / gemm_stream_status follow
+// the same convention (a per-thread buffer here).
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
-#include <mutex>
-#include <unordered_set>
 
-#include "dtc_gemm.h"
-#include "gemm16_1cta.cuh"
-#include "gemm16_2cta.cuh"
 #include "gemm16_splitk.cuh"
-#include "gemm_mxfp8.cuh"
-#include "gemm_mxfp8_2cta.cuh"
+#include "host.h"
+
+namespace dtc_host {
 
 namespace {
-
-using dtc::Gemm16Args;
-
 thread_local char g_err[1024];
+}
 
 int fail(int code, const char* fmt, ...) {
     va_list ap;
@@ -43,22 +36,29 @@ int cuda_fail(cudaError_t e, const char* what) {
     return fail(GEMM_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
-constexpr uint64_t kDefaultTimeoutNs = 2ull * 1000 * 1000 * 1000;
-constexpr int kMaxDevices = 64;
-
-struct DeviceInfo {
-    bool probed = false;
-    bool supported = false;
-    int sms = 0;
-    int major = 0, minor = 0;
-    std::unordered_set<const void*> smem_attr_set;  // kernels whose smem limit was raised
-    int clusters_for[5] = {0, 0, 0, 0, 0};         // co-resident clusters of 1, 2, 4 CTAs
-    void* static_ws = nullptr;                      // address of g_static_ws on this device
-};
-DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
-// Looks up (once per device) the SM count and compute capability of the current device.
+}  // namespace dtc_host
+
+namespace {
+
+using namespace dtc_host;
+
+// First device-side wait that gave up (0 = none); each kernel receives its address.
+__device__ int g_dtc_status;
+
+// Scratch of gemm_ex_static_workspace: the stream-K workspace (flags, then the pieces' partial
+// sums) in module memory, zero at load, so that entry point allocates nothing. 20 MiB holds the
+// stream-K workspace of up to 79 CTA pairs (158 SMs) with 256-wide tiles: 1 KB of flags + 79 x 2 x
+// 128 x 256 fp32.
+constexpr uint64_t kStaticWsBytes = 20ull << 20;
+static __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+
+// Looks up (once per device) the compute capability, the SM count and the status word's address
+// on the current device.
 int current_device(int* dev_out, DeviceInfo** info_out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -69,9 +69,15 @@ int current_device(int* dev_out, DeviceInfo** info_out) {
     if (!d.probed) {
         if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
             (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
-            (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            (e = cudaDeviceGetAttribute(&d.model.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
             return cuda_fail(e, "cudaDeviceGetAttribute");
         d.supported = (d.major == 10 && d.minor == 3);
+        if (d.supported) {
+            void* p = nullptr;
+            if ((e = cudaGetSymbolAddress(&p, g_dtc_status)) != cudaSuccess)
+                return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+            d.status = static_cast<int*>(p);
+        }
         d.probed = true;
     }
     if (!d.supported)
@@ -80,6 +86,27 @@ int current_device(int* dev_out, DeviceInfo** info_out) {
     *dev_out = dev;
     *info_out = &d;
     return GEMM_OK;
+}
+
+// The device model of the planner: resident clusters are asked once per device, on first use.
+const DevModel& device_model(DeviceInfo* d) {
+    bool need;
+    {
+        std::lock_guard<std::mutex> lk(g_dev_mu);
+        need = !d->clusters_probed;
+    }
+    if (need) {
+        // (the queries take the lock themselves to raise the kernels' shared-memory limits)
+        const int pairs = query_pair_clusters(d);
+        const int c2 = query_splitk_clusters(2, d);
+        const int c4 = query_splitk_clusters(4, d);
+        std::lock_guard<std::mutex> lk(g_dev_mu);
+        d->model.pairs = pairs;
+        d->model.clusters2 = c2;
+        d->model.clusters4 = c4;
+        d->clusters_probed = true;
+    }
+    return d->model;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -95,6 +122,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     });
     return fn;
 }
+
+}  // namespace
+
+namespace dtc_host {
 
 // Row-major 2-D tensor [outer, inner] with rows `ld` elements apart; box [box_outer, box_inner];
 // with a swizzle the box's inner extent is the swizzle width (128 or 64 bytes); out-of-bounds
@@ -137,25 +168,9 @@ int make_tmap_kchunks(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, co
     return GEMM_OK;
 }
 
-// Where the operands live, after the defaults are applied: storage order and row pitch.
-struct Operands {
-    const void* A;
-    const void* B;
-    const void* sfA;
-    const void* sfB;
-    void* C;
-    int64_t lda, ldb, ldc;  // elements between consecutive stored rows
-    bool a_mn;              // A stored [K,M] (layouts TN, TT); else [M,K]
-    bool b_mn;              // B stored [K,N] (layouts NN, TN); else [N,K]
-};
-
-bool layout_a_mn(int layout) { return layout == GEMM_LAYOUT_TN || layout == GEMM_LAYOUT_TT; }
-bool layout_b_mn(int layout) { return layout == GEMM_LAYOUT_NN || layout == GEMM_LAYOUT_TN; }
-
 // Tensor map of a 16-bit operand with `mn` elements along M (or N) and K along the reduction:
 // MN-major storage [K, mn] -> 2-D boxes {64, kBK} (128-byte swizzle); K-major storage [mn, K] ->
-// one 3-D box {64, box_rows, 2} per 128-deep stage, or a 2-D box {kBK, box_rows} with the
-// swizzle as wide as a kBK-element row.
+// one 3-D box {64, box_rows, 2} per 128-deep stage, or a 2-D box {64, box_rows} per 64-deep one.
 int tmap_operand16(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, int64_t ld, bool mn_major,
                    int64_t mn, int64_t K, int kBK, uint32_t box_rows, const char* name) {
     if (mn_major)
@@ -163,17 +178,77 @@ int tmap_operand16(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, int6
                          CU_TENSOR_MAP_SWIZZLE_128B, name);
     if (kBK == 128)
         return make_tmap_kchunks(m, dt, 2, ptr, (uint64_t)K, (uint64_t)mn, (uint64_t)ld, box_rows, name);
-    return make_tmap(m, dt, 2, ptr, (uint64_t)K, (uint64_t)mn, (uint64_t)ld, (uint32_t)kBK, box_rows,
-                     kBK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, name);
+    return make_tmap(m, dt, 2, ptr, (uint64_t)K, (uint64_t)mn, (uint64_t)ld, 64, box_rows,
+                     CU_TENSOR_MAP_SWIZZLE_128B, name);
 }
+
+// Tensor maps of a 16-bit C [M, N] (rows ldc elements apart) for the TMA-store epilogues: boxes
+// of 32 rows x 64 columns with the 128-byte swizzle, and of 32 rows x 32 columns with the 64-byte
+// swizzle (the last chunk of a 224-wide tile).
+int tmap_c16(CUtensorMap* c64, CUtensorMap* c32, CUtensorMapDataType dt, const Operands& ops,
+             int64_t M, int64_t N) {
+    int rc = make_tmap(c64, dt, 2, ops.C, (uint64_t)N, (uint64_t)M, (uint64_t)ops.ldc, 64, 32,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "C");
+    if (rc) return rc;
+    return make_tmap(c32, dt, 2, ops.C, (uint64_t)N, (uint64_t)M, (uint64_t)ops.ldc, 32, 32,
+                     CU_TENSOR_MAP_SWIZZLE_64B, "C");
+}
+
+dtc::Gemm16Args make_args(const Launch& L, int tile_m, int tile_n, int tile_k) {
+    const gemm_options* o = L.o;
+    const int sk = L.p->sk_tiles;
+    dtc::Gemm16Args a;
+    a.sk_tiles = sk;
+    a.sk_flags = sk ? static_cast<uint32_t*>(o->workspace) : nullptr;
+    a.sk_partial = sk ? reinterpret_cast<float*>(static_cast<char*>(o->workspace) + kSkFlagBytes)
+                      : nullptr;
+    a.C = L.ops->C;
+    a.ldc = L.ops->ldc;
+    a.M = L.M;
+    a.N = L.N;
+    a.K = L.K;
+    a.num_m = ceil_div(L.M, tile_m);
+    a.num_n = ceil_div(L.N, tile_n);
+    a.num_kb = ceil_div(L.K, tile_k);
+    a.timeout_ns = (o && o->timeout_ns) ? o->timeout_ns : kDefaultTimeoutNs;
+    a.fault = o ? o->fault_inject : 0;
+    a.status = L.dev->status;
+    return a;
+}
+
+dtc::GemmMxArgs mx_args(const Launch& L, int tile_m, int tile_n, int tile_k) {
+    const gemm_options* o = L.o;
+    dtc::GemmMxArgs a;
+    a.C = L.ops->C;
+    a.ldc = L.ops->ldc;
+    a.sfA = static_cast<const uint8_t*>(L.ops->sfA);
+    a.sfB = static_cast<const uint8_t*>(L.ops->sfB);
+    a.M = L.M;
+    a.N = L.N;
+    a.K = L.K;
+    a.num_m = ceil_div(L.M, tile_m);
+    a.num_n = ceil_div(L.N, tile_n);
+    a.num_kb = ceil_div(L.K, tile_k);
+    const int block = (o && o->mx_scale_block) ? o->mx_scale_block : 128;
+    a.sf_cols = ceil_div(L.K, block);
+    a.fmt_bits = o ? ((uint32_t)o->mx_a_format << 7) | ((uint32_t)o->mx_b_format << 10) : 0u;
+    a.timeout_ns = (o && o->timeout_ns) ? o->timeout_ns : kDefaultTimeoutNs;
+    a.fault = o ? o->fault_inject : 0;
+    a.status = L.dev->status;
+    return a;
+}
+
+}  // namespace dtc_host
+
+namespace {
+
+bool layout_a_mn(int layout) { return layout == GEMM_LAYOUT_TN || layout == GEMM_LAYOUT_TT; }
+bool layout_b_mn(int layout) { return layout == GEMM_LAYOUT_NN || layout == GEMM_LAYOUT_TN; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Shared argument rules of every entry point; on success fills `ops` (defaults applied).
-// Returns GEMM_OK or an error (message set).
-int validate(int dtype, const void* A, const void* B, const void* sfA, const void* sfB,
-             void* C, int64_t M, int64_t N, int64_t K, int layout, const gemm_options* o,
-             Operands* ops) {
+// Argument rules that need no CUDA call (every entry point, and the planner).
+int check_shape(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm_options* o) {
     const int64_t kMax = 2147483647;
     if (dtype < 0 || dtype > 2) return fail(GEMM_ERR_INVALID_ARG, "dtype %d is not 0, 1 or 2", dtype);
     if (layout < GEMM_LAYOUT_NT || layout > GEMM_LAYOUT_TT)
@@ -187,8 +262,6 @@ int validate(int dtype, const void* A, const void* B, const void* sfA, const voi
         return fail(GEMM_ERR_INVALID_ARG, "unknown variant %d", o->variant);
     if (o && o->split_k < 0) return fail(GEMM_ERR_INVALID_ARG, "split_k must be >= 0");
     if (o && o->tile_n < 0) return fail(GEMM_ERR_INVALID_ARG, "tile_n must be >= 0");
-    if (o && (o->lda < 0 || o->ldb < 0 || o->ldc < 0))
-        return fail(GEMM_ERR_INVALID_ARG, "lda, ldb and ldc must be >= 0");
     if (o && (o->mx_a_format < 0 || o->mx_a_format > 1 || o->mx_b_format < 0 || o->mx_b_format > 1))
         return fail(GEMM_ERR_INVALID_ARG, "mx formats must be 0 (e4m3) or 1 (e5m2)");
     if (o && o->mx_scale_block != 0 && o->mx_scale_block != 32 && o->mx_scale_block != 128)
@@ -197,6 +270,19 @@ int validate(int dtype, const void* A, const void* B, const void* sfA, const voi
         return fail(GEMM_ERR_INVALID_ARG, "the mx options apply to the block-scaled product only");
     if (o && (o->stream_k < 0 || o->stream_k > 2))
         return fail(GEMM_ERR_INVALID_ARG, "stream_k %d is not 0 (auto), 1 (required) or 2 (off)", o->stream_k);
+    return GEMM_OK;
+}
+
+// Shared argument rules of every entry point; on success fills `ops` (defaults applied).
+// Returns GEMM_OK or an error (message set). Makes no CUDA call.
+int validate(int dtype, const void* A, const void* B, const void* sfA, const void* sfB,
+             void* C, int64_t M, int64_t N, int64_t K, int layout, const gemm_options* o,
+             Operands* ops) {
+    const int64_t kMax = 2147483647;
+    int rc = check_shape(dtype, M, N, K, layout, o);
+    if (rc) return rc;
+    if (o && (o->lda < 0 || o->ldb < 0 || o->ldc < 0))
+        return fail(GEMM_ERR_INVALID_ARG, "lda, ldb and ldc must be >= 0");
     if (o && o->workspace && !aligned16(o->workspace))
         return fail(GEMM_ERR_INVALID_ARG, "the workspace is not 16-byte aligned");
     const int eb = dtype == 2 ? 1 : 2;  // operand element bytes
@@ -235,71 +321,28 @@ int validate(int dtype, const void* A, const void* B, const void* sfA, const voi
     return GEMM_OK;
 }
 
-struct Plan {
-    int variant = 0, tile_m = 0, tile_n = 0, tile_k = 64, stages = 0, split_k = 1, ctas = 0,
-        tiles = 0, cluster = 1, sk_tiles = 0;
-};
-
-// Stream-K workspace of the pair kernel for `units` pairs and tile width bn: the flags (one
-// 32-bit word per CTA, padded to 1 KB), then one 128 x bn fp32 slot per CTA.
-constexpr uint64_t kSkFlagBytes = 1024;
-uint64_t sk_workspace_bytes(int units, int bn) {
-    return kSkFlagBytes + (uint64_t)units * 2 * 128 * (uint64_t)bn * 4;
-}
-
-int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
-
-template <typename Kern>
-int ensure_smem_attr(Kern kern, int bytes, DeviceInfo* dev) {
-    const void* key = reinterpret_cast<const void*>(kern);
-    std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (!dev->smem_attr_set.count(key)) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-        dev->smem_attr_set.insert(key);
+// The kernels read and write through tensor maps of the current device: every buffer must be
+// device memory of that device (or managed memory). A pointer into another GPU's memory, or into
+// host memory, is refused here rather than read over a link.
+int check_device_ptr(const void* p, int dev, const char* name) {
+    cudaPointerAttributes a;
+    cudaError_t e = cudaPointerGetAttributes(&a, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(GEMM_ERR_INVALID_ARG, "%s (%p) is not memory CUDA knows: %s", name, p,
+                    cudaGetErrorName(e));
     }
-    return GEMM_OK;
-}
-
-// Ring depth of the pair kernel: 6 stages of 64-deep K-blocks, or 3 of 128-deep ones.
-constexpr int pair_stages(int bn, int bk) { return bk == 128 ? 3 : 6 + 0 * bn; }
-
-// Ring depth of the one-CTA kernel for each (tile width, K-block): as many stages as fit beside
-// the 32 KB of output staging (at most 225 KB in all).
-constexpr int stages_for(int bn, int bk) { return bk == 64 ? 4 + 0 * bn : 8; }
-
-// How many clusters of `cm` one-CTA GEMM CTAs (about 200 KB of shared memory each, so one per
-// SM) the device keeps resident at once. Asked once per device and cluster size.
-int resident_clusters(int cm, DeviceInfo* dev) {
-    if (dev->clusters_for[cm]) return dev->clusters_for[cm];
-    int n = dev->sms / cm;
-    if (cm > 1) {
-        auto kern = dtc::gemm16_1cta_kernel<true, false, false, 256, 64, 4, 2>;
-        using Cfg = dtc::g16::Cfg<256, 64, 4>;
-        if (ensure_smem_attr(kern, Cfg::kSmemBytes, dev) == GEMM_OK) {
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(cm * n, 1, 1);
-            cfg.blockDim = dim3(dtc::g16::kThreads, 1, 1);
-            cfg.dynamicSmemBytes = Cfg::kSmemBytes;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = cm;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            int q = 0;
-            if (cudaOccupancyMaxActiveClusters(&q, kern, &cfg) == cudaSuccess && q > 0) n = q;
-            else cudaGetLastError();
-        }
-    }
-    dev->clusters_for[cm] = std::max(1, n);
-    return dev->clusters_for[cm];
+    if (a.type == cudaMemoryTypeManaged || (a.type == cudaMemoryTypeDevice && a.device == dev))
+        return GEMM_OK;
+    if (a.type == cudaMemoryTypeDevice)
+        return fail(GEMM_ERR_INVALID_ARG, "%s is memory of device %d, not of the current device %d",
+                    name, a.device, dev);
+    return fail(GEMM_ERR_INVALID_ARG, "%s is not device memory (memory type %d)", name, (int)a.type);
 }
 
 // Busy time of the slowest cluster, in tile-width units, when every tile costs time proportional
-// to its width: (waves of tiles over the resident clusters) x (tile width).
-int64_t wave_cost(int64_t tiles, int clusters, int bn) { return (int64_t)ceil_div(tiles, clusters) * bn; }
+// to its width: (waves of tiles over the resident units) x (tile width).
+int64_t wave_cost(int64_t tiles, int units, int bn) { return (int64_t)ceil_div(tiles, units) * bn; }
 
 // Sustained fraction of tensor peak that one busy unit (an SM running 128 x BN tiles, or a CTA
 // pair running 256 x BN tiles) reaches in the main loop, measured on GB300 with bf16 NT operands
@@ -320,10 +363,17 @@ constexpr TileChoice kChoices[] = {
     {GEMM_VARIANT_2CTA, 224, 64, 0.56},
 };
 
+// Pairs a persistent pair-kernel launch may count on: half the SMs, or fewer when fewer pairs can
+// be resident at once.
+int resident_pairs(const DevModel& d) {
+    const int half = std::max(1, d.sms / 2);
+    return d.pairs > 0 ? std::min(half, d.pairs) : half;
+}
+
 // Busy time of the slowest SM, in units of (128 x 1 x K) MMA work at full rate: waves of tiles
 // over the resident units x per-SM tile width / efficiency.
-double plan_cost(int variant, int bn, double eff, int64_t M, int64_t N, int sms) {
-    const int units = variant == GEMM_VARIANT_2CTA ? std::max(1, sms / 2) : sms;
+double plan_cost(int variant, int bn, double eff, int64_t M, int64_t N, const DevModel& d) {
+    const int units = variant == GEMM_VARIANT_2CTA ? resident_pairs(d) : std::max(1, d.sms);
     const int64_t rows = variant == GEMM_VARIANT_2CTA ? ceil_div(M, 256) : ceil_div(M, 128);
     const int64_t tiles = rows * ceil_div(N, bn);
     return (double)ceil_div(tiles, units) * bn / eff;
@@ -336,31 +386,32 @@ double choice_efficiency(int variant, int bn, int bk) {
 }
 
 // Stream-K on CTA pairs (256 x 256 tiles, 128-deep stages; 64-deep on request): when the tiles
-// leave the last wave part-empty,
-// the leftover tiles are shared out over all pairs as equal runs of K-blocks, their pieces summed
-// through the caller's workspace. Taken when a large enough workspace is given, the request
-// allows the pair kernel with these tiles, and the cost model beats the plan already made: work
-// per pair / efficiency, plus 0.4 of a tile's time for the pieces' exchange and the shorter runs
-// (measured on GB300: +2-4 % on 8192^3; on 4096^2 x 8192 within 1 % of 224-wide whole tiles, on
-// average slightly ahead, which this constant encodes). Sharing a whole wave more (longer runs,
-// fewer splits) measured worse on both.
-// Required or refused with opts->stream_k.
-int plan_stream_k(int64_t M, int64_t N, int64_t K, const gemm_options* o, DeviceInfo* d, Plan* p) {
+// leave the last wave part-empty, the leftover tiles are shared out over all pairs as equal runs of
+// K-blocks, their pieces summed through the caller's workspace. A pair waits for the pieces of
+// later pairs, so every pair of the launch must be resident at once: the units are the pairs the
+// device keeps resident (at most 128, the flags' capacity). Taken when a large enough workspace is
+// given, the request allows the pair kernel with these tiles, and the cost model beats the plan
+// already made: work per pair / efficiency, plus 0.4 of a tile's time for the pieces' exchange and
+// the shorter runs (measured on GB300: +2-4 % on 8192^3; on 4096^2 x 8192 within 1 % of 224-wide
+// whole tiles, on average slightly ahead, which this constant encodes). Sharing a whole wave more
+// (longer runs, fewer splits) measured worse on both. Required or refused with opts->stream_k.
+int plan_stream_k(int64_t M, int64_t N, int64_t K, const gemm_options* o, const DevModel& d, Plan* p) {
     const int mode = o ? o->stream_k : 0;
     if (mode == 2) return GEMM_OK;
-    const int units = std::max(1, d->sms / 2);
+    const int units = resident_pairs(d);
     const int64_t tiles = (int64_t)ceil_div(M, 256) * ceil_div(N, 256);
     const int req_v = o ? o->variant : GEMM_VARIANT_AUTO;
     const bool allowed = (req_v == GEMM_VARIANT_AUTO || req_v == GEMM_VARIANT_2CTA) &&
                          (!o || o->tile_n == 0 || o->tile_n == 256) &&
                          (!o || o->tile_k == 0 || o->tile_k == 128 || o->tile_k == 64) &&
-                         (!o || o->split_k == 0) &&
+                         (!o || o->split_k == 0) && units <= kSkMaxUnits &&
                          K % 64 == 0 && p->variant != GEMM_VARIANT_SPLITK && tiles >= units &&
                          tiles % units != 0;
     const bool ws_ok = o && o->workspace && o->workspace_bytes >= sk_workspace_bytes(units, 256);
     if (mode == 1 && !allowed)
         return fail(GEMM_ERR_UNSUPPORTED, "stream-K needs the pair kernel with 256 x 256 tiles, "
-                    "K %% 64 == 0 and a tile count that is not a whole number of waves");
+                    "K %% 64 == 0, at most %d resident pairs and a tile count that is not a whole "
+                    "number of waves of the %d resident pairs", kSkMaxUnits, units);
     if (mode == 1 && !ws_ok)
         return fail(GEMM_ERR_INVALID_ARG, "stream-K needs a workspace of %llu bytes",
                     (unsigned long long)sk_workspace_bytes(units, 256));
@@ -368,14 +419,14 @@ int plan_stream_k(int64_t M, int64_t N, int64_t K, const gemm_options* o, Device
     const double eff = choice_efficiency(GEMM_VARIANT_2CTA, 256, 128);
     const double sk_cost = ((double)tiles / units + 0.4) * 256 / eff;
     const double dp_cost = plan_cost(p->variant, p->tile_n,
-                                     choice_efficiency(p->variant, p->tile_n, p->tile_k), M, N, d->sms);
+                                     choice_efficiency(p->variant, p->tile_n, p->tile_k), M, N, d);
     if (mode == 0 && sk_cost >= dp_cost) return GEMM_OK;
     p->variant = GEMM_VARIANT_2CTA;
     p->cluster = 2;
     p->tile_m = 256;
     p->tile_n = 256;
     p->tile_k = (o && o->tile_k == 64) ? 64 : 128;
-    p->stages = pair_stages(256, p->tile_k);
+    p->stages = p->tile_k == 128 ? 3 : 6;
     p->split_k = 1;
     p->tiles = (int)tiles;
     p->sk_tiles = (int)(tiles % units);
@@ -383,11 +434,15 @@ int plan_stream_k(int64_t M, int64_t N, int64_t K, const gemm_options* o, Device
     return GEMM_OK;
 }
 
+// The launch for these sizes and options on a device described by `d`: a pure function (no CUDA
+// call), so it can be asked for any device model.
 int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm_options* o,
-              DeviceInfo* d, Plan* p) {
+              const DevModel& d, Plan* p) {
     int v = o ? o->variant : GEMM_VARIANT_AUTO;
     const int want_n = o ? o->tile_n : 0;
     const bool b_mn = layout_b_mn(layout);  // B stored [K,N]: 64-column boxes
+    const int sms = std::max(1, d.sms);
+    const int pairs = resident_pairs(d);
     if (want_n && want_n != 256 && want_n != 128 && want_n != 224)
         return fail(GEMM_ERR_UNSUPPORTED, "tile width %d is not offered", want_n);
     if (want_n == 224 && b_mn && v == GEMM_VARIANT_1CTA)
@@ -403,7 +458,6 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
                                        (o->mx_scale_block == 0 || o->mx_scale_block == 128));
         if (v == GEMM_VARIANT_2CTA && !mx_default)
             return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 pair kernel takes e4m3 with 128-element scale blocks only");
-        const int64_t pair_tiles = (int64_t)ceil_div(M, 256) * ceil_div(N, dtc::gmx2::kBN);
         // The pair kernel is correct but measured slower than the one-CTA kernel on GB300
         // (2008 vs 2357 TFLOP/s on 4096 x 4096 x 8192): it is an option, never chosen here.
         if (v == GEMM_VARIANT_AUTO) v = GEMM_VARIANT_1CTA;
@@ -411,11 +465,11 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
             p->variant = v;
             p->cluster = 2;
             p->tile_m = 256;
-            p->tile_n = dtc::gmx2::kBN;
-            p->tile_k = dtc::gmx2::kBK;
-            p->stages = dtc::gmx2::kStages;
-            p->tiles = (int)pair_tiles;
-            p->ctas = 2 * std::min(p->tiles, std::max(1, d->sms / 2));
+            p->tile_n = 224;
+            p->tile_k = 256;
+            p->stages = 3;
+            p->tiles = ceil_div(M, 256) * ceil_div(N, 224);
+            p->ctas = 2 * std::min(p->tiles, pairs);
             return GEMM_OK;
         }
         p->variant = GEMM_VARIANT_1CTA;
@@ -431,7 +485,7 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
         p->tile_k = deep ? 2 * dtc::gmx::kBK : dtc::gmx::kBK;
         p->stages = deep ? dtc::gmx::Cfg<true>::kStages : dtc::gmx::Cfg<false>::kStages;
         p->tiles = ceil_div(M, p->tile_m) * ceil_div(N, p->tile_n);
-        p->ctas = std::min(p->tiles, d->sms);
+        p->ctas = std::min(p->tiles, sms);
         return GEMM_OK;
     }
     const int num_kb = ceil_div(K, 64);
@@ -441,8 +495,7 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
     if (split != 0 && split != 2 && split != 4)
         return fail(GEMM_ERR_INVALID_ARG, "split_k %d is not 2 or 4", split);
     int split_n = want_n;
-    if (v == GEMM_VARIANT_AUTO && dtype != 2 && split == 0 && want_n != 224 &&
-        tiles256 * 2 <= d->sms) {
+    if (v == GEMM_VARIANT_AUTO && split == 0 && want_n != 224 && tiles256 * 2 <= sms) {
         // Fewer 128 x 256 tiles than half the SMs: split K over a cluster of 2 or 4 CTAs per
         // 128 x 128 or 128 x 256 tile. Take the (width, split) that occupies the most SMs in one
         // wave, each CTA keeping at least 8 K-blocks of 64 (with less, the on-chip exchange of
@@ -456,7 +509,9 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
             if (want_n && c.bn != want_n) continue;
             const int64_t tl = c.bn == 128 ? tiles128 : tiles256;
             const int64_t ctas = tl * c.s;
-            if (num_kb < 8 * c.s || ctas > (int64_t)resident_clusters(c.s, d) * c.s) continue;
+            const int resident = c.s == 2 ? (d.clusters2 > 0 ? d.clusters2 : sms / 2)
+                                          : (d.clusters4 > 0 ? d.clusters4 : sms / 4);
+            if (num_kb < 8 * c.s || ctas > (int64_t)resident * c.s) continue;
             if (ctas > best_ctas || (ctas == best_ctas && c.s < split)) {
                 best_ctas = ctas;
                 split = c.s;
@@ -466,7 +521,6 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
         if (split) v = GEMM_VARIANT_SPLITK;
     }
     if (v == GEMM_VARIANT_SPLITK) {
-        if (dtype == 2) return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 product has no split-K kernel");
         if (split_n && split_n != 256 && split_n != 128)
             return fail(GEMM_ERR_UNSUPPORTED, "the split-K kernel uses 128- or 256-wide tiles");
         if (split_n == 256 && split == 4)
@@ -501,8 +555,8 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
             if (c.tile_n == 224 && b_mn && c.variant == GEMM_VARIANT_1CTA) continue;
             if (want_n && c.tile_n != want_n) continue;
             if (c.variant == GEMM_VARIANT_2CTA && (c.tile_k == 128) != (K % 64 == 0)) continue;
-            double cost = plan_cost(c.variant, c.tile_n, c.efficiency, M, N, d->sms);
-            if (c.variant == GEMM_VARIANT_2CTA && ceil_div(M, 256) * ceil_div(N, c.tile_n) < d->sms / 2)
+            double cost = plan_cost(c.variant, c.tile_n, c.efficiency, M, N, d);
+            if (c.variant == GEMM_VARIANT_2CTA && ceil_div(M, 256) * ceil_div(N, c.tile_n) < pairs)
                 cost *= 1.25;
             if (best < 0 || cost < best) {
                 best = cost;
@@ -515,36 +569,27 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
     }
     p->variant = v;
     if (v == GEMM_VARIANT_1CTA) {
-        const int num_m = ceil_div(M, 128);
-        int cm = o ? o->cluster_m : 0;
-        if (cm != 0 && cm != 1 && cm != 2)
-            return fail(GEMM_ERR_INVALID_ARG, "cluster_m %d is not 1 or 2", cm);
-        if (cm == 0) cm = 1;
-        int bk = o ? o->tile_k : 0;
-        if (bk != 0 && bk != 32 && bk != 64)
-            return fail(GEMM_ERR_INVALID_ARG, "tile_k %d is not 32 or 64", bk);
-        if (bk == 0) bk = 64;
-        const int clusters = resident_clusters(cm, d);
-        const int64_t cluster_rows = ceil_div(num_m, cm);
+        const int bk = o ? o->tile_k : 0;
+        if (bk != 0 && bk != 64)
+            return fail(GEMM_ERR_INVALID_ARG, "tile_k %d is not 64 for the one-CTA kernel", bk);
         int best = auto_n ? auto_n : 256;
         if (want_n == 224 && b_mn)
             return fail(GEMM_ERR_UNSUPPORTED, "224-wide one-CTA tiles need B stored [N,K]");
+        const int64_t rows = ceil_div(M, 128);
         if (want_n) {
             best = want_n;
         } else if (!auto_n && !b_mn) {
-            if (wave_cost(cluster_rows * ceil_div(N, 224), clusters, 224) <
-                wave_cost(cluster_rows * ceil_div(N, 256), clusters, 256))
+            if (wave_cost(rows * ceil_div(N, 224), sms, 224) < wave_cost(rows * ceil_div(N, 256), sms, 256))
                 best = 224;
         }
-        p->cluster = cm;
+        p->cluster = 1;
         p->tile_m = 128;
         p->tile_n = best;
-        p->tile_k = bk;
-        p->stages = stages_for(best, bk);
-        p->tiles = (int)cluster_rows * ceil_div(N, best);  // cluster tiles
-        p->ctas = cm * std::min(p->tiles, clusters);
+        p->tile_k = 64;
+        p->stages = 4;
+        p->tiles = (int)rows * ceil_div(N, best);
+        p->ctas = std::min(p->tiles, sms);
     } else {
-        const int pairs = std::max(1, d->sms / 2);
         p->cluster = 2;
         p->tile_m = 256;
         if (want_n) {
@@ -565,310 +610,89 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
             return fail(GEMM_ERR_UNSUPPORTED, "128-deep pair stages need K %% 64 == 0");
         if (bk == 0) bk = K % 64 == 0 ? 128 : 64;
         p->tile_k = bk;
-        p->stages = pair_stages(p->tile_n, bk);
+        p->stages = bk == 128 ? 3 : 6;
         p->tiles = ceil_div(M, 256) * ceil_div(N, p->tile_n);
         p->ctas = 2 * std::min(p->tiles, pairs);
     }
     return plan_stream_k(M, N, K, o, d, p);
 }
 
-Gemm16Args make_args(const Operands& ops, int M, int N, int K, int tile_m, int tile_n, int tile_k,
-                     const gemm_options* o, int sk_tiles = 0) {
-    Gemm16Args a;
-    a.sk_tiles = sk_tiles;
-    a.sk_flags = sk_tiles ? static_cast<uint32_t*>(o->workspace) : nullptr;
-    a.sk_partial = sk_tiles ? reinterpret_cast<float*>(static_cast<char*>(o->workspace) + kSkFlagBytes)
-                            : nullptr;
-    a.C = ops.C;
-    a.ldc = ops.ldc;
-    a.M = M;
-    a.N = N;
-    a.K = K;
-    a.num_m = (M + tile_m - 1) / tile_m;
-    a.num_n = (N + tile_n - 1) / tile_n;
-    a.num_kb = (K + tile_k - 1) / tile_k;
-    a.timeout_ns = (o && o->timeout_ns) ? o->timeout_ns : kDefaultTimeoutNs;
-    a.fault = o ? o->fault_inject : 0;
-    return a;
-}
+// A call made ready to launch: checked arguments, the device and the plan.
+struct Prepared {
+    Operands ops;
+    Plan p;
+    int dev = -1;
+    DeviceInfo* info = nullptr;
+    bool noop = false;    // M == 0 or N == 0
+    bool zero_k = false;  // K == 0: C = 0
+};
 
-template <typename Kern, typename... Params>
-int launch_cluster(Kern kern, int grid, int threads, int smem, int cluster, cudaStream_t stream,
-                   const Params&... params) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3(threads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = cluster > 1 ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, params...);
-    if (e == cudaSuccess) e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+int prepare(int dtype, const void* A, const void* B, const void* sfA, const void* sfB, void* C,
+            int64_t M, int64_t N, int64_t K, int layout, const gemm_options* o, Prepared* r) {
+    int rc = validate(dtype, A, B, sfA, sfB, C, M, N, K, layout, o, &r->ops);
+    if (rc) return rc;
+    if (M == 0 || N == 0) {
+        r->noop = true;
+        return GEMM_OK;
+    }
+    if ((rc = current_device(&r->dev, &r->info))) return rc;
+    if ((rc = check_device_ptr(C, r->dev, "C"))) return rc;
+    if (K == 0) {
+        r->zero_k = true;
+        return GEMM_OK;
+    }
+    if ((rc = check_device_ptr(A, r->dev, "A")) || (rc = check_device_ptr(B, r->dev, "B"))) return rc;
+    if (dtype == 2 &&
+        ((rc = check_device_ptr(sfA, r->dev, "sfA")) || (rc = check_device_ptr(sfB, r->dev, "sfB"))))
+        return rc;
+    if ((rc = make_plan(dtype, M, N, K, layout, o, device_model(r->info), &r->p))) return rc;
+    if (r->p.sk_tiles && (rc = check_device_ptr(o->workspace, r->dev, "the workspace"))) return rc;
     return GEMM_OK;
 }
 
-// Tensor maps of a 16-bit C [M, N] (rows ldc elements apart) for the TMA-store epilogues: boxes
-// of 32 rows x 64 columns with the 128-byte swizzle, and of 32 rows x 32 columns with the 64-byte
-// swizzle (the last chunk of a 224-wide tile).
-int tmap_c16(CUtensorMap* c64, CUtensorMap* c32, CUtensorMapDataType dt, const Operands& ops,
-             int64_t M, int64_t N) {
-    int rc = make_tmap(c64, dt, 2, ops.C, (uint64_t)N, (uint64_t)M, (uint64_t)ops.ldc, 64, 32,
-                       CU_TENSOR_MAP_SWIZZLE_128B, "C");
-    if (rc) return rc;
-    return make_tmap(c32, dt, 2, ops.C, (uint64_t)N, (uint64_t)M, (uint64_t)ops.ldc, 32, 32,
-                     CU_TENSOR_MAP_SWIZZLE_64B, "C");
-}
-
-template <bool kBF16, bool kAMN, bool kNN, int kBN, int kBK, int kStages, int kCM>
-int launch_gemm16_1cta(const Operands& ops, int M, int N, int K, const gemm_options* o,
-                       DeviceInfo* dev, const Plan& p, cudaStream_t stream) {
-    using namespace dtc::g16;
-    using Cfg = Cfg<kBN, kBK, kStages>;
-    const CUtensorMapDataType dt = kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    CUtensorMap tA, tB;
-    int rc = tmap_operand16(&tA, dt, ops.A, ops.lda, kAMN, M, K, kBK, kBM, "A");
-    if (rc) return rc;
-    if ((rc = tmap_operand16(&tB, dt, ops.B, ops.ldb, kNN, N, K, kBK, kBN / kCM, "B"))) return rc;
-    CUtensorMap tC, tC32;
-    if ((rc = tmap_c16(&tC, &tC32, dt, ops, M, N))) return rc;
-    auto kern = dtc::gemm16_1cta_kernel<kBF16, kAMN, kNN, kBN, kBK, kStages, kCM>;
-    if ((rc = ensure_smem_attr(kern, Cfg::kSmemBytes, dev))) return rc;
-    const Gemm16Args args = make_args(ops, M, N, K, kBM, kBN, kBK, o);
-    return launch_cluster(kern, p.ctas, kThreads, Cfg::kSmemBytes, kCM, stream, tA, tB, tC, tC32,
-                          args);
-}
-
-template <bool kBF16, bool kAMN, bool kNN, int kBN, int kBK, bool kSK = false>
-int launch_gemm16_2cta(const Operands& ops, int M, int N, int K, const gemm_options* o,
-                       DeviceInfo* dev, const Plan& p, cudaStream_t stream) {
-    constexpr int kStages = pair_stages(kBN, kBK);
-    using Cfg = dtc::g2::Cfg<kBN, kBK, kStages, kNN>;
-    const CUtensorMapDataType dt = kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    CUtensorMap tA, tB;
-    int rc = tmap_operand16(&tA, dt, ops.A, ops.lda, kAMN, M, K, kBK, 128, "A");
-    if (rc) return rc;
-    if ((rc = tmap_operand16(&tB, dt, ops.B, ops.ldb, kNN, N, K, kBK, Cfg::kHalfN, "B"))) return rc;
-    CUtensorMap tC, tC32;
-    if ((rc = tmap_c16(&tC, &tC32, dt, ops, M, N))) return rc;
-    auto kern = dtc::gemm16_2cta_kernel<kBF16, kAMN, kNN, kBN, kBK, kStages, kSK>;
-    if ((rc = ensure_smem_attr(kern, Cfg::kSmemBytes, dev))) return rc;
-    const Gemm16Args args = make_args(ops, M, N, K, 256, kBN, kBK, o, p.sk_tiles);
-    return launch_cluster(kern, p.ctas, dtc::g2::kThreads, Cfg::kSmemBytes, 2, stream, tA, tB, tC,
-                          tC32, args);
-}
-
-template <bool kBF16, bool kAMN, bool kNN, int kBN, int kBK, int kStages>
-int launch_1cta_cm(const Plan& p, const Operands& ops, int m, int n, int k,
-                   const gemm_options* o, DeviceInfo* dev, cudaStream_t stream) {
-    if (p.cluster == 2)
-        return launch_gemm16_1cta<kBF16, kAMN, kNN, kBN, kBK, kStages, 2>(ops, m, n, k, o, dev, p, stream);
-    return launch_gemm16_1cta<kBF16, kAMN, kNN, kBN, kBK, kStages, 1>(ops, m, n, k, o, dev, p, stream);
-}
-
-
-
-template <bool kBF16, bool kAMN, bool kNN, int kBN, int kBK, int kS>
-int launch_gemm16_splitk(const Operands& ops, int M, int N, int K, const gemm_options* o,
-                         DeviceInfo* dev, const Plan& p, cudaStream_t stream) {
-    constexpr int kStages = dtc::gsk::stages_for(kBN, kBK, kS);
-    using Cfg = dtc::gsk::Cfg<kBN, kBK, kStages, kS>;
-    const CUtensorMapDataType dt = kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    CUtensorMap tA, tB;
-    int rc = tmap_operand16(&tA, dt, ops.A, ops.lda, kAMN, M, K, kBK, 128, "A");
-    if (rc) return rc;
-    if ((rc = tmap_operand16(&tB, dt, ops.B, ops.ldb, kNN, N, K, kBK, kBN, "B"))) return rc;
-    CUtensorMap tC, tC32;
-    if ((rc = tmap_c16(&tC, &tC32, dt, ops, M, N))) return rc;
-    auto kern = dtc::gemm16_splitk_kernel<kBF16, kAMN, kNN, kBN, kBK, kStages, kS>;
-    if ((rc = ensure_smem_attr(kern, Cfg::kSmemBytes, dev))) return rc;
-    const Gemm16Args args = make_args(ops, M, N, K, 128, kBN, kBK, o);
-    return launch_cluster(kern, p.ctas, dtc::gsk::kThreads, Cfg::kSmemBytes, kS, stream, tA, tB, tC,
-                          args);
-}
-
-template <bool kBF16, bool kAMN, bool kNN>
-int launch_splitk_any(const Plan& p, const Operands& ops, int m, int n, int k,
-                      const gemm_options* o, DeviceInfo* dev, cudaStream_t stream) {
-    if (p.tile_n == 128) {
-        if (p.tile_k == 128)
-            return p.split_k == 2 ? launch_gemm16_splitk<kBF16, kAMN, kNN, 128, 128, 2>(ops, m, n, k, o, dev, p, stream)
-                                  : launch_gemm16_splitk<kBF16, kAMN, kNN, 128, 128, 4>(ops, m, n, k, o, dev, p, stream);
-        return p.split_k == 2 ? launch_gemm16_splitk<kBF16, kAMN, kNN, 128, 64, 2>(ops, m, n, k, o, dev, p, stream)
-                              : launch_gemm16_splitk<kBF16, kAMN, kNN, 128, 64, 4>(ops, m, n, k, o, dev, p, stream);
+int launch_prepared(const Prepared& r, int dtype, int64_t M, int64_t N, int64_t K,
+                    const gemm_options* o, cudaStream_t stream) {
+    if (r.noop) return GEMM_OK;
+    if (r.zero_k) {  // the empty sum: C = 0 (only the M x N region of a strided C)
+        cudaError_t e = cudaMemset2DAsync(r.ops.C, (size_t)r.ops.ldc * 2, 0, (size_t)N * 2, (size_t)M, stream);
+        return e == cudaSuccess ? GEMM_OK : cuda_fail(e, "cudaMemset2DAsync");
     }
-    return launch_gemm16_splitk<kBF16, kAMN, kNN, 256, 64, 2>(ops, m, n, k, o, dev, p, stream);
-}
-
-dtc::GemmMxArgs mx_args(const Operands& ops, int M, int N, int K, int tile_m, int tile_n,
-                        int tile_k, const gemm_options* o) {
-    dtc::GemmMxArgs a;
-    a.C = ops.C;
-    a.ldc = ops.ldc;
-    a.sfA = static_cast<const uint8_t*>(ops.sfA);
-    a.sfB = static_cast<const uint8_t*>(ops.sfB);
-    a.M = M;
-    a.N = N;
-    a.K = K;
-    a.num_m = ceil_div(M, tile_m);
-    a.num_n = ceil_div(N, tile_n);
-    a.num_kb = ceil_div(K, tile_k);
-    const int block = (o && o->mx_scale_block) ? o->mx_scale_block : 128;
-    a.sf_cols = ceil_div(K, block);
-    a.fmt_bits = o ? ((uint32_t)o->mx_a_format << 7) | ((uint32_t)o->mx_b_format << 10) : 0u;
-    a.timeout_ns = (o && o->timeout_ns) ? o->timeout_ns : kDefaultTimeoutNs;
-    a.fault = o ? o->fault_inject : 0;
-    return a;
-}
-
-int launch_mxfp8_2cta(const Operands& ops, int M, int N, int K, const gemm_options* o,
-                      DeviceInfo* dev, const Plan& p, cudaStream_t stream) {
-    using namespace dtc::gmx2;
-    CUtensorMap tA, tB;
-    int rc = make_tmap_kchunks(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ops.A, (uint64_t)K,
-                               (uint64_t)M, (uint64_t)ops.lda, kBMc, "A");
-    if (rc) return rc;
-    rc = make_tmap_kchunks(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ops.B, (uint64_t)K, (uint64_t)N,
-                           (uint64_t)ops.ldb, kHalfN, "B");
-    if (rc) return rc;
-    CUtensorMap tC, tC32;
-    if ((rc = tmap_c16(&tC, &tC32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ops, M, N))) return rc;
-    auto kern = dtc::gemm_mxfp8_2cta_kernel<0>;
-    if ((rc = ensure_smem_attr(kern, kSmemBytes, dev))) return rc;
-    const dtc::GemmMxArgs a = mx_args(ops, M, N, K, 256, kBN, kBK, o);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.ctas, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tA, tB, tC, tC32, a);
-    if (e == cudaSuccess) e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "MXFP8 pair kernel launch");
-    return GEMM_OK;
-}
-
-template <bool kDeep, bool kB32>
-int launch_mxfp8_1cta(const Operands& ops, int M, int N, int K, const gemm_options* o,
-                      DeviceInfo* dev, const Plan& p, cudaStream_t stream) {
-    using namespace dtc::gmx;
-    using C_ = Cfg<kDeep>;
-    CUtensorMap tA, tB;
-    int rc;
-    if (kDeep) {  // one 3-D box {128, rows, 2} per operand and stage (K % 128 == 0)
-        if ((rc = make_tmap_kchunks(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ops.A, (uint64_t)K,
-                                    (uint64_t)M, (uint64_t)ops.lda, kBM, "A")))
-            return rc;
-        if ((rc = make_tmap_kchunks(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ops.B, (uint64_t)K,
-                                    (uint64_t)N, (uint64_t)ops.ldb, kBN, "B")))
-            return rc;
-    } else {
-        if ((rc = make_tmap(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ops.A, (uint64_t)K, (uint64_t)M,
-                            (uint64_t)ops.lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B, "A")))
-            return rc;
-        if ((rc = make_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ops.B, (uint64_t)K, (uint64_t)N,
-                            (uint64_t)ops.ldb, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B, "B")))
-            return rc;
-    }
-    CUtensorMap tC, tC32;
-    if ((rc = tmap_c16(&tC, &tC32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ops, M, N))) return rc;
-    auto kern = dtc::gemm_mxfp8_kernel<kDeep, kB32>;
-    if ((rc = ensure_smem_attr(kern, C_::kSmemBytes, dev))) return rc;
-    const dtc::GemmMxArgs a = mx_args(ops, M, N, K, kBM, kBN, kBK, o);
-    kern<<<p.ctas, kThreads, C_::kSmemBytes, stream>>>(tA, tB, tC, tC32, a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "MXFP8 kernel launch");
-    return GEMM_OK;
-}
-
-int launch_mxfp8(const Operands& ops, int M, int N, int K, const gemm_options* o, DeviceInfo* dev,
-                 const Plan& p, cudaStream_t stream) {
-    if (p.variant == GEMM_VARIANT_2CTA) return launch_mxfp8_2cta(ops, M, N, K, o, dev, p, stream);
-    const bool b32 = o && o->mx_scale_block == 32;
-    if (p.tile_k == 2 * dtc::gmx::kBK)
-        return b32 ? launch_mxfp8_1cta<true, true>(ops, M, N, K, o, dev, p, stream)
-                   : launch_mxfp8_1cta<true, false>(ops, M, N, K, o, dev, p, stream);
-    return b32 ? launch_mxfp8_1cta<false, true>(ops, M, N, K, o, dev, p, stream)
-               : launch_mxfp8_1cta<false, false>(ops, M, N, K, o, dev, p, stream);
-}
-
-template <bool kBF16, bool kAMN, bool kNN>
-int launch_pair_width(const Plan& p, const Operands& ops, int m, int n, int k,
-                      const gemm_options* o, DeviceInfo* dev, cudaStream_t stream) {
-    if (p.sk_tiles) {  // stream-K plans are 256 wide, 128- or 64-deep
-        if (p.tile_k == 64)
-            return launch_gemm16_2cta<kBF16, kAMN, kNN, 256, 64, true>(ops, m, n, k, o, dev, p, stream);
-        return launch_gemm16_2cta<kBF16, kAMN, kNN, 256, 128, true>(ops, m, n, k, o, dev, p, stream);
-    }
-    if (p.tile_k == 128) {
-        if (p.tile_n == 224)
-            return launch_gemm16_2cta<kBF16, kAMN, kNN, 224, 128>(ops, m, n, k, o, dev, p, stream);
-        return launch_gemm16_2cta<kBF16, kAMN, kNN, 256, 128>(ops, m, n, k, o, dev, p, stream);
-    }
-    if (p.tile_n == 224) return launch_gemm16_2cta<kBF16, kAMN, kNN, 224, 64>(ops, m, n, k, o, dev, p, stream);
-    return launch_gemm16_2cta<kBF16, kAMN, kNN, 256, 64>(ops, m, n, k, o, dev, p, stream);
-}
-
-template <bool kBF16, bool kAMN>
-int launch16(const Plan& p, const Operands& ops, int m, int n, int k, const gemm_options* o,
-             DeviceInfo* dev, cudaStream_t stream) {
-    const bool bmn = ops.b_mn;  // B stored [K,N]: MN-major B, 64-column boxes
-    if (p.variant == GEMM_VARIANT_SPLITK) {
-        if (bmn) return launch_splitk_any<kBF16, kAMN, true>(p, ops, m, n, k, o, dev, stream);
-        return launch_splitk_any<kBF16, kAMN, false>(p, ops, m, n, k, o, dev, stream);
-    }
-    if (p.variant == GEMM_VARIANT_1CTA) {
-        if (p.tile_k == 32) {
-            if (bmn)
-                return launch_1cta_cm<kBF16, kAMN, true, 256, 32, stages_for(256, 32)>(p, ops, m, n, k, o, dev, stream);
-            if (p.tile_n == 224)
-                return launch_1cta_cm<kBF16, kAMN, false, 224, 32, stages_for(224, 32)>(p, ops, m, n, k, o, dev, stream);
-            return launch_1cta_cm<kBF16, kAMN, false, 256, 32, stages_for(256, 32)>(p, ops, m, n, k, o, dev, stream);
-        }
-        if (bmn)
-            return launch_1cta_cm<kBF16, kAMN, true, 256, 64, stages_for(256, 64)>(p, ops, m, n, k, o, dev, stream);
-        if (p.tile_n == 224)
-            return launch_1cta_cm<kBF16, kAMN, false, 224, 64, stages_for(224, 64)>(p, ops, m, n, k, o, dev, stream);
-        return launch_1cta_cm<kBF16, kAMN, false, 256, 64, stages_for(256, 64)>(p, ops, m, n, k, o, dev, stream);
-    }
-    if (bmn) return launch_pair_width<kBF16, kAMN, true>(p, ops, m, n, k, o, dev, stream);
-    return launch_pair_width<kBF16, kAMN, false>(p, ops, m, n, k, o, dev, stream);
+    const Launch L{&r.ops, (int)M, (int)N, (int)K, o, r.info, &r.p, stream};
+    if (dtype == 2) return launch_mx(L);
+    if (r.p.variant == GEMM_VARIANT_SPLITK) return launch16_splitk(dtype == 0, L);
+    if (r.p.variant == GEMM_VARIANT_1CTA) return launch16_1cta(dtype == 0, L);
+    return dtype == 0 ? launch16_2cta_bf16(L) : launch16_2cta_f16(L);
 }
 
 int run(int dtype, const void* A, const void* B, const void* sfA, const void* sfB, void* C,
         int64_t M, int64_t N, int64_t K, int layout, const gemm_options* o, cudaStream_t stream) {
     g_err[0] = '\0';
-    Operands ops;
-    int rc = validate(dtype, A, B, sfA, sfB, C, M, N, K, layout, o, &ops);
+    Prepared r;
+    int rc = prepare(dtype, A, B, sfA, sfB, C, M, N, K, layout, o, &r);
     if (rc) return rc;
-    if (M == 0 || N == 0) return GEMM_OK;
-    int dev;
-    DeviceInfo* info;
-    if ((rc = current_device(&dev, &info))) return rc;
-    if (K == 0) {  // the empty sum: C = 0 (only the M x N region of a strided C)
-        cudaError_t e = cudaMemset2DAsync(C, (size_t)ops.ldc * 2, 0, (size_t)N * 2, (size_t)M, stream);
-        return e == cudaSuccess ? GEMM_OK : cuda_fail(e, "cudaMemset2DAsync");
-    }
-    Plan p;
-    if ((rc = make_plan(dtype, M, N, K, layout, o, info, &p))) return rc;
-    const int m = (int)M, n = (int)N, k = (int)K;
-    if (dtype == 2) return launch_mxfp8(ops, m, n, k, o, info, p, stream);
-    if (dtype == 0)
-        return ops.a_mn ? launch16<true, true>(p, ops, m, n, k, o, info, stream)
-                        : launch16<true, false>(p, ops, m, n, k, o, info, stream);
-    return ops.a_mn ? launch16<false, true>(p, ops, m, n, k, o, info, stream)
-                    : launch16<false, false>(p, ops, m, n, k, o, info, stream);
+    return launch_prepared(r, dtype, M, N, K, o, stream);
+}
+
+void fill_info(const Plan& p, gemm_plan_info* info) {
+    info->variant = p.variant;
+    info->tile_m = p.tile_m;
+    info->tile_n = p.tile_n;
+    info->tile_k = p.tile_k;
+    info->stages = p.stages;
+    info->split_k = p.split_k;
+    info->ctas = p.ctas;
+    info->tiles = p.tiles;
+    info->cluster = p.cluster;
+    info->sk_tiles = p.sk_tiles;
+}
+
+DevModel to_model(const gemm_device_model& m) {
+    DevModel d;
+    d.sms = m.sm_count;
+    d.pairs = m.pair_clusters;
+    d.clusters2 = m.split2_clusters;
+    d.clusters4 = m.split4_clusters;
+    return d;
 }
 
 }  // namespace
@@ -910,7 +734,7 @@ int gemm_ex_static_workspace(int dtype, const void* A, const void* B, const void
         std::lock_guard<std::mutex> lk(g_dev_mu);
         if (!info->static_ws) {  // once per device (a synchronous call: not inside stream capture)
             void* p = nullptr;
-            cudaError_t e = cudaGetSymbolAddress(&p, dtc::g_static_ws);
+            cudaError_t e = cudaGetSymbolAddress(&p, g_static_ws);
             if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static workspace)");
             info->static_ws = p;
         }
@@ -918,46 +742,61 @@ int gemm_ex_static_workspace(int dtype, const void* A, const void* B, const void
     gemm_options o = {};
     if (opts) o = *opts;
     o.workspace = info->static_ws;
-    o.workspace_bytes = dtc::kStaticWsBytes;
-    // the flags must be zero when a launch starts: every completed call leaves them zero, but a
-    // call that gave up (GEMM_ERR_TIMEOUT) may not, so clear them, in stream order, each time
-    if (dtype != 2) {
+    o.workspace_bytes = kStaticWsBytes;
+    Prepared r;
+    if ((rc = prepare(dtype, A, B, sfA, sfB, C, M, N, K, layout, &o, &r))) return rc;
+    if (r.p.sk_tiles) {
+        // the flags must be zero when a launch starts: every completed call leaves them zero, but
+        // a call that gave up (GEMM_ERR_TIMEOUT) may not, so clear them, in stream order, before
+        // each launch that uses them
         cudaError_t e = cudaMemsetAsync(info->static_ws, 0, kSkFlagBytes, (cudaStream_t)stream);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static workspace flags)");
     }
-    return run(dtype, A, B, sfA, sfB, C, M, N, K, layout, &o, (cudaStream_t)stream);
+    return launch_prepared(r, dtype, M, N, K, &o, (cudaStream_t)stream);
+}
+
+int gemm_device_model_query(gemm_device_model* out) {
+    g_err[0] = '\0';
+    if (!out) return fail(GEMM_ERR_INVALID_ARG, "out is NULL");
+    int dev;
+    DeviceInfo* d;
+    int rc = current_device(&dev, &d);
+    if (rc) return rc;
+    const DevModel& m = device_model(d);
+    out->sm_count = m.sms;
+    out->pair_clusters = m.pairs;
+    out->split2_clusters = m.clusters2;
+    out->split4_clusters = m.clusters4;
+    return GEMM_OK;
+}
+
+int gemm_plan_model(const gemm_device_model* model, int dtype, int64_t M, int64_t N, int64_t K,
+                    int layout, const gemm_options* opts, gemm_plan_info* info) {
+    g_err[0] = '\0';
+    if (!model || !info) return fail(GEMM_ERR_INVALID_ARG, "model or info is NULL");
+    if (model->sm_count < 1 || model->pair_clusters < 0 || model->split2_clusters < 0 ||
+        model->split4_clusters < 0)
+        return fail(GEMM_ERR_INVALID_ARG, "the device model needs sm_count >= 1 and cluster counts >= 0");
+    int rc = check_shape(dtype, M, N, K, layout, opts);
+    if (rc) return rc;
+    Plan p;
+    if ((rc = make_plan(dtype, M, N, K, layout, opts, to_model(*model), &p))) return rc;
+    fill_info(p, info);
+    return GEMM_OK;
 }
 
 int gemm_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm_options* opts,
               gemm_plan_info* info) {
     g_err[0] = '\0';
-    const int64_t kMax = 2147483647;
     if (!info) return fail(GEMM_ERR_INVALID_ARG, "info is NULL");
-    if (dtype < 0 || dtype > 2) return fail(GEMM_ERR_INVALID_ARG, "dtype %d is not 0, 1 or 2", dtype);
-    if (layout < GEMM_LAYOUT_NT || layout > GEMM_LAYOUT_TT)
-        return fail(GEMM_ERR_INVALID_ARG, "layout %d is not NT (0), NN (1), TN (2) or TT (3)", layout);
-    if (dtype == 2 && layout != GEMM_LAYOUT_NT)
-        return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 GEMM supports the NT layout only");
-    if (M < 0 || N < 0 || K < 0 || M > kMax || N > kMax || K > kMax)
-        return fail(GEMM_ERR_INVALID_ARG, "sizes must be in [0, 2^31-1]");
-    if (opts && (opts->variant < 0 || opts->variant > 3))
-        return fail(GEMM_ERR_INVALID_ARG, "unknown variant %d", opts->variant);
+    int rc = check_shape(dtype, M, N, K, layout, opts);
+    if (rc) return rc;
     int dev;
     DeviceInfo* d;
-    int rc = current_device(&dev, &d);
-    if (rc) return rc;
+    if ((rc = current_device(&dev, &d))) return rc;
     Plan p;
-    if ((rc = make_plan(dtype, M, N, K, layout, opts, d, &p))) return rc;
-    info->variant = p.variant;
-    info->tile_m = p.tile_m;
-    info->tile_n = p.tile_n;
-    info->tile_k = p.tile_k;
-    info->stages = p.stages;
-    info->split_k = p.split_k;
-    info->ctas = p.ctas;
-    info->tiles = p.tiles;
-    info->cluster = p.cluster;
-    info->sk_tiles = p.sk_tiles;
+    if ((rc = make_plan(dtype, M, N, K, layout, opts, device_model(d), &p))) return rc;
+    fill_info(p, info);
     return GEMM_OK;
 }
 
@@ -971,15 +810,15 @@ int gemm_workspace_size(int dtype, int64_t M, int64_t N, int64_t K, int layout,
     if (o.stream_k == 2 || dtype == 2) return GEMM_OK;
     o.workspace = reinterpret_cast<void*>(uintptr_t(256));  // stands for "large enough"
     o.workspace_bytes = ~0ull;
-    gemm_plan_info info;
-    int rc = gemm_plan(dtype, M, N, K, layout, &o, &info);
+    int rc = check_shape(dtype, M, N, K, layout, &o);
     if (rc) return rc;
-    if (info.sk_tiles) {
-        int dev;
-        DeviceInfo* d;
-        if ((rc = current_device(&dev, &d))) return rc;
-        *bytes = sk_workspace_bytes(std::max(1, d->sms / 2), 256);
-    }
+    int dev;
+    DeviceInfo* d;
+    if ((rc = current_device(&dev, &d))) return rc;
+    const DevModel& m = device_model(d);
+    Plan p;
+    if ((rc = make_plan(dtype, M, N, K, layout, &o, m, &p))) return rc;
+    if (p.sk_tiles) *bytes = sk_workspace_bytes(resident_pairs(m), 256);
     return GEMM_OK;
 }
 
@@ -990,10 +829,10 @@ int gemm_stream_status(dtc_stream_t stream) {
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     int status = 0, zero = 0;
-    e = cudaMemcpyFromSymbol(&status, dtc::g_dtc_status, sizeof(int));
+    e = cudaMemcpyFromSymbol(&status, g_dtc_status, sizeof(int));
     if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
     if (status == 0) return GEMM_OK;
-    e = cudaMemcpyToSymbol(dtc::g_dtc_status, &zero, sizeof(int));
+    e = cudaMemcpyToSymbol(g_dtc_status, &zero, sizeof(int));
     if (e != cudaSuccess) return cuda_fail(e, "clearing the device status word");
     return fail(GEMM_ERR_TIMEOUT, "a device-side wait gave up (status 0x%x, site %d)", status,
                 status & 0xff);

@@ -1,5 +1,4 @@
-// gemm16_1cta.cuh -- persistent, warp-specialised bf16/fp16 GEMM, one CTA per 128 x kBN tile,
-// optionally in clusters of kCM CTAs stacked along M that share the B tile by TMA multicast.
+// gemm16_1cta.cuh -- persistent, warp-specialised bf16/fp16 GEMM, one CTA per 128 x kBN tile.
 //
 // C[M,N] = A[M,K] . Bop, fp32 accumulation in Tensor Memory, bf16/fp16 output.
 // The tile (128 x 256, K-blocks of 64) follows the example shape of TileLang SM100 Support
@@ -16,16 +15,9 @@
 // with full/empty barriers per stage (the producer waits on the inverted parity, as in the
 // 3-stage ring of tilelang (velog) section 1.3) and a double-buffered accumulator (2 x 256
 // columns) so the epilogue of one tile overlaps the main loop of the next. CTAs are persistent:
-// cluster i takes cluster tiles i, i + clusters, ... in a grouped order that keeps A and B panels
-// in L2.
+// CTA i takes tiles i, i + grid, ... in a grouped order that keeps A and B panels in L2.
 //
-// Clusters (kCM = 2 or 4): the kCM CTAs of a cluster compute the 128-row tiles mc*kCM + rank of
-// the same N-tile, so they need the same B tile. CTA `rank` loads the rank-th 1/kCM of it once
-// and multicasts it into every CTA of the cluster; each CTA still loads its own A. The stage's
-// full barrier in every CTA counts all bytes landing there, and the stage's empty barrier counts
-// one release from every CTA's MMA thread (a copy into stage s of all kCM CTAs may start only
-// when all of them are done with it). This cuts the L2 -> SM traffic per CTA and K-block from
-// 48 KiB to 16 + 32/kCM KiB, which is what bounds the kernel without clusters.
+// Every TMA load goes to the issuing CTA's own shared memory (no cluster multicast).
 #pragma once
 
 #include "gemm_common.cuh"
@@ -34,22 +26,19 @@ namespace dtc {
 
 namespace g16 {
 constexpr int kBM = 128;
+constexpr int kBK = 64;                 // K-elements per stage: one 128-byte swizzle row
 constexpr int kTmemCols = 512;          // two fp32 accumulators
 constexpr int kAccStride = 256;         // column offset of the second accumulator
 constexpr int kThreads = 192;
-constexpr int kGroupM = 8;  // cluster rows per rasterisation group
+constexpr int kGroupM = 8;              // M-tiles per rasterisation group
 constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
 
-// K-blocks of 64 (one 128-byte swizzle row of 16-bit elements) or 32 (a 64-byte swizzle row):
-// the shallower block halves a stage, so the same shared memory holds twice as many stages and a
-// larger share of the ring is in flight while one stage is being consumed.
-template <int kBN, int kBK, int kStages>
+// As many 64-deep stages as fit beside the 32 KB of output staging.
+template <int kBN, int kStages>
 struct Cfg {
     static constexpr int kAStage = kBM * kBK * 2;
     static constexpr int kBStage = kBN * kBK * 2;
     static constexpr int kStageBytes = kAStage + kBStage;
-    static constexpr int kPitch = kBK * 2;  // bytes per K-major row = swizzle width
-    static_assert(kBK == 64 || kBK == 32, "K-block of 64 or 32");
     static_assert(kStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
     static constexpr int kCBytes = 4 * 2 * 4096;  // two 4 KB output staging slots per epilogue warp
     static constexpr int kSmemBytes = kStages * kStageBytes + kCBytes + 1024;  // + alignment slack
@@ -58,23 +47,16 @@ struct Cfg {
 };
 }  // namespace g16
 
-template <bool kBF16, bool kAMN, bool kNN, int kBN, int kBK, int kStages, int kCM>
+template <bool kBF16, bool kAMN, bool kNN, int kBN, int kStages>
 __global__ void __launch_bounds__(g16::kThreads, 1)
     gemm16_1cta_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC,
                        const __grid_constant__ CUtensorMap tmC32, const Gemm16Args args) {
     using namespace g16;
-    using C_ = Cfg<kBN, kBK, kStages>;
+    using C_ = Cfg<kBN, kStages>;
     constexpr int kAStage = C_::kAStage;
-    constexpr int kPitch = C_::kPitch;
-    static_assert(kCM == 1 || kCM == 2 || kCM == 4, "cluster of 1, 2 or 4 CTAs");
-    static_assert((kBN / kCM) % 8 == 0, "each CTA's share of B is whole 8-row swizzle atoms");
-    static_assert(!kNN || (kBN % 64 == 0 && (kBN / 64) % kCM == 0),
-                  "NN: B is loaded as 64-column boxes, split evenly over the cluster");
-    constexpr int kBPartRows = kBN / kCM;                 // NT: rows of B^T this CTA loads
-    constexpr int kBPartBytes = kBPartRows * kBK * 2;     // bytes of B this CTA loads
-    constexpr uint16_t kMask = (uint16_t)((1u << kCM) - 1);
+    static_assert(!kNN || kBN % 64 == 0, "B stored [K,N] is loaded as 64-column boxes");
 
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[kStages];
@@ -90,17 +72,13 @@ __global__ void __launch_bounds__(g16::kThreads, 1)
     const uint32_t sB = base + kStages * kAStage;  // kStages x kBStage
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = kCM > 1 ? cluster_ctarank() : 0;
-    const int cluster = blockIdx.x / kCM;
-    const int clusters = gridDim.x / kCM;
-    const int num_mc = (args.num_m + kCM - 1) / kCM;  // cluster rows of kCM * 128
-    const int total = num_mc * args.num_n;
+    const int total = args.num_m * args.num_n;
     volatile int* abort = &abort_flag;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&bar_full[s]), 1);
-            mbar_init(smem_u32(&bar_empty[s]), kCM);  // one release per CTA of the cluster
+            mbar_init(smem_u32(&bar_empty[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&bar_tfull[b]), 1);
@@ -121,7 +99,6 @@ __global__ void __launch_bounds__(g16::kThreads, 1)
     }
     tc_fence_before_sync();
     __syncthreads();
-    if constexpr (kCM > 1) cluster_sync();  // every CTA's barriers exist before any multicast
     tc_fence_after_sync();
     const uint32_t tmem_base = tmem_slot;
 
@@ -130,14 +107,13 @@ __global__ void __launch_bounds__(g16::kThreads, 1)
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            for (int t = cluster; t < total && ok; t += clusters) {
-                int mc, nt;
-                tile_coords(t, num_mc, args.num_n, kGroupM, mc, nt);
-                const int mt = mc * kCM + (int)rank;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                int mt, nt;
+                tile_coords(t, args.num_m, args.num_n, kGroupM, mt, nt);
                 for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
                     const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
                     if (!wait_bounded(smem_u32(&bar_empty[s]), ph ^ 1u, abort, args.timeout_ns,
-                                      &g_dtc_status, 1)) {
+                                      args.status, 1)) {
                         ok = false;
                         break;
                     }
@@ -154,29 +130,17 @@ __global__ void __launch_bounds__(g16::kThreads, 1)
                     }
                     const uint32_t bdst = sB + s * C_::kBStage;
                     if constexpr (!kNN) {
-                        const uint32_t dst = bdst + rank * kBPartBytes;
-                        const int row = nt * kBN + (int)rank * kBPartRows;
-                        if constexpr (kCM == 1)
-                            tma_load_2d(dst, &tmB, full, kb * kBK, row);
-                        else
-                            tma_load_2d_multicast(dst, &tmB, full, kb * kBK, row, kMask);
+                        tma_load_2d(bdst, &tmB, full, kb * kBK, nt * kBN);
                     } else {
-                        constexpr int kBoxes = kBN / 64 / kCM;  // 64-column boxes per CTA
 #pragma unroll
-                        for (int j = 0; j < kBoxes; ++j) {
-                            const int box = (int)rank * kBoxes + j;
-                            const uint32_t dst = bdst + box * (64 * kBK * 2);
-                            if constexpr (kCM == 1)
-                                tma_load_2d(dst, &tmB, full, nt * kBN + box * 64, kb * kBK);
-                            else
-                                tma_load_2d_multicast(dst, &tmB, full, nt * kBN + box * 64,
-                                                      kb * kBK, kMask);
-                        }
+                        for (int j = 0; j < kBN / 64; ++j)  // 64-column boxes of kBK K-rows
+                            tma_load_2d(bdst + j * (64 * kBK * 2), &tmB, full, nt * kBN + j * 64,
+                                        kb * kBK);
                     }
                 }
             }
             if (!ok) {
-                // Let the copies already issued (ours and the multicasts into this CTA) land.
+                // Let the copies already issued land before the CTA may exit.
                 const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0;
                 for (uint32_t i = first; i < it; ++i) {
                     if (args.fault == 1 && i == 0) continue;
@@ -190,10 +154,10 @@ __global__ void __launch_bounds__(g16::kThreads, 1)
             constexpr uint32_t idesc = idesc_f16(kBF16, kNN, kBM, kBN, kAMN);
             uint32_t it = 0, acc = 0;
             bool ok = true, issued = false;
-            for (int t = cluster; t < total && ok; t += clusters) {
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const uint32_t b = acc & 1u, aph = (acc >> 1) & 1u;
                 if (!wait_bounded(smem_u32(&bar_tempty[b]), aph ^ 1u, abort, args.timeout_ns,
-                                  &g_dtc_status, 2)) {
+                                  args.status, 2)) {
                     ok = false;
                     break;
                 }
@@ -202,7 +166,7 @@ __global__ void __launch_bounds__(g16::kThreads, 1)
                 for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
                     const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
                     if (!wait_bounded(smem_u32(&bar_full[s]), ph, abort, args.timeout_ns,
-                                      &g_dtc_status, 3)) {
+                                      args.status, 3)) {
                         ok = false;
                         break;
                     }
@@ -212,20 +176,14 @@ __global__ void __launch_bounds__(g16::kThreads, 1)
                     for (int kk = 0; kk < kBK / 16; ++kk) {
                         const uint64_t adesc =
                             kAMN ? smem_desc<128>(a0 + kk * 16 * 128, 64 * kBK * 2, 1024)
-                                      : smem_desc<kPitch>(a0 + kk * 32, 16, 8 * kPitch);
+                                 : smem_desc<128>(a0 + kk * 32, 16, 1024);
                         const uint64_t bdesc =
                             kNN ? smem_desc<128>(b0 + kk * 16 * 128, 64 * kBK * 2, 1024)
-                                : smem_desc<kPitch>(b0 + kk * 32, 16, 8 * kPitch);
+                                : smem_desc<128>(b0 + kk * 32, 16, 1024);
                         mma_f16_cta1(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     issued = true;
-                    const uint32_t e = smem_u32(&bar_empty[s]);
-                    if constexpr (kCM == 1) {
-                        mma_commit_cta1(e);
-                    } else {
-#pragma unroll
-                        for (int r = 0; r < kCM; ++r) mma_commit_cta1(map_to_cta(e, r));
-                    }
+                    mma_commit_cta1(smem_u32(&bar_empty[s]));
                 }
                 if (!ok) break;
                 mma_commit_cta1(smem_u32(&bar_tfull[b]));
@@ -242,15 +200,14 @@ __global__ void __launch_bounds__(g16::kThreads, 1)
         const int q = warp & 3;  // Tensor Memory lane quarter this warp may access
         const uint32_t my_slots = base + kStages * C_::kStageBytes + (uint32_t)q * 8192u;
         uint32_t acc = 0, stores = 0;
-        for (int t = cluster; t < total; t += clusters, ++acc) {
-            int mc, nt;
-            tile_coords(t, num_mc, args.num_n, kGroupM, mc, nt);
-            const int mt = mc * kCM + (int)rank;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++acc) {
+            int mt, nt;
+            tile_coords(t, args.num_m, args.num_n, kGroupM, mt, nt);
             const uint32_t b = acc & 1u, aph = (acc >> 1) & 1u;
             int ok = 1;
             if (lane == 0)
                 ok = wait_bounded(smem_u32(&bar_tfull[b]), aph, abort, args.timeout_ns,
-                                  &g_dtc_status, 4);
+                                  args.status, 4);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after_sync();
@@ -271,14 +228,7 @@ __global__ void __launch_bounds__(g16::kThreads, 1)
     // ------------------------------ teardown ------------------------------
     tc_fence_before_sync();
     __syncthreads();
-    if constexpr (kCM > 1) cluster_sync();  // no CTA leaves while others may still write to it
     if (warp == 1) {
-        if (kCM > 1 && *abort && lane == 0) {
-            // After an abort, copies multicast into this CTA for a phase it never armed may
-            // still be in flight: give them a fixed, bounded time to land.
-            const uint64_t t0 = globaltimer_ns();
-            while (globaltimer_ns() - t0 < 1000ull * 1000) __nanosleep(1000);
-        }
         __syncwarp();
         tc_fence_after_sync();
         tmem_dealloc<1>(tmem_base, kTmemCols);

@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
                 for (int kb = w.k0; kb < w.k1; ++kb, ++it) {
                     const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
                     if (!wait_bounded(smem_u32(&bar_empty[s]), ph ^ 1u, abort, args.timeout_ns,
-                                      &g_dtc_status, 11)) {
+                                      args.status, 11)) {
                         ok = false;
                         break;
                     }
@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
             while (ok && wi.next(w)) {
                 const uint32_t b = acc & 1u, aph = (acc >> 1) & 1u;
                 if (!wait_bounded(smem_u32(&bar_tempty[b]), aph ^ 1u, abort, args.timeout_ns,
-                                  &g_dtc_status, 12)) {
+                                  args.status, 12)) {
                     ok = false;
                     break;
                 }
@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
                 const uint32_t d_tmem = tmem_base + b * kAccStride;
                 for (int kb = w.k0; kb < w.k1; ++kb) {
                     if (!wait_bounded(smem_u32(&bar_full[s]), ph, abort, args.timeout_ns,
-                                      &g_dtc_status, 13)) {
+                                      args.status, 13)) {
                         ok = false;
                         break;
                     }
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
             int ok = 1;
             if (lane == 0)
                 ok = wait_bounded<false, true>(smem_u32(&bar_tfull[b]), aph, abort,
-                                               args.timeout_ns, &g_dtc_status, 14);
+                                               args.timeout_ns, args.status, 14);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after_sync();
@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
                 for (int u = pair + 1; u <= last_unit && ok; ++u) {
                     if (sk_run_empty(u)) continue;  // a unit with no K-blocks wrote nothing
                     const uint32_t* f = args.sk_flags + u * 2 + (int)rank;
-                    if (lane == 0) ok = wait_flag_bounded(f, abort, args.timeout_ns, &g_dtc_status, 15);
+                    if (lane == 0) ok = wait_flag_bounded(f, abort, args.timeout_ns, args.status, 15);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (ok) (void)ld_acquire_gpu_u32(f);  // every lane takes its own acquire
                 }
@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
                 mbar_arrive(smem_u32(&bar_ep));
                 if (warp == 2 && lane == 0) {
                     const bool all = wait_bounded(smem_u32(&bar_ep), ep_phase, abort,
-                                                  args.timeout_ns, &g_dtc_status, 16);
+                                                  args.timeout_ns, args.status, 16);
                     if (all && ok) {
                         if (w.kind == kOther) {
                             __threadfence();

@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
             for (int kb = kb0; kb < kb1; ++kb, ++it) {
                 const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
                 if (!wait_bounded(smem_u32(&bar_empty[s]), ph ^ 1u, abort, args.timeout_ns,
-                                  &g_dtc_status, 21)) {
+                                  args.status, 21)) {
                     ok = false;
                     break;
                 }
@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
             for (int kb = kb0; kb < kb1; ++kb, ++it) {
                 const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
                 if (!wait_bounded(smem_u32(&bar_full[s]), ph, abort, args.timeout_ns,
-                                  &g_dtc_status, 23)) {
+                                  args.status, 23)) {
                     ok = false;
                     break;
                 }
@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
             const uint32_t peer = rank ^ 1u;
             int ok = 1;
             if (lane == 0)
-                ok = wait_bounded(smem_u32(&bar_tfull), 0, abort, args.timeout_ns, &g_dtc_status, 24);
+                ok = wait_bounded(smem_u32(&bar_tfull), 0, abort, args.timeout_ns, args.status, 24);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (ok) tc_fence_after_sync();
             cluster_wait();  // the peer's barriers exist
@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
                     int xok = 1;
                     if (lane == 0)
                         xok = wait_bounded<true>(smem_u32(&bar_xchg[j]), 0, abort, args.timeout_ns,
-                                                 &g_dtc_status, 25);
+                                                 args.status, 25);
                     xok = __shfl_sync(0xffffffffu, xok, 0);
                     if (!xok) break;
                     // the phase has completed: every lane takes its own acquire of it
@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
             const bool empty_slice = kb1 <= kb0;  // no K-blocks: this CTA's share is zero
             int ok = 1;
             if (lane == 0)
-                ok = wait_bounded(smem_u32(&bar_tfull), 0, abort, args.timeout_ns, &g_dtc_status, 24);
+                ok = wait_bounded(smem_u32(&bar_tfull), 0, abort, args.timeout_ns, args.status, 24);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (ok) tc_fence_after_sync();
             if (owner != rank) {
@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
                     int xok = 1;
                     if (lane == 0)
                         xok = wait_bounded<true>(smem_u32(&bar_xchg[c]), 0, abort, args.timeout_ns,
-                                                 &g_dtc_status, 25);
+                                                 args.status, 25);
                     xok = __shfl_sync(0xffffffffu, xok, 0);
                     if (!xok) break;
                     // the phase has completed: every lane takes its own acquire of it

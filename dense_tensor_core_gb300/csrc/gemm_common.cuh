@@ -1,5 +1,5 @@
-// gemm_common.cuh -- pieces shared by the GEMM kernels: the device status word, the kernel
-// argument block, the persistent tile order and the fp32 -> 16-bit output packing.
+// gemm_common.cuh -- pieces shared by the GEMM kernels: the kernel argument block, the
+// persistent tile order and the fp32 -> 16-bit output packing.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -9,16 +9,6 @@
 
 namespace dtc {
 
-__device__ int g_dtc_status;  // first device-side wait that gave up (0 = none)
-
-// Scratch of gemm_ex_static_workspace: the stream-K workspace (flags, then the pieces' partial
-// sums) in module memory, zero at load, so that entry point allocates nothing. 20 MiB holds the
-// stream-K workspace of 76 CTA pairs (152 SMs) with 256-wide tiles: 1 KB of flags + 76 x 2 x 128
-// x 256 fp32.
-constexpr uint64_t kStaticWsBytes = 20ull << 20;
-static __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
-
-
 struct Gemm16Args {
     void* C;
     int64_t ldc;  // elements between rows of C (>= N)
@@ -26,6 +16,7 @@ struct Gemm16Args {
     int num_m, num_n, num_kb;
     uint64_t timeout_ns;
     int fault;
+    int* status;  // device status word: the first wait that gives up records its site here
     // Stream-K (pair kernel): the last sk_tiles tiles are shared out as equal runs of K-blocks
     // over all units; 0 = every tile whole. Partial sums go through the caller's workspace.
     int sk_tiles;

@@ -47,6 +47,7 @@ struct GemmMxArgs {
     uint32_t fmt_bits;         // instruction-descriptor element formats of A (bits 7-9), B (10-12)
     uint64_t timeout_ns;
     int fault;
+    int* status;  // device status word: the first wait that gives up records its site here
 };
 
 namespace gmx {
@@ -171,7 +172,7 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
                 for (int st = 0; st < num_st; ++st, ++it) {
                     const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
                     if (!wait_bounded(smem_u32(&bar_empty[s]), ph ^ 1u, abort, args.timeout_ns,
-                                      &g_dtc_status, 31)) {
+                                      args.status, 31)) {
                         ok = false;
                         break;
                     }
@@ -204,7 +205,7 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const uint32_t b = acc & 1u, aph = (acc >> 1) & 1u;
                 if (!wait_bounded(smem_u32(&bar_tempty[b]), aph ^ 1u, abort, args.timeout_ns,
-                                  &g_dtc_status, 32)) {
+                                  args.status, 32)) {
                     ok = false;
                     break;
                 }
@@ -214,7 +215,7 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
                     const int kb0 = st * kBlocks;  // first K-block of the stage
                     const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
                     if (!wait_bounded(smem_u32(&bar_full[s]), ph, abort, args.timeout_ns,
-                                      &g_dtc_status, 33)) {
+                                      args.status, 33)) {
                         ok = false;
                         break;
                     }
@@ -226,7 +227,7 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
                         const uint32_t set = sit % kSfSets;
                         if (kb % grp == 0) {  // the first K-block of a scale set
                             if (!wait_bounded(smem_u32(&bar_sfull[set]), (sit / kSfSets) & 1u,
-                                              abort, args.timeout_ns, &g_dtc_status, 35)) {
+                                              abort, args.timeout_ns, args.status, 35)) {
                                 ok = false;
                                 break;
                             }
@@ -276,7 +277,7 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
             int ok = 1;
             if (lane == 0)
                 ok = wait_bounded<false, true>(smem_u32(&bar_tfull[b]), aph, abort,
-                                               args.timeout_ns, &g_dtc_status, 34);
+                                               args.timeout_ns, args.status, 34);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after_sync();
@@ -324,7 +325,7 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
             if (lane == 0)
                 w_ok = wait_bounded<false, true>(smem_u32(&bar_sempty[set]),
                                                  ((sit / kSfSets) & 1u) ^ 1u, abort,
-                                                 args.timeout_ns, &g_dtc_status, 36);
+                                                 args.timeout_ns, args.status, 36);
             w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
             if (!w_ok) break;
             tc_fence_after_sync();

@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(gmx2::kThreads, 1)
                 for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
                     const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
                     if (!wait_bounded(smem_u32(&bar_empty[s]), ph ^ 1u, abort, args.timeout_ns,
-                                      &g_dtc_status, 41)) {
+                                      args.status, 41)) {
                         ok = false;
                         break;
                     }
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(gmx2::kThreads, 1)
             for (int t = pair; t < total && ok; t += num_pairs) {
                 const uint32_t b = acc & 1u, aph = (acc >> 1) & 1u;
                 if (!wait_bounded(smem_u32(&bar_tempty[b]), aph ^ 1u, abort, args.timeout_ns,
-                                  &g_dtc_status, 42)) {
+                                  args.status, 42)) {
                     ok = false;
                     break;
                 }
@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(gmx2::kThreads, 1)
                 for (int kb = 0; kb < args.num_kb && ok; ++kb, ++it) {
                     const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
                     if (!wait_bounded(smem_u32(&bar_full[s]), ph, abort, args.timeout_ns,
-                                      &g_dtc_status, 43)) {
+                                      args.status, 43)) {
                         ok = false;
                         break;
                     }
@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(gmx2::kThreads, 1)
                         const uint32_t set = sit % kSfSets;
                         if (k128 % kGroup == 0) {
                             if (!wait_bounded(smem_u32(&bar_sfull[set]), (sit / kSfSets) & 1u,
-                                              abort, args.timeout_ns, &g_dtc_status, 45)) {
+                                              abort, args.timeout_ns, args.status, 45)) {
                                 ok = false;
                                 break;
                             }
@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(gmx2::kThreads, 1)
             int ok = 1;
             if (lane == 0)
                 ok = wait_bounded(smem_u32(&bar_tfull[b]), aph, abort, args.timeout_ns,
-                                  &g_dtc_status, 44);
+                                  args.status, 44);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after_sync();
@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(gmx2::kThreads, 1)
             int w_ok = 1;
             if (lane == 0)
                 w_ok = wait_bounded(smem_u32(&bar_sempty[set]), ((sit / kSfSets) & 1u) ^ 1u, abort,
-                                    args.timeout_ns, &g_dtc_status, 46);
+                                    args.timeout_ns, args.status, 46);
             w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
             if (!w_ok) break;
             tc_fence_after_sync();

@@ -246,18 +246,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
         : "memory");
 }
 
-// Multicast form: the tile is written at offset `dst` of every CTA in `cta_mask` (bit i = CTA
-// rank i of the cluster) and each destination's barrier at offset `bar` receives the byte count.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* m,
-                                                      uint32_t bar, int32_t c0, int32_t c1,
-                                                      uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "h"(cta_mask)
-        : "memory");
-}
-
 // 2-CTA form: the completion is signalled on `bar`, which may be the barrier of the peer CTA
 // of the pair (a shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar,

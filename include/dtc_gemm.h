@@ -17,10 +17,12 @@
  *   (velog) section 1.3 also assumes; gemm_ex takes leading dimensions (lda, ldb, ldc in
  *   gemm_options) for operands and results that are rows of larger row-major arrays.
  *
- * Pointers: A, B, C (and sfA, sfB) are DEVICE pointers on the current CUDA device, owned by the
- * caller; the library keeps no reference after the call returns. C must not overlap A, B or the
- * scales. All pointers must be 16-byte aligned (the tensor-memory-access unit's global address
- * rule), and every row must start on a 16-byte boundary (see each function).
+ * Pointers: A, B, C (and sfA, sfB, and a stream-K workspace) are DEVICE pointers of the current
+ * CUDA device (or managed memory), owned by the caller; the library keeps no reference after the
+ * call returns. A pointer into host memory or into another GPU's memory is refused with
+ * GEMM_ERR_INVALID_ARG before anything is launched. C must not overlap A, B or the scales. All
+ * pointers must be 16-byte aligned (the tensor-memory-access unit's global address rule), and
+ * every row must start on a 16-byte boundary (see each function).
  *
  * Asynchrony: every GEMM call only enqueues work on `stream` (0 = the legacy default stream) and
  * returns; the status it returns covers argument checks and the launch. A device-side wait that
@@ -53,7 +55,8 @@ typedef enum {
 
 typedef enum {
     GEMM_OK = 0,
-    GEMM_ERR_INVALID_ARG = 1, /* rejected before any CUDA call: see the rules per function */
+    GEMM_ERR_INVALID_ARG = 1, /* rejected before any launch: see the rules per function (all but
+                                 the device-memory check need no CUDA call) */
     GEMM_ERR_UNSUPPORTED = 2, /* the current device is not an sm_103 GPU, or a variant that the
                                  requested shape or layout does not allow was forced */
     GEMM_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed; the message names it */
@@ -63,8 +66,7 @@ typedef enum {
 /* Kernel variants (gemm_options.variant). AUTO picks per shape. */
 typedef enum {
     GEMM_VARIANT_AUTO = 0,
-    GEMM_VARIANT_1CTA = 1,   /* persistent 128 x 256 or 128 x 224 tiles, one CTA per tile, in
-                                clusters of 1 or 2 CTAs along M sharing B by TMA multicast */
+    GEMM_VARIANT_1CTA = 1,   /* persistent 128 x 256 or 128 x 224 tiles, one CTA per tile */
     GEMM_VARIANT_2CTA = 2,   /* persistent 256 x 256 or 256 x 224 tiles on a CTA pair
                                 (cluster 2x1, tcgen05 cta_group::2); for MXFP8 (256 x 224,
                                 K % 128 == 0) an option that is never chosen automatically */
@@ -84,10 +86,9 @@ typedef struct {
                              GEMM_ERR_TIMEOUT through gemm_stream_status. */
     int tile_n;           /* force the N-tile: 256, 224 (not SPLITK; one-CTA tiles need B stored
                              [N,K]) or 128 (SPLITK only); 0 = choose */
-    int cluster_m;        /* 1CTA only: CTAs per cluster along M sharing B by multicast (1 or
-                             2); 0 = choose */
-    int tile_k;           /* K-elements per pipeline stage: 64 or 32 (1CTA), 64 or 128 (2CTA;
-                             SPLITK with 128-wide tiles); 128 needs K % 64 == 0; 0 = choose */
+    int tile_k;           /* K-elements per pipeline stage: 64 (1CTA), 64 or 128 (2CTA; SPLITK
+                             with 128-wide tiles; 128 needs K % 64 == 0), 128 or 256 (block-scaled
+                             one-CTA kernel; 256 needs K % 128 == 0); 0 = choose */
     int64_t lda;          /* elements between consecutive stored rows of A, B, C; 0 = dense (the */
     int64_t ldb;          /* row length: K or M for A, K or N for B, N for C). At least the row */
     int64_t ldc;          /* length, and rows must start 16 bytes apart (ld x element size %
@@ -151,12 +152,15 @@ int gemm_mxfp8(const void* A, const void* B, const void* sfA, const void* sfB, v
  * NT for 2; the scale arrays stay dense). opts may be NULL (all defaults). INVALID_ARG also when
  * a leading dimension is negative, below its row length, above 2^31-1 or not a multiple of 16
  * bytes.
+ * (The products of gemm_bf16, gemm_f16 and gemm_mxfp8 with the options of the pages' GEMM call:
+ * T.gemm's trans_A / trans_B in TileLang SM100 Support (Preview), "Code Example", and the block-
+ * scaled variants of the 05 Blackwell TCGEN05 GEMM tutorial, "Advanced".)
  */
 int gemm_ex(int dtype, const void* A, const void* B, const void* sfA, const void* sfB, void* C,
             int64_t M, int64_t N, int64_t K, int layout, const gemm_options* opts,
             dtc_stream_t stream);
 
-/* What a call with these sizes and options would launch. */
+/* What a call with these sizes and options would launch (gemm_plan, gemm_plan_model). */
 typedef struct {
     int variant;  /* GEMM_VARIANT_1CTA, _2CTA or _SPLITK (never AUTO) */
     int tile_m;   /* rows of C per tile (per CTA pair for 2CTA) */
@@ -170,24 +174,51 @@ typedef struct {
     int sk_tiles; /* tiles shared out by stream-K (0 = none) */
 } gemm_plan_info;
 
-/* Fills *info with the launch that gemm_ex would make for these sizes and options. Returns
- * GEMM_OK, or the status the call would fail with (sizes/layout/dtype only; pointers are not
- * part of the plan). Makes no CUDA call except device queries. */
+/* Fills *info with the launch that gemm_ex would make for these sizes and options on the current
+ * device. Returns GEMM_OK, or the status the call would fail with (sizes/layout/dtype only;
+ * pointers are not part of the plan). Makes no CUDA call except device queries (the first call on
+ * a device asks how many clusters of the pair and split-K kernels can be resident at once). The
+ * pages have no counterpart: their kernels have one fixed tile. */
 int gemm_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm_options* opts,
               gemm_plan_info* info);
+
+/* What the planner knows about a device. The pair kernel's stream-K mode makes pairs wait for
+ * pieces other pairs compute, so it counts only on pairs that can be resident at once. */
+typedef struct {
+    int sm_count;         /* streaming multiprocessors (152 on GB300) */
+    int pair_clusters;    /* clusters of 2 CTAs of the pair kernel resident at once (0 = half
+                             the SMs) */
+    int split2_clusters;  /* clusters of 2 CTAs of the split-K kernel resident at once (0 = half
+                             the SMs) */
+    int split4_clusters;  /* clusters of 4 CTAs of the split-K kernel resident at once (0 = a
+                             quarter of the SMs) */
+} gemm_device_model;
+
+/* The current device's model (the first call asks the CUDA occupancy API). INVALID_ARG if out is
+ * NULL. The pages have no counterpart. */
+int gemm_device_model_query(gemm_device_model* out);
+
+/* gemm_plan for a described device instead of the current one: a pure function of its arguments
+ * (no CUDA call, so it also runs on a machine without a GPU). INVALID_ARG if model or info is
+ * NULL, sm_count < 1 or a cluster count is negative; otherwise as gemm_plan. The pages have no
+ * counterpart. */
+int gemm_plan_model(const gemm_device_model* model, int dtype, int64_t M, int64_t N, int64_t K,
+                    int layout, const gemm_options* opts, gemm_plan_info* info);
 
 /*
  * gemm_ex, with the library's own stream-K workspace instead of a caller's: a 20 MiB region of
  * module memory (a file-scope device array, zero when the library is loaded), so this call
  * allocates nothing, on the host or the device. The pages have no counterpart.
  *   - opts->workspace must be NULL (INVALID_ARG otherwise); the other options are gemm_ex's.
- *   - A product whose stream-K plan needs more than 20 MiB (a device with more than 152 SMs)
- *     runs without stream-K, or fails with INVALID_ARG when opts->stream_k = 1 (required).
+ *   - 20 MiB holds the stream-K workspace of up to 79 resident CTA pairs (devices of up to 158
+ *     SMs). A plan that would need more runs without stream-K, or fails with INVALID_ARG when
+ *     opts->stream_k = 1 (required).
  *   - The first call on a device looks up the region's address with cudaGetSymbolAddress (a
  *     synchronous call): make one call on the device before capturing a stream into a graph.
- *   - The region's first 1 KB (flags) must be zero when a launch starts: each call clears it
- *     with cudaMemsetAsync on `stream` before its launch (so a call after a GEMM_ERR_TIMEOUT
- *     starts clean), and every completed launch leaves it zero.
+ *   - The region's first 1 KB (flags) must be zero when a launch starts: a call whose plan uses
+ *     stream-K clears it with cudaMemsetAsync on `stream` just before its launch (so a call after
+ *     a GEMM_ERR_TIMEOUT starts clean); a call rejected by its argument checks, or whose plan
+ *     takes whole tiles, enqueues nothing but its own kernel.
  *   - There is one region per device: calls that may overlap (on different streams, or from
  *     different threads) race on it and may return wrong results. Serialise them.
  */
@@ -206,10 +237,16 @@ int gemm_workspace_size(int dtype, int64_t M, int64_t N, int64_t K, int layout,
                         const gemm_options* opts, uint64_t* bytes);
 
 /* Message for the calling thread's most recent non-OK return ("" if none). Valid until that
- * thread's next call into the library. */
+ * thread's next call into the library. The convention of the generated host code of tilelang
+ * (velog) section 1.3 (Generated Kernel Source, the host call()): every call returns an int status
+ * and the text of the last error is kept in a buffer the caller reads afterwards (there one static
+ * buffer, here one per thread). */
 const char* gemm_last_error(void);
 
 /*
+ * The asynchronous half of the same convention (tilelang (velog) section 1.3, the host call():
+ * the launch is enqueued and its status returned at once, and an error that happens later on the
+ * stream is read afterwards from the error buffer; here device-side timeouts are added to it).
  * Synchronises `stream`, then reports and clears the device status word of the current device:
  * GEMM_ERR_TIMEOUT if a kernel's bounded wait gave up since the last check (the kernel then
  * released its tensor memory and returned early, so C is incomplete), GEMM_ERR_CUDA if the

@@ -40,6 +40,27 @@ def test_header_declares_the_entry_points():
         assert n in names
 
 
+CITATIONS = ("TileLang SM100 Support", "tilelang (velog)", "05 Blackwell TCGEN05 GEMM",
+             "pages have no counterpart")
+
+
+def test_every_declaration_cites_its_passage():
+    # each entry point's comment names the page passage that defines it, or says that the pages
+    # have none
+    for h in sorted(os.listdir(HEADER_DIR)):
+        if not h.endswith(".h"):
+            continue
+        src = open(os.path.join(HEADER_DIR, h)).read()
+        for name in declared_functions():
+            m = re.search(r"\b(?:int|const char\*)\s+" + name + r"\s*\(", src)
+            if not m:
+                continue
+            start = src.rfind("*/", 0, m.start())
+            open_ = src.rfind("/*", 0, start)
+            comment = " ".join(re.sub(r"\n\s*\*(?!/)", " ", src[open_:start]).split())
+            assert any(c in comment for c in CITATIONS), f"{name}: no citation in {comment[:80]!r}"
+
+
 def test_library_exports_every_declared_symbol(L):
     for n in declared_functions():
         assert hasattr(L, n), f"{n} is declared in include/ but not exported"

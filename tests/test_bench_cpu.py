@@ -105,3 +105,30 @@ def test_reference_arm_non_zero_ranks_exit_quietly():
 def test_warmup_below_three_is_refused():
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "2"])
+
+
+def test_nvml_samples_summarised_over_the_timed_window():
+    import bench
+
+    samples = [{"t": 1.0, "sm": 1000.0, "max": 2070.0, "power": 100.0, "reasons": 0x1},
+               {"t": 2.0, "sm": 2070.0, "max": 2070.0, "power": 900.0, "reasons": 0x0},
+               {"t": 2.5, "sm": 2055.0, "max": 2070.0, "power": 1300.0, "reasons": 0x4},
+               {"t": 3.0, "sm": 2070.0, "max": 2070.0, "power": 950.0, "reasons": 0x0},
+               {"t": 9.0, "sm": 900.0, "max": 2070.0, "power": 90.0, "reasons": 0x48}]
+    r = bench.summarise_samples(samples, 1.5, 3.5)
+    assert r["window"] == "timed" and r["samples"] == 3
+    assert r["sm_mhz"] == 2070.0 and r["sm_max_mhz"] == 2070.0
+    assert r["reasons"] == ["sw_power_cap"]  # idle (0x1) outside the window is not reported
+    r = bench.summarise_samples(samples, 8.0, 10.0)
+    assert r["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
+    assert bench.summarise_samples(samples, 20.0, 21.0)["window"] == "whole run"
+
+
+def test_baseline_configs_name_known_workloads():
+    import bench
+    from dense_tensor_core_gb300 import workloads
+
+    ids = [c[0] for c in bench.BASELINE_CONFIGS]
+    assert ids == ["1", "2", "3", "4a", "4b", "5"]
+    for _, name, bound in bench.BASELINE_CONFIGS:
+        assert name in workloads.WORKLOADS and bound in ("latency", "tensor", "hbm")

@@ -83,25 +83,19 @@ def test_more_tiles_than_sms_full_parity(kind, layout, variant):
     full_check(kind, layout, 4096, 2048, 128, seed=77, variant=VARIANTS[variant])
 
 
-@pytest.mark.parametrize("tile_k", [64, 32])
-@pytest.mark.parametrize("cluster_m", [1, 2])
 @pytest.mark.parametrize("tile_n", [256, 224])
 @pytest.mark.parametrize("layout", ["NT", "NN"])
 @pytest.mark.parametrize("M,N,K", [(640, 520, 200), (384, 264, 136), (1152, 1792, 512)])
-def test_one_cta_configurations_full_parity(M, N, K, layout, tile_n, cluster_m, tile_k):
-    # every tile width, K-block depth and cluster size; 640 and 384 rows give an odd number of
-    # 128-row tiles, so with clusters of 2 one CTA of the last cluster computes rows past M (loads
-    # zeros, stores nothing); K = 200 and 136 end in a partial K-block
+def test_one_cta_configurations_full_parity(M, N, K, layout, tile_n):
+    # both tile widths; 640 and 384 rows give partial 128-row tiles; K = 200 and 136 end in a
+    # partial K-block
     if layout == "NN" and tile_n == 224:
         pytest.skip("224-wide one-CTA tiles are offered for a B stored [N,K] only")
     import dense_tensor_core_gb300 as dtc
 
-    p = dtc.gemm_plan("bf16", M, N, K, layout, variant=1, tile_n=tile_n, cluster_m=cluster_m,
-                      tile_k=tile_k)
-    assert p["cluster"] == cluster_m and p["tile_n"] == tile_n and p["tile_k"] == tile_k
-    assert p["ctas"] % cluster_m == 0
-    full_check("bf16", layout, M, N, K, seed=M + N, variant=1, tile_n=tile_n,
-               cluster_m=cluster_m, tile_k=tile_k)
+    p = dtc.gemm_plan("bf16", M, N, K, layout, variant=1, tile_n=tile_n)
+    assert p["cluster"] == 1 and p["tile_n"] == tile_n and p["tile_k"] == 64
+    full_check("bf16", layout, M, N, K, seed=M + N, variant=1, tile_n=tile_n)
 
 
 @pytest.mark.parametrize("tile_n,tile_k", [(128, 0), (128, 64), (256, 0)])
@@ -277,7 +271,7 @@ def test_repeated_calls_are_deterministic():
 
 # --- A stored transposed (TN, TT) and rows of larger arrays (leading dimensions) ---------------
 
-@pytest.mark.parametrize("variant,extra", [(1, {}), (1, dict(tile_k=32)), (1, dict(cluster_m=2)),
+@pytest.mark.parametrize("variant,extra", [(1, {}), (1, dict(tile_n=224)),
                                            (2, dict(tile_k=64)), (2, dict(tile_k=128)),
                                            (3, dict(split_k=2)), (3, dict(split_k=4, tile_k=64))])
 @pytest.mark.parametrize("layout", ["TN", "TT"])
@@ -464,3 +458,44 @@ def test_stream_k_with_rows_of_larger_arrays():
     C = Cb[:, :N].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
     ref = oracle.gemm16("bf16", "TN", A, B, M, N, K)
     check_close(values16(C, "bf16"), values16(ref, "bf16"), "stream-K, strided")
+
+
+# --- device-memory checks and the device model ---------------------------------------------------
+
+def test_host_memory_is_refused_before_launch():
+    # the kernels read through tensor maps of the current device: a host pointer (pageable or
+    # pinned) is refused with GEMM_ERR_INVALID_ARG and nothing is enqueued
+    import ctypes
+
+    import dense_tensor_core_gb300 as dtc
+
+    L = dtc.lib()
+    M = N = K = 256
+    dev_buf = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
+    C = torch.full((M, N), 7.0, dtype=torch.bfloat16, device="cuda")
+    pinned = torch.zeros((M, K), dtype=torch.bfloat16).pin_memory()
+    pageable = np.zeros((M, K), dtype=np.uint16)
+    vp = ctypes.c_void_p
+    for name, ptr in (("pinned", pinned.data_ptr()), ("pageable", pageable.ctypes.data)):
+        for args in ((ptr, dev_buf.data_ptr(), C.data_ptr()), (dev_buf.data_ptr(), ptr, C.data_ptr()),
+                     (dev_buf.data_ptr(), dev_buf.data_ptr(), ptr)):
+            rc = L.gemm_bf16(vp(args[0]), vp(args[1]), vp(args[2]), M, N, K, 0, None)
+            assert rc == 1, f"{name}: status {rc}"
+            assert b"device memory" in L.gemm_last_error()
+    dtc.gemm_stream_status()
+    assert (C.float() == 7.0).all()  # nothing ran
+
+
+def test_plan_matches_the_queried_device_model():
+    import dense_tensor_core_gb300 as dtc
+
+    m = dtc.gemm_device_model_query()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert m["sm_count"] == sms
+    assert 1 <= m["pair_clusters"] <= sms // 2
+    assert 1 <= m["split2_clusters"] <= sms // 2 and 1 <= m["split4_clusters"] <= sms // 4
+    ws = torch.zeros(32 << 20, dtype=torch.uint8, device="cuda")
+    for shape, kw in [((4096, 4096, 8192), {}), ((8192, 8192, 8192), dict(workspace=ws)),
+                      ((128, 8192, 8192), {}), ((1024, 1024, 1024), dict(layout="NN")),
+                      ((256, 256, 512), {}), ((2560, 2560, 1024), dict(workspace=ws))]:
+        assert dtc.gemm_plan("bf16", *shape, **kw) == dtc.gemm_plan("bf16", *shape, model=m, **kw)

@@ -1,0 +1,107 @@
+"""The planner without a GPU: gemm_plan_model plans for a described device (a pure function of its
+arguments), so the automatic kernel choice, stream-K and its residency guard are checked here on
+the GB300 model (152 SMs, 76 resident CTA pairs, 36 resident clusters of 4)."""
+import pytest
+import torch
+
+import dense_tensor_core_gb300 as dtc
+from dense_tensor_core_gb300 import GB300_MODEL
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from dense_tensor_core_gb300 import build
+
+    build.build()
+
+
+def plan(kind, M, N, K, layout="NT", model=GB300_MODEL, **kw):
+    return dtc.gemm_plan(kind, M, N, K, layout, model=model, **kw)
+
+
+def fake_workspace(nbytes=32 << 20):
+    # a host buffer stands in for the caller's device workspace: the planner only reads its
+    # address (non-NULL) and size; nothing is launched
+    return torch.zeros(nbytes, dtype=torch.uint8)
+
+
+def test_automatic_choice_on_gb300():
+    p = plan("bf16", 4096, 4096, 8192)  # 304 pair tiles of 256 x 224 = 4 waves of 76 pairs
+    assert (p["variant"], p["tile_m"], p["tile_n"], p["tile_k"], p["ctas"]) == (2, 256, 224, 128, 152)
+    p = plan("bf16", 8192, 8192, 8192)  # 1024 pair tiles of 256 x 256
+    assert (p["variant"], p["tile_m"], p["tile_n"], p["tile_k"]) == (2, 256, 256, 128)
+    assert plan("bf16", 4096, 4096, 8200)["tile_k"] == 64  # K % 64 != 0: 64-deep stages only
+    p = plan("bf16", 128, 8192, 8192)  # 64 tiles of 128 x 128, K split in 2
+    assert (p["variant"], p["split_k"], p["tile_n"], p["tile_k"], p["ctas"]) == (3, 2, 128, 128, 128)
+    p = plan("bf16", 128, 2048, 8192)  # 16 tiles: K split in 4
+    assert (p["variant"], p["split_k"], p["tile_n"], p["ctas"]) == (3, 4, 128, 64)
+    p = plan("f16", 1024, 1024, 1000, "NN")  # K % 64 != 0: 64-deep stages
+    assert (p["variant"], p["split_k"], p["tile_n"], p["tile_k"]) == (3, 2, 128, 64)
+    p = plan("bf16", 256, 256, 512)  # 8 K-blocks: too few to split
+    assert p["variant"] == 1 and p["cluster"] == 1 and p["tile_k"] == 64
+    p = plan("mxfp8", 4096, 4096, 8192)
+    assert (p["variant"], p["tile_n"], p["tile_k"]) == (1, 224, 256)
+
+
+def test_stream_k_on_gb300():
+    ws = fake_workspace()
+    p = plan("bf16", 8192, 8192, 8192, workspace=ws)  # 1024 tiles = 13 waves + 36
+    assert (p["variant"], p["tile_n"], p["sk_tiles"], p["ctas"]) == (2, 256, 1024 % 76, 152)
+    p = plan("bf16", 4096, 4096, 8192, workspace=ws)  # 256 tiles = 3 waves + 28
+    assert (p["variant"], p["tile_n"], p["sk_tiles"]) == (2, 256, 256 % 76)
+    assert plan("bf16", 4096, 4096, 8192)["sk_tiles"] == 0  # no workspace: whole tiles
+    assert plan("bf16", 8192, 8192, 8192, workspace=ws, stream_k=2)["sk_tiles"] == 0
+    # a whole number of waves needs no stream-K
+    assert plan("bf16", 256 * 19, 256 * 8, 8192, workspace=ws)["sk_tiles"] == 0
+
+
+def test_stream_k_counts_only_resident_pairs():
+    # The pair kernel's stream-K pairs wait for pieces other pairs compute, so the launch uses the
+    # pairs the device keeps resident, not half the SMs.
+    ws = fake_workspace()
+    fewer = dict(GB300_MODEL, pair_clusters=70)
+    M, N = 256 * 13, 256 * 77  # 1001 pair tiles: 13 waves + 13 of 76 pairs, 14 + 21 of 70
+    assert plan("bf16", M, N, 1024, workspace=ws)["sk_tiles"] == 1001 % 76
+    p = plan("bf16", M, N, 1024, model=fewer, workspace=ws)
+    assert (p["ctas"], p["sk_tiles"]) == (140, 1001 % 70)
+    # with 64 resident pairs the 1024 tiles fill whole waves: stream-K is dropped
+    p = plan("bf16", 8192, 8192, 8192, model=dict(GB300_MODEL, pair_clusters=64), workspace=ws)
+    assert p["sk_tiles"] == 0 and p["ctas"] == 128
+    with pytest.raises(dtc.GemmError) as e:
+        plan("bf16", 8192, 8192, 8192, model=dict(GB300_MODEL, pair_clusters=64), workspace=ws,
+             stream_k=1)
+    assert e.value.status == 2
+    # whole-tile pair launches are sized to the resident pairs too
+    p = plan("bf16", 8192, 8192, 8192, model=fewer)
+    assert p["ctas"] == 140
+
+
+def test_stream_k_flag_capacity():
+    # the workspace's 1 KB of flags holds 128 pairs: a device with more resident pairs runs whole
+    # tiles, and a call that requires stream-K there is refused
+    big = dict(sm_count=300, pair_clusters=150, split2_clusters=150, split4_clusters=75)
+    ws = fake_workspace(64 << 20)
+    assert plan("bf16", 8192, 8192, 8192, model=big, workspace=ws)["sk_tiles"] == 0
+    with pytest.raises(dtc.GemmError):
+        plan("bf16", 8192, 8192, 8192, model=big, workspace=ws, stream_k=1)
+
+
+def test_split_k_respects_resident_clusters():
+    # 64 tiles of 128 x 128 split in 2 need 64 resident clusters of 2; with fewer the split is
+    # not taken in one wave and the next candidate wins
+    p = plan("bf16", 128, 8192, 8192, model=dict(GB300_MODEL, split2_clusters=60))
+    assert not (p["variant"] == 3 and p["split_k"] == 2 and p["tile_n"] == 128)
+
+
+def test_plan_model_rejects_bad_models():
+    with pytest.raises(dtc.GemmError) as e:
+        plan("bf16", 256, 256, 256, model=dict(GB300_MODEL, sm_count=0))
+    assert e.value.status == 1
+    with pytest.raises(dtc.GemmError):
+        plan("bf16", 256, 256, 256, model=dict(GB300_MODEL, pair_clusters=-1))
+
+
+def test_removed_options_are_refused():
+    # the one-CTA kernel takes 64-deep stages only
+    with pytest.raises(dtc.GemmError):
+        plan("bf16", 1024, 1024, 1024, variant=1, tile_k=32)
