@@ -183,10 +183,14 @@ def test_mxfp8_error_against_k(block, variant):
         ref = values16(ref_codes, "bf16")
         err = np.abs(got - ref)
         small = np.abs(ref) < 1.0
+        # one bf16 rounding step of the reference (8 significant bits), or 2^-8 near zero
+        step = np.where(ref != 0, 2.0 ** (np.floor(np.log2(np.abs(ref) + (ref == 0))) - 7), 0.0)
+        bound = np.maximum(step, 2.0 ** -8)
         rows.append({"K": K, "block": block, "variant": variant,
                      "max_abs_err": float(err.max()),
                      "max_abs_err_ref_below_1": float(err[small].max()) if small.any() else None,
                      "max_abs_err_vs_exact_sum": float(np.abs(got - exact).max()),
+                     "max_err_in_output_steps": float((err / bound).max()),
                      "max_abs_ref": float(np.abs(ref).max())})
         check_close(got, ref, f"MXFP8 K = {K}, block {block}, variant {variant}")
     out = os.environ.get("DTC_KSWEEP_OUT")
@@ -194,7 +198,8 @@ def test_mxfp8_error_against_k(block, variant):
         with open(out, "a") as f:
             for r in rows:
                 f.write(json.dumps(r) + "\n")
-    # the error must not grow with K beyond what the output rounding explains: every output is
-    # within half a bf16 ulp of the exact sum plus the fp32 accumulation error, which stays far
-    # below the tolerance at these sizes
-    assert all(r["max_abs_err"] <= 0.05 for r in rows), rows
+    # The early warning the tolerance alone would hide: the kernel's output must stay within one
+    # output rounding step of the correctly rounded sum (fp32 accumulation may round a sum that
+    # lies near a bf16 midpoint the other way), and within 2^-8 of it near zero, at every K. A
+    # reduced-precision accumulation inside the block-scaled MMA would grow past this with K.
+    assert all(r["max_err_in_output_steps"] <= 1.0 for r in rows), rows

@@ -281,6 +281,8 @@ def test_transposed_a_full_parity(M, N, K, layout, variant, extra):
     # 264 rows leave a partial tile in M (and a partial 64-column box), K = 200 a partial K-block
     if extra.get("tile_k") == 128 and K % 64:
         pytest.skip("128-deep pair stages need K % 64 == 0")
+    if variant == 1 and extra.get("tile_n") == 224 and layout == "TN":
+        pytest.skip("224-wide one-CTA tiles are offered for a B stored [N,K] only")
     kind = "bf16" if (M + N) % 2 == 0 else "f16"
     full_check(kind, layout, M, N, K, seed=M + N + K, variant=variant, **extra)
     full_check("f16" if kind == "bf16" else "bf16", layout, M, N, K, seed=M + N + K + 1,
