@@ -9,6 +9,9 @@ end), whose header states the definition it computes and the page passages it fo
   "Code Example" and "Compilation and Usage") or ``Bop = B`` for "NN" (tilelang (velog), 1.1).
 * MXFP8: e4m3 operands times ``2^(sf-127)`` per row per 128 K-elements (05 Blackwell TCGEN05 GEMM
   tutorial, "Advanced": gemm_blockscaled with granularity 128 for A and B).
+* The other block-scaled formats of that section, read as the OCP MX family: elements e4m3, e5m2,
+  e2m3, e3m2 (fp6) or e2m1 (fp4), packed little-endian in rows; E8M0 scales per 32 or 128
+  K-elements, or UE4M3 scales per 16 (NVFP4).
 
 Arrays are numpy: 16-bit operands are passed as ``uint16`` code arrays, e4m3/E8M0 as ``uint8``.
 """
@@ -42,6 +45,19 @@ def _bind(path):
     L.dtc_oracle_dec_e5m2.argtypes = [ctypes.c_uint8]
     L.dtc_oracle_dec_e8m0.restype = ctypes.c_double
     L.dtc_oracle_dec_e8m0.argtypes = [ctypes.c_uint8]
+    for name in ("e2m3", "e3m2", "e2m1", "ue4m3"):
+        f = getattr(L, "dtc_oracle_dec_" + name)
+        f.restype = ctypes.c_double
+        f.argtypes = [ctypes.c_uint8]
+    L.dtc_oracle_format_bits.restype = ctypes.c_int
+    L.dtc_oracle_format_bits.argtypes = [ctypes.c_int]
+    L.dtc_oracle_gemm_bs.restype = ctypes.c_int
+    L.dtc_oracle_gemm_bs.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, u8p,
+                                     u8p, u8p, u8p, i64, i64, i64, u16p, dp, ctypes.c_int]
+    L.dtc_oracle_gemm_bs_sampled.restype = ctypes.c_int
+    L.dtc_oracle_gemm_bs_sampled.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, u8p, u8p, u8p, u8p, i64, i64, i64,
+                                             i64p, i64p, i64, u16p, dp]
     L.dtc_oracle_enc_bf16.restype = ctypes.c_uint16
     L.dtc_oracle_enc_bf16.argtypes = [ctypes.c_double]
     L.dtc_oracle_enc_f16.restype = ctypes.c_uint16
@@ -272,4 +288,83 @@ def gemm_mx_sampled(A, B, sfA, sfB, M, N, K, rows, cols, *, a_fmt="e4m3", b_fmt=
                                           _ptr(C, ctypes.c_uint16), _ptr(S, ctypes.c_double))
     if rc != 0:
         raise ValueError("oracle gemm_mx_sampled rejected its arguments")
+    return C, S
+
+
+# --- the general block-scaled family (OCP MX element formats, packed rows) ---------------------
+
+BS_FORMATS = {"e4m3": 0, "e5m2": 1, "e2m3": 2, "e3m2": 3, "e2m1": 4}
+BS_SCALES = {"e8m0": 0, "ue4m3": 1}
+FORMAT_BITS = {"e4m3": 8, "e5m2": 8, "e2m3": 6, "e3m2": 6, "e2m1": 4}
+
+
+def dec_e2m3(codes):
+    f = _L().dtc_oracle_dec_e2m3
+    return np.array([f(int(c)) for c in np.asarray(codes, dtype=np.uint8).ravel()])
+
+
+def dec_e3m2(codes):
+    f = _L().dtc_oracle_dec_e3m2
+    return np.array([f(int(c)) for c in np.asarray(codes, dtype=np.uint8).ravel()])
+
+
+def dec_e2m1(codes):
+    f = _L().dtc_oracle_dec_e2m1
+    return np.array([f(int(c)) for c in np.asarray(codes, dtype=np.uint8).ravel()])
+
+
+def dec_ue4m3(codes):
+    f = _L().dtc_oracle_dec_ue4m3
+    return np.array([f(int(c)) for c in np.asarray(codes, dtype=np.uint8).ravel()])
+
+
+def row_bytes(fmt, K):
+    """Bytes of one packed row of K elements of format `fmt`."""
+    return (K * FORMAT_BITS[fmt] + 7) // 8
+
+
+def _bs_inputs(A, B, sfA, sfB, M, N, K, a_fmt, b_fmt, block):
+    A = np.ascontiguousarray(A, dtype=np.uint8)
+    B = np.ascontiguousarray(B, dtype=np.uint8)
+    sfA = np.ascontiguousarray(sfA, dtype=np.uint8)
+    sfB = np.ascontiguousarray(sfB, dtype=np.uint8)
+    kb = (K + block - 1) // block
+    assert A.size == M * row_bytes(a_fmt, K) and B.size == N * row_bytes(b_fmt, K)
+    assert sfA.size == M * kb and sfB.size == N * kb
+    return A, B, sfA, sfB
+
+
+def gemm_bs(A, B, sfA, sfB, M, N, K, *, a_fmt="e4m3", b_fmt="e4m3", scale="e8m0", block=128,
+            sums=False, nthreads=None):
+    """Block-scaled GEMM, NT: A [M, row_bytes(a_fmt, K)] and B [N, row_bytes(b_fmt, K)] packed
+    rows of element codes, scales [rows, ceil(K/block)] (E8M0 or UE4M3 codes, block 16, 32 or
+    128). Output bf16 codes."""
+    A, B, sfA, sfB = _bs_inputs(A, B, sfA, sfB, M, N, K, a_fmt, b_fmt, block)
+    C = np.zeros((M, N), dtype=np.uint16)
+    S = np.zeros((M, N), dtype=np.float64) if sums else None
+    rc = _L().dtc_oracle_gemm_bs(BS_FORMATS[a_fmt], BS_FORMATS[b_fmt], BS_SCALES[scale], block,
+                                  _ptr(A, ctypes.c_uint8), _ptr(B, ctypes.c_uint8),
+                                  _ptr(sfA, ctypes.c_uint8), _ptr(sfB, ctypes.c_uint8), M, N, K,
+                                  _ptr(C, ctypes.c_uint16), _ptr(S, ctypes.c_double),
+                                  nthreads or threads())
+    if rc != 0:
+        raise ValueError("oracle gemm_bs rejected its arguments")
+    return (C, S) if sums else C
+
+
+def gemm_bs_sampled(A, B, sfA, sfB, M, N, K, rows, cols, *, a_fmt="e4m3", b_fmt="e4m3",
+                    scale="e8m0", block=128):
+    A, B, sfA, sfB = _bs_inputs(A, B, sfA, sfB, M, N, K, a_fmt, b_fmt, block)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    C = np.zeros(rows.size, dtype=np.uint16)
+    S = np.zeros(rows.size, dtype=np.float64)
+    rc = _L().dtc_oracle_gemm_bs_sampled(BS_FORMATS[a_fmt], BS_FORMATS[b_fmt], BS_SCALES[scale],
+                                          block, _ptr(A, ctypes.c_uint8), _ptr(B, ctypes.c_uint8),
+                                          _ptr(sfA, ctypes.c_uint8), _ptr(sfB, ctypes.c_uint8),
+                                          M, N, K, _ptr(rows, ctypes.c_int64),
+                                          _ptr(cols, ctypes.c_int64), rows.size,
+                                          _ptr(C, ctypes.c_uint16), _ptr(S, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle gemm_bs_sampled rejected its arguments")
     return C, S

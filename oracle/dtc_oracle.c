@@ -27,9 +27,10 @@
  *     C[m,n] = round_bf16( sum_k  e4m3(A[m,k]) * 2^(sfA[m,k/128]-127)
  *                               * e4m3(B[n,k]) * 2^(sfB[n,k/128]-127) )
  *   and the "other block-scaled formats" of the same section read as the OCP MX family the
- *   instruction supports: each operand e4m3 or e5m2, and scale blocks of g = 128 or 32
- *   K-elements (the OCP MX block size), scales [rows, ceil(K/g)]:
- *     C[m,n] = round_bf16( sum_k  fa(A[m,k]) * 2^(sfA[m,k/g]-127) * fb(B[n,k]) * 2^(sfB[n,k/g]-127) )
+ *   instruction supports: each operand e4m3, e5m2, e2m3, e3m2 or e2m1, and scale blocks of g =
+ *   128 or 32 K-elements (the OCP MX block size), E8M0 scales [rows, ceil(K/g)]; and NVFP4:
+ *   e2m1 operands with one UE4M3 scale per 16 K-elements:
+ *     C[m,n] = round_bf16( sum_k  fa(A[m,k]) * sa(sfA[m,k/g]) * fb(B[n,k]) * sb(sfB[n,k/g]) )
  *
  * Accumulation is in double. Every product of two bf16/fp16/e4m3 values, times powers of two
  * from the scales, is exact in double; only the sum carries rounding error, which for the
@@ -45,6 +46,16 @@
  *   e5m2  : OCP FP8 E5M2 (1, 5, 2; bias 15; exponent 31 = inf (m = 0) / NaN; subnormals
  *           m/4 * 2^-14; largest finite 57344).
  *   E8M0  : unsigned 8-bit exponent, value 2^(e-127); 0xFF = NaN.
+ *   The OCP MX element formats below fp8 (OCP Microscaling Formats (MX) v1.0; none has
+ *   infinities or NaNs):
+ *   e2m3  : FP6 (1, 2, 3; bias 1; subnormals m/8; largest 7.5).
+ *   e3m2  : FP6 (1, 3, 2; bias 3; subnormals m/16; largest 28).
+ *   e2m1  : FP4 (1, 2, 1; bias 1; subnormal 0.5; largest 6).
+ *   UE4M3 : the scale of NVFP4 (one per 16 elements): an e4m3 code with the sign bit clear.
+ *
+ * Packed storage of the sub-byte formats: a row of K elements of b bits (b = 4 or 6) is read as a
+ * little-endian bit stream, element k in bits [b*k, b*k + b) (fp4: byte k/2, the low nibble for
+ * even k; fp6: 4 elements in 3 bytes). A row of fp8 codes is one byte per element.
  *
  * Degenerate sizes: M == 0 or N == 0 computes nothing; K == 0 gives the empty sum, +0.
  *
@@ -130,6 +141,42 @@ double dtc_oracle_dec_e5m2(uint8_t b) {
 double dtc_oracle_dec_e8m0(uint8_t b) {
     if (b == 0xff) return NAN;
     return ldexp(1.0, (int)b - 127);
+}
+
+/* FP6 E2M3: sign bit 5, exponent bits 3-4 (bias 1), mantissa bits 0-2. */
+double dtc_oracle_dec_e2m3(uint8_t c) {
+    int sign = (c >> 5) & 1;
+    int e = (c >> 3) & 0x3;
+    int m = c & 0x7;
+    double v = e == 0 ? ldexp((double)m, -3)            /* subnormal: m/8 * 2^(1-1) */
+                      : ldexp((double)(8 + m), e - 4);  /* (1 + m/8) * 2^(e-1) */
+    return sign ? -v : v;
+}
+
+/* FP6 E3M2: sign bit 5, exponent bits 2-4 (bias 3), mantissa bits 0-1. */
+double dtc_oracle_dec_e3m2(uint8_t c) {
+    int sign = (c >> 5) & 1;
+    int e = (c >> 2) & 0x7;
+    int m = c & 0x3;
+    double v = e == 0 ? ldexp((double)m, -4)            /* subnormal: m/4 * 2^(1-3) */
+                      : ldexp((double)(4 + m), e - 5);  /* (1 + m/4) * 2^(e-3) */
+    return sign ? -v : v;
+}
+
+/* FP4 E2M1: sign bit 3, exponent bits 1-2 (bias 1), mantissa bit 0. */
+double dtc_oracle_dec_e2m1(uint8_t c) {
+    int sign = (c >> 3) & 1;
+    int e = (c >> 1) & 0x3;
+    int m = c & 0x1;
+    double v = e == 0 ? ldexp((double)m, -1)            /* subnormal: m/2 * 2^(1-1) */
+                      : ldexp((double)(2 + m), e - 2);  /* (1 + m/2) * 2^(e-1) */
+    return sign ? -v : v;
+}
+
+/* UE4M3 (NVFP4 scale): an e4m3 code whose sign bit must be clear; NaN otherwise. */
+double dtc_oracle_dec_ue4m3(uint8_t b) {
+    if (b & 0x80) return NAN;
+    return dtc_oracle_dec_e4m3(b);
 }
 
 /* ------------------------------------------------------------------------------------------ */
@@ -306,36 +353,84 @@ int dtc_oracle_gemm16_sampled(int dtype, int layout, const uint16_t* A, const ui
 
 #define DTC_ORACLE_E4M3 0
 #define DTC_ORACLE_E5M2 1
+#define DTC_ORACLE_E2M3 2
+#define DTC_ORACLE_E3M2 3
+#define DTC_ORACLE_E2M1 4
+#define DTC_ORACLE_SF_E8M0 0
+#define DTC_ORACLE_SF_UE4M3 1
 
-static double dec_fp8(int fmt, uint8_t b) {
-    return fmt == DTC_ORACLE_E5M2 ? dtc_oracle_dec_e5m2(b) : dtc_oracle_dec_e4m3(b);
+/* Bits per element of an element format; 0 if unknown. */
+int dtc_oracle_format_bits(int fmt) {
+    switch (fmt) {
+    case DTC_ORACLE_E4M3:
+    case DTC_ORACLE_E5M2: return 8;
+    case DTC_ORACLE_E2M3:
+    case DTC_ORACLE_E3M2: return 6;
+    case DTC_ORACLE_E2M1: return 4;
+    default: return 0;
+    }
 }
 
-static int mx_args_ok(int fmt_a, int fmt_b, int block) {
-    return (fmt_a == DTC_ORACLE_E4M3 || fmt_a == DTC_ORACLE_E5M2) &&
-           (fmt_b == DTC_ORACLE_E4M3 || fmt_b == DTC_ORACLE_E5M2) && (block == 32 || block == 128);
+/* Element k of a packed row (see the header comment): the b-bit field at bit b*k. */
+static uint8_t row_code(const uint8_t* row, int bits, int64_t k) {
+    if (bits == 8) return row[k];
+    int64_t bit = k * bits;
+    int64_t byte = bit / 8;
+    int shift = (int)(bit % 8);
+    unsigned v = row[byte];
+    if (shift + bits > 8) v |= (unsigned)row[byte + 1] << 8; /* the field spans two bytes */
+    return (uint8_t)((v >> shift) & ((1u << bits) - 1u));
 }
 
-/* Decode one operand with its scales applied: out[r][k] = fp8(X[r,k]) * 2^(sf[r,k/g]-127).
- * Exact in double. */
-static double* decode_scaled(int fmt, int block, const uint8_t* X, const uint8_t* sf, int64_t R,
-                             int64_t K) {
+static double dec_elem(int fmt, uint8_t c) {
+    switch (fmt) {
+    case DTC_ORACLE_E4M3: return dtc_oracle_dec_e4m3(c);
+    case DTC_ORACLE_E5M2: return dtc_oracle_dec_e5m2(c);
+    case DTC_ORACLE_E2M3: return dtc_oracle_dec_e2m3(c);
+    case DTC_ORACLE_E3M2: return dtc_oracle_dec_e3m2(c);
+    default: return dtc_oracle_dec_e2m1(c);
+    }
+}
+
+static double dec_scale(int sf_kind, uint8_t c) {
+    return sf_kind == DTC_ORACLE_SF_UE4M3 ? dtc_oracle_dec_ue4m3(c) : dtc_oracle_dec_e8m0(c);
+}
+
+static int bs_args_ok(int fmt_a, int fmt_b, int sf_kind, int block) {
+    return dtc_oracle_format_bits(fmt_a) && dtc_oracle_format_bits(fmt_b) &&
+           (sf_kind == DTC_ORACLE_SF_E8M0 || sf_kind == DTC_ORACLE_SF_UE4M3) &&
+           (block == 16 || block == 32 || block == 128);
+}
+
+/* Bytes of one packed row of K elements. */
+static int64_t row_bytes(int fmt, int64_t K) { return (K * dtc_oracle_format_bits(fmt) + 7) / 8; }
+
+/* Decode one operand with its scales applied: out[r][k] = f(X[r,k]) * s(sf[r,k/g]). Exact in
+ * double (a product of two values with at most 4 significant bits and a power of two, or of an
+ * fp8 value and a power of two). */
+static double* decode_scaled(int fmt, int sf_kind, int block, const uint8_t* X, const uint8_t* sf,
+                             int64_t R, int64_t K) {
     int64_t kb = (K + block - 1) / block;
+    int64_t rb = row_bytes(fmt, K);
+    int bits = dtc_oracle_format_bits(fmt);
     double* out = (double*)malloc(sizeof(double) * (size_t)(R * K > 0 ? R * K : 1));
     if (!out) return NULL;
     for (int64_t r = 0; r < R; ++r)
         for (int64_t k = 0; k < K; ++k)
-            out[r * K + k] = dec_fp8(fmt, X[r * K + k]) * dtc_oracle_dec_e8m0(sf[r * kb + k / block]);
+            out[r * K + k] = dec_elem(fmt, row_code(X + r * rb, bits, k)) *
+                             dec_scale(sf_kind, sf[r * kb + k / block]);
     return out;
 }
 
-int dtc_oracle_gemm_mx(int fmt_a, int fmt_b, int block, const uint8_t* A, const uint8_t* B,
-                       const uint8_t* sfA, const uint8_t* sfB, int64_t M, int64_t N, int64_t K,
-                       uint16_t* C, double* S, int nthreads) {
-    if (M < 0 || N < 0 || K < 0 || !mx_args_ok(fmt_a, fmt_b, block)) return -1;
+/* General block-scaled product, NT: A [M,K] and B [N,K] as packed rows of their formats, scales
+ * [rows, ceil(K/block)]. Output bf16 codes (and unrounded sums). */
+int dtc_oracle_gemm_bs(int fmt_a, int fmt_b, int sf_kind, int block, const uint8_t* A,
+                       const uint8_t* B, const uint8_t* sfA, const uint8_t* sfB, int64_t M,
+                       int64_t N, int64_t K, uint16_t* C, double* S, int nthreads) {
+    if (M < 0 || N < 0 || K < 0 || !bs_args_ok(fmt_a, fmt_b, sf_kind, block)) return -1;
     if (M == 0 || N == 0) return 0;
-    double* a = decode_scaled(fmt_a, block, A, sfA, M, K);
-    double* bt = decode_scaled(fmt_b, block, B, sfB, N, K);
+    double* a = decode_scaled(fmt_a, sf_kind, block, A, sfA, M, K);
+    double* bt = decode_scaled(fmt_b, sf_kind, block, B, sfB, N, K);
     if (!a || !bt) {
         free(a);
         free(bt);
@@ -348,25 +443,47 @@ int dtc_oracle_gemm_mx(int fmt_a, int fmt_b, int block, const uint8_t* A, const 
     return 0;
 }
 
-int dtc_oracle_gemm_mx_sampled(int fmt_a, int fmt_b, int block, const uint8_t* A,
+int dtc_oracle_gemm_bs_sampled(int fmt_a, int fmt_b, int sf_kind, int block, const uint8_t* A,
                                const uint8_t* B, const uint8_t* sfA, const uint8_t* sfB, int64_t M,
                                int64_t N, int64_t K, const int64_t* rows, const int64_t* cols,
                                int64_t count, uint16_t* Cout, double* Sout) {
-    if (M < 0 || N < 0 || K < 0 || count < 0 || !mx_args_ok(fmt_a, fmt_b, block)) return -1;
+    if (M < 0 || N < 0 || K < 0 || count < 0 || !bs_args_ok(fmt_a, fmt_b, sf_kind, block)) return -1;
     int64_t kb = (K + block - 1) / block;
+    int64_t ra = row_bytes(fmt_a, K), rb = row_bytes(fmt_b, K);
+    int ba = dtc_oracle_format_bits(fmt_a), bb = dtc_oracle_format_bits(fmt_b);
     for (int64_t i = 0; i < count; ++i) {
         int64_t m = rows[i], n = cols[i];
         if (m < 0 || m >= M || n < 0 || n >= N) return -1;
         double acc = 0.0;
         for (int64_t k = 0; k < K; ++k) {
-            double av = dec_fp8(fmt_a, A[m * K + k]) * dtc_oracle_dec_e8m0(sfA[m * kb + k / block]);
-            double bv = dec_fp8(fmt_b, B[n * K + k]) * dtc_oracle_dec_e8m0(sfB[n * kb + k / block]);
+            double av = dec_elem(fmt_a, row_code(A + m * ra, ba, k)) *
+                        dec_scale(sf_kind, sfA[m * kb + k / block]);
+            double bv = dec_elem(fmt_b, row_code(B + n * rb, bb, k)) *
+                        dec_scale(sf_kind, sfB[n * kb + k / block]);
             acc += av * bv;
         }
         if (Sout) Sout[i] = acc;
         if (Cout) Cout[i] = dtc_oracle_enc_bf16(acc);
     }
     return 0;
+}
+
+/* The fp8 members of the family (E8M0 scales, blocks of 32 or 128). */
+int dtc_oracle_gemm_mx(int fmt_a, int fmt_b, int block, const uint8_t* A, const uint8_t* B,
+                       const uint8_t* sfA, const uint8_t* sfB, int64_t M, int64_t N, int64_t K,
+                       uint16_t* C, double* S, int nthreads) {
+    if (fmt_a > DTC_ORACLE_E5M2 || fmt_b > DTC_ORACLE_E5M2 || block == 16) return -1;
+    return dtc_oracle_gemm_bs(fmt_a, fmt_b, DTC_ORACLE_SF_E8M0, block, A, B, sfA, sfB, M, N, K,
+                              C, S, nthreads);
+}
+
+int dtc_oracle_gemm_mx_sampled(int fmt_a, int fmt_b, int block, const uint8_t* A,
+                               const uint8_t* B, const uint8_t* sfA, const uint8_t* sfB, int64_t M,
+                               int64_t N, int64_t K, const int64_t* rows, const int64_t* cols,
+                               int64_t count, uint16_t* Cout, double* Sout) {
+    if (fmt_a > DTC_ORACLE_E5M2 || fmt_b > DTC_ORACLE_E5M2 || block == 16) return -1;
+    return dtc_oracle_gemm_bs_sampled(fmt_a, fmt_b, DTC_ORACLE_SF_E8M0, block, A, B, sfA, sfB, M,
+                                      N, K, rows, cols, count, Cout, Sout);
 }
 
 /* The pages' MXFP8 product: e4m3 x e4m3, scale blocks of 128. */

@@ -13,7 +13,7 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "dtc_oracle.c")
-PINS = ["tests/test_oracle_codecs.py", "tests/test_oracle_gemm.py"]
+PINS = ["tests/test_oracle_codecs.py", "tests/test_oracle_gemm.py", "tests/test_oracle_formats.py"]
 
 MUTANTS = {
     "nn_operand_read_as_nt": (
@@ -47,24 +47,49 @@ MUTANTS = {
         "v = ldexp((double)(8 + m), e - 9);",
     ),
     "scale_block_index_wrong": (
-        "out[r * K + k] = dec_fp8(fmt, X[r * K + k]) * dtc_oracle_dec_e8m0(sf[r * kb + k / block]);",
-        "out[r * K + k] = dec_fp8(fmt, X[r * K + k]) * dtc_oracle_dec_e8m0(sf[r * kb]);",
+        "dec_scale(sf_kind, sf[r * kb + k / block]);",
+        "dec_scale(sf_kind, sf[r * kb]);",
     ),
     "b_scaled_with_a_scales": (
-        "double* bt = decode_scaled(fmt_b, block, B, sfB, N, K);",
-        "double* bt = decode_scaled(fmt_b, block, B, sfA, N, K);",
+        "double* bt = decode_scaled(fmt_b, sf_kind, block, B, sfB, N, K);",
+        "double* bt = decode_scaled(fmt_b, sf_kind, block, B, sfA, N, K);",
     ),
     "e5m2_bias_off_by_one": (
         "v = ldexp((double)(4 + m), e - 17); /* (1 + m/4) * 2^(e-15) */",
         "v = ldexp((double)(4 + m), e - 16); /* (1 + m/4) * 2^(e-15) */",
     ),
     "b_decoded_with_a_format": (
-        "double* bt = decode_scaled(fmt_b, block, B, sfB, N, K);",
-        "double* bt = decode_scaled(fmt_a, block, B, sfB, N, K);",
+        "double* bt = decode_scaled(fmt_b, sf_kind, block, B, sfB, N, K);",
+        "double* bt = decode_scaled(fmt_a, sf_kind, block, B, sfB, N, K);",
     ),
     "scale_block_fixed_at_128": (
-        "int64_t kb = (K + block - 1) / block;\n    double* out",
-        "block = 128;\n    int64_t kb = (K + block - 1) / block;\n    double* out",
+        "int64_t kb = (K + block - 1) / block;\n    int64_t rb = row_bytes(fmt, K);",
+        "block = 128;\n    int64_t kb = (K + block - 1) / block;\n    int64_t rb = row_bytes(fmt, K);",
+    ),
+    "fp4_nibbles_swapped": (
+        "int shift = (int)(bit % 8);",
+        "int shift = bits == 4 ? 4 - (int)(bit % 8) : (int)(bit % 8);",
+    ),
+    "fp6_field_read_from_one_byte": (
+        "if (shift + bits > 8) v |= (unsigned)row[byte + 1] << 8; /* the field spans two bytes */",
+        "",
+    ),
+    "e2m3_bias_off_by_one": (
+        ": ldexp((double)(8 + m), e - 4);  /* (1 + m/8) * 2^(e-1) */",
+        ": ldexp((double)(8 + m), e - 3);  /* (1 + m/8) * 2^(e-1) */",
+    ),
+    "e3m2_subnormal_scale_wrong": (
+        "double v = e == 0 ? ldexp((double)m, -4)            /* subnormal: m/4 * 2^(1-3) */",
+        "double v = e == 0 ? ldexp((double)m, -3)            /* subnormal: m/4 * 2^(1-3) */",
+    ),
+    "e2m1_mantissa_ignored": (
+        ": ldexp((double)(2 + m), e - 2);  /* (1 + m/2) * 2^(e-1) */",
+        ": ldexp(2.0, e - 2);  /* (1 + m/2) * 2^(e-1) */",
+    ),
+    "ue4m3_sign_not_rejected": ("if (b & 0x80) return NAN;\n", ""),
+    "nvfp4_scales_read_as_e8m0": (
+        "return sf_kind == DTC_ORACLE_SF_UE4M3 ? dtc_oracle_dec_ue4m3(c) : dtc_oracle_dec_e8m0(c);",
+        "return dtc_oracle_dec_e8m0(c);",
     ),
     "f16_subnormal_scale_wrong": (
         "v = ldexp((double)m, -24); /* subnormal: m * 2^-10 * 2^-14 */",
