@@ -184,7 +184,8 @@ def _out(C, M, N, dtype, device, rows_of_larger=False):
     return C
 
 
-_MX_FORMATS = {"e4m3": 0, "e5m2": 1}
+_MX_FORMATS = {"e4m3": 0, "e5m2": 1, "e2m3": 2, "e3m2": 3, "e2m1": 4}
+_MX_BITS = {"e4m3": 8, "e5m2": 8, "e2m3": 6, "e3m2": 6, "e2m1": 4}
 
 
 def _options(variant, split_k, timeout_ns, fault_inject, tile_n=0, tile_k=0,
@@ -220,19 +221,30 @@ def gemm_f16(A, B, C=None, layout="NT", stream=None):
     return _gemm16("gemm_f16", torch.float16, A, B, C, layout, stream)
 
 
-def _check_mxfp8(A, B, sfA, sfB, rows_of_larger=False, scale_block=128):
+def _check_mxfp8(A, B, sfA, sfB, rows_of_larger=False, scale_block=128, a_format="e4m3",
+                 b_format="e4m3"):
+    """Shapes of a block-scaled call: A [M, row bytes] and B [N, row bytes] uint8 rows of element
+    codes (fp8: one byte each; fp6 / fp4: packed), scales [rows, ceil(K / scale_block)]."""
     _check_tensor(A, torch.uint8, "A", rows_of_larger)
     _check_tensor(B, torch.uint8, "B", rows_of_larger)
     _check_tensor(sfA, torch.uint8, "sfA")
     _check_tensor(sfB, torch.uint8, "sfB")
-    M, K = A.shape
-    N, Kb = B.shape
-    if Kb != K:
-        raise ValueError("A and B must both be [rows, K]")
+    M, a_bytes = A.shape
+    N, b_bytes = B.shape
+    K = a_bytes * 8 // _MX_BITS[a_format]
+    if a_bytes * 8 % _MX_BITS[a_format] or b_bytes * 8 != K * _MX_BITS[b_format]:
+        raise ValueError(f"rows of {a_bytes} ({a_format}) and {b_bytes} ({b_format}) bytes do "
+                         "not hold the same K")
     kb = (K + scale_block - 1) // scale_block
     if tuple(sfA.shape) != (M, kb) or tuple(sfB.shape) != (N, kb):
         raise ValueError(f"scales must be [M, {kb}] and [N, {kb}]")
     return M, N, K
+
+
+def _ld_elems(t, fmt):
+    """Leading dimension in elements of a uint8 tensor of packed rows (0 = dense)."""
+    ld = _ld(t)
+    return ld * 8 // _MX_BITS[fmt] if ld else 0
 
 
 def gemm_mxfp8(A, B, sfA, sfB, C=None, stream=None):
@@ -253,23 +265,27 @@ def gemm_ex(kind, A, B, C=None, layout="NT", sfA=None, sfB=None, variant=0, spli
     """Any of the three products with options (variant, split_k, wait limit, test hook). A, B
     and C may be rows of larger row-major arrays (e.g. ``big[:, :n]``); their row strides are
     passed as the leading dimensions. For the block-scaled product ("mxfp8") the element formats
-    of A and B ("e4m3" or "e5m2") and the scale block (128, the default, or 32) may be chosen.
+    of A and B ("e4m3", "e5m2", "e2m3", "e3m2" or "e2m1"; fp6 / fp4 rows packed, K inferred from
+    the row length) and the scale block (128, the default, or 32) may be chosen.
     `workspace` (a CUDA tensor of gemm_workspace_size bytes, zero-filled before its first use)
     lets the 16-bit products use stream-K; stream_k: 0 auto, 1 required, 2 off."""
     if workspace is not None and (not workspace.is_cuda or not workspace.is_contiguous()):
         raise ValueError("workspace must be a contiguous CUDA tensor")
     if kind == "mxfp8":
         M, N, K = _check_mxfp8(A, B, sfA, sfB, rows_of_larger=True,
-                               scale_block=scale_block or 128)
+                               scale_block=scale_block or 128, a_format=a_format,
+                               b_format=b_format)
         C = _out(C, M, N, torch.bfloat16, A.device, rows_of_larger=True)
+        lda, ldb = _ld_elems(A, a_format), _ld_elems(B, b_format)
     else:
         dt = torch.bfloat16 if kind == "bf16" else torch.float16
         _check_tensor(A, dt, "A", rows_of_larger=True)
         _check_tensor(B, dt, "B", rows_of_larger=True)
         M, N, K = _shapes16(A, B, layout)
         C = _out(C, M, N, dt, A.device, rows_of_larger=True)
+        lda, ldb = _ld(A), _ld(B)
     opts = _options(variant, split_k, timeout_ns, fault_inject, tile_n, tile_k,
-                    _ld(A), _ld(B), _ld(C), a_format, b_format, scale_block, workspace, stream_k)
+                    lda, ldb, _ld(C), a_format, b_format, scale_block, workspace, stream_k)
     dev = _same_device(A, B, C, sfA, sfB, workspace)
     with torch.cuda.device(dev):
         _check(lib().gemm_ex(_DTYPE[kind], _ptr(A), _ptr(B), _ptr(sfA), _ptr(sfB), _ptr(C), M, N,

@@ -16,6 +16,7 @@
 #include <cstring>
 
 #include "gemm16_splitk.cuh"
+#include "gemm_mxfp8_2cta.cuh"
 #include "host.h"
 
 namespace dtc_host {
@@ -168,6 +169,43 @@ int make_tmap_kchunks(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, co
     return GEMM_OK;
 }
 
+// Tensor map of a block-scaled operand stored as K-major rows of `bits`-bit elements (8: one byte
+// each; 6 or 4: packed, which the tensor memory access unit unpacks into 16-byte groups of 16
+// elements, 12 or 8 bytes of data then 4 or 8 bytes of padding: the layout the block-scaled MMA
+// reads for these types). A 128-element K-block takes one 128-byte swizzled row in shared memory
+// whatever the format. 2-D boxes {128, box_rows}, or with `deep` one 3-D box {128, box_rows, 2}
+// of two K-blocks (K % 128 == 0).
+int tmap_block_scaled(CUtensorMap* m, int bits, const void* ptr, uint64_t K, uint64_t rows,
+                      uint64_t row_bytes, uint32_t box_rows, bool deep, const char* name) {
+    auto fn = encode_fn();
+    if (!fn) return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
+    const CUtensorMapDataType dt = bits == 8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : bits == 6 ? CU_TENSOR_MAP_DATA_TYPE_16U6_ALIGN16B
+                                               : CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B;
+    CUresult r;
+    if (deep) {
+        cuuint64_t dims[3] = {128, rows, (K + 127) / 128};
+        cuuint64_t strides[2] = {row_bytes, (cuuint64_t)(128 * bits / 8)};
+        cuuint32_t box[3] = {128, box_rows, 2};
+        cuuint32_t estr[3] = {1, 1, 1};
+        r = fn(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        cuuint64_t dims[2] = {K, rows};
+        cuuint64_t strides[1] = {row_bytes};
+        cuuint32_t box[2] = {128, box_rows};
+        cuuint32_t estr[2] = {1, 1};
+        r = fn(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (r != CUDA_SUCCESS)
+        return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled(%s, %d-bit elements) failed with CUresult %d",
+                    name, bits, (int)r);
+    return GEMM_OK;
+}
+
 // Tensor map of a 16-bit operand with `mn` elements along M (or N) and K along the reduction:
 // MN-major storage [K, mn] -> 2-D boxes {64, kBK} (128-byte swizzle); K-major storage [mn, K] ->
 // one 3-D box {64, box_rows, 2} per 128-deep stage, or a 2-D box {64, box_rows} per 64-deep one.
@@ -216,6 +254,16 @@ dtc::Gemm16Args make_args(const Launch& L, int tile_m, int tile_n, int tile_k) {
     return a;
 }
 
+// Bits per element of a block-scaled element format (gemm_options.mx_a_format / mx_b_format).
+int mx_bits(int fmt) { return fmt <= 1 ? 8 : fmt <= 3 ? 6 : 4; }
+
+// Instruction-descriptor element format of kind::mxf8f6f4 for a gemm_options format: e4m3 0,
+// e5m2 1, e2m3 3, e3m2 4, e2m1 5 (the PTX ISA's table of the block-scaled kinds' atype / btype).
+uint32_t mx_format_code(int fmt) {
+    static const uint32_t kCode[5] = {0u, 1u, 3u, 4u, 5u};
+    return kCode[fmt];
+}
+
 dtc::GemmMxArgs mx_args(const Launch& L, int tile_m, int tile_n, int tile_k) {
     const gemm_options* o = L.o;
     dtc::GemmMxArgs a;
@@ -231,7 +279,11 @@ dtc::GemmMxArgs mx_args(const Launch& L, int tile_m, int tile_n, int tile_k) {
     a.num_kb = ceil_div(L.K, tile_k);
     const int block = (o && o->mx_scale_block) ? o->mx_scale_block : 128;
     a.sf_cols = ceil_div(L.K, block);
-    a.fmt_bits = o ? ((uint32_t)o->mx_a_format << 7) | ((uint32_t)o->mx_b_format << 10) : 0u;
+    a.fmt_bits = o ? (mx_format_code(o->mx_a_format) << 7) | (mx_format_code(o->mx_b_format) << 10) : 0u;
+    // one stage's copies: tile_k K-elements of tile_m rows of A and tile_n rows of B, counted as
+    // the bytes the tensor memory access unit writes (packed data only for fp6 / fp4)
+    const int a_bits = mx_bits(o ? o->mx_a_format : 0), b_bits = mx_bits(o ? o->mx_b_format : 0);
+    a.stage_tx = (uint32_t)((int64_t)tile_k * (tile_m * a_bits + tile_n * b_bits) / 8);
     a.timeout_ns = (o && o->timeout_ns) ? o->timeout_ns : kDefaultTimeoutNs;
     a.fault = o ? o->fault_inject : 0;
     a.status = L.dev->status;
@@ -262,8 +314,8 @@ int check_shape(int dtype, int64_t M, int64_t N, int64_t K, int layout, const ge
         return fail(GEMM_ERR_INVALID_ARG, "unknown variant %d", o->variant);
     if (o && o->split_k < 0) return fail(GEMM_ERR_INVALID_ARG, "split_k must be >= 0");
     if (o && o->tile_n < 0) return fail(GEMM_ERR_INVALID_ARG, "tile_n must be >= 0");
-    if (o && (o->mx_a_format < 0 || o->mx_a_format > 1 || o->mx_b_format < 0 || o->mx_b_format > 1))
-        return fail(GEMM_ERR_INVALID_ARG, "mx formats must be 0 (e4m3) or 1 (e5m2)");
+    if (o && (o->mx_a_format < 0 || o->mx_a_format > 4 || o->mx_b_format < 0 || o->mx_b_format > 4))
+        return fail(GEMM_ERR_INVALID_ARG, "mx formats must be 0 (e4m3), 1 (e5m2), 2 (e2m3), 3 (e3m2) or 4 (e2m1)");
     if (o && o->mx_scale_block != 0 && o->mx_scale_block != 32 && o->mx_scale_block != 128)
         return fail(GEMM_ERR_INVALID_ARG, "mx_scale_block %d is not 32 or 128", o->mx_scale_block);
     if (dtype != 2 && o && (o->mx_a_format || o->mx_b_format || o->mx_scale_block))
@@ -285,7 +337,11 @@ int validate(int dtype, const void* A, const void* B, const void* sfA, const voi
         return fail(GEMM_ERR_INVALID_ARG, "lda, ldb and ldc must be >= 0");
     if (o && o->workspace && !aligned16(o->workspace))
         return fail(GEMM_ERR_INVALID_ARG, "the workspace is not 16-byte aligned");
-    const int eb = dtype == 2 ? 1 : 2;  // operand element bytes
+    // operand element bits; the sub-byte block-scaled formats are packed rows, read by the tensor
+    // memory access unit's packed types (rows of a multiple of 128 elements and 32 bytes, 32-byte
+    // aligned base)
+    const int a_bits = dtype == 2 ? mx_bits(o ? o->mx_a_format : 0) : 16;
+    const int b_bits = dtype == 2 ? mx_bits(o ? o->mx_b_format : 0) : 16;
     ops->A = A;
     ops->B = B;
     ops->sfA = sfA;
@@ -314,10 +370,19 @@ int validate(int dtype, const void* A, const void* B, const void* sfA, const voi
     if (!A || !B) return fail(GEMM_ERR_INVALID_ARG, "A or B is NULL");
     if (!aligned16(A) || !aligned16(B)) return fail(GEMM_ERR_INVALID_ARG, "A or B is not 16-byte aligned");
     if (dtype == 2 && (!sfA || !sfB)) return fail(GEMM_ERR_INVALID_ARG, "sfA or sfB is NULL");
-    if ((ops->lda * eb) % 16)
+    const int64_t a_row = ops->lda * a_bits, b_row = ops->ldb * b_bits;  // bits between rows
+    if (a_row % 128)
         return fail(GEMM_ERR_INVALID_ARG, "lda=%lld: rows of A must start 16 bytes apart", (long long)ops->lda);
-    if ((ops->ldb * eb) % 16)
+    if (b_row % 128)
         return fail(GEMM_ERR_INVALID_ARG, "ldb=%lld: rows of B must start 16 bytes apart", (long long)ops->ldb);
+    if (a_bits < 8 || b_bits < 8) {
+        if (K % 128)
+            return fail(GEMM_ERR_INVALID_ARG, "K=%lld: the fp6/fp4 formats need K %% 128 == 0", (long long)K);
+        if ((a_bits < 8 && (a_row % 256 || (reinterpret_cast<uintptr_t>(A) & 31))) ||
+            (b_bits < 8 && (b_row % 256 || (reinterpret_cast<uintptr_t>(B) & 31))))
+            return fail(GEMM_ERR_INVALID_ARG, "fp6/fp4 operands need a 32-byte aligned base and rows "
+                        "32 bytes apart");
+    }
     return GEMM_OK;
 }
 
@@ -450,25 +515,26 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
     if (dtype == 2) {
         if (v != GEMM_VARIANT_AUTO && v != GEMM_VARIANT_1CTA && v != GEMM_VARIANT_2CTA)
             return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 product has one-CTA and pair kernels");
-        if (want_n && want_n != dtc::gmx::kBN)
-            return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 kernels use 224-wide tiles");
-        if (v == GEMM_VARIANT_2CTA && K % 128)
-            return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 pair kernel needs K %% 128 == 0");
-        const bool mx_default = !o || (o->mx_a_format == 0 && o->mx_b_format == 0 &&
-                                       (o->mx_scale_block == 0 || o->mx_scale_block == 128));
-        if (v == GEMM_VARIANT_2CTA && !mx_default)
-            return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 pair kernel takes e4m3 with 128-element scale blocks only");
-        // The pair kernel is correct but measured slower than the one-CTA kernel on GB300
-        // (2008 vs 2357 TFLOP/s on 4096 x 4096 x 8192): it is an option, never chosen here.
+        if (want_n && want_n != 224 && !(want_n == 256 && v == GEMM_VARIANT_2CTA))
+            return fail(GEMM_ERR_UNSUPPORTED, "the block-scaled kernels use 224-wide tiles (256 "
+                        "on CTA pairs)");
+        // The one-CTA kernel (128 x 224 tiles, 2 stages of 256 K-elements or 4 of 128) or the
+        // pair kernel (256 x 224 or 256 x 256 tiles, 6 stages of 128 K-elements per CTA). The
+        // pair kernel is correct for every format but measured slower on GB300 (4096 x 4096 x
+        // 8192 e4m3: 137 us against 111; 256-wide pair tiles 139 us): AUTO takes the one-CTA
+        // kernel.
         if (v == GEMM_VARIANT_AUTO) v = GEMM_VARIANT_1CTA;
         if (v == GEMM_VARIANT_2CTA) {
+            const int bk_want = o ? o->tile_k : 0;
+            if (bk_want && bk_want != 128)
+                return fail(GEMM_ERR_INVALID_ARG, "tile_k %d is not 128 for the block-scaled pair kernel", bk_want);
             p->variant = v;
             p->cluster = 2;
             p->tile_m = 256;
-            p->tile_n = 224;
-            p->tile_k = 256;
-            p->stages = 3;
-            p->tiles = ceil_div(M, 256) * ceil_div(N, 224);
+            p->tile_n = want_n ? want_n : dtc::gmx2::kBN;
+            p->tile_k = dtc::gmx2::kBK;
+            p->stages = dtc::gmx2::kStages;
+            p->tiles = ceil_div(M, 256) * ceil_div(N, p->tile_n);
             p->ctas = 2 * std::min(p->tiles, pairs);
             return GEMM_OK;
         }

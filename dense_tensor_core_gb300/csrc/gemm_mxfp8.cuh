@@ -45,6 +45,8 @@ struct GemmMxArgs {
     int num_m, num_n, num_kb;  // num_kb: 128-element K-blocks
     int sf_cols;               // bytes per scale row: ceil(K / scale block)
     uint32_t fmt_bits;         // instruction-descriptor element formats of A (bits 7-9), B (10-12)
+    uint32_t stage_tx;         // bytes one stage's copies write (fp6 / fp4: the packed data only;
+                               // the padding of each 16-byte group is not written)
     uint64_t timeout_ns;
     int fault;
     int* status;  // device status word: the first wait that gives up records its site here
@@ -178,7 +180,7 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
                     }
                     if (args.fault == 1 && it == 0) continue;  // test hook: stage never filled
                     const uint32_t full = smem_u32(&bar_full[s]);
-                    mbar_arrive_expect_tx(full, C_::kStageBytes);
+                    mbar_arrive_expect_tx(full, args.stage_tx);
                     if constexpr (kDeep) {
                         tma_load_3d(sA + s * kAStage, &tmA, full, 0, mt * kBM, st * 2);
                         tma_load_3d(sB + s * kBStage, &tmB, full, 0, nt * kBN, st * 2);

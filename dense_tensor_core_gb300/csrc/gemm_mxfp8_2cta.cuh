@@ -1,21 +1,29 @@
-// gemm_mxfp8_2cta.cuh -- persistent MXFP8 block-scaled GEMM on CTA pairs (cluster 2x1,
-// tcgen05 cta_group::2), NT layout, e4m3 x e4m3 with one E8M0 scale per row per 128 K-elements
-// for A and B, fp32 accumulation in Tensor Memory, bf16 output.
+// gemm_mxfp8_2cta.cuh -- persistent block-scaled GEMM on CTA pairs (cluster 2x1, tcgen05
+// cta_group::2), NT layout: fp8 / fp6 / fp4 elements (e4m3, e5m2, e2m3, e3m2, e2m1 for A and B
+// independently) with one E8M0 scale per row per 128 K-elements (kB32: per 32), fp32 accumulation
+// in Tensor Memory, bf16 output.
 //
 // The product of gemm_mxfp8.cuh (05 Blackwell TCGEN05 GEMM tutorial, "Advanced": gemm_blockscaled
-// with granularity 128 for both operands), on the tile shape and load pattern that feed the tensor
-// pipe best on GB300 (see gemm16_2cta.cuh): a pair computes a 256 x 224 tile; CTA r loads its own
-// 128 rows of A and its own 112 rows of B^T, each stage 256 K-elements deep (two 128-byte K-chunks
-// per row, one 3-D TMA box per operand), both CTAs' copies completing on the leader's full
-// barrier; the leader issues tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X
-// (M = 256, N = 224, K = 32), eight per stage, the four of each 128-deep half sharing its scales.
+// with granularity 128 for both operands, and "other block-scaled formats"), on the operand feed
+// that keeps the tensor pipe busy on GB300: a pair computes a 256 x 224 tile; CTA r loads its own
+// 128 rows of A and its own 112 rows of B^T, 128 K-elements per stage (one 128-byte swizzled row
+// per operand row, whatever the element format: fp6 / fp4 rows are unpacked by the tensor memory
+// access unit into 16-byte groups), in a ring of 6 stages of 30 KB per CTA. At the fp8 rate a
+// stage is 448 tensor cycles of work, so five stages in flight cover ~2200 cycles of load latency
+// (a ring of three 60 KB stages covered half that, and the kernel waited for its operands). Both
+// CTAs' copies complete on the leader's full barrier; the leader's single MMA thread issues
+// tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X (M = 256, N = 224, K = 32),
+// four per stage, with descriptors advanced by 32-bit adds, and releases each stage in both CTAs
+// with one multicast commit.
 //
-// Scales: as in the one-CTA kernel, R rows take R/32 Tensor Memory columns (row r in lane r % 32
-// of column r / 32, repeated in all four lane quarters), 4 consecutive 128-blocks packed per cell
-// and selected by the instruction's a_sf_id / b_sf_id. Each CTA holds the scales of its own 128 A
-// rows and of all 224 B rows (each CTA's datapath computes all 224 columns of its rows); its four
-// scale warps write them with tcgen05.st and arrive on the leader's scale-full barrier (8 arrivals
-// per set), and the leader's MMA thread releases a set to both CTAs with one commit each.
+// Scales, as in the one-CTA kernel: R rows take R/32 Tensor Memory columns (row r in lane r % 32
+// of column r / 32, repeated in all four lane quarters); one 32-bit cell packs 4 scale bytes of a
+// row (4 consecutive 128-element K-blocks, selected by a_sf_id / b_sf_id = K-block % 4; with
+// 32-element blocks the 4 blocks of one K-block, selected per MMA). Each CTA holds the scales of
+// its own 128 A rows and of all 224 B rows (each CTA's datapath computes all 224 columns of its
+// rows); its four scale warps write them with tcgen05.st and arrive on the leader's scale-full
+// barrier (8 arrivals per set), and the leader's MMA thread releases a set in both CTAs with one
+// multicast commit.
 //
 // Tensor Memory per CTA: accumulators at columns [0,224) and [224,448), scale sets at
 // 448 + 12*set (4 columns for A, 8 for B), set = 0..3.
@@ -26,43 +34,59 @@
 namespace dtc {
 
 namespace gmx2 {
-constexpr int kBMc = 128;  // rows of C per CTA
-constexpr int kBN = 224;   // columns of C per pair tile
-constexpr int kHalfN = kBN / 2;
-constexpr int kBK = 256;   // e4m3 elements per stage: two 128-byte K-chunks
-constexpr int kStages = 3;
+constexpr int kBMc = 128;   // rows of C per CTA
+constexpr int kBK = 128;    // K-elements per stage: one 128-byte swizzled row per operand row
+constexpr int kStages = 6;
 constexpr int kThreads = 320;
-constexpr int kAStage = kBMc * kBK;
-constexpr int kBStage = kHalfN * kBK;
-constexpr int kStageBytes = kAStage + kBStage;
-static_assert(kStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+constexpr int kAStage = kBMc * 128;
 constexpr int kCBytes = 4 * 2 * 4096;  // two 4 KB output staging slots per epilogue warp
-constexpr int kSmemBytes = kStages * kStageBytes + kCBytes + 1024;
 constexpr int kTmemCols = 512;
-constexpr int kAccStride = 224;
-constexpr int kSfBase = 448;
 constexpr int kSfSet = 12;
 constexpr int kSfSets = 4;
-constexpr int kGroup = 4;  // 128-blocks per scale set
 constexpr int kGroupM = 8;
 constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
 constexpr uint64_t kPeerSettleNs = 1000ull * 1000;
-static_assert(kSmemBytes <= 227 * 1024 - 512, "shared memory budget");
-static_assert(kSfBase + kSfSets * kSfSet <= kTmemCols, "Tensor Memory budget");
+
+// Pair tile width kBN (224 or 256). Tensor Memory holds the accumulators and 4 scale sets: two
+// 224-column accumulators (448 + 48 <= 512 columns), or one 256-column accumulator (the epilogue of
+// a tile then finishes before the next tile's first MMA).
+template <int kBN>
+struct Cfg {
+    static constexpr int kHalfN = kBN / 2;
+    static constexpr int kBStage = kHalfN * 128;
+    static constexpr int kStageBytes = kAStage + kBStage;
+    static constexpr int kAccBufs = kBN == 256 ? 1 : 2;
+    static constexpr int kAccStride = kBN;
+    static constexpr int kSfBase = kAccBufs * kBN;
+    static constexpr int kSmemBytes = kStages * kStageBytes + kCBytes + 1024;
+    static_assert(kBN == 224 || kBN == 256, "pair tiles 224 or 256 wide");
+    static_assert(kAStage % 1024 == 0 && kBStage % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+    static_assert(kSmemBytes <= 227 * 1024 - 512, "shared memory budget");
+    static_assert(kSfBase + kSfSets * kSfSet <= kTmemCols, "Tensor Memory budget");
+};
+constexpr int kBN = 224;  // the default pair tile width
 }  // namespace gmx2
 
-template <int kUnused = 0>
+template <bool kB32, int kBN>
 __global__ void __launch_bounds__(gmx2::kThreads, 1)
     gemm_mxfp8_2cta_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmC,
                            const __grid_constant__ CUtensorMap tmC32, const GemmMxArgs args) {
     using namespace gmx2;
+    using C_ = Cfg<kBN>;
+    constexpr int kHalfN = C_::kHalfN;
+    constexpr int kBStage = C_::kBStage;
+    constexpr int kStageBytes = C_::kStageBytes;
+    constexpr int kAccBufs = C_::kAccBufs;
+    constexpr int kAccStride = C_::kAccStride;
+    constexpr int kSfBase = C_::kSfBase;
+    constexpr int grp = kB32 ? 1 : 4;  // K-blocks per scale set
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[kStages];
     __shared__ __align__(8) uint64_t bar_empty[kStages];
-    __shared__ __align__(8) uint64_t bar_tfull[2];
-    __shared__ __align__(8) uint64_t bar_tempty[2];
+    __shared__ __align__(8) uint64_t bar_tfull[kAccBufs];
+    __shared__ __align__(8) uint64_t bar_tempty[kAccBufs];
     __shared__ __align__(8) uint64_t bar_sfull[kSfSets];
     __shared__ __align__(8) uint64_t bar_sempty[kSfSets];
     __shared__ __align__(8) uint64_t bar_drain;
@@ -79,8 +103,7 @@ __global__ void __launch_bounds__(gmx2::kThreads, 1)
     const int pair = blockIdx.x >> 1;
     const int num_pairs = gridDim.x >> 1;
     const int total = args.num_m * args.num_n;  // num_m counts 256-row pair tiles
-    const int nk128 = 2 * args.num_kb;          // 128-blocks per tile (the last may be padding)
-    const int groups = (nk128 + kGroup - 1) / kGroup;
+    const int groups = (args.num_kb + grp - 1) / grp;  // scale sets per tile
     volatile int* abort = &abort_flag;
 
     if (threadIdx.x == 0) {
@@ -88,7 +111,7 @@ __global__ void __launch_bounds__(gmx2::kThreads, 1)
             mbar_init(smem_u32(&bar_full[s]), 1);
             mbar_init(smem_u32(&bar_empty[s]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kAccBufs; ++b) {
             mbar_init(smem_u32(&bar_tfull[b]), 1);
             mbar_init(smem_u32(&bar_tempty[b]), 8);  // 4 epilogue warps in each CTA
         }
@@ -104,6 +127,7 @@ __global__ void __launch_bounds__(gmx2::kThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmC);
     }
     if (warp == 1) {
         tmem_alloc<2>(smem_u32(&tmem_slot), kTmemCols);
@@ -111,7 +135,7 @@ __global__ void __launch_bounds__(gmx2::kThreads, 1)
     }
     tc_fence_before_sync();
     __syncthreads();
-    cluster_sync();
+    cluster_sync();  // both CTAs' barriers exist before any copy or arrival targets them
     tc_fence_after_sync();
     const uint32_t tmem_base = tmem_slot;
 
@@ -135,18 +159,21 @@ __global__ void __launch_bounds__(gmx2::kThreads, 1)
                     if (args.fault == 1 && it == 0) continue;  // test hook: stage never filled
                     const uint32_t full_local = smem_u32(&bar_full[s]);
                     const uint32_t full_leader = map_to_cta(full_local, 0);
-                    if (leader) mbar_arrive_expect_tx(full_local, 2 * kStageBytes);
-                    tma_load_3d_pair(sA + s * kAStage, &tmA, full_leader, 0, a_row, kb * 2);
-                    tma_load_3d_pair(sB + s * kBStage, &tmB, full_leader, 0, b_row, kb * 2);
+                    if (leader) mbar_arrive_expect_tx(full_local, args.stage_tx);  // both CTAs' bytes
+                    tma_load_2d_pair(sA + s * kAStage, &tmA, full_leader, kb * kBK, a_row);
+                    tma_load_2d_pair(sB + s * kBStage, &tmB, full_leader, kb * kBK, b_row);
                 }
             }
             if (!ok && leader) {
+                // The leader's full barriers count both CTAs' copies: let those in flight land.
                 const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0;
                 for (uint32_t i = first; i < it; ++i) {
                     if (args.fault == 1 && i == 0) continue;
                     wait_drain(smem_u32(&bar_full[i % kStages]), (i / kStages) & 1u, kDrainNs);
                 }
             } else if (!ok) {
+                // The peer's copies complete on the leader's barriers, which it cannot observe:
+                // give them a fixed, bounded time to land before this CTA may exit.
                 const uint64_t t0 = globaltimer_ns();
                 while (globaltimer_ns() - t0 < kPeerSettleNs) __nanosleep(1000);
             }
@@ -154,69 +181,64 @@ __global__ void __launch_bounds__(gmx2::kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------ MMA issuer (leader CTA) ------------------------------
         if (lane == 0 && leader) {
-            constexpr uint32_t idesc0 = idesc_mxf8(256, kBN, 0, 0);
-            uint32_t it = 0, acc = 0, sit = 0;
+            const uint32_t idesc0 = idesc_mxf8(256, kBN, 0, 0) | args.fmt_bits;
+            // Operand descriptors: only the start-address field (bits 0-13: address >> 4) changes,
+            // by fixed offsets per stage and per K-step (32 bytes), so it is built once and
+            // advanced with 32-bit adds (shared addresses stay below 256 KB: no carry out).
+            const uint64_t a_desc0 = smem_desc_sw128(sA, 16, 1024);
+            const uint64_t b_desc0 = smem_desc_sw128(sB, 16, 1024);
+            const uint32_t a_hi = (uint32_t)(a_desc0 >> 32), b_hi = (uint32_t)(b_desc0 >> 32);
+            uint32_t s = 0, ph = 0, acc = 0, sit = 0;
             bool ok = true, issued = false;
             for (int t = pair; t < total && ok; t += num_pairs) {
-                const uint32_t b = acc & 1u, aph = (acc >> 1) & 1u;
-                if (!wait_bounded(smem_u32(&bar_tempty[b]), aph ^ 1u, abort, args.timeout_ns,
-                                  args.status, 42)) {
+                const uint32_t b = acc % kAccBufs, aph = (acc / kAccBufs) & 1u;
+                if (!wait_bounded<true>(smem_u32(&bar_tempty[b]), aph ^ 1u, abort, args.timeout_ns,
+                                        args.status, 42)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * kAccStride;
-                for (int kb = 0; kb < args.num_kb && ok; ++kb, ++it) {
-                    const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+                for (int kb = 0; kb < args.num_kb; ++kb) {
+                    const uint32_t set = sit % kSfSets;
+                    if (kb % grp == 0) {  // the first K-block of a scale set
+                        if (!wait_bounded<true>(smem_u32(&bar_sfull[set]), (sit / kSfSets) & 1u,
+                                                abort, args.timeout_ns, args.status, 45)) {
+                            ok = false;
+                            break;
+                        }
+                    }
                     if (!wait_bounded(smem_u32(&bar_full[s]), ph, abort, args.timeout_ns,
                                       args.status, 43)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t a0 = sA + s * kAStage, b0 = sB + s * kBStage;
-#pragma unroll 1
-                    for (int ch = 0; ch < 2; ++ch) {
-                        const int k128 = 2 * kb + ch;
-                        const uint32_t set = sit % kSfSets;
-                        if (k128 % kGroup == 0) {
-                            if (!wait_bounded(smem_u32(&bar_sfull[set]), (sit / kSfSets) & 1u,
-                                              abort, args.timeout_ns, args.status, 45)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after_sync();
-                        }
-                        const uint32_t sf_id = (uint32_t)(k128 % kGroup);
-                        const uint32_t idesc = idesc0 | (sf_id << 4) | (sf_id << 29);
-                        const uint32_t sfa = tmem_base + kSfBase + set * kSfSet;
-                        const uint32_t sfb = sfa + 4;
+                    const uint32_t a_lo = (uint32_t)a_desc0 + s * (uint32_t)(kAStage >> 4);
+                    const uint32_t b_lo = (uint32_t)b_desc0 + s * (uint32_t)(kBStage >> 4);
+                    const uint32_t sfa = tmem_base + kSfBase + set * kSfSet;
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t adesc =
-                                smem_desc_sw128(a0 + ch * (kBMc * 128) + kk * 32, 16, 1024);
-                            const uint64_t bdesc =
-                                smem_desc_sw128(b0 + ch * (kHalfN * 128) + kk * 32, 16, 1024);
-                            mma_mxf8_cta2(d_tmem, adesc, bdesc, idesc, sfa, sfb,
-                                          (kb | ch | kk) != 0 ? 1u : 0u);
-                        }
-                        issued = true;
-                        if (k128 % kGroup == kGroup - 1 || k128 == nk128 - 1) {
-                            const uint32_t e = smem_u32(&bar_sempty[set]);
-                            mma_commit_cta2(e);
-                            mma_commit_cta2(map_to_cta(e, 1));
-                            ++sit;
-                        }
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t sf_id = kB32 ? (uint32_t)kk : (uint32_t)(kb & 3);
+                        const uint32_t idesc = idesc0 | (sf_id << 4) | (sf_id << 29);
+                        const uint64_t adesc = ((uint64_t)a_hi << 32) | (a_lo + 2u * kk);
+                        const uint64_t bdesc = ((uint64_t)b_hi << 32) | (b_lo + 2u * kk);
+                        mma_mxf8_cta2(d_tmem, adesc, bdesc, idesc, sfa, sfa + 4,
+                                      (kb | kk) != 0 ? 1u : 0u);
                     }
-                    if (!ok) break;
-                    const uint32_t e = smem_u32(&bar_empty[s]);
-                    mma_commit_cta2(e);
-                    mma_commit_cta2(map_to_cta(e, 1));
+                    issued = true;
+                    mma_commit_cta2_both(smem_u32(&bar_empty[s]));  // stage free in both CTAs
+                    if (kb % grp == grp - 1 || kb == args.num_kb - 1) {
+                        mma_commit_cta2_both(smem_u32(&bar_sempty[set]));  // scale set consumed
+                        ++sit;
+                    }
+                    if (++s == (uint32_t)kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
                 if (!ok) break;
-                const uint32_t f = smem_u32(&bar_tfull[b]);
-                mma_commit_cta2(f);
-                mma_commit_cta2(map_to_cta(f, 1));
+                mma_commit_cta2_both(smem_u32(&bar_tfull[b]));
                 ++acc;
             }
             if (!ok && issued) {
@@ -232,11 +254,11 @@ __global__ void __launch_bounds__(gmx2::kThreads, 1)
         for (int t = pair; t < total; t += num_pairs, ++acc) {
             int mt, nt;
             tile_coords(t, args.num_m, args.num_n, kGroupM, mt, nt);
-            const uint32_t b = acc & 1u, aph = (acc >> 1) & 1u;
+            const uint32_t b = acc % kAccBufs, aph = (acc / kAccBufs) & 1u;
             int ok = 1;
             if (lane == 0)
-                ok = wait_bounded(smem_u32(&bar_tfull[b]), aph, abort, args.timeout_ns,
-                                  args.status, 44);
+                ok = wait_bounded<false, true>(smem_u32(&bar_tfull[b]), aph, abort,
+                                               args.timeout_ns, args.status, 44);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after_sync();
@@ -254,6 +276,8 @@ __global__ void __launch_bounds__(gmx2::kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------ scale writers (warps 6..9, both CTAs) ----------------
+        // The (tile, group) sequence of this pair, flattened so the gather of the next group
+        // (possibly of the next tile) is in flight while the current one waits for a free set.
         const int q = warp & 3;
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
         const int my_tiles = pair < total ? (total - 1 - pair) / num_pairs + 1 : 0;
@@ -283,8 +307,9 @@ __global__ void __launch_bounds__(gmx2::kThreads, 1)
             const uint32_t set = sit % kSfSets;
             int w_ok = 1;
             if (lane == 0)
-                w_ok = wait_bounded(smem_u32(&bar_sempty[set]), ((sit / kSfSets) & 1u) ^ 1u, abort,
-                                    args.timeout_ns, args.status, 46);
+                w_ok = wait_bounded<false, true>(smem_u32(&bar_sempty[set]),
+                                                 ((sit / kSfSets) & 1u) ^ 1u, abort,
+                                                 args.timeout_ns, args.status, 46);
             w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
             if (!w_ok) break;
             tc_fence_after_sync();
@@ -307,7 +332,7 @@ __global__ void __launch_bounds__(gmx2::kThreads, 1)
     // ------------------------------ teardown ------------------------------
     tc_fence_before_sync();
     __syncthreads();
-    cluster_sync();
+    cluster_sync();  // no CTA leaves while its peer may still signal its barriers
     if (warp == 1) {
         __syncwarp();
         tc_fence_after_sync();

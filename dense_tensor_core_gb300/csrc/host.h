@@ -87,6 +87,9 @@ int make_tmap(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void
               CUtensorMapSwizzle swz, const char* name);
 int make_tmap_kchunks(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* ptr,
                       uint64_t K, uint64_t rows, uint64_t ld, uint32_t box_rows, const char* name);
+int tmap_block_scaled(CUtensorMap* m, int bits, const void* ptr, uint64_t K, uint64_t rows,
+                      uint64_t row_bytes, uint32_t box_rows, bool deep, const char* name);
+int mx_bits(int fmt);
 int tmap_operand16(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, int64_t ld,
                    bool mn_major, int64_t mn, int64_t K, int kBK, uint32_t box_rows,
                    const char* name);

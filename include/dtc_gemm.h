@@ -68,8 +68,9 @@ typedef enum {
     GEMM_VARIANT_AUTO = 0,
     GEMM_VARIANT_1CTA = 1,   /* persistent 128 x 256 or 128 x 224 tiles, one CTA per tile */
     GEMM_VARIANT_2CTA = 2,   /* persistent 256 x 256 or 256 x 224 tiles on a CTA pair
-                                (cluster 2x1, tcgen05 cta_group::2); for MXFP8 (256 x 224,
-                                K % 128 == 0) an option that is never chosen automatically */
+                                (cluster 2x1, tcgen05 cta_group::2); for the block-scaled
+                                product (256 x 224, or 256 x 256 with tile_n = 256) an option
+                                that is never chosen automatically */
     GEMM_VARIANT_SPLITK = 3  /* 128 x 128 tiles with K split over a cluster of 2 or 4 CTAs, or
                                 128 x 256 tiles split over 2; each CTA copies the partial sums
                                 of the rows another CTA owns into that CTA's shared memory, and
@@ -85,16 +86,24 @@ typedef struct {
                              stage, so the consumer's bounded wait runs out and the call reports
                              GEMM_ERR_TIMEOUT through gemm_stream_status. */
     int tile_n;           /* force the N-tile: 256, 224 (not SPLITK; one-CTA tiles need B stored
-                             [N,K]) or 128 (SPLITK only); 0 = choose */
+                             [N,K]; block-scaled: 224, or 256 on CTA pairs) or 128 (SPLITK only);
+                             0 = choose */
     int tile_k;           /* K-elements per pipeline stage: 64 (1CTA), 64 or 128 (2CTA; SPLITK
                              with 128-wide tiles; 128 needs K % 64 == 0), 128 or 256 (block-scaled
-                             one-CTA kernel; 256 needs K % 128 == 0); 0 = choose */
+                             one-CTA kernel; 256 needs K % 128 == 0), 128 (block-scaled pair
+                             kernel); 0 = choose */
     int64_t lda;          /* elements between consecutive stored rows of A, B, C; 0 = dense (the */
     int64_t ldb;          /* row length: K or M for A, K or N for B, N for C). At least the row */
     int64_t ldc;          /* length, and rows must start 16 bytes apart (ld x element size %
                              16 == 0). Only the M x N region of C is written. */
-    int mx_a_format;      /* block-scaled product only: element format of A, 0 = e4m3 (OCP FP8 */
-    int mx_b_format;      /* E4M3, the default), 1 = e5m2 (OCP FP8 E5M2); likewise B */
+    int mx_a_format;      /* block-scaled product only: element format of A: 0 = e4m3 (OCP FP8 */
+    int mx_b_format;      /* E4M3, the default), 1 = e5m2 (OCP FP8 E5M2), 2 = e2m3 and 3 = e3m2
+                             (OCP MX FP6), 4 = e2m1 (OCP MX FP4); likewise B. FP6 and FP4 rows
+                             are packed: element k of a row is the 6- or 4-bit field at bit 6k or
+                             4k of the row read as a little-endian bit stream (fp4: byte k/2, low
+                             nibble for even k; fp6: 4 elements in 3 bytes). With an FP6 or FP4
+                             operand K % 128 == 0, and that operand's base is 32-byte aligned
+                             and its rows start a multiple of 32 bytes apart. */
     int mx_scale_block;   /* block-scaled product only: K-elements per E8M0 scale, 128 (0 = the
                              default, the pages' granularity) or 32 (the OCP MX block); the
                              scale arrays are then [rows, ceil(K / block)]. Non-default formats

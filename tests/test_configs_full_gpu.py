@@ -57,6 +57,6 @@ def test_block_scaled_workload_every_element(name):
                     sfB=to_device8(sfB), a_format=w.a_fmt, b_format=w.b_fmt, scale_block=w.block)
     dtc.gemm_stream_status()
     C = C.view(torch.int16).cpu().numpy().view(np.uint16)
-    ref = oracle.gemm_mx(A, B, sfA, sfB, w.M, w.N, w.K, a_fmt=w.a_fmt, b_fmt=w.b_fmt,
+    ref = oracle.gemm_bs(A, B, sfA, sfB, w.M, w.N, w.K, a_fmt=w.a_fmt, b_fmt=w.b_fmt,
                          block=w.block)
     check_close(values16(C, "bf16"), values16(ref, "bf16"), f"{name}, every element")

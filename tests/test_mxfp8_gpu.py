@@ -178,8 +178,9 @@ def test_automatic_choice():
     assert (p["variant"], p["tile_k"]) == (1, 256)
     assert dtc.gemm_plan("mxfp8", 4096, 4096, 8208)["tile_k"] == 128
     assert dtc.gemm_plan("mxfp8", 4096, 4096, 8192, variant=2)["variant"] == 2
-    with pytest.raises(dtc.GemmError):
-        dtc.gemm_plan("mxfp8", 4096, 4096, 8208, variant=2)  # the pair kernel needs K % 128 == 0
+    # the pair kernel's 128-deep stages are 2-D boxes: any K with 16-byte rows
+    p = dtc.gemm_plan("mxfp8", 4096, 4096, 8208, variant=2)
+    assert (p["variant"], p["tile_k"], p["stages"]) == (2, 128, 6)
 
 
 # --- other block-scaled formats: e5m2 elements, 32-element (OCP MX) scale blocks ---------------
@@ -188,17 +189,17 @@ def run_mx_fmt(A, B, sfA, sfB, a_fmt, b_fmt, block, **kw):
     return run_mx(A, B, sfA, sfB, a_format=a_fmt, b_format=b_fmt, scale_block=block, **kw)
 
 
-@pytest.mark.parametrize("tile_k", [128, 256])
+@pytest.mark.parametrize("variant,tile_k", [(1, 128), (1, 256), (2, 0)])
 @pytest.mark.parametrize("block", [32, 128])
 @pytest.mark.parametrize("a_fmt,b_fmt", [("e5m2", "e5m2"), ("e4m3", "e5m2"), ("e5m2", "e4m3"),
                                          ("e4m3", "e4m3")])
 @pytest.mark.parametrize("M,N,K", [(256, 448, 1024), (300, 520, 400), (129, 232, 656),
                                    (256, 224, 384)])
-def test_formats_and_blocks_full_parity(M, N, K, a_fmt, b_fmt, block, tile_k):
+def test_formats_and_blocks_full_parity(M, N, K, a_fmt, b_fmt, block, variant, tile_k):
     if tile_k == 256 and K % 128:
         pytest.skip("256-deep stages need K % 128 == 0")
     A, B, sfA, sfB = workloads.make_mx(M, N, K, M + N + K + block, a_fmt, b_fmt, block)
-    C = run_mx_fmt(A, B, sfA, sfB, a_fmt, b_fmt, block, variant=1, tile_k=tile_k)
+    C = run_mx_fmt(A, B, sfA, sfB, a_fmt, b_fmt, block, variant=variant, tile_k=tile_k)
     ref = oracle.gemm_mx(A, B, sfA, sfB, M, N, K, a_fmt=a_fmt, b_fmt=b_fmt, block=block)
     check_close(values16(C, "bf16"), values16(ref, "bf16"),
                 f"{a_fmt}x{b_fmt} block {block} {M}x{N}x{K} tile_k {tile_k}")
@@ -244,8 +245,8 @@ def test_format_options_plan():
 
     p = dtc.gemm_plan("mxfp8", 4096, 4096, 8192, scale_block=32, a_format="e5m2")
     assert (p["variant"], p["tile_k"]) == (1, 256)
-    with pytest.raises(dtc.GemmError):  # the pair kernel takes the pages' format only
-        dtc.gemm_plan("mxfp8", 4096, 4096, 8192, variant=2, scale_block=32)
+    p = dtc.gemm_plan("mxfp8", 4096, 4096, 8192, variant=2, scale_block=32, b_format="e2m1")
+    assert (p["variant"], p["tile_m"], p["tile_n"]) == (2, 256, 224)
 
 
 @pytest.mark.parametrize("variant", [1, 2])
