@@ -13,6 +13,10 @@ Recipe (the pages measure on random matrices, not on a dataset: TileLang SM100 S
   recipe below with the element rounded to the nearest fp6 / fp4 value (ties to the even code,
   saturating at the largest magnitude); rows packed as a little-endian bit stream, element k at
   bit b*k.
+* 2:4 structured-sparse A: the generator draws the stored values ~ N(0,1) [M, K/2] (rounded to
+  bf16 / fp16), then B as for the dense product, then for every group of 4 K-elements two
+  distinct positions (a uniformly random pair, in random order); metadata nibble = first | second
+  << 2, two groups per byte, the even group in the low nibble.
 * MXFP8 operands: the same generator draws x_A ~ N(0,1) [M,K], x_B ~ N(0,1) [N,K], then integer
   exponents u_A [M, ceil(K/128)] and u_B [N, ceil(K/128)] uniform in {-3..3}. Each element is
   stored as e4m3(x / 2^u) (torch's RNE conversion to float8_e4m3fn) and each scale as the E8M0
@@ -31,7 +35,7 @@ BITS = {"e4m3": 8, "e5m2": 8, "e2m3": 6, "e3m2": 6, "e2m1": 4}  # bits per eleme
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str  # "bf16", "f16" or "mxfp8"
+    kind: str  # "bf16", "f16", "mxfp8" (block-scaled) or "bf16_sp24" / "f16_sp24" (2:4 sparse A)
     layout: str  # "NT" (B is [N,K]), "NN" (B is [K,N]); a leading "T" stores A as [K,M]
     M: int
     N: int
@@ -52,6 +56,8 @@ class Workload:
             kb = (self.K + self.block - 1) // self.block
             return (self.M * self.K * BITS[self.a_fmt] // 8 + self.N * self.K * BITS[self.b_fmt] // 8
                     + (self.M + self.N) * kb + 2 * self.M * self.N)
+        if self.kind.endswith("_sp24"):  # stored values, metadata, B, C
+            return self.M * self.K + self.M * self.K // 8 + 2 * (self.N * self.K + self.M * self.N)
         return 2 * (self.M * self.K + self.N * self.K + self.M * self.N)
 
 
@@ -79,6 +85,7 @@ WORKLOADS = {
                  a_fmt="e2m1", b_fmt="e2m1", block=32),
         Workload("mxfp6_e2m3_e3m2_b32_nt_4096x4096x8192", "mxfp8", "NT", 4096, 4096, 8192, 10,
                  a_fmt="e2m3", b_fmt="e3m2", block=32),
+        Workload("bf16_sp24_nt_4096x4096x8192", "bf16_sp24", "NT", 4096, 4096, 8192, 11),
     ]
 }
 
@@ -204,7 +211,27 @@ def make_mxfp8(M: int, N: int, K: int, seed: int):
     return make_mx(M, N, K, seed)
 
 
+def make_sp24(kind: str, layout: str, M: int, N: int, K: int, seed: int):
+    """(vals [M, K/2] uint16 codes, meta [M, ceil(K/8)] uint8, B) of a 2:4 structured-sparse
+    product: B [N,K] for "NT", [K,N] for "NN". K % 4 == 0."""
+    g = torch.Generator().manual_seed(seed)
+    vals = randn16(kind, (M, K // 2), g)
+    B = randn16(kind, (N, K) if layout[1] == "T" else (K, N), g)
+    G = K // 4
+    # a random pair of distinct positions per group: the first uniform in 0..3, the second one
+    # of the other three
+    first = torch.randint(0, 4, (M, G), generator=g)
+    second = (first + torch.randint(1, 4, (M, G), generator=g)) % 4
+    nib = (first | (second << 2)).numpy().astype(np.uint8)
+    if G % 2:
+        nib = np.concatenate([nib, np.zeros((M, 1), np.uint8)], axis=1)
+    meta = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
+    return vals, meta, B
+
+
 def make(w: Workload):
+    if w.kind.endswith("_sp24"):
+        return make_sp24(w.kind[:-5], w.layout, w.M, w.N, w.K, w.seed)
     if w.kind == "mxfp8" and (BITS[w.a_fmt] < 8 or BITS[w.b_fmt] < 8):
         return make_sub_byte(w.M, w.N, w.K, w.seed, w.a_fmt, w.b_fmt, w.block)
     if w.kind == "mxfp8":

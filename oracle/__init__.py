@@ -9,6 +9,8 @@ end), whose header states the definition it computes and the page passages it fo
   "Code Example" and "Compilation and Usage") or ``Bop = B`` for "NN" (tilelang (velog), 1.1).
 * MXFP8: e4m3 operands times ``2^(sf-127)`` per row per 128 K-elements (05 Blackwell TCGEN05 GEMM
   tutorial, "Advanced": gemm_blockscaled with granularity 128 for A and B).
+* 2:4 structured-sparse A (the tutorial's gemm_sp, named in "An API-level note"): per group of
+  4 K-elements two stored values and their positions (2-bit fields of a metadata nibble).
 * The other block-scaled formats of that section, read as the OCP MX family: elements e4m3, e5m2,
   e2m3, e3m2 (fp6) or e2m1 (fp4), packed little-endian in rows; E8M0 scales per 32 or 128
   K-elements, or UE4M3 scales per 16 (NVFP4).
@@ -80,6 +82,9 @@ def _bind(path):
     L.dtc_oracle_gemm_mx_sampled.restype = ctypes.c_int
     L.dtc_oracle_gemm_mx_sampled.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, u8p, u8p,
                                              u8p, u8p, i64, i64, i64, i64p, i64p, i64, u16p, dp]
+    L.dtc_oracle_gemm_sp.restype = ctypes.c_int
+    L.dtc_oracle_gemm_sp.argtypes = [ctypes.c_int, ctypes.c_int, u16p, u8p, u16p, i64, i64, i64,
+                                     u16p, dp, ctypes.c_int]
     L.dtc_oracle_default_threads.restype = ctypes.c_int
     return L
 
@@ -368,3 +373,24 @@ def gemm_bs_sampled(A, B, sfA, sfB, M, N, K, rows, cols, *, a_fmt="e4m3", b_fmt=
     if rc != 0:
         raise ValueError("oracle gemm_bs_sampled rejected its arguments")
     return C, S
+
+
+# --- 2:4 structured-sparse A --------------------------------------------------------------------
+
+def gemm_sp(dtype, layout, vals, meta, B, M, N, K, *, sums=False, nthreads=None):
+    """Sparse-A GEMM: vals [M, K/2] 16-bit codes (two stored values per group of 4 K-elements),
+    meta [M, K/8] bytes (group g's nibble at bits 4*(g % 2) of byte g/2: bits 0-1 the position of
+    the group's first value, bits 2-3 of its second), B as for gemm16 ("NT" or "NN")."""
+    vals = np.ascontiguousarray(vals, dtype=np.uint16)
+    meta = np.ascontiguousarray(meta, dtype=np.uint8)
+    B = np.ascontiguousarray(B, dtype=np.uint16)
+    assert vals.size == M * (K // 2) and meta.size == M * ((K // 4 + 1) // 2) and B.size == N * K
+    C = np.zeros((M, N), dtype=np.uint16)
+    S = np.zeros((M, N), dtype=np.float64) if sums else None
+    rc = _L().dtc_oracle_gemm_sp(_dtype_code(dtype), _layout_code(layout),
+                                  _ptr(vals, ctypes.c_uint16), _ptr(meta, ctypes.c_uint8),
+                                  _ptr(B, ctypes.c_uint16), M, N, K, _ptr(C, ctypes.c_uint16),
+                                  _ptr(S, ctypes.c_double), nthreads or threads())
+    if rc != 0:
+        raise ValueError("oracle gemm_sp rejected its arguments")
+    return (C, S) if sums else C

@@ -57,6 +57,16 @@
  * little-endian bit stream, element k in bits [b*k, b*k + b) (fp4: byte k/2, the low nibble for
  * even k; fp6: 4 elements in 3 bytes). A row of fp8 codes is one byte per element.
  *
+ *   2:4 structured-sparse A (gemm_sp; 05 Blackwell TCGEN05 GEMM tutorial, "An API-level note",
+ *   which names the sparse GEMM among the exported forms without defining it; read as the 2:4
+ *   pattern along K): of every group of 4 consecutive K-elements of a row of A, two values are
+ *   stored, vals [M, K/2] (16-bit, the group's two values in order), and the group's two
+ *   positions (0..3) in meta [M, K/8] bytes: group g's nibble sits at bits 4*(g % 2) of byte g/2,
+ *   its bits 0-1 the position of vals[m, 2g] and bits 2-3 that of vals[m, 2g+1]:
+ *     C[m,n] = round_out( sum_g sum_{j<2} dec(vals[m,2g+j]) * dec(Bop[4g + pos_j(m,g), n]) )
+ *   with Bop as for the dense product ("NT" or "NN"). The two positions of a group differ in the
+ *   2:4 pattern; the sum above is defined either way.
+ *
  * Degenerate sizes: M == 0 or N == 0 computes nothing; K == 0 gives the empty sum, +0.
  *
  * Threads: rows of C are split across POSIX threads, one per requested worker; the
@@ -344,6 +354,50 @@ int dtc_oracle_gemm16_sampled(int dtype, int layout, const uint16_t* A, const ui
         if (Sout) Sout[i] = acc;
         if (Cout) Cout[i] = dtype == DTC_ORACLE_F16 ? dtc_oracle_enc_f16(acc) : dtc_oracle_enc_bf16(acc);
     }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* 2:4 structured-sparse A                                                                     */
+/* ------------------------------------------------------------------------------------------ */
+
+/* Position (0..3) of stored value j (0 or 1) of group g of a row of metadata. */
+static int sp_position(const uint8_t* meta_row, int64_t g, int j) {
+    uint8_t nib = (uint8_t)((meta_row[g / 2] >> (4 * (g % 2))) & 0xf);
+    return (nib >> (2 * j)) & 0x3;
+}
+
+/* Full C of the sparse product (layouts "NT" and "NN" for B). K must be a multiple of 4. */
+int dtc_oracle_gemm_sp(int dtype, int layout, const uint16_t* vals, const uint8_t* meta,
+                       const uint16_t* B, int64_t M, int64_t N, int64_t K, uint16_t* C, double* S,
+                       int nthreads) {
+    if (M < 0 || N < 0 || K < 0 || K % 4) return -1;
+    if (dtype != DTC_ORACLE_BF16 && dtype != DTC_ORACLE_F16) return -1;
+    if (layout != DTC_ORACLE_NT && layout != DTC_ORACLE_NN) return -1;
+    if (M == 0 || N == 0) return 0;
+    /* Aop as a dense [M][K] array of doubles: each stored value added at its position. */
+    double* a = (double*)calloc((size_t)(M * K > 0 ? M * K : 1), sizeof(double));
+    double* bt = (double*)malloc(sizeof(double) * (size_t)(N * K > 0 ? N * K : 1));
+    if (!a || !bt) {
+        free(a);
+        free(bt);
+        return -1;
+    }
+    const int64_t mrow = (K / 4 + 1) / 2; /* metadata bytes per row */
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t g = 0; g < K / 4; ++g)
+            for (int j = 0; j < 2; ++j)
+                a[m * K + 4 * g + sp_position(meta + m * mrow, g, j)] +=
+                    dec16(dtype, vals[m * (K / 2) + 2 * g + j]);
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k) {
+            const uint16_t code = b_is_kn(layout) ? B[k * N + n] : B[n * K + k]; /* Bop[k][n] */
+            bt[n * K + k] = dec16(dtype, code);
+        }
+    gemm_job proto = {a, bt, M, N, K, dtype, C, S, 0, 0};
+    run_rows(&proto, nthreads);
+    free(a);
+    free(bt);
     return 0;
 }
 

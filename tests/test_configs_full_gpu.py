@@ -38,7 +38,7 @@ def bench_launch16(w, A, B):
     return C.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-@pytest.mark.parametrize("name", [n for n, w in workloads.WORKLOADS.items() if w.kind != "mxfp8"])
+@pytest.mark.parametrize("name", [n for n, w in workloads.WORKLOADS.items() if w.kind in ("bf16", "f16")])
 def test_16bit_workload_every_element(name):
     w = workloads.WORKLOADS[name]
     A, B = workloads.make(w)

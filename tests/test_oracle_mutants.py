@@ -13,7 +13,8 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "dtc_oracle.c")
-PINS = ["tests/test_oracle_codecs.py", "tests/test_oracle_gemm.py", "tests/test_oracle_formats.py"]
+PINS = ["tests/test_oracle_codecs.py", "tests/test_oracle_gemm.py", "tests/test_oracle_formats.py",
+        "tests/test_oracle_sparse.py"]
 
 MUTANTS = {
     "nn_operand_read_as_nt": (
@@ -87,6 +88,22 @@ MUTANTS = {
         ": ldexp(2.0, e - 2);  /* (1 + m/2) * 2^(e-1) */",
     ),
     "ue4m3_sign_not_rejected": ("if (b & 0x80) return NAN;\n", ""),
+    "sparse_nn_operand_read_as_nt": (
+        "const uint16_t code = b_is_kn(layout) ? B[k * N + n] : B[n * K + k]; /* Bop[k][n] */",
+        "const uint16_t code = B[n * K + k]; /* Bop[k][n] */",
+    ),
+    "sparse_position_fields_swapped": (
+        "return (nib >> (2 * j)) & 0x3;",
+        "return (nib >> (2 * (1 - j))) & 0x3;",
+    ),
+    "sparse_nibbles_swapped": (
+        "uint8_t nib = (uint8_t)((meta_row[g / 2] >> (4 * (g % 2))) & 0xf);",
+        "uint8_t nib = (uint8_t)((meta_row[g / 2] >> (4 * (1 - g % 2))) & 0xf);",
+    ),
+    "sparse_value_index_wrong": (
+        "dec16(dtype, vals[m * (K / 2) + 2 * g + j]);",
+        "dec16(dtype, vals[m * (K / 2) + g + j]);",
+    ),
     "nvfp4_scales_read_as_e8m0": (
         "return sf_kind == DTC_ORACLE_SF_UE4M3 ? dtc_oracle_dec_ue4m3(c) : dtc_oracle_dec_e8m0(c);",
         "return dtc_oracle_dec_e8m0(c);",
