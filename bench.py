@@ -340,8 +340,13 @@ def oracle_rows(w, inputs, rows, cols=None):
     t0 = time.perf_counter()
     if w.kind == "mxfp8":
         A, B, sfA, sfB = inputs
-        oracle.gemm_mx(A[:rows], B[:cols], sfA[:rows], sfB[:cols], rows, cols, w.K, a_fmt=w.a_fmt,
+        oracle.gemm_bs(A[:rows], B[:cols], sfA[:rows], sfB[:cols], rows, cols, w.K, a_fmt=w.a_fmt,
                        b_fmt=w.b_fmt, block=w.block)
+    elif w.kind.endswith("_sp24"):
+        vals, meta, B = inputs
+        Bc = B[:cols] if w.layout[1] == "T" else B[:, :cols]
+        oracle.gemm_sp(w.kind[:-5], w.layout, vals[:rows], meta[:rows], np.ascontiguousarray(Bc),
+                       rows, cols, w.K)
     else:
         A, B = inputs
         # output rows m are rows of A, or its columns when A is stored [K,M]; output columns n
@@ -427,7 +432,8 @@ def run_reference(args, w):
 
 
 def kernel_of(w, plan):
-    """The name of the kernel the plan launches (as in the ncu launch list)."""
+    """The name of the kernel the plan launches (as in the ncu launch list); for the sparse
+    product the GEMM kernel (the step also launches sp24_expand_kernel before it)."""
     if w.kind == "mxfp8":
         return "gemm_mxfp8_2cta_kernel" if plan["variant"] == 2 else "gemm_mxfp8_kernel"
     return {1: "gemm16_1cta_kernel", 2: "gemm16_2cta_kernel",
@@ -488,7 +494,7 @@ def library_context(w, A, B, flush_l2, stream, steps, dev):
     K-elements in this row-major scale layout)."""
     import torch
 
-    if w.kind == "mxfp8":
+    if w.kind == "mxfp8" or w.kind.endswith("_sp24"):
         return None
     a_op = A.t() if w.layout[0] == "T" else A  # A stored [K,M] for TN and TT
     b_op = B.t() if w.layout[1] == "T" else B  # B stored [N,K] for NT and TT
@@ -536,6 +542,12 @@ def device_inputs(w, dev):
     if w.kind == "mxfp8":
         dev_in = [torch.from_numpy(x).to(dev) for x in inputs]
         return dev_in, torch.bfloat16, inputs
+    if w.kind.endswith("_sp24"):  # stored values, metadata, B
+        t16 = torch.bfloat16 if w.kind.startswith("bf16") else torch.float16
+        vals, meta, B = inputs
+        dev_in = [torch.from_numpy(vals.view(np.int16)).view(t16).to(dev),
+                  torch.from_numpy(meta).to(dev), torch.from_numpy(B.view(np.int16)).view(t16).to(dev)]
+        return dev_in, t16, inputs
     t16 = torch.bfloat16 if w.kind == "bf16" else torch.float16
     dev_in = [torch.from_numpy(x.view(np.int16)).view(t16).to(dev) for x in inputs]
     return dev_in, t16, inputs
@@ -548,19 +560,28 @@ def gemm_kwargs(args, w, dtc, dev):
 
     if w.kind == "mxfp8":
         return dict(a_format=w.a_fmt, b_format=w.b_fmt, scale_block=w.block, variant=args.variant)
+    base = w.kind[:-5] if w.kind.endswith("_sp24") else w.kind
     kw = dict(layout=w.layout, variant=args.variant, split_k=args.split_k, tile_n=args.tile_n)
     if args.stream_k != 2:
-        ws_bytes = dtc.gemm_workspace_size(w.kind, w.M, w.N, w.K, w.layout, variant=args.variant,
+        ws_bytes = dtc.gemm_workspace_size(base, w.M, w.N, w.K, w.layout, variant=args.variant,
                                            tile_n=args.tile_n, stream_k=args.stream_k)
         if ws_bytes:
             kw.update(workspace=torch.zeros(ws_bytes, dtype=torch.uint8, device=dev),
                       stream_k=args.stream_k)
+    if w.kind.endswith("_sp24"):  # the expanded A, and the dense product's stream-K workspace
+        kw["sk_workspace"] = kw.pop("workspace", None)
+        kw["sp_workspace"] = torch.empty(dtc.gemm_sp_workspace_size(base, w.M, w.K),
+                                         dtype=torch.uint8, device=dev)
     return kw
 
 
 def call(dtc, w, ins, C, kw, stream):
     if w.kind == "mxfp8":
         dtc.gemm_ex("mxfp8", ins[0], ins[1], C, sfA=ins[2], sfB=ins[3], stream=stream, **kw)
+    elif w.kind.endswith("_sp24"):
+        kw = dict(kw)
+        dtc.gemm_sp(w.kind[:-5], ins[0], ins[1], ins[2], C, workspace=kw.pop("sp_workspace"),
+                    stream=stream, **kw)
     else:
         dtc.gemm_ex(w.kind, ins[0], ins[1], C, stream=stream, **kw)
 
@@ -568,6 +589,10 @@ def call(dtc, w, ins, C, kw, stream):
 def plan_of(dtc, w, kw):
     keys = ("layout", "variant", "split_k", "tile_n", "workspace", "stream_k", "a_format",
             "b_format", "scale_block")
+    kw = dict(kw)
+    if w.kind.endswith("_sp24"):  # the dense product that runs on the expanded A
+        kw["workspace"] = kw.pop("sk_workspace", None)
+        return dtc.gemm_plan(w.kind[:-5], w.M, w.N, w.K, **{k: v for k, v in kw.items() if k in keys})
     return dtc.gemm_plan(w.kind, w.M, w.N, w.K, **{k: v for k, v in kw.items() if k in keys})
 
 
@@ -737,7 +762,8 @@ def run_ours(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": ("bf16" if w.kind == "bf16" else "f16" if w.kind == "f16"
+        "dtype": (w.kind[:-5] if w.kind.endswith("_sp24") else "bf16" if w.kind == "bf16"
+                  else "f16" if w.kind == "f16"
                   else w.a_fmt if w.a_fmt == w.b_fmt else f"{w.a_fmt}x{w.b_fmt}"),
         "data": "synthetic",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout,
@@ -759,7 +785,8 @@ def run_ours(args, w):
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "mode": "pipelined: step i+1's H2D and step i-1's D2H overlap step i's GEMM "
                         "(3 streams, 2 device buffers); pinned host memory"},
-        "gpu_launches": args.steps,  # our kernel, once per timed step of the headline
+        # our kernels per timed step of the headline: the GEMM (and the sparse expansion)
+        "gpu_launches": args.steps * (2 if w.kind.endswith("_sp24") else 1),
         "gpu_launches_whole_run": launches,  # with the end-to-end steps and the other configs
         "clocks": clocks,
         "library_context": library,

@@ -24,6 +24,8 @@ from ._binding import (  # noqa: F401
     gemm_last_error,
     gemm_mxfp8,
     gemm_plan,
+    gemm_sp,
+    gemm_sp_workspace_size,
     gemm_stream_status,
     gemm_workspace_size,
     lib,

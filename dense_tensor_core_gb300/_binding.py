@@ -88,6 +88,11 @@ def lib():
         L.gemm_ex_static_workspace.restype = i32
         L.gemm_ex_static_workspace.argtypes = [i32, vp, vp, vp, vp, vp, i64, i64, i64, i32,
                                                ctypes.POINTER(gemm_options), vp]
+        L.gemm_sp.restype = i32
+        L.gemm_sp.argtypes = [i32, vp, vp, vp, vp, i64, i64, i64, i32, ctypes.POINTER(gemm_options),
+                              vp, ctypes.c_uint64, vp]
+        L.gemm_sp_workspace_size.restype = i32
+        L.gemm_sp_workspace_size.argtypes = [i32, i64, i64, ctypes.POINTER(ctypes.c_uint64)]
         L.gemm_workspace_size.restype = i32
         L.gemm_workspace_size.argtypes = [i32, i64, i64, i64, i32, ctypes.POINTER(gemm_options),
                                           ctypes.POINTER(ctypes.c_uint64)]
@@ -351,4 +356,44 @@ def gemm_ex_static_workspace(kind, A, B, C=None, layout="NT", variant=0, tile_n=
         _check(lib().gemm_ex_static_workspace(_DTYPE[kind], _ptr(A), _ptr(B), None, None,
                                               _ptr(C), M, N, K, _layout_code(layout),
                                               ctypes.byref(opts), _stream_handle(stream, dev)))
+    return C
+
+
+def gemm_sp_workspace_size(kind, M, K):
+    """Bytes of workspace gemm_sp needs (the dense A it expands: M x K 16-bit elements)."""
+    out = ctypes.c_uint64(0)
+    _check(lib().gemm_sp_workspace_size(_DTYPE[kind], M, K, ctypes.byref(out)))
+    return out.value
+
+
+def gemm_sp(kind, vals, meta, B, C=None, layout="NT", workspace=None, variant=0, split_k=0,
+            tile_n=0, tile_k=0, stream_k=0, sk_workspace=None, stream=None):
+    """2:4 structured-sparse A times B: vals [M, K/2] ("bf16" or "f16"), meta [M, K/8] uint8
+    (per group of 4 K-elements two 2-bit positions, two groups per byte), B [N,K] ("NT") or
+    [K,N] ("NN"). `workspace` (M x K x 2 bytes of device memory) receives the expanded A; it is
+    allocated here when not given. `sk_workspace` is the dense product's stream-K workspace."""
+    dt = torch.bfloat16 if kind == "bf16" else torch.float16
+    _check_tensor(vals, dt, "vals")
+    _check_tensor(meta, torch.uint8, "meta")
+    _check_tensor(B, dt, "B", rows_of_larger=True)
+    if vals.dim() != 2 or meta.dim() != 2:
+        raise ValueError("vals and meta must be 2-D")
+    M, K = vals.shape[0], 2 * vals.shape[1]
+    if tuple(meta.shape) != (M, K // 8):
+        raise ValueError(f"meta must be [M, K/8] = {(M, K // 8)}, got {tuple(meta.shape)}")
+    name = _layout_name(layout)
+    N, Kb = (B.shape if name == "NT" else B.shape[::-1])
+    if Kb != K:
+        raise ValueError(f"B {tuple(B.shape)} does not match K = {K} ({name})")
+    C = _out(C, M, N, dt, vals.device, rows_of_larger=True)
+    if workspace is None:
+        workspace = torch.empty(max(1, M * K * 2), dtype=torch.uint8, device=vals.device)
+    opts = _options(variant, split_k, 0, 0, tile_n, tile_k, 0, _ld(B), _ld(C),
+                    workspace=sk_workspace, stream_k=stream_k)
+    dev = _same_device(vals, meta, B, C, workspace, sk_workspace)
+    with torch.cuda.device(dev):
+        _check(lib().gemm_sp(_DTYPE[kind], _ptr(vals), _ptr(meta), _ptr(B), _ptr(C), M, N, K,
+                             _layout_code(layout), ctypes.byref(opts), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(),
+                             _stream_handle(stream, dev)))
     return C

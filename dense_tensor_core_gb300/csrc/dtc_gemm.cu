@@ -821,6 +821,51 @@ int gemm_ex_static_workspace(int dtype, const void* A, const void* B, const void
     return launch_prepared(r, dtype, M, N, K, &o, (cudaStream_t)stream);
 }
 
+int gemm_sp_workspace_size(int dtype, int64_t M, int64_t K, uint64_t* bytes) {
+    g_err[0] = '\0';
+    if (!bytes) return fail(GEMM_ERR_INVALID_ARG, "bytes is NULL");
+    if (dtype != 0 && dtype != 1) return fail(GEMM_ERR_INVALID_ARG, "dtype %d is not 0 (bf16) or 1 (fp16)", dtype);
+    if (M < 0 || K < 0 || M > 2147483647 || K > 2147483647)
+        return fail(GEMM_ERR_INVALID_ARG, "sizes must be in [0, 2^31-1]");
+    *bytes = (uint64_t)M * (uint64_t)K * 2;
+    return GEMM_OK;
+}
+
+int gemm_sp(int dtype, const void* vals, const void* meta, const void* B, void* C, int64_t M,
+            int64_t N, int64_t K, int layout, const gemm_options* opts, void* workspace,
+            uint64_t workspace_bytes, dtc_stream_t stream) {
+    g_err[0] = '\0';
+    if (dtype != 0 && dtype != 1)
+        return fail(GEMM_ERR_INVALID_ARG, "dtype %d is not 0 (bf16) or 1 (fp16)", dtype);
+    if (layout != GEMM_LAYOUT_NT && layout != GEMM_LAYOUT_NN)
+        return fail(GEMM_ERR_INVALID_ARG, "the sparse product takes layout NT (0) or NN (1)");
+    if (opts && opts->lda)
+        return fail(GEMM_ERR_INVALID_ARG, "the sparse product's A rows are dense (lda must be 0)");
+    if (K % 16)
+        return fail(GEMM_ERR_INVALID_ARG, "K=%lld: the sparse product needs K %% 16 == 0", (long long)K);
+    const bool work = M > 0 && N > 0 && K > 0;
+    if (work) {
+        if (!vals || !meta) return fail(GEMM_ERR_INVALID_ARG, "vals or meta is NULL");
+        if (!aligned16(vals)) return fail(GEMM_ERR_INVALID_ARG, "vals is not 16-byte aligned");
+        if (!workspace || workspace_bytes < (uint64_t)M * (uint64_t)K * 2)
+            return fail(GEMM_ERR_INVALID_ARG, "the sparse product needs a workspace of %llu bytes "
+                        "(M x K 16-bit elements)", (unsigned long long)((uint64_t)M * (uint64_t)K * 2));
+    }
+    // the dense call on the expanded A (checks B, C, the workspace, the sizes and the options)
+    Prepared r;
+    int rc = prepare(dtype, work ? workspace : nullptr, B, nullptr, nullptr, C, M, N, K, layout,
+                     opts, &r);
+    if (rc) return rc;
+    if (work) {
+        if ((rc = check_device_ptr(vals, r.dev, "vals")) || (rc = check_device_ptr(meta, r.dev, "meta")))
+            return rc;
+        if ((rc = launch_sp24_expand(dtype == 0, vals, meta, workspace, M, K, r.info,
+                                     (cudaStream_t)stream)))
+            return rc;
+    }
+    return launch_prepared(r, dtype, M, N, K, opts, (cudaStream_t)stream);
+}
+
 int gemm_device_model_query(gemm_device_model* out) {
     g_err[0] = '\0';
     if (!out) return fail(GEMM_ERR_INVALID_ARG, "out is NULL");

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 #include <unordered_set>
 
@@ -160,6 +161,9 @@ int launch16_2cta_bf16(const Launch& L);
 int launch16_2cta_f16(const Launch& L);
 int launch16_splitk(bool bf16, const Launch& L);
 int launch_mx(const Launch& L);
+// 2:4 sparse A: writes the dense [M, K] 16-bit A into `dense` (stream-ordered).
+int launch_sp24_expand(bool bf16, const void* vals, const void* meta, void* dense, int64_t M,
+                       int64_t K, DeviceInfo* dev, cudaStream_t stream);
 
 // Resident clusters of the pair kernel and of the split-K kernels (clusters of 2 and 4).
 int query_pair_clusters(DeviceInfo* dev);

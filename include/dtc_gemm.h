@@ -236,6 +236,32 @@ int gemm_ex_static_workspace(int dtype, const void* A, const void* B, const void
                              int layout, const gemm_options* opts, dtc_stream_t stream);
 
 /*
+ * 2:4 structured-sparse A (the sparse GEMM, gemm_sp, that 05 Blackwell TCGEN05 GEMM tutorial, "An
+ * API-level note", names among the exported forms; read as the 2:4 pattern along K):
+ *   C[m,n] = round_out( sum_g sum_{j<2} vals[m,2g+j] * Bop[4g + pos_j(m,g), n] )
+ * Each group g of 4 consecutive K-elements of a row of A keeps two values, stored in order in vals
+ * [M, K/2] (bf16 for dtype 0, fp16 for 1), at two positions 0..3 given by meta [M, K/8] bytes:
+ * group g's nibble is at bits 4*(g % 2) of byte g/2 of the row, its bits 0-1 the position of
+ * vals[m, 2g] and bits 2-3 that of vals[m, 2g+1]. The two positions of a group must differ (the
+ * 2:4 pattern); where they are equal the element is the two values' sum rounded to the element
+ * type. B and C as for gemm_bf16 / gemm_f16 with layout NT or NN; opts as gemm_ex's (lda must be
+ * 0; ldb, ldc, the variant and a stream-K workspace apply to the product).
+ * The call expands A into `workspace` (device memory of the current device, 16-byte aligned, at
+ * least gemm_sp_workspace_size bytes: M x K 16-bit elements, owned by the caller) with an
+ * HBM-bound kernel, then runs the dense product on it; both are enqueued on `stream`.
+ * INVALID_ARG also when K % 16 != 0, vals is NULL or not 16-byte aligned, meta is NULL, or the
+ * workspace is missing or too small.
+ */
+int gemm_sp(int dtype, const void* vals, const void* meta, const void* B, void* C, int64_t M,
+            int64_t N, int64_t K, int layout, const gemm_options* opts, void* workspace,
+            uint64_t workspace_bytes, dtc_stream_t stream);
+
+/* Bytes of workspace gemm_sp needs (M x K x 2). INVALID_ARG for a dtype other than 0 or 1, sizes
+ * outside [0, 2^31-1] or a NULL bytes. (05 Blackwell TCGEN05 GEMM tutorial, "An API-level note":
+ * gemm_sp.) */
+int gemm_sp_workspace_size(int dtype, int64_t M, int64_t K, uint64_t* bytes);
+
+/*
  * Bytes of workspace (gemm_options.workspace) with which the call would use stream-K on CTA pairs
  * (the last, part-full wave's tiles shared out over all pairs as equal runs of K-blocks, the
  * pieces summed through the workspace); 0 when it would not (or stream_k == 2). The pages have

@@ -60,3 +60,18 @@ def test_block_scaled_workload_every_element(name):
     ref = oracle.gemm_bs(A, B, sfA, sfB, w.M, w.N, w.K, a_fmt=w.a_fmt, b_fmt=w.b_fmt,
                          block=w.block)
     check_close(values16(C, "bf16"), values16(ref, "bf16"), f"{name}, every element")
+
+
+@pytest.mark.parametrize("name", [n for n, w in workloads.WORKLOADS.items() if w.kind.endswith("_sp24")])
+def test_sparse_workload_every_element(name):
+    import dense_tensor_core_gb300 as dtc
+
+    w = workloads.WORKLOADS[name]
+    kind = w.kind[:-5]
+    vals, meta, B = workloads.make(w)
+    C = dtc.gemm_sp(kind, to_device16(vals, kind), to_device8(meta), to_device16(B, kind),
+                    layout=w.layout)
+    dtc.gemm_stream_status()
+    C = C.view(torch.int16).cpu().numpy().view(np.uint16)
+    ref = oracle.gemm_sp(kind, w.layout, vals, meta, B, w.M, w.N, w.K)
+    check_close(values16(C, kind), values16(ref, kind), f"{name}, every element")
