@@ -564,10 +564,15 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
     if (v == GEMM_VARIANT_AUTO && split == 0 && want_n != 224 && tiles256 * 2 <= sms) {
         // Fewer 128 x 256 tiles than half the SMs: split K over a cluster of 2 or 4 CTAs per
         // 128 x 128 or 128 x 256 tile. Take the (width, split) that occupies the most SMs in one
-        // wave, each CTA keeping at least 8 K-blocks of 64 (with less, the on-chip exchange of
-        // the partial sums costs more than the split saves: 256 x 256 x 512 ran 12.3 us split in
-        // 2 against 10.3 us on one-CTA tiles); on a tie the smaller split (less to reduce), then
-        // the narrower tile (a smaller exchange).
+        // wave; on a tie the smaller split (less to reduce), then the narrower tile (a smaller
+        // exchange). Each CTA keeps at least 8 K-blocks of 64, or 4 when one-CTA tiles would
+        // leave all but a few SMs idle (at most one 128 x 256 tile per 8 SMs): the on-chip
+        // exchange of the partial sums costs ~2 us, which a split pays back only when it halves
+        // a long K loop or spreads a product that would otherwise run on a handful of SMs
+        // (GB300, L2 flushed: 256 x 256 x 512 split in 2 10.2 us against 10.5-10.7 one-CTA;
+        // 384 x 640 x 768 10.2 against 12.7; 1024 x 1024 x 512, 32 one-CTA tiles, 10.9 split
+        // against 10.7).
+        const int min_kb = tiles256 * 8 <= sms ? 4 : 8;
         struct Cand { int bn, s; };
         const Cand cands[3] = {{128, 2}, {128, 4}, {256, 2}};
         int64_t best_ctas = 0;
@@ -577,7 +582,7 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
             const int64_t ctas = tl * c.s;
             const int resident = c.s == 2 ? (d.clusters2 > 0 ? d.clusters2 : sms / 2)
                                           : (d.clusters4 > 0 ? d.clusters4 : sms / 4);
-            if (num_kb < 8 * c.s || ctas > (int64_t)resident * c.s) continue;
+            if (num_kb < min_kb * c.s || ctas > (int64_t)resident * c.s) continue;
             if (ctas > best_ctas || (ctas == best_ctas && c.s < split)) {
                 best_ctas = ctas;
                 split = c.s;

@@ -139,7 +139,9 @@ def test_automatic_choice_follows_the_cost_model():
     assert (p["variant"], p["split_k"], p["tile_n"], p["ctas"]) == (3, 4, 128, 64)
     p = dtc.gemm_plan("f16", 1024, 1024, 1000, "NN")  # K % 64 != 0: 64-deep stages
     assert (p["variant"], p["split_k"], p["tile_n"], p["tile_k"]) == (3, 2, 128, 64)
-    p = dtc.gemm_plan("bf16", 256, 256, 512, "NT")  # 8 K-blocks: too few to split
+    p = dtc.gemm_plan("bf16", 256, 256, 512, "NT")  # 2 one-CTA tiles: split in 2 over 8 CTAs
+    assert (p["variant"], p["split_k"], p["ctas"]) == (3, 2, 8)
+    p = dtc.gemm_plan("bf16", 256, 256, 256, "NT")  # 4 K-blocks: too few to split
     assert p["variant"] == 1
 
 

@@ -37,8 +37,13 @@ def test_automatic_choice_on_gb300():
     assert (p["variant"], p["split_k"], p["tile_n"], p["ctas"]) == (3, 4, 128, 64)
     p = plan("f16", 1024, 1024, 1000, "NN")  # K % 64 != 0: 64-deep stages
     assert (p["variant"], p["split_k"], p["tile_n"], p["tile_k"]) == (3, 2, 128, 64)
-    p = plan("bf16", 256, 256, 512)  # 8 K-blocks: too few to split
+    # 2 one-CTA tiles of 128 x 256 would leave 150 SMs idle: 8 K-blocks are enough to split in 2
+    p = plan("bf16", 256, 256, 512)
+    assert (p["variant"], p["split_k"], p["tile_n"], p["ctas"]) == (3, 2, 128, 8)
+    p = plan("bf16", 256, 256, 256)  # 4 K-blocks: too few to split
     assert p["variant"] == 1 and p["cluster"] == 1 and p["tile_k"] == 64
+    p = plan("bf16", 1024, 1024, 512)  # 32 one-CTA tiles: a split needs 8 K-blocks per CTA
+    assert p["variant"] == 1
     p = plan("mxfp8", 4096, 4096, 8192)
     assert (p["variant"], p["tile_n"], p["tile_k"]) == (1, 224, 256)
 
