@@ -40,7 +40,7 @@ class gemm_options(ctypes.Structure):
 class gemm_plan_info(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
                 ("variant", "tile_m", "tile_n", "tile_k", "stages", "split_k", "ctas", "tiles",
-                 "cluster", "sk_tiles")]
+                 "cluster", "sk_tiles", "sf_packed")]
 
 
 class gemm_device_model(ctypes.Structure):
@@ -303,8 +303,8 @@ def gemm_plan(kind, M, N, K, layout="NT", variant=0, split_k=0, tile_n=0, tile_k
               a_format="e4m3", b_format="e4m3", scale_block=0, workspace=None, stream_k=0,
               model=None):
     """The launch the library would make for these sizes: a dict with variant, tile_m, tile_n,
-    tile_k, stages, split_k, ctas, tiles, cluster, sk_tiles (raises GemmError if the call would
-    be rejected). With `model` (a dict of gemm_device_model's fields, e.g. GB300_MODEL) the plan
+    tile_k, stages, split_k, ctas, tiles, cluster, sk_tiles, sf_packed (raises GemmError if the
+    call would be rejected). With `model` (a dict of gemm_device_model's fields, e.g. GB300_MODEL) the plan
     is made for that device description, without a GPU; otherwise for the current device."""
     opts = _options(variant, split_k, 0, 0, tile_n, tile_k, 0, 0, 0, a_format, b_format,
                     scale_block, workspace, stream_k)
@@ -331,9 +331,13 @@ def gemm_stream_status(stream=None):
     _check(lib().gemm_stream_status(_stream_handle(stream)))
 
 
-def gemm_workspace_size(kind, M, N, K, layout="NT", variant=0, tile_n=0, tile_k=0, stream_k=0):
-    """Bytes of workspace with which the call would use stream-K (0 if it would not)."""
-    opts = _options(variant, 0, 0, 0, tile_n, tile_k, stream_k=stream_k)
+def gemm_workspace_size(kind, M, N, K, layout="NT", variant=0, tile_n=0, tile_k=0, stream_k=0,
+                        a_format="e4m3", b_format="e4m3", scale_block=0):
+    """Bytes of workspace the call can use: for the 16-bit products the stream-K workspace (0 if
+    stream-K would not be used); for the block-scaled product on the one-CTA kernel the repacked
+    scale arrays (0 on the pair kernel)."""
+    opts = _options(variant, 0, 0, 0, tile_n, tile_k, a_format=a_format, b_format=b_format,
+                    scale_block=scale_block, stream_k=stream_k)
     out = ctypes.c_uint64(0)
     _check(lib().gemm_workspace_size(_DTYPE[kind], M, N, K, _layout_code(layout),
                                      ctypes.byref(opts), ctypes.byref(out)))

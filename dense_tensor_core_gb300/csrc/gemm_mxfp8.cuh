@@ -30,9 +30,19 @@
 // Roles: warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer, warps 2..5 epilogue (as in the
 // bf16 kernels), warps 6..9 scale writers. Tensor Memory: accumulators at columns [0,224) and
 // [224,448), scale sets at 448 + 12*set (4 columns for A, 8 for B), set = 0..3.
+//
+// With kTmaSf the scales come instead from a copy of the scale arrays repacked by sf_pack_kernel
+// (sf_pack.cuh) into 512-byte chunks, one per (128-row group, set): the producer loads a set's
+// chunks (A: one, B: two) with bulk copies into a slot beside the stage holding the set's first
+// K-block, on that stage's full barrier, and the MMA thread moves them into the set's columns with
+// three tcgen05.cp.32x128b.warpx4 before the set's first MMA. A copy and the MMAs after it form a
+// tcgen05 pipeline (they run in issue order); an MMA and a later copy into columns it reads do
+// not, so the MMA thread reuses a set only after the commit that follows its last MMA
+// (bar_sempty). No scale warps, no cross-warp hand-off: 6 warps.
 #pragma once
 
 #include "gemm_common.cuh"
+#include "sf_pack.cuh"
 
 namespace dtc {
 
@@ -47,6 +57,9 @@ struct GemmMxArgs {
     uint32_t fmt_bits;         // instruction-descriptor element formats of A (bits 7-9), B (10-12)
     uint32_t stage_tx;         // bytes one stage's copies write (fp6 / fp4: the packed data only;
                                // the padding of each 16-byte group is not written)
+    const uint8_t* sfA_pack;   // kTmaSf: scale chunks of A (128-row groups) and of B (tile_n-row
+    const uint8_t* sfB_pack;   // groups, two 128-row halves each), sf_pack.cuh
+    int sf_sets;               // scale sets per row: ceil(sf_cols / 4)
     uint64_t timeout_ns;
     int fault;
     int* status;  // device status word: the first wait that gives up records its site here
@@ -66,9 +79,15 @@ constexpr int kGroup = 4;      // K-blocks per scale set (one byte each per 32-b
 constexpr int kGroupM = 8;
 constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
 static_assert(kSfBase + kSfSets * kSfSet <= kTmemCols, "Tensor Memory budget");
+constexpr int kSfSetBytes = 3 * kSfChunkBytes;  // one set's chunks: A (128 rows), B (2 x 128 rows)
+static_assert(kBN <= 256, "a B tile's scales fit two 128-row chunks");
+
+constexpr int threads_for(bool tma_sf) { return tma_sf ? 192 : kThreads; }
 
 // Stage geometry: kBlocks K-blocks per stage (1: 2-D boxes, 4 stages; 2: 3-D boxes, 2 stages).
-template <bool kDeep>
+// With kTmaSf each stage has a slot for the chunks of the sets that start in it (at most one per
+// K-block).
+template <bool kDeep, bool kTmaSf = false>
 struct Cfg {
     static constexpr int kBlocks = kDeep ? 2 : 1;
     static constexpr int kStages = kDeep ? 2 : 4;
@@ -77,7 +96,8 @@ struct Cfg {
     static constexpr int kStageBytes = kAStage + kBStage;
     static_assert(kStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
     static constexpr int kCBytes = 4 * 2 * 4096;  // two 4 KB output staging slots per epilogue warp
-    static constexpr int kSmemBytes = kStages * kStageBytes + kCBytes + 1024;
+    static constexpr int kSlotBytes = kTmaSf ? kBlocks * kSfSetBytes : 0;
+    static constexpr int kSmemBytes = kStages * (kStageBytes + kSlotBytes) + kCBytes + 1024;
     static_assert(kSmemBytes <= 227 * 1024 - 256, "shared memory budget");
 };
 }  // namespace gmx
@@ -98,14 +118,14 @@ __device__ __forceinline__ uint32_t sf_word(const uint8_t* sf, int rows, int col
     return w;
 }
 
-template <bool kDeep, bool kB32>
-__global__ void __launch_bounds__(gmx::kThreads, 1)
+template <bool kDeep, bool kB32, bool kTmaSf = false>
+__global__ void __launch_bounds__(gmx::threads_for(kTmaSf), 1)
     gemm_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmC,
                       const __grid_constant__ CUtensorMap tmC32, const GemmMxArgs args) {
     using namespace gmx;
-    using C_ = Cfg<kDeep>;
+    using C_ = Cfg<kDeep, kTmaSf>;
     constexpr int kStages = C_::kStages;
     constexpr int kAStage = C_::kAStage;
     constexpr int kBStage = C_::kBStage;
@@ -124,6 +144,7 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t sA = base;
     const uint32_t sB = base + kStages * kAStage;
+    const uint32_t sSF = base + kStages * C_::kStageBytes + C_::kCBytes;  // kTmaSf: scale slots
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int total = args.num_m * args.num_n;
@@ -167,7 +188,7 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
         // ------------------------------ TMA producer ------------------------------
         if (lane == 0) {
             uint32_t it = 0;
-            bool ok = true;
+            bool ok = true, chunks_ready = false;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 int mt, nt;
                 tile_coords(t, args.num_m, args.num_n, kGroupM, mt, nt);
@@ -180,13 +201,42 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
                     }
                     if (args.fault == 1 && it == 0) continue;  // test hook: stage never filled
                     const uint32_t full = smem_u32(&bar_full[s]);
-                    mbar_arrive_expect_tx(full, args.stage_tx);
+                    uint32_t tx = args.stage_tx;
+                    if constexpr (kTmaSf) {
+#pragma unroll
+                        for (int h = 0; h < kBlocks; ++h) {
+                            const int kb = st * kBlocks + h;
+                            if (kb < args.num_kb && kb % grp == 0) tx += kSfSetBytes;
+                        }
+                    }
+                    mbar_arrive_expect_tx(full, tx);
                     if constexpr (kDeep) {
                         tma_load_3d(sA + s * kAStage, &tmA, full, 0, mt * kBM, st * 2);
                         tma_load_3d(sB + s * kBStage, &tmB, full, 0, nt * kBN, st * 2);
                     } else {
                         tma_load_2d(sA + s * kAStage, &tmA, full, st * kBK, mt * kBM);
                         tma_load_2d(sB + s * kBStage, &tmB, full, st * kBK, nt * kBN);
+                    }
+                    if constexpr (kTmaSf) {
+                        // the chunks of each set that starts in this stage, into slot h; the
+                        // kernel that writes them may still be running (it launched this one
+                        // early): wait for it before the first chunk copy
+                        if (!chunks_ready) {
+                            grid_dependency_wait();
+                            chunks_ready = true;
+                        }
+#pragma unroll
+                        for (int h = 0; h < kBlocks; ++h) {
+                            const int kb = st * kBlocks + h;
+                            if (kb >= args.num_kb || kb % grp != 0) continue;
+                            const int g = kb / grp;
+                            const uint32_t slot = sSF + s * C_::kSlotBytes + h * kSfSetBytes;
+                            bulk_load_g2s(slot, args.sfA_pack + ((int64_t)mt * args.sf_sets + g) * kSfChunkBytes,
+                                          kSfChunkBytes, full);
+                            bulk_load_g2s(slot + kSfChunkBytes,
+                                          args.sfB_pack + ((int64_t)nt * args.sf_sets + g) * 2 * kSfChunkBytes,
+                                          2 * kSfChunkBytes, full);
+                        }
                     }
                 }
             }
@@ -228,12 +278,30 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
                         if (kb >= args.num_kb) break;  // a K-block past K: zero-filled, skipped
                         const uint32_t set = sit % kSfSets;
                         if (kb % grp == 0) {  // the first K-block of a scale set
-                            if (!wait_bounded(smem_u32(&bar_sfull[set]), (sit / kSfSets) & 1u,
-                                              abort, args.timeout_ns, args.status, 35)) {
-                                ok = false;
-                                break;
+                            if constexpr (kTmaSf) {
+                                // the set's columns are free once the MMAs that last read them
+                                // are done; then copy the set from the stage's slot
+                                if (!wait_bounded(smem_u32(&bar_sempty[set]),
+                                                  ((sit / kSfSets) & 1u) ^ 1u, abort,
+                                                  args.timeout_ns, args.status, 37)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after_sync();
+                                const uint32_t slot = sSF + s * C_::kSlotBytes + h * kSfSetBytes;
+                                const uint32_t col = tmem_base + kSfBase + set * kSfSet;
+                                tmem_cp_32x128b_x4(col, smem_desc_plain(slot, 128, 128));
+                                tmem_cp_32x128b_x4(col + 4, smem_desc_plain(slot + kSfChunkBytes, 128, 128));
+                                tmem_cp_32x128b_x4(col + 8,
+                                                   smem_desc_plain(slot + 2 * kSfChunkBytes, 128, 128));
+                            } else {
+                                if (!wait_bounded(smem_u32(&bar_sfull[set]), (sit / kSfSets) & 1u,
+                                                  abort, args.timeout_ns, args.status, 35)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after_sync();
                             }
-                            tc_fence_after_sync();
                         }
                         // K-block h of the stage: 128-byte chunk h of each operand's box
                         const uint32_t a0 = sA + s * kAStage + h * (kBM * kBK);
@@ -293,7 +361,7 @@ __global__ void __launch_bounds__(gmx::kThreads, 1)
         }
         if (lane == 0) bulk_wait_group_read<0>();  // the C stores have read their slots
         __syncwarp();
-    } else {
+    } else if constexpr (!kTmaSf) {
         // ------------------------------ scale writers (warps 6..9) ------------------------------
         // The (tile, group) sequence of this CTA, flattened so the gather of the next group
         // (possibly of the next tile) is in flight while the current one waits for a free set.

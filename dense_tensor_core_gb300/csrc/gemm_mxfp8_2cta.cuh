@@ -27,6 +27,13 @@
 //
 // Tensor Memory per CTA: accumulators at columns [0,224) and [224,448), scale sets at
 // 448 + 12*set (4 columns for A, 8 for B), set = 0..3.
+//
+// With kTmaSf (224-wide tiles) the scales come repacked by sf_pack_kernel, as in the one-CTA
+// kernel: each CTA's producer loads, beside the stage that holds a set's first K-block, the chunk
+// of its own 128 A rows and the two chunks of the tile's B rows (2-D boxes of 512 and 1024 bytes
+// completing on the leader's full barrier), and the leader's MMA thread moves them into both CTAs'
+// Tensor Memory with three tcgen05.cp.cta_group::2.32x128b.warpx4 before the set's first MMA (each
+// CTA copies from its own shared memory). No scale warps: 6 warps.
 #pragma once
 
 #include "gemm_mxfp8.cuh"
@@ -47,10 +54,13 @@ constexpr int kGroupM = 8;
 constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
 constexpr uint64_t kPeerSettleNs = 1000ull * 1000;
 
+constexpr int threads_for(bool tma_sf) { return tma_sf ? 192 : kThreads; }
+
 // Pair tile width kBN (224 or 256). Tensor Memory holds the accumulators and 4 scale sets: two
 // 224-column accumulators (448 + 48 <= 512 columns), or one 256-column accumulator (the epilogue of
-// a tile then finishes before the next tile's first MMA).
-template <int kBN>
+// a tile then finishes before the next tile's first MMA). With kTmaSf each stage has a 1.5 KB slot
+// for the chunks of a set that starts in it.
+template <int kBN, bool kTmaSf = false>
 struct Cfg {
     static constexpr int kHalfN = kBN / 2;
     static constexpr int kBStage = kHalfN * 128;
@@ -58,7 +68,9 @@ struct Cfg {
     static constexpr int kAccBufs = kBN == 256 ? 1 : 2;
     static constexpr int kAccStride = kBN;
     static constexpr int kSfBase = kAccBufs * kBN;
-    static constexpr int kSmemBytes = kStages * kStageBytes + kCBytes + 1024;
+    static constexpr int kSlotBytes = kTmaSf ? gmx::kSfSetBytes : 0;
+    static constexpr int kSmemBytes = kStages * (kStageBytes + kSlotBytes) + kCBytes + 1024;
+    static_assert(!kTmaSf || kBN == 224, "repacked scales on 224-wide pair tiles");
     static_assert(kBN == 224 || kBN == 256, "pair tiles 224 or 256 wide");
     static_assert(kAStage % 1024 == 0 && kBStage % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
     static_assert(kSmemBytes <= 227 * 1024 - 512, "shared memory budget");
@@ -67,14 +79,16 @@ struct Cfg {
 constexpr int kBN = 224;  // the default pair tile width
 }  // namespace gmx2
 
-template <bool kB32, int kBN>
-__global__ void __launch_bounds__(gmx2::kThreads, 1)
+template <bool kB32, int kBN, bool kTmaSf = false>
+__global__ void __launch_bounds__(gmx2::threads_for(kTmaSf), 1)
     gemm_mxfp8_2cta_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmC,
-                           const __grid_constant__ CUtensorMap tmC32, const GemmMxArgs args) {
+                           const __grid_constant__ CUtensorMap tmC32,
+                           const __grid_constant__ CUtensorMap tmSA,
+                           const __grid_constant__ CUtensorMap tmSB, const GemmMxArgs args) {
     using namespace gmx2;
-    using C_ = Cfg<kBN>;
+    using C_ = Cfg<kBN, kTmaSf>;
     constexpr int kHalfN = C_::kHalfN;
     constexpr int kBStage = C_::kBStage;
     constexpr int kStageBytes = C_::kStageBytes;
@@ -96,6 +110,7 @@ __global__ void __launch_bounds__(gmx2::kThreads, 1)
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t sA = base;
     const uint32_t sB = base + kStages * kAStage;
+    const uint32_t sSF = base + kStages * kStageBytes + kCBytes;  // kTmaSf: scale slots
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
@@ -143,7 +158,7 @@ __global__ void __launch_bounds__(gmx2::kThreads, 1)
         // ------------------------------ TMA producer (both CTAs) ------------------------------
         if (lane == 0) {
             uint32_t it = 0;
-            bool ok = true;
+            bool ok = true, chunks_ready = false;
             for (int t = pair; t < total && ok; t += num_pairs) {
                 int mt, nt;
                 tile_coords(t, args.num_m, args.num_n, kGroupM, mt, nt);
@@ -159,9 +174,26 @@ __global__ void __launch_bounds__(gmx2::kThreads, 1)
                     if (args.fault == 1 && it == 0) continue;  // test hook: stage never filled
                     const uint32_t full_local = smem_u32(&bar_full[s]);
                     const uint32_t full_leader = map_to_cta(full_local, 0);
-                    if (leader) mbar_arrive_expect_tx(full_local, args.stage_tx);  // both CTAs' bytes
+                    const bool set_start = kTmaSf && kb % grp == 0;
+                    if (leader)  // both CTAs' bytes
+                        mbar_arrive_expect_tx(full_local, args.stage_tx + (set_start ? 2 * gmx::kSfSetBytes : 0));
                     tma_load_2d_pair(sA + s * kAStage, &tmA, full_leader, kb * kBK, a_row);
                     tma_load_2d_pair(sB + s * kBStage, &tmB, full_leader, kb * kBK, b_row);
+                    if (set_start) {
+                        // this CTA's A chunk (its 128-row group) and the tile's two B chunks, as
+                        // rows of 128 bytes of the repacked arrays; the kernel that writes them
+                        // may still be running (it launched this one early)
+                        if (!chunks_ready) {
+                            grid_dependency_wait();
+                            chunks_ready = true;
+                        }
+                        const int g = kb / grp;
+                        const uint32_t slot = sSF + s * C_::kSlotBytes;
+                        tma_load_2d_pair(slot, &tmSA, full_leader, 0,
+                                         ((mt * 2 + (int)rank) * args.sf_sets + g) * 4);
+                        tma_load_2d_pair(slot + kSfChunkBytes, &tmSB, full_leader, 0,
+                                         (nt * args.sf_sets + g) * 8);
+                    }
                 }
             }
             if (!ok && leader) {
@@ -201,7 +233,7 @@ __global__ void __launch_bounds__(gmx2::kThreads, 1)
                 const uint32_t d_tmem = tmem_base + b * kAccStride;
                 for (int kb = 0; kb < args.num_kb; ++kb) {
                     const uint32_t set = sit % kSfSets;
-                    if (kb % grp == 0) {  // the first K-block of a scale set
+                    if (!kTmaSf && kb % grp == 0) {  // the first K-block of a scale set
                         if (!wait_bounded<true>(smem_u32(&bar_sfull[set]), (sit / kSfSets) & 1u,
                                                 abort, args.timeout_ns, args.status, 45)) {
                             ok = false;
@@ -214,6 +246,26 @@ __global__ void __launch_bounds__(gmx2::kThreads, 1)
                         break;
                     }
                     tc_fence_after_sync();
+                    if constexpr (kTmaSf) {
+                        if (kb % grp == 0) {
+                            // the set's columns are free once the MMAs that last read them are
+                            // done; then both CTAs copy the set from the stage's slot
+                            if (!wait_bounded(smem_u32(&bar_sempty[set]),
+                                              ((sit / kSfSets) & 1u) ^ 1u, abort, args.timeout_ns,
+                                              args.status, 47)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after_sync();
+                            const uint32_t slot = sSF + s * C_::kSlotBytes;
+                            const uint32_t col = tmem_base + kSfBase + set * kSfSet;
+                            tmem_cp_32x128b_x4_cta2(col, smem_desc_plain(slot, 128, 128));
+                            tmem_cp_32x128b_x4_cta2(
+                                col + 4, smem_desc_plain(slot + kSfChunkBytes, 128, 128));
+                            tmem_cp_32x128b_x4_cta2(
+                                col + 8, smem_desc_plain(slot + 2 * kSfChunkBytes, 128, 128));
+                        }
+                    }
                     const uint32_t a_lo = (uint32_t)a_desc0 + s * (uint32_t)(kAStage >> 4);
                     const uint32_t b_lo = (uint32_t)b_desc0 + s * (uint32_t)(kBStage >> 4);
                     const uint32_t sfa = tmem_base + kSfBase + set * kSfSet;
@@ -274,7 +326,7 @@ __global__ void __launch_bounds__(gmx2::kThreads, 1)
         }
         if (lane == 0) bulk_wait_group_read<0>();  // the C stores have read their slots
         __syncwarp();
-    } else {
+    } else if constexpr (!kTmaSf) {
         // ------------------------------ scale writers (warps 6..9, both CTAs) ----------------
         // The (tile, group) sequence of this pair, flattened so the gather of the next group
         // (possibly of the next tile) is in flight while the current one waits for a free set.

@@ -60,7 +60,26 @@ struct Operands {
 struct Plan {
     int variant = 0, tile_m = 0, tile_n = 0, tile_k = 64, stages = 0, split_k = 1, ctas = 0,
         tiles = 0, cluster = 1, sk_tiles = 0;
+    bool sf_pack = false;  // block-scaled one-CTA kernel: scales repacked into the workspace
 };
+
+// Repacked scale arrays of the block-scaled product in a workspace (sf_pack.cuh): the chunks of A
+// (128-row groups, one 128-row half) from byte 0, those of B (tile_n-row groups, two halves) from
+// the next 1 KB boundary.
+struct SfPackLayout {
+    int sets = 0, groups_a = 0, groups_b = 0;
+    uint64_t b_offset = 0, bytes = 0;
+};
+inline SfPackLayout sf_pack_layout(int64_t M, int64_t N, int64_t sf_cols, int tile_n) {
+    SfPackLayout l;
+    l.sets = (int)((sf_cols + 3) / 4);
+    l.groups_a = (int)((M + 127) / 128);
+    l.groups_b = (int)((N + tile_n - 1) / tile_n);
+    const uint64_t a = (uint64_t)l.groups_a * l.sets * 512;
+    l.b_offset = (a + 1023) / 1024 * 1024;
+    l.bytes = l.b_offset + (uint64_t)l.groups_b * l.sets * 2 * 512;
+    return l;
+}
 
 // Stream-K workspace of the pair kernel for `units` pairs and tile width bn: the flags (one
 // 32-bit word per CTA, padded to 1 KB, so at most 128 pairs), then one 128 x bn fp32 slot per CTA.
@@ -134,6 +153,24 @@ int launch_cluster(Kern kern, int grid, int threads, int smem, int cluster, cuda
                    const Params&... params) {
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = cluster_config(grid, threads, smem, cluster, stream, attr);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, params...);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    return GEMM_OK;
+}
+
+// As launch_cluster (one CTA per cluster), for a kernel that depends on the stream's previous
+// kernel only through data it reads after griddepcontrol.wait: the launch may begin while that
+// kernel still runs (programmatic stream serialisation), so its set-up overlaps the other's tail.
+template <typename Kern, typename... Params>
+int launch_dependent(Kern kern, int grid, int threads, int smem, cudaStream_t stream,
+                     const Params&... params) {
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = cluster_config(grid, threads, smem, 1, stream, attr);
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, params...);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");

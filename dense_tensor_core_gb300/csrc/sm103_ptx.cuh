@@ -297,6 +297,27 @@ __device__ __forceinline__ void bulk_copy_smem_to_cta(uint32_t dst, uint32_t src
         : "memory");
 }
 
+// Programmatic dependent launch: the grid launched after this one on the stream with
+// programmatic serialisation may start once every CTA of this grid has run
+// launch_dependents (or exited); a thread of that grid waits in dependency_wait until this grid
+// has completed and its memory operations are visible.
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Bulk copy of `bytes` contiguous bytes from global memory into this CTA's shared memory,
+// completing on this CTA's barrier `bar` (both addresses 16-byte aligned, bytes % 16 == 0).
+__device__ __forceinline__ void bulk_load_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 // 3-D forms (c0 innermost). With a tensor map that views a row-major [rows, K] operand as
 // {64, rows, K/64} (strides: row, 128 bytes), one instruction fetches a box {64, r, 2}: two
 // 128-byte K-chunks of r rows, written as two consecutive [r][64] 128B-swizzled blocks.
@@ -396,6 +417,30 @@ __device__ __forceinline__ void mma_mxf8_cta1(uint32_t d_tmem, uint64_t adesc, u
         " [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
+}
+
+// Shared-memory descriptor of an unswizzled operand (layout type 0): 8-row x 16-byte core
+// matrices of 128 contiguous bytes, `lbo_bytes` / `sbo_bytes` apart along the two dimensions.
+__device__ __forceinline__ uint64_t smem_desc_plain(uint32_t saddr, uint32_t lbo_bytes,
+                                                    uint32_t sbo_bytes) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
+}
+
+// Tensor Memory copy of a 32-row x 128-bit matrix from shared memory (descriptor `sdesc`, rows 16
+// bytes apart) into 4 columns at `taddr`, row i to lane i of each of the four 32-lane quarters
+// (.warpx4). Asynchronous; a later tcgen05.mma of the same thread sees the copied data (the two
+// form a pipeline), a tcgen05.commit tracks its completion.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
+}
+
+// CTA-pair form, issued by the leader: each CTA of the pair copies the matrix at `sdesc` in its
+// own shared memory into its own Tensor Memory at `taddr`.
+__device__ __forceinline__ void tmem_cp_32x128b_x4_cta2(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
 }
 
 // CTA-pair form of the block-scaled MMA (M = 256 over the two CTAs of the pair).

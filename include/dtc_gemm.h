@@ -108,12 +108,16 @@ typedef struct {
                              default, the pages' granularity) or 32 (the OCP MX block); the
                              scale arrays are then [rows, ceil(K / block)]. Non-default formats
                              or blocks run on the one-CTA kernel. */
-    void* workspace;      /* 16-bit products: device scratch for stream-K (see
-                             gemm_workspace_size), owned by the caller, 16-byte aligned; NULL =
-                             none. Its first 1 KB holds flags that must be zero before the first
-                             call that uses it; every completed call leaves them zero again (after
-                             a GEMM_ERR_TIMEOUT, zero them before reuse). Calls that may run at
-                             the same time (other streams) must not share a workspace. */
+    void* workspace;      /* device scratch owned by the caller, 16-byte aligned; NULL = none
+                             (see gemm_workspace_size). 16-bit products: stream-K; its first 1 KB
+                             holds flags that must be zero before the first call that uses it;
+                             every completed call leaves them zero again (after a
+                             GEMM_ERR_TIMEOUT, zero them before reuse). Block-scaled one-CTA
+                             kernel: a large enough workspace receives the scale arrays repacked
+                             by a first kernel of the call, from which the product kernel copies
+                             them into Tensor Memory (faster, above all with 32-element scale
+                             blocks); no initial contents needed. Calls that may run at the same
+                             time (other streams) must not share a workspace. */
     uint64_t workspace_bytes;
     int stream_k;         /* 0 = use stream-K when a large enough workspace is given and the
                              cost model prefers it; 1 = required (error if not possible); 2 = off.
@@ -181,6 +185,9 @@ typedef struct {
     int tiles;    /* output tiles (times split_k work units for SPLITK) */
     int cluster;  /* CTAs per cluster */
     int sk_tiles; /* tiles shared out by stream-K (0 = none) */
+    int sf_packed; /* block-scaled one-CTA kernel: 1 = the scales are repacked into the workspace
+                      and copied into Tensor Memory by the MMA thread (see gemm_options.workspace);
+                      0 = gathered by the kernel's scale warps */
 } gemm_plan_info;
 
 /* Fills *info with the launch that gemm_ex would make for these sizes and options on the current
@@ -264,9 +271,11 @@ int gemm_sp_workspace_size(int dtype, int64_t M, int64_t K, uint64_t* bytes);
 /*
  * Bytes of workspace (gemm_options.workspace) with which the call would use stream-K on CTA pairs
  * (the last, part-full wave's tiles shared out over all pairs as equal runs of K-blocks, the
- * pieces summed through the workspace); 0 when it would not (or stream_k == 2). The pages have
- * no counterpart: their persistent 2-CTA variant (05 Blackwell TCGEN05 GEMM tutorial,
- * "Advanced") takes whole tiles. INVALID_ARG as gemm_ex; bytes must not be NULL.
+ * pieces summed through the workspace); 0 when it would not (or stream_k == 2). For the
+ * block-scaled product (dtype 2) on the one-CTA kernel: the bytes of the repacked scale arrays
+ * (about the size of sfA and sfB together), 0 on the pair kernel. The pages have no counterpart:
+ * their persistent 2-CTA variant (05 Blackwell TCGEN05 GEMM tutorial, "Advanced") takes whole
+ * tiles. INVALID_ARG as gemm_ex; bytes must not be NULL.
  */
 int gemm_workspace_size(int dtype, int64_t M, int64_t N, int64_t K, int layout,
                         const gemm_options* opts, uint64_t* bytes);

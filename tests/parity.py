@@ -59,3 +59,25 @@ def sample_positions(M, N, count=2048, seed=0, tile_m=128, tile_n=256):
     pts += list(zip(r.tolist(), c.tolist()))
     pts = sorted(set(pts))
     return np.array([p[0] for p in pts], np.int64), np.array([p[1] for p in pts], np.int64)
+
+
+def with_packed_scales(M, N, K, kw):
+    """kw for a block-scaled gemm_ex call; `pack=True` in kw is replaced by a workspace of the size
+    gemm_workspace_size reports, so the one-CTA kernel takes its scales repacked there (checked
+    through the plan)."""
+    import dense_tensor_core_gb300 as dtc
+
+    kw = dict(kw)
+    if not kw.pop("pack", False):
+        return kw
+    size_kw = {k: kw[k] for k in ("variant", "tile_n", "tile_k") if k in kw}
+    for k_in, k_out in (("a_format", "a_format"), ("b_format", "b_format"), ("scale_block", "scale_block")):
+        if k_in in kw:
+            size_kw[k_out] = kw[k_in]
+    nbytes = dtc.gemm_workspace_size("mxfp8", M, N, K, **size_kw)
+    assert nbytes > 0
+    kw["workspace"] = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    plan_kw = {k: v for k, v in kw.items() if k in ("variant", "tile_n", "tile_k", "a_format",
+                                                    "b_format", "scale_block", "workspace")}
+    assert dtc.gemm_plan("mxfp8", M, N, K, **plan_kw)["sf_packed"] == 1
+    return kw

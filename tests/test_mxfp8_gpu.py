@@ -6,7 +6,7 @@ import torch
 
 import oracle
 from dense_tensor_core_gb300 import workloads
-from parity import check_close, sample_positions, to_device8, values16
+from parity import check_close, sample_positions, to_device8, values16, with_packed_scales
 
 pytestmark = pytest.mark.gpu
 
@@ -32,10 +32,17 @@ def _bench_inputs():
 def run_mx(A, B, sfA, sfB, **kw):
     import dense_tensor_core_gb300 as dtc
 
+    kw = with_packed_scales(A.shape[0], B.shape[0], _k_of(A, kw), kw)
     C = dtc.gemm_ex("mxfp8", to_device8(A), to_device8(B), sfA=to_device8(sfA),
                     sfB=to_device8(sfB), **kw)
     dtc.gemm_stream_status()
     return C.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _k_of(A, kw):
+    # K from A's stored row (bytes per row for fp8; fp6 / fp4 rows are packed)
+    bits = {"e4m3": 8, "e5m2": 8, "e2m3": 6, "e3m2": 6, "e2m1": 4}[kw.get("a_format", "e4m3")]
+    return A.shape[1] * 8 // bits
 
 
 def check_mx(A, B, sfA, sfB, what, **kw):
@@ -89,9 +96,10 @@ def test_unit_scales_reduce_to_plain_e4m3():
     check_mx(A, B, np.full_like(sfA, 127), np.full_like(sfB, 127), "unit scales")
 
 
-@pytest.mark.parametrize("variant,tile_k", [(1, 128), (1, 256), (2, 0)])
+@pytest.mark.parametrize("variant,tile_k,pack", [(1, 128, False), (1, 256, False), (2, 0, False),
+                                                (2, 0, True)])
 @pytest.mark.parametrize("which", ["a_rows", "b_rows", "k_blocks"])
-def test_scales_varying_along_one_axis(which, variant, tile_k):
+def test_scales_varying_along_one_axis(which, variant, tile_k, pack):
     # Scales that vary along a single axis: a wrong row / column / K-block mapping of the scale
     # layout in Tensor Memory shows up as a failure of exactly one of these.
     M, N, K = 256, 448, 1024
@@ -106,7 +114,7 @@ def test_scales_varying_along_one_axis(which, variant, tile_k):
     else:
         sfA[:] = (123 + (np.arange(kb) % 7))[None, :]
         sfB[:] = (130 - (np.arange(kb) % 5))[None, :]
-    check_mx(A, B, sfA, sfB, f"scales along {which}", variant=variant, tile_k=tile_k)
+    check_mx(A, B, sfA, sfB, f"scales along {which}", variant=variant, tile_k=tile_k, pack=pack)
 
 
 def test_wide_scale_range():
@@ -118,20 +126,21 @@ def test_wide_scale_range():
     check_mx(A, B, sfA, sfB, "wide scale range")
 
 
-@pytest.mark.parametrize("variant", [1, 2])
-def test_more_tiles_than_sms(variant):
+@pytest.mark.parametrize("variant,pack", [(1, False), (2, False), (2, True)])
+def test_more_tiles_than_sms(variant, pack):
     # 200 one-CTA tiles of 128 x 224 over 152 SMs, or 100 pair tiles over 76 pairs: persistent
     # loop, both accumulators, scale sets reused across tiles
     M, N, K = 2560, 2240, 256
     A, B, sfA, sfB = workloads.make_mxfp8(M, N, K, seed=6)
-    check_mx(A, B, sfA, sfB, "more tiles than SMs", variant=variant)
+    check_mx(A, B, sfA, sfB, "more tiles than SMs", variant=variant, pack=pack)
 
 
-@pytest.mark.parametrize("variant,tile_k", [(0, 0), (1, 128), (1, 256), (2, 0)])
-def test_benchmark_size_sampled(variant, tile_k):
+@pytest.mark.parametrize("variant,tile_k,pack", [(0, 0, False), (1, 128, False), (1, 256, False),
+                                                (2, 0, False), (2, 0, True)])
+def test_benchmark_size_sampled(variant, tile_k, pack):
     w = workloads.WORKLOADS["mxfp8_nt_4096x4096x8192"]
     A, B, sfA, sfB = _bench_inputs()
-    C = run_mx(A, B, sfA, sfB, variant=variant, tile_k=tile_k)
+    C = run_mx(A, B, sfA, sfB, variant=variant, tile_k=tile_k, pack=pack)
     r, c = sample_positions(w.M, w.N, count=3000, seed=w.seed, tile_m=128, tile_n=224)
     r = np.concatenate([r, np.full(w.N, 1000), np.arange(w.M)])
     c = np.concatenate([c, np.arange(w.N), np.full(w.M, 999)])
@@ -152,19 +161,23 @@ def test_k_zero_and_empty():
     assert torch.equal(C, torch.zeros_like(C))
 
 
-@pytest.mark.parametrize("variant", [1, 2])
-def test_timeout_reports_and_recovers(variant):  # (variant 1 takes 256-deep stages: K = 512)
+@pytest.mark.parametrize("variant,pack,block", [(1, False, 128), (2, False, 128), (1, True, 32),
+                                               (2, True, 128)])
+def test_timeout_reports_and_recovers(variant, pack, block):
     import dense_tensor_core_gb300 as dtc
 
     M, N, K = 256, 448, 512
-    A, B, sfA, sfB = workloads.make_mxfp8(M, N, K, seed=7)
+    A, B, sfA, sfB = workloads.make_mx(M, N, K, 7, block=block)
     dtc.gemm_stream_status()
+    kw = with_packed_scales(M, N, K, dict(variant=variant, pack=pack, scale_block=block))
     dtc.gemm_ex("mxfp8", to_device8(A), to_device8(B), sfA=to_device8(sfA), sfB=to_device8(sfB),
-                variant=variant, timeout_ns=20_000_000, fault_inject=1)
+                timeout_ns=20_000_000, fault_inject=1, **kw)
     with pytest.raises(dtc.GemmError) as e:
         dtc.gemm_stream_status()
     assert e.value.status == 4
-    check_mx(A, B, sfA, sfB, "after timeout", variant=variant)
+    C = run_mx_fmt(A, B, sfA, sfB, "e4m3", "e4m3", block, variant=variant, pack=pack)
+    ref = oracle.gemm_mx(A, B, sfA, sfB, M, N, K, block=block)
+    check_close(values16(C, "bf16"), values16(ref, "bf16"), "after timeout")
 
 
 def test_automatic_choice():
@@ -172,11 +185,18 @@ def test_automatic_choice():
 
     if torch.cuda.get_device_properties(0).multi_processor_count != 152:
         pytest.skip("the expected choices are worked out for 152 SMs")
-    # the pair kernel is an option (variant 2); the one-CTA kernel measured faster, with 256-deep
-    # stages when K % 128 == 0
+    # the pair kernel is an option (variant 2); the one-CTA kernel measured faster, with 128-deep
+    # stages (256-deep ones on request, K % 128 == 0)
     p = dtc.gemm_plan("mxfp8", 4096, 4096, 8192)
-    assert (p["variant"], p["tile_k"]) == (1, 256)
+    assert (p["variant"], p["tile_k"], p["sf_packed"]) == (1, 128, 0)
+    assert dtc.gemm_plan("mxfp8", 4096, 4096, 8192, tile_k=256)["tile_k"] == 256
     assert dtc.gemm_plan("mxfp8", 4096, 4096, 8208)["tile_k"] == 128
+    # a workspace: repacked scales for 32-element blocks (one-CTA) and on 224-wide pair tiles
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    assert dtc.gemm_plan("mxfp8", 1024, 1024, 1024, workspace=ws)["sf_packed"] == 0
+    assert dtc.gemm_plan("mxfp8", 1024, 1024, 1024, workspace=ws, scale_block=32)["sf_packed"] == 1
+    assert dtc.gemm_plan("mxfp8", 1024, 1024, 1024, workspace=ws, variant=2)["sf_packed"] == 1
+    assert dtc.gemm_plan("mxfp8", 1024, 1024, 1024, workspace=ws, variant=2, tile_n=256)["sf_packed"] == 0
     assert dtc.gemm_plan("mxfp8", 4096, 4096, 8192, variant=2)["variant"] == 2
     # the pair kernel's 128-deep stages are 2-D boxes: any K with 16-byte rows
     p = dtc.gemm_plan("mxfp8", 4096, 4096, 8208, variant=2)
@@ -189,25 +209,29 @@ def run_mx_fmt(A, B, sfA, sfB, a_fmt, b_fmt, block, **kw):
     return run_mx(A, B, sfA, sfB, a_format=a_fmt, b_format=b_fmt, scale_block=block, **kw)
 
 
-@pytest.mark.parametrize("variant,tile_k", [(1, 128), (1, 256), (2, 0)])
+@pytest.mark.parametrize("variant,tile_k,pack", [(1, 128, False), (1, 256, False), (2, 0, False),
+                                                (1, 128, True), (1, 256, True), (2, 0, True)])
 @pytest.mark.parametrize("block", [32, 128])
 @pytest.mark.parametrize("a_fmt,b_fmt", [("e5m2", "e5m2"), ("e4m3", "e5m2"), ("e5m2", "e4m3"),
                                          ("e4m3", "e4m3")])
 @pytest.mark.parametrize("M,N,K", [(256, 448, 1024), (300, 520, 400), (129, 232, 656),
                                    (256, 224, 384)])
-def test_formats_and_blocks_full_parity(M, N, K, a_fmt, b_fmt, block, variant, tile_k):
+def test_formats_and_blocks_full_parity(M, N, K, a_fmt, b_fmt, block, variant, tile_k, pack):
     if tile_k == 256 and K % 128:
         pytest.skip("256-deep stages need K % 128 == 0")
+    if pack and variant == 1 and block == 128:
+        pytest.skip("the one-CTA kernel repacks the scales of 32-element blocks only")
     A, B, sfA, sfB = workloads.make_mx(M, N, K, M + N + K + block, a_fmt, b_fmt, block)
-    C = run_mx_fmt(A, B, sfA, sfB, a_fmt, b_fmt, block, variant=variant, tile_k=tile_k)
+    C = run_mx_fmt(A, B, sfA, sfB, a_fmt, b_fmt, block, variant=variant, tile_k=tile_k, pack=pack)
     ref = oracle.gemm_mx(A, B, sfA, sfB, M, N, K, a_fmt=a_fmt, b_fmt=b_fmt, block=block)
     check_close(values16(C, "bf16"), values16(ref, "bf16"),
                 f"{a_fmt}x{b_fmt} block {block} {M}x{N}x{K} tile_k {tile_k}")
 
 
+@pytest.mark.parametrize("pack", [False, True])
 @pytest.mark.parametrize("tile_k", [128, 256])
 @pytest.mark.parametrize("which", ["a_rows", "b_rows", "k_blocks"])
-def test_block32_scales_varying_along_one_axis(which, tile_k):
+def test_block32_scales_varying_along_one_axis(which, tile_k, pack):
     # with 32-element blocks each MMA of a K-block takes its own scale byte: scales that vary along
     # K by 32-block pin that byte selection
     M, N, K = 256, 448, 1024
@@ -222,16 +246,17 @@ def test_block32_scales_varying_along_one_axis(which, tile_k):
     else:
         sfA[:] = (123 + (np.arange(kb) % 7))[None, :]
         sfB[:] = (130 - (np.arange(kb) % 5))[None, :]
-    C = run_mx_fmt(A, B, sfA, sfB, "e4m3", "e4m3", 32, variant=1, tile_k=tile_k)
+    C = run_mx_fmt(A, B, sfA, sfB, "e4m3", "e4m3", 32, variant=1, tile_k=tile_k, pack=pack)
     ref = oracle.gemm_mx(A, B, sfA, sfB, M, N, K, block=32)
     check_close(values16(C, "bf16"), values16(ref, "bf16"), f"block-32 scales along {which}")
 
 
+@pytest.mark.parametrize("pack", [False, True])
 @pytest.mark.parametrize("name", ["mxfp8_b32_nt_4096x4096x8192", "mx_e5m2_b32_nt_4096x4096x8192"])
-def test_format_workloads_sampled(name):
+def test_format_workloads_sampled(name, pack):
     w = workloads.WORKLOADS[name]
     A, B, sfA, sfB = workloads.make(w)
-    C = run_mx_fmt(A, B, sfA, sfB, w.a_fmt, w.b_fmt, w.block)
+    C = run_mx_fmt(A, B, sfA, sfB, w.a_fmt, w.b_fmt, w.block, pack=pack)
     r, c = sample_positions(w.M, w.N, count=3000, seed=w.seed, tile_m=128, tile_n=224)
     r = np.concatenate([r, np.full(w.N, 777), np.arange(w.M)])
     c = np.concatenate([c, np.arange(w.N), np.full(w.M, 555)])
@@ -244,7 +269,7 @@ def test_format_options_plan():
     import dense_tensor_core_gb300 as dtc
 
     p = dtc.gemm_plan("mxfp8", 4096, 4096, 8192, scale_block=32, a_format="e5m2")
-    assert (p["variant"], p["tile_k"]) == (1, 256)
+    assert (p["variant"], p["tile_k"]) == (1, 128)
     p = dtc.gemm_plan("mxfp8", 4096, 4096, 8192, variant=2, scale_block=32, b_format="e2m1")
     assert (p["variant"], p["tile_m"], p["tile_n"]) == (2, 256, 224)
 

@@ -45,7 +45,25 @@ def test_automatic_choice_on_gb300():
     p = plan("bf16", 1024, 1024, 512)  # 32 one-CTA tiles: a split needs 8 K-blocks per CTA
     assert p["variant"] == 1
     p = plan("mxfp8", 4096, 4096, 8192)
-    assert (p["variant"], p["tile_n"], p["tile_k"]) == (1, 224, 256)
+    assert (p["variant"], p["tile_n"], p["tile_k"], p["sf_packed"]) == (1, 224, 128, 0)
+
+
+def test_block_scaled_repacking_policy():
+    # with a workspace the scales are repacked for 32-element blocks on the one-CTA kernel and for
+    # every block on 224-wide pair tiles; a workspace too small leaves the scale warps in charge
+    ws = fake_workspace()
+    assert plan("mxfp8", 4096, 4096, 8192, workspace=ws)["sf_packed"] == 0
+    assert plan("mxfp8", 4096, 4096, 8192, workspace=ws, scale_block=32)["sf_packed"] == 1
+    assert plan("mxfp8", 4096, 4096, 8192, workspace=ws, scale_block=32, b_format="e2m1")["sf_packed"] == 1
+    assert plan("mxfp8", 4096, 4096, 8192, workspace=ws, variant=2)["sf_packed"] == 1
+    assert plan("mxfp8", 4096, 4096, 8192, workspace=ws, variant=2, tile_n=256)["sf_packed"] == 0
+    small = fake_workspace(1024)
+    assert plan("mxfp8", 4096, 4096, 8192, workspace=small, scale_block=32)["sf_packed"] == 0
+    # the chunk layout: 32 groups of 128 A rows and 19 tiles of 224 B rows, 64 sets (K / 128) of
+    # 512-byte chunks (B: two per set), B from the first 1 KB boundary after A
+    need = (32 * 64 * 512 + 1023) // 1024 * 1024 + 19 * 64 * 2 * 512
+    assert plan("mxfp8", 4096, 4096, 8192, workspace=fake_workspace(need), scale_block=32)["sf_packed"] == 1
+    assert plan("mxfp8", 4096, 4096, 8192, workspace=fake_workspace(need - 16), scale_block=32)["sf_packed"] == 0
 
 
 def test_stream_k_on_gb300():

@@ -12,7 +12,7 @@ import torch
 
 import oracle
 from dense_tensor_core_gb300 import workloads
-from parity import check_close, sample_positions, to_device8, values16
+from parity import check_close, sample_positions, to_device8, values16, with_packed_scales
 
 pytestmark = pytest.mark.gpu
 
@@ -29,9 +29,11 @@ def built():
 def run_bs(A, B, sfA, sfB, a_fmt, b_fmt, block, **kw):
     import dense_tensor_core_gb300 as dtc
 
+    K = A.shape[1] * 8 // {"e4m3": 8, "e5m2": 8, "e2m3": 6, "e3m2": 6, "e2m1": 4}[a_fmt]
+    kw = with_packed_scales(A.shape[0], B.shape[0], K,
+                            dict(kw, a_format=a_fmt, b_format=b_fmt, scale_block=block))
     C = dtc.gemm_ex("mxfp8", to_device8(A), to_device8(B), sfA=to_device8(sfA),
-                    sfB=to_device8(sfB), a_format=a_fmt, b_format=b_fmt,
-                    scale_block=block, **kw)
+                    sfB=to_device8(sfB), **kw)
     dtc.gemm_stream_status()
     return C.view(torch.int16).cpu().numpy().view(np.uint16)
 
@@ -49,7 +51,10 @@ PAIRS = [("e2m1", "e2m1"), ("e2m3", "e3m2"), ("e3m2", "e2m1"), ("e2m1", "e4m3"),
 
 
 KERNELS = {"1cta_128": dict(variant=1, tile_k=128), "1cta_256": dict(variant=1, tile_k=256),
-           "pair": dict(variant=2), "pair_256": dict(variant=2, tile_n=256)}
+           "pair": dict(variant=2), "pair_256": dict(variant=2, tile_n=256),
+           "1cta_128_packed": dict(variant=1, tile_k=128, pack=True),
+           "1cta_256_packed": dict(variant=1, tile_k=256, pack=True),
+           "pair_packed": dict(variant=2, pack=True)}
 
 
 @pytest.mark.parametrize("kernel", list(KERNELS))
@@ -58,15 +63,21 @@ KERNELS = {"1cta_128": dict(variant=1, tile_k=128), "1cta_256": dict(variant=1, 
 @pytest.mark.parametrize("M,N,K", [(128, 224, 128), (300, 520, 384), (256, 448, 1024), (1, 8, 128),
                                    (640, 904, 256)])
 def test_formats_full_parity(M, N, K, a_fmt, b_fmt, block, kernel):
+    kw = KERNELS[kernel]
+    if kw.get("pack") and kw["variant"] == 1 and block == 128:
+        pytest.skip("the one-CTA kernel repacks the scales of 32-element blocks only")
     # K = 128 and 384 leave a half-filled 256-deep stage; 300 x 520 and 640 x 904 partial tiles
     # (and a partial 256-row pair tile)
     check_bs(M, N, K, a_fmt, b_fmt, block, seed=M + N + K + block, **KERNELS[kernel])
 
 
-@pytest.mark.parametrize("variant,tile_n", [(1, 0), (2, 0), (2, 256)])
+@pytest.mark.parametrize("variant,tile_n,pack", [(1, 0, False), (2, 0, False), (2, 256, False),
+                                                (1, 0, True), (2, 0, True)])
 @pytest.mark.parametrize("which", ["A rows", "B rows", "K-blocks"])
 @pytest.mark.parametrize("block", [32, 128])
-def test_scales_varying_along_one_axis(which, block, variant, tile_n):
+def test_scales_varying_along_one_axis(which, block, variant, tile_n, pack):
+    if pack and variant == 1 and block == 128:
+        pytest.skip("the one-CTA kernel repacks the scales of 32-element blocks only")
     # fp4 operands with every element code 2 (= 1.0); scales vary along one axis only, so any
     # mixing of rows or blocks in the scale layout changes some output
     M, N, K = 256, 448, 512
@@ -82,7 +93,7 @@ def test_scales_varying_along_one_axis(which, block, variant, tile_n):
         sfB[:] = rng.integers(124, 131, (N, 1))
     else:
         sfA[:] = rng.integers(124, 131, (1, kb))
-    C = run_bs(A, B, sfA, sfB, "e2m1", "e2m1", block, variant=variant, tile_n=tile_n)
+    C = run_bs(A, B, sfA, sfB, "e2m1", "e2m1", block, variant=variant, tile_n=tile_n, pack=pack)
     ref = oracle.gemm_bs(A, B, sfA, sfB, M, N, K, a_fmt="e2m1", b_fmt="e2m1", block=block)
     assert np.array_equal(C, ref), which  # sums of powers of two: exact
 
@@ -119,13 +130,13 @@ def test_packed_rule_violations_are_refused():
                     sfB=to_device8(sfB), a_format="e2m1", b_format="e2m1", variant=2, tile_k=256)
 
 
-@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("variant,pack", [(1, False), (2, False), (1, True), (2, True)])
 @pytest.mark.parametrize("name", ["mxfp4_b32_nt_4096x4096x8192",
                                   "mxfp6_e2m3_e3m2_b32_nt_4096x4096x8192"])
-def test_benchmark_sizes_sampled(name, variant):
+def test_benchmark_sizes_sampled(name, variant, pack):
     w = workloads.WORKLOADS[name]
     A, B, sfA, sfB = workloads.make(w)
-    C = run_bs(A, B, sfA, sfB, w.a_fmt, w.b_fmt, w.block, variant=variant)
+    C = run_bs(A, B, sfA, sfB, w.a_fmt, w.b_fmt, w.block, variant=variant, pack=pack)
     r, c = sample_positions(w.M, w.N, count=3000, seed=w.seed, tile_n=224)
     r = np.concatenate([r, np.full(w.N, w.M // 3), np.arange(w.M)])
     c = np.concatenate([c, np.arange(w.N), np.full(w.M, w.N // 5)])
