@@ -15,6 +15,7 @@
 #include <cstdio>
 #include <cstring>
 
+#include "gemm16_2cta.cuh"
 #include "gemm16_splitk.cuh"
 #include "gemm_mxfp8_2cta.cuh"
 #include "host.h"
@@ -511,7 +512,7 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
     const bool b_mn = layout_b_mn(layout);  // B stored [K,N]: 64-column boxes
     const int sms = std::max(1, d.sms);
     const int pairs = resident_pairs(d);
-    if (want_n && want_n != 256 && want_n != 128 && want_n != 224)
+    if (want_n && want_n != 256 && want_n != 128 && want_n != 224 && want_n != 64)
         return fail(GEMM_ERR_UNSUPPORTED, "tile width %d is not offered", want_n);
     if (want_n == 224 && b_mn && v == GEMM_VARIANT_1CTA)
         return fail(GEMM_ERR_UNSUPPORTED, "224-wide one-CTA tiles need B stored [N,K]");
@@ -580,6 +581,7 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
     if (split != 0 && split != 2 && split != 4)
         return fail(GEMM_ERR_INVALID_ARG, "split_k %d is not 2 or 4", split);
     int split_n = want_n;
+    int auto_n = 0;
     if (v == GEMM_VARIANT_AUTO && split == 0 && want_n != 224 && tiles256 * 2 <= sms) {
         // Fewer 128 x 256 tiles than half the SMs: split K over a cluster of 2 or 4 CTAs per
         // 128 x 128 or 128 x 256 tile. Take the (width, split) that occupies the most SMs in one
@@ -608,6 +610,19 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
                 split_n = c.bn;
             }
         }
+        // 256 x 128 pair tiles (4 stages of 128 K-elements) load as many bytes per CTA as 128 x 256
+        // tiles split in 2 and need no exchange of partial sums: taken when they give at least as
+        // many CTAs as the best split, fit in one wave and fill most of their 256 rows (512 x 4096 x
+        // 4096: 22.6 us against 24.6 split; 1024 x 2048 x 2048: 16.4 against 16.5; 1024^3, with
+        // half the CTAs of a 128 x 128 split: 12.7 against 12.3, so not taken there)
+        const int64_t pair128 = (int64_t)ceil_div(M, 256) * ceil_div(N, 128);
+        const bool rows_filled = M >= 256 && (M % 256 == 0 || M % 256 > 128);
+        if (!want_n && rows_filled && K % 64 == 0 && pair128 <= pairs && 2 * pair128 >= best_ctas &&
+            best_ctas > 0) {
+            v = GEMM_VARIANT_2CTA;
+            auto_n = 128;
+            split = 0;
+        }
         if (split) v = GEMM_VARIANT_SPLITK;
     }
     if (v == GEMM_VARIANT_SPLITK) {
@@ -633,8 +648,8 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
         p->ctas = p->tiles * p->split_k;
         return GEMM_OK;
     }
-    if (want_n == 128) return fail(GEMM_ERR_UNSUPPORTED, "128-wide tiles are offered by the split-K kernel only");
-    int auto_n = 0;
+    if ((want_n == 128 || want_n == 64) && v != GEMM_VARIANT_2CTA)
+        return fail(GEMM_ERR_UNSUPPORTED, "%d-wide tiles are offered by the split-K (128) and pair kernels only", want_n);
     if (v == GEMM_VARIANT_AUTO) {
         // Cheapest (variant, width) by the cost model; 224-wide tiles exist for a K-major B (NT,
         // TT) only. Below one wave of tiles either way, the one-CTA kernel (shorter ring fill)
@@ -699,8 +714,10 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
         if (bk == 128 && K % 64)
             return fail(GEMM_ERR_UNSUPPORTED, "128-deep pair stages need K %% 64 == 0");
         if (bk == 0) bk = K % 64 == 0 ? 128 : 64;
+        if (p->tile_n <= 128 && bk != 128)
+            return fail(GEMM_ERR_UNSUPPORTED, "%d-wide pair tiles take 128-deep stages (K %% 64 == 0)", p->tile_n);
         p->tile_k = bk;
-        p->stages = bk == 128 ? 3 : 6;
+        p->stages = dtc::g2::stages_for(p->tile_n, bk);
         p->tiles = ceil_div(M, 256) * ceil_div(N, p->tile_n);
         p->ctas = 2 * std::min(p->tiles, pairs);
     }

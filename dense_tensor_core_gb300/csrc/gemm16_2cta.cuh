@@ -48,6 +48,11 @@ constexpr uint64_t kPeerSettleNs = 1000ull * 1000;  // 1 ms
 // A B stored [K,N] (kBMN) is loaded as 64-column boxes, kBBoxes per CTA; with a 224-wide tile a
 // CTA's 112 columns take two boxes, the second only partly used (the MMA reads 112 columns through
 // the MN-major descriptor), so its stage holds whole boxes.
+// Ring depth: 6 stages of 64-deep K-blocks; of 128-deep ones 3 for 224- and 256-wide tiles and 4
+// for the narrow 64- and 128-wide tiles of small products (a CTA of 1024-deep K then has half its
+// K range in flight at once).
+constexpr int stages_for(int bn, int bk) { return bk == 128 ? (bn <= 128 ? 4 : 3) : 6; }
+
 template <int kBN, int kBK, int kStages, bool kBMN = false>
 struct Cfg {
     static constexpr int kHalfN = kBN / 2;

@@ -9,12 +9,9 @@
 namespace dtc_host {
 namespace pair16 {
 
-// Ring depth: 6 stages of 64-deep K-blocks, or 3 of 128-deep ones.
-constexpr int stages(int bk) { return bk == 128 ? 3 : 6; }
-
 template <bool kBF16, bool kAMN, bool kNN, int kBN, int kBK, bool kSK = false>
 int launch(const Launch& L) {
-    constexpr int kStages = stages(kBK);
+    constexpr int kStages = dtc::g2::stages_for(kBN, kBK);
     using Cfg = dtc::g2::Cfg<kBN, kBK, kStages, kNN>;
     const Operands& ops = *L.ops;
     const CUtensorMapDataType dt = kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -39,6 +36,8 @@ int by_shape(const Launch& L) {
     }
     if (p.tile_k == 128) {
         if (p.tile_n == 224) return launch<kBF16, kAMN, kNN, 224, 128>(L);
+        if (p.tile_n == 128) return launch<kBF16, kAMN, kNN, 128, 128>(L);
+        if (p.tile_n == 64) return launch<kBF16, kAMN, kNN, 64, 128>(L);
         return launch<kBF16, kAMN, kNN, 256, 128>(L);
     }
     if (p.tile_n == 224) return launch<kBF16, kAMN, kNN, 224, 64>(L);

@@ -162,6 +162,21 @@ def test_pair_kernel_configurations_full_parity(M, N, K, layout, tile_n, tile_k)
     full_check("f16", layout, M, N, K, seed=M + K + 1, variant=2, tile_n=tile_n, tile_k=tile_k)
 
 
+@pytest.mark.parametrize("tile_n", [128, 64])
+@pytest.mark.parametrize("layout", ["NT", "NN", "TN", "TT"])
+@pytest.mark.parametrize("M,N,K", [(640, 520, 192), (384, 200, 320), (256, 64, 64), (1280, 1792, 1024)])
+def test_pair_kernel_narrow_tiles_full_parity(M, N, K, layout, tile_n):
+    # 256 x 128 and 256 x 64 pair tiles (4 stages of 128 K-elements): each CTA holds 64 or 32 rows
+    # of B; a B stored [K,N] comes in one 64-column box per CTA, of which the MMA reads the first 32
+    # columns when the tile is 64 wide. 520 and 200 columns end in a partial tile
+    import dense_tensor_core_gb300 as dtc
+
+    p = dtc.gemm_plan("bf16", M, N, K, layout, variant=2, tile_n=tile_n)
+    assert (p["tile_m"], p["tile_n"], p["tile_k"], p["stages"]) == (256, tile_n, 128, 4)
+    full_check("bf16", layout, M, N, K, seed=M + K + tile_n, variant=2, tile_n=tile_n)
+    full_check("f16", layout, M, N, K, seed=M + K + tile_n + 1, variant=2, tile_n=tile_n)
+
+
 @pytest.mark.parametrize("M,N,tile_n", [(4096, 4096, 224), (8192, 8192, 256), (512, 448, 224)])
 def test_pair_tile_width_choice(M, N, tile_n):
     import dense_tensor_core_gb300 as dtc

@@ -128,3 +128,22 @@ def test_removed_options_are_refused():
     # the one-CTA kernel takes 64-deep stages only
     with pytest.raises(dtc.GemmError):
         plan("bf16", 1024, 1024, 1024, variant=1, tile_k=32)
+
+
+def test_narrow_pair_tiles_for_few_long_tiles():
+    # 256 x 128 pair tiles when they give as many CTAs as the best K-split (no exchange of partial
+    # sums), fit one wave of 76 pairs and fill their 256 rows
+    p = plan("bf16", 512, 4096, 4096)
+    assert (p["variant"], p["tile_m"], p["tile_n"], p["tile_k"], p["stages"], p["ctas"]) == (2, 256, 128, 128, 4, 128)
+    assert plan("bf16", 1024, 2048, 2048)["tile_n"] == 128
+    # half the CTAs of a 128 x 128 split in 2: split-K stays
+    assert plan("bf16", 1024, 1024, 1024)["variant"] == 3
+    # M = 128 would leave half of every pair tile empty; K % 64 != 0 has no 128-deep stages
+    assert plan("bf16", 128, 8192, 8192)["variant"] == 3
+    assert plan("bf16", 512, 4096, 4072)["variant"] == 3
+    # forced widths and the refusals
+    assert plan("bf16", 1024, 1024, 1024, variant=2, tile_n=64)["stages"] == 4
+    with pytest.raises(dtc.GemmError):
+        plan("bf16", 1024, 1024, 1024, variant=2, tile_n=64, tile_k=64)
+    with pytest.raises(dtc.GemmError):
+        plan("bf16", 1024, 1024, 1024, variant=1, tile_n=64)
