@@ -555,11 +555,17 @@ def device_inputs(w, dev):
 
 def gemm_kwargs(args, w, dtc, dev):
     """Options of the call a user would make for this workload: the automatic plan, and the
-    stream-K workspace the library asks for (zero-filled before first use)."""
+    workspace the library asks for (stream-K: zero-filled before first use; block-scaled: the
+    repacked scales)."""
     import torch
 
     if w.kind == "mxfp8":
-        return dict(a_format=w.a_fmt, b_format=w.b_fmt, scale_block=w.block, variant=args.variant)
+        kw = dict(a_format=w.a_fmt, b_format=w.b_fmt, scale_block=w.block, variant=args.variant)
+        ws_bytes = dtc.gemm_workspace_size("mxfp8", w.M, w.N, w.K, "NT", variant=args.variant,
+                                           a_format=w.a_fmt, b_format=w.b_fmt, scale_block=w.block)
+        if ws_bytes:
+            kw["workspace"] = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        return kw
     base = w.kind[:-5] if w.kind.endswith("_sp24") else w.kind
     kw = dict(layout=w.layout, variant=args.variant, split_k=args.split_k, tile_n=args.tile_n)
     if args.stream_k != 2:
@@ -594,6 +600,11 @@ def plan_of(dtc, w, kw):
         kw["workspace"] = kw.pop("sk_workspace", None)
         return dtc.gemm_plan(w.kind[:-5], w.M, w.N, w.K, **{k: v for k, v in kw.items() if k in keys})
     return dtc.gemm_plan(w.kind, w.M, w.N, w.K, **{k: v for k, v in kw.items() if k in keys})
+
+
+def launches_per_step(w, plan):
+    """Our kernels in one step: the GEMM, plus the 2:4 expansion or the scale repacking."""
+    return 2 if w.kind.endswith("_sp24") or plan.get("sf_packed") else 1
 
 
 def timed_steps(step, flush_l2, steps, warmup, stream, dev, world):
@@ -678,7 +689,7 @@ def run_ours(args, w):
         plan = plan_of(dtc, w, kw)
         step_ms, t0, t1 = timed_steps(lambda: call(dtc, w, dev_in, C, kw, stream), flush_l2,
                                       args.steps, args.warmup, stream, dev, world)
-        launches += args.steps
+        launches += args.steps * launches_per_step(w, plan)
         dtc.gemm_stream_status(stream)
         clocks = clk.record(t0, t1)
 
@@ -700,7 +711,7 @@ def run_ours(args, w):
         e2e_ms = run_e2e(w, dtc, host_in, dev_in, C, host_out,
                          lambda ins, Cout, st: call(dtc, w, ins, Cout, kw, st), stream, e2e_steps,
                          dev)
-        launches += e2e_steps
+        launches += e2e_steps * launches_per_step(w, plan)
         e2e_ms = max_over_ranks(e2e_ms, world)
         dtc.gemm_stream_status(stream)
         h2d = sum(t.numel() * t.element_size() for t in host_in)
@@ -727,7 +738,7 @@ def run_ours(args, w):
                     cms_list, ct0, ct1 = timed_steps(
                         lambda: call(dtc, cw, cin, cC, ckw, stream), flush_l2, cfg_steps, 5,
                         stream, dev, world)
-                    launches += cfg_steps
+                    launches += cfg_steps * launches_per_step(cw, cplan)
                     dtc.gemm_stream_status(stream)
                     cms = statistics.mean(cms_list)
                     cname = kernel_of(cw, cplan)
@@ -785,8 +796,9 @@ def run_ours(args, w):
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "mode": "pipelined: step i+1's H2D and step i-1's D2H overlap step i's GEMM "
                         "(3 streams, 2 device buffers); pinned host memory"},
-        # our kernels per timed step of the headline: the GEMM (and the sparse expansion)
-        "gpu_launches": args.steps * (2 if w.kind.endswith("_sp24") else 1),
+        # our kernels per timed step of the headline: the GEMM (and the sparse expansion or the
+        # scale repacking)
+        "gpu_launches": args.steps * launches_per_step(w, plan),
         "gpu_launches_whole_run": launches,  # with the end-to-end steps and the other configs
         "clocks": clocks,
         "library_context": library,

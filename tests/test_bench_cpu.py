@@ -132,3 +132,14 @@ def test_baseline_configs_name_known_workloads():
     assert ids == ["1", "2", "3", "4a", "4b", "5"]
     for _, name, bound in bench.BASELINE_CONFIGS:
         assert name in workloads.WORKLOADS and bound in ("latency", "tensor", "hbm")
+
+
+def test_launches_per_step_counts_the_extra_kernels():
+    import bench
+    from dense_tensor_core_gb300 import workloads
+
+    W = workloads.WORKLOADS
+    assert bench.launches_per_step(W["bf16_nt_4096x4096x8192"], {"sf_packed": 0}) == 1
+    assert bench.launches_per_step(W["bf16_sp24_nt_4096x4096x8192"], {"sf_packed": 0}) == 2
+    assert bench.launches_per_step(W["mxfp8_b32_nt_4096x4096x8192"], {"sf_packed": 1}) == 2
+    assert bench.launches_per_step(W["mxfp8_nt_4096x4096x8192"], {"sf_packed": 0}) == 1
