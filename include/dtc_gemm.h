@@ -86,12 +86,13 @@ typedef struct {
                              stage, so the consumer's bounded wait runs out and the call reports
                              GEMM_ERR_TIMEOUT through gemm_stream_status. */
     int tile_n;           /* force the N-tile: 256, 224 (not SPLITK; one-CTA tiles need B stored
-                             [N,K]; block-scaled: 224, or 256 on CTA pairs) or 128 (SPLITK only);
-                             0 = choose */
+                             [N,K]; block-scaled: 224, or 256 on CTA pairs), 128 (SPLITK and
+                             2CTA) or 64 (2CTA); 0 = choose. 2CTA tiles of 128 or 64 take 128-deep
+                             stages (K % 64 == 0) */
     int tile_k;           /* K-elements per pipeline stage: 64 (1CTA), 64 or 128 (2CTA; SPLITK
-                             with 128-wide tiles; 128 needs K % 64 == 0), 128 or 256 (block-scaled
-                             one-CTA kernel; 256 needs K % 128 == 0), 128 (block-scaled pair
-                             kernel); 0 = choose */
+                             with 128-wide tiles; 128 needs K % 64 == 0), 128 (the default) or 256
+                             (block-scaled one-CTA kernel; 256 needs K % 128 == 0), 128
+                             (block-scaled pair kernel); 0 = choose */
     int64_t lda;          /* elements between consecutive stored rows of A, B, C; 0 = dense (the */
     int64_t ldb;          /* row length: K or M for A, K or N for B, N for C). At least the row */
     int64_t ldc;          /* length, and rows must start 16 bytes apart (ld x element size %
