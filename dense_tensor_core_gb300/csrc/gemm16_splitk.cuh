@@ -83,6 +83,14 @@ struct Cfg {
 };
 }  // namespace gsk
 
+// One arrival on bar_ack of every other CTA of the cluster (release at cluster scope).
+template <int kS>
+__device__ __forceinline__ void ack_peers_n(uint32_t rank, uint32_t bar_ack) {
+#pragma unroll
+    for (uint32_t r = 0; r < (uint32_t)kS; ++r)
+        if (r != rank) mbar_arrive_cluster(map_to_cta(bar_ack, r));
+}
+
 template <bool kBF16, bool kAMN, bool kNN, int kBN, int kBK, int kStages, int kS>
 __global__ void __launch_bounds__(gsk::kThreads, 1)
     gemm16_splitk_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -98,6 +106,7 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
     __shared__ __align__(8) uint64_t bar_tfull;
     __shared__ __align__(8) uint64_t bar_xchg[C_::kPieces];
     __shared__ __align__(8) uint64_t bar_drain;
+    __shared__ __align__(8) uint64_t bar_ack;  // every owner this CTA copied into has seen it land
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
@@ -130,6 +139,7 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
                 mbar_arrive_expect_tx(smem_u32(&bar_xchg[c]), C_::kColPieceBytes);
         }
         mbar_init(smem_u32(&bar_drain), 1);
+        mbar_init(smem_u32(&bar_ack), kS - 1);  // one acknowledgement from each other CTA
         abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -289,6 +299,8 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
                     if (!xok) break;
                     // the phase has completed: every lane takes its own acquire of it
                     (void)mbar_try_wait_cluster(smem_u32(&bar_xchg[j]), 0);
+                    if (j == C_::kOwnPieces - 1 && q == 0 && lane == 0)
+                        ack_peers_n<kS>(rank, smem_u32(&bar_ack));  // every copy into this CTA landed
                     const uint32_t xrow = sX + (j * kBM + q * 32 + lane) * C_::kXPitch;
                     float acc[64];
 #pragma unroll
@@ -378,6 +390,8 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
                     if (!xok) break;
                     // the phase has completed: every lane takes its own acquire of it
                     (void)mbar_try_wait_cluster(smem_u32(&bar_xchg[c]), 0);
+                    if (c == C_::kPieces - 1 && qb == 0 && lane == 0)
+                        ack_peers_n<kS>(rank, smem_u32(&bar_ack));  // every copy into this CTA landed
                     float acc[64];
                     // sum over source ranks 0..kS-1 in that order (own rows from Tensor Memory)
     #pragma unroll
@@ -417,7 +431,11 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
     if (!cluster_waited) cluster_wait();  // complete the start-up cluster barrier
     tc_fence_before_sync();
     __syncthreads();
-    cluster_sync();  // owners have seen every copy land: none is in flight into or out of a CTA
+    // Every copy into this CTA has landed (its owners waited for them); the copies out of it read
+    // its shared memory until they land: each other CTA acknowledges when all of them have, so the
+    // CTA (and its shared memory) stays until then. No cluster-wide barrier at exit.
+    if (threadIdx.x == 0 && !*abort)
+        (void)wait_bounded<true>(smem_u32(&bar_ack), 0, abort, args.timeout_ns, args.status, 26);
     if (*abort && threadIdx.x == 0) {
         // After a timeout an owner may have stopped waiting: give copies still in flight a
         // fixed, bounded time to land before the CTAs' shared memory is released.
