@@ -345,19 +345,30 @@ def gemm_workspace_size(kind, M, N, K, layout="NT", variant=0, tile_n=0, tile_k=
 
 
 def gemm_ex_static_workspace(kind, A, B, C=None, layout="NT", variant=0, tile_n=0, tile_k=0,
-                             stream_k=0, stream=None):
-    """gemm_ex for the 16-bit products, with the library's own (module-memory) stream-K workspace:
-    allocates nothing. Calls on one device must not overlap (they share that workspace)."""
-    dt = torch.bfloat16 if kind == "bf16" else torch.float16
-    _check_tensor(A, dt, "A", rows_of_larger=True)
-    _check_tensor(B, dt, "B", rows_of_larger=True)
-    M, N, K = _shapes16(A, B, layout)
-    C = _out(C, M, N, dt, A.device, rows_of_larger=True)
-    opts = _options(variant, 0, 0, 0, tile_n, tile_k, _ld(A), _ld(B), _ld(C),
-                    stream_k=stream_k)
-    dev = _same_device(A, B, C)
+                             stream_k=0, stream=None, sfA=None, sfB=None, a_format="e4m3",
+                             b_format="e4m3", scale_block=0):
+    """gemm_ex with the library's own workspace (a region of module memory) instead of a caller's:
+    allocates nothing. It serves stream-K of the 16-bit products and the repacked scales of the
+    block-scaled product ("mxfp8": sfA / sfB and the formats as in gemm_ex). Calls on one device
+    must not overlap (they share that region)."""
+    if kind == "mxfp8":
+        M, N, K = _check_mxfp8(A, B, sfA, sfB, rows_of_larger=True,
+                               scale_block=scale_block or 128, a_format=a_format,
+                               b_format=b_format)
+        C = _out(C, M, N, torch.bfloat16, A.device, rows_of_larger=True)
+        lda, ldb = _ld_elems(A, a_format), _ld_elems(B, b_format)
+    else:
+        dt = torch.bfloat16 if kind == "bf16" else torch.float16
+        _check_tensor(A, dt, "A", rows_of_larger=True)
+        _check_tensor(B, dt, "B", rows_of_larger=True)
+        M, N, K = _shapes16(A, B, layout)
+        C = _out(C, M, N, dt, A.device, rows_of_larger=True)
+        lda, ldb = _ld(A), _ld(B)
+    opts = _options(variant, 0, 0, 0, tile_n, tile_k, lda, ldb, _ld(C), a_format, b_format,
+                    scale_block, stream_k=stream_k)
+    dev = _same_device(A, B, C, sfA, sfB)
     with torch.cuda.device(dev):
-        _check(lib().gemm_ex_static_workspace(_DTYPE[kind], _ptr(A), _ptr(B), None, None,
+        _check(lib().gemm_ex_static_workspace(_DTYPE[kind], _ptr(A), _ptr(B), _ptr(sfA), _ptr(sfB),
                                               _ptr(C), M, N, K, _layout_code(layout),
                                               ctypes.byref(opts), _stream_handle(stream, dev)))
     return C

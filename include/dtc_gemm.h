@@ -223,19 +223,22 @@ int gemm_plan_model(const gemm_device_model* model, int dtype, int64_t M, int64_
                     int layout, const gemm_options* opts, gemm_plan_info* info);
 
 /*
- * gemm_ex, with the library's own stream-K workspace instead of a caller's: a 20 MiB region of
- * module memory (a file-scope device array, zero when the library is loaded), so this call
- * allocates nothing, on the host or the device. The pages have no counterpart.
+ * gemm_ex, with the library's own workspace instead of a caller's: a 20 MiB region of module
+ * memory (a file-scope device array, zero when the library is loaded), so this call allocates
+ * nothing, on the host or the device. The pages have no counterpart.
  *   - opts->workspace must be NULL (INVALID_ARG otherwise); the other options are gemm_ex's.
+ *   - The region serves as the stream-K workspace of the 16-bit products and as the home of the
+ *     repacked scales of the block-scaled product (see gemm_options.workspace).
  *   - 20 MiB holds the stream-K workspace of up to 79 resident CTA pairs (devices of up to 158
  *     SMs). A plan that would need more runs without stream-K, or fails with INVALID_ARG when
- *     opts->stream_k = 1 (required).
- *   - The first call on a device looks up the region's address with cudaGetSymbolAddress (a
- *     synchronous call): make one call on the device before capturing a stream into a graph.
- *   - The region's first 1 KB (flags) must be zero when a launch starts: a call whose plan uses
- *     stream-K clears it with cudaMemsetAsync on `stream` just before its launch (so a call after
- *     a GEMM_ERR_TIMEOUT starts clean); a call rejected by its argument checks, or whose plan
- *     takes whole tiles, enqueues nothing but its own kernel.
+ *     opts->stream_k = 1 (required); block-scaled scales that do not fit stay with the scale
+ *     warps.
+ *   - The first call on a device looks up the region's address with cudaGetSymbolAddress, a
+ *     synchronous call.
+ *   - The region's first 1 KB (flags) must be zero when a stream-K launch starts: a call whose
+ *     plan uses stream-K clears it with cudaMemsetAsync on `stream` just before its launch (so a
+ *     call after a GEMM_ERR_TIMEOUT starts clean); a call rejected by its argument checks
+ *     enqueues nothing, one that takes whole tiles only its kernels.
  *   - There is one region per device: calls that may overlap (on different streams, or from
  *     different threads) race on it and may return wrong results. Serialise them.
  */
