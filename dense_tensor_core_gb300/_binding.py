@@ -334,8 +334,8 @@ def gemm_stream_status(stream=None):
 def gemm_workspace_size(kind, M, N, K, layout="NT", variant=0, tile_n=0, tile_k=0, stream_k=0,
                         a_format="e4m3", b_format="e4m3", scale_block=0):
     """Bytes of workspace the call can use: for the 16-bit products the stream-K workspace (0 if
-    stream-K would not be used); for the block-scaled product on the one-CTA kernel the repacked
-    scale arrays (0 on the pair kernel)."""
+    stream-K would not be used); for the block-scaled product the repacked scale arrays when the
+    plan would use them (0 otherwise)."""
     opts = _options(variant, 0, 0, 0, tile_n, tile_k, a_format=a_format, b_format=b_format,
                     scale_block=scale_block, stream_k=stream_k)
     out = ctypes.c_uint64(0)

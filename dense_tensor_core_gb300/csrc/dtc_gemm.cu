@@ -522,22 +522,33 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
         if (want_n && want_n != 224 && !(want_n == 256 && v == GEMM_VARIANT_2CTA))
             return fail(GEMM_ERR_UNSUPPORTED, "the block-scaled kernels use 224-wide tiles (256 "
                         "on CTA pairs)");
-        // The one-CTA kernel (128 x 224 tiles, 2 stages of 256 K-elements or 4 of 128) or the
-        // pair kernel (256 x 224 or 256 x 256 tiles, 6 stages of 128 K-elements per CTA). The
-        // pair kernel is correct for every format but measured slower on GB300 (4096 x 4096 x
-        // 8192 e4m3: 137 us against 111; 256-wide pair tiles 139 us): AUTO takes the one-CTA
-        // kernel.
-        if (v == GEMM_VARIANT_AUTO) v = GEMM_VARIANT_1CTA;
+        // The one-CTA kernel (128 x 224 tiles, 4 stages of 128 K-elements or 2 of 256) or the
+        // pair kernel (256 x 224 or 256 x 256 tiles, 6 stages of 128 K-elements per CTA, or 3 of
+        // 256 with repacked scales). AUTO takes the pair kernel with 256-deep stages for
+        // 128-element scale blocks when a workspace holds the repacked scales, K % 128 == 0 and
+        // the pair tiles fill at least one wave with most of their 256 rows (GB300, 4096 x 4096
+        // x 8192: e4m3 106.5 us against 110.5 on the one-CTA kernel, fp4 103.4 against 108.5,
+        // fp6 104.5 against 110.6); otherwise the one-CTA kernel (32-element blocks: 132.1
+        // against 134.1; the pair kernel's 128-deep stages 122.9-125.0 with a workspace,
+        // 137.2 without).
+        const int block_auto = (o && o->mx_scale_block) ? o->mx_scale_block : 128;
+        bool deep_pair = false;
+        if (v == GEMM_VARIANT_AUTO) {
+            const uint64_t need = sf_pack_layout(M, N, (K + block_auto - 1) / block_auto, 224).bytes;
+            const bool bk_ok = !o || o->tile_k == 0 || o->tile_k == 256;
+            deep_pair = block_auto == 128 && !want_n && bk_ok && K % 128 == 0 && o && o->workspace &&
+                        o->workspace_bytes >= need && (M % 256 == 0 || M % 256 > 128) &&
+                        (int64_t)ceil_div(M, 256) * ceil_div(N, 224) >= pairs;
+            v = deep_pair ? GEMM_VARIANT_2CTA : GEMM_VARIANT_1CTA;
+        }
         if (v == GEMM_VARIANT_2CTA) {
-            const int bk_want = o ? o->tile_k : 0;
-            if (bk_want && bk_want != 128)
-                return fail(GEMM_ERR_INVALID_ARG, "tile_k %d is not 128 for the block-scaled pair kernel", bk_want);
+            const int bk_want = deep_pair ? 256 : (o ? o->tile_k : 0);
+            if (bk_want && bk_want != 128 && bk_want != 256)
+                return fail(GEMM_ERR_INVALID_ARG, "tile_k %d is not 128 or 256 for the block-scaled pair kernel", bk_want);
             p->variant = v;
             p->cluster = 2;
             p->tile_m = 256;
             p->tile_n = want_n ? want_n : dtc::gmx2::kBN;
-            p->tile_k = dtc::gmx2::kBK;
-            p->stages = dtc::gmx2::kStages;
             p->tiles = ceil_div(M, 256) * ceil_div(N, p->tile_n);
             p->ctas = 2 * std::min(p->tiles, pairs);
             // 224-wide pair tiles take the scales repacked into a large enough workspace (e4m3,
@@ -546,6 +557,13 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
             const int block = (o && o->mx_scale_block) ? o->mx_scale_block : 128;
             const uint64_t need = sf_pack_layout(M, N, (K + block - 1) / block, p->tile_n).bytes;
             p->sf_pack = p->tile_n == 224 && o && o->workspace && o->workspace_bytes >= need;
+            // 256-deep stages (3-D boxes over 128-byte K-chunks) need K % 128 == 0 and the
+            // repacked scales
+            if (bk_want == 256 && (K % 128 || !p->sf_pack))
+                return fail(GEMM_ERR_UNSUPPORTED, "256-deep pair stages need K %% 128 == 0 and a "
+                            "workspace for the repacked scales (224-wide tiles)");
+            p->tile_k = bk_want == 256 ? 2 * dtc::gmx2::kBK : dtc::gmx2::kBK;
+            p->stages = bk_want == 256 ? dtc::gmx2::Cfg<224, true, true>::kNStages : dtc::gmx2::kStages;
             return GEMM_OK;
         }
         p->variant = GEMM_VARIANT_1CTA;

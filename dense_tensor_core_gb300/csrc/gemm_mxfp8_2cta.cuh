@@ -60,17 +60,28 @@ constexpr int threads_for(bool tma_sf) { return tma_sf ? 192 : kThreads; }
 // 224-column accumulators (448 + 48 <= 512 columns), or one 256-column accumulator (the epilogue of
 // a tile then finishes before the next tile's first MMA). With kTmaSf each stage has a 1.5 KB slot
 // for the chunks of a set that starts in it.
-template <int kBN, bool kTmaSf = false>
+//
+// With kDeep (repacked scales only) a stage holds two K-blocks: each operand comes in one 3-D box
+// {128 bytes, rows, 2} (32 KB of A and 28 KB of B per CTA, K % 128 == 0), 3 stages. A TMA
+// instruction that moves more bytes streams faster per SM, which the fp8 rate needs.
+template <int kBN, bool kTmaSf = false, bool kDeep = false>
 struct Cfg {
+    static constexpr int kBlocks = kDeep ? 2 : 1;  // 128-element K-blocks per stage
+    static constexpr int kNStages = kDeep ? 3 : kStages;
     static constexpr int kHalfN = kBN / 2;
-    static constexpr int kBStage = kHalfN * 128;
-    static constexpr int kStageBytes = kAStage + kBStage;
+    static constexpr int kAChunk = kAStage;        // one K-block of the CTA's 128 rows of A
+    static constexpr int kBChunk = kHalfN * 128;   // one K-block of its kBN/2 rows of B
+    static constexpr int kAStg = kAChunk * kBlocks;
+    static constexpr int kBStage = kBChunk * kBlocks;
+    static constexpr int kStageBytes = kAStg + kBStage;
     static constexpr int kAccBufs = kBN == 256 ? 1 : 2;
     static constexpr int kAccStride = kBN;
     static constexpr int kSfBase = kAccBufs * kBN;
-    static constexpr int kSlotBytes = kTmaSf ? gmx::kSfSetBytes : 0;
-    static constexpr int kSmemBytes = kStages * (kStageBytes + kSlotBytes) + kCBytes + 1024;
+    static constexpr int kSlotBytes = kTmaSf ? kBlocks * gmx::kSfSetBytes : 0;
+    static constexpr int kSmemBytes = kNStages * (kStageBytes + kSlotBytes) + kCBytes + 1024;
     static_assert(!kTmaSf || kBN == 224, "repacked scales on 224-wide pair tiles");
+    static_assert(!kDeep || kTmaSf, "256-deep pair stages take repacked scales");
+    static_assert(kBChunk % 1024 == 0, "chunks keep the 1024-byte swizzle alignment");
     static_assert(kBN == 224 || kBN == 256, "pair tiles 224 or 256 wide");
     static_assert(kAStage % 1024 == 0 && kBStage % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
     static_assert(kSmemBytes <= 227 * 1024 - 512, "shared memory budget");
@@ -79,7 +90,7 @@ struct Cfg {
 constexpr int kBN = 224;  // the default pair tile width
 }  // namespace gmx2
 
-template <bool kB32, int kBN, bool kTmaSf = false>
+template <bool kB32, int kBN, bool kTmaSf = false, bool kDeep = false>
 __global__ void __launch_bounds__(gmx2::threads_for(kTmaSf), 1)
     gemm_mxfp8_2cta_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
@@ -88,7 +99,10 @@ __global__ void __launch_bounds__(gmx2::threads_for(kTmaSf), 1)
                            const __grid_constant__ CUtensorMap tmSA,
                            const __grid_constant__ CUtensorMap tmSB, const GemmMxArgs args) {
     using namespace gmx2;
-    using C_ = Cfg<kBN, kTmaSf>;
+    using C_ = Cfg<kBN, kTmaSf, kDeep>;
+    constexpr int kNS = C_::kNStages;
+    constexpr int kAStg = C_::kAStg;
+    constexpr int kBlocks = C_::kBlocks;
     constexpr int kHalfN = C_::kHalfN;
     constexpr int kBStage = C_::kBStage;
     constexpr int kStageBytes = C_::kStageBytes;
@@ -97,8 +111,8 @@ __global__ void __launch_bounds__(gmx2::threads_for(kTmaSf), 1)
     constexpr int kSfBase = C_::kSfBase;
     constexpr int grp = kB32 ? 1 : 4;  // K-blocks per scale set
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bar_full[kStages];
-    __shared__ __align__(8) uint64_t bar_empty[kStages];
+    __shared__ __align__(8) uint64_t bar_full[kNS];
+    __shared__ __align__(8) uint64_t bar_empty[kNS];
     __shared__ __align__(8) uint64_t bar_tfull[kAccBufs];
     __shared__ __align__(8) uint64_t bar_tempty[kAccBufs];
     __shared__ __align__(8) uint64_t bar_sfull[kSfSets];
@@ -109,8 +123,8 @@ __global__ void __launch_bounds__(gmx2::threads_for(kTmaSf), 1)
 
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t sA = base;
-    const uint32_t sB = base + kStages * kAStage;
-    const uint32_t sSF = base + kStages * kStageBytes + kCBytes;  // kTmaSf: scale slots
+    const uint32_t sB = base + kNS * kAStg;
+    const uint32_t sSF = base + kNS * kStageBytes + kCBytes;  // kTmaSf: scale slots
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
@@ -119,10 +133,11 @@ __global__ void __launch_bounds__(gmx2::threads_for(kTmaSf), 1)
     const int num_pairs = gridDim.x >> 1;
     const int total = args.num_m * args.num_n;  // num_m counts 256-row pair tiles
     const int groups = (args.num_kb + grp - 1) / grp;  // scale sets per tile
+    const int num_st = (args.num_kb + kBlocks - 1) / kBlocks;  // stages per tile
     volatile int* abort = &abort_flag;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kNS; ++s) {
             mbar_init(smem_u32(&bar_full[s]), 1);
             mbar_init(smem_u32(&bar_empty[s]), 1);
         }
@@ -164,8 +179,8 @@ __global__ void __launch_bounds__(gmx2::threads_for(kTmaSf), 1)
                 tile_coords(t, args.num_m, args.num_n, kGroupM, mt, nt);
                 const int a_row = mt * 256 + (int)rank * kBMc;
                 const int b_row = nt * kBN + (int)rank * kHalfN;
-                for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
-                    const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+                for (int st = 0; st < num_st; ++st, ++it) {
+                    const uint32_t s = it % kNS, ph = (it / kNS) & 1u;
                     if (!wait_bounded(smem_u32(&bar_empty[s]), ph ^ 1u, abort, args.timeout_ns,
                                       args.status, 41)) {
                         ok = false;
@@ -174,34 +189,52 @@ __global__ void __launch_bounds__(gmx2::threads_for(kTmaSf), 1)
                     if (args.fault == 1 && it == 0) continue;  // test hook: stage never filled
                     const uint32_t full_local = smem_u32(&bar_full[s]);
                     const uint32_t full_leader = map_to_cta(full_local, 0);
-                    const bool set_start = kTmaSf && kb % grp == 0;
-                    if (leader)  // both CTAs' bytes
-                        mbar_arrive_expect_tx(full_local, args.stage_tx + (set_start ? 2 * gmx::kSfSetBytes : 0));
-                    tma_load_2d_pair(sA + s * kAStage, &tmA, full_leader, kb * kBK, a_row);
-                    tma_load_2d_pair(sB + s * kBStage, &tmB, full_leader, kb * kBK, b_row);
-                    if (set_start) {
-                        // this CTA's A chunk (its 128-row group) and the tile's two B chunks, as
-                        // rows of 128 bytes of the repacked arrays; the kernel that writes them
-                        // may still be running (it launched this one early)
-                        if (!chunks_ready) {
-                            grid_dependency_wait();
-                            chunks_ready = true;
+                    int sets_here = 0;  // scale sets that start in this stage
+                    if constexpr (kTmaSf) {
+#pragma unroll
+                        for (int h = 0; h < kBlocks; ++h) {
+                            const int kb = st * kBlocks + h;
+                            if (kb < args.num_kb && kb % grp == 0) ++sets_here;
                         }
-                        const int g = kb / grp;
-                        const uint32_t slot = sSF + s * C_::kSlotBytes;
-                        tma_load_2d_pair(slot, &tmSA, full_leader, 0,
-                                         ((mt * 2 + (int)rank) * args.sf_sets + g) * 4);
-                        tma_load_2d_pair(slot + kSfChunkBytes, &tmSB, full_leader, 0,
-                                         (nt * args.sf_sets + g) * 8);
+                    }
+                    if (leader)  // both CTAs' bytes
+                        mbar_arrive_expect_tx(full_local,
+                                              args.stage_tx + sets_here * 2 * gmx::kSfSetBytes);
+                    if constexpr (kDeep) {  // one 3-D box of two 128-byte K-chunks per operand
+                        tma_load_3d_pair(sA + s * kAStg, &tmA, full_leader, 0, a_row, st * 2);
+                        tma_load_3d_pair(sB + s * kBStage, &tmB, full_leader, 0, b_row, st * 2);
+                    } else {
+                        tma_load_2d_pair(sA + s * kAStg, &tmA, full_leader, st * kBK, a_row);
+                        tma_load_2d_pair(sB + s * kBStage, &tmB, full_leader, st * kBK, b_row);
+                    }
+                    if constexpr (kTmaSf) {
+#pragma unroll
+                        for (int h = 0; h < kBlocks; ++h) {
+                            const int kb = st * kBlocks + h;
+                            if (kb >= args.num_kb || kb % grp != 0) continue;
+                            // this CTA's A chunk (its 128-row group) and the tile's two B chunks,
+                            // as rows of 128 bytes of the repacked arrays; the kernel that writes
+                            // them may still be running (it launched this one early)
+                            if (!chunks_ready) {
+                                grid_dependency_wait();
+                                chunks_ready = true;
+                            }
+                            const int g = kb / grp;
+                            const uint32_t slot = sSF + s * C_::kSlotBytes + h * gmx::kSfSetBytes;
+                            tma_load_2d_pair(slot, &tmSA, full_leader, 0,
+                                             ((mt * 2 + (int)rank) * args.sf_sets + g) * 4);
+                            tma_load_2d_pair(slot + kSfChunkBytes, &tmSB, full_leader, 0,
+                                             (nt * args.sf_sets + g) * 8);
+                        }
                     }
                 }
             }
             if (!ok && leader) {
                 // The leader's full barriers count both CTAs' copies: let those in flight land.
-                const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0;
+                const uint32_t first = it > (uint32_t)kNS ? it - kNS : 0;
                 for (uint32_t i = first; i < it; ++i) {
                     if (args.fault == 1 && i == 0) continue;
-                    wait_drain(smem_u32(&bar_full[i % kStages]), (i / kStages) & 1u, kDrainNs);
+                    wait_drain(smem_u32(&bar_full[i % kNS]), (i / kNS) & 1u, kDrainNs);
                 }
             } else if (!ok) {
                 // The peer's copies complete on the leader's barriers, which it cannot observe:
@@ -231,60 +264,70 @@ __global__ void __launch_bounds__(gmx2::threads_for(kTmaSf), 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * kAccStride;
-                for (int kb = 0; kb < args.num_kb; ++kb) {
-                    const uint32_t set = sit % kSfSets;
-                    if (!kTmaSf && kb % grp == 0) {  // the first K-block of a scale set
-                        if (!wait_bounded<true>(smem_u32(&bar_sfull[set]), (sit / kSfSets) & 1u,
-                                                abort, args.timeout_ns, args.status, 45)) {
-                            ok = false;
-                            break;
-                        }
-                    }
+                for (int st = 0; st < num_st && ok; ++st) {
                     if (!wait_bounded(smem_u32(&bar_full[s]), ph, abort, args.timeout_ns,
                                       args.status, 43)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    if constexpr (kTmaSf) {
-                        if (kb % grp == 0) {
-                            // the set's columns are free once the MMAs that last read them are
-                            // done; then both CTAs copy the set from the stage's slot
-                            if (!wait_bounded(smem_u32(&bar_sempty[set]),
-                                              ((sit / kSfSets) & 1u) ^ 1u, abort, args.timeout_ns,
-                                              args.status, 47)) {
-                                ok = false;
-                                break;
+#pragma unroll
+                    for (int h = 0; h < kBlocks; ++h) {
+                        const int kb = st * kBlocks + h;
+                        if (kb >= args.num_kb) break;  // a K-block past K: zero-filled, skipped
+                        const uint32_t set = sit % kSfSets;
+                        if (kb % grp == 0) {  // the first K-block of a scale set
+                            if constexpr (kTmaSf) {
+                                // the set's columns are free once the MMAs that last read them
+                                // are done; then both CTAs copy the set from the stage's slot
+                                if (!wait_bounded(smem_u32(&bar_sempty[set]),
+                                                  ((sit / kSfSets) & 1u) ^ 1u, abort,
+                                                  args.timeout_ns, args.status, 47)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after_sync();
+                                const uint32_t slot = sSF + s * C_::kSlotBytes + h * gmx::kSfSetBytes;
+                                const uint32_t col = tmem_base + kSfBase + set * kSfSet;
+                                tmem_cp_32x128b_x4_cta2(col, smem_desc_plain(slot, 128, 128));
+                                tmem_cp_32x128b_x4_cta2(
+                                    col + 4, smem_desc_plain(slot + kSfChunkBytes, 128, 128));
+                                tmem_cp_32x128b_x4_cta2(
+                                    col + 8, smem_desc_plain(slot + 2 * kSfChunkBytes, 128, 128));
+                            } else {
+                                if (!wait_bounded<true>(smem_u32(&bar_sfull[set]),
+                                                        (sit / kSfSets) & 1u, abort,
+                                                        args.timeout_ns, args.status, 45)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after_sync();
                             }
-                            tc_fence_after_sync();
-                            const uint32_t slot = sSF + s * C_::kSlotBytes;
-                            const uint32_t col = tmem_base + kSfBase + set * kSfSet;
-                            tmem_cp_32x128b_x4_cta2(col, smem_desc_plain(slot, 128, 128));
-                            tmem_cp_32x128b_x4_cta2(
-                                col + 4, smem_desc_plain(slot + kSfChunkBytes, 128, 128));
-                            tmem_cp_32x128b_x4_cta2(
-                                col + 8, smem_desc_plain(slot + 2 * kSfChunkBytes, 128, 128));
+                        }
+                        // K-block h of the stage: 128-byte chunk h of each operand's box
+                        const uint32_t a_lo = (uint32_t)a_desc0 + s * (uint32_t)(kAStg >> 4) +
+                                              (uint32_t)h * (uint32_t)(C_::kAChunk >> 4);
+                        const uint32_t b_lo = (uint32_t)b_desc0 + s * (uint32_t)(kBStage >> 4) +
+                                              (uint32_t)h * (uint32_t)(C_::kBChunk >> 4);
+                        const uint32_t sfa = tmem_base + kSfBase + set * kSfSet;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint32_t sf_id = kB32 ? (uint32_t)kk : (uint32_t)(kb & 3);
+                            const uint32_t idesc = idesc0 | (sf_id << 4) | (sf_id << 29);
+                            const uint64_t adesc = ((uint64_t)a_hi << 32) | (a_lo + 2u * kk);
+                            const uint64_t bdesc = ((uint64_t)b_hi << 32) | (b_lo + 2u * kk);
+                            mma_mxf8_cta2(d_tmem, adesc, bdesc, idesc, sfa, sfa + 4,
+                                          (kb | kk) != 0 ? 1u : 0u);
+                        }
+                        issued = true;
+                        if (kb % grp == grp - 1 || kb == args.num_kb - 1) {
+                            mma_commit_cta2_both(smem_u32(&bar_sempty[set]));  // set consumed
+                            ++sit;
                         }
                     }
-                    const uint32_t a_lo = (uint32_t)a_desc0 + s * (uint32_t)(kAStage >> 4);
-                    const uint32_t b_lo = (uint32_t)b_desc0 + s * (uint32_t)(kBStage >> 4);
-                    const uint32_t sfa = tmem_base + kSfBase + set * kSfSet;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t sf_id = kB32 ? (uint32_t)kk : (uint32_t)(kb & 3);
-                        const uint32_t idesc = idesc0 | (sf_id << 4) | (sf_id << 29);
-                        const uint64_t adesc = ((uint64_t)a_hi << 32) | (a_lo + 2u * kk);
-                        const uint64_t bdesc = ((uint64_t)b_hi << 32) | (b_lo + 2u * kk);
-                        mma_mxf8_cta2(d_tmem, adesc, bdesc, idesc, sfa, sfa + 4,
-                                      (kb | kk) != 0 ? 1u : 0u);
-                    }
-                    issued = true;
+                    if (!ok) break;
                     mma_commit_cta2_both(smem_u32(&bar_empty[s]));  // stage free in both CTAs
-                    if (kb % grp == grp - 1 || kb == args.num_kb - 1) {
-                        mma_commit_cta2_both(smem_u32(&bar_sempty[set]));  // scale set consumed
-                        ++sit;
-                    }
-                    if (++s == (uint32_t)kStages) {
+                    if (++s == (uint32_t)kNS) {
                         s = 0;
                         ph ^= 1u;
                     }
@@ -301,7 +344,7 @@ __global__ void __launch_bounds__(gmx2::threads_for(kTmaSf), 1)
     } else if (warp < 6) {
         // ------------------------------ epilogue (warps 2..5, both CTAs) ---------------------
         const int q = warp & 3;
-        const uint32_t my_slots = base + kStages * kStageBytes + (uint32_t)q * 8192u;
+        const uint32_t my_slots = base + kNS * kStageBytes + (uint32_t)q * 8192u;
         uint32_t acc = 0, stores = 0;
         for (int t = pair; t < total; t += num_pairs, ++acc) {
             int mt, nt;

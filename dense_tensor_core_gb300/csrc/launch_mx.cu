@@ -26,25 +26,26 @@ int launch_sf_pack(const Launch& L, const SfPackLayout& l) {
     return GEMM_OK;
 }
 
-template <bool kB32, int kBN, bool kTmaSf>
+template <bool kB32, int kBN, bool kTmaSf, bool kDeep = false>
 int launch_pair(const Launch& L) {
     using namespace dtc::gmx2;
-    using C_ = Cfg<kBN, kTmaSf>;
+    using C_ = Cfg<kBN, kTmaSf, kDeep>;
     const Operands& ops = *L.ops;
     const int a_bits = mx_bits(L.o ? L.o->mx_a_format : 0);
     const int b_bits = mx_bits(L.o ? L.o->mx_b_format : 0);
     CUtensorMap tA, tB, tC, tC32;
     int rc = tmap_block_scaled(&tA, a_bits, ops.A, (uint64_t)L.K, (uint64_t)L.M,
-                               (uint64_t)ops.lda * a_bits / 8, kBMc, false, "A");
+                               (uint64_t)ops.lda * a_bits / 8, kBMc, kDeep, "A");
     if (rc) return rc;
     if ((rc = tmap_block_scaled(&tB, b_bits, ops.B, (uint64_t)L.K, (uint64_t)L.N,
-                                (uint64_t)ops.ldb * b_bits / 8, C_::kHalfN, false, "B")))
+                                (uint64_t)ops.ldb * b_bits / 8, C_::kHalfN, kDeep, "B")))
         return rc;
     if ((rc = tmap_c16(&tC, &tC32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ops, L.M, L.N))) return rc;
-    auto kern = dtc::gemm_mxfp8_2cta_kernel<kB32, kBN, kTmaSf>;
+    auto kern = dtc::gemm_mxfp8_2cta_kernel<kB32, kBN, kTmaSf, kDeep>;
     if ((rc = ensure_smem_attr(kern, C_::kSmemBytes, L.dev))) return rc;
-    // 256 rows of A and kBN of B per stage: both CTAs' copies, armed on the leader's barrier
+    // 256 rows of A and kBN of B per K-block: both CTAs' copies, armed on the leader's barrier
     dtc::GemmMxArgs a = mx_args(L, 256, kBN, kBK);
+    a.stage_tx *= C_::kBlocks;  // a 256-deep stage holds two K-blocks
     CUtensorMap tSA = tA, tSB = tA;  // (unused without repacked scales)
     if constexpr (kTmaSf) {
         // the repacked arrays as rows of 128 bytes: a chunk is 4 rows (A) or 8 (B's two halves)
@@ -125,6 +126,8 @@ int launch_mx(const Launch& L) {
     if (L.p->variant == GEMM_VARIANT_2CTA) {
         if (L.p->tile_n == 256)
             return b32 ? launch_pair<true, 256, false>(L) : launch_pair<false, 256, false>(L);
+        if (L.p->sf_pack && L.p->tile_k == 2 * dtc::gmx2::kBK)
+            return b32 ? launch_pair<true, 224, true, true>(L) : launch_pair<false, 224, true, true>(L);
         if (L.p->sf_pack)
             return b32 ? launch_pair<true, 224, true>(L) : launch_pair<false, 224, true>(L);
         return b32 ? launch_pair<true, 224, false>(L) : launch_pair<false, 224, false>(L);

@@ -91,8 +91,9 @@ typedef struct {
                              stages (K % 64 == 0) */
     int tile_k;           /* K-elements per pipeline stage: 64 (1CTA), 64 or 128 (2CTA; SPLITK
                              with 128-wide tiles; 128 needs K % 64 == 0), 128 (the default) or 256
-                             (block-scaled one-CTA kernel; 256 needs K % 128 == 0), 128
-                             (block-scaled pair kernel); 0 = choose */
+                             (block-scaled one-CTA kernel; 256 needs K % 128 == 0), 128 or 256
+                             (block-scaled pair kernel; 256 needs K % 128 == 0 and the repacked
+                             scales); 0 = choose */
     int64_t lda;          /* elements between consecutive stored rows of A, B, C; 0 = dense (the */
     int64_t ldb;          /* row length: K or M for A, K or N for B, N for C). At least the row */
     int64_t ldc;          /* length, and rows must start 16 bytes apart (ld x element size %
@@ -113,12 +114,12 @@ typedef struct {
                              (see gemm_workspace_size). 16-bit products: stream-K; its first 1 KB
                              holds flags that must be zero before the first call that uses it;
                              every completed call leaves them zero again (after a
-                             GEMM_ERR_TIMEOUT, zero them before reuse). Block-scaled one-CTA
-                             kernel: a large enough workspace receives the scale arrays repacked
-                             by a first kernel of the call, from which the product kernel copies
-                             them into Tensor Memory (faster, above all with 32-element scale
-                             blocks); no initial contents needed. Calls that may run at the same
-                             time (other streams) must not share a workspace. */
+                             GEMM_ERR_TIMEOUT, zero them before reuse). Block-scaled product: a
+                             large enough workspace receives the scale arrays repacked by a first
+                             kernel of the call, from which the product kernel copies them into
+                             Tensor Memory (see gemm_workspace_size for when); no initial contents
+                             needed. Calls that may run at the same time (other streams) must not
+                             share a workspace. */
     uint64_t workspace_bytes;
     int stream_k;         /* 0 = use stream-K when a large enough workspace is given and the
                              cost model prefers it; 1 = required (error if not possible); 2 = off.
@@ -276,8 +277,11 @@ int gemm_sp_workspace_size(int dtype, int64_t M, int64_t K, uint64_t* bytes);
  * Bytes of workspace (gemm_options.workspace) with which the call would use stream-K on CTA pairs
  * (the last, part-full wave's tiles shared out over all pairs as equal runs of K-blocks, the
  * pieces summed through the workspace); 0 when it would not (or stream_k == 2). For the
- * block-scaled product (dtype 2) on the one-CTA kernel: the bytes of the repacked scale arrays
- * (about the size of sfA and sfB together), 0 on the pair kernel. The pages have no counterpart:
+ * block-scaled product (dtype 2): the bytes of the repacked scale arrays (about the size of sfA
+ * and sfB together) when the call would use them -- AUTO with 128-element blocks, K % 128 == 0
+ * and at least a wave of 256 x 224 tiles (the pair kernel with 256-deep stages), 32-element
+ * blocks (the one-CTA kernel), or the pair kernel forced with 224-wide tiles -- else 0. The
+ * pages have no counterpart:
  * their persistent 2-CTA variant (05 Blackwell TCGEN05 GEMM tutorial, "Advanced") takes whole
  * tiles. INVALID_ARG as gemm_ex; bytes must not be NULL.
  */

@@ -1,7 +1,7 @@
 """Every element of C at the benchmark workloads' full sizes, against the full CPU oracle.
 
 Each product is launched the way the benchmark times it: the library's automatic plan, with the
-stream-K workspace gemm_workspace_size asks for when it asks for one. The oracle computes every
+workspace gemm_workspace_size asks for when it asks for one (block-scaled products also without). The oracle computes every
 output (fp64 sums on all host cores, one rounding), so this is the complete parity check at the
 sizes the performance figures are quoted on; the sampled checks in the other files cover the
 forced kernel variants at these sizes.
@@ -53,13 +53,19 @@ def test_block_scaled_workload_every_element(name):
 
     w = workloads.WORKLOADS[name]
     A, B, sfA, sfB = workloads.make(w)
-    C = dtc.gemm_ex("mxfp8", to_device8(A), to_device8(B), sfA=to_device8(sfA),
-                    sfB=to_device8(sfB), a_format=w.a_fmt, b_format=w.b_fmt, scale_block=w.block)
-    dtc.gemm_stream_status()
-    C = C.view(torch.int16).cpu().numpy().view(np.uint16)
+    fmt = dict(a_format=w.a_fmt, b_format=w.b_fmt, scale_block=w.block)
     ref = oracle.gemm_bs(A, B, sfA, sfB, w.M, w.N, w.K, a_fmt=w.a_fmt, b_fmt=w.b_fmt,
                          block=w.block)
-    check_close(values16(C, "bf16"), values16(ref, "bf16"), f"{name}, every element")
+    # without a workspace (scale warps) and with the one gemm_workspace_size asks for (repacked
+    # scales, the plan the benchmark times)
+    ws_bytes = dtc.gemm_workspace_size("mxfp8", w.M, w.N, w.K, **fmt)
+    for ws in [None] + ([torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")] if ws_bytes else []):
+        C = dtc.gemm_ex("mxfp8", to_device8(A), to_device8(B), sfA=to_device8(sfA),
+                        sfB=to_device8(sfB), workspace=ws, **fmt)
+        dtc.gemm_stream_status()
+        C = C.view(torch.int16).cpu().numpy().view(np.uint16)
+        check_close(values16(C, "bf16"), values16(ref, "bf16"),
+                    f"{name}, every element, {'no workspace' if ws is None else 'workspace'}")
 
 
 @pytest.mark.parametrize("name", [n for n, w in workloads.WORKLOADS.items() if w.kind.endswith("_sp24")])

@@ -97,7 +97,7 @@ def test_unit_scales_reduce_to_plain_e4m3():
 
 
 @pytest.mark.parametrize("variant,tile_k,pack", [(1, 128, False), (1, 256, False), (2, 0, False),
-                                                (2, 0, True)])
+                                                (2, 0, True), (2, 256, True)])
 @pytest.mark.parametrize("which", ["a_rows", "b_rows", "k_blocks"])
 def test_scales_varying_along_one_axis(which, variant, tile_k, pack):
     # Scales that vary along a single axis: a wrong row / column / K-block mapping of the scale
@@ -126,17 +126,18 @@ def test_wide_scale_range():
     check_mx(A, B, sfA, sfB, "wide scale range")
 
 
-@pytest.mark.parametrize("variant,pack", [(1, False), (2, False), (2, True)])
-def test_more_tiles_than_sms(variant, pack):
+@pytest.mark.parametrize("variant,pack,tile_k", [(1, False, 0), (2, False, 0), (2, True, 0),
+                                                (2, True, 256)])
+def test_more_tiles_than_sms(variant, pack, tile_k):
     # 200 one-CTA tiles of 128 x 224 over 152 SMs, or 100 pair tiles over 76 pairs: persistent
     # loop, both accumulators, scale sets reused across tiles
     M, N, K = 2560, 2240, 256
     A, B, sfA, sfB = workloads.make_mxfp8(M, N, K, seed=6)
-    check_mx(A, B, sfA, sfB, "more tiles than SMs", variant=variant, pack=pack)
+    check_mx(A, B, sfA, sfB, "more tiles than SMs", variant=variant, pack=pack, tile_k=tile_k)
 
 
 @pytest.mark.parametrize("variant,tile_k,pack", [(0, 0, False), (1, 128, False), (1, 256, False),
-                                                (2, 0, False), (2, 0, True)])
+                                                (2, 0, False), (2, 0, True), (2, 256, True)])
 def test_benchmark_size_sampled(variant, tile_k, pack):
     w = workloads.WORKLOADS["mxfp8_nt_4096x4096x8192"]
     A, B, sfA, sfB = _bench_inputs()
@@ -210,7 +211,8 @@ def run_mx_fmt(A, B, sfA, sfB, a_fmt, b_fmt, block, **kw):
 
 
 @pytest.mark.parametrize("variant,tile_k,pack", [(1, 128, False), (1, 256, False), (2, 0, False),
-                                                (1, 128, True), (1, 256, True), (2, 0, True)])
+                                                (1, 128, True), (1, 256, True), (2, 0, True),
+                                                (2, 256, True)])
 @pytest.mark.parametrize("block", [32, 128])
 @pytest.mark.parametrize("a_fmt,b_fmt", [("e5m2", "e5m2"), ("e4m3", "e5m2"), ("e5m2", "e4m3"),
                                          ("e4m3", "e4m3")])

@@ -49,10 +49,20 @@ def test_automatic_choice_on_gb300():
 
 
 def test_block_scaled_repacking_policy():
-    # with a workspace the scales are repacked for 32-element blocks on the one-CTA kernel and for
-    # every block on 224-wide pair tiles; a workspace too small leaves the scale warps in charge
+    # with a workspace the scales are repacked: 128-element blocks go to the pair kernel with
+    # 256-deep stages (when K % 128 == 0 and the pair tiles fill a wave), 32-element blocks to the
+    # one-CTA kernel; every block on 224-wide pair tiles when the pair is forced; a workspace too
+    # small leaves the scale warps in charge
     ws = fake_workspace()
-    assert plan("mxfp8", 4096, 4096, 8192, workspace=ws)["sf_packed"] == 0
+    p = plan("mxfp8", 4096, 4096, 8192, workspace=ws)
+    assert (p["variant"], p["tile_m"], p["tile_n"], p["tile_k"], p["stages"], p["sf_packed"]) == (2, 256, 224, 256, 3, 1)
+    assert plan("mxfp8", 4096, 4096, 8192)["variant"] == 1  # no workspace: one-CTA, scale warps
+    assert plan("mxfp8", 4096, 4096, 8200, workspace=ws)["variant"] == 1  # K % 128 != 0
+    assert plan("mxfp8", 1024, 1024, 1024, workspace=ws)["variant"] == 1  # 20 pair tiles < 76
+    assert plan("mxfp8", 4096, 4096, 8192, workspace=ws, tile_k=128)["variant"] == 1
+    with pytest.raises(dtc.GemmError):  # 256-deep pair stages need the repacked scales
+        plan("mxfp8", 4096, 4096, 8192, variant=2, tile_k=256)
+    assert plan("mxfp8", 4096, 4096, 8192, workspace=ws, scale_block=32)["variant"] == 1
     assert plan("mxfp8", 4096, 4096, 8192, workspace=ws, scale_block=32)["sf_packed"] == 1
     assert plan("mxfp8", 4096, 4096, 8192, workspace=ws, scale_block=32, b_format="e2m1")["sf_packed"] == 1
     assert plan("mxfp8", 4096, 4096, 8192, workspace=ws, variant=2)["sf_packed"] == 1

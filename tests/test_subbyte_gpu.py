@@ -54,7 +54,8 @@ KERNELS = {"1cta_128": dict(variant=1, tile_k=128), "1cta_256": dict(variant=1, 
            "pair": dict(variant=2), "pair_256": dict(variant=2, tile_n=256),
            "1cta_128_packed": dict(variant=1, tile_k=128, pack=True),
            "1cta_256_packed": dict(variant=1, tile_k=256, pack=True),
-           "pair_packed": dict(variant=2, pack=True)}
+           "pair_packed": dict(variant=2, pack=True),
+           "pair_256deep_packed": dict(variant=2, tile_k=256, pack=True)}
 
 
 @pytest.mark.parametrize("kernel", list(KERNELS))
