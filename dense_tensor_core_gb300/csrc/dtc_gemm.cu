@@ -527,10 +527,9 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
         // 256 with repacked scales). AUTO takes the pair kernel with 256-deep stages for
         // 128-element scale blocks when a workspace holds the repacked scales, K % 128 == 0 and
         // the pair tiles fill at least one wave with most of their 256 rows (GB300, 4096 x 4096
-        // x 8192: e4m3 106.5 us against 110.5 on the one-CTA kernel, fp4 103.4 against 108.5,
-        // fp6 104.5 against 110.6); otherwise the one-CTA kernel (32-element blocks: 132.1
-        // against 134.1; the pair kernel's 128-deep stages 122.9-125.0 with a workspace,
-        // 137.2 without).
+        // x 8192: e4m3 102.4 us against 108.8 on the one-CTA kernel, fp4 and fp6 100.4 against
+        // 106.8 and 108.8); otherwise the one-CTA kernel (32-element blocks: 115.7 against
+        // 133.2; the pair kernel's 128-deep stages 118.8 with a workspace, 137.2 without).
         const int block_auto = (o && o->mx_scale_block) ? o->mx_scale_block : 128;
         bool deep_pair = false;
         if (v == GEMM_VARIANT_AUTO) {
@@ -584,9 +583,9 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
         p->ctas = std::min(p->tiles, sms);
         // With 32-element scale blocks and a large enough workspace the scales are repacked
         // there and reach Tensor Memory by bulk copy and tcgen05.cp instead of through the
-        // kernel's scale warps: 4096 x 4096 x 8192 e4m3 ran 132 us against 307. With 128-element
-        // blocks the scale warps keep up (110.5 us against 111.6 repacked, the repacking
-        // included), so they stay.
+        // kernel's scale warps: 4096 x 4096 x 8192 e4m3 ran 115.7 us against 307. With
+        // 128-element blocks the scale warps keep up (108.8 us against 109.6 repacked, the
+        // repacking included), so they stay.
         const int block = (o && o->mx_scale_block) ? o->mx_scale_block : 128;
         const uint64_t need = sf_pack_layout(M, N, (K + block - 1) / block, p->tile_n).bytes;
         p->sf_pack = block == 32 && o && o->workspace && o->workspace_bytes >= need;

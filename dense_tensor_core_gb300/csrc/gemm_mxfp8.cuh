@@ -151,6 +151,13 @@ __global__ void __launch_bounds__(gmx::threads_for(kTmaSf), 1)
     constexpr int grp = kB32 ? 1 : kGroup;  // K-blocks per scale set
     const int groups = (args.num_kb + grp - 1) / grp;
     const int num_st = (args.num_kb + kBlocks - 1) / kBlocks;  // stages per tile
+    // Refilling a scale set's columns needs the MMAs that last read them done. Passing a stage's
+    // full barrier already proves every MMA of the stages a whole ring earlier done (the stage was
+    // refilled only after the commit that followed them), so with full sets (every tile's K-blocks
+    // a multiple of the set length) spaced at least a ring apart the explicit wait, and the commit
+    // it waits for, are not needed.
+    constexpr bool kSfRingSafe = (kSfSets - 1) * grp + 1 >= kStages * kBlocks;
+    const bool sf_wait = kTmaSf && !(kSfRingSafe && args.num_kb % grp == 0);
     volatile int* abort = &abort_flag;
 
     if (threadIdx.x == 0) {
@@ -281,13 +288,15 @@ __global__ void __launch_bounds__(gmx::threads_for(kTmaSf), 1)
                             if constexpr (kTmaSf) {
                                 // the set's columns are free once the MMAs that last read them
                                 // are done; then copy the set from the stage's slot
-                                if (!wait_bounded(smem_u32(&bar_sempty[set]),
-                                                  ((sit / kSfSets) & 1u) ^ 1u, abort,
-                                                  args.timeout_ns, args.status, 37)) {
-                                    ok = false;
-                                    break;
+                                if (sf_wait) {
+                                    if (!wait_bounded(smem_u32(&bar_sempty[set]),
+                                                      ((sit / kSfSets) & 1u) ^ 1u, abort,
+                                                      args.timeout_ns, args.status, 37)) {
+                                        ok = false;
+                                        break;
+                                    }
+                                    tc_fence_after_sync();
                                 }
-                                tc_fence_after_sync();
                                 const uint32_t slot = sSF + s * C_::kSlotBytes + h * kSfSetBytes;
                                 const uint32_t col = tmem_base + kSfBase + set * kSfSet;
                                 tmem_cp_32x128b_x4(col, smem_desc_plain(slot, 128, 128));
@@ -319,7 +328,8 @@ __global__ void __launch_bounds__(gmx::threads_for(kTmaSf), 1)
                         }
                         issued = true;
                         if (kb % grp == grp - 1 || kb == args.num_kb - 1) {
-                            mma_commit_cta1(smem_u32(&bar_sempty[set]));  // scale set consumed
+                            if (!kTmaSf || sf_wait)  // scale set consumed
+                                mma_commit_cta1(smem_u32(&bar_sempty[set]));
                             ++sit;
                         }
                     }

@@ -134,6 +134,13 @@ __global__ void __launch_bounds__(gmx2::threads_for(kTmaSf), 1)
     const int total = args.num_m * args.num_n;  // num_m counts 256-row pair tiles
     const int groups = (args.num_kb + grp - 1) / grp;  // scale sets per tile
     const int num_st = (args.num_kb + kBlocks - 1) / kBlocks;  // stages per tile
+    // Refilling a scale set's columns needs the MMAs that last read them done. Passing a stage's
+    // full barrier already proves every MMA of the stages a whole ring earlier done (the stage was
+    // refilled only after the commit that followed them), so with full sets (every tile's K-blocks
+    // a multiple of the set length) spaced at least a ring apart the explicit wait, and the commit
+    // it waits for, are not needed.
+    constexpr bool kSfRingSafe = (kSfSets - 1) * grp + 1 >= kNS * kBlocks;
+    const bool sf_wait = kTmaSf && !(kSfRingSafe && args.num_kb % grp == 0);
     volatile int* abort = &abort_flag;
 
     if (threadIdx.x == 0) {
@@ -280,13 +287,15 @@ __global__ void __launch_bounds__(gmx2::threads_for(kTmaSf), 1)
                             if constexpr (kTmaSf) {
                                 // the set's columns are free once the MMAs that last read them
                                 // are done; then both CTAs copy the set from the stage's slot
-                                if (!wait_bounded(smem_u32(&bar_sempty[set]),
-                                                  ((sit / kSfSets) & 1u) ^ 1u, abort,
-                                                  args.timeout_ns, args.status, 47)) {
-                                    ok = false;
-                                    break;
+                                if (sf_wait) {
+                                    if (!wait_bounded(smem_u32(&bar_sempty[set]),
+                                                      ((sit / kSfSets) & 1u) ^ 1u, abort,
+                                                      args.timeout_ns, args.status, 47)) {
+                                        ok = false;
+                                        break;
+                                    }
+                                    tc_fence_after_sync();
                                 }
-                                tc_fence_after_sync();
                                 const uint32_t slot = sSF + s * C_::kSlotBytes + h * gmx::kSfSetBytes;
                                 const uint32_t col = tmem_base + kSfBase + set * kSfSet;
                                 tmem_cp_32x128b_x4_cta2(col, smem_desc_plain(slot, 128, 128));
@@ -321,7 +330,8 @@ __global__ void __launch_bounds__(gmx2::threads_for(kTmaSf), 1)
                         }
                         issued = true;
                         if (kb % grp == grp - 1 || kb == args.num_kb - 1) {
-                            mma_commit_cta2_both(smem_u32(&bar_sempty[set]));  // set consumed
+                            if (!kTmaSf || sf_wait)  // set consumed
+                                mma_commit_cta2_both(smem_u32(&bar_sempty[set]));
                             ++sit;
                         }
                     }
