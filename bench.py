@@ -342,6 +342,10 @@ def oracle_rows(w, inputs, rows, cols=None):
         A, B, sfA, sfB = inputs
         oracle.gemm_bs(A[:rows], B[:cols], sfA[:rows], sfB[:cols], rows, cols, w.K, a_fmt=w.a_fmt,
                        b_fmt=w.b_fmt, block=w.block)
+    elif w.kind == "nvfp4":
+        A, B, sfA, sfB = inputs
+        oracle.gemm_bs(A[:rows], B[:cols], sfA[:rows], sfB[:cols], rows, cols, w.K, a_fmt="e2m1",
+                       b_fmt="e2m1", scale="ue4m3", block=16)
     elif w.kind.endswith("_sp24"):
         vals, meta, B = inputs
         Bc = B[:cols] if w.layout[1] == "T" else B[:, :cols]
@@ -432,8 +436,9 @@ def run_reference(args, w):
 
 
 def kernel_of(w, plan):
-    """The name of the kernel the plan launches (as in the ncu launch list); for the sparse
-    product the GEMM kernel (the step also launches sp24_expand_kernel before it)."""
+    """The name of the kernel the plan launches (as in the ncu launch list); for the sparse and
+    NVFP4 products the GEMM kernel (the step also launches sp24_expand_kernel or
+    nvfp4_expand_kernel before it)."""
     if w.kind == "mxfp8":
         return "gemm_mxfp8_2cta_kernel" if plan["variant"] == 2 else "gemm_mxfp8_kernel"
     return {1: "gemm16_1cta_kernel", 2: "gemm16_2cta_kernel",
@@ -491,10 +496,10 @@ def library_context(w, A, B, flush_l2, stream, steps, dev):
     """torch.matmul (cuBLAS) on the same device operands, with the same L2 flush and per-step
     CUDA-event timing: a context figure beside ours, not a baseline and not on our path. None for
     the block-scaled workloads (torch has no product with one E8M0 scale per row per 128 or 32
-    K-elements in this row-major scale layout)."""
+    K-elements, or one UE4M3 scale per 16, in this row-major scale layout)."""
     import torch
 
-    if w.kind == "mxfp8" or w.kind.endswith("_sp24"):
+    if w.kind in ("mxfp8", "nvfp4") or w.kind.endswith("_sp24"):
         return None
     a_op = A.t() if w.layout[0] == "T" else A  # A stored [K,M] for TN and TT
     b_op = B.t() if w.layout[1] == "T" else B  # B stored [N,K] for NT and TT
@@ -539,7 +544,7 @@ def device_inputs(w, dev):
     from dense_tensor_core_gb300 import workloads
 
     inputs = workloads.make(w)
-    if w.kind == "mxfp8":
+    if w.kind in ("mxfp8", "nvfp4"):
         dev_in = [torch.from_numpy(x).to(dev) for x in inputs]
         return dev_in, torch.bfloat16, inputs
     if w.kind.endswith("_sp24"):  # stored values, metadata, B
@@ -566,7 +571,7 @@ def gemm_kwargs(args, w, dtc, dev):
         if ws_bytes:
             kw["workspace"] = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         return kw
-    base = w.kind[:-5] if w.kind.endswith("_sp24") else w.kind
+    base = w.kind[:-5] if w.kind.endswith("_sp24") else "bf16" if w.kind == "nvfp4" else w.kind
     kw = dict(layout=w.layout, variant=args.variant, split_k=args.split_k, tile_n=args.tile_n)
     if args.stream_k != 2:
         ws_bytes = dtc.gemm_workspace_size(base, w.M, w.N, w.K, w.layout, variant=args.variant,
@@ -578,6 +583,11 @@ def gemm_kwargs(args, w, dtc, dev):
         kw["sk_workspace"] = kw.pop("workspace", None)
         kw["sp_workspace"] = torch.empty(dtc.gemm_sp_workspace_size(base, w.M, w.K),
                                          dtype=torch.uint8, device=dev)
+    if w.kind == "nvfp4":  # the operands expanded to bf16, and the product's stream-K workspace
+        kw.pop("layout")
+        kw["sk_workspace"] = kw.pop("workspace", None)
+        kw["nv_workspace"] = torch.empty(dtc.gemm_nvfp4_workspace_size(w.M, w.N, w.K),
+                                         dtype=torch.uint8, device=dev)
     return kw
 
 
@@ -588,6 +598,10 @@ def call(dtc, w, ins, C, kw, stream):
         kw = dict(kw)
         dtc.gemm_sp(w.kind[:-5], ins[0], ins[1], ins[2], C, workspace=kw.pop("sp_workspace"),
                     stream=stream, **kw)
+    elif w.kind == "nvfp4":
+        kw = dict(kw)
+        dtc.gemm_nvfp4(ins[0], ins[1], ins[2], ins[3], C, workspace=kw.pop("nv_workspace"),
+                       stream=stream, **kw)
     else:
         dtc.gemm_ex(w.kind, ins[0], ins[1], C, stream=stream, **kw)
 
@@ -596,15 +610,17 @@ def plan_of(dtc, w, kw):
     keys = ("layout", "variant", "split_k", "tile_n", "workspace", "stream_k", "a_format",
             "b_format", "scale_block")
     kw = dict(kw)
-    if w.kind.endswith("_sp24"):  # the dense product that runs on the expanded A
+    if w.kind.endswith("_sp24") or w.kind == "nvfp4":  # the dense product on the expanded operands
         kw["workspace"] = kw.pop("sk_workspace", None)
-        return dtc.gemm_plan(w.kind[:-5], w.M, w.N, w.K, **{k: v for k, v in kw.items() if k in keys})
+        base = "bf16" if w.kind == "nvfp4" else w.kind[:-5]
+        return dtc.gemm_plan(base, w.M, w.N, w.K, **{k: v for k, v in kw.items() if k in keys})
     return dtc.gemm_plan(w.kind, w.M, w.N, w.K, **{k: v for k, v in kw.items() if k in keys})
 
 
 def launches_per_step(w, plan):
-    """Our kernels in one step: the GEMM, plus the 2:4 expansion or the scale repacking."""
-    return 2 if w.kind.endswith("_sp24") or plan.get("sf_packed") else 1
+    """Our kernels in one step: the GEMM, plus the 2:4 or NVFP4 expansion or the scale
+    repacking."""
+    return 2 if w.kind.endswith("_sp24") or w.kind == "nvfp4" or plan.get("sf_packed") else 1
 
 
 def timed_steps(step, flush_l2, steps, warmup, stream, dev, world):
@@ -644,6 +660,10 @@ def roofline_of(w, kernel_ms, bound, kernel_name, peaks, peak_src):
         # fp8 dense rate = 2x the bf16 rate (nominal 4.5 vs 2.25 PFLOP/s)
         peak = 2.0 * peaks["bf16_tflops"]
         note = f"2 x {peak_src} bf16 burst (nominal fp8:bf16 ratio)"
+    elif w.kind == "nvfp4":
+        peak = peaks["bf16_tflops"]
+        note = (f"{peak_src} bf16 burst: the NVFP4 product runs on the bf16 tensor cores after "
+                "the exact expansion of its operands (the fp4-rate kind is not used)")
     else:
         peak = peaks["bf16_tflops"]
         note = f"{peak_src} bf16 burst (kernel timed alone)"
@@ -773,13 +793,15 @@ def run_ours(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": (w.kind[:-5] if w.kind.endswith("_sp24") else "bf16" if w.kind == "bf16"
+        "dtype": (w.kind[:-5] if w.kind.endswith("_sp24") else "bf16" if w.kind in ("bf16", "nvfp4")
                   else "f16" if w.kind == "f16"
                   else w.a_fmt if w.a_fmt == w.b_fmt else f"{w.a_fmt}x{w.b_fmt}"),
         "data": "synthetic",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout,
                    "kind": w.kind, "variant": kernel_name,
                    **({"scale_block": w.block} if w.kind == "mxfp8" else {}),
+                   **({"inputs": "e2m1 x e2m1, UE4M3 scales per 16, expanded to bf16"}
+                      if w.kind == "nvfp4" else {}),
                    "tile": f"{plan['tile_m']}x{plan['tile_n']}x{plan['tile_k']}",
                    "stages": plan["stages"], "split_k": plan["split_k"], "ctas": plan["ctas"],
                    "stream_k_tiles": plan["sk_tiles"],

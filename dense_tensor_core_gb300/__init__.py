@@ -1,4 +1,5 @@
-"""GB300 (sm_103a) dense GEMM: C = A . B with bf16/fp16 or MXFP8 operands, fp32 accumulation.
+"""GB300 (sm_103a) dense GEMM: C = A . B with bf16/fp16, block-scaled (MX family) or NVFP4
+operands, fp32 accumulation.
 
 The compute runs in the CUDA library ``libdtc_gemm.so`` (C ABI in ``include/dtc_gemm.h``). This
 package is a thin ctypes binding with the same function names: it checks and marshals torch
@@ -23,6 +24,8 @@ from ._binding import (  # noqa: F401
     gemm_f16,
     gemm_last_error,
     gemm_mxfp8,
+    gemm_nvfp4,
+    gemm_nvfp4_workspace_size,
     gemm_plan,
     gemm_sp,
     gemm_sp_workspace_size,

@@ -93,6 +93,11 @@ def lib():
                               vp, ctypes.c_uint64, vp]
         L.gemm_sp_workspace_size.restype = i32
         L.gemm_sp_workspace_size.argtypes = [i32, i64, i64, ctypes.POINTER(ctypes.c_uint64)]
+        L.gemm_nvfp4.restype = i32
+        L.gemm_nvfp4.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ctypes.POINTER(gemm_options),
+                                 vp, ctypes.c_uint64, vp]
+        L.gemm_nvfp4_workspace_size.restype = i32
+        L.gemm_nvfp4_workspace_size.argtypes = [i64, i64, i64, ctypes.POINTER(ctypes.c_uint64)]
         L.gemm_workspace_size.restype = i32
         L.gemm_workspace_size.argtypes = [i32, i64, i64, i64, i32, ctypes.POINTER(gemm_options),
                                           ctypes.POINTER(ctypes.c_uint64)]
@@ -371,6 +376,48 @@ def gemm_ex_static_workspace(kind, A, B, C=None, layout="NT", variant=0, tile_n=
         _check(lib().gemm_ex_static_workspace(_DTYPE[kind], _ptr(A), _ptr(B), _ptr(sfA), _ptr(sfB),
                                               _ptr(C), M, N, K, _layout_code(layout),
                                               ctypes.byref(opts), _stream_handle(stream, dev)))
+    return C
+
+
+def gemm_nvfp4_workspace_size(M, N, K):
+    """Bytes of workspace gemm_nvfp4 needs (A and B expanded to bf16, A padded to 256 bytes)."""
+    out = ctypes.c_uint64(0)
+    _check(lib().gemm_nvfp4_workspace_size(M, N, K, ctypes.byref(out)))
+    return out.value
+
+
+def gemm_nvfp4(A, B, sfA, sfB, C=None, workspace=None, variant=0, split_k=0, tile_n=0, tile_k=0,
+               stream_k=0, sk_workspace=None, timeout_ns=0, stream=None):
+    """NVFP4 product, NT: A [M, K/2] and B [N, K/2] uint8 (packed e2m1 codes, element k in the
+    low nibble of byte k/2 for even k), sfA [M, K/16] and sfB [N, K/16] uint8 (UE4M3 scales).
+    `workspace` (gemm_nvfp4_workspace_size bytes of device memory) receives A and B expanded to
+    bf16; it is allocated here when not given. `sk_workspace` is the bf16 product's stream-K
+    workspace. Returns C [M,N] bf16."""
+    for t, name in ((A, "A"), (B, "B"), (sfA, "sfA"), (sfB, "sfB")):
+        _check_tensor(t, torch.uint8, name)
+        if t.dim() != 2:
+            raise ValueError(f"{name} must be 2-D")
+    M, K = A.shape[0], 2 * A.shape[1]
+    N = B.shape[0]
+    if B.shape[1] * 2 != K:
+        raise ValueError(f"B {tuple(B.shape)} does not match A {tuple(A.shape)}")
+    if K % 16:
+        raise ValueError(f"K = {K}: NVFP4 needs whole 16-element scale blocks")
+    if tuple(sfA.shape) != (M, K // 16) or tuple(sfB.shape) != (N, K // 16):
+        raise ValueError(f"sfA / sfB must be {(M, K // 16)} / {(N, K // 16)}, got "
+                         f"{tuple(sfA.shape)} / {tuple(sfB.shape)}")
+    C = _out(C, M, N, torch.bfloat16, A.device, rows_of_larger=True)
+    if workspace is None:
+        workspace = torch.empty(max(1, gemm_nvfp4_workspace_size(M, N, K)), dtype=torch.uint8,
+                                device=A.device)
+    opts = _options(variant, split_k, timeout_ns, 0, tile_n, tile_k, 0, 0, _ld(C),
+                    workspace=sk_workspace, stream_k=stream_k)
+    dev = _same_device(A, B, sfA, sfB, C, workspace, sk_workspace)
+    with torch.cuda.device(dev):
+        _check(lib().gemm_nvfp4(_ptr(A), _ptr(B), _ptr(sfA), _ptr(sfB), _ptr(C), M, N, K,
+                                ctypes.byref(opts), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(),
+                                _stream_handle(stream, dev)))
     return C
 
 

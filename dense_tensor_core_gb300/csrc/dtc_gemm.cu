@@ -926,6 +926,62 @@ int gemm_sp(int dtype, const void* vals, const void* meta, const void* B, void* 
     return launch_prepared(r, dtype, M, N, K, opts, (cudaStream_t)stream);
 }
 
+// NVFP4 workspace: the expanded A (bf16 [M,K]) at offset 0, the expanded B (bf16 [N,K]) at the
+// next 256-byte boundary.
+uint64_t nvfp4_b_offset(int64_t M, int64_t K) {
+    return ((uint64_t)M * (uint64_t)K * 2 + 255) & ~(uint64_t)255;
+}
+
+int gemm_nvfp4_workspace_size(int64_t M, int64_t N, int64_t K, uint64_t* bytes) {
+    g_err[0] = '\0';
+    if (!bytes) return fail(GEMM_ERR_INVALID_ARG, "bytes is NULL");
+    if (M < 0 || N < 0 || K < 0 || M > 2147483647 || N > 2147483647 || K > 2147483647)
+        return fail(GEMM_ERR_INVALID_ARG, "sizes must be in [0, 2^31-1]");
+    *bytes = nvfp4_b_offset(M, K) + (uint64_t)N * (uint64_t)K * 2;
+    return GEMM_OK;
+}
+
+int gemm_nvfp4(const void* A, const void* B, const void* sfA, const void* sfB, void* C, int64_t M,
+               int64_t N, int64_t K, const gemm_options* opts, void* workspace,
+               uint64_t workspace_bytes, dtc_stream_t stream) {
+    g_err[0] = '\0';
+    if (K % 16)
+        return fail(GEMM_ERR_INVALID_ARG, "K=%lld: NVFP4 needs K %% 16 == 0 (whole scale blocks)",
+                    (long long)K);
+    if (opts && (opts->lda || opts->ldb))
+        return fail(GEMM_ERR_INVALID_ARG, "NVFP4 rows are dense (lda and ldb must be 0)");
+    if (opts && (opts->mx_a_format || opts->mx_b_format || opts->mx_scale_block))
+        return fail(GEMM_ERR_INVALID_ARG, "NVFP4 fixes the element formats and the scale block "
+                    "(mx_a_format, mx_b_format and mx_scale_block must be 0)");
+    const bool work = M > 0 && N > 0 && K > 0;
+    uint64_t need = 0;
+    if (M >= 0 && N >= 0 && K >= 0 && M <= 2147483647 && N <= 2147483647 && K <= 2147483647)
+        need = nvfp4_b_offset(M, K) + (uint64_t)N * (uint64_t)K * 2;
+    char* ws = static_cast<char*>(workspace);
+    if (work) {
+        if (!A || !B || !sfA || !sfB) return fail(GEMM_ERR_INVALID_ARG, "A, B, sfA or sfB is NULL");
+        if (!aligned16(A) || !aligned16(B))
+            return fail(GEMM_ERR_INVALID_ARG, "A and B must be 16-byte aligned");
+        if (!workspace || !aligned16(workspace) || workspace_bytes < need)
+            return fail(GEMM_ERR_INVALID_ARG, "NVFP4 needs a 16-byte aligned workspace of %llu bytes "
+                        "(the operands expanded to bf16)", (unsigned long long)need);
+    }
+    // the bf16 product of the expanded operands (checks C, the sizes and the other options)
+    Prepared r;
+    int rc = prepare(0, work ? ws : nullptr, work ? ws + nvfp4_b_offset(M, K) : nullptr, nullptr,
+                     nullptr, C, M, N, K, GEMM_LAYOUT_NT, opts, &r);
+    if (rc) return rc;
+    if (work) {
+        if ((rc = check_device_ptr(A, r.dev, "A")) || (rc = check_device_ptr(B, r.dev, "B")) ||
+            (rc = check_device_ptr(sfA, r.dev, "sfA")) || (rc = check_device_ptr(sfB, r.dev, "sfB")))
+            return rc;
+        if ((rc = launch_nvfp4_expand(A, sfA, B, sfB, ws, ws + nvfp4_b_offset(M, K), M, N, K, r.info,
+                                      (cudaStream_t)stream)))
+            return rc;
+    }
+    return launch_prepared(r, 0, M, N, K, opts, (cudaStream_t)stream);
+}
+
 int gemm_device_model_query(gemm_device_model* out) {
     g_err[0] = '\0';
     if (!out) return fail(GEMM_ERR_INVALID_ARG, "out is NULL");

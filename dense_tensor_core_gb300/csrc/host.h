@@ -201,6 +201,10 @@ int launch_mx(const Launch& L);
 // 2:4 sparse A: writes the dense [M, K] 16-bit A into `dense` (stream-ordered).
 int launch_sp24_expand(bool bf16, const void* vals, const void* meta, void* dense, int64_t M,
                        int64_t K, DeviceInfo* dev, cudaStream_t stream);
+// NVFP4 operands (packed e2m1 rows, UE4M3 scales per 16) to bf16 [M,K] / [N,K] (nvfp4_expand.cuh).
+int launch_nvfp4_expand(const void* A, const void* sfA, const void* B, const void* sfB,
+                        void* a_out, void* b_out, int64_t M, int64_t N, int64_t K,
+                        DeviceInfo* dev, cudaStream_t stream);
 
 // Resident clusters of the pair kernel and of the split-K kernels (clusters of 2 and 4).
 int query_pair_clusters(DeviceInfo* dev);

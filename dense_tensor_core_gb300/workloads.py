@@ -35,7 +35,8 @@ BITS = {"e4m3": 8, "e5m2": 8, "e2m3": 6, "e3m2": 6, "e2m1": 4}  # bits per eleme
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str  # "bf16", "f16", "mxfp8" (block-scaled) or "bf16_sp24" / "f16_sp24" (2:4 sparse A)
+    kind: str  # "bf16", "f16", "mxfp8" (block-scaled, E8M0 scales), "nvfp4" (e2m1, UE4M3 scales
+    #            per 16) or "bf16_sp24" / "f16_sp24" (2:4 sparse A)
     layout: str  # "NT" (B is [N,K]), "NN" (B is [K,N]); a leading "T" stores A as [K,M]
     M: int
     N: int
@@ -56,6 +57,8 @@ class Workload:
             kb = (self.K + self.block - 1) // self.block
             return (self.M * self.K * BITS[self.a_fmt] // 8 + self.N * self.K * BITS[self.b_fmt] // 8
                     + (self.M + self.N) * kb + 2 * self.M * self.N)
+        if self.kind == "nvfp4":  # packed e2m1 rows, one scale byte per 16 elements, bf16 C
+            return (self.M + self.N) * (self.K // 2 + self.K // 16) + 2 * self.M * self.N
         if self.kind.endswith("_sp24"):  # stored values, metadata, B, C
             return self.M * self.K + self.M * self.K // 8 + 2 * (self.N * self.K + self.M * self.N)
         return 2 * (self.M * self.K + self.N * self.K + self.M * self.N)
@@ -86,6 +89,8 @@ WORKLOADS = {
         Workload("mxfp6_e2m3_e3m2_b32_nt_4096x4096x8192", "mxfp8", "NT", 4096, 4096, 8192, 10,
                  a_fmt="e2m3", b_fmt="e3m2", block=32),
         Workload("bf16_sp24_nt_4096x4096x8192", "bf16_sp24", "NT", 4096, 4096, 8192, 11),
+        Workload("nvfp4_nt_4096x4096x8192", "nvfp4", "NT", 4096, 4096, 8192, 12,
+                 a_fmt="e2m1", b_fmt="e2m1", block=16),
     ]
 }
 
@@ -205,6 +210,26 @@ def make_sub_byte(M: int, N: int, K: int, seed: int, a_fmt: str, b_fmt: str, blo
     return A, B, (ua + 127).to(torch.uint8).numpy(), (ub + 127).to(torch.uint8).numpy()
 
 
+def make_nvfp4(M: int, N: int, K: int, seed: int):
+    """(A [M, K/2], B [N, K/2] packed e2m1 rows, sfA [M, K/16], sfB [N, K/16] UE4M3 codes) of an
+    NVFP4 product, K % 16 == 0. Elements: e2m1(2x) with x ~ N(0,1) (round to nearest, ties to the
+    even code, saturating at 6), so the codes spread over the whole e2m1 range; scales: UE4M3
+    codes with exponent field uniform in {4..10} and mantissa uniform in {0..7} (values 2^-3 ..
+    1.875 * 2^3), independent per (row, 16-element block)."""
+    g = torch.Generator().manual_seed(seed)
+    kb = K // 16
+
+    def operand(rows):
+        x = 2.0 * torch.randn((rows, K), generator=g, dtype=torch.float32).numpy().astype(np.float64)
+        e = torch.randint(4, 11, (rows, kb), generator=g, dtype=torch.int32)
+        m = torch.randint(0, 8, (rows, kb), generator=g, dtype=torch.int32)
+        return (pack_rows(quantise_sub_byte(x, "e2m1"), 4), ((e << 3) | m).to(torch.uint8).numpy())
+
+    A, sfA = operand(M)
+    B, sfB = operand(N)
+    return A, B, sfA, sfB
+
+
 def make_mxfp8(M: int, N: int, K: int, seed: int):
     """(A [M,K] e4m3, B [N,K] e4m3, sfA [M,kb] E8M0, sfB [N,kb] E8M0) as uint8 codes, kb =
     ceil(K/128)."""
@@ -230,6 +255,8 @@ def make_sp24(kind: str, layout: str, M: int, N: int, K: int, seed: int):
 
 
 def make(w: Workload):
+    if w.kind == "nvfp4":
+        return make_nvfp4(w.M, w.N, w.K, w.seed)
     if w.kind.endswith("_sp24"):
         return make_sp24(w.kind[:-5], w.layout, w.M, w.N, w.K, w.seed)
     if w.kind == "mxfp8" and (BITS[w.a_fmt] < 8 or BITS[w.b_fmt] < 8):

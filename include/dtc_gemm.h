@@ -274,6 +274,34 @@ int gemm_sp(int dtype, const void* vals, const void* meta, const void* B, void* 
 int gemm_sp_workspace_size(int dtype, int64_t M, int64_t K, uint64_t* bytes);
 
 /*
+ * NVFP4 block-scaled GEMM, NT only (the NVFP4 member of the "other block-scaled formats" of the
+ * 05 Blackwell TCGEN05 GEMM tutorial, "Advanced": gemm_blockscaled):
+ *   C[m,n] = bf16( sum_k e2m1(A[m,k]) ue4m3(sfA[m,k/16]) * e2m1(B[n,k]) ue4m3(sfB[n,k/16]) )
+ *   A: [M, K/2] bytes, B: [N, K/2] bytes: packed e2m1 (OCP MX FP4) codes, element k of a row in
+ *   the low nibble of byte k/2 for even k, the high nibble for odd k. sfA: [M, K/16], sfB:
+ *   [N, K/16] UE4M3 scale bytes (e4m3 codes with the sign bit clear; a code with the sign bit
+ *   set, or the e4m3 NaN code, scales to NaN). C: [M,N] bf16.
+ * The call writes A and B multiplied by their scales into `workspace` as bf16 (exact: at most 5
+ * significant bits per product) with an HBM-bound kernel, then runs the bf16 product of the two on
+ * the tensor cores; both are enqueued on `stream`. `workspace` is device memory of the current
+ * device, 16-byte aligned, of at least gemm_nvfp4_workspace_size bytes, owned by the caller; its
+ * contents need no initial value and are overwritten. opts may be NULL; the variant, tile, ldc,
+ * wait limit and stream-K options (with opts->workspace as the stream-K workspace) apply to the
+ * product; lda, ldb, mx_a_format, mx_b_format and mx_scale_block must be 0.
+ * INVALID_ARG as for gemm_bf16, and also when K % 16 != 0, A or B is NULL or not 16-byte aligned,
+ * sfA or sfB is NULL, or the workspace is NULL, misaligned or too small (the checks on A, B, the
+ * scales and the workspace apply when M, N and K are all non-zero).
+ */
+int gemm_nvfp4(const void* A, const void* B, const void* sfA, const void* sfB, void* C,
+               int64_t M, int64_t N, int64_t K, const gemm_options* opts, void* workspace,
+               uint64_t workspace_bytes, dtc_stream_t stream);
+
+/* Bytes of workspace gemm_nvfp4 needs: the expanded A (M x K bf16), padded to 256 bytes, then the
+ * expanded B (N x K bf16). INVALID_ARG for sizes outside [0, 2^31-1] or a NULL bytes. (05 Blackwell
+ * TCGEN05 GEMM tutorial, "Advanced": gemm_blockscaled.) */
+int gemm_nvfp4_workspace_size(int64_t M, int64_t N, int64_t K, uint64_t* bytes);
+
+/*
  * Bytes of workspace (gemm_options.workspace) with which the call would use stream-K on CTA pairs
  * (the last, part-full wave's tiles shared out over all pairs as equal runs of K-blocks, the
  * pieces summed through the workspace); 0 when it would not (or stream_k == 2). For the

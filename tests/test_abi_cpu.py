@@ -36,7 +36,7 @@ def L():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("gemm_bf16", "gemm_f16", "gemm_mxfp8", "gemm_ex", "gemm_plan", "gemm_last_error",
-              "gemm_stream_status"):
+              "gemm_stream_status", "gemm_nvfp4", "gemm_nvfp4_workspace_size"):
         assert n in names
 
 
@@ -159,6 +159,51 @@ def test_block_scaled_options_rejected_before_cuda(L, dtype, opt):
                    ctypes.byref(o), None)
     assert rc == INVALID
     assert L.gemm_last_error()
+
+
+def _nvfp4(L, A=0x1000, B=0x2000, sfA=0x10, sfB=0x20, C=0x3000, M=16, N=16, K=32, opts=None,
+           ws=0x40000, ws_bytes=1 << 20):
+    vp = ctypes.c_void_p
+    return L.gemm_nvfp4(vp(A), vp(B), vp(sfA), vp(sfB), vp(C), M, N, K,
+                        ctypes.byref(opts) if opts is not None else None, vp(ws), ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(K=24),             # not whole 16-element scale blocks
+    dict(K=-16),
+    dict(A=0),
+    dict(sfB=0),
+    dict(A=0x1008),         # packed rows must start 16-byte aligned
+    dict(C=0),
+    dict(ws=0),             # no workspace
+    dict(ws=0x40008),       # misaligned workspace
+    dict(ws_bytes=2047),    # one byte short: 16 x 32 x 2 for A padded to 1024, + 1024 for B
+    dict(N=12),             # C rows of 24 bytes
+])
+def test_nvfp4_rules(L, kw):
+    assert _nvfp4(L, **kw) == INVALID
+    assert L.gemm_last_error()
+
+
+@pytest.mark.parametrize("opt", [dict(lda=16), dict(ldb=32), dict(mx_scale_block=16),
+                                 dict(mx_a_format=4)])
+def test_nvfp4_rejects_options_that_do_not_apply(L, opt):
+    from dense_tensor_core_gb300._binding import gemm_options
+
+    o = gemm_options()
+    for k, v in opt.items():
+        setattr(o, k, v)
+    assert _nvfp4(L, opts=o) == INVALID
+
+
+def test_nvfp4_empty_output_and_workspace_size(L):
+    assert _nvfp4(L, A=0, B=0, sfA=0, sfB=0, C=0, M=0, ws=0, ws_bytes=0) == 0
+    out = ctypes.c_uint64(0)
+    assert L.gemm_nvfp4_workspace_size(16, 16, 32, ctypes.byref(out)) == 0
+    assert out.value == 2048  # A: 16 x 32 x 2 = 1024 (already a multiple of 256), B: 1024
+    assert L.gemm_nvfp4_workspace_size(3, 5, 16, ctypes.byref(out)) == 0
+    assert out.value == 256 + 5 * 16 * 2  # A's 96 bytes padded to 256
+    assert L.gemm_nvfp4_workspace_size(-1, 5, 16, ctypes.byref(out)) == INVALID
 
 
 def test_static_workspace_entry_refuses_a_caller_workspace(L):
