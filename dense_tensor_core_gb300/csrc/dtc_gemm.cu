@@ -519,66 +519,50 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
     if (dtype == 2) {
         if (v != GEMM_VARIANT_AUTO && v != GEMM_VARIANT_1CTA && v != GEMM_VARIANT_2CTA)
             return fail(GEMM_ERR_UNSUPPORTED, "the MXFP8 product has one-CTA and pair kernels");
-        if (want_n && want_n != 224 && !(want_n == 256 && v == GEMM_VARIANT_2CTA))
-            return fail(GEMM_ERR_UNSUPPORTED, "the block-scaled kernels use 224-wide tiles (256 "
-                        "on CTA pairs)");
-        // The one-CTA kernel (128 x 224 tiles, 4 stages of 128 K-elements or 2 of 256) or the
-        // pair kernel (256 x 224 or 256 x 256 tiles, 6 stages of 128 K-elements per CTA, or 3 of
-        // 256 with repacked scales). AUTO takes the pair kernel with 256-deep stages for
-        // 128-element scale blocks when a workspace holds the repacked scales, K % 128 == 0 and
-        // the pair tiles fill at least one wave with most of their 256 rows (GB300, 4096 x 4096
-        // x 8192: e4m3 102.4 us against 108.8 on the one-CTA kernel, fp4 and fp6 100.4 against
-        // 106.8 and 108.8); otherwise the one-CTA kernel (32-element blocks: 115.7 against
-        // 133.2; the pair kernel's 128-deep stages 118.8 with a workspace, 137.2 without).
-        const int block_auto = (o && o->mx_scale_block) ? o->mx_scale_block : 128;
-        bool deep_pair = false;
+        if (want_n && want_n != 224)
+            return fail(GEMM_ERR_UNSUPPORTED, "the block-scaled kernels use 224-wide tiles");
+        const int bk_want = o ? o->tile_k : 0;
+        if (bk_want && bk_want != 128 && bk_want != 256)
+            return fail(GEMM_ERR_INVALID_ARG, "tile_k %d is not 128 or 256 for the block-scaled kernels", bk_want);
+        const int block = (o && o->mx_scale_block) ? o->mx_scale_block : 128;
+        const uint64_t need = sf_pack_layout(M, N, (K + block - 1) / block, 224).bytes;
+        const bool ws = o && o->workspace && o->workspace_bytes >= need;
+        // Two kernels. The pair kernel (256 x 224 tiles, 3 stages of 256 K-elements, scales
+        // repacked into the workspace) takes 128-element scale blocks with K % 128 == 0; AUTO
+        // takes it when a workspace holds the repacked scales and the pair tiles fill at least
+        // one wave with most of their 256 rows (GB300, 4096 x 4096 x 8192: e4m3 102.4 us against
+        // 108.8 on the one-CTA kernel, fp4 and fp6 100.4 against 106.8 and 108.8). The one-CTA
+        // kernel (128 x 224 tiles, 4 stages of 128 K-elements) takes everything else.
         if (v == GEMM_VARIANT_AUTO) {
-            const uint64_t need = sf_pack_layout(M, N, (K + block_auto - 1) / block_auto, 224).bytes;
-            const bool bk_ok = !o || o->tile_k == 0 || o->tile_k == 256;
-            deep_pair = block_auto == 128 && !want_n && bk_ok && K % 128 == 0 && o && o->workspace &&
-                        o->workspace_bytes >= need && (M % 256 == 0 || M % 256 > 128) &&
-                        (int64_t)ceil_div(M, 256) * ceil_div(N, 224) >= pairs;
-            v = deep_pair ? GEMM_VARIANT_2CTA : GEMM_VARIANT_1CTA;
+            const bool pair = block == 128 && ws && K % 128 == 0 && bk_want != 128 &&
+                              (M % 256 == 0 || M % 256 > 128) &&
+                              (int64_t)ceil_div(M, 256) * ceil_div(N, 224) >= pairs;
+            v = pair ? GEMM_VARIANT_2CTA : GEMM_VARIANT_1CTA;
         }
         if (v == GEMM_VARIANT_2CTA) {
-            const int bk_want = deep_pair ? 256 : (o ? o->tile_k : 0);
-            if (bk_want && bk_want != 128 && bk_want != 256)
-                return fail(GEMM_ERR_INVALID_ARG, "tile_k %d is not 128 or 256 for the block-scaled pair kernel", bk_want);
+            if (block != 128 || K % 128 || !ws || bk_want == 128)
+                return fail(GEMM_ERR_UNSUPPORTED, "the block-scaled pair kernel takes 128-element "
+                            "scale blocks, K %% 128 == 0, 256-deep stages and a workspace of %llu "
+                            "bytes for the repacked scales", (unsigned long long)need);
             p->variant = v;
             p->cluster = 2;
             p->tile_m = 256;
-            p->tile_n = want_n ? want_n : dtc::gmx2::kBN;
+            p->tile_n = dtc::gmx2::kBN;
+            p->tile_k = dtc::gmx2::kBlocks * dtc::gmx2::kBK;
+            p->stages = dtc::gmx2::kNStages;
             p->tiles = ceil_div(M, 256) * ceil_div(N, p->tile_n);
             p->ctas = 2 * std::min(p->tiles, pairs);
-            // 224-wide pair tiles take the scales repacked into a large enough workspace (e4m3,
-            // 4096 x 4096 x 8192: 125 us against 137 with 128-element blocks, 148 against 455
-            // with 32-element ones)
-            const int block = (o && o->mx_scale_block) ? o->mx_scale_block : 128;
-            const uint64_t need = sf_pack_layout(M, N, (K + block - 1) / block, p->tile_n).bytes;
-            p->sf_pack = p->tile_n == 224 && o && o->workspace && o->workspace_bytes >= need;
-            // 256-deep stages (3-D boxes over 128-byte K-chunks) need K % 128 == 0 and the
-            // repacked scales
-            if (bk_want == 256 && (K % 128 || !p->sf_pack))
-                return fail(GEMM_ERR_UNSUPPORTED, "256-deep pair stages need K %% 128 == 0 and a "
-                            "workspace for the repacked scales (224-wide tiles)");
-            p->tile_k = bk_want == 256 ? 2 * dtc::gmx2::kBK : dtc::gmx2::kBK;
-            p->stages = bk_want == 256 ? dtc::gmx2::Cfg<224, true, true>::kNStages : dtc::gmx2::kStages;
+            p->sf_pack = true;
             return GEMM_OK;
         }
+        if (bk_want == 256)
+            return fail(GEMM_ERR_UNSUPPORTED, "the one-CTA block-scaled kernel takes 128-deep "
+                        "stages (256-deep ones are the pair kernel's)");
         p->variant = GEMM_VARIANT_1CTA;
         p->tile_m = dtc::gmx::kBM;
         p->tile_n = dtc::gmx::kBN;
-        // 256-deep stages (3-D boxes over 128-byte K-chunks) need K % 128 == 0
-        const int bk_want = o ? o->tile_k : 0;
-        if (bk_want && bk_want != 128 && bk_want != 256)
-            return fail(GEMM_ERR_INVALID_ARG, "tile_k %d is not 128 or 256 for the MXFP8 kernel", bk_want);
-        if (bk_want == 256 && K % 128)
-            return fail(GEMM_ERR_UNSUPPORTED, "256-deep MXFP8 stages need K %% 128 == 0");
-        // 128-deep stages by default: on GB300 (4096 x 4096 x 8192) they ran as fast as 256-deep
-        // ones for e4m3 (110.5 us both) and faster for fp6 (110.2 against 120.8)
-        const bool deep = bk_want == 256;
-        p->tile_k = deep ? 2 * dtc::gmx::kBK : dtc::gmx::kBK;
-        p->stages = deep ? dtc::gmx::Cfg<true>::kStages : dtc::gmx::Cfg<false>::kStages;
+        p->tile_k = dtc::gmx::kBK;
+        p->stages = dtc::gmx::Cfg<>::kStages;
         p->tiles = ceil_div(M, p->tile_m) * ceil_div(N, p->tile_n);
         p->ctas = std::min(p->tiles, sms);
         // With 32-element scale blocks and a large enough workspace the scales are repacked
@@ -586,9 +570,7 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
         // kernel's scale warps: 4096 x 4096 x 8192 e4m3 ran 115.7 us against 307. With
         // 128-element blocks the scale warps keep up (108.8 us against 109.6 repacked, the
         // repacking included), so they stay.
-        const int block = (o && o->mx_scale_block) ? o->mx_scale_block : 128;
-        const uint64_t need = sf_pack_layout(M, N, (K + block - 1) / block, p->tile_n).bytes;
-        p->sf_pack = block == 32 && o && o->workspace && o->workspace_bytes >= need;
+        p->sf_pack = block == 32 && ws;
         return GEMM_OK;
     }
     const int num_kb = ceil_div(K, 64);

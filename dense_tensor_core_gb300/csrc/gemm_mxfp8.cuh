@@ -9,9 +9,10 @@
 // The instruction takes one scale per row per 32 K-elements. With granularity 128 the four MMAs
 // of a 128-deep K-block all use the same scales. A K-block of 128 e4m3 = 128 bytes per row = one
 // 128-byte swizzle row, and the shared-memory descriptors are those of the bf16 kernels (32 bytes
-// per MMA step). A pipeline stage is one K-block (2-D boxes, any K) or, with kDeep, two (one 3-D
-// box {128, rows, 2} per operand, K % 128 == 0): the larger TMA instructions stream faster per SM,
-// though only two 88 KB stages fit.
+// per MMA step). A pipeline stage is one K-block (2-D boxes, any K), in a ring of 4. (Stages of two
+// K-blocks, one 3-D box per operand, fit only twice beside the output staging and measured level
+// or slower here -- 110.9 against 112.7 us, fp6 110.9 against 122.6 on 4096 x 4096 x 8192 -- so
+// this kernel does not take them; the pair kernel does.)
 //
 // Scales live in Tensor Memory. For an operand of R rows (128 for A, 224 for B) they take R/32
 // columns: row r sits in lane r % 32 of column r / 32, repeated in each of the four 32-lane
@@ -84,13 +85,13 @@ static_assert(kBN <= 256, "a B tile's scales fit two 128-row chunks");
 
 constexpr int threads_for(bool tma_sf) { return tma_sf ? 192 : kThreads; }
 
-// Stage geometry: kBlocks K-blocks per stage (1: 2-D boxes, 4 stages; 2: 3-D boxes, 2 stages).
+// Stage geometry: one K-block per stage (2-D boxes), 4 stages.
 // With kTmaSf each stage has a slot for the chunks of the sets that start in it (at most one per
 // K-block).
-template <bool kDeep, bool kTmaSf = false>
+template <bool kTmaSf = false>
 struct Cfg {
-    static constexpr int kBlocks = kDeep ? 2 : 1;
-    static constexpr int kStages = kDeep ? 2 : 4;
+    static constexpr int kBlocks = 1;
+    static constexpr int kStages = 4;
     static constexpr int kAStage = kBM * kBK * kBlocks;
     static constexpr int kBStage = kBN * kBK * kBlocks;
     static constexpr int kStageBytes = kAStage + kBStage;
@@ -118,14 +119,14 @@ __device__ __forceinline__ uint32_t sf_word(const uint8_t* sf, int rows, int col
     return w;
 }
 
-template <bool kDeep, bool kB32, bool kTmaSf = false>
+template <bool kB32, bool kTmaSf = false>
 __global__ void __launch_bounds__(gmx::threads_for(kTmaSf), 1)
     gemm_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmC,
                       const __grid_constant__ CUtensorMap tmC32, const GemmMxArgs args) {
     using namespace gmx;
-    using C_ = Cfg<kDeep, kTmaSf>;
+    using C_ = Cfg<kTmaSf>;
     constexpr int kStages = C_::kStages;
     constexpr int kAStage = C_::kAStage;
     constexpr int kBStage = C_::kBStage;
@@ -217,13 +218,8 @@ __global__ void __launch_bounds__(gmx::threads_for(kTmaSf), 1)
                         }
                     }
                     mbar_arrive_expect_tx(full, tx);
-                    if constexpr (kDeep) {
-                        tma_load_3d(sA + s * kAStage, &tmA, full, 0, mt * kBM, st * 2);
-                        tma_load_3d(sB + s * kBStage, &tmB, full, 0, nt * kBN, st * 2);
-                    } else {
-                        tma_load_2d(sA + s * kAStage, &tmA, full, st * kBK, mt * kBM);
-                        tma_load_2d(sB + s * kBStage, &tmB, full, st * kBK, nt * kBN);
-                    }
+                    tma_load_2d(sA + s * kAStage, &tmA, full, st * kBK, mt * kBM);
+                    tma_load_2d(sB + s * kBStage, &tmB, full, st * kBK, nt * kBN);
                     if constexpr (kTmaSf) {
                         // the chunks of each set that starts in this stage, into slot h; the
                         // kernel that writes them may still be running (it launched this one

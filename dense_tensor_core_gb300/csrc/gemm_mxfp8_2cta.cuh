@@ -1,39 +1,39 @@
 // gemm_mxfp8_2cta.cuh -- persistent block-scaled GEMM on CTA pairs (cluster 2x1, tcgen05
 // cta_group::2), NT layout: fp8 / fp6 / fp4 elements (e4m3, e5m2, e2m3, e3m2, e2m1 for A and B
-// independently) with one E8M0 scale per row per 128 K-elements (kB32: per 32), fp32 accumulation
-// in Tensor Memory, bf16 output.
+// independently) with one E8M0 scale per row per 128 K-elements, fp32 accumulation in Tensor
+// Memory, bf16 output.
 //
 // The product of gemm_mxfp8.cuh (05 Blackwell TCGEN05 GEMM tutorial, "Advanced": gemm_blockscaled
 // with granularity 128 for both operands, and "other block-scaled formats"), on the operand feed
-// that keeps the tensor pipe busy on GB300: a pair computes a 256 x 224 tile; CTA r loads its own
-// 128 rows of A and its own 112 rows of B^T, 128 K-elements per stage (one 128-byte swizzled row
-// per operand row, whatever the element format: fp6 / fp4 rows are unpacked by the tensor memory
-// access unit into 16-byte groups), in a ring of 6 stages of 30 KB per CTA. At the fp8 rate a
-// stage is 448 tensor cycles of work, so five stages in flight cover ~2200 cycles of load latency
-// (a ring of three 60 KB stages covered half that, and the kernel waited for its operands). Both
-// CTAs' copies complete on the leader's full barrier; the leader's single MMA thread issues
+// that keeps the tensor pipe busiest on GB300: a pair computes a 256 x 224 tile; CTA r loads its
+// own 128 rows of A and its own 112 rows of B^T, 256 K-elements per stage, each operand in one 3-D
+// box {128 bytes, rows, 2} over the array viewed as [K/128][rows][128 bytes] (one 128-byte swizzled
+// row per operand row and K-block, whatever the element format: fp6 / fp4 rows are unpacked by the
+// tensor memory access unit into 16-byte groups), 32 KB of A and 28 KB of B per CTA per stage, in
+// a ring of 3 stages (K % 128 == 0). A TMA instruction that moves more bytes streams faster per
+// SM, which the fp8 rate needs: 2-D boxes of one K-block per stage, in a ring of 6, ran 118.8 us
+// on 4096 x 4096 x 8192 against 102.4 here. Both CTAs' copies complete on the leader's full
+// barrier; the leader's single MMA thread issues
 // tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X (M = 256, N = 224, K = 32),
-// four per stage, with descriptors advanced by 32-bit adds, and releases each stage in both CTAs
+// eight per stage, with descriptors advanced by 32-bit adds, and releases each stage in both CTAs
 // with one multicast commit.
 //
 // Scales, as in the one-CTA kernel: R rows take R/32 Tensor Memory columns (row r in lane r % 32
-// of column r / 32, repeated in all four lane quarters); one 32-bit cell packs 4 scale bytes of a
-// row (4 consecutive 128-element K-blocks, selected by a_sf_id / b_sf_id = K-block % 4; with
-// 32-element blocks the 4 blocks of one K-block, selected per MMA). Each CTA holds the scales of
-// its own 128 A rows and of all 224 B rows (each CTA's datapath computes all 224 columns of its
-// rows); its four scale warps write them with tcgen05.st and arrive on the leader's scale-full
-// barrier (8 arrivals per set), and the leader's MMA thread releases a set in both CTAs with one
-// multicast commit.
+// of column r / 32, repeated in all four lane quarters); one 32-bit cell packs the scale bytes of
+// 4 consecutive 128-element K-blocks of a row, selected by a_sf_id / b_sf_id = K-block % 4. Each
+// CTA holds the scales of its own 128 A rows and of all 224 B rows (each CTA's datapath computes
+// all 224 columns of its rows). They come repacked by sf_pack_kernel (sf_pack.cuh) into the
+// caller's workspace: each CTA's producer loads, beside the stage that holds a scale set's first
+// K-block, the 512-byte chunk of its own 128 A rows and the two chunks of the tile's B rows (2-D
+// boxes of 512 and 1024 bytes completing on the leader's full barrier), and the leader's MMA
+// thread moves them into both CTAs' Tensor Memory with three tcgen05.cp.cta_group::2.32x128b.warpx4
+// before the set's first MMA (each CTA copies from its own shared memory). That point, where the
+// MMAs change scale set anyway and the stage's operands have landed, is where the copies cost
+// least: copies issued a stage earlier (between two MMAs of one set), ahead of the full-barrier
+// wait, or from a second thread all measured slower.
 //
 // Tensor Memory per CTA: accumulators at columns [0,224) and [224,448), scale sets at
 // 448 + 12*set (4 columns for A, 8 for B), set = 0..3.
-//
-// With kTmaSf (224-wide tiles) the scales come repacked by sf_pack_kernel, as in the one-CTA
-// kernel: each CTA's producer loads, beside the stage that holds a set's first K-block, the chunk
-// of its own 128 A rows and the two chunks of the tile's B rows (2-D boxes of 512 and 1024 bytes
-// completing on the leader's full barrier), and the leader's MMA thread moves them into both CTAs'
-// Tensor Memory with three tcgen05.cp.cta_group::2.32x128b.warpx4 before the set's first MMA (each
-// CTA copies from its own shared memory). No scale warps: 6 warps.
 #pragma once
 
 #include "gemm_mxfp8.cuh"
@@ -42,56 +42,40 @@ namespace dtc {
 
 namespace gmx2 {
 constexpr int kBMc = 128;   // rows of C per CTA
-constexpr int kBK = 128;    // K-elements per stage: one 128-byte swizzled row per operand row
-constexpr int kStages = 6;
-constexpr int kThreads = 320;
-constexpr int kAStage = kBMc * 128;
+constexpr int kBN = 224;    // columns of C per pair tile
+constexpr int kHalfN = kBN / 2;
+constexpr int kBK = 128;    // K-elements per K-block: one 128-byte swizzled row per operand row
+constexpr int kBlocks = 2;  // K-blocks per stage
+constexpr int kNStages = 3;
+constexpr int kThreads = 192;  // producer, MMA, 4 epilogue warps
+constexpr int kAChunk = kBMc * 128;    // one K-block of the CTA's 128 rows of A
+constexpr int kBChunk = kHalfN * 128;  // one K-block of its 112 rows of B
+constexpr int kAStg = kAChunk * kBlocks;
+constexpr int kBStage = kBChunk * kBlocks;
+constexpr int kStageBytes = kAStg + kBStage;
 constexpr int kCBytes = 4 * 2 * 4096;  // two 4 KB output staging slots per epilogue warp
 constexpr int kTmemCols = 512;
+constexpr int kAccStride = kBN;
+constexpr int kSfBase = 2 * kBN;       // after the two accumulators
 constexpr int kSfSet = 12;
 constexpr int kSfSets = 4;
+constexpr int kGroup = 4;  // K-blocks per scale set
+constexpr int kSlotBytes = gmx::kSfSetBytes;  // a stage starts at most one scale set
+constexpr int kSmemBytes = kNStages * (kStageBytes + kSlotBytes) + kCBytes + 1024;
 constexpr int kGroupM = 8;
 constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
 constexpr uint64_t kPeerSettleNs = 1000ull * 1000;
-
-constexpr int threads_for(bool tma_sf) { return tma_sf ? 192 : kThreads; }
-
-// Pair tile width kBN (224 or 256). Tensor Memory holds the accumulators and 4 scale sets: two
-// 224-column accumulators (448 + 48 <= 512 columns), or one 256-column accumulator (the epilogue of
-// a tile then finishes before the next tile's first MMA). With kTmaSf each stage has a 1.5 KB slot
-// for the chunks of a set that starts in it.
-//
-// With kDeep (repacked scales only) a stage holds two K-blocks: each operand comes in one 3-D box
-// {128 bytes, rows, 2} (32 KB of A and 28 KB of B per CTA, K % 128 == 0), 3 stages. A TMA
-// instruction that moves more bytes streams faster per SM, which the fp8 rate needs.
-template <int kBN, bool kTmaSf = false, bool kDeep = false>
-struct Cfg {
-    static constexpr int kBlocks = kDeep ? 2 : 1;  // 128-element K-blocks per stage
-    static constexpr int kNStages = kDeep ? 3 : kStages;
-    static constexpr int kHalfN = kBN / 2;
-    static constexpr int kAChunk = kAStage;        // one K-block of the CTA's 128 rows of A
-    static constexpr int kBChunk = kHalfN * 128;   // one K-block of its kBN/2 rows of B
-    static constexpr int kAStg = kAChunk * kBlocks;
-    static constexpr int kBStage = kBChunk * kBlocks;
-    static constexpr int kStageBytes = kAStg + kBStage;
-    static constexpr int kAccBufs = kBN == 256 ? 1 : 2;
-    static constexpr int kAccStride = kBN;
-    static constexpr int kSfBase = kAccBufs * kBN;
-    static constexpr int kSlotBytes = kTmaSf ? kBlocks * gmx::kSfSetBytes : 0;
-    static constexpr int kSmemBytes = kNStages * (kStageBytes + kSlotBytes) + kCBytes + 1024;
-    static_assert(!kTmaSf || kBN == 224, "repacked scales on 224-wide pair tiles");
-    static_assert(!kDeep || kTmaSf, "256-deep pair stages take repacked scales");
-    static_assert(kBChunk % 1024 == 0, "chunks keep the 1024-byte swizzle alignment");
-    static_assert(kBN == 224 || kBN == 256, "pair tiles 224 or 256 wide");
-    static_assert(kAStage % 1024 == 0 && kBStage % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
-    static_assert(kSmemBytes <= 227 * 1024 - 512, "shared memory budget");
-    static_assert(kSfBase + kSfSets * kSfSet <= kTmemCols, "Tensor Memory budget");
-};
-constexpr int kBN = 224;  // the default pair tile width
+static_assert(kBChunk % 1024 == 0, "chunks keep the 1024-byte swizzle alignment");
+static_assert(kAStg % 1024 == 0 && kBStage % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+static_assert(kSmemBytes <= 227 * 1024 - 512, "shared memory budget");
+static_assert(kSfBase + kSfSets * kSfSet <= kTmemCols, "Tensor Memory budget");
+static_assert(kGroup % kBlocks == 0, "scale sets start at stage boundaries");
 }  // namespace gmx2
 
-template <bool kB32, int kBN, bool kTmaSf = false, bool kDeep = false>
-__global__ void __launch_bounds__(gmx2::threads_for(kTmaSf), 1)
+// (A template so that every translation unit that includes this header may define it; the one
+// instantiation is the 224-wide tile.)
+template <int kTileN = gmx2::kBN>
+__global__ void __launch_bounds__(gmx2::kThreads, 1)
     gemm_mxfp8_2cta_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmC,
@@ -99,23 +83,14 @@ __global__ void __launch_bounds__(gmx2::threads_for(kTmaSf), 1)
                            const __grid_constant__ CUtensorMap tmSA,
                            const __grid_constant__ CUtensorMap tmSB, const GemmMxArgs args) {
     using namespace gmx2;
-    using C_ = Cfg<kBN, kTmaSf, kDeep>;
-    constexpr int kNS = C_::kNStages;
-    constexpr int kAStg = C_::kAStg;
-    constexpr int kBlocks = C_::kBlocks;
-    constexpr int kHalfN = C_::kHalfN;
-    constexpr int kBStage = C_::kBStage;
-    constexpr int kStageBytes = C_::kStageBytes;
-    constexpr int kAccBufs = C_::kAccBufs;
-    constexpr int kAccStride = C_::kAccStride;
-    constexpr int kSfBase = C_::kSfBase;
-    constexpr int grp = kB32 ? 1 : 4;  // K-blocks per scale set
+    static_assert(kTileN == kBN, "one tile width");
+    constexpr int kNS = kNStages;
+    constexpr int grp = kGroup;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[kNS];
     __shared__ __align__(8) uint64_t bar_empty[kNS];
-    __shared__ __align__(8) uint64_t bar_tfull[kAccBufs];
-    __shared__ __align__(8) uint64_t bar_tempty[kAccBufs];
-    __shared__ __align__(8) uint64_t bar_sfull[kSfSets];
+    __shared__ __align__(8) uint64_t bar_tfull[2];
+    __shared__ __align__(8) uint64_t bar_tempty[2];
     __shared__ __align__(8) uint64_t bar_sempty[kSfSets];
     __shared__ __align__(8) uint64_t bar_drain;
     __shared__ uint32_t tmem_slot;
@@ -124,7 +99,7 @@ __global__ void __launch_bounds__(gmx2::threads_for(kTmaSf), 1)
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t sA = base;
     const uint32_t sB = base + kNS * kAStg;
-    const uint32_t sSF = base + kNS * kStageBytes + kCBytes;  // kTmaSf: scale slots
+    const uint32_t sSF = base + kNS * kStageBytes + kCBytes;  // scale slots
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
@@ -132,7 +107,6 @@ __global__ void __launch_bounds__(gmx2::threads_for(kTmaSf), 1)
     const int pair = blockIdx.x >> 1;
     const int num_pairs = gridDim.x >> 1;
     const int total = args.num_m * args.num_n;  // num_m counts 256-row pair tiles
-    const int groups = (args.num_kb + grp - 1) / grp;  // scale sets per tile
     const int num_st = (args.num_kb + kBlocks - 1) / kBlocks;  // stages per tile
     // Refilling a scale set's columns needs the MMAs that last read them done. Passing a stage's
     // full barrier already proves every MMA of the stages a whole ring earlier done (the stage was
@@ -140,7 +114,7 @@ __global__ void __launch_bounds__(gmx2::threads_for(kTmaSf), 1)
     // a multiple of the set length) spaced at least a ring apart the explicit wait, and the commit
     // it waits for, are not needed.
     constexpr bool kSfRingSafe = (kSfSets - 1) * grp + 1 >= kNS * kBlocks;
-    const bool sf_wait = kTmaSf && !(kSfRingSafe && args.num_kb % grp == 0);
+    const bool sf_wait = !(kSfRingSafe && args.num_kb % grp == 0);
     volatile int* abort = &abort_flag;
 
     if (threadIdx.x == 0) {
@@ -148,14 +122,11 @@ __global__ void __launch_bounds__(gmx2::threads_for(kTmaSf), 1)
             mbar_init(smem_u32(&bar_full[s]), 1);
             mbar_init(smem_u32(&bar_empty[s]), 1);
         }
-        for (int b = 0; b < kAccBufs; ++b) {
+        for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&bar_tfull[b]), 1);
             mbar_init(smem_u32(&bar_tempty[b]), 8);  // 4 epilogue warps in each CTA
         }
-        for (int b = 0; b < kSfSets; ++b) {
-            mbar_init(smem_u32(&bar_sfull[b]), 8);  // 4 scale warps in each CTA
-            mbar_init(smem_u32(&bar_sempty[b]), 1);
-        }
+        for (int b = 0; b < kSfSets; ++b) mbar_init(smem_u32(&bar_sempty[b]), 1);
         mbar_init(smem_u32(&bar_drain), 1);
         abort_flag = 0;
         fence_barrier_init();
@@ -196,43 +167,28 @@ __global__ void __launch_bounds__(gmx2::threads_for(kTmaSf), 1)
                     if (args.fault == 1 && it == 0) continue;  // test hook: stage never filled
                     const uint32_t full_local = smem_u32(&bar_full[s]);
                     const uint32_t full_leader = map_to_cta(full_local, 0);
-                    int sets_here = 0;  // scale sets that start in this stage
-                    if constexpr (kTmaSf) {
-#pragma unroll
-                        for (int h = 0; h < kBlocks; ++h) {
-                            const int kb = st * kBlocks + h;
-                            if (kb < args.num_kb && kb % grp == 0) ++sets_here;
-                        }
-                    }
+                    const int kb0 = st * kBlocks;
+                    const bool set_start = kb0 % grp == 0;  // a scale set starts in this stage
                     if (leader)  // both CTAs' bytes
                         mbar_arrive_expect_tx(full_local,
-                                              args.stage_tx + sets_here * 2 * gmx::kSfSetBytes);
-                    if constexpr (kDeep) {  // one 3-D box of two 128-byte K-chunks per operand
-                        tma_load_3d_pair(sA + s * kAStg, &tmA, full_leader, 0, a_row, st * 2);
-                        tma_load_3d_pair(sB + s * kBStage, &tmB, full_leader, 0, b_row, st * 2);
-                    } else {
-                        tma_load_2d_pair(sA + s * kAStg, &tmA, full_leader, st * kBK, a_row);
-                        tma_load_2d_pair(sB + s * kBStage, &tmB, full_leader, st * kBK, b_row);
-                    }
-                    if constexpr (kTmaSf) {
-#pragma unroll
-                        for (int h = 0; h < kBlocks; ++h) {
-                            const int kb = st * kBlocks + h;
-                            if (kb >= args.num_kb || kb % grp != 0) continue;
-                            // this CTA's A chunk (its 128-row group) and the tile's two B chunks,
-                            // as rows of 128 bytes of the repacked arrays; the kernel that writes
-                            // them may still be running (it launched this one early)
-                            if (!chunks_ready) {
-                                grid_dependency_wait();
-                                chunks_ready = true;
-                            }
-                            const int g = kb / grp;
-                            const uint32_t slot = sSF + s * C_::kSlotBytes + h * gmx::kSfSetBytes;
-                            tma_load_2d_pair(slot, &tmSA, full_leader, 0,
-                                             ((mt * 2 + (int)rank) * args.sf_sets + g) * 4);
-                            tma_load_2d_pair(slot + kSfChunkBytes, &tmSB, full_leader, 0,
-                                             (nt * args.sf_sets + g) * 8);
+                                              args.stage_tx + (set_start ? 2 * gmx::kSfSetBytes : 0));
+                    // one 3-D box of two 128-byte K-chunks per operand
+                    tma_load_3d_pair(sA + s * kAStg, &tmA, full_leader, 0, a_row, st * 2);
+                    tma_load_3d_pair(sB + s * kBStage, &tmB, full_leader, 0, b_row, st * 2);
+                    if (set_start) {
+                        // this CTA's A chunk (its 128-row group) and the tile's two B chunks, as
+                        // rows of 128 bytes of the repacked arrays; the kernel that writes them
+                        // may still be running (it launched this one early)
+                        if (!chunks_ready) {
+                            grid_dependency_wait();
+                            chunks_ready = true;
                         }
+                        const int g = kb0 / grp;
+                        const uint32_t slot = sSF + s * kSlotBytes;
+                        tma_load_2d_pair(slot, &tmSA, full_leader, 0,
+                                         ((mt * 2 + (int)rank) * args.sf_sets + g) * 4);
+                        tma_load_2d_pair(slot + kSfChunkBytes, &tmSB, full_leader, 0,
+                                         (nt * args.sf_sets + g) * 8);
                     }
                 }
             }
@@ -263,7 +219,7 @@ __global__ void __launch_bounds__(gmx2::threads_for(kTmaSf), 1)
             uint32_t s = 0, ph = 0, acc = 0, sit = 0;
             bool ok = true, issued = false;
             for (int t = pair; t < total && ok; t += num_pairs) {
-                const uint32_t b = acc % kAccBufs, aph = (acc / kAccBufs) & 1u;
+                const uint32_t b = acc & 1u, aph = (acc >> 1) & 1u;
                 if (!wait_bounded<true>(smem_u32(&bar_tempty[b]), aph ^ 1u, abort, args.timeout_ns,
                                         args.status, 42)) {
                     ok = false;
@@ -283,45 +239,36 @@ __global__ void __launch_bounds__(gmx2::threads_for(kTmaSf), 1)
                         const int kb = st * kBlocks + h;
                         if (kb >= args.num_kb) break;  // a K-block past K: zero-filled, skipped
                         const uint32_t set = sit % kSfSets;
-                        if (kb % grp == 0) {  // the first K-block of a scale set
-                            if constexpr (kTmaSf) {
-                                // the set's columns are free once the MMAs that last read them
-                                // are done; then both CTAs copy the set from the stage's slot
-                                if (sf_wait) {
-                                    if (!wait_bounded(smem_u32(&bar_sempty[set]),
-                                                      ((sit / kSfSets) & 1u) ^ 1u, abort,
-                                                      args.timeout_ns, args.status, 47)) {
-                                        ok = false;
-                                        break;
-                                    }
-                                    tc_fence_after_sync();
-                                }
-                                const uint32_t slot = sSF + s * C_::kSlotBytes + h * gmx::kSfSetBytes;
-                                const uint32_t col = tmem_base + kSfBase + set * kSfSet;
-                                tmem_cp_32x128b_x4_cta2(col, smem_desc_plain(slot, 128, 128));
-                                tmem_cp_32x128b_x4_cta2(
-                                    col + 4, smem_desc_plain(slot + kSfChunkBytes, 128, 128));
-                                tmem_cp_32x128b_x4_cta2(
-                                    col + 8, smem_desc_plain(slot + 2 * kSfChunkBytes, 128, 128));
-                            } else {
-                                if (!wait_bounded<true>(smem_u32(&bar_sfull[set]),
-                                                        (sit / kSfSets) & 1u, abort,
-                                                        args.timeout_ns, args.status, 45)) {
+                        if (kb % grp == 0) {
+                            // the first K-block of a scale set: its columns are free once the
+                            // MMAs that last read them are done; then both CTAs copy the set
+                            // from the stage's slot
+                            if (sf_wait) {
+                                if (!wait_bounded(smem_u32(&bar_sempty[set]),
+                                                  ((sit / kSfSets) & 1u) ^ 1u, abort,
+                                                  args.timeout_ns, args.status, 47)) {
                                     ok = false;
                                     break;
                                 }
                                 tc_fence_after_sync();
                             }
+                            const uint32_t slot = sSF + s * kSlotBytes;
+                            const uint32_t col = tmem_base + kSfBase + set * kSfSet;
+                            tmem_cp_32x128b_x4_cta2(col, smem_desc_plain(slot, 128, 128));
+                            tmem_cp_32x128b_x4_cta2(
+                                col + 4, smem_desc_plain(slot + kSfChunkBytes, 128, 128));
+                            tmem_cp_32x128b_x4_cta2(
+                                col + 8, smem_desc_plain(slot + 2 * kSfChunkBytes, 128, 128));
                         }
                         // K-block h of the stage: 128-byte chunk h of each operand's box
                         const uint32_t a_lo = (uint32_t)a_desc0 + s * (uint32_t)(kAStg >> 4) +
-                                              (uint32_t)h * (uint32_t)(C_::kAChunk >> 4);
+                                              (uint32_t)h * (uint32_t)(kAChunk >> 4);
                         const uint32_t b_lo = (uint32_t)b_desc0 + s * (uint32_t)(kBStage >> 4) +
-                                              (uint32_t)h * (uint32_t)(C_::kBChunk >> 4);
+                                              (uint32_t)h * (uint32_t)(kBChunk >> 4);
                         const uint32_t sfa = tmem_base + kSfBase + set * kSfSet;
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
-                            const uint32_t sf_id = kB32 ? (uint32_t)kk : (uint32_t)(kb & 3);
+                            const uint32_t sf_id = (uint32_t)(kb & 3);
                             const uint32_t idesc = idesc0 | (sf_id << 4) | (sf_id << 29);
                             const uint64_t adesc = ((uint64_t)a_hi << 32) | (a_lo + 2u * kk);
                             const uint64_t bdesc = ((uint64_t)b_hi << 32) | (b_lo + 2u * kk);
@@ -330,7 +277,7 @@ __global__ void __launch_bounds__(gmx2::threads_for(kTmaSf), 1)
                         }
                         issued = true;
                         if (kb % grp == grp - 1 || kb == args.num_kb - 1) {
-                            if (!kTmaSf || sf_wait)  // set consumed
+                            if (sf_wait)  // set consumed
                                 mma_commit_cta2_both(smem_u32(&bar_sempty[set]));
                             ++sit;
                         }
@@ -351,7 +298,7 @@ __global__ void __launch_bounds__(gmx2::threads_for(kTmaSf), 1)
                 wait_drain(smem_u32(&bar_drain), 0, kDrainNs);
             }
         }
-    } else if (warp < 6) {
+    } else {
         // ------------------------------ epilogue (warps 2..5, both CTAs) ---------------------
         const int q = warp & 3;
         const uint32_t my_slots = base + kNS * kStageBytes + (uint32_t)q * 8192u;
@@ -359,7 +306,7 @@ __global__ void __launch_bounds__(gmx2::threads_for(kTmaSf), 1)
         for (int t = pair; t < total; t += num_pairs, ++acc) {
             int mt, nt;
             tile_coords(t, args.num_m, args.num_n, kGroupM, mt, nt);
-            const uint32_t b = acc % kAccBufs, aph = (acc / kAccBufs) & 1u;
+            const uint32_t b = acc & 1u, aph = (acc >> 1) & 1u;
             int ok = 1;
             if (lane == 0)
                 ok = wait_bounded<false, true>(smem_u32(&bar_tfull[b]), aph, abort,
@@ -379,59 +326,6 @@ __global__ void __launch_bounds__(gmx2::threads_for(kTmaSf), 1)
         }
         if (lane == 0) bulk_wait_group_read<0>();  // the C stores have read their slots
         __syncwarp();
-    } else if constexpr (!kTmaSf) {
-        // ------------------------------ scale writers (warps 6..9, both CTAs) ----------------
-        // The (tile, group) sequence of this pair, flattened so the gather of the next group
-        // (possibly of the next tile) is in flight while the current one waits for a free set.
-        const int q = warp & 3;
-        const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-        const int my_tiles = pair < total ? (total - 1 - pair) / num_pairs + 1 : 0;
-        const int steps = my_tiles * groups;
-        const uint32_t sfull_leader0 = map_to_cta(smem_u32(&bar_sfull[0]), 0);
-        uint32_t wa[4], wb[8];
-        auto gather = [&](int step, uint32_t (&ga)[4], uint32_t (&gb)[8]) {
-            const int t = pair + (step / groups) * num_pairs;
-            const int g = step % groups;
-            int mt, nt;
-            tile_coords(t, args.num_m, args.num_n, kGroupM, mt, nt);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                ga[j] = sf_word(args.sfA, args.M, args.sf_cols,
-                                mt * 256 + (int)rank * kBMc + lane + 32 * j, g);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                gb[j] = j < kBN / 32
-                            ? sf_word(args.sfB, args.N, args.sf_cols, nt * kBN + lane + 32 * j, g)
-                            : 0u;
-        };
-        if (steps > 0) gather(0, wa, wb);
-        for (int step = 0; step < steps; ++step) {
-            uint32_t na[4], nb[8];
-            if (step + 1 < steps) gather(step + 1, na, nb);
-            const uint32_t sit = (uint32_t)step;
-            const uint32_t set = sit % kSfSets;
-            int w_ok = 1;
-            if (lane == 0)
-                w_ok = wait_bounded<false, true>(smem_u32(&bar_sempty[set]),
-                                                 ((sit / kSfSets) & 1u) ^ 1u, abort,
-                                                 args.timeout_ns, args.status, 46);
-            w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-            if (!w_ok) break;
-            tc_fence_after_sync();
-            const uint32_t col = tmem_base + kSfBase + set * kSfSet;
-            tmem_store_4cols(col + lane_addr, wa[0], wa[1], wa[2], wa[3]);
-            tmem_store_8cols(col + 4 + lane_addr, wb);
-            tmem_store_wait();
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(sfull_leader0 + set * 8);
-            if (step + 1 < steps) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) wa[j] = na[j];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) wb[j] = nb[j];
-            }
-        }
     }
 
     // ------------------------------ teardown ------------------------------

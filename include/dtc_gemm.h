@@ -69,8 +69,9 @@ typedef enum {
     GEMM_VARIANT_1CTA = 1,   /* persistent 128 x 256 or 128 x 224 tiles, one CTA per tile */
     GEMM_VARIANT_2CTA = 2,   /* persistent 256 x 256 or 256 x 224 tiles on a CTA pair
                                 (cluster 2x1, tcgen05 cta_group::2); for the block-scaled
-                                product (256 x 224, or 256 x 256 with tile_n = 256) an option
-                                that is never chosen automatically */
+                                product 256 x 224 tiles with 256-deep stages, for 128-element
+                                scale blocks, K % 128 == 0 and a workspace that receives the
+                                repacked scales (see gemm_workspace_size) */
     GEMM_VARIANT_SPLITK = 3  /* 128 x 128 tiles with K split over a cluster of 2 or 4 CTAs, or
                                 128 x 256 tiles split over 2; each CTA copies the partial sums
                                 of the rows another CTA owns into that CTA's shared memory, and
@@ -86,14 +87,12 @@ typedef struct {
                              stage, so the consumer's bounded wait runs out and the call reports
                              GEMM_ERR_TIMEOUT through gemm_stream_status. */
     int tile_n;           /* force the N-tile: 256, 224 (not SPLITK; one-CTA tiles need B stored
-                             [N,K]; block-scaled: 224, or 256 on CTA pairs), 128 (SPLITK and
-                             2CTA) or 64 (2CTA); 0 = choose. 2CTA tiles of 128 or 64 take 128-deep
-                             stages (K % 64 == 0) */
+                             [N,K]; block-scaled: 224 only), 128 (SPLITK and 2CTA) or 64 (2CTA);
+                             0 = choose. 2CTA tiles of 128 or 64 take 128-deep stages
+                             (K % 64 == 0) */
     int tile_k;           /* K-elements per pipeline stage: 64 (1CTA), 64 or 128 (2CTA; SPLITK
-                             with 128-wide tiles; 128 needs K % 64 == 0), 128 (the default) or 256
-                             (block-scaled one-CTA kernel; 256 needs K % 128 == 0), 128 or 256
-                             (block-scaled pair kernel; 256 needs K % 128 == 0 and the repacked
-                             scales); 0 = choose */
+                             with 128-wide tiles; 128 needs K % 64 == 0); block-scaled: 128 (the
+                             one-CTA kernel) or 256 (the pair kernel); 0 = choose */
     int64_t lda;          /* elements between consecutive stored rows of A, B, C; 0 = dense (the */
     int64_t ldb;          /* row length: K or M for A, K or N for B, N for C). At least the row */
     int64_t ldc;          /* length, and rows must start 16 bytes apart (ld x element size %
@@ -108,8 +107,8 @@ typedef struct {
                              and its rows start a multiple of 32 bytes apart. */
     int mx_scale_block;   /* block-scaled product only: K-elements per E8M0 scale, 128 (0 = the
                              default, the pages' granularity) or 32 (the OCP MX block); the
-                             scale arrays are then [rows, ceil(K / block)]. Non-default formats
-                             or blocks run on the one-CTA kernel. */
+                             scale arrays are then [rows, ceil(K / block)]. 32-element blocks run
+                             on the one-CTA kernel. */
     void* workspace;      /* device scratch owned by the caller, 16-byte aligned; NULL = none
                              (see gemm_workspace_size). 16-bit products: stream-K; its first 1 KB
                              holds flags that must be zero before the first call that uses it;
@@ -187,9 +186,10 @@ typedef struct {
     int tiles;    /* output tiles (times split_k work units for SPLITK) */
     int cluster;  /* CTAs per cluster */
     int sk_tiles; /* tiles shared out by stream-K (0 = none) */
-    int sf_packed; /* block-scaled one-CTA kernel: 1 = the scales are repacked into the workspace
-                      and copied into Tensor Memory by the MMA thread (see gemm_options.workspace);
-                      0 = gathered by the kernel's scale warps */
+    int sf_packed; /* block-scaled product: 1 = the scales are repacked into the workspace and
+                      copied into Tensor Memory by the MMA thread (the pair kernel always; the
+                      one-CTA kernel for 32-element blocks given a workspace; see
+                      gemm_options.workspace); 0 = gathered by the one-CTA kernel's scale warps */
 } gemm_plan_info;
 
 /* Fills *info with the launch that gemm_ex would make for these sizes and options on the current
@@ -307,9 +307,9 @@ int gemm_nvfp4_workspace_size(int64_t M, int64_t N, int64_t K, uint64_t* bytes);
  * pieces summed through the workspace); 0 when it would not (or stream_k == 2). For the
  * block-scaled product (dtype 2): the bytes of the repacked scale arrays (about the size of sfA
  * and sfB together) when the call would use them -- AUTO with 128-element blocks, K % 128 == 0
- * and at least a wave of 256 x 224 tiles (the pair kernel with 256-deep stages), 32-element
- * blocks (the one-CTA kernel), or the pair kernel forced with 224-wide tiles -- else 0. The
- * pages have no counterpart:
+ * and at least a wave of 256 x 224 tiles, or the pair kernel forced (the pair kernel with
+ * 256-deep stages), and 32-element blocks (the one-CTA kernel) -- else 0; UNSUPPORTED when the
+ * pair kernel is forced for a call it does not take. The pages have no counterpart:
  * their persistent 2-CTA variant (05 Blackwell TCGEN05 GEMM tutorial, "Advanced") takes whole
  * tiles. INVALID_ARG as gemm_ex; bytes must not be NULL.
  */

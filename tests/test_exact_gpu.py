@@ -22,7 +22,7 @@ import torch
 
 import oracle
 from dense_tensor_core_gb300 import workloads
-from parity import check_close, to_device8, to_device16, values16
+from parity import check_close, to_device8, to_device16, values16, with_packed_scales
 
 pytestmark = pytest.mark.gpu
 
@@ -174,9 +174,10 @@ def test_mxfp8_error_against_k(block, variant):
     rows = []
     for K in SWEEP_K:
         A, B, sfA, sfB = workloads.make_mx(M, N, K, seed=K + block, block=block)
+        kw = with_packed_scales(M, N, K, dict(scale_block=block if block != 128 else 0,
+                                              variant=variant, pack=variant == 2))
         C = dtc.gemm_ex("mxfp8", to_device8(A), to_device8(B), sfA=to_device8(sfA),
-                        sfB=to_device8(sfB), scale_block=block if block != 128 else 0,
-                        variant=variant)
+                        sfB=to_device8(sfB), **kw)
         dtc.gemm_stream_status()
         got = values16(C.view(torch.int16).cpu().numpy().view(np.uint16), "bf16")
         ref_codes, exact = oracle.gemm_mx(A, B, sfA, sfB, M, N, K, block=block, sums=True)

@@ -53,7 +53,6 @@ def check_mx(A, B, sfA, sfB, what, **kw):
     return check_close(values16(C, "bf16"), values16(ref, "bf16"), what)
 
 
-@pytest.mark.parametrize("tile_k", [128, 256])
 @pytest.mark.parametrize("M,N,K", [
     (128, 224, 128),    # one tile, one K-block, one scale group
     (256, 448, 1024),   # 4 tiles, 8 K-blocks = 2 scale groups
@@ -63,15 +62,13 @@ def check_mx(A, B, sfA, sfB, what, **kw):
     (129, 232, 656),    # a row / 8 columns past a tile; 6 K-blocks (one partial group)
     (640, 896, 2048),   # 20 tiles, 16 K-blocks
 ])
-def test_small_shapes_full_parity(M, N, K, tile_k):
-    # 128-deep stages (2-D boxes, any K) or 256-deep ones (3-D boxes of two K-blocks, K % 128 == 0)
-    if tile_k == 256 and K % 128:
-        pytest.skip("256-deep stages need K % 128 == 0")
+def test_small_shapes_full_parity(M, N, K):
+    # the one-CTA kernel: 128-deep stages (2-D boxes, any K with 16-byte rows)
     import dense_tensor_core_gb300 as dtc
 
-    assert dtc.gemm_plan("mxfp8", M, N, K, variant=1, tile_k=tile_k)["tile_k"] == tile_k
+    assert dtc.gemm_plan("mxfp8", M, N, K, variant=1)["tile_k"] == 128
     A, B, sfA, sfB = workloads.make_mxfp8(M, N, K, seed=M + N + K)
-    check_mx(A, B, sfA, sfB, f"mxfp8 {M}x{N}x{K} tile_k {tile_k}", variant=1, tile_k=tile_k)
+    check_mx(A, B, sfA, sfB, f"mxfp8 {M}x{N}x{K}", variant=1)
 
 
 @pytest.mark.parametrize("M,N,K", [
@@ -83,11 +80,10 @@ def test_small_shapes_full_parity(M, N, K, tile_k):
     (1280, 2240, 640),  # 50 pair tiles, 640 = 2.5 stages of 256 (half-padded last stage)
 ])
 def test_pair_kernel_full_parity(M, N, K):
-    import dense_tensor_core_gb300 as dtc
-
-    assert dtc.gemm_plan("mxfp8", M, N, K, variant=2)["tile_m"] == 256
+    # the pair kernel: 256-deep stages, the scales repacked into a workspace (the helper checks
+    # through the plan that the call takes them)
     A, B, sfA, sfB = workloads.make_mxfp8(M, N, K, seed=M + N + K + 1)
-    check_mx(A, B, sfA, sfB, f"mxfp8 pair {M}x{N}x{K}", variant=2)
+    check_mx(A, B, sfA, sfB, f"mxfp8 pair {M}x{N}x{K}", variant=2, pack=True)
 
 
 def test_unit_scales_reduce_to_plain_e4m3():
@@ -96,8 +92,7 @@ def test_unit_scales_reduce_to_plain_e4m3():
     check_mx(A, B, np.full_like(sfA, 127), np.full_like(sfB, 127), "unit scales")
 
 
-@pytest.mark.parametrize("variant,tile_k,pack", [(1, 128, False), (1, 256, False), (2, 0, False),
-                                                (2, 0, True), (2, 256, True)])
+@pytest.mark.parametrize("variant,tile_k,pack", [(1, 128, False), (2, 0, True), (2, 256, True)])
 @pytest.mark.parametrize("which", ["a_rows", "b_rows", "k_blocks"])
 def test_scales_varying_along_one_axis(which, variant, tile_k, pack):
     # Scales that vary along a single axis: a wrong row / column / K-block mapping of the scale
@@ -126,8 +121,7 @@ def test_wide_scale_range():
     check_mx(A, B, sfA, sfB, "wide scale range")
 
 
-@pytest.mark.parametrize("variant,pack,tile_k", [(1, False, 0), (2, False, 0), (2, True, 0),
-                                                (2, True, 256)])
+@pytest.mark.parametrize("variant,pack,tile_k", [(1, False, 0), (2, True, 0), (2, True, 256)])
 def test_more_tiles_than_sms(variant, pack, tile_k):
     # 200 one-CTA tiles of 128 x 224 over 152 SMs, or 100 pair tiles over 76 pairs: persistent
     # loop, both accumulators, scale sets reused across tiles
@@ -136,8 +130,8 @@ def test_more_tiles_than_sms(variant, pack, tile_k):
     check_mx(A, B, sfA, sfB, "more tiles than SMs", variant=variant, pack=pack, tile_k=tile_k)
 
 
-@pytest.mark.parametrize("variant,tile_k,pack", [(0, 0, False), (1, 128, False), (1, 256, False),
-                                                (2, 0, False), (2, 0, True), (2, 256, True)])
+@pytest.mark.parametrize("variant,tile_k,pack", [(0, 0, False), (0, 0, True), (1, 128, False),
+                                                (2, 256, True)])
 def test_benchmark_size_sampled(variant, tile_k, pack):
     w = workloads.WORKLOADS["mxfp8_nt_4096x4096x8192"]
     A, B, sfA, sfB = _bench_inputs()
@@ -162,8 +156,7 @@ def test_k_zero_and_empty():
     assert torch.equal(C, torch.zeros_like(C))
 
 
-@pytest.mark.parametrize("variant,pack,block", [(1, False, 128), (2, False, 128), (1, True, 32),
-                                               (2, True, 128)])
+@pytest.mark.parametrize("variant,pack,block", [(1, False, 128), (1, True, 32), (2, True, 128)])
 def test_timeout_reports_and_recovers(variant, pack, block):
     import dense_tensor_core_gb300 as dtc
 
@@ -186,22 +179,30 @@ def test_automatic_choice():
 
     if torch.cuda.get_device_properties(0).multi_processor_count != 152:
         pytest.skip("the expected choices are worked out for 152 SMs")
-    # the pair kernel is an option (variant 2); the one-CTA kernel measured faster, with 128-deep
-    # stages (256-deep ones on request, K % 128 == 0)
+    # without a workspace: the one-CTA kernel, 128-deep stages, scales through its scale warps
     p = dtc.gemm_plan("mxfp8", 4096, 4096, 8192)
     assert (p["variant"], p["tile_k"], p["sf_packed"]) == (1, 128, 0)
-    assert dtc.gemm_plan("mxfp8", 4096, 4096, 8192, tile_k=256)["tile_k"] == 256
-    assert dtc.gemm_plan("mxfp8", 4096, 4096, 8208)["tile_k"] == 128
-    # a workspace: repacked scales for 32-element blocks (one-CTA) and on 224-wide pair tiles
-    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
-    assert dtc.gemm_plan("mxfp8", 1024, 1024, 1024, workspace=ws)["sf_packed"] == 0
-    assert dtc.gemm_plan("mxfp8", 1024, 1024, 1024, workspace=ws, scale_block=32)["sf_packed"] == 1
+    # with one: the pair kernel (256-deep stages, repacked scales) where it fills a wave and
+    # K % 128 == 0; repacked scales on the one-CTA kernel for 32-element blocks
+    ws = torch.empty(64 << 20, dtype=torch.uint8, device="cuda")
+    p = dtc.gemm_plan("mxfp8", 4096, 4096, 8192, workspace=ws)
+    assert (p["variant"], p["tile_k"], p["stages"], p["sf_packed"]) == (2, 256, 3, 1)
+    assert dtc.gemm_plan("mxfp8", 4096, 4096, 8208, workspace=ws)["variant"] == 1
+    assert dtc.gemm_plan("mxfp8", 4096, 4096, 8192, workspace=ws, tile_k=128)["variant"] == 1
+    p = dtc.gemm_plan("mxfp8", 4096, 4096, 8192, workspace=ws, scale_block=32)
+    assert (p["variant"], p["sf_packed"]) == (1, 1)
+    p = dtc.gemm_plan("mxfp8", 1024, 1024, 1024, workspace=ws)  # 20 pair tiles: under a wave
+    assert (p["variant"], p["sf_packed"]) == (1, 0)
     assert dtc.gemm_plan("mxfp8", 1024, 1024, 1024, workspace=ws, variant=2)["sf_packed"] == 1
-    assert dtc.gemm_plan("mxfp8", 1024, 1024, 1024, workspace=ws, variant=2, tile_n=256)["sf_packed"] == 0
-    assert dtc.gemm_plan("mxfp8", 4096, 4096, 8192, variant=2)["variant"] == 2
-    # the pair kernel's 128-deep stages are 2-D boxes: any K with 16-byte rows
-    p = dtc.gemm_plan("mxfp8", 4096, 4096, 8208, variant=2)
-    assert (p["variant"], p["tile_k"], p["stages"]) == (2, 128, 6)
+    # what the pair kernel does not take
+    for kw in (dict(variant=2), dict(variant=2, workspace=ws, scale_block=32),
+               dict(variant=2, workspace=ws, tile_k=128), dict(variant=2, workspace=ws, tile_n=256),
+               dict(variant=1, tile_k=256)):
+        with pytest.raises(dtc.GemmError) as e:
+            dtc.gemm_plan("mxfp8", 4096, 4096, 8192, **kw)
+        assert e.value.status == 2, kw
+    with pytest.raises(dtc.GemmError):
+        dtc.gemm_plan("mxfp8", 4096, 4096, 8208, variant=2, workspace=ws)
 
 
 # --- other block-scaled formats: e5m2 elements, 32-element (OCP MX) scale blocks ---------------
@@ -210,17 +211,15 @@ def run_mx_fmt(A, B, sfA, sfB, a_fmt, b_fmt, block, **kw):
     return run_mx(A, B, sfA, sfB, a_format=a_fmt, b_format=b_fmt, scale_block=block, **kw)
 
 
-@pytest.mark.parametrize("variant,tile_k,pack", [(1, 128, False), (1, 256, False), (2, 0, False),
-                                                (1, 128, True), (1, 256, True), (2, 0, True),
-                                                (2, 256, True)])
+@pytest.mark.parametrize("variant,tile_k,pack", [(1, 128, False), (1, 128, True), (2, 0, True)])
 @pytest.mark.parametrize("block", [32, 128])
 @pytest.mark.parametrize("a_fmt,b_fmt", [("e5m2", "e5m2"), ("e4m3", "e5m2"), ("e5m2", "e4m3"),
                                          ("e4m3", "e4m3")])
 @pytest.mark.parametrize("M,N,K", [(256, 448, 1024), (300, 520, 400), (129, 232, 656),
                                    (256, 224, 384)])
 def test_formats_and_blocks_full_parity(M, N, K, a_fmt, b_fmt, block, variant, tile_k, pack):
-    if tile_k == 256 and K % 128:
-        pytest.skip("256-deep stages need K % 128 == 0")
+    if variant == 2 and (block != 128 or K % 128):
+        pytest.skip("the pair kernel takes 128-element blocks and K % 128 == 0")
     if pack and variant == 1 and block == 128:
         pytest.skip("the one-CTA kernel repacks the scales of 32-element blocks only")
     A, B, sfA, sfB = workloads.make_mx(M, N, K, M + N + K + block, a_fmt, b_fmt, block)
@@ -231,9 +230,8 @@ def test_formats_and_blocks_full_parity(M, N, K, a_fmt, b_fmt, block, variant, t
 
 
 @pytest.mark.parametrize("pack", [False, True])
-@pytest.mark.parametrize("tile_k", [128, 256])
 @pytest.mark.parametrize("which", ["a_rows", "b_rows", "k_blocks"])
-def test_block32_scales_varying_along_one_axis(which, tile_k, pack):
+def test_block32_scales_varying_along_one_axis(which, pack):
     # with 32-element blocks each MMA of a K-block takes its own scale byte: scales that vary along
     # K by 32-block pin that byte selection
     M, N, K = 256, 448, 1024
@@ -248,7 +246,7 @@ def test_block32_scales_varying_along_one_axis(which, tile_k, pack):
     else:
         sfA[:] = (123 + (np.arange(kb) % 7))[None, :]
         sfB[:] = (130 - (np.arange(kb) % 5))[None, :]
-    C = run_mx_fmt(A, B, sfA, sfB, "e4m3", "e4m3", 32, variant=1, tile_k=tile_k, pack=pack)
+    C = run_mx_fmt(A, B, sfA, sfB, "e4m3", "e4m3", 32, variant=1, pack=pack)
     ref = oracle.gemm_mx(A, B, sfA, sfB, M, N, K, block=32)
     check_close(values16(C, "bf16"), values16(ref, "bf16"), f"block-32 scales along {which}")
 
@@ -272,8 +270,9 @@ def test_format_options_plan():
 
     p = dtc.gemm_plan("mxfp8", 4096, 4096, 8192, scale_block=32, a_format="e5m2")
     assert (p["variant"], p["tile_k"]) == (1, 128)
-    p = dtc.gemm_plan("mxfp8", 4096, 4096, 8192, variant=2, scale_block=32, b_format="e2m1")
-    assert (p["variant"], p["tile_m"], p["tile_n"]) == (2, 256, 224)
+    ws = torch.empty(64 << 20, dtype=torch.uint8, device="cuda")
+    p = dtc.gemm_plan("mxfp8", 4096, 4096, 8192, variant=2, b_format="e2m1", workspace=ws)
+    assert (p["variant"], p["tile_m"], p["tile_n"], p["tile_k"]) == (2, 256, 224, 256)
 
 
 @pytest.mark.parametrize("variant", [1, 2])
@@ -289,8 +288,9 @@ def test_rows_of_larger_arrays(variant):
     Ab[:, :K] = to_device8(A)
     Bb[:, :K] = to_device8(B)
     Cb = torch.full((M, N + 24), float("nan"), dtype=torch.bfloat16, device="cuda")
+    kw = with_packed_scales(M, N, K, dict(variant=variant, pack=variant == 2))
     dtc.gemm_ex("mxfp8", Ab[:, :K], Bb[:, :K], Cb[:, :N], sfA=to_device8(sfA), sfB=to_device8(sfB),
-                variant=variant)
+                **kw)
     dtc.gemm_stream_status()
     assert torch.isnan(Cb[:, N:].float()).all(), "padding columns of C were written"
     C = Cb[:, :N].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
@@ -298,7 +298,7 @@ def test_rows_of_larger_arrays(variant):
     check_close(values16(C, "bf16"), values16(ref, "bf16"), f"strided mxfp8 variant {variant}")
 
 
-@pytest.mark.parametrize("variant,tile_k", [(1, 128), (1, 256), (2, 0)])
+@pytest.mark.parametrize("variant,tile_k", [(1, 128), (2, 0)])
 def test_writes_exactly_C(variant, tile_k):
     # C inside a NaN-filled buffer: every element overwritten, nothing around it touched (224-wide
     # tiles end in a 32-column chunk; 520 columns and 300 rows leave partial chunks and bands)
@@ -309,8 +309,9 @@ def test_writes_exactly_C(variant, tile_k):
     guard = 4096
     buf = torch.full((guard * 2 + M * N,), float("nan"), dtype=torch.bfloat16, device="cuda")
     C = buf[guard:guard + M * N].view(M, N)
+    kw = with_packed_scales(M, N, K, dict(variant=variant, tile_k=tile_k, pack=variant == 2))
     dtc.gemm_ex("mxfp8", to_device8(A), to_device8(B), C, sfA=to_device8(sfA), sfB=to_device8(sfB),
-                variant=variant, tile_k=tile_k)
+                **kw)
     dtc.gemm_stream_status()
     h = buf.float().cpu()
     assert torch.isnan(h[:guard]).all() and torch.isnan(h[guard + M * N:]).all()

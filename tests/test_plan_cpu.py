@@ -51,8 +51,8 @@ def test_automatic_choice_on_gb300():
 def test_block_scaled_repacking_policy():
     # with a workspace the scales are repacked: 128-element blocks go to the pair kernel with
     # 256-deep stages (when K % 128 == 0 and the pair tiles fill a wave), 32-element blocks to the
-    # one-CTA kernel; every block on 224-wide pair tiles when the pair is forced; a workspace too
-    # small leaves the scale warps in charge
+    # one-CTA kernel; the pair kernel takes nothing else; a workspace too small leaves the scale
+    # warps in charge
     ws = fake_workspace()
     p = plan("mxfp8", 4096, 4096, 8192, workspace=ws)
     assert (p["variant"], p["tile_m"], p["tile_n"], p["tile_k"], p["stages"], p["sf_packed"]) == (2, 256, 224, 256, 3, 1)
@@ -60,13 +60,18 @@ def test_block_scaled_repacking_policy():
     assert plan("mxfp8", 4096, 4096, 8200, workspace=ws)["variant"] == 1  # K % 128 != 0
     assert plan("mxfp8", 1024, 1024, 1024, workspace=ws)["variant"] == 1  # 20 pair tiles < 76
     assert plan("mxfp8", 4096, 4096, 8192, workspace=ws, tile_k=128)["variant"] == 1
-    with pytest.raises(dtc.GemmError):  # 256-deep pair stages need the repacked scales
-        plan("mxfp8", 4096, 4096, 8192, variant=2, tile_k=256)
+    for kw in (dict(variant=2), dict(variant=2, tile_k=256),  # no workspace for the scales
+               dict(variant=2, workspace=ws, scale_block=32), dict(variant=2, workspace=ws, tile_k=128),
+               dict(variant=2, workspace=ws, tile_n=256), dict(variant=1, tile_k=256)):
+        with pytest.raises(dtc.GemmError) as e:
+            plan("mxfp8", 4096, 4096, 8192, **kw)
+        assert e.value.status == 2, kw
+    with pytest.raises(dtc.GemmError):  # K % 128 != 0
+        plan("mxfp8", 4096, 4096, 8200, variant=2, workspace=ws)
     assert plan("mxfp8", 4096, 4096, 8192, workspace=ws, scale_block=32)["variant"] == 1
     assert plan("mxfp8", 4096, 4096, 8192, workspace=ws, scale_block=32)["sf_packed"] == 1
     assert plan("mxfp8", 4096, 4096, 8192, workspace=ws, scale_block=32, b_format="e2m1")["sf_packed"] == 1
-    assert plan("mxfp8", 4096, 4096, 8192, workspace=ws, variant=2)["sf_packed"] == 1
-    assert plan("mxfp8", 4096, 4096, 8192, workspace=ws, variant=2, tile_n=256)["sf_packed"] == 0
+    assert plan("mxfp8", 1024, 1024, 1024, workspace=ws, variant=2)["sf_packed"] == 1
     small = fake_workspace(1024)
     assert plan("mxfp8", 4096, 4096, 8192, workspace=small, scale_block=32)["sf_packed"] == 0
     # the chunk layout: 32 groups of 128 A rows and 19 tiles of 224 B rows, 64 sets (K / 128) of

@@ -47,31 +47,32 @@ def test_static_workspace_matches_caller_workspace_two_calls(M, N, K, layout, st
         assert torch.equal(C_ref.view(torch.int16), C_own.view(torch.int16)), f"call {call}"
 
 
-@pytest.mark.parametrize("variant", [1, 2])
-def test_static_workspace_holds_repacked_scales(variant):
-    # 32-element scale blocks on the one-CTA kernel, and the pair kernel: the scales are repacked
-    # into the library's region instead of a caller's workspace; bit for bit equal, two calls
+@pytest.mark.parametrize("variant,block", [(1, 32), (2, 128)])
+def test_static_workspace_holds_repacked_scales(variant, block):
+    # 32-element scale blocks on the one-CTA kernel, and the pair kernel with 128-element ones:
+    # the scales are repacked into the library's region instead of a caller's workspace; bit for
+    # bit equal, two calls
     import numpy as np
 
     import dense_tensor_core_gb300 as dtc
     from parity import to_device8
 
     M, N, K = 640, 904, 1024
-    A, B, sfA, sfB = workloads.make_mx(M, N, K, 12, block=32)
+    A, B, sfA, sfB = workloads.make_mx(M, N, K, 12, block=block)
     At, Bt, sAt, sBt = (to_device8(x) for x in (A, B, sfA, sfB))
-    nbytes = dtc.gemm_workspace_size("mxfp8", M, N, K, variant=variant, scale_block=32)
+    nbytes = dtc.gemm_workspace_size("mxfp8", M, N, K, variant=variant, scale_block=block)
     assert nbytes > 0
     ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
-    assert dtc.gemm_plan("mxfp8", M, N, K, variant=variant, scale_block=32, workspace=ws)["sf_packed"] == 1
+    assert dtc.gemm_plan("mxfp8", M, N, K, variant=variant, scale_block=block, workspace=ws)["sf_packed"] == 1
     C_ref = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     C_own = torch.empty_like(C_ref)
     for call in range(2):
         C_ref.fill_(float("nan"))
         C_own.fill_(float("nan"))
-        dtc.gemm_ex("mxfp8", At, Bt, C_ref, sfA=sAt, sfB=sBt, scale_block=32, variant=variant,
+        dtc.gemm_ex("mxfp8", At, Bt, C_ref, sfA=sAt, sfB=sBt, scale_block=block, variant=variant,
                     workspace=ws)
         before = torch.cuda.memory_allocated()
-        dtc.gemm_ex_static_workspace("mxfp8", At, Bt, C_own, sfA=sAt, sfB=sBt, scale_block=32,
+        dtc.gemm_ex_static_workspace("mxfp8", At, Bt, C_own, sfA=sAt, sfB=sBt, scale_block=block,
                                      variant=variant)
         assert torch.cuda.memory_allocated() == before
         dtc.gemm_stream_status()
