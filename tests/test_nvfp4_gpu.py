@@ -149,3 +149,19 @@ def test_argument_errors():
     with pytest.raises(dtc.GemmError) as e:  # too small a workspace
         run(A, B, sfA, sfB, workspace=torch.empty(64 * 128, dtype=torch.uint8, device="cuda"))
     assert e.value.status == 1
+
+
+def test_c_rows_of_a_larger_array():
+    # C as a view into a wider row-major array: ldc goes to the bf16 product; the padding columns
+    # stay untouched
+    import dense_tensor_core_gb300 as dtc
+
+    M, N, K = 200, 264, 320
+    A, B, sfA, sfB = workloads.make_nvfp4(M, N, K, seed=9)
+    Cb = torch.full((M, N + 40), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dtc.gemm_nvfp4(to_device8(A), to_device8(B), to_device8(sfA), to_device8(sfB), C=Cb[:, :N])
+    dtc.gemm_stream_status()
+    assert torch.isnan(Cb[:, N:].float()).all(), "padding columns of C were written"
+    C = Cb[:, :N].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    check_close(values16(C, "bf16"), values16(ref(A, B, sfA, sfB, M, N, K), "bf16"),
+                "nvfp4 into rows of a larger C")
