@@ -577,8 +577,9 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
     const int64_t tiles256 = (int64_t)ceil_div(M, 128) * ceil_div(N, 256);
     const int64_t tiles128 = (int64_t)ceil_div(M, 128) * ceil_div(N, 128);
     int split = o ? o->split_k : 0;
-    if (split != 0 && split != 2 && split != 4)
-        return fail(GEMM_ERR_INVALID_ARG, "split_k %d is not 2 or 4", split);
+    if (split != 0 && split != 1 && split != 2 && split != 4)
+        return fail(GEMM_ERR_INVALID_ARG, "split_k %d is not 1, 2 or 4", split);
+    if (split == 1 && v == GEMM_VARIANT_AUTO) v = GEMM_VARIANT_SPLITK;
     int split_n = want_n;
     int auto_n = 0;
     if (v == GEMM_VARIANT_AUTO && split == 0 && want_n != 224 && tiles256 * 2 <= sms) {
@@ -609,6 +610,15 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
                 split_n = c.bn;
             }
         }
+        // A short K (at most 8 K-blocks of 64): one CTA per 128 x 64 tile with the whole K, no
+        // exchange, where that gives at least as many CTAs as the split (256 x 256 x 512: 9.2 us
+        // against 10.3 split in 2; 1024^3 level at 12.2; the skinny 128 x 8192 x 8192, K = 8192,
+        // 37.0 against 31.4, so not there)
+        const int64_t tiles64 = (int64_t)ceil_div(M, 128) * ceil_div(N, 64);
+        if (split && !want_n && K <= 512 && K % 64 == 0 && tiles64 >= best_ctas && tiles64 <= sms) {
+            split = 1;
+            split_n = 64;
+        }
         // 256 x 128 pair tiles (4 stages of 128 K-elements) load as many bytes per CTA as 128 x 256
         // tiles split in 2 and need no exchange of partial sums: taken when they give at least as
         // many CTAs as the best split, fit in one wave and fill most of their 256 rows (512 x 4096 x
@@ -623,6 +633,23 @@ int make_plan(int dtype, int64_t M, int64_t N, int64_t K, int layout, const gemm
             split = 0;
         }
         if (split) v = GEMM_VARIANT_SPLITK;
+    }
+    if (v == GEMM_VARIANT_SPLITK && split == 1) {
+        // one CTA per 128 x 64 tile with the whole K (128-deep stages): no exchange
+        if (split_n && split_n != 64)
+            return fail(GEMM_ERR_UNSUPPORTED, "the split-K kernel's unsplit mode uses 64-wide tiles");
+        if (K % 64 || (o && o->tile_k && o->tile_k != 128))
+            return fail(GEMM_ERR_UNSUPPORTED, "the unsplit split-K mode takes 128-deep stages (K %% 64 == 0)");
+        p->variant = v;
+        p->split_k = 1;
+        p->cluster = 1;
+        p->tile_m = 128;
+        p->tile_n = 64;
+        p->tile_k = 128;
+        p->stages = dtc::gsk::stages_for(64, 128, 1);
+        p->tiles = (int)((int64_t)ceil_div(M, 128) * ceil_div(N, 64));
+        p->ctas = p->tiles;
+        return GEMM_OK;
     }
     if (v == GEMM_VARIANT_SPLITK) {
         if (split_n && split_n != 256 && split_n != 128)

@@ -30,7 +30,9 @@
 // would move half-filled ones. The start-up cluster barrier is split: every thread arrives after
 // the set-up, and a thread waits only before its first copy into a peer (or at the end), so the
 // main loop does not wait for the other CTAs to start.
-// One cluster per tile, not persistent: a product of T tiles launches T * kS CTAs.
+// One cluster per tile, not persistent: a product of T tiles launches T * kS CTAs. With kS = 1 (64-
+// wide tiles) a CTA takes the whole K of its tile and stores it itself: no exchange, no reduction
+// (the skinny product: 128 CTAs, each streaming its 64 rows of B once with all of A from the L2).
 #pragma once
 
 #include "gemm_common.cuh"
@@ -77,7 +79,7 @@ struct Cfg {
     static constexpr int kCStaging = kStaging + (kColOwn ? 4 : 4 / kS) * 2 * 4096;
     static_assert(kCStaging <= kRing, "the staging copies must fit over the ring");
     static_assert(kBK == 64 || kBK == 128, "K-block of 64 or 128");
-    static_assert(kS == 2 || kS == 4, "K split over 2 or 4 CTAs");
+    static_assert(kS == 1 || kS == 2 || kS == 4, "K split over 1, 2 or 4 CTAs");
     static_assert(kBN % 64 == 0 && kBN <= 256, "the accumulator is read 64 columns at a time");
     static_assert(kSmemBytes <= 227 * 1024 - 256, "shared memory budget");
 };
@@ -139,7 +141,7 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
                 mbar_arrive_expect_tx(smem_u32(&bar_xchg[c]), C_::kColPieceBytes);
         }
         mbar_init(smem_u32(&bar_drain), 1);
-        mbar_init(smem_u32(&bar_ack), kS - 1);  // one acknowledgement from each other CTA
+        if constexpr (kS > 1) mbar_init(smem_u32(&bar_ack), kS - 1);  // one from each other CTA
         abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -434,8 +436,9 @@ __global__ void __launch_bounds__(gsk::kThreads, 1)
     // Every copy into this CTA has landed (its owners waited for them); the copies out of it read
     // its shared memory until they land: each other CTA acknowledges when all of them have, so the
     // CTA (and its shared memory) stays until then. No cluster-wide barrier at exit.
-    if (threadIdx.x == 0 && !*abort)
-        (void)wait_bounded<true>(smem_u32(&bar_ack), 0, abort, args.timeout_ns, args.status, 26);
+    if constexpr (kS > 1)
+        if (threadIdx.x == 0 && !*abort)
+            (void)wait_bounded<true>(smem_u32(&bar_ack), 0, abort, args.timeout_ns, args.status, 26);
     if (*abort && threadIdx.x == 0) {
         // After a timeout an owner may have stopped waiting: give copies still in flight a
         // fixed, bounded time to land before the CTAs' shared memory is released.

@@ -27,6 +27,7 @@ int launch(const Launch& L) {
 template <bool kBF16, bool kAMN, bool kNN>
 int by_shape(const Launch& L) {
     const Plan& p = *L.p;
+    if (p.split_k == 1) return launch<kBF16, kAMN, kNN, 64, 128, 1>(L);  // whole K, 64-wide tiles
     if (p.tile_n == 128) {
         if (p.tile_k == 128)
             return p.split_k == 2 ? launch<kBF16, kAMN, kNN, 128, 128, 2>(L)

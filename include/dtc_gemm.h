@@ -76,12 +76,15 @@ typedef enum {
                                 128 x 256 tiles split over 2; each CTA copies the partial sums
                                 of the rows another CTA owns into that CTA's shared memory, and
                                 the owner reduces and stores them (few-tile products, such as
-                                the skinny memory-bound M = 128 case) */
+                                the skinny memory-bound M = 128 case); or, unsplit, one CTA per
+                                128 x 64 tile with the whole K (few tiles with a short K) */
 } gemm_variant;
 
 typedef struct {
     int variant;          /* a gemm_variant; GEMM_VARIANT_AUTO (0) chooses per shape */
-    int split_k;          /* SPLITK only: number of K-slices (2 or 4), 0 = choose */
+    int split_k;          /* SPLITK only: number of K-slices (2 or 4), or 1: one CTA per
+                             128 x 64 tile with the whole K (no exchange; K % 64 == 0); 0 =
+                             choose */
     uint64_t timeout_ns;  /* limit of every device-side wait; 0 = the default (2 s) */
     int fault_inject;     /* test hook, 0 in normal use. 1 = the load producer skips its first
                              stage, so the consumer's bounded wait runs out and the call reports

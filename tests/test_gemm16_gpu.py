@@ -122,6 +122,21 @@ def test_split_k_full_parity(M, N, K, layout, split_k, tile_n, tile_k):
     full_check("f16", layout, M, N, K, seed=M + K + 1, **kw)
 
 
+@pytest.mark.parametrize("layout", ["NT", "NN", "TN", "TT"])
+@pytest.mark.parametrize("M,N,K", [(128, 2048, 4096), (296, 520, 1024), (64, 264, 64),
+                                   (136, 200, 192), (256, 392, 640)])
+def test_unsplit_mode_full_parity(M, N, K, layout):
+    # the split-K kernel with one CTA per 128 x 64 tile and the whole K (no exchange): partial
+    # tiles in M and N, one K-block (K = 64), a half-filled last 128-deep stage (K = 192); every
+    # stored row a multiple of 16 bytes in all four layouts
+    import dense_tensor_core_gb300 as dtc
+
+    p = dtc.gemm_plan("bf16", M, N, K, layout, variant=3, split_k=1)
+    assert (p["variant"], p["split_k"], p["cluster"], p["tile_n"], p["tile_k"]) == (3, 1, 1, 64, 128)
+    full_check("bf16", layout, M, N, K, seed=M + K + 7, variant=3, split_k=1)
+    full_check("f16", layout, M, N, K, seed=M + K + 8, variant=3, split_k=1)
+
+
 def test_automatic_choice_follows_the_cost_model():
     import dense_tensor_core_gb300 as dtc
 
@@ -139,8 +154,8 @@ def test_automatic_choice_follows_the_cost_model():
     assert (p["variant"], p["split_k"], p["tile_n"], p["ctas"]) == (3, 4, 128, 64)
     p = dtc.gemm_plan("f16", 1024, 1024, 1000, "NN")  # K % 64 != 0: 64-deep stages
     assert (p["variant"], p["split_k"], p["tile_n"], p["tile_k"]) == (3, 2, 128, 64)
-    p = dtc.gemm_plan("bf16", 256, 256, 512, "NT")  # 2 one-CTA tiles: split in 2 over 8 CTAs
-    assert (p["variant"], p["split_k"], p["ctas"]) == (3, 2, 8)
+    p = dtc.gemm_plan("bf16", 256, 256, 512, "NT")  # 2 one-CTA tiles, short K: 8 unsplit 128x64
+    assert (p["variant"], p["split_k"], p["tile_n"], p["ctas"]) == (3, 1, 64, 8)
     p = dtc.gemm_plan("bf16", 256, 256, 256, "NT")  # 4 K-blocks: too few to split
     assert p["variant"] == 1
 

@@ -37,9 +37,12 @@ def test_automatic_choice_on_gb300():
     assert (p["variant"], p["split_k"], p["tile_n"], p["ctas"]) == (3, 4, 128, 64)
     p = plan("f16", 1024, 1024, 1000, "NN")  # K % 64 != 0: 64-deep stages
     assert (p["variant"], p["split_k"], p["tile_n"], p["tile_k"]) == (3, 2, 128, 64)
-    # 2 one-CTA tiles of 128 x 256 would leave 150 SMs idle: 8 K-blocks are enough to split in 2
+    # 2 one-CTA tiles of 128 x 256 would leave 150 SMs idle; with K this short the 8 tiles of
+    # 128 x 64 with the whole K each beat a split in 2 (no exchange)
     p = plan("bf16", 256, 256, 512)
-    assert (p["variant"], p["split_k"], p["tile_n"], p["ctas"]) == (3, 2, 128, 8)
+    assert (p["variant"], p["split_k"], p["tile_n"], p["ctas"], p["cluster"]) == (3, 1, 64, 8, 1)
+    p = plan("bf16", 256, 256, 1024)  # a longer K: split (in 4 here)
+    assert (p["variant"], p["split_k"], p["tile_n"], p["ctas"]) == (3, 4, 128, 16)
     p = plan("bf16", 256, 256, 256)  # 4 K-blocks: too few to split
     assert p["variant"] == 1 and p["cluster"] == 1 and p["tile_k"] == 64
     p = plan("bf16", 1024, 1024, 512)  # 32 one-CTA tiles: a split needs 8 K-blocks per CTA
