@@ -277,8 +277,10 @@ def gemm_ex(kind, A, B, C=None, layout="NT", sfA=None, sfB=None, variant=0, spli
     passed as the leading dimensions. For the block-scaled product ("mxfp8") the element formats
     of A and B ("e4m3", "e5m2", "e2m3", "e3m2" or "e2m1"; fp6 / fp4 rows packed, K inferred from
     the row length) and the scale block (128, the default, or 32) may be chosen.
-    `workspace` (a CUDA tensor of gemm_workspace_size bytes, zero-filled before its first use)
-    lets the 16-bit products use stream-K; stream_k: 0 auto, 1 required, 2 off."""
+    `workspace` (a CUDA tensor of gemm_workspace_size bytes): for the 16-bit products the
+    stream-K workspace (zero-filled before its first use; stream_k: 0 auto, 1 required, 2 off);
+    for the block-scaled product the home of the repacked scales, which the pair kernel needs
+    and the one-CTA kernel uses with 32-element blocks."""
     if workspace is not None and (not workspace.is_cuda or not workspace.is_contiguous()):
         raise ValueError("workspace must be a contiguous CUDA tensor")
     if kind == "mxfp8":
