@@ -140,12 +140,20 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
             bool ok = true;
             WorkIter wi(pair, num_pairs, total, sk_tiles, args.num_kb);
             WorkItem w;
+            int whole = 0;  // whole tiles this pair has loaded
             while (ok && wi.next(w)) {
                 int mt, nt;
                 tile_coords(w.tile, args.num_m, args.num_n, kGroupM, mt, nt);
                 const int a_row = mt * 256 + (int)rank * kBMc;
                 const int b_row = nt * kBN + (int)rank * C_::kHalfN;
-                for (int kb = w.k0; kb < w.k1; ++kb, ++it) {
+                // Every other whole tile reads its K-blocks last to first: the pairs move through
+                // their tiles in waves, so a wave then starts on the K-slices of the operand panels
+                // the wave before read last, which are still in the L2 (4096 x 4096 x 8192: DRAM
+                // reads 249 MB against 291, ~1 % faster; 8192^3: 918 MB against 1057). The MMA
+                // thread is unaffected: it accumulates whatever K-block a stage holds.
+                const bool reverse = w.kind == kWhole && (whole++ & 1);
+                for (int kbi = w.k0; kbi < w.k1; ++kbi, ++it) {
+                    const int kb = reverse ? w.k0 + w.k1 - 1 - kbi : kbi;
                     const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
                     if (!wait_bounded(smem_u32(&bar_empty[s]), ph ^ 1u, abort, args.timeout_ns,
                                       args.status, 11)) {
