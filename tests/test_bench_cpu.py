@@ -143,3 +143,21 @@ def test_launches_per_step_counts_the_extra_kernels():
     assert bench.launches_per_step(W["bf16_sp24_nt_4096x4096x8192"], {"sf_packed": 0}) == 2
     assert bench.launches_per_step(W["mxfp8_b32_nt_4096x4096x8192"], {"sf_packed": 1}) == 2
     assert bench.launches_per_step(W["mxfp8_nt_4096x4096x8192"], {"sf_packed": 0}) == 1
+    assert bench.launches_per_step(W["nvfp4_nt_4096x4096x8192"], {"sf_packed": 0}) == 2
+
+
+def test_nvfp4_workload_bytes_and_inputs():
+    # the NVFP4 workload's compulsory bytes (packed e2m1 rows, a UE4M3 byte per 16 elements, bf16
+    # C) and the shapes and code ranges its generator produces
+    import numpy as np
+
+    from dense_tensor_core_gb300 import workloads
+
+    w = workloads.WORKLOADS["nvfp4_nt_4096x4096x8192"]
+    assert w.min_bytes == 2 * 4096 * (4096 + 512) + 2 * 4096 * 4096
+    A, B, sfA, sfB = workloads.make_nvfp4(64, 48, 96, seed=3)
+    assert A.shape == (64, 48) and B.shape == (48, 48) and sfA.shape == (64, 6) and sfB.shape == (48, 6)
+    e = sfA >> 3
+    assert ((e >= 4) & (e <= 10)).all() and not (sfA & 0x80).any()
+    nib = np.concatenate([A & 15, A >> 4]).ravel()
+    assert set(np.unique(nib)) <= set(range(16)) and len(np.unique(nib)) > 8
