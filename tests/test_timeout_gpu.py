@@ -24,8 +24,9 @@ def built():
         pytest.skip("no CUDA device")
 
 
-@pytest.mark.parametrize("variant", [1, 2, 3])
-def test_wait_that_nothing_completes_reports_timeout_then_recovers(variant):
+@pytest.mark.parametrize("variant,split_k", [(1, 0), (2, 0), (3, 0), (3, 1)])
+def test_wait_that_nothing_completes_reports_timeout_then_recovers(variant, split_k):
+    # (3, 1): the split-K kernel's unsplit mode, which tears down without acknowledgements
     import dense_tensor_core_gb300 as dtc
 
     M, N, K = 512, 512, 512
@@ -33,13 +34,14 @@ def test_wait_that_nothing_completes_reports_timeout_then_recovers(variant):
     At, Bt = to_device16(A, "bf16"), to_device16(B, "bf16")
     dtc.gemm_stream_status()  # start from a clear status word
     t0 = time.time()
-    dtc.gemm_ex("bf16", At, Bt, variant=variant, timeout_ns=20_000_000, fault_inject=1)
+    dtc.gemm_ex("bf16", At, Bt, variant=variant, split_k=split_k, timeout_ns=20_000_000,
+                fault_inject=1)
     with pytest.raises(dtc.GemmError) as e:
         dtc.gemm_stream_status()
     assert e.value.status == 4  # GEMM_ERR_TIMEOUT
     assert time.time() - t0 < 30
     dtc.gemm_stream_status()  # the status word was cleared by the report
-    C = dtc.gemm_ex("bf16", At, Bt, variant=variant)
+    C = dtc.gemm_ex("bf16", At, Bt, variant=variant, split_k=split_k)
     dtc.gemm_stream_status()
     ref = oracle.gemm16("bf16", "NT", A, B, M, N, K)
     got = C.view(torch.int16).cpu().numpy().view(np.uint16)
