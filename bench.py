@@ -22,6 +22,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -107,26 +108,57 @@ def code_text(src):
     return " ".join("".join(out).split())
 
 
-def source_hash():
-    """Hash of the kernel sources' code (comments and layout ignored): the DRAM traffic recorded by
-    an ncu capture stays valid while the code it was taken on is unchanged."""
+# The translation units that launch each benchmarked kernel: with the headers they include they
+# define the kernel, and the planner (dtc_gemm.cu) decides its launch.
+KERNEL_UNITS = {
+    "gemm16_1cta_kernel": ["launch_1cta.cu"],
+    "gemm16_2cta_kernel": ["launch_2cta_bf16.cu", "launch_2cta_f16.cu"],
+    "gemm16_splitk_kernel": ["launch_splitk.cu"],
+    "gemm_mxfp8_kernel": ["launch_mx.cu"],
+    "gemm_mxfp8_2cta_kernel": ["launch_mx.cu"],
+}
+
+
+def include_closure(units):
+    """The files of `units` and every local header they include, directly or not."""
+    seen, todo = set(), list(units)
+    while todo:
+        f = todo.pop()
+        path = os.path.join(CSRC, f)
+        if f in seen or not os.path.exists(path):
+            continue
+        seen.add(f)
+        with open(path, encoding="utf-8") as fh:
+            todo += re.findall(r'#include\s+"([^"]+)"', fh.read())
+    return seen
+
+
+def source_hash(kernel=None):
+    """Hash of the code (comments and layout ignored) of the sources that define `kernel`'s
+    launches: its launcher translation units with the headers they include, and the planner's own
+    text; of all kernel sources for any other kernel. The DRAM traffic recorded by an ncu capture
+    stays valid while that code is unchanged."""
+    if kernel in KERNEL_UNITS:
+        files = include_closure(KERNEL_UNITS[kernel]) | {"dtc_gemm.cu"}
+    else:
+        files = {f for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh", ".h"))}
     h = hashlib.sha256()
-    for f in sorted(os.listdir(CSRC)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(CSRC, f), encoding="utf-8") as fh:
-                h.update(f.encode() + b"\0" + code_text(fh.read()).encode())
+    for f in sorted(files):
+        with open(os.path.join(CSRC, f), encoding="utf-8") as fh:
+            h.update(f.encode() + b"\0" + code_text(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload, kernel):
-    """DRAM bytes per launch from the committed ncu summary, if taken on the current source."""
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current source of
+    that kernel."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
     e = rec.get(workload, {})
-    if e.get("kernel") != kernel or e.get("source_sha") != source_hash():
+    if e.get("kernel") != kernel or e.get("source_sha") != source_hash(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 

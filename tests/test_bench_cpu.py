@@ -39,6 +39,24 @@ def test_traffic_record_is_dropped_when_the_kernel_source_changes(tmp_path, monk
     assert bench.recorded_traffic("w", "k") is None
 
 
+def test_kernel_hash_follows_only_that_kernels_sources(tmp_path, monkeypatch):
+    # a kernel's hash covers its launcher units, the headers they include and the planner's own
+    # text: a change to another kernel's source leaves it unchanged
+    d = tmp_path / "csrc"
+    d.mkdir()
+    (d / "launch_splitk.cu").write_text('#include "gemm16_splitk.cuh"\nint a;\n')
+    (d / "gemm16_splitk.cuh").write_text('#include "common.cuh"\nint b;\n')
+    (d / "common.cuh").write_text("int c;\n")
+    (d / "dtc_gemm.cu").write_text('#include "gemm16_splitk.cuh"\nint d;\n')
+    (d / "other.cuh").write_text("int e;\n")
+    monkeypatch.setattr(bench, "CSRC", str(d))
+    h0, all0 = bench.source_hash("gemm16_splitk_kernel"), bench.source_hash()
+    (d / "other.cuh").write_text("int e2;\n")
+    assert bench.source_hash("gemm16_splitk_kernel") == h0 and bench.source_hash() != all0
+    (d / "common.cuh").write_text("int c2;\n")
+    assert bench.source_hash("gemm16_splitk_kernel") != h0
+
+
 def test_code_hash_ignores_comments_but_not_code():
     a = 'int f(int x) {  // add one\n    return x + 1; /* done */ }\nconst char* s = "a // b";\n'
     b = 'int f(int x) {\n  return x + 1;   }\n// a note\nconst char* s = "a // b";\n'
