@@ -44,12 +44,14 @@ struct Nvfp4Operand {
     int64_t rows;
 };
 
-// Value of a UE4M3 scale code as fp32 (exact), NaN for codes that are not UE4M3 values.
-__device__ __forceinline__ float ue4m3_value(uint32_t c) {
-    const uint32_t e = (c >> 3) & 15u, m = c & 7u;
-    if ((c & 0x80u) || (e == 15u && m == 7u)) return __uint_as_float(0x7FC00000u);
-    if (e == 0) return (float)m * 0x1p-9f;
-    return __uint_as_float(((e - 7u + 127u) << 23) | (m << 20));
+// bf16 bits of a UE4M3 scale code (exact): a normal code 0.eeee.mmm (e >= 1) has exponent e + 120
+// and mantissa mmm << 4, by integer arithmetic; the subnormal codes (e = 0, m / 8 * 2^-6) go
+// through fp32; a code with the sign bit set, or the NaN code 0x7F, gives a bf16 NaN.
+__device__ __forceinline__ uint32_t ue4m3_bf16_bits(uint32_t c) {
+    if ((c & 0x80u) || c == 0x7Fu) return 0x7FC0u;
+    if ((c & 0x78u) == 0)
+        return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn((float)(c & 7u) * 0x1p-9f));
+    return ((c & 0x7Fu) << 4) + 0x3C00u;
 }
 
 // e2m1 -> bf16 by byte lookup: the bf16 of magnitude code n (0..7: 0, 0.5, 1, 1.5, 2, 3, 4, 6) is
@@ -60,22 +62,23 @@ constexpr uint32_t kHi0 = 0x3F3F3F00u, kHi1 = 0x40404040u;  // 00 3F 3F 3F | 40 
 // 8 packed e2m1 codes (element 2j in the low nibble of byte j) times the scale pair s2, as 4
 // words of two bf16 (element 2j in the low half of word j). The magnitudes of elements 2j and
 // 2j + 1 become the selectors of two byte permutations (one into the low-byte table, one into
-// the high-byte table, the unused selector nibbles picking the zero entry 0); the sign bits are
-// moved to bits 15 and 31. The products are exact (at most 5 significant bits), so the bf16
-// multiply rounds nothing.
+// the high-byte table, the unused selector nibbles picking the zero entry 0; a permutation reads
+// only the low 16 bits of its selector). A third permutation takes byte j of the sign bits, once
+// shifted left by 4 (element 2j's sign to bit 7) into byte 1 and once as they are (element
+// 2j + 1's) into byte 3, i.e. to bits 15 and 31. The products are exact (at most 5 significant
+// bits), so the bf16 multiply rounds nothing.
 __device__ __forceinline__ void e2m1x8_times(uint32_t c, __nv_bfloat162 s2, uint32_t (&out)[4]) {
     const uint32_t lo_mag = c & 0x07070707u;         // even elements' magnitudes, one per byte
     const uint32_t hi_mag = (c >> 4) & 0x07070707u;  // odd elements'
     const uint32_t i01 = __byte_perm(lo_mag, hi_mag, 0x5140);  // m0 m1 m2 m3
     const uint32_t i23 = __byte_perm(lo_mag, hi_mag, 0x7362);  // m4 m5 m6 m7
-    const uint32_t sel[4] = {i01 & 0xFFFFu, i01 >> 16, i23 & 0xFFFFu, i23 >> 16};
-    const uint32_t sign[4] = {((c << 12) & 0x8000u) | ((c << 24) & 0x80000000u),
-                              ((c << 4) & 0x8000u) | ((c << 16) & 0x80000000u),
-                              ((c >> 4) & 0x8000u) | ((c << 8) & 0x80000000u),
-                              ((c >> 12) & 0x8000u) | (c & 0x80000000u)};
+    const uint32_t sel[4] = {i01, i01 >> 16, i23, i23 >> 16};
+    const uint32_t sgn = c & 0x88888888u;
+    const uint32_t sgn4 = sgn << 4;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        uint32_t w = __byte_perm(kLo0, kLo1, sel[j]) | __byte_perm(kHi0, kHi1, sel[j] << 4) | sign[j];
+        const uint32_t sign = __byte_perm(sgn4, sgn, (j << 4) | ((4 + j) << 12)) & 0x80008000u;
+        uint32_t w = __byte_perm(kLo0, kLo1, sel[j]) | __byte_perm(kHi0, kHi1, sel[j] << 4) | sign;
         __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&w);
         v = __hmul2(v, s2);
         out[j] = *reinterpret_cast<uint32_t*>(&v);
@@ -106,7 +109,9 @@ __global__ void __launch_bounds__(kThreads)
         for (int u = 0; u < kUnroll; ++u) {
             const int64_t i = base + (int64_t)u * kThreads;
             if (i >= units) continue;
-            const __nv_bfloat162 s2 = __bfloat162bfloat162(__float2bfloat16_rn(ue4m3_value(sc[u])));
+            uint32_t sb = ue4m3_bf16_bits(sc[u]);
+            sb |= sb << 16;
+            const __nv_bfloat162 s2 = *reinterpret_cast<__nv_bfloat162*>(&sb);
             uint32_t w[4];
             e2m1x8_times(v[u], s2, w);
             *reinterpret_cast<uint4*>(op.out + i * 8) = make_uint4(w[0], w[1], w[2], w[3]);
