@@ -4,6 +4,13 @@ row each, outputs bit for bit equal. Named to be collected last; it also passes 
 import pytest
 import torch
 
+
+def allocations():
+    """torch's cumulative count of device allocation requests: a call that allocates nothing
+    leaves it unchanged, and unlike the bytes in use it does not move when the garbage collector
+    frees an earlier test's tensors meanwhile."""
+    return torch.cuda.memory_stats().get("allocation.all.allocated", 0)
+
 from dense_tensor_core_gb300 import workloads
 from parity import to_device16
 
@@ -40,9 +47,9 @@ def test_static_workspace_matches_caller_workspace_two_calls(M, N, K, layout, st
         C_own.fill_(float("nan"))
         dtc.gemm_ex("bf16", At, Bt, C_ref, layout=layout, workspace=ws if nbytes else None,
                     stream_k=stream_k)
-        before = torch.cuda.memory_allocated()
+        before = allocations()
         dtc.gemm_ex_static_workspace("bf16", At, Bt, C_own, layout=layout, stream_k=stream_k)
-        assert torch.cuda.memory_allocated() == before  # nothing allocated through torch either
+        assert allocations() == before  # nothing allocated through torch either
         dtc.gemm_stream_status()
         assert torch.equal(C_ref.view(torch.int16), C_own.view(torch.int16)), f"call {call}"
 
@@ -71,10 +78,10 @@ def test_static_workspace_holds_repacked_scales(variant, block):
         C_own.fill_(float("nan"))
         dtc.gemm_ex("mxfp8", At, Bt, C_ref, sfA=sAt, sfB=sBt, scale_block=block, variant=variant,
                     workspace=ws)
-        before = torch.cuda.memory_allocated()
+        before = allocations()
         dtc.gemm_ex_static_workspace("mxfp8", At, Bt, C_own, sfA=sAt, sfB=sBt, scale_block=block,
                                      variant=variant)
-        assert torch.cuda.memory_allocated() == before
+        assert allocations() == before
         dtc.gemm_stream_status()
         assert torch.equal(C_ref.view(torch.int16), C_own.view(torch.int16)), f"call {call}"
     assert not np.isnan(C_own.float().cpu().numpy()).any()
