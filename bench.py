@@ -558,7 +558,7 @@ def library_context(w, A, B, flush_l2, stream, steps, dev):
 # The benchmark configurations of the pages' workloads (one JSON row each in `configs`), with the
 # roofline that bounds each: the tiny and the 1024^3 products are launch- and occupancy-bound, the
 # skinny M = 128 product is HBM-bound, the rest tensor-bound.
-BASELINE_CONFIGS = [
+BENCH_CONFIGS = [
     ("1", "bf16_nt_256x256x512", "latency"),
     ("2", "f16_nn_1024x1024x1024", "latency"),
     ("3", "bf16_nt_4096x4096x8192", "tensor"),
@@ -777,7 +777,7 @@ def run_ours(args, w):
         configs = {}
         if not args.no_configs and world == 1:
             cfg_steps = max(20, min(args.steps, 200))
-            for cid, name, bound in BASELINE_CONFIGS:
+            for cid, name, bound in BENCH_CONFIGS:
                 cw = workloads.WORKLOADS[name]
                 if name == w.name:
                     cms, cplan, ct0, ct1, cname, clib = kernel_ms, plan, t0, t1, kernel_name, library

@@ -142,13 +142,13 @@ def test_nvml_samples_summarised_over_the_timed_window():
     assert bench.summarise_samples(samples, 20.0, 21.0)["window"] == "whole run"
 
 
-def test_baseline_configs_name_known_workloads():
+def test_bench_configs_name_known_workloads():
     import bench
     from dense_tensor_core_gb300 import workloads
 
-    ids = [c[0] for c in bench.BASELINE_CONFIGS]
+    ids = [c[0] for c in bench.BENCH_CONFIGS]
     assert ids == ["1", "2", "3", "4a", "4b", "5"]
-    for _, name, bound in bench.BASELINE_CONFIGS:
+    for _, name, bound in bench.BENCH_CONFIGS:
         assert name in workloads.WORKLOADS and bound in ("latency", "tensor", "hbm")
 
 
